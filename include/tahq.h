@@ -1,0 +1,149 @@
+/*
+ * tahq.h -- C ABI of the GB300 (sm_103a) TAH-Quant activation codec.
+ *
+ * The codec compresses the [tokens x channels] activation tensor that one pipeline
+ * stage sends to the next and restores it on the receiving stage, as described in
+ * "TAH-Quant: Effective Activation Quantization in Pipeline Parallelism over Slow
+ * Network" (arXiv 2506.01352v2), §3.1-§3.5 and Algorithm 1 (stage a sends
+ * Q(a(xi)), stage b de-quantises it).
+ *
+ * Conventions shared by every entry point
+ *   - The caller owns all memory.  Tensor, output and workspace pointers are DEVICE
+ *     pointers on the current CUDA device; the library allocates nothing.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream).  The return code covers host-side argument
+ *     checks and kernel-launch errors only.
+ *   - Errors found on the device (non-finite input, a bounded wait that gave up, an
+ *     inconsistent select, a bit width outside 1..8, a stream shorter than its slots)
+ *     set bits of a 32-bit status word at the head of the workspace.  The word is
+ *     cleared at the start of every call and read by tahq_get_device_status().  No
+ *     kernel traps or waits without a bound.
+ *   - Layout: x and out are row-major [tokens, channels].  Tile t covers channels
+ *     [w*tile, (w+1)*tile) of token t / (channels/tile), w = t % (channels/tile).
+ *   - Alignment: x, out and codes 16 B; workspace 256 B; scales, zeros 4 B.
+ *   - Limits: tile a power of two in 8..128 dividing channels (so pivots fit a byte and
+ *     every slot is whole bytes); hblock a power of two in 2..tile; 1 <= bits_lo <
+ *     bits_hi <= 8; bits_lo <= budget <= bits_hi; tokens_per_group divides tokens
+ *     (0 = one group of all tokens) and a group holds fewer than 2^31 tiles;
+ *     tokens * channels < 2^40.
+ */
+#ifndef TAHQ_H
+#define TAHQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TAHQ_OK = 0,
+    TAHQ_ERR_ARG = 1,          /* an argument is outside the limits above             */
+    TAHQ_ERR_UNSUPPORTED = 2,  /* valid for the method, not built here (e.g. tile 96) */
+    TAHQ_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small          */
+    TAHQ_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed         */
+    TAHQ_ERR_DEVICE_STATUS = 5 /* the device status word is non-zero                  */
+} tahq_status;
+
+typedef enum { TAHQ_F32 = 0, TAHQ_BF16 = 1 } tahq_dtype;
+
+/* Bits of the device status word. */
+#define TAHQ_DEV_NONFINITE 0x1u          /* an input tile sum or key was not finite     */
+#define TAHQ_DEV_WAIT_TIMEOUT 0x2u       /* a cross-block wait gave up after its bound  */
+#define TAHQ_DEV_SELECT_MISMATCH 0x4u    /* candidate count disagreed with histogram    */
+#define TAHQ_DEV_BAD_BITS 0x8u           /* decode: a bit width outside 1..8 or pivot   */
+#define TAHQ_DEV_STREAM_OVERRUN 0x10u    /* decode: slots run past codes_bytes          */
+
+/*
+ * Exact size in bytes of the packed code stream for these parameters.  §3.4: the
+ * mixed-precision payload is a contiguous uint8 stream of a fixed shape.  Each group of
+ * tokens_per_group tokens has n_g = tokens_per_group * channels / tile tiles, of which
+ * K = floor((budget - bits_lo) * n_g / (bits_hi - bits_lo)) carry bits_hi and the rest
+ * bits_lo, so every group occupies n_g*tile*bits_lo/8 + K*tile*(bits_hi-bits_lo)/8 bytes.
+ * Returns 0 for invalid arguments (and for tokens == 0).
+ */
+size_t tahq_payload_size(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                         float budget, int64_t tokens_per_group);
+
+/* Number K of tiles per group that receive bits_hi (formula above); -1 if invalid. */
+int64_t tahq_hi_count(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                      float budget, int64_t tokens_per_group);
+
+/*
+ * Bytes of device workspace tahq_encode needs for these parameters (status word,
+ * per-group entropy histograms, select candidates, per-tile keys, scan words).
+ * Returns 0 for invalid arguments.  The workspace may be reused by later calls on the
+ * same stream; calls that overlap on the device must not share a workspace.
+ */
+size_t tahq_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock, int bits_lo,
+                           int bits_hi, float budget, int64_t tokens_per_group);
+
+/*
+ * Encode x (dtype f32 or bf16, [tokens, channels]) -- §3.1-§3.4:
+ *   per tile: entropy key (§3.2 eq. (1)-(2), Shannon sign), outlier ratio r (§3.3
+ *   eq. (3), tau = 2.0) and pivot d = first arg-max |x|;
+ *   per group: the K tiles of highest (key, then lowest tile index) get bits_hi (§3.2
+ *   "Top-p% tile selection"), the others bits_lo;
+ *   per tile: if r > tau, swap positions 0 and d and apply the Sylvester Hadamard
+ *   transform to every hblock-wide block, scaled by 1/sqrt(hblock) (§3.3 eq. (4));
+ *   then min/max asymmetric quantisation to b bits (round to nearest even) and
+ *   LSB-first packing into the tile's slot; slots follow each other in tile order.
+ * Outputs (device, caller-allocated):
+ *   codes  [tahq_payload_size(...)] bytes
+ *   scales [n_tiles] fp32  step (max-min)/(2^b-1), 0 for a constant tile
+ *   zeros  [n_tiles] fp32  tile minimum (the de-quantisation offset)
+ *   bits   [n_tiles] u8    bits_lo or bits_hi
+ *   pivots [n_tiles] u8    d for transformed tiles, 0xFF otherwise
+ * n_tiles = tokens * channels / tile.  Returns TAHQ_ERR_ARG / _UNSUPPORTED /
+ * _WORKSPACE before launching anything, TAHQ_ERR_CUDA on a launch failure.
+ */
+tahq_status tahq_encode(const void *x, tahq_dtype dtype, int64_t tokens, int64_t channels, int tile,
+                        int hblock, int bits_lo, int bits_hi, float budget,
+                        int64_t tokens_per_group, uint8_t *codes, float *scales, float *zeros,
+                        uint8_t *bits, uint8_t *pivots, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* Bytes of device workspace tahq_decode needs; 0 for invalid arguments. */
+size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile);
+
+/*
+ * Decode -- the inverse path of §3.3 ("apply H_G^T to the de-quantised values") and
+ * Algorithm 1 step 5: unpack each tile's codes from its slot (slot offsets are the
+ * running sum of tile*bits[t]/8 in tile order, so no group structure is needed),
+ * v = fma(q, scale, zero); if pivots[t] != 0xFF: Hadamard per hblock block, scale
+ * 1/sqrt(hblock), swap positions 0 and pivots[t].  out is fp32 [tokens, channels].
+ * codes_bytes bounds every read of codes: a stream shorter than its slots sets
+ * TAHQ_DEV_STREAM_OVERRUN (the affected tiles decode to 0) instead of reading past it.
+ */
+tahq_status tahq_decode(const uint8_t *codes, size_t codes_bytes, const float *scales,
+                        const float *zeros, const uint8_t *bits, const uint8_t *pivots,
+                        int64_t tokens, int64_t channels, int tile, int hblock, float *out,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Copy the device status word of the last call that used `workspace` into *status_out
+ * (may be NULL) after synchronising `stream` (only that stream).  Returns TAHQ_OK if
+ * the word is zero, TAHQ_ERR_DEVICE_STATUS if not, TAHQ_ERR_CUDA if the copy failed.
+ */
+tahq_status tahq_get_device_status(const void *workspace, uint32_t *status_out, void *stream);
+
+/* Human-readable name of a tahq_status value (static string, never NULL). */
+const char *tahq_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tahq_version(void);
+
+/*
+ * The host-side tables the kernels use for the canonical base-2 logarithm:
+ * T[i] = nearest float to log2(1 + i/128), R[i] = nearest float to 1/(1 + i/128),
+ * k[j] = nearest float to (-1)^j / ((j+1) ln 2), j = 0..3.  Exposed so that a CPU test
+ * can check them without a GPU.  T and R hold 128 floats, k 4.
+ */
+void tahq_log2_tables(float *T, float *R, float *k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TAHQ_H */

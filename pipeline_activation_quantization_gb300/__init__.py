@@ -1,0 +1,224 @@
+"""GB300 (sm_103a) TAH-Quant activation codec: a thin binding of ``include/tahq.h``.
+
+The ``tahq_*`` functions have the names and arguments of the C ABI; they only marshal
+arguments (torch tensors become device pointers, the current torch stream is passed
+unless one is given).  Every step of the codec runs in the CUDA kernels of
+``libtahq.so``; there is no CPU fallback, and importing fails loudly when the library
+has not been built (``python -m pipeline_activation_quantization_gb300.build``).
+
+``encode`` / ``decode`` are conveniences that allocate outputs and workspace with torch
+(device memory only) and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import build as _build
+
+__all__ = [
+    "TAHQ_F32", "TAHQ_BF16", "TahqError", "lib", "tahq_payload_size", "tahq_hi_count",
+    "tahq_workspace_size", "tahq_decode_workspace_size", "tahq_encode", "tahq_decode",
+    "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
+    "encode", "decode", "EXPORTED_SYMBOLS",
+]
+
+TAHQ_F32, TAHQ_BF16 = 0, 1
+STATUS_NAMES = {0: "TAHQ_OK", 1: "TAHQ_ERR_ARG", 2: "TAHQ_ERR_UNSUPPORTED", 3: "TAHQ_ERR_WORKSPACE",
+                4: "TAHQ_ERR_CUDA", 5: "TAHQ_ERR_DEVICE_STATUS"}
+DEV_NONFINITE, DEV_WAIT_TIMEOUT, DEV_SELECT_MISMATCH, DEV_BAD_BITS, DEV_STREAM_OVERRUN = 1, 2, 4, 8, 16
+
+# Every extern "C" function declared in include/tahq.h.
+EXPORTED_SYMBOLS = (
+    "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode",
+    "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
+    "tahq_status_string", "tahq_version", "tahq_log2_tables",
+)
+
+
+class TahqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def lib(path: str | None = None):
+    """Load ``libtahq.so`` (build it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libtahq.so not found at {path}")
+    L = C.CDLL(path)
+    i64, i32, sz, p, f32 = C.c_int64, C.c_int, C.c_size_t, C.c_void_p, C.c_float
+    sig = {
+        "tahq_payload_size": (sz, [i64, i64, i32, i32, i32, f32, i64]),
+        "tahq_hi_count": (i64, [i64, i64, i32, i32, i32, f32, i64]),
+        "tahq_workspace_size": (sz, [i64, i64, i32, i32, i32, i32, f32, i64]),
+        "tahq_decode_workspace_size": (sz, [i64, i64, i32]),
+        "tahq_encode": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64,
+                              p, p, p, p, p, p, sz, p]),
+        "tahq_decode": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, p, p, sz, p]),
+        "tahq_get_device_status": (i32, [p, C.POINTER(C.c_uint32), p]),
+        "tahq_status_string": (C.c_char_p, [i32]),
+        "tahq_version": (i32, []),
+        "tahq_log2_tables": (None, [p, p, p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------------------ C-ABI names
+
+def tahq_payload_size(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group) -> int:
+    return lib().tahq_payload_size(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group)
+
+
+def tahq_hi_count(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group) -> int:
+    return lib().tahq_hi_count(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group)
+
+
+def tahq_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget, tokens_per_group) -> int:
+    return lib().tahq_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                                     tokens_per_group)
+
+
+def tahq_decode_workspace_size(tokens, channels, tile) -> int:
+    return lib().tahq_decode_workspace_size(tokens, channels, tile)
+
+
+def tahq_encode(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                tokens_per_group, codes, scales, zeros, bits, pivots, workspace,
+                workspace_bytes, stream=None) -> int:
+    return lib().tahq_encode(_ptr(x), dtype, tokens, channels, tile, hblock, bits_lo, bits_hi,
+                             budget, tokens_per_group, _ptr(codes), _ptr(scales), _ptr(zeros),
+                             _ptr(bits), _ptr(pivots), _ptr(workspace), workspace_bytes,
+                             _stream(stream))
+
+
+def tahq_decode(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile, hblock,
+                out, workspace, workspace_bytes, stream=None) -> int:
+    return lib().tahq_decode(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros), _ptr(bits),
+                             _ptr(pivots), tokens, channels, tile, hblock, _ptr(out),
+                             _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def tahq_get_device_status(workspace, stream=None) -> tuple[int, int]:
+    """-> (tahq_status, raw status word)."""
+    word = C.c_uint32(0)
+    rc = lib().tahq_get_device_status(_ptr(workspace), C.byref(word), _stream(stream))
+    return rc, word.value
+
+
+def tahq_status_string(status: int) -> str:
+    return lib().tahq_status_string(status).decode()
+
+
+def tahq_version() -> int:
+    return lib().tahq_version()
+
+
+def tahq_log2_tables():
+    import numpy as np
+    T = np.zeros(128, np.float32); R = np.zeros(128, np.float32); k = np.zeros(4, np.float32)
+    lib().tahq_log2_tables(T.ctypes.data, R.ctypes.data, k.ctypes.data)
+    return T, R, k
+
+
+# ------------------------------------------------------------------ conveniences (torch memory)
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise TahqError(rc, what)
+
+
+def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_hi: int = 4,
+           budget: float = 3.5, tokens_per_group: int = 0, out: dict | None = None,
+           workspace=None, stream=None) -> dict:
+    """Encode a CUDA tensor ``x`` ([tokens, channels], float32 or bfloat16).
+
+    Returns ``{"codes", "scales", "zeros", "bits", "pivots", "workspace"}`` (torch tensors on
+    x's device).  Pass ``out`` / ``workspace`` from an earlier call to reuse them.
+    """
+    import torch
+    if not x.is_cuda:
+        raise ValueError("tahq.encode needs a CUDA tensor")
+    if x.dtype == torch.float32:
+        dt = TAHQ_F32
+    elif x.dtype == torch.bfloat16:
+        dt = TAHQ_BF16
+    else:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    x = x.contiguous()
+    T, Cc = x.shape
+    h = hblock or tile
+    n = T * (Cc // tile)
+    pay = tahq_payload_size(T, Cc, tile, bits_lo, bits_hi, budget, tokens_per_group)
+    ws = tahq_workspace_size(T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group)
+    if ws == 0:
+        raise TahqError(1, "tahq_workspace_size")
+    dev = x.device
+    if out is None:
+        out = {
+            "codes": torch.empty(max(pay, 16), dtype=torch.uint8, device=dev),
+            "scales": torch.empty(n, dtype=torch.float32, device=dev),
+            "zeros": torch.empty(n, dtype=torch.float32, device=dev),
+            "bits": torch.empty(n, dtype=torch.uint8, device=dev),
+            "pivots": torch.empty(n, dtype=torch.uint8, device=dev),
+        }
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    rc = tahq_encode(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
+                     out["codes"], out["scales"], out["zeros"], out["bits"], out["pivots"],
+                     workspace, workspace.numel(), stream)
+    _check(rc, "tahq_encode")
+    res = dict(out)
+    res["codes"] = out["codes"][:pay]
+    res["workspace"] = workspace
+    res["payload_bytes"] = pay
+    return res
+
+
+def decode(enc: dict, tokens: int, channels: int, tile: int = 64, hblock: int | None = None,
+           out=None, workspace=None, stream=None):
+    """Decode the dict returned by ``encode`` into a float32 CUDA tensor [tokens, channels]."""
+    import torch
+    dev = enc["scales"].device
+    h = hblock or tile
+    ws = tahq_decode_workspace_size(tokens, channels, tile)
+    if ws == 0:
+        raise TahqError(1, "tahq_decode_workspace_size")
+    if out is None:
+        out = torch.empty((tokens, channels), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    codes = enc["codes"]
+    rc = tahq_decode(codes, codes.numel(), enc["scales"], enc["zeros"], enc["bits"], enc["pivots"],
+                     tokens, channels, tile, h, out, workspace, workspace.numel(), stream)
+    _check(rc, "tahq_decode")
+    return out

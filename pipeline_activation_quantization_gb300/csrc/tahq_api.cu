@@ -1,0 +1,311 @@
+// tahq_api.cu -- the C ABI of the codec (declared in include/tahq.h): argument checks,
+// workspace layout, and the launch sequence on the caller's stream.  Allocates nothing.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tahq.h"
+#include "tahq_launch.h"
+
+namespace {
+
+using tahq::LgTables;
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tables of the canonical base-2 logarithm (nearest floats of double-precision values).
+const LgTables& lg_tables() {
+  static LgTables tabs;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int i = 0; i < 128; i++) {
+      const double c = 1.0 + i / 128.0;
+      tabs.T[i] = (float)std::log2(c);
+      tabs.R[i] = (float)(1.0 / c);
+    }
+    const double ln2 = 0.69314718055994530942;
+    for (int j = 0; j < 4; j++) tabs.k[j] = (float)(((j % 2) ? -1.0 : 1.0) / ((j + 1) * ln2));
+  });
+  return tabs;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+struct Shape {
+  long long T, C, n, n_g, n_groups, K, group_bytes, payload;
+  int G, h, lo, hi;
+};
+
+// Shape checks shared by every entry point.  hblock < 0 means "not given".
+tahq_status check_shape(long long T, long long C, int G, int h, Shape& s) {
+  if (T < 0 || C <= 0) return TAHQ_ERR_ARG;
+  if (G < 8 || G > 128 || G % 8) return TAHQ_ERR_ARG;
+  if (!is_pow2(G)) return TAHQ_ERR_UNSUPPORTED;
+  if (C % G) return TAHQ_ERR_ARG;
+  if (h >= 0 && (h < 2 || h > G || !is_pow2(h))) return TAHQ_ERR_ARG;
+  if (T > 0 && C > (1ll << 40) / T) return TAHQ_ERR_ARG;
+  s.T = T;
+  s.C = C;
+  s.G = G;
+  s.h = h;
+  s.n = T * (C / G);
+  return TAHQ_OK;
+}
+
+tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, float budget,
+                        long long S, Shape& s) {
+  tahq_status st = check_shape(T, C, G, h, s);
+  if (st != TAHQ_OK) return st;
+  if (lo < 1 || hi > 8 || lo >= hi) return TAHQ_ERR_ARG;
+  if (!(std::isfinite(budget) && (double)budget >= lo && (double)budget <= hi)) return TAHQ_ERR_ARG;
+  if (S < 0) return TAHQ_ERR_ARG;
+  if (S == 0) S = T;
+  if (T > 0 && T % S) return TAHQ_ERR_ARG;
+  s.lo = lo;
+  s.hi = hi;
+  s.n_g = S * (C / G);
+  if (s.n_g >= (1ll << 31)) return TAHQ_ERR_UNSUPPORTED;
+  s.n_groups = (T > 0) ? T / S : 0;
+  s.K = (long long)std::floor(((double)budget - lo) * (double)s.n_g / (double)(hi - lo));
+  s.group_bytes = s.n_g * G * lo / 8 + s.K * G * (hi - lo) / 8;
+  s.payload = s.n_groups * s.group_bytes;
+  return TAHQ_OK;
+}
+
+struct EncLayout {
+  size_t status, ticket, cand_cnt, sel, hist_coarse, hist_fine, lookback, ctrl_end, keys, cand,
+      total;
+};
+
+// Look-back words are sized for fp32 input, whose smaller chunks need the most of them.
+EncLayout enc_layout(const Shape& s) {
+  EncLayout L{};
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 16);
+  L.ticket = off;
+  off = align_up(off + 64);
+  L.cand_cnt = off;
+  off = align_up(off + 4 * (size_t)s.n_groups);
+  L.sel = off;
+  off = align_up(off + sizeof(tahq::SelResult) * (size_t)s.n_groups);
+  L.hist_coarse = off;
+  off = align_up(off + 4ull * tahq::kCoarseBins * (size_t)s.n_groups);
+  L.hist_fine = off;
+  off = align_up(off + 4ull * tahq::kFineBins * (size_t)s.n_groups);
+  L.lookback = off;
+  const long long chunks = tahq::encode_chunks(0, s.G, s.n_g, s.n_groups);
+  off = align_up(off + 8 * (size_t)chunks);
+  L.ctrl_end = off;
+  L.keys = off;
+  off = align_up(off + 4 * (size_t)s.n);
+  L.cand = off;
+  off = align_up(off + 8 * (size_t)s.n);
+  L.total = off;
+  return L;
+}
+
+struct DecLayout {
+  size_t status, ticket, lookback, total;
+};
+
+DecLayout dec_layout(const Shape& s) {
+  DecLayout L{};
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 16);
+  L.ticket = off;
+  off = align_up(off + 64);
+  L.lookback = off;
+  off = align_up(off + 8 * (size_t)tahq::decode_chunks(s.G, s.n));
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tahq_payload_size(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                         float budget, int64_t tokens_per_group) {
+  Shape s;
+  if (check_codec(tokens, channels, tile, -1, bits_lo, bits_hi, budget, tokens_per_group, s) !=
+      TAHQ_OK)
+    return 0;
+  return (size_t)s.payload;
+}
+
+int64_t tahq_hi_count(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                      float budget, int64_t tokens_per_group) {
+  Shape s;
+  if (check_codec(tokens, channels, tile, -1, bits_lo, bits_hi, budget, tokens_per_group, s) !=
+      TAHQ_OK)
+    return -1;
+  return s.K;
+}
+
+size_t tahq_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock, int bits_lo,
+                           int bits_hi, float budget, int64_t tokens_per_group) {
+  Shape s;
+  if (check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget, tokens_per_group,
+                  s) != TAHQ_OK)
+    return 0;
+  return enc_layout(s).total;
+}
+
+size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile) {
+  Shape s;
+  if (check_shape(tokens, channels, tile, -1, s) != TAHQ_OK) return 0;
+  return dec_layout(s).total;
+}
+
+tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                        int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                        int64_t tokens_per_group, uint8_t* codes, float* scales, float* zeros,
+                        uint8_t* bits, uint8_t* pivots, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  Shape s;
+  tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                               tokens_per_group, s);
+  if (st != TAHQ_OK) return st;
+  if (hblock < 0) return TAHQ_ERR_ARG;
+  if (dtype != TAHQ_F32 && dtype != TAHQ_BF16) return TAHQ_ERR_ARG;
+  if (s.n > 0) {
+    if (!x || !codes || !scales || !zeros || !bits || !pivots) return TAHQ_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(zeros, 4))
+      return TAHQ_ERR_ARG;
+  }
+  if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
+  const bool bf16 = dtype == TAHQ_BF16;
+  const EncLayout L = enc_layout(s);
+  if (workspace_bytes < L.total) return TAHQ_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, L.ctrl_end, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  if (s.n == 0) return TAHQ_OK;
+  const int sms = num_sms_current();
+  if (sms <= 0) return TAHQ_ERR_CUDA;
+
+  tahq::EncodeArgs a{};
+  a.x = x;
+  a.bf16 = bf16;
+  a.G = s.G;
+  a.h = s.h;
+  a.lo = s.lo;
+  a.hi = s.hi;
+  a.c_h = (float)(1.0 / std::sqrt((double)s.h));
+  a.n_tiles = s.n;
+  a.n_g = s.n_g;
+  a.n_groups = s.n_groups;
+  a.K = s.K;
+  a.group_bytes = s.group_bytes;
+  a.num_sms = sms;
+  a.tabs = &lg_tables();
+  a.codes = codes;
+  a.scales = scales;
+  a.zeros = zeros;
+  a.bits = bits;
+  a.pivots = pivots;
+  a.status = at<uint32_t>(workspace, L.status);
+  a.ticket = at<uint32_t>(workspace, L.ticket);
+  a.cand_cnt = at<uint32_t>(workspace, L.cand_cnt);
+  a.sel = at<tahq::SelResult>(workspace, L.sel);
+  a.hist_coarse = at<uint32_t>(workspace, L.hist_coarse);
+  a.hist_fine = at<uint32_t>(workspace, L.hist_fine);
+  a.lookback = at<unsigned long long>(workspace, L.lookback);
+  a.keys = at<float>(workspace, L.keys);
+  a.cand = at<unsigned long long>(workspace, L.cand);
+  return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}
+
+tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* scales,
+                        const float* zeros, const uint8_t* bits, const uint8_t* pivots,
+                        int64_t tokens, int64_t channels, int tile, int hblock, float* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  tahq_status st = check_shape(tokens, channels, tile, hblock, s);
+  if (st != TAHQ_OK) return st;
+  if (hblock < 0) return TAHQ_ERR_ARG;
+  if (s.n > 0) {
+    if (!scales || !zeros || !bits || !pivots || !out) return TAHQ_ERR_ARG;
+    if (codes_bytes > 0 && (!codes || !aligned(codes, 16))) return TAHQ_ERR_ARG;
+    if (!aligned(out, 16) || !aligned(scales, 4) || !aligned(zeros, 4)) return TAHQ_ERR_ARG;
+  }
+  if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
+  const DecLayout L = dec_layout(s);
+  if (workspace_bytes < L.total) return TAHQ_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, L.total, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  if (s.n == 0) return TAHQ_OK;
+  const int sms = num_sms_current();
+  if (sms <= 0) return TAHQ_ERR_CUDA;
+  tahq::DecodeArgs a{};
+  a.codes = codes;
+  a.codes_bytes = codes_bytes;
+  a.scales = scales;
+  a.zeros = zeros;
+  a.bits = bits;
+  a.pivots = pivots;
+  a.G = s.G;
+  a.h = s.h;
+  a.c_h = (float)(1.0 / std::sqrt((double)s.h));
+  a.n_tiles = s.n;
+  a.num_sms = sms;
+  a.out = out;
+  a.status = at<uint32_t>(workspace, L.status);
+  a.ticket = at<uint32_t>(workspace, L.ticket);
+  a.lookback = at<unsigned long long>(workspace, L.lookback);
+  return tahq::launch_decode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}
+
+tahq_status tahq_get_device_status(const void* workspace, uint32_t* status_out, void* stream) {
+  if (!workspace) return TAHQ_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return TAHQ_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  if (status_out) *status_out = word;
+  return word ? TAHQ_ERR_DEVICE_STATUS : TAHQ_OK;
+}
+
+const char* tahq_status_string(int status) {
+  switch (status) {
+    case TAHQ_OK: return "TAHQ_OK";
+    case TAHQ_ERR_ARG: return "TAHQ_ERR_ARG: an argument is outside the supported limits";
+    case TAHQ_ERR_UNSUPPORTED: return "TAHQ_ERR_UNSUPPORTED: valid parameters not built here";
+    case TAHQ_ERR_WORKSPACE: return "TAHQ_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case TAHQ_ERR_CUDA: return "TAHQ_ERR_CUDA: a CUDA call or kernel launch failed";
+    case TAHQ_ERR_DEVICE_STATUS: return "TAHQ_ERR_DEVICE_STATUS: the device reported an error";
+  }
+  return "unknown tahq_status";
+}
+
+int tahq_version(void) { return kVersion; }
+
+void tahq_log2_tables(float* T, float* R, float* k) {
+  const LgTables& t = lg_tables();
+  if (T) std::memcpy(T, t.T, sizeof t.T);
+  if (R) std::memcpy(R, t.R, sizeof t.R);
+  if (k) std::memcpy(k, t.k, sizeof t.k);
+}
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// tahq_device.cuh -- device building blocks of the sm_103a TAH-Quant codec.
+//
+// Arithmetic that decides an integer (the entropy key that ranks tiles, the outlier
+// flag, the quantised codes) is spelled out with explicit round-to-nearest intrinsics
+// (__fadd_rn, __fmul_rn, __fdiv_rn, __fmaf_rn), so that no contraction or reordering
+// can change a result.  The evaluation order is the canonical one of the codec:
+//   - pairwise sums: sum(x[0..n)) = sum(x[0..n/2)) + sum(x[n/2..n)),
+//   - lg(x) = e + (T[i] + r * P(r)), r = (m - c_i) * R[i], P a Horner polynomial,
+//   - entropy key H = lg(L) - S / L, L = sum |a|, S = sum |a| lg |a|,
+//   - Hadamard stages len = 1, 2, 4, ... then x RN(1/sqrt(h)),
+//   - u = (v - min) * inv, inv = Q / (max - min), code = rint(u) clamped to [0, Q].
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tahq {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Device status word bits (mirror the TAHQ_DEV_* macros of tahq.h).
+constexpr uint32_t kStNonFinite = 0x1u;
+constexpr uint32_t kStWaitTimeout = 0x2u;
+constexpr uint32_t kStSelectMismatch = 0x4u;
+constexpr uint32_t kStBadBits = 0x8u;
+constexpr uint32_t kStOverrun = 0x10u;
+
+// Tables of the canonical logarithm, passed to kernels by value and copied to shared
+// memory (indexed loads from the parameter bank would serialise).
+struct LgTables {
+  float T[128];
+  float R[128];
+  float k[4];
+};
+
+// One group's threshold: a tile is hi iff mode == kSelAll, or mode == kSelThreshold and
+// its composite rank key >= theta.
+struct SelResult {
+  unsigned long long theta;
+  uint32_t mode;
+  uint32_t pad;
+};
+constexpr uint32_t kSelNone = 0, kSelAll = 1, kSelThreshold = 2;
+
+// Fine-histogram geometry: bucket = floor(H * 8192) clamped to [0, 65535] (H is in bits,
+// 0 <= H <= log2(tile) <= 7), coarse bucket = bucket >> 8.
+constexpr int kFineBins = 65536;
+constexpr int kCoarseBins = 256;
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+  atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ canonical logarithm
+
+// kNoFraction: the caller guarantees that x has no mantissa bits below the top 7
+// (true for every bf16 value, normal or subnormal), so r == 0 and P is skipped; the
+// result is identical to the general path because r * P(r) = +0 there.
+template <bool kNoFraction>
+__device__ __forceinline__ float lg_canon(float x, const float* sT, const float* sR,
+                                          const float* sk) {
+  uint32_t b = __float_as_uint(x);
+  int e = (int)(b >> 23) - 127;
+  if ((b >> 23) == 0u) {  // subnormal: normalise by 2^24, exactly
+    b = __float_as_uint(__fmul_rn(x, 16777216.0f));
+    e = (int)(b >> 23) - 151;
+  }
+  const int i = (int)((b >> 16) & 0x7Fu);
+  float t;
+  if (kNoFraction) {
+    t = sT[i];
+  } else {
+    const float m = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+    const float c = __uint_as_float(0x3F800000u | ((uint32_t)i << 16));  // 1 + i/128
+    const float f = __fsub_rn(m, c);                                     // exact
+    const float r = __fmul_rn(f, sR[i]);
+    float p = __fmaf_rn(sk[3], r, sk[2]);
+    p = __fmaf_rn(p, r, sk[1]);
+    p = __fmaf_rn(p, r, sk[0]);
+    t = __fadd_rn(sT[i], __fmul_rn(p, r));
+  }
+  return __fadd_rn((float)e, t);
+}
+
+// Order-preserving 32-bit image of a float key (-0 is folded onto +0 first).
+__device__ __forceinline__ uint32_t order_key(float h) {
+  const uint32_t b = __float_as_uint(__fadd_rn(h, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Composite rank key of tile t_local of a group: larger = ranked earlier
+// (higher entropy first, then lower tile index).
+__device__ __forceinline__ unsigned long long rank_key(float h, uint32_t t_local) {
+  return ((unsigned long long)order_key(h) << 32) | (unsigned long long)(0xFFFFFFFFu - t_local);
+}
+
+__device__ __forceinline__ int fine_bin(float h) {
+  if (!(h >= 0.0f)) return 0;          // negative rounding residue or NaN
+  if (!(h < 8.0f)) return kFineBins - 1;
+  return (int)__fmul_rn(h, 8192.0f);   // truncation == floor for h >= 0
+}
+
+// ------------------------------------------------------------------ tile geometry
+
+// A tile of G values is spread over L = G / V consecutive lanes of a warp ("team"),
+// each lane holding V consecutive values.
+template <int kV, int kG>
+struct Geom {
+  static constexpr int V = kV;
+  static constexpr int G = kG;
+  static constexpr int L = kG / kV;
+  static constexpr int TPW = 32 / L;  // tiles per warp per step
+  static_assert(kG % kV == 0 && L >= 1 && L <= 32, "tile must span 1..32 lanes");
+};
+
+// Pairwise sum of the lane's V values.
+template <int V>
+__device__ __forceinline__ float lane_pairwise(const float* v) {
+  if constexpr (V == 8) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
+                     __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7])));
+  } else {
+    static_assert(V == 4, "V is 4 or 8");
+    return __fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3]));
+  }
+}
+
+// Continue the pairwise tree across the L lanes of a team (xor 1, 2, ..., L/2).
+template <int L>
+__device__ __forceinline__ float team_sum(float s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) s = __fadd_rn(s, __shfl_xor_sync(kFull, s, o));
+  return s;
+}
+
+template <int L>
+__device__ __forceinline__ float team_min(float s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) s = fminf(s, __shfl_xor_sync(kFull, s, o));
+  return s;
+}
+
+template <int L>
+__device__ __forceinline__ float team_max(float s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) s = fmaxf(s, __shfl_xor_sync(kFull, s, o));
+  return s;
+}
+
+// Top-2 magnitudes with the first arg-max, merged across the team.
+template <int L>
+__device__ __forceinline__ void team_top2(float& m1, int& i1, float& m2) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) {
+    const float om1 = __shfl_xor_sync(kFull, m1, o);
+    const int oi1 = __shfl_xor_sync(kFull, i1, o);
+    const float om2 = __shfl_xor_sync(kFull, m2, o);
+    if (om1 > m1 || (om1 == m1 && oi1 < i1)) {
+      m2 = fmaxf(m1, om2);
+      m1 = om1;
+      i1 = oi1;
+    } else {
+      m2 = fmaxf(m2, om1);
+    }
+  }
+}
+
+// In-register Sylvester FWHT of every h-block of the team's tile (h | G, h a power of
+// two), stages len = 1, 2, ..., h/2 in that order; the pair (j, j+len) -> (a+b, a-b).
+// Stages with len < V stay in the lane (indices are compile-time after unrolling);
+// stages with len >= V pair lane sub with lane sub ^ (len / V).  h is warp-uniform.
+template <int V, int L>
+__device__ __forceinline__ void team_fwht(float* v, int h, int sub) {
+#pragma unroll
+  for (int s = 0; (1 << s) < V; s++) {
+    const int len = 1 << s;
+    if (len < h) {
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        if ((j & len) == 0) {
+          const float a = v[j], b = v[j | len];
+          v[j] = __fadd_rn(a, b);
+          v[j | len] = __fsub_rn(a, b);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; (1 << s) < L; s++) {
+    const int lanes = 1 << s;
+    if (lanes * V < h) {
+      const bool upper = (sub & lanes) != 0;
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        const float o = __shfl_xor_sync(kFull, v[j], lanes);
+        v[j] = upper ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+      }
+    }
+  }
+}
+
+// Swap tile positions 0 and d (d < G) across the team: lane 0 of the team holds
+// position 0, lane d / V holds position d.  All lanes of the warp must call this.
+template <int V>
+__device__ __forceinline__ void team_swap0(float* v, int d, int sub, int team_base_lane) {
+  const int dl = d / V, dj = d % V;
+  float vd = v[0];
+#pragma unroll
+  for (int j = 0; j < V; j++)
+    if (j == dj) vd = v[j];
+  const float x0 = __shfl_sync(kFull, v[0], team_base_lane);
+  const float xd = __shfl_sync(kFull, vd, team_base_lane + dl);
+  if (d != 0) {
+    if (sub == 0) v[0] = xd;
+#pragma unroll
+    for (int j = 0; j < V; j++)
+      if (sub == dl && j == dj) v[j] = x0;
+  }
+}
+
+// ------------------------------------------------------------------ bounded waits
+
+constexpr long long kSpinLimit = 1ll << 22;  // ~0.5 s of 128 ns naps
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Decoupled look-back words: top two bits = state, low 62 bits = value.
+constexpr unsigned long long kLbAgg = 1ull << 62;
+constexpr unsigned long long kLbPre = 2ull << 62;
+constexpr unsigned long long kLbVal = (1ull << 62) - 1;
+
+// Exclusive prefix of chunk `c` over chunks [first, c): called by one thread after it
+// published its own aggregate.  Chunks are handed out in increasing order by an atomic
+// ticket, so every predecessor is already running.  Gives up (status bit, prefix 0)
+// after kSpinLimit naps rather than wait without a bound.
+__device__ __forceinline__ unsigned long long lookback_prefix(const unsigned long long* words,
+                                                              long long c, long long first,
+                                                              uint32_t* status) {
+  unsigned long long acc = 0;
+  long long p = c - 1;
+  long long spins = 0;
+  while (p >= first) {
+    const unsigned long long w = ld_acquire_u64(words + p);
+    const unsigned long long st = w & ~kLbVal;
+    if (st == kLbPre) {
+      acc += w & kLbVal;
+      return acc;
+    }
+    if (st == kLbAgg) {
+      acc += w & kLbVal;
+      --p;
+      continue;
+    }
+    if (++spins > kSpinLimit) {
+      set_status(status, kStWaitTimeout);
+      return 0;
+    }
+    __nanosleep(128);
+  }
+  return acc;
+}
+
+}  // namespace tahq

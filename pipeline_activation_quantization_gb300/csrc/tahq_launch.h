@@ -1,0 +1,63 @@
+// tahq_launch.h -- host-side launch interface between the C ABI (tahq_api.cu) and the
+// kernel translation units (tahq_encode.cu, tahq_decode.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tahq_device.cuh"
+
+namespace tahq {
+
+// Everything one encode launch sequence needs; pointers are device pointers carved out
+// of the caller's output buffers and workspace.
+struct EncodeArgs {
+  const void* x;
+  bool bf16;
+  int G, h, lo, hi;
+  float c_h;                 // RN(1/sqrt(h))
+  long long n_tiles, n_g, n_groups, K, group_bytes;
+  int num_sms;
+  const LgTables* tabs;
+  uint8_t* codes;
+  float* scales;
+  float* zeros;
+  uint8_t* bits;
+  uint8_t* pivots;
+  // workspace
+  uint32_t* status;
+  uint32_t* ticket;
+  uint32_t* cand_cnt;        // [n_groups]
+  SelResult* sel;            // [n_groups]
+  uint32_t* hist_coarse;     // [n_groups * kCoarseBins]
+  uint32_t* hist_fine;       // [n_groups * kFineBins]
+  unsigned long long* lookback;  // [encode_chunks]
+  float* keys;               // [n_tiles]
+  unsigned long long* cand;  // [n_tiles]
+};
+
+struct DecodeArgs {
+  const uint8_t* codes;
+  unsigned long long codes_bytes;
+  const float* scales;
+  const float* zeros;
+  const uint8_t* bits;
+  const uint8_t* pivots;
+  int G, h;
+  float c_h;
+  long long n_tiles;
+  int num_sms;
+  float* out;
+  uint32_t* status;
+  uint32_t* ticket;
+  unsigned long long* lookback;  // [decode_chunks]
+};
+
+// Number of look-back chunks the encode / decode kernels use for these shapes.
+long long encode_chunks(int bf16, int G, long long n_g, long long n_groups);
+long long decode_chunks(int G, long long n_tiles);
+
+cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace tahq
