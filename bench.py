@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Throughput of the sm_103a TAH-Quant activation codec (encode + decode round trip).
+
+One step = tahq_encode + tahq_decode of one synthetic activation tensor that is already
+resident in HBM (the whole hot path).  Default workload: the Llama-7B-like pipeline
+boundary, 8 x 2048 x 4096 bf16 (16384 tokens), tile = Hadamard block = 64, bits {3, 4},
+budget 3.0, ranking per 2048-token sample.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W --workload c3|c2|c4|c5 ...]
+  python bench.py --impl reference     # the CPU oracle on the host cores (reference arm)
+
+value = input-activation GB/s of the round trip, all ranks together (replicas: each GPU
+encodes and decodes its own tensor, no collective on the data path).  Every step is timed
+with CUDA events on the launching stream; L2 is flushed (a 256 MiB write) between steps,
+outside the events.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "encode+decode GB/s of activations (tokens/s) and % of GB300 HBM roofline"
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _workload(args) -> synth.Workload:
+    w = synth.WORKLOADS[args.workload]
+    kw = {}
+    if args.tile:
+        kw["tile"] = args.tile
+        kw["hblock"] = args.tile
+    if args.hblock:
+        kw["hblock"] = args.hblock
+    if args.budget is not None:
+        kw["budget"] = args.budget
+    return w.with_params(**kw) if kw else w
+
+
+def _config(w: synth.Workload, extra=None) -> dict:
+    c = {"workload": w.name, "tokens": w.tokens, "channels": w.channels, "input_dtype": w.dtype,
+         "tile": w.tile, "hblock": w.hblock, "bits": [w.bits_lo, w.bits_hi], "budget": w.budget,
+         "tokens_per_group": w.tokens_per_group, "seed": w.seed,
+         "l2": "flushed between steps (256 MiB write, outside the events)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def _alg_bytes(w: synth.Workload, payload: int):
+    n = w.tokens * w.channels // w.tile
+    in_b = w.in_bytes
+    enc = in_b + payload + 10 * n
+    dec = payload + 10 * n + 4 * w.elements
+    return in_b, enc, dec
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed loop runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
+    kernel sources changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    e = rec.get(f"{kernel}|{workload}")
+    if not e or e.get("src_sha") != _src_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def _src_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "pipeline_activation_quantization_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+
+def _oracle_step(x, w, tokens):
+    import oracle
+    xs = x[:tokens]
+    S = min(w.tokens_per_group or w.tokens, tokens)
+    r = oracle.encode(xs, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S)
+    oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], tokens, w.channels,
+                  w.tile, w.hblock)
+
+
+def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0) -> dict:
+    """The oracle, single thread, on whole token groups of the same tensor."""
+    S = w.tokens_per_group or w.tokens
+    t0 = time.perf_counter()
+    _oracle_step(x, w, S)
+    one = time.perf_counter() - t0
+    groups = max(1, min(w.tokens // S, int(target_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for g in range(groups):
+        _oracle_step(x[g * S:], w, S)
+    dt = time.perf_counter() - t0
+    toks = groups * S
+    gbs = toks * w.channels * (4 if w.dtype == "f32" else 2) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": round(toks / dt, 1),
+            "sample": f"{groups} of {w.tokens // S} token groups ({toks} tokens) encoded+decoded, "
+                      f"single-threaded scalar C (-O2 -ffp-contract=off), {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = _workload(args)
+    x = synth.generate(w)
+    S = w.tokens_per_group or w.tokens
+    tok = S
+    for _ in range(args.warmup):
+        _oracle_step(x, w, tok)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        g = k % max(1, w.tokens // S)
+        _oracle_step(x[g * S:], w, tok)
+    dt = time.perf_counter() - t0
+    in_b = tok * w.channels * (4 if w.dtype == "f32" else 2)
+    gbs = in_b * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(w, {"sample_tokens_per_step": tok}),
+        "tokens_per_s": round(tok * args.steps / dt, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step encodes+decodes one {tok}-token group of the "
+                                   f"workload on one host core (scalar C oracle)"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ the CUDA path
+
+def run_gpu(args):
+    import torch
+    import pipeline_activation_quantization_gb300 as tq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = _workload(args)
+    T, C, G, h = w.tokens, w.channels, w.tile, w.hblock
+    x_np = synth.generate(w, index=rank)
+    dev = torch.device("cuda", local)
+    if w.dtype == "bf16":
+        x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(x_np).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    with torch.cuda.stream(stream):
+        enc = tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
+        y = tq.decode(enc, T, C, G, h)
+        dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8, device=dev)
+    payload = enc["payload_bytes"]
+    out_bufs = {k: enc[k] for k in ("codes", "scales", "zeros", "bits", "pivots")}
+    ws = enc["workspace"]
+    K_hi = tq.tahq_hi_count(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
+    n_g = (w.tokens_per_group or T) * (C // G)
+    launches = 3 + (1 if 0 < K_hi < n_g else 0) + 1   # stats, [collect], final, quant; decode
+
+    def step(ev):
+        ev[0].record(stream)
+        tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group, out=out_bufs,
+                  workspace=ws, stream=stream)
+        ev[1].record(stream)
+        tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
+        ev[2].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step(warm)
+    stream.synchronize()
+    barrier()
+    sampler = ClockSampler(local)
+    with sampler:
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.fill_(k & 255)
+                step(evs[k])
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    enc_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    tot_ms = sum(enc_ms) + sum(dec_ms)
+    rc, word = tq.tahq_get_device_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {word:#x} after the timed loop")
+    if dist is not None:
+        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+
+    in_b, enc_b, dec_b = _alg_bytes(w, payload)
+    peak, peak_kind = _peaks()
+    ms_step = tot_ms / args.steps
+    value = world * in_b * args.steps / (tot_ms * 1e-3) / 1e9
+    e_ms, d_ms = statistics.mean(enc_ms), statistics.mean(dec_ms)
+    enc_gbs, dec_gbs = enc_b / (e_ms * 1e-3) / 1e9, dec_b / (d_ms * 1e-3) / 1e9
+    dom = ("k_decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
+    dom_name = f"k_decode<{G}>" if dom[0] == "k_decode" else "tahq_encode (4 kernels)"
+
+    # end to end through the public API: pinned host input -> device, encode, decode,
+    # decoded tensor -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.from_numpy(x_np.view(np.int16) if w.dtype == "bf16" else x_np).pin_memory()
+        y_host = torch.empty((T, C), dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(x)
+        n_e2e = max(3, min(20, args.steps))
+        with torch.cuda.stream(stream):
+            def e2e_step():
+                if w.dtype == "bf16":
+                    x_dev.view(torch.int16).copy_(x_host, non_blocking=True)
+                else:
+                    x_dev.copy_(x_host, non_blocking=True)
+                tq.encode(x_dev, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
+                          out=out_bufs, workspace=ws, stream=stream)
+                tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
+                y_host.copy_(y, non_blocking=True)
+            e2e_step()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": round(world * in_b / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": 4 * w.elements,
+               "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
+
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, x_np)
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}"}),
+        "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
+        "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "encode": {"ms": round(e_ms, 5), "alg_bytes": enc_b, "GB_s": round(enc_gbs, 2),
+                   "frac": round(enc_gbs / peak, 4), "input_GB_s": round(in_b / (e_ms * 1e-3) / 1e9, 2),
+                   "tokens_per_s": round(T / (e_ms * 1e-3), 1)},
+        "decode": {"ms": round(d_ms, 5), "alg_bytes": dec_b, "GB_s": round(dec_gbs, 2),
+                   "frac": round(dec_gbs / peak, 4), "tokens_per_s": round(T / (d_ms * 1e-3), 1)},
+        "roofline": {"bound": "hbm", "kernel": dom_name,
+                     "achieved": round(dom[1] / (dom[2] * 1e-3) / 1e9, 2), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
+                     "frac": round(dom[1] / (dom[2] * 1e-3) / 1e9 / peak, 4),
+                     "traffic": _traffic_for(dom_name, w.name)},
+        "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+        "gpu_launches_per_step": launches, "clocks": clocks,
+        "wall_s_timed_loop": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="tahq", choices=["tahq", "reference"])
+    ap.add_argument("--workload", default="c3", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--hblock", type=int, default=0)
+    ap.add_argument("--budget", type=float, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        if args.steps == 2000:
+            args.steps = 8
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

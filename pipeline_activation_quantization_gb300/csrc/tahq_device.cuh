@@ -82,8 +82,12 @@ __device__ __forceinline__ float lg_canon(float x, const float* sT, const float*
   return __fadd_rn((float)e, t);
 }
 
-// Order-preserving 32-bit image of a float key (-0 is folded onto +0 first).
+// Order-preserving 32-bit image of a float key (-0 is folded onto +0 first).  NaN (only
+// from non-finite input) maps to the lowest rank, as fine_bin puts it in bucket 0, so
+// the histogram and the rank keys always agree and a group never gets more than K hi
+// tiles.
 __device__ __forceinline__ uint32_t order_key(float h) {
+  if (h != h) return 0u;
   const uint32_t b = __float_as_uint(__fadd_rn(h, 0.0f));
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }

@@ -349,7 +349,8 @@ struct QuantCfg {
 
 template <typename Tin, int G>
 __global__ void __launch_bounds__(256) k_quant(
-    const Tin* __restrict__ x, long long n_g, long long group_bytes, int lo, int hi, int h,
+    const Tin* __restrict__ x, long long n_g, long long group_bytes, long long codes_bytes,
+    int lo, int hi, int h,
     float c_h, const float* __restrict__ keys, const uint8_t* __restrict__ piv_in,
     const SelResult* __restrict__ sel, uint8_t* __restrict__ codes, float* __restrict__ scales,
     float* __restrict__ zeros, uint8_t* __restrict__ bits,
@@ -421,9 +422,13 @@ __global__ void __launch_bounds__(256) k_quant(
       }
       s_base = g * group_bytes + lc * (long long)CH * slot_lo + (long long)prefix * slot_d;
     }
-    const int chunk_bytes = nt * slot_lo + (int)chunk_hi * slot_d;
+    int chunk_bytes = nt * slot_lo + (int)chunk_hi * slot_d;
     __syncthreads();
     const long long base = s_base;
+    if (base + chunk_bytes > codes_bytes) {  // only if the select went wrong: never write past
+      if (threadIdx.x == 0) set_status(status, kStSelectMismatch);
+      chunk_bytes = (int)max(0ll, codes_bytes - base);
+    }
     const int pad = (int)(base & 15);
     const int stage_words = (pad + chunk_bytes + 15) / 16 * 4;
     for (int i = threadIdx.x; i < stage_words; i += Cf::kThreads) s_stage[i] = 0u;
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(256) k_quant(
         if (degenerate) q = 0u;
         acc |= (unsigned long long)q << (j * b);
       }
-      if (valid) {
+      if (valid && (int)s_off[kt] + G * b / 8 <= chunk_bytes) {
         const int pos = 8 * (pad + (int)s_off[kt]) + sub * V * b;
         const int wi = pos >> 5, sh = pos & 31;
         const unsigned long long lo64 = acc << sh;
@@ -538,7 +543,8 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   const long long n_chunks = encode_chunks(a.bf16, G, a.n_g, a.n_groups);
   const int quant_blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   k_quant<Tin, G><<<quant_blocks, 256, 0, st>>>(
-      x, a.n_g, a.group_bytes, a.lo, a.hi, a.h, a.c_h, a.keys, a.pivots, a.sel, a.codes,
+      x, a.n_g, a.group_bytes, a.n_groups * a.group_bytes, a.lo, a.hi, a.h, a.c_h, a.keys,
+      a.pivots, a.sel, a.codes,
       a.scales, a.zeros, a.bits, a.lookback, a.ticket, a.status, n_chunks);
   return cudaGetLastError();
 }

@@ -7,8 +7,12 @@ Every tensor is row-major ``[tokens, channels]``. ``bf16`` tensors are returned 
 ``uint16`` bit patterns (rounded from fp32 to nearest-even); ``f32`` tensors as
 ``float32``. Draws come from ``numpy.random.Generator(PCG64(seed))`` in a fixed
 order: base values, per-token RMS, outlier channels, per-channel factors,
-element positions, signs. Base values are drawn in float64 in blocks of 1024
-rows and rounded to float32; counts use Python ``round``.
+element positions, signs. Tensor ``index`` of a workload uses the seed sequence
+``SeedSequence([seed, index])``; its first child draws everything but the base
+values, and child ``1 + i`` draws the base values of rows ``[1024 i, 1024 (i+1))``
+(so blocks can be drawn on several host threads with the same result). Normal
+draws are float32; the others are drawn in float64 and rounded to float32.
+Counts use Python ``round``.
 
 The workloads stand in for the activations that "TAH-Quant: Effective Activation
 Quantization in Pipeline Parallelism over Slow Network" sends between stages
@@ -17,6 +21,9 @@ Quantization in Pipeline Parallelism over Slow Network" sends between stages
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "generate", "f32_to_bf16_bits", "bf16_bits_to_f32",
@@ -81,30 +88,40 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _draw_rows(rng: np.random.Generator, tokens: int, channels: int, draw) -> np.ndarray:
+def _draw_rows(blocks, tokens: int, channels: int, draw, threads: int) -> np.ndarray:
     out = np.empty((tokens, channels), dtype=np.float32)
-    for r0 in range(0, tokens, _ROW_BLOCK):
+
+    def one(i):
+        r0 = i * _ROW_BLOCK
         r1 = min(tokens, r0 + _ROW_BLOCK)
-        out[r0:r1] = draw(rng, (r1 - r0, channels)).astype(np.float32)
+        out[r0:r1] = draw(np.random.Generator(np.random.PCG64(blocks[i])), (r1 - r0, channels))
+
+    n = (tokens + _ROW_BLOCK - 1) // _ROW_BLOCK
+    if threads > 1 and n > 1:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(n)))
+    else:
+        for i in range(n):
+            one(i)
     return out
 
 
-def _values(w: Workload, rng: np.random.Generator) -> np.ndarray:
+def _values(w: Workload, rng: np.random.Generator, blocks, threads: int) -> np.ndarray:
     T, C = w.tokens, w.channels
     if w.dist == "gauss_fixed_channels":
-        x = _draw_rows(rng, T, C, lambda g, s: g.standard_normal(s))
+        x = _draw_rows(blocks, T, C, lambda g, s: g.standard_normal(s, dtype=np.float32), threads)
         chans = [c for c in (7, 300, 611, 1000) if c < C]
         x[:, chans] *= np.float32(50.0)
         return x
     if w.dist == "student_t":
-        x = _draw_rows(rng, T, C, lambda g, s: 0.5 * g.standard_t(3.0, s))
+        x = _draw_rows(blocks, T, C, lambda g, s: 0.5 * g.standard_t(3.0, s), threads)
         k = round(0.005 * C)
         chans = rng.choice(C, k, replace=False)
         fac = np.exp(rng.uniform(np.log(20.0), np.log(100.0), k)).astype(np.float32)
         x[:, chans] *= fac[None, :]
         return x
     if w.dist == "gauss_rms_spikes":
-        x = _draw_rows(rng, T, C, lambda g, s: g.standard_normal(s))
+        x = _draw_rows(blocks, T, C, lambda g, s: g.standard_normal(s, dtype=np.float32), threads)
         rms = rng.lognormal(0.0, 0.5, T).astype(np.float32)
         x *= rms[:, None]
         k = round(0.002 * C)
@@ -116,7 +133,7 @@ def _values(w: Workload, rng: np.random.Generator) -> np.ndarray:
         x.reshape(-1)[pos] = np.float32(500.0) * sign
         return x
     if w.dist == "laplace":
-        x = _draw_rows(rng, T, C, lambda g, s: g.laplace(0.0, 1.0, s))
+        x = _draw_rows(blocks, T, C, lambda g, s: g.laplace(0.0, 1.0, s), threads)
         k = round(0.001 * C)
         chans = rng.choice(C, k, replace=False)
         x[:, chans] *= np.float32(50.0)
@@ -124,15 +141,18 @@ def _values(w: Workload, rng: np.random.Generator) -> np.ndarray:
     raise ValueError(f"unknown distribution {w.dist!r}")
 
 
-def generate(w: Workload, rng: np.random.Generator | None = None) -> np.ndarray:
-    """Draw one ``[tokens, channels]`` tensor for workload ``w``.
+def generate(w: Workload, index: int = 0, threads: int | None = None) -> np.ndarray:
+    """Draw tensor number ``index`` ([tokens, channels]) of workload ``w``.
 
-    Pass ``rng`` to draw several fresh tensors from one stream (the 50-tensor
-    steady-state run of the 8192-channel workload draws them in sequence).
+    The steady-state run of the 8192-channel workload uses fresh tensors
+    ``index = 0, 1, 2, ...`` of the same seed.
     """
-    if rng is None:
-        rng = np.random.Generator(np.random.PCG64(w.seed))
-    x = _values(w, rng)
+    n_blocks = (w.tokens + _ROW_BLOCK - 1) // _ROW_BLOCK
+    kids = np.random.SeedSequence([w.seed, index]).spawn(1 + n_blocks)
+    rng = np.random.Generator(np.random.PCG64(kids[0]))
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
+    x = _values(w, rng, kids[1:], threads)
     if w.dtype == "bf16":
         return f32_to_bf16_bits(x)
     return x
