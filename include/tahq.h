@@ -122,6 +122,40 @@ tahq_status tahq_decode(const uint8_t *codes, size_t codes_bytes, const float *s
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Size of the fixed device scratch array behind tahq_decode_noalloc: 256 KiB, held in
+ * the memory of every GPU that loads the library until the process exits.  It bounds
+ * the shapes that entry point accepts: tahq_decode_workspace_size(tokens, channels,
+ * tile) must not exceed it, i.e. at most 32704 look-back chunks -- about 4.2 M tiles of
+ * width 128, 8.4 M of width 64, 16.7 M of width 32, 33.5 M of width 16, 67 M of width 8.
+ */
+#define TAHQ_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+/*
+ * tahq_decode for callers that cannot allocate device memory at all -- for example a
+ * receiving stage whose runtime plans every device buffer in advance and gives the codec
+ * only its inputs and outputs, or a C caller with no device allocator, for which a
+ * cudaMalloc inside the receive loop would also stall the whole device.  (The paper has
+ * no counterpart to this entry point: it is a packaging choice of this library.)
+ * Same arguments and results as tahq_decode, minus the workspace: the scratch comes from
+ * a fixed array inside the library (TAHQ_NOALLOC_SCRATCH_BYTES).  Nothing is allocated:
+ * no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - Shapes that need more scratch than the array holds are rejected with
+ *     TAHQ_ERR_WORKSPACE before anything is launched.
+ *   - Every call on a device shares the one array.  Each call clears the part it uses
+ *     first, but calls whose work overlaps on the GPU (other streams, other host threads)
+ *     race on it: order them on one stream or use tahq_decode with separate workspaces.
+ *   - device_status (device pointer, may be NULL) receives a copy of the call's device
+ *     status word (TAHQ_DEV_* bits) when the decode kernel has finished, ordered on
+ *     `stream`.
+ */
+tahq_status tahq_decode_noalloc(const uint8_t *codes, size_t codes_bytes, const float *scales,
+                                const float *zeros, const uint8_t *bits, const uint8_t *pivots,
+                                int64_t tokens, int64_t channels, int tile, int hblock,
+                                float *out, uint32_t *device_status, void *stream);
+
+/*
  * Copy the device status word of the last call that used `workspace` into *status_out
  * (may be NULL) after synchronising `stream` (only that stream).  Returns TAHQ_OK if
  * the word is zero, TAHQ_ERR_DEVICE_STATUS if not, TAHQ_ERR_CUDA if the copy failed.

@@ -20,7 +20,7 @@ __all__ = [
     "TAHQ_F32", "TAHQ_BF16", "TahqError", "lib", "tahq_payload_size", "tahq_hi_count",
     "tahq_workspace_size", "tahq_decode_workspace_size", "tahq_encode", "tahq_decode",
     "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
-    "encode", "decode", "EXPORTED_SYMBOLS",
+    "tahq_decode_noalloc", "encode", "decode", "EXPORTED_SYMBOLS",
 ]
 
 TAHQ_F32, TAHQ_BF16 = 0, 1
@@ -32,7 +32,7 @@ DEV_NONFINITE, DEV_WAIT_TIMEOUT, DEV_SELECT_MISMATCH, DEV_BAD_BITS, DEV_STREAM_O
 EXPORTED_SYMBOLS = (
     "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode",
     "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
-    "tahq_status_string", "tahq_version", "tahq_log2_tables",
+    "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
 )
 
 
@@ -67,6 +67,7 @@ def lib(path: str | None = None):
         "tahq_status_string": (C.c_char_p, [i32]),
         "tahq_version": (i32, []),
         "tahq_log2_tables": (None, [p, p, p]),
+        "tahq_decode_noalloc": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, p, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -126,6 +127,15 @@ def tahq_decode(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channel
     return lib().tahq_decode(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros), _ptr(bits),
                              _ptr(pivots), tokens, channels, tile, hblock, _ptr(out),
                              _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def tahq_decode_noalloc(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile,
+                        hblock, out, device_status=None, stream=None) -> int:
+    """tahq_decode without a workspace, for callers that cannot allocate device memory
+    (the scratch is a fixed array inside the library; see include/tahq.h)."""
+    return lib().tahq_decode_noalloc(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros),
+                                     _ptr(bits), _ptr(pivots), tokens, channels, tile, hblock,
+                                     _ptr(out), _ptr(device_status), _stream(stream))
 
 
 def tahq_get_device_status(workspace, stream=None) -> tuple[int, int]:
