@@ -35,7 +35,8 @@
  *     by (H descending, tile index ascending).
  *   - pivot goes to tile position 0; with hblock h < G the Hadamard is block diagonal.
  *   - Sylvester natural order, FWHT stages len = 1, 2, 4, ..., then x RN(1/sqrt(h)).
- *   - quantizer: min/max affine, float zero-point = min, round to nearest even;
+ *   - quantizer: min/max affine, float zero-point = min (a zero minimum emitted as +0),
+ *     round to nearest even;
  *     a tile whose range max-min is below 2^-120 (this includes max == min) is
  *     encoded as constant: scale 0, all codes 0, zero = min.
  *   - code k of a tile occupies bits [k*b, k*b+b) of its slot, LSB first within
@@ -243,7 +244,7 @@ void oracle_quantize_tile(const float *v, int G, int b, uint8_t *q, float *scale
     }
     int Q = (1 << b) - 1;
     float D = mx - mn;
-    *zero = mn;
+    *zero = mn + 0.0f;   /* a minimum of zero is emitted as +0 (the set's -0/+0 are equal) */
     if (!(D >= 0x1p-120f)) {
         *scale = 0.0f;
         for (int k = 0; k < G; k++) { q[k] = 0; if (near) near[k] = 0; }
