@@ -87,8 +87,8 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
 }
 
 struct EncLayout {
-  size_t status, ticket, cand_cnt, sel, hist_coarse, hist_fine, lookback, ctrl_end, keys, cand,
-      total;
+  size_t status, ticket, cand_cnt, doneA, doneB, selready, sel, hist_coarse, hist_fine, lookback,
+      ctrl_end, keys, cand, total;
 };
 
 // Look-back words are sized for fp32 input, whose smaller chunks need the most of them.
@@ -100,6 +100,12 @@ EncLayout enc_layout(const Shape& s) {
   L.ticket = off;
   off = align_up(off + 64);
   L.cand_cnt = off;
+  off = align_up(off + 4 * (size_t)s.n_groups);
+  L.doneA = off;
+  off = align_up(off + 4 * (size_t)s.n_groups);
+  L.doneB = off;
+  off = align_up(off + 4 * (size_t)s.n_groups);
+  L.selready = off;
   off = align_up(off + 4 * (size_t)s.n_groups);
   L.sel = off;
   off = align_up(off + sizeof(tahq::SelResult) * (size_t)s.n_groups);
@@ -227,6 +233,9 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.status = at<uint32_t>(workspace, L.status);
   a.ticket = at<uint32_t>(workspace, L.ticket);
   a.cand_cnt = at<uint32_t>(workspace, L.cand_cnt);
+  a.doneA = at<uint32_t>(workspace, L.doneA);
+  a.doneB = at<uint32_t>(workspace, L.doneB);
+  a.selready = at<uint32_t>(workspace, L.selready);
   a.sel = at<tahq::SelResult>(workspace, L.sel);
   a.hist_coarse = at<uint32_t>(workspace, L.hist_coarse);
   a.hist_fine = at<uint32_t>(workspace, L.hist_fine);

@@ -2,141 +2,145 @@
 //
 // "TAH-Quant: Effective Activation Quantization in Pipeline Parallelism over Slow
 // Network" (arXiv 2506.01352v2):
-//   k_stats          §3.2 eq. (1)-(2) entropy key, §3.3 eq. (3) outlier ratio + pivot,
-//                    plus the per-group key histograms the allocator selects from;
-//   k_select_collect §3.2 "Top-p% tile selection": locate the histogram bucket that holds
-//   k_select_final   the K-th ranked tile of each group and resolve it exactly;
-//   k_quant          §3.3 pivot swap + eq. (4) Hadamard, asymmetric quantizer, and the
-//                    §3.4 contiguous uint8 stream (slot offsets by a decoupled look-back).
+//   stats    §3.2 eq. (1)-(2): entropy key of every tile, plus the per-group key
+//            histograms the allocator selects from;
+//   select   §3.2 "Top-p% tile selection": the K tiles of highest (key, -index) of each
+//            group get the high bit width -- histogram bucket, then an exact radix
+//            select among the candidates of that bucket;
+//   quant    §3.3 eq. (3) outlier ratio and pivot, pivot swap + eq. (4) Hadamard, the
+//            asymmetric quantizer, and §3.4's contiguous uint8 stream.
+//
+// k_encode runs the three as work items of one persistent kernel.  Items are handed out
+// in increasing order by an atomic ticket and only ever wait for earlier items, so every
+// wait ends.  The order keeps a group's input in L2 between its stats pass and its
+// quantize pass: round r = the select items of group r-1, then the stats items of group
+// r interleaved with the quantize items of group r-lag.  Each block double-buffers 32 KB
+// input chunks in shared memory with bulk (TMA) copies.  A quantize item finds its
+// offset in the stream from the hi-tile counts of the group's earlier chunks; a count
+// not yet published is computed on the spot from the keys, so that search never waits.
+//
+// k_encode_flat covers allocations that do not depend on the ranking (K = 0 or K = n_g,
+// every tile gets the same width): one streaming pass, fixed slot offsets.
+//
+// Within a chunk, pass 1 quantises every tile that provably needs no transform (two or
+// more values with |v| >= max|v| / 2 give r <= tau); pass 2 takes the remaining tiles,
+// compacted, and applies the exact ratio test, pivot swap and Hadamard transform.
 #include <algorithm>
 #include <cfloat>
 
 #include "tahq_device.cuh"
 #include "tahq_launch.h"
+#include "tahq_tile.cuh"
 
 namespace tahq {
 
-template <typename Tin>
-struct InTraits;
-template <>
-struct InTraits<float> {
-  static constexpr int V = 4;
-  static constexpr bool kNoFraction = false;
-};
-template <>
-struct InTraits<uint16_t> {  // bf16 bit patterns
-  static constexpr int V = 8;
-  static constexpr bool kNoFraction = true;
-};
-
-// One 16-byte streaming load of a lane's V consecutive values, widened to fp32.
-template <typename Tin>
-__device__ __forceinline__ void load_lane(const Tin* __restrict__ x, long long elem, float* v) {
-  uint4 w;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-               : "l"(x + elem));
-  if constexpr (sizeof(Tin) == 4) {
-    v[0] = __uint_as_float(w.x);
-    v[1] = __uint_as_float(w.y);
-    v[2] = __uint_as_float(w.z);
-    v[3] = __uint_as_float(w.w);
-  } else {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      v[2 * j] = __uint_as_float(ws[j] << 16);            // element 2j: low half
-      v[2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u); // element 2j+1: high half
-    }
-  }
-}
-
-__device__ __forceinline__ void load_tables(const LgTables& tabs, float* sT, float* sR, float* sk) {
-  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
-    sT[i] = tabs.T[i];
-    sR[i] = tabs.R[i];
-  }
-  if (threadIdx.x < 4) sk[threadIdx.x] = tabs.k[threadIdx.x];
-}
-
-// ====================================================================== tile statistics
+constexpr int kChunkBytes = 32768;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
 template <typename Tin, int G>
-__global__ void __launch_bounds__(256) k_stats(const Tin* __restrict__ x, long long n_tiles,
-                                               long long n_g, LgTables tabs,
-                                               float* __restrict__ keys,
-                                               uint8_t* __restrict__ pivots,
-                                               uint32_t* __restrict__ hist_coarse,
-                                               uint32_t* __restrict__ hist_fine,
-                                               uint32_t* __restrict__ status) {
-  constexpr int V = InTraits<Tin>::V;
-  using Gm = Geom<V, G>;
-  constexpr int L = Gm::L;
-  __shared__ float sT[128], sR[128], sk[4];
-  load_tables(tabs, sT, sR, sk);
-  __syncthreads();
+struct Cfg {
+  using Gm = TileGeom<Tin, G>;
+  static constexpr int V = Gm::V, W = Gm::W, L = Gm::L, TPW = Gm::TPW;
+  static constexpr int CH = kChunkBytes / (G * (int)sizeof(Tin));  // tiles per chunk
+  static constexpr int kSteps = CH / (kWarps * TPW);               // warp steps per chunk
+  static constexpr int kPer = (CH + kThreads - 1) / kThreads;      // tiles per thread (scan)
+  static constexpr int kStage = CH * G + 64;                       // b <= 8, plus slack
+  static_assert(kSteps * kWarps * TPW == CH, "chunk must be whole warp steps");
+  static_assert(kPer <= 32, "hi flags are kept in one word per thread");
+};
 
-  const int lane = threadIdx.x & 31;
-  const int team = lane / L, sub = lane % L;
-  const long long n_steps = (n_tiles + Gm::TPW - 1) / Gm::TPW;
-  const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long step = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; step < n_steps;
-       step += n_warps) {
-    const long long t = step * Gm::TPW + team;
-    const bool valid = t < n_tiles;
-    float v[V];
-    if (valid) {
-      load_lane<Tin>(x, t * G + sub * V, v);
-    } else {
-#pragma unroll
-      for (int j = 0; j < V; j++) v[j] = 0.0f;
-    }
-    float m[V];
-#pragma unroll
-    for (int j = 0; j < V; j++) m[j] = fabsf(v[j]);
+template <typename Tin, int G>
+struct alignas(128) EncSmem {
+  using C = Cfg<Tin, G>;
+  unsigned char buf[2][kChunkBytes];
+  unsigned char stage[C::kStage];
+  float Trep[128 * 32];  // lg tables replicated per bank: entry i of lane l at i*32 + l
+  float Rrep[InTraits<Tin>::kNoFraction ? 4 : 128 * 32];
+  float T[128], R[128], k[4];
+  float scale[C::CH], zero[C::CH];
+  uint16_t off[C::CH];
+  uint16_t cand[C::CH];
+  uint8_t bits[C::CH], piv[C::CH];
+  uint32_t hist[kCoarseBins];
+  uint32_t scan[kWarps + 4];
+  unsigned long long bar[2];
+  long long next, base;
+  uint32_t last, ncand;
+};
 
-    // top-2 magnitudes and the first arg-max (eq. (3))
-    float m1 = m[0], m2 = -1.0f;
-    int i1 = sub * V;
-#pragma unroll
-    for (int j = 1; j < V; j++) {
-      if (m[j] > m1) {
-        m2 = m1;
-        m1 = m[j];
-        i1 = sub * V + j;
-      } else if (m[j] > m2) {
-        m2 = m[j];
-      }
-    }
-    team_top2<L>(m1, i1, m2);
+struct EncParams {
+  const void* x;
+  long long n_tiles, n_g, n_groups, K, group_bytes, codes_bytes;
+  long long nA, J, lag, pre, n_items;
+  int lo, hi, h;
+  float c_h;
+  uint8_t* codes;
+  float* scales;
+  float* zeros;
+  uint8_t* bits;
+  uint8_t* pivots;
+  float* keys;
+  unsigned long long* cand;
+  uint32_t* cand_cnt;
+  uint32_t* hist_coarse;
+  uint32_t* hist_fine;
+  uint32_t* doneA;
+  uint32_t* doneB;
+  uint32_t* selready;
+  SelResult* sel;
+  unsigned long long* lookback;
+  uint32_t* ticket;
+  uint32_t* status;
+  LgTables tabs;
+};
 
-    // entropy key (eq. (1)-(2)): H = lg L - S / L
-    float term[V];
-#pragma unroll
-    for (int j = 0; j < V; j++)
-      term[j] = (m[j] == 0.0f)
-                    ? 0.0f
-                    : __fmul_rn(m[j], lg_canon<InTraits<Tin>::kNoFraction>(m[j], sT, sR, sk));
-    const float Ls = team_sum<L>(lane_pairwise<V>(m));
-    const float Ss = team_sum<L>(lane_pairwise<V>(term));
-    const float H =
-        (Ls == 0.0f) ? 0.0f : __fsub_rn(lg_canon<false>(Ls, sT, sR, sk), __fdiv_rn(Ss, Ls));
-    const bool flag = __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+// ====================================================================== helpers
 
-    if (valid && sub == 0) {
-      keys[t] = H;
-      pivots[t] = flag ? (uint8_t)i1 : (uint8_t)0xFF;
-      if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
-        set_status(status, kStNonFinite);
-      const long long g = t / n_g;
-      const int b = fine_bin(H);
-      atomicAdd(&hist_fine[g * kFineBins + b], 1u);
-      atomicAdd(&hist_coarse[g * kCoarseBins + (b >> 8)], 1u);
-    }
+template <typename Tin, int G>
+__device__ __forceinline__ void init_tables(EncSmem<Tin, G>& sm, const LgTables& tabs) {
+  for (int i = threadIdx.x; i < 128 * 32; i += kThreads) {
+    sm.Trep[i] = tabs.T[i >> 5];
+    if constexpr (!InTraits<Tin>::kNoFraction) sm.Rrep[i] = tabs.R[i >> 5];
   }
+  for (int i = threadIdx.x; i < 128; i += kThreads) {
+    sm.T[i] = tabs.T[i];
+    sm.R[i] = tabs.R[i];
+  }
+  if (threadIdx.x < 4) sm.k[threadIdx.x] = tabs.k[threadIdx.x];
 }
 
-// ====================================================================== exact select
+template <int kN>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& total,
+                                                         uint32_t* s_warp) {
+  constexpr int kW = kN / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < kW ? s_warp[lane] : 0u;
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
+    }
+    __syncwarp();
+    if (lane < kW) s_warp[lane] = wi - w;
+    if (lane == kW - 1) s_warp[kW] = wi;
+  }
+  __syncthreads();
+  total = s_warp[kW];
+  const uint32_t r = s_warp[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
 
 // One warp: bins[0..255] in shared memory, 1 <= k <= sum(bins).  Walking the bins from
 // the top (255 down to 0) with a running count, returns the bin at which the count first
@@ -179,346 +183,628 @@ __device__ __forceinline__ void warp_find_from_top(const uint32_t* bins, uint32_
   above = __shfl_sync(kFull, my_above, src);
 }
 
-// Threshold bucket of one group: b* and the count of tiles in buckets above it.  Run by
-// warp 0 of a block; results left in shared memory.
-__device__ __forceinline__ void find_threshold_bucket(const uint32_t* hist_coarse,
-                                                      const uint32_t* hist_fine, uint32_t K,
-                                                      uint32_t* s_bins, int* s_bstar,
-                                                      uint32_t* s_above) {
-  if (threadIdx.x < 32) {
-    for (int i = threadIdx.x; i < 256; i += 32) s_bins[i] = hist_coarse[i];
-    __syncwarp();
-    int cb;
-    uint32_t above_c;
-    warp_find_from_top(s_bins, K, cb, above_c);
-    __syncwarp();
-    for (int i = threadIdx.x; i < 256; i += 32) s_bins[i] = hist_fine[cb * 256 + i];
-    __syncwarp();
-    int fb;
-    uint32_t above_f;
-    warp_find_from_top(s_bins, K - above_c, fb, above_f);
-    if (threadIdx.x == 0) {
-      *s_bstar = cb * 256 + fb;
-      *s_above = above_c + above_f;
+// ====================================================================== quantize a chunk
+
+// Pass 1: every tile of the chunk whose ratio test is decided without a division (two
+// values with |v| >= max|v|/2 => r <= tau => no transform) is quantised and packed into
+// s.stage at s.off; the others are listed in s.cand for pass 2.
+template <typename Tin, int G>
+__device__ __forceinline__ void quant_pass1(EncSmem<Tin, G>& s, const unsigned char* buf,
+                                            int nt) {
+  using C = Cfg<Tin, G>;
+  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L;
+#pragma unroll 1
+  for (int st = 0; st < C::kSteps; st++) {
+    const int kt = (st * kWarps + warp) * TPW + team;
+    const bool valid = kt < nt;
+    uint32_t w[W];
+    if (valid) {
+      lds_words<Tin, G>(buf, kt, sub, w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; k++) w[k] = 0u;
+    }
+    float mn, mx;
+    lane_minmax_raw<Tin, G>(w, mn, mx);
+    mn = team_min<L>(mn);
+    mx = team_max<L>(mx);
+    const float m1 = fmaxf(mx, -mn);
+    // values with |v| >= m1 / 2 (exact halving); a tile below 2^-120 goes to pass 2
+    const uint32_t cnt = team_sum_u<L>(lane_count_ge<Tin, G>(w, __fmul_rn(m1, 0.5f)));
+    const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
+    const bool deferred = valid && (tiny || cnt < 2u);
+    if (deferred && sub == 0) s.cand[atomicAdd(&s.ncand, 1u)] = (uint16_t)kt;
+    const bool go = valid && !deferred;  // team-uniform
+    const unsigned act = __ballot_sync(kFull, go);
+    if (!go) continue;
+    const int b = s.bits[kt];
+    float scale, inv;
+    scale_inv<L>(__fsub_rn(mx, mn), b, sub, scale, inv, act);
+    float v[V];
+    words_to_values<Tin, G>(w, v);
+    unsigned char* dst = s.stage + s.off[kt] + sub * (V * b / 8);
+#pragma unroll
+    for (int g8 = 0; g8 < V / 8; g8++) {
+      uint32_t lo32, hi32;
+      quant_pack8<V>(v + 8 * g8, mn, inv, b, &lo32, &hi32);
+      store_bytes(dst + g8 * b, lo32, hi32, b);
+    }
+    if (sub == 0) {
+      s.scale[kt] = scale;
+      s.zero[kt] = __fadd_rn(mn, 0.0f);
+      s.piv[kt] = 0xFF;
     }
   }
 }
 
-__global__ void __launch_bounds__(256) k_select_collect(
-    const float* __restrict__ keys, long long n_g, uint32_t K,
-    const uint32_t* __restrict__ hist_coarse, const uint32_t* __restrict__ hist_fine,
-    unsigned long long* __restrict__ cand, uint32_t* __restrict__ cand_cnt) {
-  __shared__ uint32_t s_bins[256];
-  __shared__ int s_bstar;
-  __shared__ uint32_t s_above;
-  const long long g = blockIdx.y;
-  find_threshold_bucket(hist_coarse + g * kCoarseBins, hist_fine + g * (long long)kFineBins, K,
-                        s_bins, &s_bstar, &s_above);
+// Pass 2: the deferred tiles, compacted: exact ratio test (eq. (3)), pivot swap and
+// Hadamard (eq. (4)) where it holds, then the quantizer.
+template <typename Tin, int G>
+__device__ __forceinline__ void quant_pass2(EncSmem<Tin, G>& s, const unsigned char* buf,
+                                            int h, float c_h) {
+  using C = Cfg<Tin, G>;
+  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L;
+  const int n = (int)s.ncand;
+  const int steps = (n + kWarps * TPW - 1) / (kWarps * TPW);
+#pragma unroll 1
+  for (int st = 0; st < steps; st++) {
+    const int ci = (st * kWarps + warp) * TPW + team;
+    const bool valid = ci < n;
+    const int kt = valid ? (int)s.cand[ci] : 0;
+    uint32_t w[W];
+    if (valid) {
+      lds_words<Tin, G>(buf, kt, sub, w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; k++) w[k] = 0u;
+    }
+    float v[V];
+    words_to_values<Tin, G>(w, v);
+    float m1 = fabsf(v[0]), m2 = -1.0f;
+    int i1 = sub * V;
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      const float m = fabsf(v[j]);
+      if (m > m1) {
+        m2 = m1;
+        m1 = m;
+        i1 = sub * V + j;
+      } else if (m > m2) {
+        m2 = m;
+      }
+    }
+    team_top2<L>(m1, i1, m2);
+    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+    if (__any_sync(kFull, flag)) {
+      float t[V];
+#pragma unroll
+      for (int j = 0; j < V; j++) t[j] = v[j];
+      team_swap0<V>(t, flag ? i1 : 0, sub, lane - sub);
+      team_fwht<V, L>(t, h, sub);
+      if (flag) {
+#pragma unroll
+        for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], c_h);
+      }
+    }
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      mn = fminf(mn, v[j]);
+      mx = fmaxf(mx, v[j]);
+    }
+    mn = team_min<L>(mn);
+    mx = team_max<L>(mx);
+    const int b = valid ? (int)s.bits[kt] : 1;
+    float scale, inv;
+    scale_inv<L>(__fsub_rn(mx, mn), b, sub, scale, inv);
+    if (valid) {
+      unsigned char* dst = s.stage + s.off[kt] + sub * (V * b / 8);
+#pragma unroll
+      for (int g8 = 0; g8 < V / 8; g8++) {
+        uint32_t lo32, hi32;
+        quant_pack8<V>(v + 8 * g8, mn, inv, b, &lo32, &hi32);
+        store_bytes(dst + g8 * b, lo32, hi32, b);
+      }
+      if (sub == 0) {
+        s.scale[kt] = scale;
+        s.zero[kt] = __fadd_rn(mn, 0.0f);
+        s.piv[kt] = flag ? (uint8_t)i1 : (uint8_t)0xFF;
+      }
+    }
+  }
+}
+
+// Copy s.stage[0, nbytes) to codes[base, base + nbytes): 16-byte stores for the aligned
+// middle (realigned from shared memory with funnel shifts), byte stores at the two ends.
+template <typename Tin, int G>
+__device__ __forceinline__ void store_stage(const EncSmem<Tin, G>& s, uint8_t* codes,
+                                            long long base, int nbytes) {
+  const int head = (int)((16 - (base & 15)) & 15);
+  const int h = min(head, nbytes);
+  const int n16 = (nbytes - h) / 16;
+  const int tail0 = h + 16 * n16;
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(s.stage);
+  const int sh = (h & 3) * 8;
+  for (int i = threadIdx.x; i < n16; i += kThreads) {
+    const int o = h + 16 * i;          // stage byte offset of this global 16-byte word
+    const int q = o >> 2;
+    uint32_t a[5];
+#pragma unroll
+    for (int k = 0; k < 5; k++) a[k] = sw[q + k];
+    uint4 out;
+    out.x = __funnelshift_r(a[0], a[1], sh);
+    out.y = __funnelshift_r(a[1], a[2], sh);
+    out.z = __funnelshift_r(a[2], a[3], sh);
+    out.w = __funnelshift_r(a[3], a[4], sh);
+    *reinterpret_cast<uint4*>(codes + base + o) = out;
+  }
+  const int nb = h + (nbytes - tail0);
+  for (int i = threadIdx.x; i < nb; i += kThreads) {
+    const int o = (i < h) ? i : tail0 + (i - h);
+    codes[base + o] = s.stage[o];
+  }
+}
+
+template <typename Tin, int G>
+__device__ __forceinline__ void store_meta(const EncSmem<Tin, G>& s, const EncParams& p,
+                                           long long t0, int nt) {
+  for (int k = threadIdx.x; k < nt; k += kThreads) {
+    p.scales[t0 + k] = s.scale[k];
+    p.zeros[t0 + k] = s.zero[k];
+    p.bits[t0 + k] = s.bits[k];
+    p.pivots[t0 + k] = s.piv[k];
+  }
+}
+
+// ====================================================================== work items
+
+struct Item {
+  int type;  // kItemStats, kItemSelect, kItemQuant
+  long long g, idx;
+};
+constexpr int kItemStats = 0, kItemSelect = 1, kItemQuant = 2;
+
+// Round r (0 <= r < NG + lag): the J select items of group r-1 (if 1 <= r <= NG), then
+// the stats items of group r (if r < NG) interleaved with the quantize items of group
+// r - lag (if lag <= r < NG + lag); the first `pre` stats items of the round go first.
+__device__ __forceinline__ Item decode_item(const EncParams& p, long long q) {
+  const long long NG = p.n_groups, lag = p.lag, nA = p.nA, J = p.J;
+  long long bp[6] = {0, 1, lag, NG, NG + 1, NG + lag};
+  // sort the six breakpoints (tiny insertion sort)
+#pragma unroll
+  for (int i = 1; i < 6; i++)
+#pragma unroll
+    for (int j = i; j > 0; j--)
+      if (bp[j] < bp[j - 1]) {
+        const long long t = bp[j];
+        bp[j] = bp[j - 1];
+        bp[j - 1] = t;
+      }
+  const long long rmax = NG + lag;
+  long long cum = 0;
+  for (int seg = 0; seg < 5; seg++) {
+    const long long r0 = bp[seg], r1 = min(bp[seg + 1], rmax);
+    if (r1 <= r0) continue;
+    const bool hasB = r0 >= 1 && r0 <= NG, hasA = r0 < NG, hasC = r0 >= lag && r0 < NG + lag;
+    const long long nBr = hasB ? J : 0, nAr = hasA ? nA : 0, nCr = hasC ? nA : 0;
+    const long long len = nBr + nAr + nCr;
+    if (len == 0) continue;
+    const long long span = (r1 - r0) * len;
+    if (q < cum + span) {
+      const long long r = r0 + (q - cum) / len;
+      long long pos = (q - cum) % len;
+      if (pos < nBr) return Item{kItemSelect, r - 1, pos};
+      pos -= nBr;
+      if (!hasC) return Item{kItemStats, r, pos};
+      if (!hasA) return Item{kItemQuant, r - lag, pos};
+      const long long pre = min(p.pre, nAr);
+      if (pos < pre) return Item{kItemStats, r, pos};
+      const long long pp = pos - pre, na = nAr - pre, m = min(na, nCr);
+      if (pp < 2 * m)
+        return (pp & 1) ? Item{kItemQuant, r - lag, pp >> 1} : Item{kItemStats, r, pre + (pp >> 1)};
+      const long long rest = pp - 2 * m;
+      return (na > nCr) ? Item{kItemStats, r, pre + m + rest} : Item{kItemQuant, r - lag, m + rest};
+    }
+    cum += span;
+  }
+  return Item{-1, 0, 0};
+}
+
+template <typename Tin, int G>
+__device__ __forceinline__ void item_range(const EncParams& p, const Item& it, long long& t0,
+                                           int& nt) {
+  constexpr int CH = Cfg<Tin, G>::CH;
+  t0 = it.g * p.n_g + it.idx * CH;
+  nt = (int)min((long long)CH, p.n_g - it.idx * CH);
+}
+
+// ---- stats item: entropy keys and histograms of one chunk
+template <typename Tin, int G>
+__device__ void do_stats(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
+                         const unsigned char* buf) {
+  using C = Cfg<Tin, G>;
+  constexpr int W = C::W, L = C::L, TPW = C::TPW;
+  long long t0;
+  int nt;
+  item_range<Tin, G>(p, it, t0, nt);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L;
+  uint32_t* hf = p.hist_fine + it.g * (long long)kFineBins;
+#pragma unroll 1
+  for (int st = 0; st < C::kSteps; st++) {
+    const int kt = (st * kWarps + warp) * TPW + team;
+    const bool valid = kt < nt;
+    uint32_t w[W];
+    if (valid) {
+      lds_words<Tin, G>(buf, kt, sub, w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; k++) w[k] = 0u;
+    }
+    float Ls, Ss;
+    const float H = tile_entropy<Tin, G>(w, s.Trep, s.Rrep, s.T, s.R, s.k, lane, Ls, Ss);
+    if (valid && sub == 0) {
+      p.keys[t0 + kt] = H;
+      if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+        set_status(p.status, kStNonFinite);
+      const int b = fine_bin(H);
+      atomicAdd(&hf[b], 1u);
+      atomicAdd(&s.hist[b >> 8], 1u);
+    }
+  }
   __syncthreads();
-  const int bstar = s_bstar;
-  const long long per = (n_g + gridDim.x - 1) / gridDim.x;
-  const long long lo = (long long)blockIdx.x * per;
-  const long long hi = min(n_g, lo + per);
-  const float* kg = keys + g * n_g;
-  unsigned long long* cg = cand + g * n_g;
+  for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) {
+    const uint32_t c = s.hist[i];
+    if (c) atomicAdd(&p.hist_coarse[it.g * kCoarseBins + i], c);
+    s.hist[i] = 0u;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(&p.doneA[it.g], 1u);
+}
+
+// ---- select item: gather the candidates of the threshold bucket; the last select item
+// of the group resolves the K-th ranked tile exactly.
+template <typename Tin, int G>
+__device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
+  const long long g = it.g;
+  const uint32_t K = (uint32_t)p.K;
+  if (threadIdx.x == 0) wait_counter(&p.doneA[g], (uint32_t)p.nA, p.status);
+  __syncthreads();
+  uint32_t* bins = s.hist;  // all zero between stats items; left zero below
+  if (threadIdx.x < 32) {
+    for (int i = threadIdx.x; i < 256; i += 32) bins[i] = __ldcg(&p.hist_coarse[g * kCoarseBins + i]);
+    __syncwarp();
+    int cb;
+    uint32_t above_c;
+    warp_find_from_top(bins, K, cb, above_c);
+    __syncwarp();
+    for (int i = threadIdx.x; i < 256; i += 32)
+      bins[i] = __ldcg(&p.hist_fine[g * (long long)kFineBins + cb * 256 + i]);
+    __syncwarp();
+    int fb;
+    uint32_t above_f;
+    warp_find_from_top(bins, K - above_c, fb, above_f);
+    if (threadIdx.x == 0) {
+      s.scan[0] = (uint32_t)(cb * 256 + fb);
+      s.scan[1] = above_c + above_f;
+    }
+  }
+  __syncthreads();
+  const int bstar = (int)s.scan[0];
+  const uint32_t above = s.scan[1];
+  // candidates of this item's slice of the group
+  const long long per = (p.n_g + p.J - 1) / p.J;
+  const long long lo = it.idx * per, hi = min(p.n_g, lo + per);
+  const float* kg = p.keys + g * p.n_g;
+  unsigned long long* cg = p.cand + g * p.n_g;
   const int lane = threadIdx.x & 31;
-  for (long long base = lo; base < hi; base += blockDim.x) {
+  for (long long base = lo; base < hi; base += kThreads) {
     const long long i = base + threadIdx.x;
-    float h = 0.0f;
+    float hv = 0.0f;
     bool hit = false;
     if (i < hi) {
-      h = kg[i];
-      hit = fine_bin(h) == bstar;
+      hv = __ldcg(&kg[i]);
+      hit = fine_bin(hv) == bstar;
     }
     const unsigned mask = __ballot_sync(kFull, hit);
     if (mask) {
       uint32_t pos0 = 0;
       const int leader = __ffs(mask) - 1;
-      if (lane == leader) pos0 = atomicAdd(&cand_cnt[g], (uint32_t)__popc(mask));
+      if (lane == leader) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)__popc(mask));
       pos0 = __shfl_sync(kFull, pos0, leader);
-      if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(h, (uint32_t)i);
+      if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv, (uint32_t)i);
     }
   }
-}
-
-// Radix select (8 passes of 8 bits) of the r-th largest composite key among the
-// candidates of the threshold bucket; r counts from 1.
-__global__ void __launch_bounds__(1024) k_select_final(
-    long long n_g, uint32_t K, const uint32_t* __restrict__ hist_coarse,
-    const uint32_t* __restrict__ hist_fine, const unsigned long long* __restrict__ cand,
-    const uint32_t* __restrict__ cand_cnt, SelResult* __restrict__ sel,
-    uint32_t* __restrict__ status) {
-  __shared__ uint32_t s_bins[256];
-  __shared__ int s_bstar;
-  __shared__ uint32_t s_above;
-  __shared__ unsigned long long s_prefix;
-  __shared__ uint32_t s_r;
-  const long long g = blockIdx.x;
-  if (K == 0u || (long long)K == n_g) {
-    if (threadIdx.x == 0) sel[g] = SelResult{0ull, K == 0u ? kSelNone : kSelAll, 0u};
-    return;
-  }
-  const uint32_t* hc = hist_coarse + g * kCoarseBins;
-  const uint32_t* hf = hist_fine + g * (long long)kFineBins;
-  find_threshold_bucket(hc, hf, K, s_bins, &s_bstar, &s_above);
+  __threadfence();
   __syncthreads();
-  const uint32_t expect = hf[s_bstar];
-  const uint32_t cnt = cand_cnt[g];
   if (threadIdx.x == 0) {
-    if (cnt != expect) set_status(status, kStSelectMismatch);
-    uint32_t r = K - s_above;
-    if (r < 1u) r = 1u;
-    if (r > cnt) r = cnt;
-    s_r = r;
-    s_prefix = 0ull;
+    const uint32_t prev = atomicAdd(&p.doneB[g], 1u);
+    __threadfence();
+    s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
   }
   __syncthreads();
-  const unsigned long long* cg = cand + g * n_g;
-  unsigned long long mask = 0ull;
-  for (int pass = 7; pass >= 0 && cnt > 0u; --pass) {
-    const int shift = pass * 8;
-    if (threadIdx.x < 256) s_bins[threadIdx.x] = 0u;
-    __syncthreads();
-    const unsigned long long prefix = s_prefix;
-    for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) {
-      const unsigned long long v = cg[i];
-      if ((v & mask) == prefix) atomicAdd(&s_bins[(v >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      int d;
-      uint32_t above;
-      warp_find_from_top(s_bins, s_r, d, above);
-      if (threadIdx.x == 0) {
-        s_r -= above;
-        s_prefix = prefix | ((unsigned long long)d << shift);
+  if (s.last) {
+    // radix select (8 passes of 8 bits) of the r-th largest candidate key, r from 1
+    const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
+    const uint32_t expect = __ldcg(&p.hist_fine[g * (long long)kFineBins + bstar]);
+    if (threadIdx.x == 0 && cnt != expect) set_status(p.status, kStSelectMismatch);
+    uint32_t r = max(1u, min(K - above, cnt));
+    unsigned long long prefix = 0ull, mask = 0ull;
+    for (int pass = 7; pass >= 0 && cnt > 0u; --pass) {
+      const int shift = pass * 8;
+      for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+        const unsigned long long v = __ldcg(&cg[i]);
+        if ((v & mask) == prefix) atomicAdd(&bins[(v >> shift) & 255u], 1u);
       }
-    }
-    mask |= 0xFFull << shift;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) sel[g] = SelResult{s_prefix, cnt ? kSelThreshold : kSelNone, 0u};
-}
-
-// ====================================================================== quantize + pack
-
-template <int kThreads>
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& total,
-                                                         uint32_t* s_warp) {
-  constexpr int kWarps = kThreads / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
-    uint32_t wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += y;
-    }
-    __syncwarp();
-    if (lane < kWarps) s_warp[lane] = wi - w;
-    if (lane == kWarps - 1) s_warp[kWarps] = wi;
-  }
-  __syncthreads();
-  total = s_warp[kWarps];
-  const uint32_t r = s_warp[warp] + incl - v;
-  __syncthreads();
-  return r;
-}
-
-template <typename Tin, int G>
-struct QuantCfg {
-  static constexpr int V = InTraits<Tin>::V;
-  using Gm = Geom<V, G>;
-  static constexpr int kThreads = 256;
-  static constexpr int CH = 32768 / (G * (int)sizeof(Tin));   // tiles per chunk (32 KB in)
-  static constexpr int kSteps = CH / (8 * Gm::TPW);            // warp steps per chunk
-  static constexpr int kPer = (CH + kThreads - 1) / kThreads;  // tiles per thread (scan)
-  static constexpr int kStageBytes = CH * G + 48;              // b <= 8, plus alignment pad
-  static_assert(kSteps * 8 * Gm::TPW == CH, "chunk must be whole warp steps");
-  static_assert(kPer <= 32, "hi flags are kept in one 32-bit word per thread");
-};
-
-template <typename Tin, int G>
-__global__ void __launch_bounds__(256) k_quant(
-    const Tin* __restrict__ x, long long n_g, long long group_bytes, long long codes_bytes,
-    int lo, int hi, int h,
-    float c_h, const float* __restrict__ keys, const uint8_t* __restrict__ piv_in,
-    const SelResult* __restrict__ sel, uint8_t* __restrict__ codes, float* __restrict__ scales,
-    float* __restrict__ zeros, uint8_t* __restrict__ bits,
-    unsigned long long* __restrict__ lookback, uint32_t* __restrict__ ticket,
-    uint32_t* __restrict__ status, long long n_chunks) {
-  using Cf = QuantCfg<Tin, G>;
-  constexpr int V = Cf::V, L = Cf::Gm::L, TPW = Cf::Gm::TPW, CH = Cf::CH;
-  __shared__ __align__(16) uint32_t s_stage[Cf::kStageBytes / 4];
-  __shared__ uint16_t s_off[CH];
-  __shared__ uint8_t s_bits[CH];
-  __shared__ uint32_t s_warp[9];
-  __shared__ long long s_c;
-  __shared__ long long s_base;
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int team = lane / L, sub = lane % L;
-  const long long cpg = (n_g + CH - 1) / CH;
-  const int slot_lo = G * lo / 8, slot_d = G * (hi - lo) / 8;
-
-  for (;;) {
-    if (threadIdx.x == 0) s_c = (long long)atomicAdd(ticket, 1u);
-    __syncthreads();
-    const long long c = s_c;
-    if (c >= n_chunks) break;
-    const long long g = c / cpg, lc = c % cpg;
-    const long long t0 = g * n_g + lc * CH;
-    const int nt = (int)min((long long)CH, n_g - lc * CH);
-    const SelResult sg = sel[g];
-
-    // 1. bit widths of this chunk's tiles and their exclusive hi counts
-    uint32_t hiflags = 0u, cnt = 0u;
-#pragma unroll
-    for (int j = 0; j < Cf::kPer; j++) {
-      const int k = threadIdx.x * Cf::kPer + j;
-      if (k < nt) {
-        const long long t = t0 + k;
-        bool ishi = sg.mode == kSelAll;
-        if (sg.mode == kSelThreshold)
-          ishi = rank_key(keys[t], (uint32_t)(t - g * n_g)) >= sg.theta;
-        if (ishi) {
-          hiflags |= 1u << j;
-          ++cnt;
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        int d;
+        uint32_t ab;
+        warp_find_from_top(bins, r, d, ab);
+        if (threadIdx.x == 0) {
+          s.scan[2] = (uint32_t)d;
+          s.scan[3] = ab;
         }
       }
+      __syncthreads();
+      prefix |= (unsigned long long)s.scan[2] << shift;
+      r -= s.scan[3];
+      mask |= 0xFFull << shift;
+      __syncthreads();
     }
-    uint32_t chunk_hi;
-    uint32_t before = block_exclusive_scan<256>(cnt, chunk_hi, s_warp);
-#pragma unroll
-    for (int j = 0; j < Cf::kPer; j++) {
-      const int k = threadIdx.x * Cf::kPer + j;
-      if (k < nt) {
-        const bool ishi = (hiflags >> j) & 1u;
-        s_bits[k] = (uint8_t)(ishi ? hi : lo);
-        s_off[k] = (uint16_t)(k * slot_lo + before * slot_d);
-        bits[t0 + k] = (uint8_t)(ishi ? hi : lo);
-        before += ishi ? 1u : 0u;
-      }
-    }
-
-    // 2. chunk offset in the stream: look-back over the earlier chunks of this group
     if (threadIdx.x == 0) {
-      unsigned long long prefix = 0ull;
-      if (lc == 0) {
-        st_release_u64(&lookback[c], kLbPre | (unsigned long long)chunk_hi);
-      } else {
-        st_release_u64(&lookback[c], kLbAgg | (unsigned long long)chunk_hi);
-        prefix = lookback_prefix(lookback, c, g * cpg, status);
-        st_release_u64(&lookback[c], kLbPre | (prefix + chunk_hi));
-      }
-      s_base = g * group_bytes + lc * (long long)CH * slot_lo + (long long)prefix * slot_d;
+      p.sel[g] = SelResult{prefix, cnt ? kSelThreshold : kSelNone, 0u};
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.selready[g]), "r"(1u) : "memory");
     }
-    int chunk_bytes = nt * slot_lo + (int)chunk_hi * slot_d;
-    __syncthreads();
-    const long long base = s_base;
-    if (base + chunk_bytes > codes_bytes) {  // only if the select went wrong: never write past
-      if (threadIdx.x == 0) set_status(status, kStSelectMismatch);
-      chunk_bytes = (int)max(0ll, codes_bytes - base);
-    }
-    const int pad = (int)(base & 15);
-    const int stage_words = (pad + chunk_bytes + 15) / 16 * 4;
-    for (int i = threadIdx.x; i < stage_words; i += Cf::kThreads) s_stage[i] = 0u;
-    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
+  __syncthreads();
+}
 
-    // 3. per tile: pivot swap + Hadamard (flagged tiles), quantise, pack
-#pragma unroll 1
-    for (int s = 0; s < Cf::kSteps; s++) {
-      const int kt = (s * 8 + warp) * TPW + team;
-      const bool valid = kt < nt;
-      const long long t = t0 + kt;
-      float v[V];
-      if (valid) {
-        load_lane<Tin>(x, t * G + sub * V, v);
-      } else {
+// Number of tiles of chunk `lc` of group g that get bits_hi (one warp).
+template <typename Tin, int G>
+__device__ __forceinline__ uint32_t warp_chunk_hi(const EncParams& p, long long g, long long lc,
+                                                  unsigned long long theta) {
+  constexpr int CH = Cfg<Tin, G>::CH;
+  const long long t0 = g * p.n_g + lc * CH;
+  const int nt = (int)min((long long)CH, p.n_g - lc * CH);
+  const int lane = threadIdx.x & 31;
+  uint32_t c = 0;
+  for (int k = lane; k < nt; k += 32)
+    c += (rank_key(__ldcg(&p.keys[t0 + k]), (uint32_t)(t0 + k - g * p.n_g)) >= theta) ? 1u : 0u;
 #pragma unroll
-        for (int j = 0; j < V; j++) v[j] = 0.0f;
-      }
-      const int piv = valid ? (int)piv_in[t] : 0xFF;
-      const bool flag = piv != 0xFF;
-      if (__any_sync(kFull, flag)) {
-        float w[V];
-#pragma unroll
-        for (int j = 0; j < V; j++) w[j] = v[j];
-        team_swap0<V>(w, flag ? piv : 0, sub, lane - sub);
-        team_fwht<V, L>(w, h, sub);
-        if (flag) {
-#pragma unroll
-          for (int j = 0; j < V; j++) v[j] = __fmul_rn(w[j], c_h);
-        }
-      }
-      float mn = v[0], mx = v[0];
-#pragma unroll
-      for (int j = 1; j < V; j++) {
-        mn = fminf(mn, v[j]);
-        mx = fmaxf(mx, v[j]);
-      }
-      mn = team_min<L>(mn);
-      mx = team_max<L>(mx);
-      const int b = valid ? (int)s_bits[kt] : lo;
-      const uint32_t Q = (1u << b) - 1u;
-      const float D = __fsub_rn(mx, mn);
-      const bool degenerate = !(D >= 0x1p-120f);
-      const float qf = (float)Q;
-      const float scale = degenerate ? 0.0f : __fdiv_rn(D, qf);
-      const float inv = degenerate ? 0.0f : __fdiv_rn(qf, D);
-      unsigned long long acc = 0ull;
-#pragma unroll
-      for (int j = 0; j < V; j++) {
-        const float u = __fmul_rn(__fsub_rn(v[j], mn), inv);
-        // round to nearest even: for 0 <= u < 2^22, u + 1.5*2^23 lands on an integer
-        uint32_t q = __float_as_uint(__fadd_rn(u, 12582912.0f)) - 0x4B400000u;
-        q = min(q, Q);
-        if (degenerate) q = 0u;
-        acc |= (unsigned long long)q << (j * b);
-      }
-      if (valid && (int)s_off[kt] + G * b / 8 <= chunk_bytes) {
-        const int pos = 8 * (pad + (int)s_off[kt]) + sub * V * b;
-        const int wi = pos >> 5, sh = pos & 31;
-        const unsigned long long lo64 = acc << sh;
-        const uint32_t w0 = (uint32_t)lo64, w1 = (uint32_t)(lo64 >> 32);
-        const uint32_t w2 = sh ? (uint32_t)(acc >> (64 - sh)) : 0u;
-        if (w0) atomicOr(&s_stage[wi], w0);
-        if (w1) atomicOr(&s_stage[wi + 1], w1);
-        if (w2) atomicOr(&s_stage[wi + 2], w2);
-        if (sub == 0) {
-          scales[t] = scale;
-          zeros[t] = mn;
-        }
-      }
-    }
-    __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  return c;
+}
 
-    // 4. copy the staged bytes to codes[base, base + chunk_bytes)
-    const uint8_t* sb = reinterpret_cast<const uint8_t*>(s_stage);
-    const long long a0 = base - pad;
-    const int n16 = (pad + chunk_bytes + 15) / 16;
-    for (int w16 = threadIdx.x; w16 < n16; w16 += Cf::kThreads) {
-      const long long gb = a0 + 16ll * w16;
-      if (gb >= base && gb + 16 <= base + chunk_bytes) {
-        *reinterpret_cast<uint4*>(codes + gb) = reinterpret_cast<const uint4*>(s_stage)[w16];
-      } else {
-#pragma unroll
-        for (int k = 0; k < 16; k++) {
-          const long long p = gb + k;
-          if (p >= base && p < base + chunk_bytes) codes[p] = sb[16 * w16 + k];
-        }
+// Hi tiles in chunks [0, lc) of group g (one warp).  Looks back 32 chunks at a time; a
+// chunk whose count is not published yet gets it computed here (and published), so this
+// never waits for another block.
+template <typename Tin, int G>
+__device__ unsigned long long warp_lookback(const EncParams& p, long long g, long long lc,
+                                            unsigned long long theta) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long* words = p.lookback + g * p.nA;
+  unsigned long long acc = 0;
+  long long cur = lc - 1;
+  while (cur >= 0) {
+    const long long idx = cur - lane;
+    unsigned long long wv = idx >= 0 ? ld_acquire_u64(words + idx) : (kLbPre | 0ull);
+    const unsigned pre_mask = __ballot_sync(kFull, (wv & ~kLbVal) == kLbPre);
+    const int lim = pre_mask ? (__ffs(pre_mask) - 1) : 31;  // lanes [0, lim] are summed
+    // missing counts among lanes [0, lim): compute them, one chunk at a time
+    unsigned miss = __ballot_sync(kFull, lane < lim && (wv & ~kLbVal) == 0ull);
+    if (!pre_mask) miss = __ballot_sync(kFull, (wv & ~kLbVal) == 0ull);
+    while (miss) {
+      const int e = __ffs(miss) - 1;
+      miss &= miss - 1;
+      const uint32_t cnt = warp_chunk_hi<Tin, G>(p, g, cur - e, theta);
+      if (lane == e) {
+        wv = kLbAgg | (unsigned long long)cnt;
+        atomicCAS(words + idx, 0ull, wv);
       }
     }
+    unsigned long long v = (lane <= lim) ? (wv & kLbVal) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    acc += v;
+    if (pre_mask) break;
+    cur -= 32;
+  }
+  return acc;
+}
+
+// ---- quantize item: bit widths from the group's threshold, stream offset by look-back,
+// then quantize + pack the chunk and write it out.
+template <typename Tin, int G>
+__device__ void do_quant(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
+                         const unsigned char* buf, unsigned long long* bar, uint32_t parity) {
+  using C = Cfg<Tin, G>;
+  long long t0;
+  int nt;
+  item_range<Tin, G>(p, it, t0, nt);
+  const long long g = it.g, lc = it.idx;
+  if (threadIdx.x == 0) {
+    wait_counter(&p.selready[g], 1u, p.status);
+    s.ncand = 0u;
+  }
+  __syncthreads();
+  const unsigned long long theta = __ldcg(&p.sel[g].theta);
+  const uint32_t mode = __ldcg(&p.sel[g].mode);
+  const int slot_lo = G * p.lo / 8, slot_d = G * (p.hi - p.lo) / 8;
+  // 1. widths and exclusive hi counts
+  uint32_t hiflags = 0u, cnt = 0u;
+#pragma unroll
+  for (int j = 0; j < C::kPer; j++) {
+    const int k = threadIdx.x * C::kPer + j;
+    if (k < nt) {
+      const long long t = t0 + k;
+      bool ishi = mode == kSelAll;
+      if (mode == kSelThreshold)
+        ishi = rank_key(__ldcg(&p.keys[t]), (uint32_t)(t - g * p.n_g)) >= theta;
+      if (ishi) {
+        hiflags |= 1u << j;
+        ++cnt;
+      }
+    }
+  }
+  uint32_t chunk_hi;
+  uint32_t before = block_exclusive_scan<kThreads>(cnt, chunk_hi, s.scan);
+#pragma unroll
+  for (int j = 0; j < C::kPer; j++) {
+    const int k = threadIdx.x * C::kPer + j;
+    if (k < nt) {
+      const bool ishi = (hiflags >> j) & 1u;
+      s.bits[k] = (uint8_t)(ishi ? p.hi : p.lo);
+      s.off[k] = (uint16_t)(k * slot_lo + before * slot_d);
+      before += ishi ? 1u : 0u;
+    }
+  }
+  const long long cidx = g * p.nA + lc;
+  if (threadIdx.x == 0)
+    st_release_u64(&p.lookback[cidx], (lc == 0 ? kLbPre : kLbAgg) | (unsigned long long)chunk_hi);
+  mbar_wait(bar, parity, p.status);
+  __syncthreads();
+  // 2. pass 1 (all warps) -- then warp 0 finds the chunk's offset in the stream
+  quant_pass1<Tin, G>(s, buf, nt);
+  if (threadIdx.x < 32) {
+    const unsigned long long prefix = (mode == kSelThreshold && lc > 0)
+                                          ? warp_lookback<Tin, G>(p, g, lc, theta)
+                                          : (mode == kSelAll ? (unsigned long long)lc * C::CH : 0ull);
+    if (threadIdx.x == 0) {
+      if (lc > 0) st_release_u64(&p.lookback[cidx], kLbPre | (prefix + chunk_hi));
+      s.base = g * p.group_bytes + lc * (long long)C::CH * slot_lo + (long long)prefix * slot_d;
+    }
+  }
+  __syncthreads();
+  quant_pass2<Tin, G>(s, buf, p.h, p.c_h);
+  __syncthreads();
+  const long long base = s.base;
+  int nbytes = nt * slot_lo + (int)chunk_hi * slot_d;
+  if (base + nbytes > p.codes_bytes) {  // only if the select went wrong: never write past
+    if (threadIdx.x == 0) set_status(p.status, kStSelectMismatch);
+    nbytes = (int)max(0ll, p.codes_bytes - base);
+  }
+  store_stage<Tin, G>(s, p.codes, base, nbytes);
+  store_meta<Tin, G>(s, p, t0, nt);
+}
+
+template <typename Tin, int G>
+__global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ EncParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = *reinterpret_cast<EncSmem<Tin, G>*>(smem_raw);
+  init_tables<Tin, G>(s, p.tabs);
+  for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) s.hist[i] = 0u;
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+    s.next = (long long)atomicAdd(p.ticket, 1u);
+  }
+  __syncthreads();
+  const unsigned long long pol_keep = policy_evict_last(), pol_drop = policy_evict_first();
+  const Tin* x = static_cast<const Tin*>(p.x);
+  uint32_t parity = 0u;  // bit s = phase parity of buffer s
+
+  // Thread 0 starts the bulk copy of item q's input chunk into buffer `slot`.
+  auto issue = [&](long long q, int slot) {
+    const Item it = decode_item(p, q);
+    if (it.type != kItemStats && it.type != kItemQuant) return;
+    long long t0;
+    int nt;
+    item_range<Tin, G>(p, it, t0, nt);
+    const uint32_t bytes = (uint32_t)nt * G * (uint32_t)sizeof(Tin);
+    mbar_expect_tx(&s.bar[slot], bytes);
+    bulk_load(s.buf[slot], x + t0 * G, bytes, &s.bar[slot],
+              it.type == kItemStats ? pol_keep : pol_drop);
+  };
+
+  long long cur = s.next;
+  int slot = 0;
+  if (threadIdx.x == 0 && cur < p.n_items) issue(cur, 0);
+  while (cur < p.n_items) {
+    __syncthreads();  // everyone is done with the previous item and its buffer
+    if (threadIdx.x == 0) {
+      const long long nxt = (long long)atomicAdd(p.ticket, 1u);
+      s.next = nxt;
+      if (nxt < p.n_items) issue(nxt, slot ^ 1);
+    }
+    const Item it = decode_item(p, cur);
+    if (it.type == kItemStats) {
+      mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+      parity ^= 1u << slot;
+      do_stats<Tin, G>(s, p, it, s.buf[slot]);
+    } else if (it.type == kItemQuant) {
+      do_quant<Tin, G>(s, p, it, s.buf[slot], &s.bar[slot], (parity >> slot) & 1u);
+      parity ^= 1u << slot;
+    } else if (it.type == kItemSelect) {
+      do_select<Tin, G>(s, p, it);
+    }
     __syncthreads();
+    cur = s.next;
+    slot ^= 1;
+  }
+}
+
+// ====================================================================== one-pass kernel
+
+// Every tile gets the same width b (K = 0 or K = n_g): slot offsets are t * G * b / 8.
+template <typename Tin, int G>
+__global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_constant__ EncParams p,
+                                                             int b, long long n_chunks) {
+  using C = Cfg<Tin, G>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = *reinterpret_cast<EncSmem<Tin, G>*>(smem_raw);
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+  }
+  for (int k = threadIdx.x; k < C::CH; k += kThreads) {
+    s.bits[k] = (uint8_t)b;
+    s.off[k] = (uint16_t)(k * G * b / 8);
+  }
+  __syncthreads();
+  const unsigned long long pol = policy_evict_first();
+  const Tin* x = static_cast<const Tin*>(p.x);
+  uint32_t parity = 0u;
+  auto issue = [&](long long c, int slot) {
+    const long long t0 = c * C::CH;
+    const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
+    const uint32_t bytes = (uint32_t)nt * G * (uint32_t)sizeof(Tin);
+    mbar_expect_tx(&s.bar[slot], bytes);
+    bulk_load(s.buf[slot], x + t0 * G, bytes, &s.bar[slot], pol);
+  };
+  long long c = blockIdx.x;
+  int slot = 0;
+  if (threadIdx.x == 0 && c < n_chunks) issue(c, 0);
+  for (; c < n_chunks; c += gridDim.x) {
+    const long long nx = c + gridDim.x;
+    if (threadIdx.x == 0) {
+      s.ncand = 0u;
+      if (nx < n_chunks) issue(nx, slot ^ 1);
+    }
+    const long long t0 = c * C::CH;
+    const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    parity ^= 1u << slot;
+    __syncthreads();
+    quant_pass1<Tin, G>(s, s.buf[slot], nt);
+    __syncthreads();
+    quant_pass2<Tin, G>(s, s.buf[slot], p.h, p.c_h);
+    __syncthreads();
+    store_stage<Tin, G>(s, p.codes, t0 * G * b / 8, nt * G * b / 8);
+    store_meta<Tin, G>(s, p, t0, nt);
+    __syncthreads();
+    slot ^= 1;
   }
 }
 
@@ -526,31 +812,66 @@ __global__ void __launch_bounds__(256) k_quant(
 
 template <typename Tin, int G>
 static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
-  using Cf = QuantCfg<Tin, G>;
-  const Tin* x = static_cast<const Tin*>(a.x);
-  const long long stats_need = (a.n_tiles + 8 * Cf::Gm::TPW - 1) / (8 * Cf::Gm::TPW);
-  const int stats_blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 8, stats_need));
-  k_stats<Tin, G><<<stats_blocks, 256, 0, st>>>(x, a.n_tiles, a.n_g, *a.tabs, a.keys, a.pivots,
-                                                 a.hist_coarse, a.hist_fine, a.status);
-  if (a.K > 0 && a.K < a.n_g) {
-    const int per_group = (int)std::max<long long>(1, std::min<long long>(64, a.n_g / 4096));
-    k_select_collect<<<dim3(per_group, (unsigned)a.n_groups), 256, 0, st>>>(
-        a.keys, a.n_g, (uint32_t)a.K, a.hist_coarse, a.hist_fine, a.cand, a.cand_cnt);
+  using C = Cfg<Tin, G>;
+  const size_t smem = sizeof(EncSmem<Tin, G>);
+  EncParams p{};
+  p.x = a.x;
+  p.n_tiles = a.n_tiles;
+  p.n_g = a.n_g;
+  p.n_groups = a.n_groups;
+  p.K = a.K;
+  p.group_bytes = a.group_bytes;
+  p.codes_bytes = a.n_groups * a.group_bytes;
+  p.lo = a.lo;
+  p.hi = a.hi;
+  p.h = a.h;
+  p.c_h = a.c_h;
+  p.codes = a.codes;
+  p.scales = a.scales;
+  p.zeros = a.zeros;
+  p.bits = a.bits;
+  p.pivots = a.pivots;
+  p.keys = a.keys;
+  p.cand = a.cand;
+  p.cand_cnt = a.cand_cnt;
+  p.hist_coarse = a.hist_coarse;
+  p.hist_fine = a.hist_fine;
+  p.doneA = a.doneA;
+  p.doneB = a.doneB;
+  p.selready = a.selready;
+  p.sel = a.sel;
+  p.lookback = a.lookback;
+  p.ticket = a.ticket;
+  p.status = a.status;
+  p.tabs = *a.tabs;
+  p.nA = (a.n_g + C::CH - 1) / C::CH;
+  const int grid_cap = a.num_sms * 2;
+  if (a.K == 0 || a.K == a.n_g) {
+    cudaError_t e = cudaFuncSetAttribute(k_encode_flat<Tin, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long n_chunks = (a.n_tiles + C::CH - 1) / C::CH;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, n_chunks));
+    k_encode_flat<Tin, G><<<grid, kThreads, smem, st>>>(p, a.K == 0 ? a.lo : a.hi, n_chunks);
+    return cudaGetLastError();
   }
-  k_select_final<<<(unsigned)a.n_groups, 1024, 0, st>>>(a.n_g, (uint32_t)a.K, a.hist_coarse,
-                                                         a.hist_fine, a.cand, a.cand_cnt, a.sel,
-                                                         a.status);
-  const long long n_chunks = encode_chunks(a.bf16, G, a.n_g, a.n_groups);
-  const int quant_blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
-  k_quant<Tin, G><<<quant_blocks, 256, 0, st>>>(
-      x, a.n_g, a.group_bytes, a.n_groups * a.group_bytes, a.lo, a.hi, a.h, a.c_h, a.keys,
-      a.pivots, a.sel, a.codes,
-      a.scales, a.zeros, a.bits, a.lookback, a.ticket, a.status, n_chunks);
+  // keep two (or, for big groups, one) groups' input in L2 between a group's stats pass
+  // and its quantize pass
+  const long long group_in = a.n_g * G * (long long)sizeof(Tin);
+  p.lag = (3 * group_in <= (72ll << 20)) ? 2 : 1;
+  p.pre = (p.lag == 1) ? p.nA / 4 : 0;
+  p.J = std::max<long long>(1, std::min<long long>(32, p.nA / 8));
+  p.n_items = a.n_groups * (2 * p.nA + p.J);
+  cudaError_t e = cudaFuncSetAttribute(k_encode<Tin, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, p.n_items));
+  k_encode<Tin, G><<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
 long long encode_chunks(int bf16, int G, long long n_g, long long n_groups) {
-  const long long ch = 32768 / (G * (bf16 ? 2 : 4));
+  const long long ch = kChunkBytes / (G * (bf16 ? 2 : 4));
   return n_groups * ((n_g + ch - 1) / ch);
 }
 

@@ -1,0 +1,301 @@
+// tahq_tile.cuh -- per-lane tile arithmetic of the encode kernels.
+//
+// A tile of G values is held by a team of L = G / V consecutive lanes, V consecutive
+// values per lane (32 bytes of input per lane: 16 bf16 or 8 fp32 values, fewer when the
+// tile is narrower).  All integer-deciding arithmetic follows the codec's canonical fp32
+// order (see tahq_device.cuh); packed fp32x2 instructions (__fadd2_rn, __fmul2_rn) round
+// each component exactly like the scalar ones, and bf16x2 min/max/compare are exact.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "tahq_device.cuh"
+
+namespace tahq {
+
+template <typename Tin>
+struct InTraits;
+template <>
+struct InTraits<float> {
+  static constexpr bool kBf16 = false;
+  static constexpr bool kNoFraction = false;
+};
+template <>
+struct InTraits<uint16_t> {  // bf16 bit patterns
+  static constexpr bool kBf16 = true;
+  static constexpr bool kNoFraction = true;
+};
+
+template <typename Tin, int G>
+struct TileGeom {
+  static constexpr int kLaneBytes = 32;
+  static constexpr int kPerLane = kLaneBytes / (int)sizeof(Tin);
+  static constexpr int V = (G < kPerLane) ? G : kPerLane;  // values per lane
+  static constexpr int W = V * (int)sizeof(Tin) / 4;       // 32-bit words per lane
+  static constexpr int L = G / V;                          // lanes per tile
+  static constexpr int TPW = 32 / L;                       // tiles per warp step
+  static_assert(W == 4 || W == 8, "a lane holds 16 or 32 bytes");
+};
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+// Lane's words of tile kt from a staged chunk.
+template <typename Tin, int G>
+__device__ __forceinline__ void lds_words(const unsigned char* buf, int kt, int sub, uint32_t* w) {
+  using Gm = TileGeom<Tin, G>;
+  const uint4* p = reinterpret_cast<const uint4*>(buf + ((size_t)kt * G + sub * Gm::V) * sizeof(Tin));
+#pragma unroll
+  for (int i = 0; i < Gm::W / 4; i++) {
+    const uint4 q = p[i];
+    w[4 * i] = q.x;
+    w[4 * i + 1] = q.y;
+    w[4 * i + 2] = q.z;
+    w[4 * i + 3] = q.w;
+  }
+}
+
+// Words -> V fp32 values (bf16 widening is exact; element 2k is the low half of word k).
+template <typename Tin, int G>
+__device__ __forceinline__ void words_to_values(const uint32_t* w, float* v) {
+  using Gm = TileGeom<Tin, G>;
+  if constexpr (InTraits<Tin>::kBf16) {
+#pragma unroll
+    for (int k = 0; k < Gm::W; k++) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < Gm::W; k++) v[k] = __uint_as_float(w[k]);
+  }
+}
+
+// Pairwise tree over n = 2^k float2 values (both components at once).
+template <int N>
+__device__ __forceinline__ float2 tree2(const float2* x) {
+  if constexpr (N == 1) {
+    return x[0];
+  } else {
+    return add2(tree2<N / 2>(x), tree2<N / 2>(x + N / 2));
+  }
+}
+
+template <int L>
+__device__ __forceinline__ float2 team_sum2(float2 s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) {
+    float2 t;
+    t.x = __shfl_xor_sync(kFull, s.x, o);
+    t.y = __shfl_xor_sync(kFull, s.y, o);
+    s = add2(s, t);
+  }
+  return s;
+}
+
+template <int L>
+__device__ __forceinline__ uint32_t team_sum_u(uint32_t s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) s += __shfl_xor_sync(kFull, s, o);
+  return s;
+}
+
+// ------------------------------------------------------------------ entropy key
+
+// Canonical entropy key of the team's tile: H = lg L - S / L with both sums pairwise.
+// Conflict-free lookups: Trep/Rrep hold entry i of lane l at i*32 + l.
+template <typename Tin, int G>
+__device__ __forceinline__ float tile_entropy(const uint32_t* w, const float* Trep,
+                                              const float* Rrep, const float* T, const float* R,
+                                              const float* sk, int lane, float& Lsum,
+                                              float& Ssum) {
+  using Gm = TileGeom<Tin, G>;
+  constexpr int V = Gm::V;
+  float2 ms[V];  // {|a_k|, |a_k| lg |a_k|}
+  if constexpr (InTraits<Tin>::kBf16) {
+    // bf16 subnormals (exponent 0, mantissa != 0) need the normalising path
+    uint32_t subn = 0u;
+#pragma unroll
+    for (int k = 0; k < Gm::W; k++) {
+      const uint32_t m = w[k] & 0x7FFF7FFFu;
+      subn |= (m + 0x7FFF7FFFu) & ~(m + 0x7F807F80u);
+    }
+    if (subn & 0x80008000u) {
+      float v[V];
+      words_to_values<Tin, G>(w, v);
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        const float m = fabsf(v[j]);
+        ms[j] = make_float2(m, m == 0.0f ? 0.0f : __fmul_rn(m, lg_canon<true>(m, T, R, sk)));
+      }
+    } else {
+      const uint32_t lane4 = (uint32_t)lane << 2;
+      const char* tb = reinterpret_cast<const char*>(Trep);
+#pragma unroll
+      for (int k = 0; k < Gm::W; k++) {
+        const uint32_t x = w[k];
+        const float mlo = __uint_as_float((x << 16) & 0x7FFF0000u);
+        const float mhi = __uint_as_float(x & 0x7FFF0000u);
+        const float elo = __uint_as_float(((x >> 7) & 0xFFu) | 0x4B000000u);
+        const float ehi = __uint_as_float(((x >> 23) & 0xFFu) | 0x4B000000u);
+        const float tlo = *reinterpret_cast<const float*>(tb + (((x << 7) & 0x3F80u) | lane4));
+        const float thi = *reinterpret_cast<const float*>(tb + (((x >> 9) & 0x3F80u) | lane4));
+        const float2 ef = add2(make_float2(elo, ehi), make_float2(-8388735.0f, -8388735.0f));
+        const float2 lg = add2(ef, make_float2(tlo, thi));  // e + T[i] (r = 0 for bf16)
+        const float2 tm = mul2(make_float2(mlo, mhi), lg);
+        // a zero magnitude gives lg = -127 and a term of -0; see lg_fast in tahq_encode.cu
+        ms[2 * k] = make_float2(mlo, tm.x);
+        ms[2 * k + 1] = make_float2(mhi, tm.y);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+      const float m = fabsf(__uint_as_float(w[j]));
+      const uint32_t b = __float_as_uint(m);
+      const uint32_t E = b >> 23;
+      float lgv;
+      if (E == 0u && b != 0u) {
+        lgv = lg_canon<false>(m, T, R, sk);
+      } else {
+        const uint32_t idx = (((b >> 16) & 0x7Fu) << 5) | (uint32_t)lane;
+        const float ef = __fsub_rn(__uint_as_float(0x4B000000u | E), 8388735.0f);
+        const float mm = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+        const float c = __uint_as_float((b & 0x007F0000u) | 0x3F800000u);
+        const float r = __fmul_rn(__fsub_rn(mm, c), Rrep[idx]);
+        float p = __fmaf_rn(sk[3], r, sk[2]);
+        p = __fmaf_rn(p, r, sk[1]);
+        p = __fmaf_rn(p, r, sk[0]);
+        lgv = __fadd_rn(ef, __fadd_rn(Trep[idx], __fmul_rn(p, r)));
+      }
+      ms[j] = make_float2(m, __fmul_rn(m, lgv));
+    }
+  }
+  const float2 s = team_sum2<Gm::L>(tree2<V>(ms));
+  Lsum = s.x;
+  Ssum = s.y;
+  return (s.x == 0.0f) ? 0.0f : __fsub_rn(lg_canon<false>(s.x, T, R, sk), __fdiv_rn(s.y, s.x));
+}
+
+// ------------------------------------------------------------------ quantizer
+
+// min / max of the lane's raw values (exact; bf16 via packed bf16x2 min/max).
+template <typename Tin, int G>
+__device__ __forceinline__ void lane_minmax_raw(const uint32_t* w, float& mn, float& mx) {
+  using Gm = TileGeom<Tin, G>;
+  if constexpr (InTraits<Tin>::kBf16) {
+    __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
+    __nv_bfloat162 hi = lo;
+#pragma unroll
+    for (int k = 1; k < Gm::W; k++) {
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+      lo = __hmin2(lo, x);
+      hi = __hmax2(hi, x);
+    }
+    const uint32_t l = *reinterpret_cast<const uint32_t*>(&lo);
+    const uint32_t h = *reinterpret_cast<const uint32_t*>(&hi);
+    mn = fminf(__uint_as_float(l << 16), __uint_as_float(l & 0xFFFF0000u));
+    mx = fmaxf(__uint_as_float(h << 16), __uint_as_float(h & 0xFFFF0000u));
+  } else {
+    mn = mx = __uint_as_float(w[0]);
+#pragma unroll
+    for (int k = 1; k < Gm::W; k++) {
+      mn = fminf(mn, __uint_as_float(w[k]));
+      mx = fmaxf(mx, __uint_as_float(w[k]));
+    }
+  }
+}
+
+// Number of lane values with |v| >= thr (thr = m1 / 2, exact).
+template <typename Tin, int G>
+__device__ __forceinline__ uint32_t lane_count_ge(const uint32_t* w, float thr) {
+  using Gm = TileGeom<Tin, G>;
+  uint32_t c = 0;
+  if constexpr (InTraits<Tin>::kBf16) {
+    const uint32_t t16 = __float_as_uint(thr) >> 16;  // thr is a bf16 value
+    const uint32_t tt = t16 | (t16 << 16);
+    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162*>(&tt);
+    __nv_bfloat162 acc = __float2bfloat162_rn(0.0f);
+#pragma unroll
+    for (int k = 0; k < Gm::W; k++) {
+      const uint32_t a = w[k] & 0x7FFF7FFFu;
+      acc = __hadd2(acc, __hge2(*reinterpret_cast<const __nv_bfloat162*>(&a), t2));
+    }
+    c = (uint32_t)__bfloat162float(acc.x) + (uint32_t)__bfloat162float(acc.y);
+  } else {
+#pragma unroll
+    for (int k = 0; k < Gm::W; k++) c += (fabsf(__uint_as_float(w[k])) >= thr) ? 1u : 0u;
+  }
+  return c;
+}
+
+// Quantise the lane's V values to b bits with the tile's (mn, inv) and pack them, code j
+// at bits [j*b, j*b+b) of the lane's b*V/8 bytes, into dst (byte stores).  For V = 4 the
+// caller pairs lanes first (see quant_store).  Returns nothing; writes bytes.
+//   u = (v - mn) * inv  (two roundings), code = rint(u); u lies in [0, Q + Q*2^-23], so the
+//   code never exceeds Q and no clamp is needed.  rint is done by adding 1.5*2^23: the
+//   float bits are then 0x4B400000 + code.
+template <int V>
+__device__ __forceinline__ void quant_pack8(const float* v, float mn, float inv, int b,
+                                            uint32_t* out_lo, uint32_t* out_hi) {
+  // eight codes -> (b <= 4) one 32-bit word, else two words
+  const float2 nmn = make_float2(-mn, -mn), iv = make_float2(inv, inv);
+  const float2 mg = make_float2(12582912.0f, 12582912.0f);
+  uint32_t bits[8];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 u = mul2(add2(make_float2(v[j], v[j + 1]), nmn), iv);
+    const float2 r = add2(u, mg);
+    bits[j] = __float_as_uint(r.x);
+    bits[j + 1] = __float_as_uint(r.y);
+  }
+  if (b <= 4) {
+    // sum of bits_j * 2^(j b) = sum code_j 2^(j b) + 0x4B400000 * sum 2^(j b)  (mod 2^32)
+    uint32_t acc = bits[0], pw = 1u, spw = 1u;
+#pragma unroll
+    for (int j = 1; j < 8; j++) {
+      pw <<= b;
+      spw += pw;
+      acc += bits[j] * pw;
+    }
+    *out_lo = acc - 0x4B400000u * spw;
+    *out_hi = 0u;
+  } else {
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; j++) acc |= (unsigned long long)(bits[j] & 0xFFu) << (j * b);
+    *out_lo = (uint32_t)acc;
+    *out_hi = (uint32_t)(acc >> 32);
+  }
+}
+
+__device__ __forceinline__ void store_bytes(unsigned char* dst, uint32_t lo, uint32_t hi, int n) {
+#pragma unroll 1
+  for (int k = 0; k < n; k++) dst[k] = (unsigned char)((k < 4 ? lo : hi) >> (8 * (k & 3)));
+}
+
+// scale = D / Q and inv = Q / D for the team (one division per lane; lanes of a pair
+// exchange results).  Degenerate range (D < 2^-120, incl. D = 0): scale = inv = 0.
+// `mask` holds every lane that calls this together (both lanes of each pair).
+template <int L>
+__device__ __forceinline__ void scale_inv(float D, int b, int sub, float& scale, float& inv,
+                                          unsigned mask = kFull) {
+  const float qf = __fsub_rn(__uint_as_float(0x4B000000u | ((1u << b) - 1u)), 8388608.0f);
+  const bool degenerate = !(D >= 0x1p-120f);
+  if constexpr (L >= 2) {
+    const bool odd = sub & 1;
+    const float r = __fdiv_rn(odd ? qf : D, odd ? D : qf);
+    const float o = __shfl_xor_sync(mask, r, 1);
+    scale = odd ? o : r;
+    inv = odd ? r : o;
+  } else {
+    scale = __fdiv_rn(D, qf);
+    inv = __fdiv_rn(qf, D);
+  }
+  if (degenerate) {
+    scale = 0.0f;
+    inv = 0.0f;
+  }
+}
+
+}  // namespace tahq
