@@ -3,8 +3,8 @@
 // A tile of G values is held by a team of L = G / V consecutive lanes, V consecutive
 // values per lane (32 bytes of input per lane: 16 bf16 or 8 fp32 values, fewer when the
 // tile is narrower).  All integer-deciding arithmetic follows the codec's canonical fp32
-// order (see tahq_device.cuh); packed fp32x2 instructions (__fadd2_rn, __fmul2_rn) round
-// each component exactly like the scalar ones, and bf16x2 min/max/compare are exact.
+// order (see tahq_device.cuh); packed fp32x2 adds round each component exactly like the
+// scalar add, and bf16x2 min/max/compare are exact.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,8 +37,21 @@ struct TileGeom {
   static_assert(W == 4 || W == 8, "a lane holds 16 or 32 bytes");
 };
 
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// Packed fp32x2 add, each component rounded to nearest even exactly like the scalar
+// add.  Products stay scalar (__fmul_rn): a packed multiply followed by an add was
+// measured to be fused into a single-rounding multiply-add on this target, which breaks
+// the canonical two-rounding order; an add followed by anything cannot be fused.
+__device__ __forceinline__ unsigned long long pk2(float2 a) {
+  return ((unsigned long long)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+}
+__device__ __forceinline__ float2 upk2(unsigned long long r) {
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
+  return upk2(d);
+}
 
 // Lane's words of tile kt from a staged chunk.
 template <typename Tin, int G>
@@ -142,7 +155,7 @@ __device__ __forceinline__ float tile_entropy(const uint32_t* w, const float* Tr
         const float thi = *reinterpret_cast<const float*>(tb + (((x >> 9) & 0x3F80u) | lane4));
         const float2 ef = add2(make_float2(elo, ehi), make_float2(-8388735.0f, -8388735.0f));
         const float2 lg = add2(ef, make_float2(tlo, thi));  // e + T[i] (r = 0 for bf16)
-        const float2 tm = mul2(make_float2(mlo, mhi), lg);
+        const float2 tm = make_float2(__fmul_rn(mlo, lg.x), __fmul_rn(mhi, lg.y));
         // a zero magnitude gives lg = -127 and a term of -0; see lg_fast in tahq_encode.cu
         ms[2 * k] = make_float2(mlo, tm.x);
         ms[2 * k + 1] = make_float2(mhi, tm.y);
@@ -239,13 +252,13 @@ template <int V>
 __device__ __forceinline__ void quant_pack8(const float* v, float mn, float inv, int b,
                                             uint32_t* out_lo, uint32_t* out_hi) {
   // eight codes -> (b <= 4) one 32-bit word, else two words
-  const float2 nmn = make_float2(-mn, -mn), iv = make_float2(inv, inv);
+  const float2 nmn = make_float2(-mn, -mn);
   const float2 mg = make_float2(12582912.0f, 12582912.0f);
   uint32_t bits[8];
 #pragma unroll
   for (int j = 0; j < 8; j += 2) {
-    const float2 u = mul2(add2(make_float2(v[j], v[j + 1]), nmn), iv);
-    const float2 r = add2(u, mg);
+    const float2 a = add2(make_float2(v[j], v[j + 1]), nmn);
+    const float2 r = add2(make_float2(__fmul_rn(a.x, inv), __fmul_rn(a.y, inv)), mg);
     bits[j] = __float_as_uint(r.x);
     bits[j + 1] = __float_as_uint(r.y);
   }
