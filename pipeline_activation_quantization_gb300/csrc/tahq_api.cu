@@ -87,7 +87,7 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
 }
 
 struct EncLayout {
-  size_t status, ticket, cand_cnt, doneA, doneB, selready, sel, hist_coarse, hist_fine, lookback,
+  size_t status, ticket, cand_cnt, doneA, doneB, doneB2, selready, sel, hist_coarse, hist_fine, lookback,
       ctrl_end, keys, cand, total;
 };
 
@@ -104,6 +104,8 @@ EncLayout enc_layout(const Shape& s) {
   L.doneA = off;
   off = align_up(off + 4 * (size_t)s.n_groups);
   L.doneB = off;
+  off = align_up(off + 4 * (size_t)s.n_groups);
+  L.doneB2 = off;
   off = align_up(off + 4 * (size_t)s.n_groups);
   L.selready = off;
   off = align_up(off + 4 * (size_t)s.n_groups);
@@ -235,6 +237,7 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.cand_cnt = at<uint32_t>(workspace, L.cand_cnt);
   a.doneA = at<uint32_t>(workspace, L.doneA);
   a.doneB = at<uint32_t>(workspace, L.doneB);
+  a.doneB2 = at<uint32_t>(workspace, L.doneB2);
   a.selready = at<uint32_t>(workspace, L.selready);
   a.sel = at<tahq::SelResult>(workspace, L.sel);
   a.hist_coarse = at<uint32_t>(workspace, L.hist_coarse);

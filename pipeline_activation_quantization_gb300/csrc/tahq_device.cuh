@@ -193,11 +193,13 @@ __device__ __forceinline__ void team_fwht(float* v, int h, int sub) {
   for (int s = 0; (1 << s) < L; s++) {
     const int lanes = 1 << s;
     if (lanes * V < h) {
-      const bool upper = (sub & lanes) != 0;
+      // lower lane: v + o; upper lane: o - v.  fma(+-1, v, o) rounds exactly once, like
+      // the add / subtract it stands for.
+      const float sg = (sub & lanes) ? -1.0f : 1.0f;
 #pragma unroll
       for (int j = 0; j < V; j++) {
         const float o = __shfl_xor_sync(kFull, v[j], lanes);
-        v[j] = upper ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+        v[j] = __fmaf_rn(sg, v[j], o);
       }
     }
   }

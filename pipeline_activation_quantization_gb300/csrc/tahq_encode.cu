@@ -13,11 +13,10 @@
 // k_encode runs the three as work items of one persistent kernel.  Items are handed out
 // in increasing order by an atomic ticket and only ever wait for earlier items, so every
 // wait ends.  The order keeps a group's input in L2 between its stats pass and its
-// quantize pass: round r = the select items of group r-1, then the stats items of group
-// r interleaved with the quantize items of group r-lag.  Each block double-buffers 32 KB
-// input chunks in shared memory with bulk (TMA) copies.  A quantize item finds its
-// offset in the stream from the hi-tile counts of the group's earlier chunks; a count
-// not yet published is computed on the spot from the keys, so that search never waits.
+// quantize pass (see decode_item for the round layout).  Each block double-buffers 32 KB
+// input chunks in shared memory with bulk (TMA) copies.  Offsets items count the hi
+// tiles of every chunk once the group's threshold is known and scan the counts into
+// the chunks' offsets in the stream, so a quantize item never waits on another chunk.
 //
 // k_encode_flat covers allocations that do not depend on the ranking (K = 0 or K = n_g,
 // every tile gets the same width): one streaming pass, fixed slot offsets.
@@ -35,6 +34,7 @@
 namespace tahq {
 
 constexpr int kChunkBytes = 32768;
+constexpr uint8_t kDeferred = 0xFE;  // pass-1 marker of a tile left to pass 2
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
@@ -46,9 +46,16 @@ struct Cfg {
   static constexpr int kSteps = CH / (kWarps * TPW);               // warp steps per chunk
   static constexpr int kPer = (CH + kThreads - 1) / kThreads;      // tiles per thread (scan)
   static constexpr int kStage = CH * G + 64;                       // b <= 8, plus slack
+  static constexpr int NS = CH / kWarps;                           // tiles owned by a warp
   static_assert(kSteps * kWarps * TPW == CH, "chunk must be whole warp steps");
   static_assert(kPer <= 32, "hi flags are kept in one word per thread");
 };
+
+struct Item {
+  int type;  // kItemStats, kItemSelect, kItemOffsets, kItemQuant
+  long long g, idx;
+};
+constexpr int kItemStats = 0, kItemSelect = 1, kItemOffsets = 2, kItemQuant = 3;
 
 template <typename Tin, int G>
 struct alignas(128) EncSmem {
@@ -59,12 +66,14 @@ struct alignas(128) EncSmem {
   float Rrep[InTraits<Tin>::kNoFraction ? 4 : 128 * 32];
   float T[128], R[128], k[4];
   float scale[C::CH], zero[C::CH];
+  float ta[C::CH], tb[C::CH];  // per-tile pairs: (L, S) in stats, (min, max) then inv in quant
   uint16_t off[C::CH];
   uint16_t cand[C::CH];
   uint8_t bits[C::CH], piv[C::CH];
   uint32_t hist[kCoarseBins];
   uint32_t scan[kWarps + 4];
   unsigned long long bar[2];
+  Item item[2];
   long long next, base;
   uint32_t last, ncand;
 };
@@ -87,7 +96,8 @@ struct EncParams {
   uint32_t* hist_fine;
   uint32_t* doneA;
   uint32_t* doneB;
-  uint32_t* selready;
+  uint32_t* doneB2;
+  uint32_t* selready;  // 1 once sel[g] is published, 2 once the chunk offsets are
   SelResult* sel;
   unsigned long long* lookback;
   uint32_t* ticket;
@@ -185,16 +195,30 @@ __device__ __forceinline__ void warp_find_from_top(const uint32_t* bins, uint32_
 
 // ====================================================================== quantize a chunk
 
-// Pass 1: every tile of the chunk whose ratio test is decided without a division (two
-// values with |v| >= max|v|/2 => r <= tau => no transform) is quantised and packed into
-// s.stage at s.off; the others are listed in s.cand for pass 2.
+// Tile `l` (0 <= l < NS) of warp `warp`: the tiles a warp handles over all its steps.
 template <typename Tin, int G>
-__device__ __forceinline__ void quant_pass1(EncSmem<Tin, G>& s, const unsigned char* buf,
-                                            int nt) {
+__device__ __forceinline__ int warp_tile(int l, int warp) {
   using C = Cfg<Tin, G>;
-  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW;
+  return ((l / C::TPW) * kWarps + warp) * C::TPW + (l % C::TPW);
+}
+
+// Quantise and pack the chunk's tiles into s.stage (s.bits / s.off must be ready).  Each
+// warp handles its own NS tiles with no block-wide barrier:
+//   phase 1, per warp step: the tile's min / max and the two-values test -- two values
+//            with |v| >= max|v|/2 give r <= tau, so no transform; tiles that fail it
+//            (or are below 2^-120) are deferred;
+//   phase 2, one lane per tile: scale = D/Q, inv = Q/D, zero-point;
+//   phase 3, per warp step: quantise and pack the tiles that were not deferred;
+//   pass 2:  the deferred tiles, compacted: exact ratio test (eq. (3)), pivot swap and
+//            Hadamard (eq. (4)) where it holds, then the quantizer.
+template <typename Tin, int G>
+__device__ __forceinline__ void quant_chunk(EncSmem<Tin, G>& s, const unsigned char* buf, int nt,
+                                            int h, float c_h) {
+  using C = Cfg<Tin, G>;
+  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW, NS = C::NS;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = lane / L, sub = lane % L;
+  // phase 1
 #pragma unroll 1
   for (int st = 0; st < C::kSteps; st++) {
     const int kt = (st * kWarps + warp) * TPW + team;
@@ -208,53 +232,69 @@ __device__ __forceinline__ void quant_pass1(EncSmem<Tin, G>& s, const unsigned c
     }
     float mn, mx;
     lane_minmax_raw<Tin, G>(w, mn, mx);
+    const float lane_amax = fmaxf(mx, -mn);
     mn = team_min<L>(mn);
     mx = team_max<L>(mx);
     const float m1 = fmaxf(mx, -mn);
-    // values with |v| >= m1 / 2 (exact halving); a tile below 2^-120 goes to pass 2
-    const uint32_t cnt = team_sum_u<L>(lane_count_ge<Tin, G>(w, __fmul_rn(m1, 0.5f)));
-    const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
-    const bool deferred = valid && (tiny || cnt < 2u);
-    if (deferred && sub == 0) s.cand[atomicAdd(&s.ncand, 1u)] = (uint16_t)kt;
-    const bool go = valid && !deferred;  // team-uniform
-    const unsigned act = __ballot_sync(kFull, go);
-    if (!go) continue;
-    const int b = s.bits[kt];
-    float scale, inv;
-    scale_inv<L>(__fsub_rn(mx, mn), b, sub, scale, inv, act);
-    float v[V];
-    words_to_values<Tin, G>(w, v);
-    unsigned char* dst = s.stage + s.off[kt] + sub * (V * b / 8);
-#pragma unroll
-    for (int g8 = 0; g8 < V / 8; g8++) {
-      uint32_t lo32, hi32;
-      quant_pack8<V>(v + 8 * g8, mn, inv, b, &lo32, &hi32);
-      store_bytes(dst + g8 * b, lo32, hi32, b);
+    const float thr = __fmul_rn(m1, 0.5f);  // exact halving for m1 >= 2^-120
+    bool two;
+    if constexpr (L >= 2) {
+      two = team_two_ge<L>(lane_amax, thr, team);
+    } else {
+      two = lane_count_ge<Tin, G>(w, thr) >= 2u;
     }
-    if (sub == 0) {
-      s.scale[kt] = scale;
-      s.zero[kt] = __fadd_rn(mn, 0.0f);
-      s.piv[kt] = 0xFF;
+    const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
+    if (valid && sub == 0) {
+      s.piv[kt] = (tiny || !two) ? kDeferred : (uint8_t)0xFF;
+      s.ta[kt] = mn;
+      s.tb[kt] = mx;
     }
   }
-}
-
-// Pass 2: the deferred tiles, compacted: exact ratio test (eq. (3)), pivot swap and
-// Hadamard (eq. (4)) where it holds, then the quantizer.
-template <typename Tin, int G>
-__device__ __forceinline__ void quant_pass2(EncSmem<Tin, G>& s, const unsigned char* buf,
-                                            int h, float c_h) {
-  using C = Cfg<Tin, G>;
-  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int team = lane / L, sub = lane % L;
-  const int n = (int)s.ncand;
-  const int steps = (n + kWarps * TPW - 1) / (kWarps * TPW);
+  __syncwarp();
+  // phase 2 (and the list of deferred tiles, kept in this warp's part of s.cand)
+  uint16_t* dl = s.cand + warp * NS;
+  int ndef = 0;
 #pragma unroll 1
-  for (int st = 0; st < steps; st++) {
-    const int ci = (st * kWarps + warp) * TPW + team;
-    const bool valid = ci < n;
-    const int kt = valid ? (int)s.cand[ci] : 0;
+  for (int l0 = 0; l0 < NS; l0 += 32) {
+    const int l = l0 + lane;
+    const int kt = warp_tile<Tin, G>(l, warp);
+    const bool valid = l < NS && kt < nt;
+    const bool def = valid && s.piv[kt] == kDeferred;
+    const unsigned dm = __ballot_sync(kFull, def);
+    if (def) dl[ndef + __popc(dm & ((1u << lane) - 1u))] = (uint16_t)kt;
+    ndef += __popc(dm);
+    if (valid && !def) {
+      const float mn = s.ta[kt], mx = s.tb[kt];
+      const int b = s.bits[kt];
+      const float qf = __fsub_rn(__uint_as_float(0x4B000000u | ((1u << b) - 1u)), 8388608.0f);
+      const float D = __fsub_rn(mx, mn);
+      const bool degenerate = !(D >= 0x1p-120f);
+      s.scale[kt] = degenerate ? 0.0f : __fdiv_rn(D, qf);
+      s.tb[kt] = degenerate ? 0.0f : __fdiv_rn(qf, D);  // inv
+      s.zero[kt] = __fadd_rn(mn, 0.0f);
+    }
+  }
+  __syncwarp();
+  // phase 3
+#pragma unroll 1
+  for (int st = 0; st < C::kSteps; st++) {
+    const int kt = (st * kWarps + warp) * TPW + team;
+    if (kt >= nt || s.piv[kt] == kDeferred) continue;
+    const float mn = s.ta[kt];
+    const float inv = s.tb[kt];
+    const int b = s.bits[kt];
+    uint32_t w[W];
+    lds_words<Tin, G>(buf, kt, sub, w);
+    float v[V];
+    words_to_values<Tin, G>(w, v);
+    quant_store<V>(v, mn, inv, b, s.stage + s.off[kt] + sub * (V * b / 8));
+  }
+  // pass 2
+#pragma unroll 1
+  for (int j0 = 0; j0 < ndef; j0 += TPW) {
+    const int ci = j0 + team;
+    const bool valid = ci < ndef;
+    const int kt = valid ? (int)dl[ci] : 0;
     uint32_t w[W];
     if (valid) {
       lds_words<Tin, G>(buf, kt, sub, w);
@@ -302,13 +342,7 @@ __device__ __forceinline__ void quant_pass2(EncSmem<Tin, G>& s, const unsigned c
     float scale, inv;
     scale_inv<L>(__fsub_rn(mx, mn), b, sub, scale, inv);
     if (valid) {
-      unsigned char* dst = s.stage + s.off[kt] + sub * (V * b / 8);
-#pragma unroll
-      for (int g8 = 0; g8 < V / 8; g8++) {
-        uint32_t lo32, hi32;
-        quant_pack8<V>(v + 8 * g8, mn, inv, b, &lo32, &hi32);
-        store_bytes(dst + g8 * b, lo32, hi32, b);
-      }
+      quant_store<V>(v, mn, inv, b, s.stage + s.off[kt] + sub * (V * b / 8));
       if (sub == 0) {
         s.scale[kt] = scale;
         s.zero[kt] = __fadd_rn(mn, 0.0f);
@@ -362,19 +396,17 @@ __device__ __forceinline__ void store_meta(const EncSmem<Tin, G>& s, const EncPa
 
 // ====================================================================== work items
 
-struct Item {
-  int type;  // kItemStats, kItemSelect, kItemQuant
-  long long g, idx;
-};
-constexpr int kItemStats = 0, kItemSelect = 1, kItemQuant = 2;
 
-// Round r (0 <= r < NG + lag): the J select items of group r-1 (if 1 <= r <= NG), then
-// the stats items of group r (if r < NG) interleaved with the quantize items of group
-// r - lag (if lag <= r < NG + lag); the first `pre` stats items of the round go first.
+// Round r (0 <= r < NG + lag) of the work queue:
+//   the J select items of group r-1        (if 1 <= r <= NG)
+//   the first `pre` stats items of group r (if r < NG)
+//   the J offset items of group r-1        (if 1 <= r <= NG)
+//   the other stats items of group r interleaved with the quantize items of group r-lag.
+// A group's select items come after all its stats items, its offset items after its
+// select items, and its quantize items (round >= r+1) after its offset items.
 __device__ __forceinline__ Item decode_item(const EncParams& p, long long q) {
   const long long NG = p.n_groups, lag = p.lag, nA = p.nA, J = p.J;
   long long bp[6] = {0, 1, lag, NG, NG + 1, NG + lag};
-  // sort the six breakpoints (tiny insertion sort)
 #pragma unroll
   for (int i = 1; i < 6; i++)
 #pragma unroll
@@ -390,23 +422,24 @@ __device__ __forceinline__ Item decode_item(const EncParams& p, long long q) {
     const long long r0 = bp[seg], r1 = min(bp[seg + 1], rmax);
     if (r1 <= r0) continue;
     const bool hasB = r0 >= 1 && r0 <= NG, hasA = r0 < NG, hasC = r0 >= lag && r0 < NG + lag;
-    const long long nBr = hasB ? J : 0, nAr = hasA ? nA : 0, nCr = hasC ? nA : 0;
-    const long long len = nBr + nAr + nCr;
+    const long long nB = hasB ? J : 0, nAr = hasA ? nA : 0, nCr = hasC ? nA : 0;
+    const long long len = 2 * nB + nAr + nCr;
     if (len == 0) continue;
     const long long span = (r1 - r0) * len;
     if (q < cum + span) {
       const long long r = r0 + (q - cum) / len;
       long long pos = (q - cum) % len;
-      if (pos < nBr) return Item{kItemSelect, r - 1, pos};
-      pos -= nBr;
-      if (!hasC) return Item{kItemStats, r, pos};
-      if (!hasA) return Item{kItemQuant, r - lag, pos};
+      if (pos < nB) return Item{kItemSelect, r - 1, pos};
+      pos -= nB;
       const long long pre = min(p.pre, nAr);
       if (pos < pre) return Item{kItemStats, r, pos};
-      const long long pp = pos - pre, na = nAr - pre, m = min(na, nCr);
-      if (pp < 2 * m)
-        return (pp & 1) ? Item{kItemQuant, r - lag, pp >> 1} : Item{kItemStats, r, pre + (pp >> 1)};
-      const long long rest = pp - 2 * m;
+      pos -= pre;
+      if (pos < nB) return Item{kItemOffsets, r - 1, pos};
+      pos -= nB;
+      const long long na = nAr - pre, m = min(na, nCr);
+      if (pos < 2 * m)
+        return (pos & 1) ? Item{kItemQuant, r - lag, pos >> 1} : Item{kItemStats, r, pre + (pos >> 1)};
+      const long long rest = pos - 2 * m;
       return (na > nCr) ? Item{kItemStats, r, pre + m + rest} : Item{kItemQuant, r - lag, m + rest};
     }
     cum += span;
@@ -422,18 +455,19 @@ __device__ __forceinline__ void item_range(const EncParams& p, const Item& it, l
   nt = (int)min((long long)CH, p.n_g - it.idx * CH);
 }
 
-// ---- stats item: entropy keys and histograms of one chunk
+// ---- stats item: entropy keys and histograms of one chunk.  Per warp step the team
+// reduces its tile's two sums (lane 0 keeps them); then one lane per tile of the warp
+// forms the key, writes it and adds it to the group's histograms.
 template <typename Tin, int G>
 __device__ void do_stats(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
                          const unsigned char* buf) {
   using C = Cfg<Tin, G>;
-  constexpr int W = C::W, L = C::L, TPW = C::TPW;
+  constexpr int W = C::W, L = C::L, TPW = C::TPW, NS = C::NS;
   long long t0;
   int nt;
   item_range<Tin, G>(p, it, t0, nt);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = lane / L, sub = lane % L;
-  uint32_t* hf = p.hist_fine + it.g * (long long)kFineBins;
 #pragma unroll 1
   for (int st = 0; st < C::kSteps; st++) {
     const int kt = (st * kWarps + warp) * TPW + team;
@@ -445,22 +479,34 @@ __device__ void do_stats(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
 #pragma unroll
       for (int k = 0; k < W; k++) w[k] = 0u;
     }
-    float Ls, Ss;
-    const float H = tile_entropy<Tin, G>(w, s.Trep, s.Rrep, s.T, s.R, s.k, lane, Ls, Ss);
+    const float2 ls = tile_sums<Tin, G>(w, s.Trep, s.Rrep, s.T, s.R, s.k, lane);
     if (valid && sub == 0) {
+      s.ta[kt] = ls.x;
+      s.tb[kt] = ls.y;
+    }
+  }
+  __syncwarp();
+  uint32_t* hf = p.hist_fine + it.g * (long long)kFineBins;
+  uint32_t* hc = p.hist_coarse + it.g * kCoarseBins;
+#pragma unroll 1
+  for (int l0 = 0; l0 < NS; l0 += 32) {
+    const int l = l0 + lane;
+    const int kt = warp_tile<Tin, G>(l, warp);
+    const bool valid = l < NS && kt < nt;
+    int cb = -1;
+    if (valid) {
+      const float Ls = s.ta[kt], Ss = s.tb[kt];
+      const float H = entropy_key(Ls, Ss, s.T, s.R, s.k);
       p.keys[t0 + kt] = H;
       if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
         set_status(p.status, kStNonFinite);
       const int b = fine_bin(H);
       atomicAdd(&hf[b], 1u);
-      atomicAdd(&s.hist[b >> 8], 1u);
+      cb = b >> 8;
     }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) {
-    const uint32_t c = s.hist[i];
-    if (c) atomicAdd(&p.hist_coarse[it.g * kCoarseBins + i], c);
-    s.hist[i] = 0u;
+    // coarse bins: one atomic per distinct bin in the warp
+    const unsigned same = __match_any_sync(kFull, cb);
+    if (cb >= 0 && lane == __ffs(same) - 1) atomicAdd(&hc[cb], (uint32_t)__popc(same));
   }
   __threadfence();
   __syncthreads();
@@ -569,61 +615,65 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
   __syncthreads();
 }
 
-// Number of tiles of chunk `lc` of group g that get bits_hi (one warp).
+// ---- offsets item: hi-tile count of each of its chunks; the last offsets item of the
+// group turns the counts into exclusive prefixes (chunk offsets in the stream).
 template <typename Tin, int G>
-__device__ __forceinline__ uint32_t warp_chunk_hi(const EncParams& p, long long g, long long lc,
-                                                  unsigned long long theta) {
+__device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
   constexpr int CH = Cfg<Tin, G>::CH;
-  const long long t0 = g * p.n_g + lc * CH;
-  const int nt = (int)min((long long)CH, p.n_g - lc * CH);
-  const int lane = threadIdx.x & 31;
-  uint32_t c = 0;
-  for (int k = lane; k < nt; k += 32)
-    c += (rank_key(__ldcg(&p.keys[t0 + k]), (uint32_t)(t0 + k - g * p.n_g)) >= theta) ? 1u : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-  return c;
-}
-
-// Hi tiles in chunks [0, lc) of group g (one warp).  Looks back 32 chunks at a time; a
-// chunk whose count is not published yet gets it computed here (and published), so this
-// never waits for another block.
-template <typename Tin, int G>
-__device__ unsigned long long warp_lookback(const EncParams& p, long long g, long long lc,
-                                            unsigned long long theta) {
-  const int lane = threadIdx.x & 31;
+  const long long g = it.g;
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status);
+  __syncthreads();
+  const unsigned long long theta = __ldcg(&p.sel[g].theta);
+  const uint32_t mode = __ldcg(&p.sel[g].mode);
   unsigned long long* words = p.lookback + g * p.nA;
-  unsigned long long acc = 0;
-  long long cur = lc - 1;
-  while (cur >= 0) {
-    const long long idx = cur - lane;
-    unsigned long long wv = idx >= 0 ? ld_acquire_u64(words + idx) : (kLbPre | 0ull);
-    const unsigned pre_mask = __ballot_sync(kFull, (wv & ~kLbVal) == kLbPre);
-    const int lim = pre_mask ? (__ffs(pre_mask) - 1) : 31;  // lanes [0, lim] are summed
-    // missing counts among lanes [0, lim): compute them, one chunk at a time
-    unsigned miss = __ballot_sync(kFull, lane < lim && (wv & ~kLbVal) == 0ull);
-    if (!pre_mask) miss = __ballot_sync(kFull, (wv & ~kLbVal) == 0ull);
-    while (miss) {
-      const int e = __ffs(miss) - 1;
-      miss &= miss - 1;
-      const uint32_t cnt = warp_chunk_hi<Tin, G>(p, g, cur - e, theta);
-      if (lane == e) {
-        wv = kLbAgg | (unsigned long long)cnt;
-        atomicCAS(words + idx, 0ull, wv);
-      }
+  const long long per = (p.nA + p.J - 1) / p.J;
+  const long long c0 = it.idx * per, c1 = min(p.nA, c0 + per);
+  // one warp per chunk: count the chunk's hi tiles
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long long c = c0 + warp; c < c1; c += kWarps) {
+    const long long t0 = g * p.n_g + c * CH;
+    const int nt = (int)min((long long)CH, p.n_g - c * CH);
+    uint32_t cnt = 0;
+    for (int k = lane; k < nt; k += 32) {
+      bool ishi = mode == kSelAll;
+      if (mode == kSelThreshold)
+        ishi = rank_key(__ldcg(&p.keys[t0 + k]), (uint32_t)(t0 + k - g * p.n_g)) >= theta;
+      cnt += ishi ? 1u : 0u;
     }
-    unsigned long long v = (lane <= lim) ? (wv & kLbVal) : 0ull;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    acc += v;
-    if (pre_mask) break;
-    cur -= 32;
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+    if (lane == 0) words[c] = cnt;
   }
-  return acc;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t prev = atomicAdd(&p.doneB2[g], 1u);
+    __threadfence();
+    s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s.last) {
+    // exclusive prefix of the nA counts: each thread sums a contiguous run, one block scan
+    const long long run = (p.nA + kThreads - 1) / kThreads;
+    const long long r0 = min(p.nA, (long long)threadIdx.x * run), r1 = min(p.nA, r0 + run);
+    unsigned long long mine = 0;
+    for (long long c = r0; c < r1; c++) mine += __ldcg(&words[c]);
+    uint32_t tot;
+    unsigned long long acc = block_exclusive_scan<kThreads>((uint32_t)mine, tot, s.scan);
+    for (long long c = r0; c < r1; c++) {
+      const unsigned long long v = __ldcg(&words[c]);
+      words[c] = acc;
+      acc += v;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.selready[g]), "r"(2u) : "memory");
+  }
 }
 
-// ---- quantize item: bit widths from the group's threshold, stream offset by look-back,
-// then quantize + pack the chunk and write it out.
+// ---- quantize item: bit widths from the group's threshold, the chunk's stream offset
+// from the offsets items, then quantize + pack the chunk and write it out.
 template <typename Tin, int G>
 __device__ void do_quant(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
                          const unsigned char* buf, unsigned long long* bar, uint32_t parity) {
@@ -632,15 +682,13 @@ __device__ void do_quant(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
   int nt;
   item_range<Tin, G>(p, it, t0, nt);
   const long long g = it.g, lc = it.idx;
-  if (threadIdx.x == 0) {
-    wait_counter(&p.selready[g], 1u, p.status);
-    s.ncand = 0u;
-  }
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status);
   __syncthreads();
   const unsigned long long theta = __ldcg(&p.sel[g].theta);
   const uint32_t mode = __ldcg(&p.sel[g].mode);
+  const unsigned long long prefix = __ldcg(&p.lookback[g * p.nA + lc]);
   const int slot_lo = G * p.lo / 8, slot_d = G * (p.hi - p.lo) / 8;
-  // 1. widths and exclusive hi counts
+  // widths and exclusive hi counts inside the chunk
   uint32_t hiflags = 0u, cnt = 0u;
 #pragma unroll
   for (int j = 0; j < C::kPer; j++) {
@@ -668,26 +716,11 @@ __device__ void do_quant(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
       before += ishi ? 1u : 0u;
     }
   }
-  const long long cidx = g * p.nA + lc;
-  if (threadIdx.x == 0)
-    st_release_u64(&p.lookback[cidx], (lc == 0 ? kLbPre : kLbAgg) | (unsigned long long)chunk_hi);
   mbar_wait(bar, parity, p.status);
   __syncthreads();
-  // 2. pass 1 (all warps) -- then warp 0 finds the chunk's offset in the stream
-  quant_pass1<Tin, G>(s, buf, nt);
-  if (threadIdx.x < 32) {
-    const unsigned long long prefix = (mode == kSelThreshold && lc > 0)
-                                          ? warp_lookback<Tin, G>(p, g, lc, theta)
-                                          : (mode == kSelAll ? (unsigned long long)lc * C::CH : 0ull);
-    if (threadIdx.x == 0) {
-      if (lc > 0) st_release_u64(&p.lookback[cidx], kLbPre | (prefix + chunk_hi));
-      s.base = g * p.group_bytes + lc * (long long)C::CH * slot_lo + (long long)prefix * slot_d;
-    }
-  }
+  quant_chunk<Tin, G>(s, buf, nt, p.h, p.c_h);
   __syncthreads();
-  quant_pass2<Tin, G>(s, buf, p.h, p.c_h);
-  __syncthreads();
-  const long long base = s.base;
+  const long long base = g * p.group_bytes + lc * (long long)C::CH * slot_lo + (long long)prefix * slot_d;
   int nbytes = nt * slot_lo + (int)chunk_hi * slot_d;
   if (base + nbytes > p.codes_bytes) {  // only if the select went wrong: never write past
     if (threadIdx.x == 0) set_status(p.status, kStSelectMismatch);
@@ -714,9 +747,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
   const Tin* x = static_cast<const Tin*>(p.x);
   uint32_t parity = 0u;  // bit s = phase parity of buffer s
 
-  // Thread 0 starts the bulk copy of item q's input chunk into buffer `slot`.
-  auto issue = [&](long long q, int slot) {
-    const Item it = decode_item(p, q);
+  // Thread 0 starts the bulk copy of item `it`'s input chunk into buffer `slot`.
+  auto issue = [&](const Item& it, int slot) {
     if (it.type != kItemStats && it.type != kItemQuant) return;
     long long t0;
     int nt;
@@ -727,17 +759,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
               it.type == kItemStats ? pol_keep : pol_drop);
   };
 
+  // Thread 0 decodes each item once (s.item[slot]) when it dequeues it.
   long long cur = s.next;
   int slot = 0;
-  if (threadIdx.x == 0 && cur < p.n_items) issue(cur, 0);
+  if (threadIdx.x == 0 && cur < p.n_items) {
+    s.item[0] = decode_item(p, cur);
+    issue(s.item[0], 0);
+  }
   while (cur < p.n_items) {
     __syncthreads();  // everyone is done with the previous item and its buffer
     if (threadIdx.x == 0) {
       const long long nxt = (long long)atomicAdd(p.ticket, 1u);
       s.next = nxt;
-      if (nxt < p.n_items) issue(nxt, slot ^ 1);
+      if (nxt < p.n_items) {
+        s.item[slot ^ 1] = decode_item(p, nxt);
+        issue(s.item[slot ^ 1], slot ^ 1);
+      }
     }
-    const Item it = decode_item(p, cur);
+    const Item it = s.item[slot];
     if (it.type == kItemStats) {
       mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
       parity ^= 1u << slot;
@@ -747,6 +786,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
       parity ^= 1u << slot;
     } else if (it.type == kItemSelect) {
       do_select<Tin, G>(s, p, it);
+    } else if (it.type == kItemOffsets) {
+      do_offsets<Tin, G>(s, p, it);
     }
     __syncthreads();
     cur = s.next;
@@ -788,18 +829,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
   if (threadIdx.x == 0 && c < n_chunks) issue(c, 0);
   for (; c < n_chunks; c += gridDim.x) {
     const long long nx = c + gridDim.x;
-    if (threadIdx.x == 0) {
-      s.ncand = 0u;
-      if (nx < n_chunks) issue(nx, slot ^ 1);
-    }
+    if (threadIdx.x == 0 && nx < n_chunks) issue(nx, slot ^ 1);
     const long long t0 = c * C::CH;
     const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
     mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
     parity ^= 1u << slot;
     __syncthreads();
-    quant_pass1<Tin, G>(s, s.buf[slot], nt);
-    __syncthreads();
-    quant_pass2<Tin, G>(s, s.buf[slot], p.h, p.c_h);
+    quant_chunk<Tin, G>(s, s.buf[slot], nt, p.h, p.c_h);
     __syncthreads();
     store_stage<Tin, G>(s, p.codes, t0 * G * b / 8, nt * G * b / 8);
     store_meta<Tin, G>(s, p, t0, nt);
@@ -838,6 +874,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.hist_fine = a.hist_fine;
   p.doneA = a.doneA;
   p.doneB = a.doneB;
+  p.doneB2 = a.doneB2;
   p.selready = a.selready;
   p.sel = a.sel;
   p.lookback = a.lookback;
@@ -859,9 +896,9 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   // and its quantize pass
   const long long group_in = a.n_g * G * (long long)sizeof(Tin);
   p.lag = (3 * group_in <= (72ll << 20)) ? 2 : 1;
-  p.pre = (p.lag == 1) ? p.nA / 4 : 0;
-  p.J = std::max<long long>(1, std::min<long long>(32, p.nA / 8));
-  p.n_items = a.n_groups * (2 * p.nA + p.J);
+  p.pre = (p.lag == 1) ? p.nA / 4 : p.nA / 8;
+  p.J = std::max<long long>(1, std::min<long long>(256, p.nA / 8));
+  p.n_items = a.n_groups * (2 * p.nA + 2 * p.J);
   cudaError_t e = cudaFuncSetAttribute(k_encode<Tin, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -30,6 +30,7 @@ struct EncodeArgs {
   uint32_t* cand_cnt;        // [n_groups]
   uint32_t* doneA;           // [n_groups] finished stats items
   uint32_t* doneB;           // [n_groups] finished select items
+  uint32_t* doneB2;          // [n_groups] finished offsets items
   uint32_t* selready;        // [n_groups] 1 once sel[g] is published
   SelResult* sel;            // [n_groups]
   uint32_t* hist_coarse;     // [n_groups * kCoarseBins]

@@ -115,13 +115,13 @@ __device__ __forceinline__ uint32_t team_sum_u(uint32_t s) {
 
 // ------------------------------------------------------------------ entropy key
 
-// Canonical entropy key of the team's tile: H = lg L - S / L with both sums pairwise.
+// The two sums of the team's tile that the entropy key needs: L = sum |a_k| and
+// S = sum |a_k| lg |a_k|, both pairwise (returned as {L, S} in every lane of the team).
 // Conflict-free lookups: Trep/Rrep hold entry i of lane l at i*32 + l.
 template <typename Tin, int G>
-__device__ __forceinline__ float tile_entropy(const uint32_t* w, const float* Trep,
-                                              const float* Rrep, const float* T, const float* R,
-                                              const float* sk, int lane, float& Lsum,
-                                              float& Ssum) {
+__device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep,
+                                            const float* Rrep, const float* T, const float* R,
+                                            const float* sk, int lane) {
   using Gm = TileGeom<Tin, G>;
   constexpr int V = Gm::V;
   float2 ms[V];  // {|a_k|, |a_k| lg |a_k|}
@@ -184,10 +184,13 @@ __device__ __forceinline__ float tile_entropy(const uint32_t* w, const float* Tr
       ms[j] = make_float2(m, __fmul_rn(m, lgv));
     }
   }
-  const float2 s = team_sum2<Gm::L>(tree2<V>(ms));
-  Lsum = s.x;
-  Ssum = s.y;
-  return (s.x == 0.0f) ? 0.0f : __fsub_rn(lg_canon<false>(s.x, T, R, sk), __fdiv_rn(s.y, s.x));
+  return team_sum2<Gm::L>(tree2<V>(ms));
+}
+
+// Entropy key in bits from the two sums: H = lg L - S / L (0 for an all-zero tile).
+__device__ __forceinline__ float entropy_key(float Ls, float Ss, const float* T, const float* R,
+                                             const float* sk) {
+  return (Ls == 0.0f) ? 0.0f : __fsub_rn(lg_canon<false>(Ls, T, R, sk), __fdiv_rn(Ss, Ls));
 }
 
 // ------------------------------------------------------------------ quantizer
@@ -219,6 +222,16 @@ __device__ __forceinline__ void lane_minmax_raw(const uint32_t* w, float& mn, fl
   }
 }
 
+// Whether two or more values of the team's tile have |v| >= thr, from a lane-level test
+// (for L >= 2: two lanes whose own max |v| reaches thr; one lane alone is inconclusive
+// and returns false).  `lane_amax` is the lane's own max |v|.
+template <int L>
+__device__ __forceinline__ bool team_two_ge(float lane_amax, float thr, int team) {
+  const unsigned m = __ballot_sync(kFull, lane_amax >= thr);
+  const unsigned mine = (m >> (team * L)) & ((L == 32) ? 0xFFFFFFFFu : ((1u << L) - 1u));
+  return __popc(mine) >= 2;
+}
+
 // Number of lane values with |v| >= thr (thr = m1 / 2, exact).
 template <typename Tin, int G>
 __device__ __forceinline__ uint32_t lane_count_ge(const uint32_t* w, float thr) {
@@ -242,16 +255,11 @@ __device__ __forceinline__ uint32_t lane_count_ge(const uint32_t* w, float thr) 
   return c;
 }
 
-// Quantise the lane's V values to b bits with the tile's (mn, inv) and pack them, code j
-// at bits [j*b, j*b+b) of the lane's b*V/8 bytes, into dst (byte stores).  For V = 4 the
-// caller pairs lanes first (see quant_store).  Returns nothing; writes bytes.
-//   u = (v - mn) * inv  (two roundings), code = rint(u); u lies in [0, Q + Q*2^-23], so the
-//   code never exceeds Q and no clamp is needed.  rint is done by adding 1.5*2^23: the
-//   float bits are then 0x4B400000 + code.
-template <int V>
-__device__ __forceinline__ void quant_pack8(const float* v, float mn, float inv, int b,
-                                            uint32_t* out_lo, uint32_t* out_hi) {
-  // eight codes -> (b <= 4) one 32-bit word, else two words
+// Quantise 8 values to b bits with the tile's (mn, inv); code j at bits [j*b, j*b+b).
+//   u = (v - mn) * inv  (two roundings), code = rint(u).  u lies in [0, Q + Q*2^-23], so
+//   the code never exceeds Q and no clamp is needed.  rint is done by adding 1.5*2^23:
+//   the float bits are then 0x4B400000 + code.  Returns the 8b-bit field (b <= 8).
+__device__ __forceinline__ unsigned long long quant8(const float* v, float mn, float inv, int b) {
   const float2 nmn = make_float2(-mn, -mn);
   const float2 mg = make_float2(12582912.0f, 12582912.0f);
   uint32_t bits[8];
@@ -271,20 +279,53 @@ __device__ __forceinline__ void quant_pack8(const float* v, float mn, float inv,
       spw += pw;
       acc += bits[j] * pw;
     }
-    *out_lo = acc - 0x4B400000u * spw;
-    *out_hi = 0u;
-  } else {
-    unsigned long long acc = 0ull;
+    return (unsigned long long)(acc - 0x4B400000u * spw);
+  }
+  unsigned long long acc = 0ull;
 #pragma unroll
-    for (int j = 0; j < 8; j++) acc |= (unsigned long long)(bits[j] & 0xFFu) << (j * b);
-    *out_lo = (uint32_t)acc;
-    *out_hi = (uint32_t)(acc >> 32);
+  for (int j = 0; j < 8; j++) acc |= (unsigned long long)(bits[j] & 0xFFu) << (j * b);
+  return acc;
+}
+
+// Store n (<= 16) bytes, given as a little-endian 128-bit value (lo, hi), at a shared
+// memory address, with the widest naturally aligned stores the address and n allow.
+__device__ __forceinline__ void sts_bytes(unsigned char* dst, unsigned long long lo,
+                                          unsigned long long hi, int n) {
+  const uint32_t a = (uint32_t)(uintptr_t)dst;
+  if (((a | (uint32_t)n) & 7u) == 0u) {
+    unsigned long long* d = reinterpret_cast<unsigned long long*>(dst);
+    d[0] = lo;
+    if (n == 16) d[1] = hi;
+  } else if (((a | (uint32_t)n) & 3u) == 0u) {
+    uint32_t* d = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll 1
+    for (int k = 0; k < n / 4; k++) d[k] = (uint32_t)((k < 2 ? lo : hi) >> (32 * (k & 1)));
+  } else if (((a | (uint32_t)n) & 1u) == 0u) {
+    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll 1
+    for (int k = 0; k < n / 2; k++) d[k] = (uint16_t)((k < 4 ? lo : hi) >> (16 * (k & 3)));
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < n; k++) dst[k] = (unsigned char)((k < 8 ? lo : hi) >> (8 * (k & 7)));
   }
 }
 
-__device__ __forceinline__ void store_bytes(unsigned char* dst, uint32_t lo, uint32_t hi, int n) {
-#pragma unroll 1
-  for (int k = 0; k < n; k++) dst[k] = (unsigned char)((k < 4 ? lo : hi) >> (8 * (k & 3)));
+// Quantise and pack the lane's V values (8 or 16) into its V*b/8 bytes at dst.
+template <int V>
+__device__ __forceinline__ void quant_store(const float* v, float mn, float inv, int b,
+                                            unsigned char* dst) {
+  unsigned long long lo = quant8(v, mn, inv, b), hi = 0ull;
+  if constexpr (V == 16) {
+    const unsigned long long q1 = quant8(v + 8, mn, inv, b);
+    const int sh = 8 * b;  // 24..64 bits
+    if (sh < 64) {
+      lo |= q1 << sh;
+      hi = q1 >> (64 - sh);
+    } else {
+      hi = q1;
+    }
+  }
+  sts_bytes(dst, lo, hi, V * b / 8);
 }
 
 // scale = D / Q and inv = Q / D for the team (one division per lane; lanes of a pair
