@@ -5,11 +5,14 @@
 // values") and Algorithm 1 step 5 (stage b de-quantises what it received); the stream
 // layout is §3.4's contiguous uint8 buffer with slots in tile order.
 //
-// One block decodes a chunk of consecutive tiles: slot offsets come from the running sum
-// of tile*bits/8 (block scan + decoupled look-back over earlier chunks), the chunk's
-// bytes are staged in shared memory with 16-byte loads, and each team of G/8 lanes
-// unpacks, de-quantises (fma(q, scale, zero)), inverse-transforms flagged tiles
-// (Hadamard, x 1/sqrt(h), swap positions 0 and d) and stores 8 floats per lane.
+// Three launches.  k_dec_totals: the slot bytes of every chunk of consecutive tiles (one
+// warp per chunk, from the bit widths).  k_dec_scan: one block turns them into each
+// chunk's byte offset in the stream.  k_decode: blocks take chunks in a grid-stride
+// loop; a block scan gives each tile's offset inside its chunk, the chunk's bytes and
+// metadata are staged in shared memory, and each team of G/8 lanes then
+// unpacks 8 codes per lane, de-quantises (fma(q, scale, zero)) and stores 8 floats per
+// lane.  Transformed tiles (pivot != 0xFF) are collected per warp and handled in a
+// second, compacted pass: Hadamard per hblock, x 1/sqrt(h), swap positions 0 and d.
 #include <algorithm>
 
 #include "tahq_device.cuh"
@@ -17,10 +20,10 @@
 
 namespace tahq {
 
-template <int kThreads>
+template <int kN>
 __device__ __forceinline__ uint32_t block_exclusive_scan_dec(uint32_t v, uint32_t& total,
                                                              uint32_t* s_warp) {
-  constexpr int kWarps = kThreads / 32;
+  constexpr int kW = kN / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -31,7 +34,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_dec(uint32_t v, uint32_
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
+    const uint32_t w = lane < kW ? s_warp[lane] : 0u;
     uint32_t wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -39,57 +42,168 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_dec(uint32_t v, uint32_
       if (lane >= o) wi += y;
     }
     __syncwarp();
-    if (lane < kWarps) s_warp[lane] = wi - w;
-    if (lane == kWarps - 1) s_warp[kWarps] = wi;
+    if (lane < kW) s_warp[lane] = wi - w;
+    if (lane == kW - 1) s_warp[kW] = wi;
   }
   __syncthreads();
-  total = s_warp[kWarps];
+  total = s_warp[kW];
   const uint32_t r = s_warp[warp] + incl - v;
   __syncthreads();
   return r;
 }
 
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+
 template <int G>
 struct DecCfg {
-  static constexpr int V = 8;
+  static constexpr int V = 8;  // codes / output floats per lane
   using Gm = Geom<V, G>;
-  static constexpr int kThreads = 256;
+  static constexpr int L = Gm::L, TPW = Gm::TPW;
   static constexpr int kSteps = 8;
-  static constexpr int CH = 8 * kSteps * Gm::TPW;             // tiles per chunk
-  static constexpr int kPer = (CH + kThreads - 1) / kThreads;
-  static constexpr int kStageBytes = CH * G + 48;              // b <= 8, plus pad
+  static constexpr int CH = kDecWarps * kSteps * TPW;  // tiles per chunk
+  static constexpr int NS = kSteps * TPW;              // tiles per warp
+  static constexpr int kPer = (CH + kDecThreads - 1) / kDecThreads;
+  static constexpr int kStage = CH * G + 64;           // b <= 8, plus pad and slack
 };
 
 template <int G>
-__global__ void __launch_bounds__(256) k_decode(DecodeArgs a, long long n_chunks) {
-  using Cf = DecCfg<G>;
-  constexpr int V = Cf::V, L = Cf::Gm::L, TPW = Cf::Gm::TPW, CH = Cf::CH;
-  __shared__ __align__(16) uint32_t s_stage[Cf::kStageBytes / 4];
-  __shared__ uint16_t s_off[CH];
-  __shared__ uint8_t s_bits[CH];
-  __shared__ uint32_t s_warp[9];
-  __shared__ long long s_c;
-  __shared__ unsigned long long s_base;
+struct alignas(16) DecSmem {
+  using C = DecCfg<G>;
+  uint32_t stage[C::kStage / 4];
+  float scale[C::CH], zero[C::CH];
+  uint16_t off[C::CH];
+  uint16_t flagged[C::CH];
+  uint8_t bits[C::CH], piv[C::CH];
+  uint32_t scan[kDecWarps + 1];
+};
 
+// Bytes of all slots of chunk c (bit widths outside 1..8 count as 0, as in the scan).
+template <int G>
+__device__ __forceinline__ uint32_t warp_chunk_bytes(const uint8_t* bits, long long n_tiles,
+                                                     long long c) {
+  constexpr int CH = DecCfg<G>::CH;
+  const long long t0 = c * CH;
+  const int nt = (int)min((long long)CH, n_tiles - t0);
+  const int lane = threadIdx.x & 31;
+  uint32_t sum = 0;
+  for (int k = lane; k < nt; k += 32) {
+    const int b = bits[t0 + k];
+    sum += (b >= 1 && b <= 8) ? (uint32_t)(G * b / 8) : 0u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  return sum;
+}
+
+__device__ __forceinline__ unsigned long long pk(float2 a) {
+  return ((unsigned long long)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+}
+__device__ __forceinline__ float2 upk(unsigned long long r) {
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+// (q0, q1) * s + z componentwise, each an fma rounded once (as fmaf).
+__device__ __forceinline__ float2 fma2(float2 q, float2 s, float2 z) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(q)), "l"(pk(s)), "l"(pk(z)));
+  return upk(d);
+}
+__device__ __forceinline__ float2 addp(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+
+// The lane's 8 codes of b bits (b whole bytes at stage byte `start`), de-quantised.
+__device__ __forceinline__ void dequant8(const uint32_t* sw, int start, int b, float sc, float mn,
+                                         float* v) {
+  const int q = start >> 2, sh = (start & 3) * 8;
+  const uint32_t w0 = sw[q], w1 = sw[q + 1], w2 = sw[q + 2];
+  const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
+  const unsigned long long acc = ((unsigned long long)hi << 32) | lo;
+  const uint32_t mask = (1u << b) - 1u;
+  const float2 s2 = make_float2(sc, sc), z2 = make_float2(mn, mn);
+  const float2 m2 = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const uint32_t c0 = (uint32_t)(acc >> (j * b)) & mask;
+    const uint32_t c1 = (uint32_t)(acc >> ((j + 1) * b)) & mask;
+    // (float)q exactly: the bits 0x4B000000 | q are 2^23 + q
+    const float2 qf = addp(make_float2(__uint_as_float(0x4B000000u | c0),
+                                       __uint_as_float(0x4B000000u | c1)), m2);
+    const float2 r = fma2(qf, s2, z2);
+    v[j] = r.x;
+    v[j + 1] = r.y;
+  }
+}
+
+// Slot bytes of every chunk (one warp per chunk); bit widths outside 1..8 count as 0.
+template <int G>
+__global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long long n_chunks) {
+  const long long c = (long long)blockIdx.x * kDecWarps + (threadIdx.x >> 5);
+  if (c >= n_chunks) return;
+  const uint32_t tot = warp_chunk_bytes<G>(a.bits, a.n_tiles, c);
+  if ((threadIdx.x & 31) == 0) a.lookback[c] = tot;
+}
+
+// Exclusive prefix of the chunk totals, in place (one block); flags a stream shorter
+// than the sum of all slots.
+__global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_chunks) {
+  __shared__ unsigned long long s_w[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long run = (n_chunks + 1023) / 1024;
+  const long long r0 = min(n_chunks, (long long)threadIdx.x * run), r1 = min(n_chunks, r0 + run);
+  unsigned long long mine = 0;
+  for (long long c = r0; c < r1; c++) mine += a.lookback[c];
+  unsigned long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long w = s_w[lane];
+    unsigned long long wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
+    }
+    __syncwarp();
+    s_w[lane] = wi - w;
+    if (lane == 31) s_w[32] = wi;
+  }
+  __syncthreads();
+  unsigned long long acc = s_w[warp] + incl - mine;
+  for (long long c = r0; c < r1; c++) {
+    const unsigned long long v = a.lookback[c];
+    a.lookback[c] = acc;
+    acc += v;
+  }
+  if (threadIdx.x == 0 && s_w[32] > a.codes_bytes) set_status(a.status, kStOverrun);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long n_chunks) {
+  using C = DecCfg<G>;
+  constexpr int V = C::V, L = C::L, TPW = C::TPW, CH = C::CH, NS = C::NS;
+  __shared__ DecSmem<G> s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = lane / L, sub = lane % L;
   const unsigned long long limit = a.codes_bytes;
-  const uint8_t* sb = reinterpret_cast<const uint8_t*>(s_stage);
 
-  for (;;) {
-    if (threadIdx.x == 0) s_c = (long long)atomicAdd(a.ticket, 1u);
-    __syncthreads();
-    const long long c = s_c;
-    if (c >= n_chunks) break;
+  for (long long c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     const long long t0 = c * CH;
     const int nt = (int)min((long long)CH, a.n_tiles - t0);
 
-    // 1. slot sizes of this chunk and their exclusive running sum
+    // 1. slot sizes of this chunk and their exclusive running sum; metadata staged
     uint32_t mine = 0u;
-    uint8_t bl[Cf::kPer];
+    uint8_t bl[C::kPer];
 #pragma unroll
-    for (int j = 0; j < Cf::kPer; j++) {
-      const int k = threadIdx.x * Cf::kPer + j;
+    for (int j = 0; j < C::kPer; j++) {
+      const int k = threadIdx.x * C::kPer + j;
       bl[j] = 0;
       if (k < nt) {
         int b = a.bits[t0 + k];
@@ -101,39 +215,29 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, long long n_chunks
         mine += (uint32_t)(G * b / 8);
       }
     }
+    for (int k = threadIdx.x; k < nt; k += kDecThreads) {
+      s.scale[k] = a.scales[t0 + k];
+      s.zero[k] = a.zeros[t0 + k];
+      s.piv[k] = a.pivots[t0 + k];
+    }
     uint32_t chunk_bytes;
-    uint32_t off = block_exclusive_scan_dec<256>(mine, chunk_bytes, s_warp);
+    uint32_t off = block_exclusive_scan_dec<kDecThreads>(mine, chunk_bytes, s.scan);
 #pragma unroll
-    for (int j = 0; j < Cf::kPer; j++) {
-      const int k = threadIdx.x * Cf::kPer + j;
+    for (int j = 0; j < C::kPer; j++) {
+      const int k = threadIdx.x * C::kPer + j;
       if (k < nt) {
-        s_bits[k] = bl[j];
-        s_off[k] = (uint16_t)off;
+        s.bits[k] = bl[j];
+        s.off[k] = (uint16_t)off;
         off += (uint32_t)(G * bl[j] / 8);
       }
     }
-
-    // 2. byte offset of the chunk: look-back over all earlier chunks
-    if (threadIdx.x == 0) {
-      unsigned long long prefix = 0ull;
-      if (c == 0) {
-        st_release_u64(&a.lookback[c], kLbPre | (unsigned long long)chunk_bytes);
-      } else {
-        st_release_u64(&a.lookback[c], kLbAgg | (unsigned long long)chunk_bytes);
-        prefix = lookback_prefix(a.lookback, c, 0, a.status);
-        st_release_u64(&a.lookback[c], kLbPre | (prefix + chunk_bytes));
-      }
-      if (prefix + chunk_bytes > limit) set_status(a.status, kStOverrun);
-      s_base = prefix;
-    }
-    __syncthreads();
-    const unsigned long long base = s_base;
+    const unsigned long long base = a.lookback[c];  // written by k_dec_scan
     const int pad = (int)(base & 15ull);
 
-    // 3. stage [base, base + chunk_bytes) in shared memory, never reading past codes_bytes
+    // 3. stage [base, base + chunk_bytes), never reading past codes_bytes
     const unsigned long long a0 = base - (unsigned long long)pad;
     const int n16 = (pad + (int)chunk_bytes + 15) / 16;
-    for (int w16 = threadIdx.x; w16 < n16; w16 += Cf::kThreads) {
+    for (int w16 = threadIdx.x; w16 < n16; w16 += kDecThreads) {
       const unsigned long long gb = a0 + 16ull * w16;
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
       if (gb + 16ull <= limit) {
@@ -144,62 +248,61 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, long long n_chunks
           if (gb + k < limit) tmp[k >> 2] |= (uint32_t)a.codes[gb + k] << (8 * (k & 3));
         w = make_uint4(tmp[0], tmp[1], tmp[2], tmp[3]);
       }
-      reinterpret_cast<uint4*>(s_stage)[w16] = w;
+      reinterpret_cast<uint4*>(s.stage)[w16] = w;
     }
     __syncthreads();
 
-    // 4. per tile: unpack, de-quantise, inverse transform, store
+    // 4. untransformed tiles; transformed ones are listed for the second pass
+    uint16_t* fl = s.flagged + warp * NS;
+    int nflag = 0;
 #pragma unroll 1
-    for (int s = 0; s < Cf::kSteps; s++) {
-      const int kt = (s * 8 + warp) * TPW + team;
-      const bool valid = kt < nt;
-      const long long t = t0 + kt;
-      int b = 0, piv = 0xFF;
-      float sc = 0.0f, mn = 0.0f;
-      bool ok = false;
+    for (int st = 0; st < C::kSteps; st++) {
+      const int kt = (st * kDecWarps + warp) * TPW + team;
+      bool valid = kt < nt, ok = false, flag = false;
+      int b = 0;
       if (valid) {
-        b = s_bits[kt];
-        piv = a.pivots[t];
-        sc = a.scales[t];
-        mn = a.zeros[t];
-        ok = b > 0 && base + s_off[kt] + (unsigned long long)(G * b / 8) <= limit;
+        b = s.bits[kt];
+        const int piv = s.piv[kt];
+        ok = b > 0 && base + s.off[kt] + (unsigned long long)(G * b / 8) <= limit;
         if (piv != 0xFF && piv >= G) {
           if (sub == 0) set_status(a.status, kStBadBits);
           ok = false;
         }
+        flag = ok && piv != 0xFF;
       }
-      unsigned long long acc = 0ull;
-      if (ok) {
-        const int start = pad + (int)s_off[kt] + sub * b;  // V = 8 codes = b whole bytes
-        for (int k = 0; k < b; k++) acc |= (unsigned long long)sb[start + k] << (8 * k);
-      }
-      const uint32_t qmask = (b >= 1) ? ((1u << b) - 1u) : 0u;
+      const unsigned fm = __ballot_sync(kFull, flag && sub == 0);
+      if (flag && sub == 0) fl[nflag + __popc(fm & ((1u << lane) - 1u))] = (uint16_t)kt;
+      nflag += __popc(fm);
+      if (!valid || flag) continue;
       float v[V];
-#pragma unroll
-      for (int j = 0; j < V; j++) {
-        const uint32_t q = (uint32_t)(acc >> (j * b)) & qmask;
-        v[j] = __fmaf_rn(__uint2float_rn(q), sc, mn);
-      }
-      const bool flag = ok && piv != 0xFF;
-      if (__any_sync(kFull, flag)) {
-        float w[V];
-#pragma unroll
-        for (int j = 0; j < V; j++) w[j] = v[j];
-        team_fwht<V, L>(w, a.h, sub);
-#pragma unroll
-        for (int j = 0; j < V; j++) w[j] = __fmul_rn(w[j], a.c_h);
-        team_swap0<V>(w, flag ? piv : 0, sub, lane - sub);
-        if (flag) {
-#pragma unroll
-          for (int j = 0; j < V; j++) v[j] = w[j];
-        }
-      }
-      if (!ok) {
+      if (ok) {
+        dequant8(s.stage, pad + (int)s.off[kt] + sub * b, b, s.scale[kt], s.zero[kt], v);
+      } else {
 #pragma unroll
         for (int j = 0; j < V; j++) v[j] = 0.0f;
       }
+      float4* o = reinterpret_cast<float4*>(a.out + (t0 + kt) * G + sub * V);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    __syncwarp();
+    // 5. transformed tiles of this warp, TPW at a time
+#pragma unroll 1
+    for (int j0 = 0; j0 < nflag; j0 += TPW) {
+      const int ci = j0 + team;
+      const bool valid = ci < nflag;
+      const int kt = valid ? (int)fl[ci] : 0;
+      const int b = valid ? (int)s.bits[kt] : 1;
+      const int piv = valid ? (int)s.piv[kt] : 0;
+      float v[V];
+      dequant8(s.stage, valid ? pad + (int)s.off[kt] + sub * b : 0, b, valid ? s.scale[kt] : 0.0f,
+               valid ? s.zero[kt] : 0.0f, v);
+      team_fwht<V, L>(v, a.h, sub);
+#pragma unroll
+      for (int j = 0; j < V; j++) v[j] = __fmul_rn(v[j], a.c_h);
+      team_swap0<V>(v, piv, sub, lane - sub);
       if (valid) {
-        float4* o = reinterpret_cast<float4*>(a.out + t * G + sub * V);
+        float4* o = reinterpret_cast<float4*>(a.out + (t0 + kt) * G + sub * V);
         o[0] = make_float4(v[0], v[1], v[2], v[3]);
         o[1] = make_float4(v[4], v[5], v[6], v[7]);
       }
@@ -209,15 +312,17 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a, long long n_chunks
 }
 
 long long decode_chunks(int G, long long n_tiles) {
-  const long long ch = 8ll * 8 * (32 / (G / 8));
+  const long long ch = (long long)kDecWarps * 8 * (32 / (G / 8));
   return (n_tiles + ch - 1) / ch;
 }
 
 template <int G>
 static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   const long long n_chunks = decode_chunks(G, a.n_tiles);
-  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
-  k_decode<G><<<blocks, 256, 0, st>>>(a, n_chunks);
+  k_dec_totals<G><<<(unsigned)((n_chunks + kDecWarps - 1) / kDecWarps), kDecThreads, 0, st>>>(a, n_chunks);
+  k_dec_scan<<<1, 1024, 0, st>>>(a, n_chunks);
+  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 4, n_chunks));
+  k_decode<G><<<blocks, kDecThreads, 0, st>>>(a, n_chunks);
   return cudaGetLastError();
 }
 

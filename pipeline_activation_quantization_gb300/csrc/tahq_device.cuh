@@ -238,6 +238,18 @@ __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned l
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Look-back words carry state and value in one 64-bit word, so reading them needs no
+// ordering with any other data: relaxed accesses at gpu scope are enough.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Decoupled look-back words: top two bits = state, low 62 bits = value.
 constexpr unsigned long long kLbAgg = 1ull << 62;
 constexpr unsigned long long kLbPre = 2ull << 62;
