@@ -2,9 +2,10 @@
 """Throughput of the sm_103a TAH-Quant activation codec (encode + decode round trip).
 
 One step = tahq_encode + tahq_decode of one synthetic activation tensor that is already
-resident in HBM (the whole hot path).  Default workload: the Llama-7B-like pipeline
-boundary, 8 x 2048 x 4096 bf16 (16384 tokens), tile = Hadamard block = 64, bits {3, 4},
-budget 3.0, ranking per 2048-token sample.  Prints one JSON line (rank 0).
+resident in HBM (the whole hot path).  Default workload: the 70B-width pipeline
+boundary, 16 x 2048 x 8192 fp32 (32768 tokens), tile = Hadamard block = 128, bits
+{3, 4}, budget 3.5, ranking per 2048-token sample; steps cycle through several fresh
+seeded tensors of that distribution.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N --steps K --warmup W --workload c3|c2|c4|c5 ...]
   python bench.py --impl reference     # the CPU oracle on the host cores (reference arm)
@@ -185,13 +186,17 @@ def run_reference(args):
     w = _workload(args)
     x = synth.generate(w)
     S = w.tokens_per_group or w.tokens
-    tok = S
+    # size each step's sample so that warm-up + timed steps take about 90 s of host time
+    t0 = time.perf_counter()
+    _oracle_step(x, w, 16)
+    per_token = (time.perf_counter() - t0) / 16
+    tok = int(max(1, min(S, 90.0 / max(1, args.steps + args.warmup) / max(per_token, 1e-9))))
     for _ in range(args.warmup):
         _oracle_step(x, w, tok)
     t0 = time.perf_counter()
     for k in range(args.steps):
-        g = k % max(1, w.tokens // S)
-        _oracle_step(x[g * S:], w, tok)
+        g = k % max(1, w.tokens // tok)
+        _oracle_step(x[g * tok:], w, tok)
     dt = time.perf_counter() - t0
     in_b = tok * w.channels * (4 if w.dtype == "f32" else 2)
     gbs = in_b * args.steps / dt / 1e9
@@ -203,8 +208,9 @@ def run_reference(args):
         "config": _config(w, {"sample_tokens_per_step": tok}),
         "tokens_per_s": round(tok * args.steps / dt, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step encodes+decodes one {tok}-token group of the "
-                                   f"workload on one host core (scalar C oracle)"},
+                         "sample": f"each step encodes+decodes {tok} consecutive tokens of the "
+                                   f"workload (ranked as one group of {tok} tokens) on one host "
+                                   f"core (scalar C oracle)"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -234,12 +240,18 @@ def run_gpu(args):
 
     w = _workload(args)
     T, C, G, h = w.tokens, w.channels, w.tile, w.hblock
-    x_np = synth.generate(w, index=rank)
+    n_tensors = args.tensors or (3 if args.workload == "c5" else 1)
     dev = torch.device("cuda", local)
-    if w.dtype == "bf16":
-        x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
-    else:
-        x = torch.from_numpy(x_np).to(dev)
+    xs, x_np = [], None
+    for i in range(n_tensors):
+        xi = synth.generate(w, index=rank * n_tensors + i)
+        if x_np is None:
+            x_np = xi
+        if w.dtype == "bf16":
+            xs.append(torch.from_numpy(xi.view(np.int16)).to(dev).view(torch.bfloat16))
+        else:
+            xs.append(torch.from_numpy(xi).to(dev))
+    x = xs[0]
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -252,12 +264,14 @@ def run_gpu(args):
     ws = enc["workspace"]
     K_hi = tq.tahq_hi_count(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
     n_g = (w.tokens_per_group or T) * (C // G)
-    launches = 3 + (1 if 0 < K_hi < n_g else 0) + 1   # stats, [collect], final, quant; decode
+    launches = 1 + 3   # encode: one kernel; decode: totals, scan, decode
+    enc_kernel = (f"k_encode<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>" if 0 < K_hi < n_g
+                  else f"k_encode_flat<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>")
 
-    def step(ev):
+    def step(ev, k=0):
         ev[0].record(stream)
-        tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group, out=out_bufs,
-                  workspace=ws, stream=stream)
+        tq.encode(xs[k % n_tensors], G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
+                  out=out_bufs, workspace=ws, stream=stream)
         ev[1].record(stream)
         tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
         ev[2].record(stream)
@@ -276,7 +290,7 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             for k in range(args.steps):
                 flush.fill_(k & 255)
-                step(evs[k])
+                step(evs[k], k)
         stream.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier()
@@ -297,8 +311,8 @@ def run_gpu(args):
     value = world * in_b * args.steps / (tot_ms * 1e-3) / 1e9
     e_ms, d_ms = statistics.mean(enc_ms), statistics.mean(dec_ms)
     enc_gbs, dec_gbs = enc_b / (e_ms * 1e-3) / 1e9, dec_b / (d_ms * 1e-3) / 1e9
-    dom = ("k_decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
-    dom_name = f"k_decode<{G}>" if dom[0] == "k_decode" else "tahq_encode (4 kernels)"
+    dom = ("decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
+    dom_name = f"k_decode<{G}> (+ k_dec_totals, k_dec_scan)" if dom[0] == "decode" else enc_kernel
 
     # end to end through the public API: pinned host input -> device, encode, decode,
     # decoded tensor -> pinned host
@@ -339,7 +353,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}"}),
+        "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}",
+                                                     "fresh_tensors_cycled": n_tensors}),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
         "encode": {"ms": round(e_ms, 5), "alg_bytes": enc_b, "GB_s": round(enc_gbs, 2),
@@ -369,7 +384,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="tahq", choices=["tahq", "reference"])
-    ap.add_argument("--workload", default="c3", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="c5", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tensors", type=int, default=0,
+                    help="distinct seeded tensors cycled over the steps (default 3 for c5, else 1)")
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--hblock", type=int, default=0)
     ap.add_argument("--budget", type=float, default=None)
@@ -379,8 +396,6 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
-        if args.steps == 2000:
-            args.steps = 8
         return run_reference(args)
     return run_gpu(args)
 
