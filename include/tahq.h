@@ -125,8 +125,9 @@ tahq_status tahq_decode(const uint8_t *codes, size_t codes_bytes, const float *s
  * Size of the fixed device scratch array behind tahq_decode_noalloc: 256 KiB, held in
  * the memory of every GPU that loads the library until the process exits.  It bounds
  * the shapes that entry point accepts: tahq_decode_workspace_size(tokens, channels,
- * tile) must not exceed it, i.e. at most 32704 look-back chunks -- about 4.2 M tiles of
- * width 128, 8.4 M of width 64, 16.7 M of width 32, 33.5 M of width 16, 67 M of width 8.
+ * tile) must not exceed it, i.e. at most 52288 decode chunks (4 bytes each, plus 8 bytes
+ * per 8 chunks) -- about 6.7 M tiles of width 128, 13.4 M of width 64, 26.8 M of width 32,
+ * 53.5 M of width 16, 107 M of width 8.
  */
 #define TAHQ_NOALLOC_SCRATCH_BYTES (256u * 1024u)
 

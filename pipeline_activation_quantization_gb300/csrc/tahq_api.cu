@@ -128,7 +128,7 @@ EncLayout enc_layout(const Shape& s) {
 }
 
 struct DecLayout {
-  size_t status, ticket, lookback, total;
+  size_t status, ticket, ctot, bsum, total;
 };
 
 DecLayout dec_layout(const Shape& s) {
@@ -138,8 +138,10 @@ DecLayout dec_layout(const Shape& s) {
   off = align_up(off + 16);
   L.ticket = off;
   off = align_up(off + 64);
-  L.lookback = off;
-  off = align_up(off + 8 * (size_t)tahq::decode_chunks(s.G, s.n));
+  L.ctot = off;
+  off = align_up(off + 4 * (size_t)tahq::decode_chunks(s.G, s.n));
+  L.bsum = off;
+  off = align_up(off + 8 * (size_t)tahq::decode_blocks(s.G, s.n));
   L.total = off;
   return L;
 }
@@ -265,7 +267,8 @@ tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* s
   const DecLayout L = dec_layout(s);
   if (workspace_bytes < L.total) return TAHQ_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, L.total, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  // status and ticket; the offset arrays are written in full before they are read
+  if (cudaMemsetAsync(workspace, 0, L.ctot, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
   if (s.n == 0) return TAHQ_OK;
   const int sms = num_sms_current();
   if (sms <= 0) return TAHQ_ERR_CUDA;
@@ -284,7 +287,8 @@ tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* s
   a.out = out;
   a.status = at<uint32_t>(workspace, L.status);
   a.ticket = at<uint32_t>(workspace, L.ticket);
-  a.lookback = at<unsigned long long>(workspace, L.lookback);
+  a.ctot = at<uint32_t>(workspace, L.ctot);
+  a.bsum = at<unsigned long long>(workspace, L.bsum);
   return tahq::launch_decode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 

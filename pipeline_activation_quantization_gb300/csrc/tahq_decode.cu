@@ -6,8 +6,8 @@
 // layout is §3.4's contiguous uint8 buffer with slots in tile order.
 //
 // Three launches.  k_dec_totals: the slot bytes of every chunk of consecutive tiles (one
-// warp per chunk, from the bit widths).  k_dec_scan: one block turns them into each
-// chunk's byte offset in the stream.  k_decode: blocks take chunks in a grid-stride
+// warp per chunk, from the bit widths) and their running sum inside each block of 8
+// chunks.  k_dec_scan: one block turns the block totals into stream offsets.  k_decode: blocks take chunks in a grid-stride
 // loop; a block scan gives each tile's offset inside its chunk, the chunk's bytes and
 // metadata are staged in shared memory, and each team of G/8 lanes then
 // unpacks 8 codes per lane, de-quantises (fma(q, scale, zero)) and stores 8 floats per
@@ -137,52 +137,78 @@ __device__ __forceinline__ void dequant8(const uint32_t* sw, int start, int b, f
   }
 }
 
-// Slot bytes of every chunk (one warp per chunk); bit widths outside 1..8 count as 0.
+// Slot bytes of every chunk (one warp per chunk, kDecChunksPerBlock chunks per block);
+// bit widths outside 1..8 count as 0.  Each chunk gets its offset inside its block
+// (ctot), each block its total (bsum, turned into stream offsets by k_dec_scan).
+static_assert(kDecWarps == kDecChunksPerBlock, "one warp per chunk of a block");
 template <int G>
 __global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long long n_chunks) {
-  const long long c = (long long)blockIdx.x * kDecWarps + (threadIdx.x >> 5);
-  if (c >= n_chunks) return;
-  const uint32_t tot = warp_chunk_bytes<G>(a.bits, a.n_tiles, c);
-  if ((threadIdx.x & 31) == 0) a.lookback[c] = tot;
-}
-
-// Exclusive prefix of the chunk totals, in place (one block); flags a stream shorter
-// than the sum of all slots.
-__global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_chunks) {
-  __shared__ unsigned long long s_w[33];
+  __shared__ uint32_t s_t[kDecWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long run = (n_chunks + 1023) / 1024;
-  const long long r0 = min(n_chunks, (long long)threadIdx.x * run), r1 = min(n_chunks, r0 + run);
-  unsigned long long mine = 0;
-  for (long long c = r0; c < r1; c++) mine += a.lookback[c];
-  unsigned long long incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_w[warp] = incl;
+  const long long c = (long long)blockIdx.x * kDecWarps + warp;
+  const uint32_t tot = c < n_chunks ? warp_chunk_bytes<G>(a.bits, a.n_tiles, c) : 0u;
+  if (lane == 0) s_t[warp] = tot;
   __syncthreads();
   if (warp == 0) {
-    const unsigned long long w = s_w[lane];
-    unsigned long long wi = w;
+    const uint32_t v = lane < kDecWarps ? s_t[lane] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < kDecWarps; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long cc = (long long)blockIdx.x * kDecWarps + lane;
+    if (lane < kDecWarps && cc < n_chunks) a.ctot[cc] = incl - v;
+    if (lane == kDecWarps - 1) a.bsum[blockIdx.x] = incl;
+  }
+}
+
+// Exclusive prefix of the block totals, in place (one block of 1024 threads, coalesced
+// passes of 4096 entries); flags a stream shorter than the sum of all slots.
+__global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blocks) {
+  constexpr int kPer = 4, kPass = 1024 * kPer;
+  __shared__ unsigned long long s_w[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long carry = 0;
+  for (long long p0 = 0; p0 < n_blocks; p0 += kPass) {
+    const long long i0 = p0 + (long long)threadIdx.x * kPer;
+    unsigned long long v[kPer], mine = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; j++) {
+      v[j] = i0 + j < n_blocks ? a.bsum[i0 + j] : 0ull;
+      mine += v[j];
+    }
+    unsigned long long incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += y;
+      const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
     }
-    __syncwarp();
-    s_w[lane] = wi - w;
-    if (lane == 31) s_w[32] = wi;
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long w = s_w[lane];
+      unsigned long long wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, wi, o);
+        if (lane >= o) wi += y;
+      }
+      __syncwarp();
+      s_w[lane] = wi - w;
+      if (lane == 31) s_w[32] = wi;
+    }
+    __syncthreads();
+    unsigned long long acc = carry + s_w[warp] + incl - mine;
+#pragma unroll
+    for (int j = 0; j < kPer; j++) {
+      if (i0 + j < n_blocks) a.bsum[i0 + j] = acc;
+      acc += v[j];
+    }
+    carry += s_w[32];
+    __syncthreads();
   }
-  __syncthreads();
-  unsigned long long acc = s_w[warp] + incl - mine;
-  for (long long c = r0; c < r1; c++) {
-    const unsigned long long v = a.lookback[c];
-    a.lookback[c] = acc;
-    acc += v;
-  }
-  if (threadIdx.x == 0 && s_w[32] > a.codes_bytes) set_status(a.status, kStOverrun);
+  if (threadIdx.x == 0 && carry > a.codes_bytes) set_status(a.status, kStOverrun);
 }
 
 template <int G>
@@ -231,7 +257,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
         off += (uint32_t)(G * bl[j] / 8);
       }
     }
-    const unsigned long long base = a.lookback[c];  // written by k_dec_scan
+    // written by k_dec_totals and k_dec_scan
+    const unsigned long long base = a.bsum[c / kDecChunksPerBlock] + a.ctot[c];
     const int pad = (int)(base & 15ull);
 
     // 3. stage [base, base + chunk_bytes), never reading past codes_bytes
@@ -319,8 +346,9 @@ long long decode_chunks(int G, long long n_tiles) {
 template <int G>
 static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   const long long n_chunks = decode_chunks(G, a.n_tiles);
-  k_dec_totals<G><<<(unsigned)((n_chunks + kDecWarps - 1) / kDecWarps), kDecThreads, 0, st>>>(a, n_chunks);
-  k_dec_scan<<<1, 1024, 0, st>>>(a, n_chunks);
+  const long long n_blocks = decode_blocks(G, a.n_tiles);
+  k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks);
+  k_dec_scan<<<1, 1024, 0, st>>>(a, n_blocks);
   const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 4, n_chunks));
   k_decode<G><<<blocks, kDecThreads, 0, st>>>(a, n_chunks);
   return cudaGetLastError();

@@ -54,12 +54,18 @@ struct DecodeArgs {
   float* out;
   uint32_t* status;
   uint32_t* ticket;
-  unsigned long long* lookback;  // [decode_chunks]
+  uint32_t* ctot;                // [decode_chunks] chunk offset inside its block of 8 chunks
+  unsigned long long* bsum;      // [decode_blocks] stream offset of each block of 8 chunks
 };
 
-// Number of look-back chunks the encode / decode kernels use for these shapes.
+// Number of look-back chunks the encode kernels use for these shapes.
 long long encode_chunks(int bf16, int G, long long n_g, long long n_groups);
+// Number of decode chunks, and of blocks of kDecChunksPerBlock chunks, for these shapes.
+constexpr int kDecChunksPerBlock = 8;
 long long decode_chunks(int G, long long n_tiles);
+inline long long decode_blocks(int G, long long n_tiles) {
+  return (decode_chunks(G, n_tiles) + kDecChunksPerBlock - 1) / kDecChunksPerBlock;
+}
 
 cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);

@@ -55,12 +55,12 @@ def test_noalloc_decode_matches_decode_twice(name):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     import torch
-    # width-8 tiles: 2048 tiles per look-back chunk, so 32705 chunks need more than 256 KiB
-    T, C, G = 32705 * 2048 * 8 // 1024, 1024, 8
+    # width-8 tiles: 2048 tiles per decode chunk, so 52289 chunks need more than 256 KiB
+    T, C, G = 52289 * 2048 * 8 // 1024, 1024, 8
     assert tq.tahq_decode_workspace_size(T, C, G) > 256 * 1024
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
     f = torch.zeros(4, dtype=torch.float32, device="cuda")
     rc = tq.tahq_decode_noalloc(dummy, 16, f, f, dummy, dummy, T, C, G, G, f)
     assert rc == 3        # TAHQ_ERR_WORKSPACE, before anything is launched
     # the largest accepted shape for this width is still accepted by the size check
-    assert tq.tahq_decode_workspace_size(32704 * 2048 * 8 // 1024, C, G) <= 256 * 1024
+    assert tq.tahq_decode_workspace_size(52288 * 2048 * 8 // 1024, C, G) <= 256 * 1024
