@@ -170,10 +170,12 @@ const char *tahq_status_string(int status);
 int tahq_version(void);
 
 /*
- * The host-side tables the kernels use for the canonical base-2 logarithm:
- * T[i] = nearest float to log2(1 + i/128), R[i] = nearest float to 1/(1 + i/128),
- * k[j] = nearest float to (-1)^j / ((j+1) ln 2), j = 0..3.  Exposed so that a CPU test
- * can check them without a GPU.  T and R hold 128 floats, k 4.
+ * The host-side tables the kernels use for the canonical base-2 logarithm
+ * (lg x = e + fmaf(P(r), r, T[i]), r = fmaf(m, R[i], -1) for x = 2^e m, i = the top 7
+ * fraction bits of m, P(r) = fmaf(fmaf(k[2], r, k[1]), r, k[0])):
+ * R[i] = nearest float to 1/(1 + i/128), T[i] = nearest float to -log2(R[i]),
+ * k[j] = nearest float to (-1)^j / ((j+1) ln 2), j = 0..2.  Exposed so that a CPU test
+ * can check them without a GPU.  T and R hold 128 floats, k 3.
  */
 void tahq_log2_tables(float *T, float *R, float *k);
 

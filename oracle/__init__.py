@@ -87,7 +87,7 @@ def _f32(a) -> np.ndarray:
 # ----------------------------------------------------------------------------- scalars
 
 def log2_tables():
-    T = np.zeros(128, np.float32); R = np.zeros(128, np.float32); k = np.zeros(4, np.float32)
+    T = np.zeros(128, np.float32); R = np.zeros(128, np.float32); k = np.zeros(3, np.float32)
     lib().oracle_log2_tables(_ptr(T), _ptr(R), _ptr(k))
     return T, R, k
 

@@ -28,7 +28,8 @@
  *     -sum p log p.  eps, varsigma -> 0 with 0 log 0 = 0, an all-zero tile has H = 0,
  *     log base 2 (the base does not change the ranking).
  *   - With p_k = m_k / L (L = sum m_k), -sum p_k lg p_k = lg L - (sum m_k lg m_k) / L.
- *     That form is evaluated, in fp32, in a fixed order: pairwise sums, our own lg.
+ *     That form is evaluated, in fp32, in a fixed order: pairwise sums (the first level
+ *     of sum m_k lg m_k as one fused multiply-add per pair), our own table-driven lg.
  *   - rho = 1e-12f, strict r > tau, pivot = lowest index among equal maxima.
  *   - ranking scope: each group of tokens_per_group consecutive tokens (a "sample");
  *     K = floor((budget - lo) * n_g / (hi - lo)) tiles of a group get hi bits, chosen
@@ -36,7 +37,8 @@
  *   - pivot goes to tile position 0; with hblock h < G the Hadamard is block diagonal.
  *   - Sylvester natural order, FWHT stages len = 1, 2, 4, ..., then x RN(1/sqrt(h)).
  *   - quantizer: min/max affine, float zero-point = min (a zero minimum emitted as +0),
- *     round to nearest even;
+ *     code = the integer nearest (ties to even) to the exact product of the rounded
+ *     v - min and the rounded Q / (max - min);
  *     a tile whose range max-min is below 2^-120 (this includes max == min) is
  *     encoded as constant: scale 0, all codes 0, zero = min.
  *   - code k of a tile occupies bits [k*b, k*b+b) of its slot, LSB first within
@@ -57,16 +59,16 @@
 #define ORACLE_BF16 1
 
 /* ------------------------------------------------------------------------------------ */
-/* The canonical base-2 logarithm.                                                       */
+/* The canonical base-2 logarithm (table-driven, in the manner of Tang's logarithm).     */
 /*                                                                                       */
-/* x = 2^e * m with m in [1, 2).  c_i = 1 + i/128 where i is the top 7 bits of m's       */
-/* fraction, so c_i <= m < c_i + 1/128 and f = m - c_i is exact.                         */
-/*   lg(x) = e + (T[i] + P(r)),  r = f * R[i],  T[i] = log2(c_i),  R[i] = 1/c_i,         */
-/* where P is the Mercator series of log2(1 + r) cut after r^4 (|r| < 2^-7, so the      */
-/* truncation error is below 1e-11), evaluated in Horner form with fmaf.                 */
-/* T and R are the float32 values nearest to their double-precision values.              */
+/* x = 2^e * m with m in [1, 2).  i = the top 7 bits of m's fraction, c_i = 1 + i/128,   */
+/* R_i = the float nearest 1/c_i, T_i = the float nearest -log2(R_i) (R_i as stored).    */
+/*   r = fmaf(m, R_i, -1)        (m R_i - 1, rounded once; |r| < 2^-7 (1 + 2^-7))        */
+/*   lg(x) = e + fmaf(P(r), r, T_i),  P(r) = fmaf(fmaf(k3, r, k2), r, k1)                 */
+/* since log2(m) = -log2(R_i) + log2(1 + r).  k_j = (-1)^(j+1) / (j ln 2): the Mercator   */
+/* series of log2(1 + r) cut after r^3 (truncation below 2e-9).                           */
 /* ------------------------------------------------------------------------------------ */
-static float T_tab[128], R_tab[128], P_k[5];
+static float T_tab[128], R_tab[128], P_k[4];
 static int tables_ready = 0;
 
 static void init_tables(void)
@@ -74,11 +76,11 @@ static void init_tables(void)
     if (tables_ready) return;
     for (int i = 0; i < 128; i++) {
         double c = 1.0 + (double)i / 128.0;
-        T_tab[i] = (float)log2(c);
         R_tab[i] = (float)(1.0 / c);
+        T_tab[i] = (float)(-log2((double)R_tab[i]));
     }
     const double ln2 = 0.69314718055994530942;
-    for (int j = 1; j <= 4; j++)      /* log2(1+r) = sum_j (-1)^(j+1) r^j / (j ln 2) */
+    for (int j = 1; j <= 3; j++)      /* log2(1+r) = sum_j (-1)^(j+1) r^j / (j ln 2) */
         P_k[j] = (float)(((j % 2) ? 1.0 : -1.0) / ((double)j * ln2));
     tables_ready = 1;
 }
@@ -88,7 +90,7 @@ void oracle_log2_tables(float *T, float *R, float *k)
     init_tables();
     memcpy(T, T_tab, sizeof T_tab);
     memcpy(R, R_tab, sizeof R_tab);
-    for (int j = 0; j < 4; j++) k[j] = P_k[j + 1];
+    for (int j = 0; j < 3; j++) k[j] = P_k[j + 1];
 }
 
 static uint32_t f2u(float x) { uint32_t u; memcpy(&u, &x, 4); return u; }
@@ -106,13 +108,10 @@ float oracle_lg(float x)
     }
     int i = (int)((b >> 16) & 0x7Fu);
     float m = u2f((b & 0x007FFFFFu) | 0x3F800000u);   /* m in [1, 2) */
-    float c = 1.0f + (float)i / 128.0f;                 /* exact */
-    float f = m - c;                                     /* exact */
-    float r = f * R_tab[i];
-    float p = fmaf(P_k[4], r, P_k[3]);
-    p = fmaf(p, r, P_k[2]);
+    float r = fmaf(m, R_tab[i], -1.0f);
+    float p = fmaf(P_k[3], r, P_k[2]);
     p = fmaf(p, r, P_k[1]);
-    float t = T_tab[i] + p * r;
+    float t = fmaf(p, r, T_tab[i]);
     return (float)e + t;
 }
 
@@ -132,16 +131,23 @@ float oracle_pairwise_sum(const float *x, int n)
 /* Per-tile statistics (§3.2 eq. (1)-(2), §3.3 eq. (3)).                                 */
 /* ------------------------------------------------------------------------------------ */
 
-/* Entropy key in bits:  H = lg L - S / L,  L = sum m_k,  S = sum m_k lg m_k. */
+/* Entropy key in bits:  H = lg L - S / L,  L = sum m_k,  S = sum m_k lg m_k.
+ * Both sums are pairwise over the tile in natural order.  The first level of S is one
+ * fused step per pair: fmaf(m_{2j+1}, lg m_{2j+1}, m_{2j} lg m_{2j}) (the even product
+ * rounded, the odd one exact inside the fma); a zero magnitude contributes a zero term. */
 float oracle_entropy_key(const float *a, int G)
 {
-    float m[128], term[128];
+    float m[128], lm[128], L1[64], S1[64];
     for (int k = 0; k < G; k++) {
         m[k] = fabsf(a[k]);
-        term[k] = (m[k] == 0.0f) ? 0.0f : m[k] * oracle_lg(m[k]);
+        lm[k] = (m[k] == 0.0f) ? 0.0f : oracle_lg(m[k]);
     }
-    float L = oracle_pairwise_sum(m, G);
-    float S = oracle_pairwise_sum(term, G);
+    for (int j = 0; j < G / 2; j++) {
+        L1[j] = m[2 * j] + m[2 * j + 1];
+        S1[j] = fmaf(m[2 * j + 1], lm[2 * j + 1], m[2 * j] * lm[2 * j]);
+    }
+    float L = oracle_pairwise_sum(L1, G / 2);
+    float S = oracle_pairwise_sum(S1, G / 2);
     if (L == 0.0f) return 0.0f;
     return oracle_lg(L) - S / L;
 }
@@ -232,8 +238,10 @@ void oracle_hadamard_dense(const double *x, double *y, int h)
 /* Asymmetric uniform quantizer (§3.3) and bit packing (§3.4).                           */
 /* ------------------------------------------------------------------------------------ */
 
-/* Quantise G values to b bits.  near[k] (optional) is set when the pre-rounding value
- * u_k lies within 1e-5 * max(1, |u_k|) of a .5 rounding boundary. */
+/* Quantise G values to b bits: code_k = round-half-even(u_k), u_k = (v_k - mn) * inv
+ * with v_k - mn and inv = Q / D each rounded to float and the product exact (one
+ * rounding from the two floats to the code).  near[k] (optional) is set when u_k lies
+ * within 1e-5 * max(1, |u_k|) of a .5 rounding boundary. */
 void oracle_quantize_tile(const float *v, int G, int b, uint8_t *q, float *scale, float *zero,
                           uint8_t *near)
 {
@@ -253,13 +261,12 @@ void oracle_quantize_tile(const float *v, int G, int b, uint8_t *q, float *scale
     *scale = D / (float)Q;
     float inv = (float)Q / D;
     for (int k = 0; k < G; k++) {
-        float u = (v[k] - mn) * inv;
-        float r = rintf(u);
-        if (r < 0.0f) r = 0.0f;
-        if (r > (float)Q) r = (float)Q;
+        double du = (double)(v[k] - mn) * (double)inv;   /* exact: 24 x 24 bits */
+        double r = rint(du);
+        if (r < 0.0) r = 0.0;
+        if (r > (double)Q) r = (double)Q;
         q[k] = (uint8_t)r;
         if (near) {
-            double du = (double)u;
             double frac = du - floor(du);
             double tol = 1e-5 * (fabs(du) > 1.0 ? fabs(du) : 1.0);
             near[k] = (fabs(frac - 0.5) <= tol) ? 1 : 0;

@@ -155,7 +155,7 @@ def tahq_version() -> int:
 
 def tahq_log2_tables():
     import numpy as np
-    T = np.zeros(128, np.float32); R = np.zeros(128, np.float32); k = np.zeros(4, np.float32)
+    T = np.zeros(128, np.float32); R = np.zeros(128, np.float32); k = np.zeros(3, np.float32)
     lib().tahq_log2_tables(T.ctypes.data, R.ctypes.data, k.ctypes.data)
     return T, R, k
 

@@ -11,7 +11,7 @@ namespace {
 
 using tahq::LgTables;
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 20000;  // 2.0.0: one-rounding quantizer, fused entropy leaves
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -23,13 +23,18 @@ const LgTables& lg_tables() {
   static LgTables tabs;
   static std::once_flag once;
   std::call_once(once, [] {
+    const double ln2 = 0.69314718055994530942;
+    for (int j = 0; j < 3; j++) tabs.k[j] = (float)(((j % 2) ? -1.0 : 1.0) / ((j + 1) * ln2));
     for (int i = 0; i < 128; i++) {
       const double c = 1.0 + i / 128.0;
-      tabs.T[i] = (float)std::log2(c);
       tabs.R[i] = (float)(1.0 / c);
+      tabs.T[i] = (float)(-std::log2((double)tabs.R[i]));
+      // fraction part of lg(c_i) by the general path (c_i is exact in float)
+      const float r = std::fmaf((float)c, tabs.R[i], -1.0f);
+      float p = std::fmaf(tabs.k[2], r, tabs.k[1]);
+      p = std::fmaf(p, r, tabs.k[0]);
+      tabs.TB[i] = std::fmaf(p, r, tabs.T[i]);
     }
-    const double ln2 = 0.69314718055994530942;
-    for (int j = 0; j < 4; j++) tabs.k[j] = (float)(((j % 2) ? -1.0 : 1.0) / ((j + 1) * ln2));
   });
   return tabs;
 }

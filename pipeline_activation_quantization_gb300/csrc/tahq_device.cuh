@@ -27,10 +27,15 @@ constexpr uint32_t kStOverrun = 0x10u;
 
 // Tables of the canonical logarithm, passed to kernels by value and copied to shared
 // memory (indexed loads from the parameter bank would serialise).
+//   T[i] = RN(-log2 R[i]), R[i] = RN(1 / c_i), c_i = 1 + i/128, k = Mercator coefficients
+//   (1/ln2, -1/(2 ln2), 1/(3 ln2)); TB[i] = the fraction part of lg(c_i) as the general
+//   path computes it (fmaf(P(r), r, T[i]) with r = fmaf(c_i, R[i], -1)), for inputs whose
+//   mantissa has no bits below the top 7 (every bf16 value).
 struct LgTables {
   float T[128];
   float R[128];
-  float k[4];
+  float TB[128];
+  float k[3];
 };
 
 // One group's threshold: a tile is hi iff mode == kSelAll, or mode == kSelThreshold and
@@ -53,12 +58,14 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
 
 // ------------------------------------------------------------------ canonical logarithm
 
-// kNoFraction: the caller guarantees that x has no mantissa bits below the top 7
-// (true for every bf16 value, normal or subnormal), so r == 0 and P is skipped; the
-// result is identical to the general path because r * P(r) = +0 there.
+// The canonical base-2 logarithm of a positive finite float: x = 2^e m, m in [1, 2),
+// i = top 7 fraction bits, r = fmaf(m, R[i], -1), lg = e + fmaf(P(r), r, T[i]) with
+// P(r) = fmaf(fmaf(k3, r, k2), r, k1).  kNoFraction: the caller guarantees that x has no
+// mantissa bits below the top 7 (true for every bf16 value, normal or subnormal), so
+// m = c_i and the fraction part is the precomputed TB[i] -- the same value.
 template <bool kNoFraction>
 __device__ __forceinline__ float lg_canon(float x, const float* sT, const float* sR,
-                                          const float* sk) {
+                                          const float* sTB, const float* sk) {
   uint32_t b = __float_as_uint(x);
   int e = (int)(b >> 23) - 127;
   if ((b >> 23) == 0u) {  // subnormal: normalise by 2^24, exactly
@@ -68,16 +75,13 @@ __device__ __forceinline__ float lg_canon(float x, const float* sT, const float*
   const int i = (int)((b >> 16) & 0x7Fu);
   float t;
   if (kNoFraction) {
-    t = sT[i];
+    t = sTB[i];
   } else {
     const float m = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-    const float c = __uint_as_float(0x3F800000u | ((uint32_t)i << 16));  // 1 + i/128
-    const float f = __fsub_rn(m, c);                                     // exact
-    const float r = __fmul_rn(f, sR[i]);
-    float p = __fmaf_rn(sk[3], r, sk[2]);
-    p = __fmaf_rn(p, r, sk[1]);
+    const float r = __fmaf_rn(m, sR[i], -1.0f);
+    float p = __fmaf_rn(sk[2], r, sk[1]);
     p = __fmaf_rn(p, r, sk[0]);
-    t = __fadd_rn(sT[i], __fmul_rn(p, r));
+    t = __fmaf_rn(p, r, sT[i]);
   }
   return __fadd_rn((float)e, t);
 }

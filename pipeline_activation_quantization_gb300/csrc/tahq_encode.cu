@@ -64,7 +64,7 @@ struct alignas(128) EncSmem {
   unsigned char stage[C::kStage];
   float Trep[128 * 32];  // lg tables replicated per bank: entry i of lane l at i*32 + l
   float Rrep[InTraits<Tin>::kNoFraction ? 4 : 128 * 32];
-  float T[128], R[128], k[4];
+  LgTables tabs;
   float scale[C::CH], zero[C::CH];
   float ta[C::CH], tb[C::CH];  // per-tile pairs: (L, S) in stats, (min, max) then inv in quant
   uint16_t off[C::CH];
@@ -110,14 +110,19 @@ struct EncParams {
 template <typename Tin, int G>
 __device__ __forceinline__ void init_tables(EncSmem<Tin, G>& sm, const LgTables& tabs) {
   for (int i = threadIdx.x; i < 128 * 32; i += kThreads) {
-    sm.Trep[i] = tabs.T[i >> 5];
-    if constexpr (!InTraits<Tin>::kNoFraction) sm.Rrep[i] = tabs.R[i >> 5];
+    if constexpr (InTraits<Tin>::kNoFraction) {
+      sm.Trep[i] = tabs.TB[i >> 5];
+    } else {
+      sm.Trep[i] = tabs.T[i >> 5];
+      sm.Rrep[i] = tabs.R[i >> 5];
+    }
   }
   for (int i = threadIdx.x; i < 128; i += kThreads) {
-    sm.T[i] = tabs.T[i];
-    sm.R[i] = tabs.R[i];
+    sm.tabs.T[i] = tabs.T[i];
+    sm.tabs.R[i] = tabs.R[i];
+    sm.tabs.TB[i] = tabs.TB[i];
   }
-  if (threadIdx.x < 4) sm.k[threadIdx.x] = tabs.k[threadIdx.x];
+  if (threadIdx.x < 3) sm.tabs.k[threadIdx.x] = tabs.k[threadIdx.x];
 }
 
 template <int kN>
@@ -479,7 +484,7 @@ __device__ void do_stats(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
 #pragma unroll
       for (int k = 0; k < W; k++) w[k] = 0u;
     }
-    const float2 ls = tile_sums<Tin, G>(w, s.Trep, s.Rrep, s.T, s.R, s.k, lane);
+    const float2 ls = tile_sums<Tin, G>(w, s.Trep, s.Rrep, s.tabs, lane);
     if (valid && sub == 0) {
       s.ta[kt] = ls.x;
       s.tb[kt] = ls.y;
@@ -496,7 +501,7 @@ __device__ void do_stats(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
     int cb = -1;
     if (valid) {
       const float Ls = s.ta[kt], Ss = s.tb[kt];
-      const float H = entropy_key(Ls, Ss, s.T, s.R, s.k);
+      const float H = entropy_key(Ls, Ss, s.tabs);
       p.keys[t0 + kt] = H;
       if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
         set_status(p.status, kStNonFinite);

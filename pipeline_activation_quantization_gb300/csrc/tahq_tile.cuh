@@ -52,6 +52,12 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
   return upk2(d);
 }
+// Packed fused multiply-add: a * b + c per component, rounded once (as fmaf).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+  return upk2(d);
+}
 
 // Lane's words of tile kt from a staged chunk.
 template <typename Tin, int G>
@@ -116,15 +122,16 @@ __device__ __forceinline__ uint32_t team_sum_u(uint32_t s) {
 // ------------------------------------------------------------------ entropy key
 
 // The two sums of the team's tile that the entropy key needs: L = sum |a_k| and
-// S = sum |a_k| lg |a_k|, both pairwise (returned as {L, S} in every lane of the team).
-// Conflict-free lookups: Trep/Rrep hold entry i of lane l at i*32 + l.
+// S = sum |a_k| lg |a_k|, both pairwise in natural order (returned as {L, S} in every
+// lane of the team).  The first level of S is fmaf(m_odd, lg m_odd, RN(m_even lg m_even))
+// per pair.  Conflict-free lookups: Trep/Rrep hold entry i of lane l at i*32 + l (Trep =
+// TB for bf16 input, T for fp32).
 template <typename Tin, int G>
 __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep,
-                                            const float* Rrep, const float* T, const float* R,
-                                            const float* sk, int lane) {
+                                            const float* Rrep, const LgTables& tb, int lane) {
   using Gm = TileGeom<Tin, G>;
   constexpr int V = Gm::V;
-  float2 ms[V];  // {|a_k|, |a_k| lg |a_k|}
+  float2 ls[V / 2];  // level 1: {m_2j + m_2j+1, fused pair of S}
   if constexpr (InTraits<Tin>::kBf16) {
     // bf16 subnormals (exponent 0, mantissa != 0) need the normalising path
     uint32_t subn = 0u;
@@ -137,13 +144,15 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep
       float v[V];
       words_to_values<Tin, G>(w, v);
 #pragma unroll
-      for (int j = 0; j < V; j++) {
-        const float m = fabsf(v[j]);
-        ms[j] = make_float2(m, m == 0.0f ? 0.0f : __fmul_rn(m, lg_canon<true>(m, T, R, sk)));
+      for (int j = 0; j < V; j += 2) {
+        const float m0 = fabsf(v[j]), m1 = fabsf(v[j + 1]);
+        const float l0 = m0 == 0.0f ? 0.0f : lg_canon<true>(m0, tb.T, tb.R, tb.TB, tb.k);
+        const float l1 = m1 == 0.0f ? 0.0f : lg_canon<true>(m1, tb.T, tb.R, tb.TB, tb.k);
+        ls[j / 2] = make_float2(__fadd_rn(m0, m1), __fmaf_rn(m1, l1, __fmul_rn(m0, l0)));
       }
     } else {
       const uint32_t lane4 = (uint32_t)lane << 2;
-      const char* tb = reinterpret_cast<const char*>(Trep);
+      const char* tbl = reinterpret_cast<const char*>(Trep);
 #pragma unroll
       for (int k = 0; k < Gm::W; k++) {
         const uint32_t x = w[k];
@@ -151,46 +160,45 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep
         const float mhi = __uint_as_float(x & 0x7FFF0000u);
         const float elo = __uint_as_float(((x >> 7) & 0xFFu) | 0x4B000000u);
         const float ehi = __uint_as_float(((x >> 23) & 0xFFu) | 0x4B000000u);
-        const float tlo = *reinterpret_cast<const float*>(tb + (((x << 7) & 0x3F80u) | lane4));
-        const float thi = *reinterpret_cast<const float*>(tb + (((x >> 9) & 0x3F80u) | lane4));
+        const float tlo = *reinterpret_cast<const float*>(tbl + (((x << 7) & 0x3F80u) | lane4));
+        const float thi = *reinterpret_cast<const float*>(tbl + (((x >> 9) & 0x3F80u) | lane4));
         const float2 ef = add2(make_float2(elo, ehi), make_float2(-8388735.0f, -8388735.0f));
-        const float2 lg = add2(ef, make_float2(tlo, thi));  // e + T[i] (r = 0 for bf16)
-        const float2 tm = make_float2(__fmul_rn(mlo, lg.x), __fmul_rn(mhi, lg.y));
-        // a zero magnitude gives lg = -127 and a term of -0; see lg_fast in tahq_encode.cu
-        ms[2 * k] = make_float2(mlo, tm.x);
-        ms[2 * k + 1] = make_float2(mhi, tm.y);
+        const float2 lg = add2(ef, make_float2(tlo, thi));  // e + TB[i]
+        // a zero magnitude gives lg = -127 and a zero term (its sign cannot reach H)
+        ls[k] = make_float2(__fadd_rn(mlo, mhi), __fmaf_rn(mhi, lg.y, __fmul_rn(mlo, lg.x)));
       }
     }
   } else {
+    float lgv[V], m[V];
 #pragma unroll
     for (int j = 0; j < V; j++) {
-      const float m = fabsf(__uint_as_float(w[j]));
-      const uint32_t b = __float_as_uint(m);
+      m[j] = fabsf(__uint_as_float(w[j]));
+      const uint32_t b = __float_as_uint(m[j]);
       const uint32_t E = b >> 23;
-      float lgv;
       if (E == 0u && b != 0u) {
-        lgv = lg_canon<false>(m, T, R, sk);
-      } else {
+        lgv[j] = lg_canon<false>(m[j], tb.T, tb.R, tb.TB, tb.k);
+      } else {  // normal, or zero (lg = -127, a zero term)
         const uint32_t idx = (((b >> 16) & 0x7Fu) << 5) | (uint32_t)lane;
         const float ef = __fsub_rn(__uint_as_float(0x4B000000u | E), 8388735.0f);
         const float mm = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-        const float c = __uint_as_float((b & 0x007F0000u) | 0x3F800000u);
-        const float r = __fmul_rn(__fsub_rn(mm, c), Rrep[idx]);
-        float p = __fmaf_rn(sk[3], r, sk[2]);
-        p = __fmaf_rn(p, r, sk[1]);
-        p = __fmaf_rn(p, r, sk[0]);
-        lgv = __fadd_rn(ef, __fadd_rn(Trep[idx], __fmul_rn(p, r)));
+        const float r = __fmaf_rn(mm, Rrep[idx], -1.0f);
+        float p = __fmaf_rn(tb.k[2], r, tb.k[1]);
+        p = __fmaf_rn(p, r, tb.k[0]);
+        lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, Trep[idx]));
       }
-      ms[j] = make_float2(m, __fmul_rn(m, lgv));
     }
+#pragma unroll
+    for (int j = 0; j < V; j += 2)
+      ls[j / 2] = make_float2(__fadd_rn(m[j], m[j + 1]),
+                              __fmaf_rn(m[j + 1], lgv[j + 1], __fmul_rn(m[j], lgv[j])));
   }
-  return team_sum2<Gm::L>(tree2<V>(ms));
+  return team_sum2<Gm::L>(tree2<V / 2>(ls));
 }
 
 // Entropy key in bits from the two sums: H = lg L - S / L (0 for an all-zero tile).
-__device__ __forceinline__ float entropy_key(float Ls, float Ss, const float* T, const float* R,
-                                             const float* sk) {
-  return (Ls == 0.0f) ? 0.0f : __fsub_rn(lg_canon<false>(Ls, T, R, sk), __fdiv_rn(Ss, Ls));
+__device__ __forceinline__ float entropy_key(float Ls, float Ss, const LgTables& tb) {
+  return (Ls == 0.0f) ? 0.0f
+                      : __fsub_rn(lg_canon<false>(Ls, tb.T, tb.R, tb.TB, tb.k), __fdiv_rn(Ss, Ls));
 }
 
 // ------------------------------------------------------------------ quantizer
@@ -256,17 +264,19 @@ __device__ __forceinline__ uint32_t lane_count_ge(const uint32_t* w, float thr) 
 }
 
 // Quantise 8 values to b bits with the tile's (mn, inv); code j at bits [j*b, j*b+b).
-//   u = (v - mn) * inv  (two roundings), code = rint(u).  u lies in [0, Q + Q*2^-23], so
-//   the code never exceeds Q and no clamp is needed.  rint is done by adding 1.5*2^23:
-//   the float bits are then 0x4B400000 + code.  Returns the 8b-bit field (b <= 8).
+//   code = the integer nearest (v - mn) * inv, the difference rounded and the product
+//   exact: fmaf(v - mn, inv, 1.5*2^23) rounds at integer spacing (ties to even), and the
+//   float bits are then 0x4B400000 + code.  The product lies in [0, Q (1 + 2^-24)], so
+//   the code never exceeds Q and no clamp is needed.  Returns the 8b-bit field (b <= 8).
 __device__ __forceinline__ unsigned long long quant8(const float* v, float mn, float inv, int b) {
   const float2 nmn = make_float2(-mn, -mn);
   const float2 mg = make_float2(12582912.0f, 12582912.0f);
+  const float2 inv2 = make_float2(inv, inv);
   uint32_t bits[8];
 #pragma unroll
   for (int j = 0; j < 8; j += 2) {
     const float2 a = add2(make_float2(v[j], v[j + 1]), nmn);
-    const float2 r = add2(make_float2(__fmul_rn(a.x, inv), __fmul_rn(a.y, inv)), mg);
+    const float2 r = fma2(a, inv2, mg);
     bits[j] = __float_as_uint(r.x);
     bits[j + 1] = __float_as_uint(r.y);
   }

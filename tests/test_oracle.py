@@ -49,9 +49,11 @@ def test_lg_error_bound_all_exponents_and_subnormals():
 def test_lg_tables_are_nearest_floats():
     T, R, k = oracle.log2_tables()
     i = np.arange(128, dtype=np.float64)
-    assert np.array_equal(T, np.log2(1 + i / 128).astype(F32))
     assert np.array_equal(R, (1 / (1 + i / 128)).astype(F32))
-    j = np.arange(1, 5)
+    # T_i = -log2 of the stored R_i, so log2(m) = T_i + log2(m R_i) holds exactly
+    assert np.array_equal(T, (-np.log2(R.astype(np.float64))).astype(F32))
+    assert T[0] == 0 and np.all(np.diff(T) > 0) and T[-1] < 1
+    j = np.arange(1, 4)
     assert np.array_equal(k, (((-1.0) ** (j + 1)) / (j * math.log(2))).astype(F32))
 
 
@@ -236,6 +238,38 @@ def test_quantizer_bounds(b):
         vh = np.array([np.float32(np.float64(qq) * s + z) for qq in q])   # fma: single rounding
         err = np.abs(vh.astype(np.float64) - v)
         assert np.all(err <= s / 2 * (1 + 1e-3) + 4 * _ulp(v) + 4 * _ulp(z))
+
+
+@pytest.mark.parametrize("b", [2, 3, 4, 8])
+def test_quantizer_codes_are_nearest_integers_of_the_exact_product(b):
+    # code_k = the integer nearest (v_k - mn) * inv computed exactly, ties to even; the
+    # inputs include products that fall within one fp32 rounding of a .5 boundary
+    from fractions import Fraction
+    Q = (1 << b) - 1
+    rng = np.random.default_rng(40 + b)
+    tiles = list(synth.random_tiles(41, 60, 64, "mixed"))
+    for _ in range(60):    # values on (k + 1/2) / inv, nudged by one ulp either way
+        base = rng.standard_normal(64).astype(F32)
+        mn, mx = F32(base.min()), F32(base.max())
+        inv = F32(F32(Q) / F32(mx - mn))
+        k = rng.integers(0, Q, 64)
+        tgt = ((k + 0.5) / np.float64(inv) + np.float64(mn)).astype(F32)
+        tgt = np.nextafter(tgt, rng.choice([-np.inf, np.inf], 64).astype(F32)).astype(F32)
+        v = np.clip(tgt, mn, mx).astype(F32)
+        v[0], v[1] = mn, mx
+        tiles.append(v)
+    for v in tiles:
+        q, s, z, _ = oracle.quantize_tile(v, b)
+        mn, mx = F32(v.min()), F32(v.max())
+        if float(mx) - float(mn) < 2.0 ** -120:
+            continue
+        inv = F32(F32(Q) / F32(mx - mn))
+        for vk, qk in zip(v, q):
+            u = Fraction(float(F32(vk - mn))) * Fraction(float(inv))
+            n = int(u)                      # u >= 0
+            frac = u - n
+            want = n + 1 if frac > Fraction(1, 2) or (frac == Fraction(1, 2) and n % 2) else n
+            assert int(qk) == min(want, Q), (float(u), int(qk))
 
 
 def test_quantizer_error_falls_with_bits():
