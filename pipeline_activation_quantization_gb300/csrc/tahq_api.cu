@@ -93,10 +93,10 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
 
 struct EncLayout {
   size_t status, ticket, cand_cnt, doneA, doneB, doneB2, selready, sel, hist_coarse, hist_fine, lookback,
-      ctrl_end, keys, cand, total;
+      ctrl_end, keys, cand, scratch_lo, scratch_hi, total;
 };
 
-// Look-back words are sized for fp32 input, whose smaller chunks need the most of them.
+// Offset words are sized for the input type that needs the most compaction chunks.
 EncLayout enc_layout(const Shape& s) {
   EncLayout L{};
   size_t off = 0;
@@ -121,13 +121,19 @@ EncLayout enc_layout(const Shape& s) {
   L.hist_fine = off;
   off = align_up(off + 4ull * tahq::kFineBins * (size_t)s.n_groups);
   L.lookback = off;
-  const long long chunks = tahq::encode_chunks(0, s.G, s.n_g, s.n_groups);
+  const long long chunks = std::max(tahq::encode_chunks(0, s.G, s.hi, s.n_g, s.n_groups),
+                                    tahq::encode_chunks(1, s.G, s.hi, s.n_g, s.n_groups));
   off = align_up(off + 8 * (size_t)chunks);
   L.ctrl_end = off;
   L.keys = off;
   off = align_up(off + 4 * (size_t)s.n);
   L.cand = off;
   off = align_up(off + 8 * (size_t)s.n);
+  // every tile quantised at both widths, fixed slots (read back by the compaction)
+  L.scratch_lo = off;
+  off = align_up(off + (size_t)s.n * (size_t)(s.G * s.lo / 8));
+  L.scratch_hi = off;
+  off = align_up(off + (size_t)s.n * (size_t)(s.G * s.hi / 8));
   L.total = off;
   return L;
 }
@@ -252,6 +258,8 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.lookback = at<unsigned long long>(workspace, L.lookback);
   a.keys = at<float>(workspace, L.keys);
   a.cand = at<unsigned long long>(workspace, L.cand);
+  a.scratch_lo = at<uint8_t>(workspace, L.scratch_lo);
+  a.scratch_hi = at<uint8_t>(workspace, L.scratch_hi);
   return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 

@@ -35,9 +35,11 @@ struct EncodeArgs {
   SelResult* sel;            // [n_groups]
   uint32_t* hist_coarse;     // [n_groups * kCoarseBins]
   uint32_t* hist_fine;       // [n_groups * kFineBins]
-  unsigned long long* lookback;  // [encode_chunks]
+  unsigned long long* lookback;  // [encode_chunks] compaction chunk counts, then offsets
   float* keys;               // [n_tiles]
   unsigned long long* cand;  // [n_tiles]
+  uint8_t* scratch_lo;       // [n_tiles * G * lo / 8] every tile quantised at bits_lo
+  uint8_t* scratch_hi;       // [n_tiles * G * hi / 8] every tile quantised at bits_hi
 };
 
 struct DecodeArgs {
@@ -58,8 +60,10 @@ struct DecodeArgs {
   unsigned long long* bsum;      // [decode_blocks] stream offset of each block of 8 chunks
 };
 
-// Number of look-back chunks the encode kernels use for these shapes.
-long long encode_chunks(int bf16, int G, long long n_g, long long n_groups);
+// Tiles per compaction chunk of the encode kernel, and the number of compaction chunks
+// (one offset word each) for these shapes.
+long long encode_cchunk_tiles(int bf16, int G, int hi);
+long long encode_chunks(int bf16, int G, int hi, long long n_g, long long n_groups);
 // Number of decode chunks, and of blocks of kDecChunksPerBlock chunks, for these shapes.
 constexpr int kDecChunksPerBlock = 8;
 long long decode_chunks(int G, long long n_tiles);

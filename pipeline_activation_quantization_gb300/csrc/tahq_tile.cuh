@@ -124,11 +124,11 @@ __device__ __forceinline__ uint32_t team_sum_u(uint32_t s) {
 // The two sums of the team's tile that the entropy key needs: L = sum |a_k| and
 // S = sum |a_k| lg |a_k|, both pairwise in natural order (returned as {L, S} in every
 // lane of the team).  The first level of S is fmaf(m_odd, lg m_odd, RN(m_even lg m_even))
-// per pair.  Conflict-free lookups: Trep/Rrep hold entry i of lane l at i*32 + l (Trep =
-// TB for bf16 input, T for fp32).
+// per pair.  Conflict-free lookups: `rep` holds entry i of lane l at index i*32 + l
+// (floats TB[i] for bf16 input, float2 (T[i], R[i]) for fp32).
 template <typename Tin, int G>
-__device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep,
-                                            const float* Rrep, const LgTables& tb, int lane) {
+__device__ __forceinline__ float2 tile_sums(const uint32_t* w, const void* rep, const LgTables& tb,
+                                            int lane) {
   using Gm = TileGeom<Tin, G>;
   constexpr int V = Gm::V;
   float2 ls[V / 2];  // level 1: {m_2j + m_2j+1, fused pair of S}
@@ -152,7 +152,7 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep
       }
     } else {
       const uint32_t lane4 = (uint32_t)lane << 2;
-      const char* tbl = reinterpret_cast<const char*>(Trep);
+      const char* tbl = static_cast<const char*>(rep);
 #pragma unroll
       for (int k = 0; k < Gm::W; k++) {
         const uint32_t x = w[k];
@@ -178,13 +178,13 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const float* Trep
       if (E == 0u && b != 0u) {
         lgv[j] = lg_canon<false>(m[j], tb.T, tb.R, tb.TB, tb.k);
       } else {  // normal, or zero (lg = -127, a zero term)
-        const uint32_t idx = (((b >> 16) & 0x7Fu) << 5) | (uint32_t)lane;
+        const float2 tr = static_cast<const float2*>(rep)[(((b >> 16) & 0x7Fu) << 5) | (uint32_t)lane];
         const float ef = __fsub_rn(__uint_as_float(0x4B000000u | E), 8388735.0f);
         const float mm = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-        const float r = __fmaf_rn(mm, Rrep[idx], -1.0f);
+        const float r = __fmaf_rn(mm, tr.y, -1.0f);
         float p = __fmaf_rn(tb.k[2], r, tb.k[1]);
         p = __fmaf_rn(p, r, tb.k[0]);
-        lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, Trep[idx]));
+        lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, tr.x));
       }
     }
 #pragma unroll
