@@ -1,0 +1,1253 @@
+// tahq_encode.cuh -- encode kernels of the TAH-Quant activation codec for sm_103a
+// (instantiated per input type by tahq_encode_f32.cu and tahq_encode_bf16.cu).
+//
+// "TAH-Quant: Effective Activation Quantization in Pipeline Parallelism over Slow
+// Network" (arXiv 2506.01352v2):
+//   §3.2 eq. (1)-(2): entropy key of every tile and the per-group key histograms;
+//   §3.2 "Top-p% tile selection": the K tiles of highest (key, -index) of each group get
+//        the high bit width -- histogram bucket, then an exact selection among the
+//        candidates of that bucket;
+//   §3.3 eq. (3) outlier ratio and pivot, pivot swap + eq. (4) Hadamard, the asymmetric
+//        quantizer; §3.4's contiguous uint8 stream.
+//
+// The input is read from HBM once.  k_encode runs four kinds of work item in one
+// persistent kernel:
+//   tiles    (per 32 KB input chunk) entropy key + histograms, range, pretest, the exact
+//            outlier test / pivot swap / Hadamard where needed, and the tile quantised at
+//            BOTH candidate widths into two scratch streams with fixed slots;
+//   select   (per group) the K-th ranked key: candidates of the histogram bucket that
+//            holds it, then their exact rank;
+//   offsets  (per group) every tile's width, hi counts per compaction chunk, their
+//            exclusive prefix;
+//   compact  (per compaction chunk) copy each tile's slot of its width from scratch to
+//            its place in the stream, and its scale; the scratch lines are then dropped
+//            from L2 without being written back.
+// Items are handed out in increasing order by an atomic ticket and only wait for earlier
+// items, so every wait ends (and each is bounded anyway).  The ticket order interleaves
+// one group's tiles items with the compaction of the group two (or one) before, so the
+// scratch a compaction reads is still in L2.
+//
+// k_encode_flat covers allocations that do not depend on the ranking (K = 0 or K = n_g:
+// every tile gets the same width): one pass straight into the stream, no keys.
+//
+// Two data layouts, chosen per (input type, tile width):
+//   line   (tiles of >= 128 bytes) one lane = one 128-byte line, chunks staged by 2-D
+//          tensor copies with the 128-byte swizzle (tahq_line.cuh);
+//   narrow (smaller tiles) a team of L lanes holds a tile, 32 bytes per lane, chunks
+//          staged by 1-D bulk copies (tahq_tile.cuh).
+// In both, a tile that fails the cheap two-values pretest (two values of magnitude
+// >= max / 2 rule out r > tau) is handled again exactly, with the whole team or warp.
+#pragma once
+
+#include <algorithm>
+#include <cfloat>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+
+#include "tahq_device.cuh"
+#include "tahq_launch.h"
+#include "tahq_line.cuh"
+#include "tahq_tile.cuh"
+
+namespace tahq {
+
+constexpr int kChunkBytes = kEncChunkBytes;
+constexpr uint8_t kDeferred = 0xFE;  // narrow layout: pass-1 marker of a tile left to pass 2
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCC = kEncMaxCC;     // tiles per compaction chunk, at most
+constexpr int kRankMax = 2048;        // candidates ranked in one pass (else radix select)
+
+template <typename Tin, int G>
+struct Cfg {
+  static constexpr bool kBf16 = InTraits<Tin>::kBf16;
+  static constexpr bool kLine = G * (int)sizeof(Tin) >= 128;
+  static constexpr int CH = kChunkBytes / (G * (int)sizeof(Tin));  // tiles per input chunk
+  // narrow layout: a team of L lanes per tile, V values per lane
+  using Gm = TileGeom<Tin, G>;
+  static constexpr int V = Gm::V, W = Gm::W, L = Gm::L, TPW = Gm::TPW;
+  static constexpr int kSteps = CH / (kWarps * TPW);  // warp steps per chunk
+  static constexpr int NS = CH / kWarps;              // tiles owned by a warp
+  static constexpr int kArr = kLine ? 1 : CH;         // per-tile arrays of the narrow layout
+  static_assert(kLine || kSteps * kWarps * TPW == CH, "chunk must be whole warp steps");
+};
+
+// A 2-D tensor-copy descriptor (the driver's CUtensorMap, opaque here).
+struct alignas(64) TmaDesc {
+  unsigned char bytes[128];
+};
+
+struct Item {
+  int type;  // kItemTiles, kItemSelect, kItemOffsets, kItemCompact
+  long long g, idx;
+};
+constexpr int kItemTiles = 0, kItemSelect = 1, kItemOffsets = 2, kItemCompact = 3;
+
+template <typename Tin, int G>
+struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
+  using C = Cfg<Tin, G>;
+  unsigned char buf[2][kChunkBytes];  // input chunks (a compaction uses its slot's as stage)
+  LgTables tabs;
+  // narrow layout, per tile of the input chunk: (L, S) in stats, then (min, max) and
+  // (inv_lo, inv_hi or scale); deferred lists
+  float ta[C::kArr], tb[C::kArr], tc[C::kArr];
+  uint8_t piv[C::kArr];
+  uint16_t dl[C::CH];  // deferred tiles (line: one list per block; narrow: per warp)
+  uint32_t ndef;       // line layout: length of dl
+  uint32_t hist[kCoarseBins];
+  uint32_t scan[kWarps + 4];
+  unsigned long long bar[2];
+  Item item[2];
+  long long next;
+  uint32_t last;
+};
+
+struct EncParams {
+  TmaDesc tmap;  // line layout: the input as [rows of 128 bytes]
+  const void* x;
+  long long n_tiles, n_g, n_groups, K, group_bytes, codes_bytes;
+  long long nA, nC, CHC, J, lag, pre1, pre2, n_items;
+  uint32_t seg_n;
+  uint32_t seg[5][8];
+  int lo, hi, h, flat_b;
+  int slot_lo, slot_hi;
+  uint32_t stage_lo_bytes;  // offset of the hi stage after the lo stage
+  float c_h;
+  uint8_t* codes;
+  float* scales;
+  float* zeros;
+  uint8_t* bits;
+  uint8_t* pivots;
+  uint8_t* scratch_lo;
+  uint8_t* scratch_hi;
+  float* keys;
+  unsigned long long* cand;
+  uint32_t* cand_cnt;
+  uint32_t* hist_coarse;
+  uint32_t* hist_fine;
+  uint32_t* doneA;
+  uint32_t* doneB;
+  uint32_t* doneB2;
+  uint32_t* selready;  // 1 once sel[g] is published, 2 once the compaction offsets are
+  SelResult* sel;
+  unsigned long long* lookback;  // per group: hi count, then offset, of each compaction chunk
+  uint32_t* ticket;
+  uint32_t* status;
+  LgTables tabs;
+};
+
+// ====================================================================== helpers
+
+template <typename Tin, int G>
+__device__ __forceinline__ void init_tables(EncSmem<Tin, G>& sm, const LgTables& tabs) {
+  for (int i = threadIdx.x; i < 128 * 32; i += kThreads) {
+    if constexpr (Cfg<Tin, G>::kBf16) {
+      g_lgTB[i] = tabs.TB[i >> 5];
+    } else {
+      g_lgT[i] = tabs.T[i >> 5];
+      g_lgR[i] = tabs.R[i >> 5];
+    }
+  }
+  for (int i = threadIdx.x; i < 128; i += kThreads) {
+    sm.tabs.T[i] = tabs.T[i];
+    sm.tabs.R[i] = tabs.R[i];
+    sm.tabs.TB[i] = tabs.TB[i];
+  }
+  if (threadIdx.x < 3) sm.tabs.k[threadIdx.x] = tabs.k[threadIdx.x];
+}
+
+template <int kN>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& total,
+                                                         uint32_t* s_warp) {
+  constexpr int kW = kN / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < kW ? s_warp[lane] : 0u;
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
+    }
+    __syncwarp();
+    if (lane < kW) s_warp[lane] = wi - w;
+    if (lane == kW - 1) s_warp[kW] = wi;
+  }
+  __syncthreads();
+  total = s_warp[kW];
+  const uint32_t r = s_warp[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// One warp: bins[0..255] in shared memory, 1 <= k <= sum(bins).  Walking the bins from
+// the top (255 down to 0) with a running count, returns the bin at which the count first
+// reaches k and the count strictly above that bin.
+__device__ __forceinline__ void warp_find_from_top(const uint32_t* bins, uint32_t k, int& bin,
+                                                   uint32_t& above) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8], s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+    c[j] = bins[255 - (lane * 8 + j)];
+    s += c[j];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t excl = incl - s;
+  const unsigned hit = __ballot_sync(kFull, incl >= k);
+  const int src = hit ? (__ffs(hit) - 1) : 31;
+  int my_bin = 0;
+  uint32_t my_above = 0;
+  if (lane == src) {
+    uint32_t cum = excl;
+    my_bin = 255 - (lane * 8 + 7);
+    my_above = cum;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      if (cum + c[j] >= k) {
+        my_bin = 255 - (lane * 8 + j);
+        my_above = cum;
+        break;
+      }
+      cum += c[j];
+    }
+  }
+  bin = __shfl_sync(kFull, my_bin, src);
+  above = __shfl_sync(kFull, my_above, src);
+}
+
+__device__ __forceinline__ float qmax_f(int b) {
+  return __fsub_rn(__uint_as_float(0x4B000000u | ((1u << b) - 1u)), 8388608.0f);
+}
+
+// Per-tile results of the tiles pass that do not depend on the width chosen later:
+// zero-point, pivot, and the range D (in `scales` until the compaction turns it into
+// D / Q).  In the one-width pass the scale and width are final at once.
+__device__ __forceinline__ void put_meta(const EncParams& p, long long t, float mn, uint8_t piv,
+                                         float d_or_scale, bool flat) {
+  p.zeros[t] = __fadd_rn(mn, 0.0f);
+  p.pivots[t] = piv;
+  p.scales[t] = d_or_scale;
+  if (flat) p.bits[t] = (uint8_t)p.flat_b;
+}
+
+// ====================================================================== tiles: line layout
+
+// Deferred tiles, a team of L lanes (V values each) per tile: list[j] for j = first +
+// team, first + TPW + team, ... while j < n (first / step warp-uniform): the exact ratio
+// test (eq. (3)), pivot swap and Hadamard (eq. (4)) where it holds, range, both widths.
+template <typename Tin, int G, bool kSwz>
+__device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned char* buf,
+                                            const uint16_t* list, int n, int first, int step,
+                                            long long t0, bool flat, unsigned char* stage_lo,
+                                            unsigned char* stage_hi) {
+  using C = Cfg<Tin, G>;
+  constexpr int V = C::V, W = C::W, L = C::L;
+  const int lane = threadIdx.x & 31;
+  const int team = lane / L, sub = lane % L;
+  const int lo = flat ? p.flat_b : p.lo, hi = p.hi;
+  const int slot_lo = G * lo / 8;
+#pragma unroll 1
+  for (int j0 = first; j0 < n; j0 += step) {
+    const int ci = j0 + team;
+    const bool valid = ci < n;
+    const int kt = valid ? (int)list[ci] : 0;
+    uint32_t w[W];
+    if (valid) {
+      if constexpr (kSwz) {
+        lds_words_swz<Tin, G>(buf, kt, sub, w);
+      } else {
+        lds_words<Tin, G>(buf, kt, sub, w);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; k++) w[k] = 0u;
+    }
+    float v[V];
+    words_to_values<Tin, G>(w, v);
+    float m1 = fabsf(v[0]), m2 = -1.0f;
+    int i1 = sub * V;
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      const float m = fabsf(v[j]);
+      if (m > m1) {
+        m2 = m1;
+        m1 = m;
+        i1 = sub * V + j;
+      } else if (m > m2) {
+        m2 = m;
+      }
+    }
+    team_top2<L>(m1, i1, m2);
+    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+    if (__any_sync(kFull, flag)) {
+      float t[V];
+#pragma unroll
+      for (int j = 0; j < V; j++) t[j] = v[j];
+      team_swap0<V>(t, flag ? i1 : 0, sub, lane - sub);
+      team_fwht<V, L>(t, p.h, sub);
+      if (flag) {
+#pragma unroll
+        for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], p.c_h);
+      }
+    }
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      mn = fminf(mn, v[j]);
+      mx = fmaxf(mx, v[j]);
+    }
+    mn = team_min<L>(mn);
+    mx = team_max<L>(mx);
+    const float D = __fsub_rn(mx, mn);
+    float scale_lo, inv_lo, scale_hi, inv_hi;
+    scale_inv<L>(D, valid ? lo : 1, sub, scale_lo, inv_lo);
+    scale_inv<L>(D, valid ? hi : 1, sub, scale_hi, inv_hi);
+    if (valid) {
+      quant_store<V>(v, mn, inv_lo, lo, stage_lo + kt * slot_lo + sub * (V * lo / 8));
+      if (!flat) quant_store<V>(v, mn, inv_hi, hi, stage_hi + kt * p.slot_hi + sub * (V * hi / 8));
+      if (sub == 0)
+        put_meta(p, t0 + kt, mn, flag ? (uint8_t)i1 : (uint8_t)0xFF, flat ? scale_lo : D, flat);
+    }
+  }
+}
+
+// Tiles pass over one staged chunk, line layout: each warp takes 32 consecutive lines.
+// kLo / kHi: the two widths when known at compile time (0: from p).
+template <typename Tin, int G, int kLo, int kHi>
+__device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& p, long long g,
+                                           long long t0, int nt, const unsigned char* buf,
+                                           bool flat, unsigned char* stage_lo,
+                                           unsigned char* stage_hi) {
+  using LG = LineGeom<Tin, G>;
+  constexpr int LPT = LG::LPT, NE = LG::NE;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int line = warp * 32 + lane;
+  const int kt = line / LPT, sub = line % LPT;
+  const bool valid = kt < nt;
+  uint32_t w[32];
+  lds_line(buf, line, w);
+
+  // entropy key and histograms (§3.2)
+  if (!flat) {
+    float2 ls = line_sums<Tin>(w, s.tabs, lane);
+    ls = team_sum2<LPT>(ls);
+    int cb = -1;
+    if (valid && sub == 0) {
+      const float H = entropy_key(ls.x, ls.y, s.tabs);
+      p.keys[t0 + kt] = H;
+      if (!(ls.x <= FLT_MAX) || !(fabsf(ls.y) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+        set_status(p.status, kStNonFinite);
+      const int b = fine_bin(H);
+      atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
+      cb = b >> 8;
+    }
+    const unsigned same = __match_any_sync(kFull, cb);
+    if (cb >= 0 && lane == __ffs(same) - 1)
+      atomicAdd(&p.hist_coarse[g * kCoarseBins + cb], (uint32_t)__popc(same));
+  }
+
+  // range and the two-values pretest
+  float mn, mx, ga[NE / 8];
+  line_minmax<Tin>(w, mn, mx, ga);
+  mn = team_min<LPT>(mn);
+  mx = team_max<LPT>(mx);
+  const float m1 = fmaxf(mx, -mn);
+  const float thr = __fmul_rn(m1, 0.5f);  // exact halving for m1 >= 2^-120
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
+  cnt = team_sum_u<LPT>(cnt);
+  const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
+  const bool deferred = tiny || cnt < 2u;
+
+  // widths: Q_lo / D and Q_hi / D (or D / Q_b), split over the team's lanes
+  const int lo = kLo ? kLo : (flat ? p.flat_b : p.lo);
+  const int hi = kHi ? kHi : p.hi;
+  const float D = __fsub_rn(mx, mn);
+  float inv_lo, r1;
+  if constexpr (LPT >= 2) {
+    const bool odd = sub & 1;
+    const float num = odd ? (flat ? D : qmax_f(hi)) : qmax_f(lo);
+    const float den = odd ? (flat ? qmax_f(lo) : D) : D;
+    const float r = __fdiv_rn(num, den);
+    const float o = __shfl_xor_sync(kFull, r, 1);
+    inv_lo = odd ? o : r;
+    r1 = odd ? r : o;
+  } else {
+    inv_lo = __fdiv_rn(qmax_f(lo), D);
+    r1 = flat ? __fdiv_rn(D, qmax_f(lo)) : __fdiv_rn(qmax_f(hi), D);
+  }
+  if (!(D >= 0x1p-120f)) inv_lo = r1 = 0.0f;
+  if (valid && !deferred) {
+    line_quant<Tin, kLo>(w, mn, inv_lo, lo, stage_lo + kt * (G * lo / 8) + sub * (NE * lo / 8));
+    if (!flat)
+      line_quant<Tin, kHi>(w, mn, r1, hi, stage_hi + kt * (G * hi / 8) + sub * (NE * hi / 8));
+    if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, flat ? r1 : D, flat);
+  }
+  // tiles the pretest could not clear: one list for the block, teams of the whole block
+  // take them in turn (outlier channels sit at fixed tile positions, so per-warp lists
+  // would load some warps far more than others)
+  if (valid && deferred && sub == 0) s.dl[atomicAdd(&s.ndef, 1u)] = (uint16_t)kt;
+  __syncthreads();
+  constexpr int TPW = Cfg<Tin, G>::TPW;
+  pass2_teams<Tin, G, true>(p, buf, s.dl, (int)s.ndef, warp * TPW, kWarps * TPW, t0, flat,
+                            stage_lo, stage_hi);
+}
+
+// ====================================================================== tiles: narrow layout
+
+// Tile `l` (0 <= l < NS) of warp `warp`: the tiles a warp handles over all its steps.
+template <typename Tin, int G>
+__device__ __forceinline__ int warp_tile(int l, int warp) {
+  using C = Cfg<Tin, G>;
+  return ((l / C::TPW) * kWarps + warp) * C::TPW + (l % C::TPW);
+}
+
+// Tiles pass over one staged chunk, narrow layout (a team of L lanes per tile, V values
+// per lane; each warp handles its own NS tiles with no block-wide barrier):
+//   stats    per warp step the team's two sums; then one lane per tile forms the key;
+//   phase 1  per warp step the tile's min / max and the two-values test (two lanes whose
+//            own max |v| reaches max / 2); tiles that fail it are deferred;
+//   phase 2  one lane per tile: the two divisions and the tile's metadata;
+//   phase 3  per warp step: quantise and pack the tiles that were not deferred;
+//   pass 2   the deferred tiles, compacted: exact ratio test (eq. (3)), pivot swap and
+//            Hadamard (eq. (4)) where it holds, then the quantizer.
+template <typename Tin, int G>
+__device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams& p, long long g,
+                                             long long t0, int nt, const unsigned char* buf,
+                                             bool flat, unsigned char* stage_lo,
+                                             unsigned char* stage_hi) {
+  using C = Cfg<Tin, G>;
+  constexpr int V = C::V, W = C::W, L = C::L, TPW = C::TPW, NS = C::NS;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L;
+  const int lo = flat ? p.flat_b : p.lo, hi = p.hi;
+  const int slot_lo = G * lo / 8;
+
+  if (!flat) {
+#pragma unroll 1
+    for (int st = 0; st < C::kSteps; st++) {
+      const int kt = (st * kWarps + warp) * TPW + team;
+      const bool valid = kt < nt;
+      uint32_t w[W];
+      if (valid) {
+        lds_words<Tin, G>(buf, kt, sub, w);
+      } else {
+#pragma unroll
+        for (int k = 0; k < W; k++) w[k] = 0u;
+      }
+      const float2 ls = tile_sums<Tin, G>(w, s.tabs, lane);
+      if (valid && sub == 0) {
+        s.ta[kt] = ls.x;
+        s.tb[kt] = ls.y;
+      }
+    }
+    __syncwarp();
+    uint32_t* hf = p.hist_fine + g * (long long)kFineBins;
+    uint32_t* hc = p.hist_coarse + g * kCoarseBins;
+#pragma unroll 1
+    for (int l0 = 0; l0 < NS; l0 += 32) {
+      const int l = l0 + lane;
+      const int kt = warp_tile<Tin, G>(l, warp);
+      const bool valid = l < NS && kt < nt;
+      int cb = -1;
+      if (valid) {
+        const float Ls = s.ta[kt], Ss = s.tb[kt];
+        const float H = entropy_key(Ls, Ss, s.tabs);
+        p.keys[t0 + kt] = H;
+        if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+          set_status(p.status, kStNonFinite);
+        const int b = fine_bin(H);
+        atomicAdd(&hf[b], 1u);
+        cb = b >> 8;
+      }
+      const unsigned same = __match_any_sync(kFull, cb);
+      if (cb >= 0 && lane == __ffs(same) - 1) atomicAdd(&hc[cb], (uint32_t)__popc(same));
+    }
+    __syncwarp();
+  }
+  // phase 1
+#pragma unroll 1
+  for (int st = 0; st < C::kSteps; st++) {
+    const int kt = (st * kWarps + warp) * TPW + team;
+    const bool valid = kt < nt;
+    uint32_t w[W];
+    if (valid) {
+      lds_words<Tin, G>(buf, kt, sub, w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; k++) w[k] = 0u;
+    }
+    float mn, mx;
+    lane_minmax_raw<Tin, G>(w, mn, mx);
+    const float lane_amax = fmaxf(mx, -mn);
+    mn = team_min<L>(mn);
+    mx = team_max<L>(mx);
+    const float m1 = fmaxf(mx, -mn);
+    const float thr = __fmul_rn(m1, 0.5f);
+    bool two;
+    if constexpr (L >= 2) {
+      two = team_two_ge<L>(lane_amax, thr, team);
+    } else {
+      two = lane_count_ge<Tin, G>(w, thr) >= 2u;
+    }
+    const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
+    if (valid && sub == 0) {
+      s.piv[kt] = (tiny || !two) ? kDeferred : (uint8_t)0xFF;
+      s.ta[kt] = mn;
+      s.tb[kt] = mx;
+    }
+  }
+  __syncwarp();
+  // phase 2 (and the list of deferred tiles, kept in this warp's part of s.dl)
+  uint16_t* dl = s.dl + warp * NS;
+  int ndef = 0;
+#pragma unroll 1
+  for (int l0 = 0; l0 < NS; l0 += 32) {
+    const int l = l0 + lane;
+    const int kt = warp_tile<Tin, G>(l, warp);
+    const bool valid = l < NS && kt < nt;
+    const bool def = valid && s.piv[kt] == kDeferred;
+    const unsigned dm = __ballot_sync(kFull, def);
+    if (def) dl[ndef + __popc(dm & ((1u << lane) - 1u))] = (uint16_t)kt;
+    ndef += __popc(dm);
+    if (valid && !def) {
+      const float mn = s.ta[kt], mx = s.tb[kt];
+      const float D = __fsub_rn(mx, mn);
+      const bool degenerate = !(D >= 0x1p-120f);
+      const float inv_lo = degenerate ? 0.0f : __fdiv_rn(qmax_f(lo), D);
+      const float r1 =
+          degenerate ? 0.0f : (flat ? __fdiv_rn(D, qmax_f(lo)) : __fdiv_rn(qmax_f(hi), D));
+      s.tb[kt] = inv_lo;
+      s.tc[kt] = r1;
+      put_meta(p, t0 + kt, mn, (uint8_t)0xFF, flat ? r1 : D, flat);
+    }
+  }
+  __syncwarp();
+  // phase 3
+#pragma unroll 1
+  for (int st = 0; st < C::kSteps; st++) {
+    const int kt = (st * kWarps + warp) * TPW + team;
+    if (kt >= nt || s.piv[kt] == kDeferred) continue;
+    const float mn = s.ta[kt];
+    uint32_t w[W];
+    lds_words<Tin, G>(buf, kt, sub, w);
+    float v[V];
+    words_to_values<Tin, G>(w, v);
+    quant_store<V>(v, mn, s.tb[kt], lo, stage_lo + kt * slot_lo + sub * (V * lo / 8));
+    if (!flat) quant_store<V>(v, mn, s.tc[kt], hi, stage_hi + kt * p.slot_hi + sub * (V * hi / 8));
+  }
+  // pass 2
+  pass2_teams<Tin, G, false>(p, buf, dl, ndef, 0, TPW, t0, flat, stage_lo, stage_hi);
+}
+
+// ====================================================================== stores
+
+// Copy stage[0, nbytes) to dst[base, base + nbytes): 16-byte stores for the aligned
+// middle (realigned from shared memory with funnel shifts), byte stores at the two ends.
+__device__ __forceinline__ void store_stage(const unsigned char* stage, uint8_t* dst,
+                                            long long base, int nbytes) {
+  const int head = (int)((16 - (base & 15)) & 15);
+  const int h = min(head, nbytes);
+  const int n16 = (nbytes - h) / 16;
+  const int tail0 = h + 16 * n16;
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage);
+  const int sh = (h & 3) * 8;
+  for (int i = threadIdx.x; i < n16; i += kThreads) {
+    const int o = h + 16 * i;  // stage byte offset of this global 16-byte word
+    const int q = o >> 2;
+    uint32_t a[5];
+#pragma unroll
+    for (int k = 0; k < 5; k++) a[k] = sw[q + k];
+    uint4 out;
+    out.x = __funnelshift_r(a[0], a[1], sh);
+    out.y = __funnelshift_r(a[1], a[2], sh);
+    out.z = __funnelshift_r(a[2], a[3], sh);
+    out.w = __funnelshift_r(a[3], a[4], sh);
+    *reinterpret_cast<uint4*>(dst + base + o) = out;
+  }
+  const int nb = h + (nbytes - tail0);
+  for (int i = threadIdx.x; i < nb; i += kThreads) {
+    const int o = (i < h) ? i : tail0 + (i - h);
+    dst[base + o] = stage[o];
+  }
+}
+
+// ====================================================================== work items
+
+// Round r (0 <= r < NG + lag) of the work queue:
+//   the first pre1 tiles items of group r  (if r < NG)
+//   the J select items of group r-1        (if 1 <= r <= NG)
+//   the next pre2 tiles items of group r
+//   the J offsets items of group r-1       (if 1 <= r <= NG)
+//   the other tiles items of group r spread evenly among the compaction items of group
+//   r-lag.
+// A group's select items come after all its tiles items, its offsets items after its
+// select items, and its compaction items (round >= r+1) after its offsets items.  The
+// tiles items in front of the select and offsets items give the ones they wait for time
+// to finish.  32-bit arithmetic: the host keeps the item count below 2^31 (and
+// pos * nC below 2^32).
+__device__ __forceinline__ Item decode_item(const EncParams& p, uint32_t q) {
+  // segments of rounds with the same make-up (host-computed, see queue_segments)
+  for (uint32_t i = 0; i < p.seg_n; i++) {
+    const uint32_t* sg = p.seg[i];
+    if (q >= sg[7]) continue;
+    const uint32_t len = sg[5], nB = sg[2], nAr = sg[3], nCr = sg[4];
+    const uint32_t r = sg[0] + (q - sg[6]) / len;
+    uint32_t pos = (q - sg[6]) % len;
+    const uint32_t pre1 = min((uint32_t)p.pre1, nAr);
+    const uint32_t pre2 = min((uint32_t)p.pre2, nAr - pre1);
+    if (pos < pre1) return Item{kItemTiles, (long long)r, (long long)pos};
+    pos -= pre1;
+    if (pos < nB) return Item{kItemSelect, (long long)r - 1, (long long)pos};
+    pos -= nB;
+    if (pos < pre2) return Item{kItemTiles, (long long)r, (long long)(pre1 + pos)};
+    pos -= pre2;
+    if (pos < nB) return Item{kItemOffsets, (long long)r - 1, (long long)pos};
+    pos -= nB;
+    // the remaining na tiles items and nCr compaction items, compaction evenly spread:
+    // position pos holds a compaction item iff floor((pos+1) nCr / n) > floor(pos nCr / n)
+    const uint32_t na = nAr - pre1 - pre2, n = na + nCr;
+    const uint32_t before = pos * nCr / n, upto = (pos + 1u) * nCr / n;
+    if (upto > before) return Item{kItemCompact, (long long)(r - (uint32_t)p.lag), (long long)before};
+    return Item{kItemTiles, (long long)r, (long long)(pre1 + pre2 + pos - before)};
+  }
+  return Item{-1, 0, 0};
+}
+
+// Rounds r in [r0, r1) have the same items: the breakpoints 0, 1, lag, NG, NG + 1,
+// NG + lag cut the rounds into at most 5 such segments.  seg[i] = {r0, r1, nB, nA, nC,
+// len, first item, end item}.
+static void queue_segments(EncParams& p) {
+  const long long NG = p.n_groups, lag = p.lag;
+  long long bp[6] = {0, 1, lag, NG, NG + 1, NG + lag};
+  std::sort(bp, bp + 6);
+  const long long rmax = NG + lag;
+  long long cum = 0;
+  p.seg_n = 0;
+  for (int k = 0; k < 5; k++) {
+    const long long r0 = bp[k], r1 = std::min(bp[k + 1], rmax);
+    if (r1 <= r0) continue;
+    const bool hasB = r0 >= 1 && r0 <= NG, hasA = r0 < NG, hasC = r0 >= lag && r0 < NG + lag;
+    const long long nB = hasB ? p.J : 0, nA = hasA ? p.nA : 0, nC = hasC ? p.nC : 0;
+    const long long len = 2 * nB + nA + nC;
+    if (len == 0) continue;
+    const long long span = (r1 - r0) * len;
+    uint32_t* sg = p.seg[p.seg_n++];
+    sg[0] = (uint32_t)r0;
+    sg[1] = (uint32_t)r1;
+    sg[2] = (uint32_t)nB;
+    sg[3] = (uint32_t)nA;
+    sg[4] = (uint32_t)nC;
+    sg[5] = (uint32_t)len;
+    sg[6] = (uint32_t)cum;
+    sg[7] = (uint32_t)(cum + span);
+    cum += span;
+  }
+}
+
+template <typename Tin, int G>
+__device__ __forceinline__ void tiles_range(const EncParams& p, const Item& it, long long& t0,
+                                            int& nt) {
+  constexpr int CH = Cfg<Tin, G>::CH;
+  t0 = it.g * p.n_g + it.idx * CH;
+  nt = (int)min((long long)CH, p.n_g - it.idx * CH);
+}
+
+// ---- tiles item: the whole per-tile computation of one input chunk, both widths into
+// the scratch streams.
+template <typename Tin, int G, int kLo, int kHi>
+__device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
+                         const unsigned char* buf, unsigned char* stage_lo,
+                         unsigned char* stage_hi) {
+  long long t0;
+  int nt;
+  tiles_range<Tin, G>(p, it, t0, nt);
+  if constexpr (Cfg<Tin, G>::kLine) {
+    tiles_line<Tin, G, kLo, kHi>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
+  } else {
+    tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) s.ndef = 0u;
+  store_stage(stage_lo, p.scratch_lo, t0 * p.slot_lo, nt * p.slot_lo);
+  store_stage(stage_hi, p.scratch_hi, t0 * p.slot_hi, nt * p.slot_hi);
+  // the block's writes, ordered by the barrier, are published by one gpu-scope fence
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&p.doneA[it.g], 1u);
+  }
+}
+
+// ---- select item: gather the candidates of the threshold bucket; the last select item
+// of the group resolves the K-th ranked tile exactly.
+template <typename Tin, int G>
+__device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
+                          unsigned char* scratch) {
+  const long long g = it.g;
+  const uint32_t K = (uint32_t)p.K;
+  if (threadIdx.x == 0) wait_counter(&p.doneA[g], (uint32_t)p.nA, p.status);
+  __syncthreads();
+  uint32_t* bins = s.hist;  // all zero between items; left zero below
+  if (threadIdx.x < 32) {
+    for (int i = threadIdx.x; i < 256; i += 32) bins[i] = __ldcg(&p.hist_coarse[g * kCoarseBins + i]);
+    __syncwarp();
+    int cb;
+    uint32_t above_c;
+    warp_find_from_top(bins, K, cb, above_c);
+    __syncwarp();
+    for (int i = threadIdx.x; i < 256; i += 32)
+      bins[i] = __ldcg(&p.hist_fine[g * (long long)kFineBins + cb * 256 + i]);
+    __syncwarp();
+    int fb;
+    uint32_t above_f;
+    warp_find_from_top(bins, K - above_c, fb, above_f);
+    if (threadIdx.x == 0) {
+      s.scan[0] = (uint32_t)(cb * 256 + fb);
+      s.scan[1] = above_c + above_f;
+    }
+  }
+  __syncthreads();
+  const int bstar = (int)s.scan[0];
+  const uint32_t above = s.scan[1];
+  // candidates of this item's slice of the group
+  const long long per = (p.n_g + p.J - 1) / p.J;
+  const long long lo = it.idx * per, hi = min(p.n_g, lo + per);
+  const float* kg = p.keys + g * p.n_g;
+  unsigned long long* cg = p.cand + g * p.n_g;
+  const int lane = threadIdx.x & 31;
+  for (long long base = lo; base < hi; base += kThreads) {
+    const long long i = base + threadIdx.x;
+    float hv = 0.0f;
+    bool hit = false;
+    if (i < hi) {
+      hv = __ldcg(&kg[i]);
+      hit = fine_bin(hv) == bstar;
+    }
+    const unsigned mask = __ballot_sync(kFull, hit);
+    if (mask) {
+      uint32_t pos0 = 0;
+      const int leader = __ffs(mask) - 1;
+      if (lane == leader) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)__popc(mask));
+      pos0 = __shfl_sync(kFull, pos0, leader);
+      if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv, (uint32_t)i);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.doneB[g], 1u);
+    __threadfence();
+    s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s.last) {
+    const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
+    const uint32_t expect = __ldcg(&p.hist_fine[g * (long long)kFineBins + bstar]);
+    if (threadIdx.x == 0 && cnt != expect) set_status(p.status, kStSelectMismatch);
+    const uint32_t r = max(1u, min(K - above, cnt));  // rank (from 1) inside the bucket
+    unsigned long long theta = 0ull;
+    if (cnt > 0u && cnt <= (uint32_t)kRankMax) {
+      // one pass: the candidate with exactly r - 1 larger keys (rank keys are distinct)
+      unsigned long long* ck = reinterpret_cast<unsigned long long*>(scratch);
+      for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) ck[i] = __ldcg(&cg[i]);
+      if (threadIdx.x == 0) s.scan[2] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+        const unsigned long long ki = ck[i];
+        uint32_t larger = 0;
+        for (uint32_t j = 0; j < cnt; j++) larger += ck[j] > ki ? 1u : 0u;
+        if (larger == r - 1u) s.scan[2] = i;
+      }
+      __syncthreads();
+      theta = ck[s.scan[2]];
+      __syncthreads();
+    } else if (cnt > 0u) {
+      // radix select (8 passes of 8 bits) of the r-th largest candidate key
+      uint32_t rr = r;
+      unsigned long long prefix = 0ull, mask = 0ull;
+      for (int pass = 7; pass >= 0; --pass) {
+        const int shift = pass * 8;
+        for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+          const unsigned long long v = __ldcg(&cg[i]);
+          if ((v & mask) == prefix) atomicAdd(&bins[(v >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+          int d;
+          uint32_t ab;
+          warp_find_from_top(bins, rr, d, ab);
+          if (threadIdx.x == 0) {
+            s.scan[2] = (uint32_t)d;
+            s.scan[3] = ab;
+          }
+        }
+        __syncthreads();
+        prefix |= (unsigned long long)s.scan[2] << shift;
+        rr -= s.scan[3];
+        mask |= 0xFFull << shift;
+        __syncthreads();
+      }
+      theta = prefix;
+    }
+    if (threadIdx.x == 0) {
+      p.sel[g] = SelResult{theta, cnt ? kSelThreshold : kSelNone, 0u};
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.selready[g]), "r"(1u) : "memory");
+    }
+  }
+  for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
+  __syncthreads();
+}
+
+// ---- offsets item: the width and the scale of every tile of its compaction chunks and
+// their hi counts; the last offsets item of the group turns the counts into exclusive
+// prefixes.
+template <typename Tin, int G>
+__device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
+  const long long g = it.g;
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status);
+  __syncthreads();
+  const unsigned long long theta = __ldcg(&p.sel[g].theta);
+  const uint32_t mode = __ldcg(&p.sel[g].mode);
+  unsigned long long* words = p.lookback + g * p.nC;
+  const long long per = (p.nC + p.J - 1) / p.J;
+  const long long c0 = it.idx * per, c1 = min(p.nC, c0 + per);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long long c = c0 + warp; c < c1; c += kWarps) {
+    const long long tl0 = c * p.CHC;
+    const int nt = (int)min(p.CHC, p.n_g - tl0);
+    const long long t0 = g * p.n_g + tl0;
+    uint32_t cnt = 0;
+    for (int k = lane; k < nt; k += 32) {
+      bool ishi = mode == kSelAll;
+      if (mode == kSelThreshold)
+        ishi = rank_key(__ldcg(&p.keys[t0 + k]), (uint32_t)(tl0 + k)) >= theta;
+      const int b = ishi ? p.hi : p.lo;
+      p.bits[t0 + k] = (uint8_t)b;
+      // the range D left by the tiles pass becomes the scale D / Q
+      const float D = __ldcg(&p.scales[t0 + k]);
+      p.scales[t0 + k] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
+      cnt += ishi ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+    if (lane == 0) words[c] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.doneB2[g], 1u);
+    __threadfence();
+    s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s.last) {
+    // exclusive prefix of the nC counts: each thread sums a contiguous run, one block scan
+    const long long run = (p.nC + kThreads - 1) / kThreads;
+    const long long r0 = min(p.nC, (long long)threadIdx.x * run), r1 = min(p.nC, r0 + run);
+    unsigned long long mine = 0;
+    for (long long c = r0; c < r1; c++) mine += __ldcg(&words[c]);
+    uint32_t tot;
+    unsigned long long acc = block_exclusive_scan<kThreads>((uint32_t)mine, tot, s.scan);
+    for (long long c = r0; c < r1; c++) {
+      const unsigned long long v = __ldcg(&words[c]);
+      words[c] = acc;
+      acc += v;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.selready[g]), "r"(2u) : "memory");
+    }
+  }
+}
+
+// Copy every tile's slot of its width from scratch into the stage, in units of Unit.
+template <typename Unit>
+__device__ __forceinline__ void gather_units(const uint16_t* off, const uint8_t* cbits,
+                                             const EncParams& p, long long t0, int nt,
+                                             unsigned char* stage) {
+  constexpr int U = (int)sizeof(Unit);
+  const int uph = p.slot_hi / U, upl = p.slot_lo / U;
+  const int total = nt * uph;
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    const int k = i / uph, u = i - k * uph;
+    const bool ishi = cbits[k] == (uint8_t)p.hi;
+    if (!ishi && u >= upl) continue;
+    const Unit* src = ishi ? reinterpret_cast<const Unit*>(p.scratch_hi + (t0 + k) * p.slot_hi)
+                           : reinterpret_cast<const Unit*>(p.scratch_lo + (t0 + k) * p.slot_lo);
+    *reinterpret_cast<Unit*>(stage + off[k] + u * U) = __ldcg(src + u);
+  }
+}
+
+// Drop the whole 128-byte lines of [a, b) from L2 without writing them back.
+__device__ __forceinline__ void discard_lines(const uint8_t* base, long long a, long long b) {
+  const long long first = (a + 127) / 128, last = b / 128;
+  for (long long l = first + threadIdx.x; l < last; l += kThreads)
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(base + l * 128) : "memory");
+}
+
+// ---- compaction item: widths from the offsets items, slots from scratch, the chunk's
+// place in the stream from the prefix of hi counts.  `stage` holds
+// the chunk's bytes, `off` / `cbits` (CHC entries each) every tile's place and width.
+template <typename Tin, int G>
+__device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
+                           unsigned char* stage, uint16_t* off, uint8_t* cbits) {
+  const long long g = it.g, cc = it.idx;
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status);
+  __syncthreads();
+  const long long tl0 = cc * p.CHC;
+  const int nt = (int)min(p.CHC, p.n_g - tl0);
+  const long long t0 = g * p.n_g + tl0;
+  const unsigned long long prefix = __ldcg(&p.lookback[g * p.nC + cc]);
+  const int slot_lo = p.slot_lo, slot_d = p.slot_hi - p.slot_lo;
+  constexpr int kPer = kMaxCC / kThreads;
+  uint32_t hiflags = 0u, cnt = 0u;
+  uint8_t bl[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; j++) {
+    const int k = threadIdx.x * kPer + j;
+    bl[j] = 0;
+    if (k < nt) {
+      bl[j] = __ldcg(&p.bits[t0 + k]);
+      if (bl[j] == (uint8_t)p.hi) {
+        hiflags |= 1u << j;
+        ++cnt;
+      }
+    }
+  }
+  uint32_t chunk_hi;
+  uint32_t before = block_exclusive_scan<kThreads>(cnt, chunk_hi, s.scan);
+#pragma unroll
+  for (int j = 0; j < kPer; j++) {
+    const int k = threadIdx.x * kPer + j;
+    if (k < nt) {
+      cbits[k] = bl[j];
+      off[k] = (uint16_t)(k * slot_lo + before * slot_d);
+      before += (hiflags >> j) & 1u;
+    }
+  }
+  __syncthreads();
+  const int u = __ffs(p.slot_lo | p.slot_hi | 16) - 1;  // log2 of the largest common unit
+  if (u >= 4) {
+    gather_units<uint4>(off, cbits, p, t0, nt, stage);
+  } else if (u == 3) {
+    gather_units<unsigned long long>(off, cbits, p, t0, nt, stage);
+  } else if (u == 2) {
+    gather_units<unsigned int>(off, cbits, p, t0, nt, stage);
+  } else if (u == 1) {
+    gather_units<unsigned short>(off, cbits, p, t0, nt, stage);
+  } else {
+    gather_units<unsigned char>(off, cbits, p, t0, nt, stage);
+  }
+  __syncthreads();
+  const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
+  int nbytes = nt * slot_lo + (int)chunk_hi * slot_d;
+  if (base + nbytes > p.codes_bytes) {  // only if the select went wrong: never write past
+    if (threadIdx.x == 0) set_status(p.status, kStSelectMismatch);
+    nbytes = (int)max(0ll, p.codes_bytes - base);
+  }
+  store_stage(stage, p.codes, base, nbytes);
+  discard_lines(p.scratch_lo, t0 * slot_lo, (t0 + nt) * slot_lo);
+  discard_lines(p.scratch_hi, t0 * p.slot_hi, (t0 + nt) * p.slot_hi);
+}
+
+// ====================================================================== kernels
+
+template <typename Tin, int G>
+__device__ __forceinline__ void issue_chunk(EncSmem<Tin, G>& s, const EncParams& p, long long t0,
+                                            int nt, int slot, unsigned long long pol) {
+  if constexpr (Cfg<Tin, G>::kLine) {
+    // the whole box (256 rows); rows past the tensor are zero-filled and still counted
+    mbar_expect_tx(&s.bar[slot], (uint32_t)kChunkBytes);
+    const int row = (int)(t0 * G * (long long)sizeof(Tin) / 128);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(s.buf[slot])),
+        "l"(reinterpret_cast<unsigned long long>(&p.tmap)), "r"(0), "r"(row),
+        "r"(smem_u32(&s.bar[slot])), "l"(pol)
+        : "memory");
+  } else {
+    const uint32_t bytes = (uint32_t)nt * G * (uint32_t)sizeof(Tin);
+    mbar_expect_tx(&s.bar[slot], bytes);
+    bulk_load(s.buf[slot], static_cast<const Tin*>(p.x) + t0 * G, bytes, &s.bar[slot], pol);
+  }
+}
+
+template <typename Tin, int G>
+__device__ __forceinline__ EncSmem<Tin, G>& enc_smem(unsigned char* raw) {
+  const uint32_t a = smem_u32(raw);
+  return *reinterpret_cast<EncSmem<Tin, G>*>(raw + ((1024u - (a & 1023u)) & 1023u));
+}
+
+template <typename Tin, int G, int kLo, int kHi>
+__global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ EncParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
+  unsigned char* stage_lo = reinterpret_cast<unsigned char*>(&s) + sizeof(EncSmem<Tin, G>);
+  unsigned char* stage_hi = stage_lo + p.stage_lo_bytes;
+  init_tables<Tin, G>(s, p.tabs);
+  for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) s.hist[i] = 0u;
+  uint32_t ahead = 0u;  // thread 0: the ticket after the next one, dequeued early
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+    s.ndef = 0u;
+    s.next = (long long)atomicAdd(p.ticket, 1u);
+    ahead = atomicAdd(p.ticket, 1u);
+  }
+  __syncthreads();
+  const unsigned long long pol = policy_evict_first();  // the input is read once
+  uint32_t parity = 0u;  // bit s = phase parity of buffer s
+
+  // Thread 0 starts the copy of a tiles item's input chunk into buffer `slot`.
+  auto issue = [&](const Item& it, int slot) {
+    if (it.type != kItemTiles) return;
+    long long t0;
+    int nt;
+    tiles_range<Tin, G>(p, it, t0, nt);
+    issue_chunk<Tin, G>(s, p, t0, nt, slot, pol);
+  };
+
+  // Thread 0 decodes each item once (s.item[slot]) when it dequeues it.
+  long long cur = s.next;
+  int slot = 0;
+  if (threadIdx.x == 0 && cur < p.n_items) {
+    s.item[0] = decode_item(p, (uint32_t)cur);
+    issue(s.item[0], 0);
+  }
+  while (cur < p.n_items) {
+    __syncthreads();  // everyone is done with the previous item and its buffer
+    if (threadIdx.x == 0) {
+      // a block holds up to three tickets (the item it works on, the next one, one more)
+      // and works through them in order; items only wait for smaller tickets, so the
+      // smallest item in work never waits for an item that has not started
+      const long long nxt = (long long)ahead;
+      s.next = nxt;
+      if (nxt < p.n_items) {
+        s.item[slot ^ 1] = decode_item(p, (uint32_t)nxt);
+        issue(s.item[slot ^ 1], slot ^ 1);
+        ahead = atomicAdd(p.ticket, 1u);
+      }
+    }
+    const Item it = s.item[slot];
+    if (it.type == kItemTiles) {
+      mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+      parity ^= 1u << slot;
+      do_tiles<Tin, G, kLo, kHi>(s, p, it, s.buf[slot], stage_lo, stage_hi);
+    } else if (it.type == kItemCompact) {
+      // the tiles stages are free during a compaction: they hold its per-tile arrays
+      do_compact<Tin, G>(s, p, it, s.buf[slot], reinterpret_cast<uint16_t*>(stage_lo),
+                         stage_lo + 2 * kMaxCC);
+    } else if (it.type == kItemSelect) {
+      do_select<Tin, G>(s, p, it, s.buf[slot]);
+    } else if (it.type == kItemOffsets) {
+      do_offsets<Tin, G>(s, p, it);
+    }
+    __syncthreads();
+    cur = s.next;
+    slot ^= 1;
+  }
+}
+
+// Every tile gets the same width b (K = 0 or K = n_g): slot offsets are t * G * b / 8.
+template <typename Tin, int G, int kB>
+__global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_constant__ EncParams p,
+                                                             long long n_chunks) {
+  using C = Cfg<Tin, G>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
+  unsigned char* stage = reinterpret_cast<unsigned char*>(&s) + sizeof(EncSmem<Tin, G>);
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+    s.ndef = 0u;
+  }
+  __syncthreads();
+  const unsigned long long pol = policy_evict_first();
+  uint32_t parity = 0u;
+  const int slot_b = G * p.flat_b / 8;
+  long long c = blockIdx.x;
+  int slot = 0;
+  if (threadIdx.x == 0 && c < n_chunks)
+    issue_chunk<Tin, G>(s, p, c * C::CH, (int)min((long long)C::CH, p.n_tiles - c * C::CH), 0, pol);
+  for (; c < n_chunks; c += gridDim.x) {
+    const long long nx = c + gridDim.x;
+    if (threadIdx.x == 0 && nx < n_chunks)
+      issue_chunk<Tin, G>(s, p, nx * C::CH, (int)min((long long)C::CH, p.n_tiles - nx * C::CH),
+                          slot ^ 1, pol);
+    const long long t0 = c * C::CH;
+    const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    parity ^= 1u << slot;
+    __syncthreads();
+    if constexpr (C::kLine) {
+      tiles_line<Tin, G, kB, 0>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
+    } else {
+      tiles_narrow<Tin, G>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s.ndef = 0u;
+    store_stage(stage, p.codes, t0 * slot_b, nt * slot_b);
+    __syncthreads();
+    slot ^= 1;
+  }
+}
+
+// ====================================================================== launchers
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The input viewed as [rows][128 bytes], boxes of 256 rows (one 32 KB chunk), 128-byte
+// swizzle.
+static cudaError_t make_line_map(TmaDesc* d, const void* x, bool bf16, long long n_tiles, int G) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const int esize = bf16 ? 2 : 4;
+  const long long rows = n_tiles * G * esize / 128;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)(128 / esize), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), 256u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        2, const_cast<void*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "descriptor size");
+  std::memcpy(d->bytes, &m, sizeof m);
+  return cudaSuccess;
+}
+
+template <typename Tin, int G>
+static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
+  using C = Cfg<Tin, G>;
+  EncParams p{};
+  p.x = a.x;
+  p.n_tiles = a.n_tiles;
+  p.n_g = a.n_g;
+  p.n_groups = a.n_groups;
+  p.K = a.K;
+  p.group_bytes = a.group_bytes;
+  p.codes_bytes = a.n_groups * a.group_bytes;
+  p.lo = a.lo;
+  p.hi = a.hi;
+  p.h = a.h;
+  p.c_h = a.c_h;
+  p.slot_lo = G * a.lo / 8;
+  p.slot_hi = G * a.hi / 8;
+  p.codes = a.codes;
+  p.scales = a.scales;
+  p.zeros = a.zeros;
+  p.bits = a.bits;
+  p.pivots = a.pivots;
+  p.scratch_lo = a.scratch_lo;
+  p.scratch_hi = a.scratch_hi;
+  p.keys = a.keys;
+  p.cand = a.cand;
+  p.cand_cnt = a.cand_cnt;
+  p.hist_coarse = a.hist_coarse;
+  p.hist_fine = a.hist_fine;
+  p.doneA = a.doneA;
+  p.doneB = a.doneB;
+  p.doneB2 = a.doneB2;
+  p.selready = a.selready;
+  p.sel = a.sel;
+  p.lookback = a.lookback;
+  p.ticket = a.ticket;
+  p.status = a.status;
+  p.tabs = *a.tabs;
+  if constexpr (C::kLine) {
+    const cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid_cap = a.num_sms * 2;
+  const bool flat = a.K == 0 || a.K == a.n_g;
+  p.flat_b = a.K == 0 ? a.lo : a.hi;
+  const int b_first = flat ? p.flat_b : a.lo;
+  p.stage_lo_bytes = (uint32_t)((C::CH * G * b_first / 8 + 64 + 127) / 128 * 128);
+  const uint32_t stage_hi_bytes = flat ? 0u : (uint32_t)(C::CH * G * a.hi / 8 + 64);
+  // the stages also hold a compaction chunk's per-tile arrays (3 bytes per tile)
+  const size_t stages = std::max<size_t>(p.stage_lo_bytes + stage_hi_bytes, flat ? 0 : 3 * kMaxCC);
+  const size_t smem = sizeof(EncSmem<Tin, G>) + 1024 + stages;
+  if (flat) {
+    void (*kern)(EncParams, long long) = k_encode_flat<Tin, G, 0>;
+    if constexpr (C::kLine) {  // the common widths, compiled with the width known
+      if (p.flat_b == 3) kern = k_encode_flat<Tin, G, 3>;
+      if (p.flat_b == 4) kern = k_encode_flat<Tin, G, 4>;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long n_chunks = (a.n_tiles + C::CH - 1) / C::CH;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, n_chunks));
+    kern<<<grid, kThreads, smem, st>>>(p, n_chunks);
+    return cudaGetLastError();
+  }
+  p.nA = (a.n_g + C::CH - 1) / C::CH;
+  p.CHC = encode_cchunk_tiles(C::kBf16, G, a.hi);
+  p.nC = (a.n_g + p.CHC - 1) / p.CHC;
+  // keep the scratch of three (or, for big groups, two) groups in L2 between a group's
+  // tiles pass and its compaction
+  const long long group_scratch = a.n_g * (long long)(p.slot_lo + p.slot_hi);
+  p.lag = (3 * group_scratch <= (64ll << 20)) ? 2 : 1;
+  // one tiles item per block before the select items (the group's last tiles items
+  // finish meanwhile), an eighth of the group before the offsets items
+  p.pre1 = std::min<long long>(p.nA, grid_cap);
+  p.pre2 = std::min<long long>(p.nA - p.pre1, p.nA / 8);
+  p.J = std::max<long long>(1, std::min<long long>(256, p.nA / 8));
+  p.n_items = a.n_groups * (p.nA + 2 * p.J + p.nC);
+  if (p.n_items >= (1ll << 31) || (p.nA + 2 * p.J + p.nC) * p.nC >= (1ll << 32))
+    return cudaErrorInvalidValue;
+  queue_segments(p);
+  void (*kern)(EncParams) = k_encode<Tin, G, 0, 0>;
+  if constexpr (C::kLine) {
+    if (a.lo == 3 && a.hi == 4) kern = k_encode<Tin, G, 3, 4>;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, p.n_items));
+  kern<<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tahq

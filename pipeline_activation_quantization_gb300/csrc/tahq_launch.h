@@ -60,6 +60,10 @@ struct DecodeArgs {
   unsigned long long* bsum;      // [decode_blocks] stream offset of each block of 8 chunks
 };
 
+// Encode geometry: bytes of input per tiles item; tiles per compaction chunk, at most.
+constexpr int kEncChunkBytes = 32768;
+constexpr int kEncMaxCC = 2048;
+
 // Tiles per compaction chunk of the encode kernel, and the number of compaction chunks
 // (one offset word each) for these shapes.
 long long encode_cchunk_tiles(int bf16, int G, int hi);
@@ -72,6 +76,8 @@ inline long long decode_blocks(int G, long long n_tiles) {
 }
 
 cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t st);
+cudaError_t launch_encode_f32(const EncodeArgs& a, cudaStream_t st);
+cudaError_t launch_encode_bf16(const EncodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace tahq

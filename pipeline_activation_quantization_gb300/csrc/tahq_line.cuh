@@ -59,29 +59,27 @@ __device__ __forceinline__ void lds_line(const unsigned char* buf, int line, uin
 
 // ------------------------------------------------------------------ entropy sums
 
-// lg of a pair of normal (or zero) magnitudes given as bits, with the (T, R) table
-// replicated per bank (entry i of lane l at float2 index i * 32 + l).  A zero magnitude
-// gives lg = -127 (its term m lg m is then a zero).
-__device__ __forceinline__ float2 lg_pair_f32(uint32_t a, uint32_t b, const char* trb,
-                                              uint32_t lane8, const LgTables& tb) {
-  const float2 ta = *reinterpret_cast<const float2*>(trb + (((a >> 8) & 0x7F00u) | lane8));
-  const float2 tbv = *reinterpret_cast<const float2*>(trb + (((b >> 8) & 0x7F00u) | lane8));
+// lg of a pair of normal (or zero) magnitudes given as bits (tables g_lgT / g_lgR).  A
+// zero magnitude gives lg = -127 (its term m lg m is then a zero).
+__device__ __forceinline__ float2 lg_pair_f32(uint32_t a, uint32_t b, uint32_t lane4,
+                                              const LgTables& tb) {
+  const uint32_t oa = ((a >> 9) & 0x3F80u) | lane4, ob = ((b >> 9) & 0x3F80u) | lane4;
   const float2 F = make_float2(__uint_as_float((a >> 23) | 0x4B000000u),
                                __uint_as_float((b >> 23) | 0x4B000000u));
   const float2 mm = make_float2(__uint_as_float((a & 0x007FFFFFu) | 0x3F800000u),
                                 __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u));
-  const float2 r = fma2(mm, make_float2(ta.y, tbv.y), make_float2(-1.0f, -1.0f));
+  const float2 r = fma2(mm, make_float2(lg_tab(g_lgR, oa), lg_tab(g_lgR, ob)),
+                        make_float2(-1.0f, -1.0f));
   float2 p = fma2(make_float2(tb.k[2], tb.k[2]), r, make_float2(tb.k[1], tb.k[1]));
   p = fma2(p, r, make_float2(tb.k[0], tb.k[0]));
-  const float2 t = fma2(p, r, make_float2(ta.x, tbv.x));
+  const float2 t = fma2(p, r, make_float2(lg_tab(g_lgT, oa), lg_tab(g_lgT, ob)));
   const float2 ef = add2(F, make_float2(-8388735.0f, -8388735.0f));  // exponent - 127, exact
   return add2(ef, t);
 }
 
 // {L, S} of one fp32 line: L = pairwise sum of m_k, S = pairwise sum of the fused pairs
 // fmaf(m_2j+1, lg m_2j+1, RN(m_2j lg m_2j)); both in natural order over the 32 values.
-__device__ __forceinline__ float2 line_sums_f32(const uint32_t* w, const float2* TRrep,
-                                                const LgTables& tb, int lane) {
+__device__ __forceinline__ float2 line_sums_f32(const uint32_t* w, const LgTables& tb, int lane) {
   uint32_t mb[32];
 #pragma unroll
   for (int k = 0; k < 32; k++) mb[k] = w[k] & 0x7FFFFFFFu;
@@ -92,12 +90,11 @@ __device__ __forceinline__ float2 line_sums_f32(const uint32_t* w, const float2*
   mn = min(mn, mb[31]);
   float2 m2[16], l2[16];
   if (mn >= 0x00800000u) {
-    const char* trb = reinterpret_cast<const char*>(TRrep);
-    const uint32_t lane8 = (uint32_t)lane << 3;
+    const uint32_t lane4 = (uint32_t)lane << 2;
 #pragma unroll
     for (int k = 0; k < 16; k++) {
       m2[k] = make_float2(__uint_as_float(mb[k]), __uint_as_float(mb[k + 16]));
-      l2[k] = lg_pair_f32(mb[k], mb[k + 16], trb, lane8, tb);
+      l2[k] = lg_pair_f32(mb[k], mb[k + 16], lane4, tb);
     }
   } else {
 #pragma unroll
@@ -120,15 +117,13 @@ __device__ __forceinline__ float2 line_sums_f32(const uint32_t* w, const float2*
 
 // {L, S} of one bf16 line (64 values; word k holds values 2k (low half) and 2k + 1).
 // The lg of a bf16 magnitude is exact from the table: e + TB[top 7 fraction bits].
-__device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const float* TBrep,
-                                                 const LgTables& tb, int lane) {
+__device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const LgTables& tb, int lane) {
   // any half with exponent field 0 (zero or subnormal)?  those take the general lg
   uint32_t em = 0xFFFFFFFFu;
 #pragma unroll
   for (int k = 0; k < 32; k++) em = __vminu2(em, w[k] & 0x7F807F80u);
   float2 L1[16], S1[16];
   if ((em & 0xFFFFu) != 0u && (em >> 16) != 0u) {
-    const char* tbl = reinterpret_cast<const char*>(TBrep);
     const uint32_t lane4 = (uint32_t)lane << 2;
 #pragma unroll
     for (int k = 0; k < 16; k++) {
@@ -141,12 +136,10 @@ __device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const float*
                                      __uint_as_float(((b >> 7) & 0xFFu) | 0x4B000000u));
       const float2 ehi = make_float2(__uint_as_float(((a >> 23) & 0xFFu) | 0x4B000000u),
                                      __uint_as_float(((b >> 23) & 0xFFu) | 0x4B000000u));
-      const float2 tlo =
-          make_float2(*reinterpret_cast<const float*>(tbl + (((a << 7) & 0x3F80u) | lane4)),
-                      *reinterpret_cast<const float*>(tbl + (((b << 7) & 0x3F80u) | lane4)));
-      const float2 thi =
-          make_float2(*reinterpret_cast<const float*>(tbl + (((a >> 9) & 0x3F80u) | lane4)),
-                      *reinterpret_cast<const float*>(tbl + (((b >> 9) & 0x3F80u) | lane4)));
+      const float2 tlo = make_float2(lg_tab(g_lgTB, ((a << 7) & 0x3F80u) | lane4),
+                                     lg_tab(g_lgTB, ((b << 7) & 0x3F80u) | lane4));
+      const float2 thi = make_float2(lg_tab(g_lgTB, ((a >> 9) & 0x3F80u) | lane4),
+                                     lg_tab(g_lgTB, ((b >> 9) & 0x3F80u) | lane4));
       const float2 c127 = make_float2(-8388735.0f, -8388735.0f);
       const float2 llo = add2(add2(elo, c127), tlo);
       const float2 lhi = add2(add2(ehi, c127), thi);
@@ -176,12 +169,11 @@ __device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const float*
 }
 
 template <typename Tin>
-__device__ __forceinline__ float2 line_sums(const uint32_t* w, const void* rep, const LgTables& tb,
-                                            int lane) {
+__device__ __forceinline__ float2 line_sums(const uint32_t* w, const LgTables& tb, int lane) {
   if constexpr (InTraits<Tin>::kBf16) {
-    return line_sums_bf16(w, static_cast<const float*>(rep), tb, lane);
+    return line_sums_bf16(w, tb, lane);
   } else {
-    return line_sums_f32(w, static_cast<const float2*>(rep), tb, lane);
+    return line_sums_f32(w, tb, lane);
   }
 }
 
@@ -303,6 +295,98 @@ __device__ __forceinline__ void line_quant_store(const uint32_t* w, float mn, fl
     const unsigned long long f2 = pack8(q + 16, b), f3 = pack8(q + 24, b);
     sts_two(dst, f0, f1, b);
     sts_two(dst + 2 * b, f2, f3, b);
+  }
+}
+
+// ---- the same with the width known at compile time (no width branches; adjacent value
+// pairs as loaded; the lane's bytes stored as whole 32-bit words)
+
+template <int B>
+__device__ __forceinline__ unsigned long long pack8_ct(const uint32_t* q) {
+  if constexpr (B <= 4) {
+    uint32_t acc = q[0];
+    uint32_t spw = 1u;
+#pragma unroll
+    for (int j = 1; j < 8; j++) {
+      acc += q[j] << (j * B);
+      spw += 1u << (j * B);
+    }
+    return (unsigned long long)(acc - 0x4B400000u * spw);
+  } else {
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; j++) acc |= (unsigned long long)(q[j] & 0xFFu) << (j * B);
+    return acc;
+  }
+}
+
+__host__ __device__ constexpr int lowbit_cap16(int n) { return (n & -n) < 16 ? (n & -n) : 16; }
+
+// NF fields of 8 codes (8B bits each), concatenated, stored as NF * B / 4 words at dst
+// (aligned to AL bytes).
+template <int B, int NF, int AL>
+__device__ __forceinline__ void store_fields(unsigned char* dst, const unsigned long long* f) {
+  constexpr int NW = NF * B / 4, FB = 8 * B;
+  static_assert(NF * B % 4 == 0, "whole words");
+  uint32_t word[NW];
+#pragma unroll
+  for (int k = 0; k < NW; k++) {
+    const int bit = 32 * k, fi = bit / FB, off = bit % FB;
+    unsigned long long v = f[fi] >> off;
+    if (off + 32 > FB && fi + 1 < NF) v |= f[fi + 1] << (FB - off);
+    word[k] = (uint32_t)v;
+  }
+  if constexpr (AL >= 16 && NW % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < NW; k += 4)
+      *reinterpret_cast<uint4*>(dst + 4 * k) = make_uint4(word[k], word[k + 1], word[k + 2], word[k + 3]);
+  } else if constexpr (AL >= 8 && NW % 2 == 0) {
+#pragma unroll
+    for (int k = 0; k < NW; k += 2)
+      *reinterpret_cast<uint2*>(dst + 4 * k) = make_uint2(word[k], word[k + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NW; k++) *reinterpret_cast<uint32_t*>(dst + 4 * k) = word[k];
+  }
+}
+
+// Quantise the lane's line at B bits (compile time) and store its NE * B / 8 bytes; dst
+// is aligned to the largest power of two (<= 16) dividing NE * B / 8.
+template <typename Tin, int B>
+__device__ __forceinline__ void line_quant_store_ct(const uint32_t* w, float mn, float inv,
+                                                    unsigned char* dst) {
+  constexpr int NE = 128 / (int)sizeof(Tin), NF = NE / 8;
+  const float2 nmn = make_float2(-mn, -mn), inv2 = make_float2(inv, inv);
+  unsigned long long f[NF];
+#pragma unroll
+  for (int g = 0; g < NF; g++) {
+    uint32_t q[8];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      float2 v;
+      if constexpr (InTraits<Tin>::kBf16) {
+        const uint32_t x = w[4 * g + k];
+        v = make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+      } else {
+        v = make_float2(__uint_as_float(w[8 * g + 2 * k]), __uint_as_float(w[8 * g + 2 * k + 1]));
+      }
+      const float2 r = qpair(v, nmn, inv2);
+      q[2 * k] = __float_as_uint(r.x);
+      q[2 * k + 1] = __float_as_uint(r.y);
+    }
+    f[g] = pack8_ct<B>(q);
+  }
+  store_fields<B, NF, lowbit_cap16(NE * B / 8)>(dst, f);
+}
+
+// Width B known at compile time (B > 0) or not (B == 0, width b).
+template <typename Tin, int B>
+__device__ __forceinline__ void line_quant(const uint32_t* w, float mn, float inv, int b,
+                                           unsigned char* dst) {
+  if constexpr (B > 0) {
+    line_quant_store_ct<Tin, B>(w, mn, inv, dst);
+  } else {
+    line_quant_store<Tin>(w, mn, inv, b, dst);
   }
 }
 

@@ -37,6 +37,18 @@ struct TileGeom {
   static_assert(W == 4 || W == 8, "a lane holds 16 or 32 bytes");
 };
 
+// Canonical lg tables replicated per bank, in static shared memory of the encode kernels
+// (filled by each block at start): entry i for lane l at index i * 32 + l, so the 32 lanes'
+// lookups never share a bank.
+static __shared__ float g_lgT[128 * 32];   // fp32 input: T
+static __shared__ float g_lgR[128 * 32];   // fp32 input: R
+static __shared__ float g_lgTB[128 * 32];  // bf16 input: TB
+
+// Byte offset of entry i for `lane` (i < 128): i * 128 + lane * 4.
+__device__ __forceinline__ float lg_tab(const float* tab, uint32_t byte_off) {
+  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(tab) + byte_off);
+}
+
 // Packed fp32x2 add, each component rounded to nearest even exactly like the scalar
 // add.  Products stay scalar (__fmul_rn): a packed multiply followed by an add was
 // measured to be fused into a single-rounding multiply-add on this target, which breaks
@@ -124,11 +136,9 @@ __device__ __forceinline__ uint32_t team_sum_u(uint32_t s) {
 // The two sums of the team's tile that the entropy key needs: L = sum |a_k| and
 // S = sum |a_k| lg |a_k|, both pairwise in natural order (returned as {L, S} in every
 // lane of the team).  The first level of S is fmaf(m_odd, lg m_odd, RN(m_even lg m_even))
-// per pair.  Conflict-free lookups: `rep` holds entry i of lane l at index i*32 + l
-// (floats TB[i] for bf16 input, float2 (T[i], R[i]) for fp32).
+// per pair.  Table lookups go to the per-bank replicated g_lgT / g_lgR / g_lgTB.
 template <typename Tin, int G>
-__device__ __forceinline__ float2 tile_sums(const uint32_t* w, const void* rep, const LgTables& tb,
-                                            int lane) {
+__device__ __forceinline__ float2 tile_sums(const uint32_t* w, const LgTables& tb, int lane) {
   using Gm = TileGeom<Tin, G>;
   constexpr int V = Gm::V;
   float2 ls[V / 2];  // level 1: {m_2j + m_2j+1, fused pair of S}
@@ -152,7 +162,6 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const void* rep, 
       }
     } else {
       const uint32_t lane4 = (uint32_t)lane << 2;
-      const char* tbl = static_cast<const char*>(rep);
 #pragma unroll
       for (int k = 0; k < Gm::W; k++) {
         const uint32_t x = w[k];
@@ -160,8 +169,8 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const void* rep, 
         const float mhi = __uint_as_float(x & 0x7FFF0000u);
         const float elo = __uint_as_float(((x >> 7) & 0xFFu) | 0x4B000000u);
         const float ehi = __uint_as_float(((x >> 23) & 0xFFu) | 0x4B000000u);
-        const float tlo = *reinterpret_cast<const float*>(tbl + (((x << 7) & 0x3F80u) | lane4));
-        const float thi = *reinterpret_cast<const float*>(tbl + (((x >> 9) & 0x3F80u) | lane4));
+        const float tlo = lg_tab(g_lgTB, ((x << 7) & 0x3F80u) | lane4);
+        const float thi = lg_tab(g_lgTB, ((x >> 9) & 0x3F80u) | lane4);
         const float2 ef = add2(make_float2(elo, ehi), make_float2(-8388735.0f, -8388735.0f));
         const float2 lg = add2(ef, make_float2(tlo, thi));  // e + TB[i]
         // a zero magnitude gives lg = -127 and a zero term (its sign cannot reach H)
@@ -178,13 +187,13 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const void* rep, 
       if (E == 0u && b != 0u) {
         lgv[j] = lg_canon<false>(m[j], tb.T, tb.R, tb.TB, tb.k);
       } else {  // normal, or zero (lg = -127, a zero term)
-        const float2 tr = static_cast<const float2*>(rep)[(((b >> 16) & 0x7Fu) << 5) | (uint32_t)lane];
+        const uint32_t off = ((b >> 9) & 0x3F80u) | ((uint32_t)lane << 2);
         const float ef = __fsub_rn(__uint_as_float(0x4B000000u | E), 8388735.0f);
         const float mm = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-        const float r = __fmaf_rn(mm, tr.y, -1.0f);
+        const float r = __fmaf_rn(mm, lg_tab(g_lgR, off), -1.0f);
         float p = __fmaf_rn(tb.k[2], r, tb.k[1]);
         p = __fmaf_rn(p, r, tb.k[0]);
-        lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, tr.x));
+        lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, lg_tab(g_lgT, off)));
       }
     }
 #pragma unroll
