@@ -264,8 +264,11 @@ def run_gpu(args):
     ws = enc["workspace"]
     K_hi = tq.tahq_hi_count(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
     n_g = (w.tokens_per_group or T) * (C // G)
-    launches = 1 + 3   # encode: one kernel; decode: totals, scan, decode
-    enc_kernel = (f"k_encode<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>" if 0 < K_hi < n_g
+    ranked = 0 < K_hi < n_g
+    # encode: the queue table and the persistent kernel (ranked) or one kernel (one width);
+    # decode: totals, scan, decode
+    launches = (2 if ranked else 1) + 3
+    enc_kernel = (f"k_encode<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}> (+ k_items)" if ranked
                   else f"k_encode_flat<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>")
 
     def step(ev, k=0):

@@ -93,7 +93,7 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
 
 struct EncLayout {
   size_t status, ticket, cand_cnt, doneA, doneB, doneB2, selready, sel, hist_coarse, hist_fine, lookback,
-      ctrl_end, keys, cand, scratch_lo, scratch_hi, total;
+      ctrl_end, keys, cand, scratch_lo, scratch_hi, items, items_cap, total;
 };
 
 // Offset words are sized for the input type that needs the most compaction chunks.
@@ -134,6 +134,11 @@ EncLayout enc_layout(const Shape& s) {
   off = align_up(off + (size_t)s.n * (size_t)(s.G * s.lo / 8));
   L.scratch_hi = off;
   off = align_up(off + (size_t)s.n * (size_t)(s.G * s.hi / 8));
+  // the decoded work queue, sized for the input type with the most items
+  L.items = off;
+  L.items_cap = (size_t)std::max(tahq::encode_queue_items(0, s.G, s.hi, s.n_g, s.n_groups),
+                                 tahq::encode_queue_items(1, s.G, s.hi, s.n_g, s.n_groups));
+  off = align_up(off + 8 * L.items_cap);
   L.total = off;
   return L;
 }
@@ -260,6 +265,8 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.cand = at<unsigned long long>(workspace, L.cand);
   a.scratch_lo = at<uint8_t>(workspace, L.scratch_lo);
   a.scratch_hi = at<uint8_t>(workspace, L.scratch_hi);
+  a.items = at<unsigned long long>(workspace, L.items);
+  a.items_cap = (long long)L.items_cap;
   return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 

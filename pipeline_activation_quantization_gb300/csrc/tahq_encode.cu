@@ -1,6 +1,8 @@
 // tahq_encode.cu -- host side of the encode launch: geometry of the compaction chunks
 // and the dispatch to the per-input-type instantiations (tahq_encode_f32.cu,
 // tahq_encode_bf16.cu).
+#include <algorithm>
+
 #include "tahq_launch.h"
 
 namespace tahq {
@@ -15,6 +17,20 @@ long long encode_cchunk_tiles(int bf16, int G, int hi) {
 long long encode_chunks(int bf16, int G, int hi, long long n_g, long long n_groups) {
   const long long chc = encode_cchunk_tiles(bf16, G, hi);
   return n_groups * ((n_g + chc - 1) / chc);
+}
+
+// An offsets item covers at most 256 compaction chunks (their counts collect in shared
+// memory); otherwise one select / offsets item per 8 tiles items, at most 256.
+long long encode_sel_items(long long nA, long long nC) {
+  return std::max<long long>({1ll, std::min<long long>(256, nA / 8), (nC + 255) / 256});
+}
+
+long long encode_queue_items(int bf16, int G, int hi, long long n_g, long long n_groups) {
+  const long long ch = kEncChunkBytes / (G * (bf16 ? 2 : 4));
+  const long long nA = (n_g + ch - 1) / ch;
+  const long long chc = encode_cchunk_tiles(bf16, G, hi);
+  const long long nC = (n_g + chc - 1) / chc;
+  return n_groups * (nA + 2 * encode_sel_items(nA, nC) + nC);
 }
 
 cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t st) {

@@ -79,6 +79,9 @@ struct alignas(64) TmaDesc {
   unsigned char bytes[128];
 };
 
+// Barrier of the block's 256 threads (named barrier 1).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 struct Item {
   int type;  // kItemTiles, kItemSelect, kItemOffsets, kItemCompact
   long long g, idx;
@@ -98,9 +101,8 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
   uint32_t ndef;       // line layout: length of dl
   uint32_t hist[kCoarseBins];
   uint32_t scan[kWarps + 4];
-  unsigned long long bar[2];
+  unsigned long long bar[2];  // the slot's input chunk has landed
   Item item[2];
-  long long next;
   uint32_t last;
 };
 
@@ -135,6 +137,7 @@ struct EncParams {
   unsigned long long* lookback;  // per group: hi count, then offset, of each compaction chunk
   uint32_t* ticket;
   uint32_t* status;
+  unsigned long long* items;  // [n_items] the decoded queue
   LgTables tabs;
 };
 
@@ -170,7 +173,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& t
     if (lane >= o) incl += y;
   }
   if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
+  csync();
   if (warp == 0) {
     const uint32_t w = lane < kW ? s_warp[lane] : 0u;
     uint32_t wi = w;
@@ -183,10 +186,10 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& t
     if (lane < kW) s_warp[lane] = wi - w;
     if (lane == kW - 1) s_warp[kW] = wi;
   }
-  __syncthreads();
+  csync();
   total = s_warp[kW];
   const uint32_t r = s_warp[warp] + incl - v;
-  __syncthreads();
+  csync();
   return r;
 }
 
@@ -248,10 +251,10 @@ __device__ __forceinline__ void put_meta(const EncParams& p, long long t, float 
 
 // ====================================================================== tiles: line layout
 
-// Deferred tiles, a team of L lanes (V values each) per tile: list[j] for j = first +
+// Deferred tiles of the narrow layout, a team of L lanes (V values each) per tile: list[j] for j = first +
 // team, first + TPW + team, ... while j < n (first / step warp-uniform): the exact ratio
 // test (eq. (3)), pivot swap and Hadamard (eq. (4)) where it holds, range, both widths.
-template <typename Tin, int G, bool kSwz>
+template <typename Tin, int G>
 __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned char* buf,
                                             const uint16_t* list, int n, int first, int step,
                                             long long t0, bool flat, unsigned char* stage_lo,
@@ -269,11 +272,7 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
     const int kt = valid ? (int)list[ci] : 0;
     uint32_t w[W];
     if (valid) {
-      if constexpr (kSwz) {
-        lds_words_swz<Tin, G>(buf, kt, sub, w);
-      } else {
-        lds_words<Tin, G>(buf, kt, sub, w);
-      }
+      lds_words<Tin, G>(buf, kt, sub, w);
     } else {
 #pragma unroll
       for (int k = 0; k < W; k++) w[k] = 0u;
@@ -327,6 +326,105 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
   }
 }
 
+// Deferred tiles of the line layout, one block-wide list: teams of L = G / V2 lanes (V2 =
+// 4 fp32 or 8 bf16 values, one 16-byte unit per lane; a whole warp per fp32 tile of 128)
+// take list entries warp * TPW + team, + kWarps * TPW, ...: exact ratio test (eq. (3)),
+// pivot swap and Hadamard (eq. (4)) where it holds, range, and the slots of both widths
+// (8 / V2 lanes gather each group of 8 codes).
+template <typename Tin, int G>
+__device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned char* buf,
+                                           const uint16_t* list, int n, long long t0, bool flat,
+                                           int lo, int hi, unsigned char* stage_lo,
+                                           unsigned char* stage_hi) {
+  constexpr bool kBf = InTraits<Tin>::kBf16;
+  constexpr int V = kBf ? 8 : 4, L = G / V, TPW = 32 / L, LPT = LineGeom<Tin, G>::LPT;
+  constexpr int kGrp = 8 / V;  // lanes per group of 8 codes
+  static_assert(L >= 2 && L <= 32, "team of 2..32 lanes");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L, base = lane - sub;
+#pragma unroll 1
+  for (int j0 = warp * TPW; j0 < n; j0 += kWarps * TPW) {
+    const int ci = j0 + team;
+    const bool valid = ci < n;
+    const int kt = valid ? (int)list[ci] : 0;
+    const int line = kt * LPT + (sub >> 3);
+    const uint4 q = *reinterpret_cast<const uint4*>(buf + line * 128 + (((sub & 7) ^ (line & 7)) << 4));
+    float v[V];
+    if constexpr (kBf) {
+      const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        v[2 * k] = __uint_as_float(wq[k] << 16);
+        v[2 * k + 1] = __uint_as_float(wq[k] & 0xFFFF0000u);
+      }
+    } else {
+      v[0] = __uint_as_float(q.x);
+      v[1] = __uint_as_float(q.y);
+      v[2] = __uint_as_float(q.z);
+      v[3] = __uint_as_float(q.w);
+    }
+    float m1 = fabsf(v[0]), m2 = -1.0f;
+    int i1 = sub * V;
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      const float m = fabsf(v[j]);
+      if (m > m1) {
+        m2 = m1;
+        m1 = m;
+        i1 = sub * V + j;
+      } else if (m > m2) {
+        m2 = m;
+      }
+    }
+    team_top2<L>(m1, i1, m2);
+    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+    if (__any_sync(kFull, flag)) {
+      float t[V];
+#pragma unroll
+      for (int j = 0; j < V; j++) t[j] = v[j];
+      team_swap0<V>(t, flag ? i1 : 0, sub, base);
+      team_fwht<V, L>(t, p.h, sub);
+      if (flag) {
+#pragma unroll
+        for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], p.c_h);
+      }
+    }
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      mn = fminf(mn, v[j]);
+      mx = fmaxf(mx, v[j]);
+    }
+    mn = team_min<L>(mn);
+    mx = team_max<L>(mx);
+    const float D = __fsub_rn(mx, mn);
+    // lane 0 of the team: Q_lo / D; lane 1: Q_hi / D (or D / Q_b in the one-width pass)
+    const float num = sub == 1 ? (flat ? D : qmax_f(hi)) : qmax_f(lo);
+    const float den = sub == 1 ? (flat ? qmax_f(lo) : D) : D;
+    const float r = __fdiv_rn(num, den);
+    const float r0 = __shfl_sync(kFull, r, base), r1s = __shfl_sync(kFull, r, base + 1);
+    const bool degenerate = !(D >= 0x1p-120f);
+    const float inv_lo = degenerate ? 0.0f : r0, r1 = degenerate ? 0.0f : r1s;
+#pragma unroll
+    for (int w2 = 0; w2 < 2; w2++) {
+      if (w2 == 1 && flat) break;
+      const int b = w2 ? hi : lo;
+      const float inv = w2 ? r1 : inv_lo;
+      unsigned long long f = 0ull;
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
+        f |= (unsigned long long)(__float_as_uint(c) - 0x4B400000u) << (j * b);
+      }
+      if constexpr (kGrp > 1) f |= __shfl_down_sync(kFull, f, 1) << (V * b);
+      unsigned char* slot = (w2 ? stage_hi : stage_lo) + kt * (G * b / 8);
+      if (valid && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
+    }
+    if (valid && sub == 0)
+      put_meta(p, t0 + kt, mn, flag ? (uint8_t)i1 : (uint8_t)0xFF, flat ? r1 : D, flat);
+  }
+}
+
 // Tiles pass over one staged chunk, line layout: each warp takes 32 consecutive lines.
 // kLo / kHi: the two widths when known at compile time (0: from p).
 template <typename Tin, int G, int kLo, int kHi>
@@ -340,12 +438,9 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   const int line = warp * 32 + lane;
   const int kt = line / LPT, sub = line % LPT;
   const bool valid = kt < nt;
-  uint32_t w[32];
-  lds_line(buf, line, w);
-
   // entropy key and histograms (§3.2)
   if (!flat) {
-    float2 ls = line_sums<Tin>(w, s.tabs, lane);
+    float2 ls = line_sums<Tin>(buf, line, s.tabs, lane);
     ls = team_sum2<LPT>(ls);
     int cb = -1;
     if (valid && sub == 0) {
@@ -363,6 +458,8 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   }
 
   // range and the two-values pretest
+  uint32_t w[32];
+  lds_line(buf, line, w);
   float mn, mx, ga[NE / 8];
   line_minmax<Tin>(w, mn, mx, ga);
   mn = team_min<LPT>(mn);
@@ -404,10 +501,8 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   // take them in turn (outlier channels sit at fixed tile positions, so per-warp lists
   // would load some warps far more than others)
   if (valid && deferred && sub == 0) s.dl[atomicAdd(&s.ndef, 1u)] = (uint16_t)kt;
-  __syncthreads();
-  constexpr int TPW = Cfg<Tin, G>::TPW;
-  pass2_teams<Tin, G, true>(p, buf, s.dl, (int)s.ndef, warp * TPW, kWarps * TPW, t0, flat,
-                            stage_lo, stage_hi);
+  csync();
+  pass2_line<Tin, G>(p, buf, s.dl, (int)s.ndef, t0, flat, lo, hi, stage_lo, stage_hi);
 }
 
 // ====================================================================== tiles: narrow layout
@@ -554,7 +649,7 @@ __device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams
     if (!flat) quant_store<V>(v, mn, s.tc[kt], hi, stage_hi + kt * p.slot_hi + sub * (V * hi / 8));
   }
   // pass 2
-  pass2_teams<Tin, G, false>(p, buf, dl, ndef, 0, TPW, t0, flat, stage_lo, stage_hi);
+  pass2_teams<Tin, G>(p, buf, dl, ndef, 0, TPW, t0, flat, stage_lo, stage_hi);
 }
 
 // ====================================================================== stores
@@ -684,12 +779,12 @@ __device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
   } else {
     tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
   }
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) s.ndef = 0u;
   store_stage(stage_lo, p.scratch_lo, t0 * p.slot_lo, nt * p.slot_lo);
   store_stage(stage_hi, p.scratch_hi, t0 * p.slot_hi, nt * p.slot_hi);
   // the block's writes, ordered by the barrier, are published by one gpu-scope fence
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(&p.doneA[it.g], 1u);
@@ -704,7 +799,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
   const long long g = it.g;
   const uint32_t K = (uint32_t)p.K;
   if (threadIdx.x == 0) wait_counter(&p.doneA[g], (uint32_t)p.nA, p.status);
-  __syncthreads();
+  csync();
   uint32_t* bins = s.hist;  // all zero between items; left zero below
   if (threadIdx.x < 32) {
     for (int i = threadIdx.x; i < 256; i += 32) bins[i] = __ldcg(&p.hist_coarse[g * kCoarseBins + i]);
@@ -724,7 +819,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
       s.scan[1] = above_c + above_f;
     }
   }
-  __syncthreads();
+  csync();
   const int bstar = (int)s.scan[0];
   const uint32_t above = s.scan[1];
   // candidates of this item's slice of the group
@@ -750,14 +845,14 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
       if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv, (uint32_t)i);
     }
   }
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     __threadfence();
     const uint32_t prev = atomicAdd(&p.doneB[g], 1u);
     __threadfence();
     s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
   }
-  __syncthreads();
+  csync();
   if (s.last) {
     const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
     const uint32_t expect = __ldcg(&p.hist_fine[g * (long long)kFineBins + bstar]);
@@ -769,16 +864,16 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
       unsigned long long* ck = reinterpret_cast<unsigned long long*>(scratch);
       for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) ck[i] = __ldcg(&cg[i]);
       if (threadIdx.x == 0) s.scan[2] = 0u;
-      __syncthreads();
+      csync();
       for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
         const unsigned long long ki = ck[i];
         uint32_t larger = 0;
         for (uint32_t j = 0; j < cnt; j++) larger += ck[j] > ki ? 1u : 0u;
         if (larger == r - 1u) s.scan[2] = i;
       }
-      __syncthreads();
+      csync();
       theta = ck[s.scan[2]];
-      __syncthreads();
+      csync();
     } else if (cnt > 0u) {
       // radix select (8 passes of 8 bits) of the r-th largest candidate key
       uint32_t rr = r;
@@ -786,12 +881,12 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
       for (int pass = 7; pass >= 0; --pass) {
         const int shift = pass * 8;
         for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
-        __syncthreads();
+        csync();
         for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
           const unsigned long long v = __ldcg(&cg[i]);
           if ((v & mask) == prefix) atomicAdd(&bins[(v >> shift) & 255u], 1u);
         }
-        __syncthreads();
+        csync();
         if (threadIdx.x < 32) {
           int d;
           uint32_t ab;
@@ -801,11 +896,11 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
             s.scan[3] = ab;
           }
         }
-        __syncthreads();
+        csync();
         prefix |= (unsigned long long)s.scan[2] << shift;
         rr -= s.scan[3];
         mask |= 0xFFull << shift;
-        __syncthreads();
+        csync();
       }
       theta = prefix;
     }
@@ -816,7 +911,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
     }
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
-  __syncthreads();
+  csync();
 }
 
 // ---- offsets item: the width and the scale of every tile of its compaction chunks and
@@ -826,41 +921,45 @@ template <typename Tin, int G>
 __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
   const long long g = it.g;
   if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status);
-  __syncthreads();
+  csync();
   const unsigned long long theta = __ldcg(&p.sel[g].theta);
   const uint32_t mode = __ldcg(&p.sel[g].mode);
   unsigned long long* words = p.lookback + g * p.nC;
   const long long per = (p.nC + p.J - 1) / p.J;
   const long long c0 = it.idx * per, c1 = min(p.nC, c0 + per);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (long long c = c0 + warp; c < c1; c += kWarps) {
-    const long long tl0 = c * p.CHC;
-    const int nt = (int)min(p.CHC, p.n_g - tl0);
-    const long long t0 = g * p.n_g + tl0;
-    uint32_t cnt = 0;
-    for (int k = lane; k < nt; k += 32) {
-      bool ishi = mode == kSelAll;
-      if (mode == kSelThreshold)
-        ishi = rank_key(__ldcg(&p.keys[t0 + k]), (uint32_t)(tl0 + k)) >= theta;
+  // every thread one tile at a time; a warp's 32 tiles lie in one compaction chunk
+  // (chunks hold a multiple of 32 tiles), whose hi count collects in s.hist[c - c0]
+  const long long tl_begin = c0 * p.CHC, tl_end = min(p.n_g, c1 * p.CHC);
+  const int lane = threadIdx.x & 31;
+  for (long long tb = tl_begin; tb < tl_end; tb += kThreads) {
+    const long long tl = tb + threadIdx.x;
+    bool ishi = false;
+    if (tl < tl_end) {
+      const long long t = g * p.n_g + tl;
+      ishi = mode == kSelAll;
+      if (mode == kSelThreshold) ishi = rank_key(__ldcg(&p.keys[t]), (uint32_t)tl) >= theta;
       const int b = ishi ? p.hi : p.lo;
-      p.bits[t0 + k] = (uint8_t)b;
+      p.bits[t] = (uint8_t)b;
       // the range D left by the tiles pass becomes the scale D / Q
-      const float D = __ldcg(&p.scales[t0 + k]);
-      p.scales[t0 + k] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
-      cnt += ishi ? 1u : 0u;
+      const float D = __ldcg(&p.scales[t]);
+      p.scales[t] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
-    if (lane == 0) words[c] = cnt;
+    const unsigned hm = __ballot_sync(kFull, ishi);
+    if (lane == 0 && hm) atomicAdd(&s.hist[(int)((tb + (threadIdx.x & ~31)) / p.CHC - c0)], (uint32_t)__popc(hm));
   }
-  __syncthreads();
+  csync();
+  for (long long c = c0 + threadIdx.x; c < c1; c += kThreads) {
+    words[c] = s.hist[c - c0];
+    s.hist[c - c0] = 0u;  // bins are all zero between items
+  }
+  csync();
   if (threadIdx.x == 0) {
     __threadfence();
     const uint32_t prev = atomicAdd(&p.doneB2[g], 1u);
     __threadfence();
     s.last = (prev == (uint32_t)p.J - 1u) ? 1u : 0u;
   }
-  __syncthreads();
+  csync();
   if (s.last) {
     // exclusive prefix of the nC counts: each thread sums a contiguous run, one block scan
     const long long run = (p.nC + kThreads - 1) / kThreads;
@@ -874,7 +973,7 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       words[c] = acc;
       acc += v;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) {
       __threadfence();
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.selready[g]), "r"(2u) : "memory");
@@ -915,7 +1014,7 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
                            unsigned char* stage, uint16_t* off, uint8_t* cbits) {
   const long long g = it.g, cc = it.idx;
   if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status);
-  __syncthreads();
+  csync();
   const long long tl0 = cc * p.CHC;
   const int nt = (int)min(p.CHC, p.n_g - tl0);
   const long long t0 = g * p.n_g + tl0;
@@ -947,7 +1046,7 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       before += (hiflags >> j) & 1u;
     }
   }
-  __syncthreads();
+  csync();
   const int u = __ffs(p.slot_lo | p.slot_hi | 16) - 1;  // log2 of the largest common unit
   if (u >= 4) {
     gather_units<uint4>(off, cbits, p, t0, nt, stage);
@@ -960,7 +1059,7 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   } else {
     gather_units<unsigned char>(off, cbits, p, t0, nt, stage);
   }
-  __syncthreads();
+  csync();
   const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
   int nbytes = nt * slot_lo + (int)chunk_hi * slot_d;
   if (base + nbytes > p.codes_bytes) {  // only if the select went wrong: never write past
@@ -1000,6 +1099,21 @@ __device__ __forceinline__ EncSmem<Tin, G>& enc_smem(unsigned char* raw) {
   return *reinterpret_cast<EncSmem<Tin, G>*>(raw + ((1024u - (a & 1023u)) & 1023u));
 }
 
+// The queue, decoded once per call: one 64-bit record per ticket (type in bits 62-63,
+// group in bits 40-61, index in bits 0-39).
+__device__ __forceinline__ unsigned long long pack_item(const Item& it) {
+  return ((unsigned long long)(it.type & 3) << 62) | ((unsigned long long)it.g << 40) |
+         (unsigned long long)it.idx;
+}
+__device__ __forceinline__ Item unpack_item(unsigned long long r) {
+  return Item{(int)(r >> 62), (long long)((r >> 40) & 0x3FFFFFull), (long long)(r & 0xFFFFFFFFFFull)};
+}
+
+static __global__ void __launch_bounds__(256) k_items(const __grid_constant__ EncParams p) {
+  const long long q = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (q < p.n_items) p.items[q] = pack_item(decode_item(p, (uint32_t)q));
+}
+
 template <typename Tin, int G, int kLo, int kHi>
 __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ EncParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1008,50 +1122,49 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
   unsigned char* stage_hi = stage_lo + p.stage_lo_bytes;
   init_tables<Tin, G>(s, p.tabs);
   for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) s.hist[i] = 0u;
-  uint32_t ahead = 0u;  // thread 0: the ticket after the next one, dequeued early
+  const unsigned long long pol = policy_evict_first();  // the input is read once
+  const uint32_t n_items = (uint32_t)p.n_items;
+  // Thread 0 runs the queue two items ahead: ticket tk2 (item i + 2) and the record
+  // rec1 of item i + 1 are requested one item before they are used.
+  uint32_t tk1 = 0u, tk2 = 0u;
+  unsigned long long rec1 = 0ull;
+  auto record = [&](uint32_t t) { return t < n_items ? __ldcg(p.items + t) : ~0ull; };
+  auto start = [&](unsigned long long r, int slot) {  // publish the item, start its copy
+    const Item it = r == ~0ull ? Item{-1, 0, 0} : unpack_item(r);
+    s.item[slot] = it;
+    if (it.type == kItemTiles) {
+      long long t0;
+      int nt;
+      tiles_range<Tin, G>(p, it, t0, nt);
+      issue_chunk<Tin, G>(s, p, t0, nt, slot, pol);
+    }
+  };
   if (threadIdx.x == 0) {
     mbar_init(&s.bar[0], 1);
     mbar_init(&s.bar[1], 1);
     fence_barrier_init();
     s.ndef = 0u;
-    s.next = (long long)atomicAdd(p.ticket, 1u);
-    ahead = atomicAdd(p.ticket, 1u);
+    start(record(atomicAdd(p.ticket, 1u)), 0);
+    tk1 = atomicAdd(p.ticket, 1u);
+    rec1 = record(tk1);
+    tk2 = atomicAdd(p.ticket, 1u);
   }
-  __syncthreads();
-  const unsigned long long pol = policy_evict_first();  // the input is read once
   uint32_t parity = 0u;  // bit s = phase parity of buffer s
-
-  // Thread 0 starts the copy of a tiles item's input chunk into buffer `slot`.
-  auto issue = [&](const Item& it, int slot) {
-    if (it.type != kItemTiles) return;
-    long long t0;
-    int nt;
-    tiles_range<Tin, G>(p, it, t0, nt);
-    issue_chunk<Tin, G>(s, p, t0, nt, slot, pol);
-  };
-
-  // Thread 0 decodes each item once (s.item[slot]) when it dequeues it.
-  long long cur = s.next;
-  int slot = 0;
-  if (threadIdx.x == 0 && cur < p.n_items) {
-    s.item[0] = decode_item(p, (uint32_t)cur);
-    issue(s.item[0], 0);
-  }
-  while (cur < p.n_items) {
-    __syncthreads();  // everyone is done with the previous item and its buffer
+  for (int slot = 0;; slot ^= 1) {
+    csync();  // everyone is done with the previous item, its buffer and shared state
     if (threadIdx.x == 0) {
-      // a block holds up to three tickets (the item it works on, the next one, one more)
-      // and works through them in order; items only wait for smaller tickets, so the
-      // smallest item in work never waits for an item that has not started
-      const long long nxt = (long long)ahead;
-      s.next = nxt;
-      if (nxt < p.n_items) {
-        s.item[slot ^ 1] = decode_item(p, (uint32_t)nxt);
-        issue(s.item[slot ^ 1], slot ^ 1);
-        ahead = atomicAdd(p.ticket, 1u);
+      // a block holds up to four tickets and works through them in order; items only
+      // wait for smaller tickets, so the smallest item in work never waits for an item
+      // that has not started
+      start(rec1, slot ^ 1);
+      if (tk1 < n_items) {
+        tk1 = tk2;
+        rec1 = record(tk1);
+        if (tk1 < n_items) tk2 = atomicAdd(p.ticket, 1u);
       }
     }
     const Item it = s.item[slot];
+    if (it.type < 0) break;
     if (it.type == kItemTiles) {
       mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
       parity ^= 1u << slot;
@@ -1065,9 +1178,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     } else if (it.type == kItemOffsets) {
       do_offsets<Tin, G>(s, p, it);
     }
-    __syncthreads();
-    cur = s.next;
-    slot ^= 1;
   }
 }
 
@@ -1085,7 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
     fence_barrier_init();
     s.ndef = 0u;
   }
-  __syncthreads();
+  csync();
   const unsigned long long pol = policy_evict_first();
   uint32_t parity = 0u;
   const int slot_b = G * p.flat_b / 8;
@@ -1102,16 +1212,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
     const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
     mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
     parity ^= 1u << slot;
-    __syncthreads();
+    csync();
     if constexpr (C::kLine) {
       tiles_line<Tin, G, kB, 0>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
     } else {
       tiles_narrow<Tin, G>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) s.ndef = 0u;
     store_stage(stage, p.codes, t0 * slot_b, nt * slot_b);
-    __syncthreads();
+    csync();
     slot ^= 1;
   }
 }
@@ -1195,6 +1305,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.sel = a.sel;
   p.lookback = a.lookback;
   p.ticket = a.ticket;
+  p.items = a.items;
   p.status = a.status;
   p.tabs = *a.tabs;
   if constexpr (C::kLine) {
@@ -1234,8 +1345,9 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   // finish meanwhile), an eighth of the group before the offsets items
   p.pre1 = std::min<long long>(p.nA, grid_cap);
   p.pre2 = std::min<long long>(p.nA - p.pre1, p.nA / 8);
-  p.J = std::max<long long>(1, std::min<long long>(256, p.nA / 8));
+  p.J = encode_sel_items(p.nA, p.nC);
   p.n_items = a.n_groups * (p.nA + 2 * p.J + p.nC);
+  if (p.n_items > a.items_cap) return cudaErrorInvalidValue;
   if (p.n_items >= (1ll << 31) || (p.nA + 2 * p.J + p.nC) * p.nC >= (1ll << 32))
     return cudaErrorInvalidValue;
   queue_segments(p);
@@ -1246,6 +1358,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, p.n_items));
+  k_items<<<(unsigned)((p.n_items + 255) / 256), 256, 0, st>>>(p);
   kern<<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }

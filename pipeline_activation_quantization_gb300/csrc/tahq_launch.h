@@ -40,6 +40,8 @@ struct EncodeArgs {
   unsigned long long* cand;  // [n_tiles]
   uint8_t* scratch_lo;       // [n_tiles * G * lo / 8] every tile quantised at bits_lo
   uint8_t* scratch_hi;       // [n_tiles * G * hi / 8] every tile quantised at bits_hi
+  unsigned long long* items; // [items_cap] the decoded work queue
+  long long items_cap;
 };
 
 struct DecodeArgs {
@@ -68,6 +70,9 @@ constexpr int kEncMaxCC = 2048;
 // (one offset word each) for these shapes.
 long long encode_cchunk_tiles(int bf16, int G, int hi);
 long long encode_chunks(int bf16, int G, int hi, long long n_g, long long n_groups);
+// Select (and offsets) items per group; work-queue items of a whole encode.
+long long encode_sel_items(long long nA, long long nC);
+long long encode_queue_items(int bf16, int G, int hi, long long n_g, long long n_groups);
 // Number of decode chunks, and of blocks of kDecChunksPerBlock chunks, for these shapes.
 constexpr int kDecChunksPerBlock = 8;
 long long decode_chunks(int G, long long n_tiles);

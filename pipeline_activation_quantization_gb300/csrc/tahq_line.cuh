@@ -77,57 +77,72 @@ __device__ __forceinline__ float2 lg_pair_f32(uint32_t a, uint32_t b, uint32_t l
   return add2(ef, t);
 }
 
-// {L, S} of one fp32 line: L = pairwise sum of m_k, S = pairwise sum of the fused pairs
-// fmaf(m_2j+1, lg m_2j+1, RN(m_2j lg m_2j)); both in natural order over the 32 values.
-__device__ __forceinline__ float2 line_sums_f32(const uint32_t* w, const LgTables& tb, int lane) {
-  uint32_t mb[32];
+// Half h (16 words, bytes [64 h, 64 h + 64)) of line `line` of a swizzled chunk.
+__device__ __forceinline__ void lds_half(const unsigned char* buf, int line, int h, uint32_t* w) {
+  const unsigned char* base = buf + line * 128;
+  const int x = (line & 7) << 4;
 #pragma unroll
-  for (int k = 0; k < 32; k++) mb[k] = w[k] & 0x7FFFFFFFu;
+  for (int j = 0; j < 4; j++) {
+    const uint4 q = *reinterpret_cast<const uint4*>(base + (((4 * h + j) << 4) ^ x));
+    w[4 * j] = q.x;
+    w[4 * j + 1] = q.y;
+    w[4 * j + 2] = q.z;
+    w[4 * j + 3] = q.w;
+  }
+}
+
+// {L, S} of 16 fp32 values: L = pairwise sum of m_k, S = pairwise sum of the fused pairs
+// fmaf(m_2j+1, lg m_2j+1, RN(m_2j lg m_2j)); natural order.  Packed pairs (k, k + 8) keep
+// every level of the tree.
+__device__ __forceinline__ float2 half_sums_f32(const uint32_t* w, const LgTables& tb, int lane) {
+  uint32_t mb[16];
+#pragma unroll
+  for (int k = 0; k < 16; k++) mb[k] = w[k] & 0x7FFFFFFFu;
   // zero or subnormal magnitudes present?  (rare: those take the general lg)
   uint32_t mn = mb[0];
 #pragma unroll
-  for (int k = 1; k + 1 < 32; k += 2) mn = __vimin3_u32(mn, mb[k], mb[k + 1]);
-  mn = min(mn, mb[31]);
-  float2 m2[16], l2[16];
+  for (int k = 1; k + 1 < 16; k += 2) mn = __vimin3_u32(mn, mb[k], mb[k + 1]);
+  mn = min(mn, mb[15]);
+  float2 m2[8], l2[8];
   if (mn >= 0x00800000u) {
     const uint32_t lane4 = (uint32_t)lane << 2;
 #pragma unroll
-    for (int k = 0; k < 16; k++) {
-      m2[k] = make_float2(__uint_as_float(mb[k]), __uint_as_float(mb[k + 16]));
-      l2[k] = lg_pair_f32(mb[k], mb[k + 16], lane4, tb);
+    for (int k = 0; k < 8; k++) {
+      m2[k] = make_float2(__uint_as_float(mb[k]), __uint_as_float(mb[k + 8]));
+      l2[k] = lg_pair_f32(mb[k], mb[k + 8], lane4, tb);
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; k++) {
-      const float a = __uint_as_float(mb[k]), b = __uint_as_float(mb[k + 16]);
+    for (int k = 0; k < 8; k++) {
+      const float a = __uint_as_float(mb[k]), b = __uint_as_float(mb[k + 8]);
       m2[k] = make_float2(a, b);
       l2[k] = make_float2(a == 0.0f ? 0.0f : lg_canon<false>(a, tb.T, tb.R, tb.TB, tb.k),
                           b == 0.0f ? 0.0f : lg_canon<false>(b, tb.T, tb.R, tb.TB, tb.k));
     }
   }
-  float2 L1[8], S1[8];
+  float2 L1[4], S1[4];
 #pragma unroll
-  for (int j = 0; j < 8; j++) {
+  for (int j = 0; j < 4; j++) {
     L1[j] = add2(m2[2 * j], m2[2 * j + 1]);
     S1[j] = fma2(m2[2 * j + 1], l2[2 * j + 1], mul2(m2[2 * j], l2[2 * j]));
   }
-  const float2 Lt = tree2<8>(L1), St = tree2<8>(S1);
+  const float2 Lt = tree2<4>(L1), St = tree2<4>(S1);
   return make_float2(__fadd_rn(Lt.x, Lt.y), __fadd_rn(St.x, St.y));
 }
 
-// {L, S} of one bf16 line (64 values; word k holds values 2k (low half) and 2k + 1).
+// {L, S} of 16 words of bf16 (32 values; word k holds values 2k (low half) and 2k + 1).
 // The lg of a bf16 magnitude is exact from the table: e + TB[top 7 fraction bits].
-__device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const LgTables& tb, int lane) {
-  // any half with exponent field 0 (zero or subnormal)?  those take the general lg
+__device__ __forceinline__ float2 half_sums_bf16(const uint32_t* w, const LgTables& tb, int lane) {
+  // any half-word with exponent field 0 (zero or subnormal)?  those take the general lg
   uint32_t em = 0xFFFFFFFFu;
 #pragma unroll
-  for (int k = 0; k < 32; k++) em = __vminu2(em, w[k] & 0x7F807F80u);
-  float2 L1[16], S1[16];
+  for (int k = 0; k < 16; k++) em = __vminu2(em, w[k] & 0x7F807F80u);
+  float2 L1[8], S1[8];
   if ((em & 0xFFFFu) != 0u && (em >> 16) != 0u) {
     const uint32_t lane4 = (uint32_t)lane << 2;
 #pragma unroll
-    for (int k = 0; k < 16; k++) {
-      const uint32_t a = w[k], b = w[k + 16];
+    for (int k = 0; k < 8; k++) {
+      const uint32_t a = w[k], b = w[k + 8];
       const float2 mlo = make_float2(__uint_as_float((a << 16) & 0x7FFF0000u),
                                      __uint_as_float((b << 16) & 0x7FFF0000u));
       const float2 mhi = make_float2(__uint_as_float(a & 0x7FFF0000u),
@@ -148,33 +163,43 @@ __device__ __forceinline__ float2 line_sums_bf16(const uint32_t* w, const LgTabl
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; k++) {
-      float l[2], s[2];
+    for (int k = 0; k < 8; k++) {
+      float l[2], sm[2];
 #pragma unroll
       for (int q = 0; q < 2; q++) {
-        const uint32_t x = w[k + 16 * q];
+        const uint32_t x = w[k + 8 * q];
         const float a = __uint_as_float((x << 16) & 0x7FFF0000u);
         const float b = __uint_as_float(x & 0x7FFF0000u);
         const float la = a == 0.0f ? 0.0f : lg_canon<true>(a, tb.T, tb.R, tb.TB, tb.k);
         const float lb = b == 0.0f ? 0.0f : lg_canon<true>(b, tb.T, tb.R, tb.TB, tb.k);
         l[q] = __fadd_rn(a, b);
-        s[q] = __fmaf_rn(b, lb, __fmul_rn(a, la));
+        sm[q] = __fmaf_rn(b, lb, __fmul_rn(a, la));
       }
       L1[k] = make_float2(l[0], l[1]);
-      S1[k] = make_float2(s[0], s[1]);
+      S1[k] = make_float2(sm[0], sm[1]);
     }
   }
-  const float2 Lt = tree2<16>(L1), St = tree2<16>(S1);
+  const float2 Lt = tree2<8>(L1), St = tree2<8>(S1);
   return make_float2(__fadd_rn(Lt.x, Lt.y), __fadd_rn(St.x, St.y));
 }
 
+// {L, S} of line `line` of a swizzled chunk, half by half: the line's tree is
+// (half 0) + (half 1), each half pairwise in natural order.
 template <typename Tin>
-__device__ __forceinline__ float2 line_sums(const uint32_t* w, const LgTables& tb, int lane) {
-  if constexpr (InTraits<Tin>::kBf16) {
-    return line_sums_bf16(w, tb, lane);
-  } else {
-    return line_sums_f32(w, tb, lane);
+__device__ __forceinline__ float2 line_sums(const unsigned char* buf, int line, const LgTables& tb,
+                                            int lane) {
+  float2 r[2];
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    uint32_t w[16];
+    lds_half(buf, line, h, w);
+    if constexpr (InTraits<Tin>::kBf16) {
+      r[h] = half_sums_bf16(w, tb, lane);
+    } else {
+      r[h] = half_sums_f32(w, tb, lane);
+    }
   }
+  return add2(r[0], r[1]);
 }
 
 // ------------------------------------------------------------------ range and pretest
