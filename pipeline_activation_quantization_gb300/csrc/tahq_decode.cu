@@ -96,22 +96,30 @@ __device__ __forceinline__ uint32_t warp_chunk_bytes(const uint8_t* bits, long l
   return sum;
 }
 
-__device__ __forceinline__ unsigned long long pk(float2 a) {
-  return ((unsigned long long)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
-}
-__device__ __forceinline__ float2 upk(unsigned long long r) {
-  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
-}
-// (q0, q1) * s + z componentwise, each an fma rounded once (as fmaf).
+// Packed ops on register pairs (mov.b64 {lo, hi}): (q0, q1) * s + z componentwise, each an
+// fma rounded once (as fmaf); and the packed add.
 __device__ __forceinline__ float2 fma2(float2 q, float2 s, float2 z) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(q)), "l"(pk(s)), "l"(pk(z)));
-  return upk(d);
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(q.x), "f"(q.y), "f"(s.x), "f"(s.y), "f"(z.x), "f"(z.y));
+  return d;
 }
 __device__ __forceinline__ float2 addp(float2 a, float2 b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
-  return upk(d);
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 // The lane's 8 codes of b bits (b whole bytes at stage byte `start`), de-quantised.

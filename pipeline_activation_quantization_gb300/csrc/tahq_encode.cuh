@@ -114,6 +114,7 @@ struct EncParams {
   uint32_t seg_n;
   uint32_t seg[5][8];
   int lo, hi, h, flat_b;
+  int direct;  // compaction copies slots straight from scratch (16-byte aligned throughout)
   int slot_lo, slot_hi;
   uint32_t stage_lo_bytes;  // offset of the hi stage after the lo stage
   float c_h;
@@ -440,7 +441,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   const bool valid = kt < nt;
   // entropy key and histograms (§3.2)
   if (!flat) {
-    float2 ls = line_sums<Tin>(buf, line, s.tabs, lane);
+    float2 ls = line_sums<Tin>(buf, line, s.tabs, lg_consts(s.tabs, lane));
     ls = team_sum2<LPT>(ls);
     int cb = -1;
     if (valid && sub == 0) {
@@ -779,10 +780,12 @@ __device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
   } else {
     tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
   }
+  const long long b_lo = t0 * p.slot_lo, b_hi = t0 * p.slot_hi;
+  const uint32_t n_lo = (uint32_t)nt * p.slot_lo, n_hi = (uint32_t)nt * p.slot_hi;
   csync();
   if (threadIdx.x == 0) s.ndef = 0u;
-  store_stage(stage_lo, p.scratch_lo, t0 * p.slot_lo, nt * p.slot_lo);
-  store_stage(stage_hi, p.scratch_hi, t0 * p.slot_hi, nt * p.slot_hi);
+  store_stage(stage_lo, p.scratch_lo, b_lo, (int)n_lo);
+  store_stage(stage_hi, p.scratch_hi, b_hi, (int)n_hi);
   // the block's writes, ordered by the barrier, are published by one gpu-scope fence
   csync();
   if (threadIdx.x == 0) {
@@ -1020,14 +1023,17 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   const long long t0 = g * p.n_g + tl0;
   const unsigned long long prefix = __ldcg(&p.lookback[g * p.nC + cc]);
   const int slot_lo = p.slot_lo, slot_d = p.slot_hi - p.slot_lo;
+  const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
+  // each thread takes `per` consecutive tiles; a block scan gives their places
   constexpr int kPer = kMaxCC / kThreads;
+  const int per = (nt + kThreads - 1) / kThreads;
   uint32_t hiflags = 0u, cnt = 0u;
   uint8_t bl[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; j++) {
-    const int k = threadIdx.x * kPer + j;
+    const int k = threadIdx.x * per + j;
     bl[j] = 0;
-    if (k < nt) {
+    if (j < per && k < nt) {
       bl[j] = __ldcg(&p.bits[t0 + k]);
       if (bl[j] == (uint8_t)p.hi) {
         hiflags |= 1u << j;
@@ -1037,10 +1043,35 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   }
   uint32_t chunk_hi;
   uint32_t before = block_exclusive_scan<kThreads>(cnt, chunk_hi, s.scan);
+  if (p.direct) {
+    // slots and chunk bases on 16-byte boundaries: copy straight from scratch
+#pragma unroll
+    for (int j = 0; j < kPer; j++) {
+      const int k = threadIdx.x * per + j;
+      if (j < per && k < nt) {
+        const bool ishi = (hiflags >> j) & 1u;
+        const int sb = ishi ? p.slot_hi : slot_lo;
+        const long long o = base + (long long)k * slot_lo + (long long)before * slot_d;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            ishi ? p.scratch_hi + (t0 + k) * p.slot_hi : p.scratch_lo + (t0 + k) * slot_lo);
+        uint4* dst = reinterpret_cast<uint4*>(p.codes + o);
+        if (o + sb <= p.codes_bytes) {
+          for (int u = 0; u < sb / 16; u++) dst[u] = __ldcg(src + u);
+        } else {
+          set_status(p.status, kStSelectMismatch);  // only if the select went wrong
+        }
+        before += ishi ? 1u : 0u;
+      }
+    }
+    csync();
+    discard_lines(p.scratch_lo, t0 * slot_lo, (t0 + nt) * slot_lo);
+    discard_lines(p.scratch_hi, t0 * p.slot_hi, (t0 + nt) * p.slot_hi);
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < kPer; j++) {
-    const int k = threadIdx.x * kPer + j;
-    if (k < nt) {
+    const int k = threadIdx.x * per + j;
+    if (j < per && k < nt) {
       cbits[k] = bl[j];
       off[k] = (uint16_t)(k * slot_lo + before * slot_d);
       before += (hiflags >> j) & 1u;
@@ -1060,7 +1091,6 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
     gather_units<unsigned char>(off, cbits, p, t0, nt, stage);
   }
   csync();
-  const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
   int nbytes = nt * slot_lo + (int)chunk_hi * slot_d;
   if (base + nbytes > p.codes_bytes) {  // only if the select went wrong: never write past
     if (threadIdx.x == 0) set_status(p.status, kStSelectMismatch);
@@ -1286,6 +1316,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.c_h = a.c_h;
   p.slot_lo = G * a.lo / 8;
   p.slot_hi = G * a.hi / 8;
+  p.direct = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 1 : 0;
   p.codes = a.codes;
   p.scales = a.scales;
   p.zeros = a.zeros;

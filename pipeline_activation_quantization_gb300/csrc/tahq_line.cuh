@@ -27,9 +27,15 @@ struct LineGeom {
 };
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
-  return upk2(d);
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 __device__ __forceinline__ float min3f(float a, float b, float c) {
@@ -59,21 +65,40 @@ __device__ __forceinline__ void lds_line(const unsigned char* buf, int line, uin
 
 // ------------------------------------------------------------------ entropy sums
 
+// Constant operand pairs of the packed lg, built once in registers by the caller (read
+// per use from shared memory they cost more than the arithmetic itself).
+struct LgConsts {
+  float2 k2, k1, k0;  // polynomial coefficients, both halves
+  float2 m1;          // (-1, -1)
+  float2 c127;        // -(2^23 + 127): exponent field + 2^23 -> exponent
+  uint32_t lane4;     // lane * 4: column of the per-bank tables
+};
+
+__device__ __forceinline__ LgConsts lg_consts(const LgTables& tb, int lane) {
+  LgConsts c;
+  c.k2 = make_float2(tb.k[2], tb.k[2]);
+  c.k1 = make_float2(tb.k[1], tb.k[1]);
+  c.k0 = make_float2(tb.k[0], tb.k[0]);
+  c.m1 = make_float2(-1.0f, -1.0f);
+  c.c127 = make_float2(-8388735.0f, -8388735.0f);
+  c.lane4 = (uint32_t)lane << 2;
+  return c;
+}
+
 // lg of a pair of normal (or zero) magnitudes given as bits (tables g_lgT / g_lgR).  A
 // zero magnitude gives lg = -127 (its term m lg m is then a zero).
-__device__ __forceinline__ float2 lg_pair_f32(uint32_t a, uint32_t b, uint32_t lane4,
-                                              const LgTables& tb) {
+__device__ __forceinline__ float2 lg_pair_f32(uint32_t a, uint32_t b, const LgConsts& c) {
+  const uint32_t lane4 = c.lane4;
   const uint32_t oa = ((a >> 9) & 0x3F80u) | lane4, ob = ((b >> 9) & 0x3F80u) | lane4;
   const float2 F = make_float2(__uint_as_float((a >> 23) | 0x4B000000u),
                                __uint_as_float((b >> 23) | 0x4B000000u));
   const float2 mm = make_float2(__uint_as_float((a & 0x007FFFFFu) | 0x3F800000u),
                                 __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u));
-  const float2 r = fma2(mm, make_float2(lg_tab(g_lgR, oa), lg_tab(g_lgR, ob)),
-                        make_float2(-1.0f, -1.0f));
-  float2 p = fma2(make_float2(tb.k[2], tb.k[2]), r, make_float2(tb.k[1], tb.k[1]));
-  p = fma2(p, r, make_float2(tb.k[0], tb.k[0]));
+  const float2 r = fma2(mm, make_float2(lg_tab(g_lgR, oa), lg_tab(g_lgR, ob)), c.m1);
+  float2 p = fma2(c.k2, r, c.k1);
+  p = fma2(p, r, c.k0);
   const float2 t = fma2(p, r, make_float2(lg_tab(g_lgT, oa), lg_tab(g_lgT, ob)));
-  const float2 ef = add2(F, make_float2(-8388735.0f, -8388735.0f));  // exponent - 127, exact
+  const float2 ef = add2(F, c.c127);  // exponent - 127, exact
   return add2(ef, t);
 }
 
@@ -94,7 +119,8 @@ __device__ __forceinline__ void lds_half(const unsigned char* buf, int line, int
 // {L, S} of 16 fp32 values: L = pairwise sum of m_k, S = pairwise sum of the fused pairs
 // fmaf(m_2j+1, lg m_2j+1, RN(m_2j lg m_2j)); natural order.  Packed pairs (k, k + 8) keep
 // every level of the tree.
-__device__ __forceinline__ float2 half_sums_f32(const uint32_t* w, const LgTables& tb, int lane) {
+__device__ __forceinline__ float2 half_sums_f32(const uint32_t* w, const LgTables& tb,
+                                                const LgConsts& c) {
   uint32_t mb[16];
 #pragma unroll
   for (int k = 0; k < 16; k++) mb[k] = w[k] & 0x7FFFFFFFu;
@@ -105,11 +131,10 @@ __device__ __forceinline__ float2 half_sums_f32(const uint32_t* w, const LgTable
   mn = min(mn, mb[15]);
   float2 m2[8], l2[8];
   if (mn >= 0x00800000u) {
-    const uint32_t lane4 = (uint32_t)lane << 2;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
       m2[k] = make_float2(__uint_as_float(mb[k]), __uint_as_float(mb[k + 8]));
-      l2[k] = lg_pair_f32(mb[k], mb[k + 8], lane4, tb);
+      l2[k] = lg_pair_f32(mb[k], mb[k + 8], c);
     }
   } else {
 #pragma unroll
@@ -132,14 +157,15 @@ __device__ __forceinline__ float2 half_sums_f32(const uint32_t* w, const LgTable
 
 // {L, S} of 16 words of bf16 (32 values; word k holds values 2k (low half) and 2k + 1).
 // The lg of a bf16 magnitude is exact from the table: e + TB[top 7 fraction bits].
-__device__ __forceinline__ float2 half_sums_bf16(const uint32_t* w, const LgTables& tb, int lane) {
+__device__ __forceinline__ float2 half_sums_bf16(const uint32_t* w, const LgTables& tb,
+                                                 const LgConsts& c) {
   // any half-word with exponent field 0 (zero or subnormal)?  those take the general lg
   uint32_t em = 0xFFFFFFFFu;
 #pragma unroll
   for (int k = 0; k < 16; k++) em = __vminu2(em, w[k] & 0x7F807F80u);
   float2 L1[8], S1[8];
   if ((em & 0xFFFFu) != 0u && (em >> 16) != 0u) {
-    const uint32_t lane4 = (uint32_t)lane << 2;
+    const uint32_t lane4 = c.lane4;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
       const uint32_t a = w[k], b = w[k + 8];
@@ -155,9 +181,8 @@ __device__ __forceinline__ float2 half_sums_bf16(const uint32_t* w, const LgTabl
                                      lg_tab(g_lgTB, ((b << 7) & 0x3F80u) | lane4));
       const float2 thi = make_float2(lg_tab(g_lgTB, ((a >> 9) & 0x3F80u) | lane4),
                                      lg_tab(g_lgTB, ((b >> 9) & 0x3F80u) | lane4));
-      const float2 c127 = make_float2(-8388735.0f, -8388735.0f);
-      const float2 llo = add2(add2(elo, c127), tlo);
-      const float2 lhi = add2(add2(ehi, c127), thi);
+      const float2 llo = add2(add2(elo, c.c127), tlo);
+      const float2 lhi = add2(add2(ehi, c.c127), thi);
       L1[k] = add2(mlo, mhi);
       S1[k] = fma2(mhi, lhi, mul2(mlo, llo));
     }
@@ -187,16 +212,16 @@ __device__ __forceinline__ float2 half_sums_bf16(const uint32_t* w, const LgTabl
 // (half 0) + (half 1), each half pairwise in natural order.
 template <typename Tin>
 __device__ __forceinline__ float2 line_sums(const unsigned char* buf, int line, const LgTables& tb,
-                                            int lane) {
+                                            const LgConsts& c) {
   float2 r[2];
 #pragma unroll
   for (int h = 0; h < 2; h++) {
     uint32_t w[16];
     lds_half(buf, line, h, w);
     if constexpr (InTraits<Tin>::kBf16) {
-      r[h] = half_sums_bf16(w, tb, lane);
+      r[h] = half_sums_bf16(w, tb, c);
     } else {
-      r[h] = half_sums_f32(w, tb, lane);
+      r[h] = half_sums_f32(w, tb, c);
     }
   }
   return add2(r[0], r[1]);
@@ -276,8 +301,9 @@ __device__ __forceinline__ void sts_two(unsigned char* dst, unsigned long long f
 }
 
 // code bits (0x4B400000 + code) of a pair of values: fmaf(v - mn, inv, 1.5 * 2^23)
-__device__ __forceinline__ float2 qpair(float2 v, float2 nmn, float2 inv2) {
-  return fma2(add2(v, nmn), inv2, make_float2(12582912.0f, 12582912.0f));
+// (mg = the pair (1.5 * 2^23, 1.5 * 2^23))
+__device__ __forceinline__ float2 qpair(float2 v, float2 nmn, float2 inv2, float2 mg) {
+  return fma2(add2(v, nmn), inv2, mg);
 }
 
 // Quantise the lane's line with (mn, inv) at b bits and store its NE * b / 8 bytes.
@@ -285,6 +311,7 @@ template <typename Tin>
 __device__ __forceinline__ void line_quant_store(const uint32_t* w, float mn, float inv, int b,
                                                  unsigned char* dst) {
   const float2 nmn = make_float2(-mn, -mn), inv2 = make_float2(inv, inv);
+  const float2 mg = make_float2(12582912.0f, 12582912.0f);
   if constexpr (InTraits<Tin>::kBf16) {
     // 64 values: word k -> values 2k, 2k + 1; eight fields of 8 codes (4 words each)
 #pragma unroll
@@ -298,7 +325,7 @@ __device__ __forceinline__ void line_quant_store(const uint32_t* w, float mn, fl
         for (int k = 0; k < 4; k++) {
           const uint32_t x = w[4 * g + k];
           const float2 r = qpair(make_float2(__uint_as_float(x << 16),
-                                             __uint_as_float(x & 0xFFFF0000u)), nmn, inv2);
+                                             __uint_as_float(x & 0xFFFF0000u)), nmn, inv2, mg);
           q[2 * k] = __float_as_uint(r.x);
           q[2 * k + 1] = __float_as_uint(r.y);
         }
@@ -312,7 +339,7 @@ __device__ __forceinline__ void line_quant_store(const uint32_t* w, float mn, fl
 #pragma unroll
     for (int k = 0; k < 16; k++) {
       const float2 r = qpair(make_float2(__uint_as_float(w[k]), __uint_as_float(w[k + 16])),
-                             nmn, inv2);
+                             nmn, inv2, mg);
       q[k] = __float_as_uint(r.x);
       q[k + 16] = __float_as_uint(r.y);
     }
@@ -382,6 +409,7 @@ __device__ __forceinline__ void line_quant_store_ct(const uint32_t* w, float mn,
                                                     unsigned char* dst) {
   constexpr int NE = 128 / (int)sizeof(Tin), NF = NE / 8;
   const float2 nmn = make_float2(-mn, -mn), inv2 = make_float2(inv, inv);
+  const float2 mg = make_float2(12582912.0f, 12582912.0f);
   unsigned long long f[NF];
 #pragma unroll
   for (int g = 0; g < NF; g++) {
@@ -395,7 +423,7 @@ __device__ __forceinline__ void line_quant_store_ct(const uint32_t* w, float mn,
       } else {
         v = make_float2(__uint_as_float(w[8 * g + 2 * k]), __uint_as_float(w[8 * g + 2 * k + 1]));
       }
-      const float2 r = qpair(v, nmn, inv2);
+      const float2 r = qpair(v, nmn, inv2, mg);
       q[2 * k] = __float_as_uint(r.x);
       q[2 * k + 1] = __float_as_uint(r.y);
     }

@@ -53,22 +53,31 @@ __device__ __forceinline__ float lg_tab(const float* tab, uint32_t byte_off) {
 // add.  Products stay scalar (__fmul_rn): a packed multiply followed by an add was
 // measured to be fused into a single-rounding multiply-add on this target, which breaks
 // the canonical two-rounding order; an add followed by anything cannot be fused.
-__device__ __forceinline__ unsigned long long pk2(float2 a) {
-  return ((unsigned long long)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
-}
-__device__ __forceinline__ float2 upk2(unsigned long long r) {
-  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
-}
+// The two halves go to the instruction as a register pair (mov.b64 {lo, hi}), so the
+// compiler can place them without shifting or moving values around.
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
-  return upk2(d);
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 // Packed fused multiply-add: a * b + c per component, rounded once (as fmaf).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
-  return upk2(d);
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
 // Lane's words of tile kt from a staged chunk.
@@ -179,6 +188,7 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const LgTables& t
     }
   } else {
     float lgv[V], m[V];
+    const float k2 = tb.k[2], k1 = tb.k[1], k0 = tb.k[0];  // once, not per value
 #pragma unroll
     for (int j = 0; j < V; j++) {
       m[j] = fabsf(__uint_as_float(w[j]));
@@ -191,8 +201,8 @@ __device__ __forceinline__ float2 tile_sums(const uint32_t* w, const LgTables& t
         const float ef = __fsub_rn(__uint_as_float(0x4B000000u | E), 8388735.0f);
         const float mm = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
         const float r = __fmaf_rn(mm, lg_tab(g_lgR, off), -1.0f);
-        float p = __fmaf_rn(tb.k[2], r, tb.k[1]);
-        p = __fmaf_rn(p, r, tb.k[0]);
+        float p = __fmaf_rn(k2, r, k1);
+        p = __fmaf_rn(p, r, k0);
         lgv[j] = __fadd_rn(ef, __fmaf_rn(p, r, lg_tab(g_lgT, off)));
       }
     }
