@@ -56,6 +56,11 @@ def _workload(args) -> synth.Workload:
         kw["hblock"] = args.hblock
     if args.budget is not None:
         kw["budget"] = args.budget
+    if args.tokens:
+        T, S = args.tokens, w.tokens_per_group
+        shape = f"{T // S}x{S}x{w.channels}" if S else f"{T}x{w.channels}"
+        kw["tokens"] = T
+        kw["name"] = f"{w.name.split('_')[0]}_{shape}_{w.dtype}"
     return w.with_params(**kw) if kw else w
 
 
@@ -390,6 +395,8 @@ def main():
     ap.add_argument("--workload", default="c5", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tensors", type=int, default=0,
                     help="distinct seeded tensors cycled over the steps (default 3 for c5, else 1)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload on its first N tokens (a multiple of its token group)")
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--hblock", type=int, default=0)
     ap.add_argument("--budget", type=float, default=None)
