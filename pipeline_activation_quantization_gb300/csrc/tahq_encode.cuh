@@ -327,11 +327,30 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
   }
 }
 
-// Deferred tiles of the line layout, one block-wide list: teams of L = G / V2 lanes (V2 =
-// 4 fp32 or 8 bf16 values, one 16-byte unit per lane; a whole warp per fp32 tile of 128)
-// take list entries warp * TPW + team, + kWarps * TPW, ...: exact ratio test (eq. (3)),
-// pivot swap and Hadamard (eq. (4)) where it holds, range, and the slots of both widths
-// (8 / V2 lanes gather each group of 8 codes).
+// Warp-wide reductions of the redux unit (one instruction per warp).
+__device__ __forceinline__ float warp_max_abs(float x) {
+  float r;
+  asm("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float warp_max_f(float x) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float warp_min_f(float x) {
+  float r;
+  asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Deferred tiles of the line layout (the pretest could not rule out r > tau), one
+// block-wide list: teams of L = G / V lanes (V = 4 fp32 or 8 bf16 values, one 16-byte
+// unit per lane; a whole warp per fp32 tile of 128) take list entries warp * TPW + team,
+// + kWarps * TPW, ...  The main pass has already written every tile's slots and metadata
+// as untransformed; here the exact ratio test (eq. (3)) runs, and only the tiles it flags
+// get the pivot swap and Hadamard (eq. (4)), a new range and new slots of both widths
+// (8 / V lanes gather each group of 8 codes).
 template <typename Tin, int G>
 __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned char* buf,
                                            const uint16_t* list, int n, long long t0, bool flat,
@@ -364,40 +383,65 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
       v[2] = __uint_as_float(q.z);
       v[3] = __uint_as_float(q.w);
     }
-    float m1 = fabsf(v[0]), m2 = -1.0f;
-    int i1 = sub * V;
+    // top two magnitudes and the first arg-max of the tile
+    float m1, m2;
+    int i1;
+    if constexpr (L == 32) {
+      float la = fabsf(v[0]);
 #pragma unroll
-    for (int j = 1; j < V; j++) {
-      const float m = fabsf(v[j]);
-      if (m > m1) {
-        m2 = m1;
-        m1 = m;
-        i1 = sub * V + j;
-      } else if (m > m2) {
-        m2 = m;
+      for (int j = 1; j < V; j++) la = fmaxf(la, fabsf(v[j]));
+      m1 = warp_max_abs(la);
+      int jj = V;
+#pragma unroll
+      for (int j = V - 1; j >= 0; j--)
+        if (fabsf(v[j]) == m1) jj = j;
+      const unsigned hit = __ballot_sync(kFull, jj < V);
+      const int src = hit ? __ffs(hit) - 1 : 0;
+      i1 = __shfl_sync(kFull, lane * V + (jj < V ? jj : 0), src);
+      float l2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < V; j++)
+        if (lane * V + j != i1) l2 = fmaxf(l2, fabsf(v[j]));
+      m2 = warp_max_f(l2);
+    } else {
+      m1 = fabsf(v[0]);
+      m2 = -1.0f;
+      i1 = sub * V;
+#pragma unroll
+      for (int j = 1; j < V; j++) {
+        const float m = fabsf(v[j]);
+        if (m > m1) {
+          m2 = m1;
+          m1 = m;
+          i1 = sub * V + j;
+        } else if (m > m2) {
+          m2 = m;
+        }
       }
+      team_top2<L>(m1, i1, m2);
     }
-    team_top2<L>(m1, i1, m2);
     const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
-    if (__any_sync(kFull, flag)) {
-      float t[V];
+    if (!__any_sync(kFull, flag)) continue;  // the main pass's slots stand
+    float t[V];
 #pragma unroll
-      for (int j = 0; j < V; j++) t[j] = v[j];
-      team_swap0<V>(t, flag ? i1 : 0, sub, base);
-      team_fwht<V, L>(t, p.h, sub);
-      if (flag) {
+    for (int j = 0; j < V; j++) t[j] = v[j];
+    team_swap0<V>(t, flag ? i1 : 0, sub, base);
+    team_fwht<V, L>(t, p.h, sub);
 #pragma unroll
-        for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], p.c_h);
-      }
-    }
+    for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], p.c_h);
     float mn = v[0], mx = v[0];
 #pragma unroll
     for (int j = 1; j < V; j++) {
       mn = fminf(mn, v[j]);
       mx = fmaxf(mx, v[j]);
     }
-    mn = team_min<L>(mn);
-    mx = team_max<L>(mx);
+    if constexpr (L == 32) {
+      mn = warp_min_f(mn);
+      mx = warp_max_f(mx);
+    } else {
+      mn = team_min<L>(mn);
+      mx = team_max<L>(mx);
+    }
     const float D = __fsub_rn(mx, mn);
     // lane 0 of the team: Q_lo / D; lane 1: Q_hi / D (or D / Q_b in the one-width pass)
     const float num = sub == 1 ? (flat ? D : qmax_f(hi)) : qmax_f(lo);
@@ -419,10 +463,9 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
       }
       if constexpr (kGrp > 1) f |= __shfl_down_sync(kFull, f, 1) << (V * b);
       unsigned char* slot = (w2 ? stage_hi : stage_lo) + kt * (G * b / 8);
-      if (valid && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
+      if (flag && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
     }
-    if (valid && sub == 0)
-      put_meta(p, t0 + kt, mn, flag ? (uint8_t)i1 : (uint8_t)0xFF, flat ? r1 : D, flat);
+    if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, flat ? r1 : D, flat);
   }
 }
 
@@ -471,8 +514,10 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
 #pragma unroll
   for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
   cnt = team_sum_u<LPT>(cnt);
-  const bool tiny = !(m1 >= 0x1p-120f) || !(m1 <= FLT_MAX);
-  const bool deferred = tiny || cnt < 2u;
+  // a maximum below 2^-120 can never give r > tau (the ratio is below 1e-24); a tile whose
+  // maximum is not finite goes to the exact test
+  const bool small = m1 < 0x1p-120f;
+  const bool deferred = !small && (!(m1 <= FLT_MAX) || cnt < 2u);
 
   // widths: Q_lo / D and Q_hi / D (or D / Q_b), split over the team's lanes
   const int lo = kLo ? kLo : (flat ? p.flat_b : p.lo);
@@ -492,7 +537,8 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
     r1 = flat ? __fdiv_rn(D, qmax_f(lo)) : __fdiv_rn(qmax_f(hi), D);
   }
   if (!(D >= 0x1p-120f)) inv_lo = r1 = 0.0f;
-  if (valid && !deferred) {
+  // every tile as untransformed; the exact test below redoes the ones it flags
+  if (valid) {
     line_quant<Tin, kLo>(w, mn, inv_lo, lo, stage_lo + kt * (G * lo / 8) + sub * (NE * lo / 8));
     if (!flat)
       line_quant<Tin, kHi>(w, mn, r1, hi, stage_hi + kt * (G * hi / 8) + sub * (NE * hi / 8));
@@ -500,7 +546,8 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   }
   // tiles the pretest could not clear: one list for the block, teams of the whole block
   // take them in turn (outlier channels sit at fixed tile positions, so per-warp lists
-  // would load some warps far more than others)
+  // would load some warps far more than others).  The barrier also orders the main
+  // pass's slot writes before the exact path overwrites flagged slots.
   if (valid && deferred && sub == 0) s.dl[atomicAdd(&s.ndef, 1u)] = (uint16_t)kt;
   csync();
   pass2_line<Tin, G>(p, buf, s.dl, (int)s.ndef, t0, flat, lo, hi, stage_lo, stage_hi);
