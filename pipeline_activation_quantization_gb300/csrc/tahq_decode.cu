@@ -357,7 +357,9 @@ static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   const long long n_blocks = decode_blocks(G, a.n_tiles);
   k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks);
   k_dec_scan<<<1, 1024, 0, st>>>(a, n_blocks);
-  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 4, n_chunks));
+  // 6 blocks per SM: what registers (40) and shared memory allow, so that the blocks'
+  // load, scan and unpack phases overlap
+  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   k_decode<G><<<blocks, kDecThreads, 0, st>>>(a, n_chunks);
   return cudaGetLastError();
 }
