@@ -157,7 +157,7 @@ DecLayout dec_layout(const Shape& s) {
   L.ctot = off;
   off = align_up(off + 4 * (size_t)tahq::decode_chunks(s.G, s.n));
   L.bsum = off;
-  off = align_up(off + 8 * (size_t)tahq::decode_blocks(s.G, s.n));
+  off = align_up(off + 8 * ((size_t)tahq::decode_blocks(s.G, s.n) + 1));
   L.total = off;
   return L;
 }

@@ -70,7 +70,7 @@ struct DecCfg {
 template <int G>
 struct alignas(16) DecSmem {
   using C = DecCfg<G>;
-  uint32_t stage[C::kStage / 4];
+  uint32_t stage[2][C::kStage / 4];  // this chunk's bytes and the next one's, in flight
   float scale[C::CH], zero[C::CH];
   uint16_t off[C::CH];
   uint16_t flagged[C::CH];
@@ -216,19 +216,79 @@ __global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blo
     carry += s_w[32];
     __syncthreads();
   }
-  if (threadIdx.x == 0 && carry > a.codes_bytes) set_status(a.status, kStOverrun);
+  if (threadIdx.x == 0) {
+    a.bsum[n_blocks] = carry;  // the end of the last slot
+    if (carry > a.codes_bytes) set_status(a.status, kStOverrun);
+  }
+}
+
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), in the thread's
+// current copy group.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Start copying the bytes of chunk c (from the 16-byte boundary at or below its first
+// byte) into `stage`; returns that first byte's offset in the stage.  Bytes past
+// codes_bytes are never read (the last partial 16 bytes go by plain loads), and a chunk
+// longer than its largest possible size is cut (the offsets were corrupted).
+template <int G>
+__device__ __forceinline__ int issue_chunk_bytes(const DecodeArgs& a, long long c, long long n_chunks,
+                                                 long long n_blocks, uint32_t* stage) {
+  using C = DecCfg<G>;
+  auto start = [&](long long cc) {
+    return cc < n_chunks ? a.bsum[cc / kDecChunksPerBlock] + a.ctot[cc] : a.bsum[n_blocks];
+  };
+  const unsigned long long base = start(c), end = max(base, start(c + 1));
+  const int pad = (int)(base & 15ull);
+  const unsigned long long a0 = base - (unsigned long long)pad;
+  const unsigned long long bytes = min(end - base, (unsigned long long)(C::CH * G));
+  const int n16 = (pad + (int)bytes + 15) / 16;
+  const unsigned long long limit = a.codes_bytes;
+  for (int w16 = threadIdx.x; w16 < n16; w16 += kDecThreads) {
+    const unsigned long long gb = a0 + 16ull * w16;
+    if (gb + 16ull <= limit) {
+      cp_async16(stage + 4 * w16, a.codes + gb);
+    } else {
+      uint32_t tmp[4] = {0u, 0u, 0u, 0u};
+      for (int k = 0; k < 16; k++)
+        if (gb + k < limit) tmp[k >> 2] |= (uint32_t)a.codes[gb + k] << (8 * (k & 3));
+      reinterpret_cast<uint4*>(stage)[w16] = make_uint4(tmp[0], tmp[1], tmp[2], tmp[3]);
+    }
+  }
+  cp_async_commit();
+  return pad;
 }
 
 template <int G>
-__global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long n_chunks) {
+__global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long n_chunks,
+                                                        long long n_blocks) {
   using C = DecCfg<G>;
   constexpr int V = C::V, L = C::L, TPW = C::TPW, CH = C::CH, NS = C::NS;
-  __shared__ DecSmem<G> s;
+  extern __shared__ __align__(16) unsigned char dec_smem[];
+  DecSmem<G>& s = *reinterpret_cast<DecSmem<G>*>(dec_smem);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = lane / L, sub = lane % L;
   const unsigned long long limit = a.codes_bytes;
 
-  for (long long c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+  // the bytes of the block's first chunk; in each iteration the next chunk's bytes are
+  // copied while this one is unpacked
+  int slot = 0;
+  int pad = blockIdx.x < n_chunks ? issue_chunk_bytes<G>(a, blockIdx.x, n_chunks, n_blocks, s.stage[0]) : 0;
+  for (long long c = blockIdx.x; c < n_chunks; c += gridDim.x, slot ^= 1) {
+    const long long cn = c + gridDim.x;
+    int pad_next = 0;
+    if (cn < n_chunks) {
+      pad_next = issue_chunk_bytes<G>(a, cn, n_chunks, n_blocks, s.stage[slot ^ 1]);
+    } else {
+      cp_async_commit();  // an empty group keeps the wait below uniform
+    }
+    const uint32_t* stage = s.stage[slot];
     const long long t0 = c * CH;
     const int nt = (int)min((long long)CH, a.n_tiles - t0);
 
@@ -267,24 +327,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
     }
     // written by k_dec_totals and k_dec_scan
     const unsigned long long base = a.bsum[c / kDecChunksPerBlock] + a.ctot[c];
-    const int pad = (int)(base & 15ull);
-
-    // 3. stage [base, base + chunk_bytes), never reading past codes_bytes
-    const unsigned long long a0 = base - (unsigned long long)pad;
-    const int n16 = (pad + (int)chunk_bytes + 15) / 16;
-    for (int w16 = threadIdx.x; w16 < n16; w16 += kDecThreads) {
-      const unsigned long long gb = a0 + 16ull * w16;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (gb + 16ull <= limit) {
-        w = __ldg(reinterpret_cast<const uint4*>(a.codes + gb));
-      } else {
-        uint32_t tmp[4] = {0u, 0u, 0u, 0u};
-        for (int k = 0; k < 16; k++)
-          if (gb + k < limit) tmp[k >> 2] |= (uint32_t)a.codes[gb + k] << (8 * (k & 3));
-        w = make_uint4(tmp[0], tmp[1], tmp[2], tmp[3]);
-      }
-      reinterpret_cast<uint4*>(s.stage)[w16] = w;
-    }
+    (void)chunk_bytes;
+    cp_async_wait_prev();  // this chunk's bytes have landed
     __syncthreads();
 
     // 4. untransformed tiles; transformed ones are listed for the second pass
@@ -311,7 +355,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
       if (!valid || flag) continue;
       float v[V];
       if (ok) {
-        dequant8(s.stage, pad + (int)s.off[kt] + sub * b, b, s.scale[kt], s.zero[kt], v);
+        dequant8(stage, pad + (int)s.off[kt] + sub * b, b, s.scale[kt], s.zero[kt], v);
       } else {
 #pragma unroll
         for (int j = 0; j < V; j++) v[j] = 0.0f;
@@ -330,7 +374,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
       const int b = valid ? (int)s.bits[kt] : 1;
       const int piv = valid ? (int)s.piv[kt] : 0;
       float v[V];
-      dequant8(s.stage, valid ? pad + (int)s.off[kt] + sub * b : 0, b, valid ? s.scale[kt] : 0.0f,
+      dequant8(stage, valid ? pad + (int)s.off[kt] + sub * b : 0, b, valid ? s.scale[kt] : 0.0f,
                valid ? s.zero[kt] : 0.0f, v);
       team_fwht<V, L>(v, a.h, sub);
 #pragma unroll
@@ -343,6 +387,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
       }
     }
     __syncthreads();
+    pad = pad_next;
   }
 }
 
@@ -360,7 +405,10 @@ static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   // 6 blocks per SM: what registers (40) and shared memory allow, so that the blocks'
   // load, scan and unpack phases overlap
   const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
-  k_decode<G><<<blocks, kDecThreads, 0, st>>>(a, n_chunks);
+  const size_t smem = sizeof(DecSmem<G>);
+  const cudaError_t e = cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_decode<G><<<blocks, kDecThreads, smem, st>>>(a, n_chunks, n_blocks);
   return cudaGetLastError();
 }
 

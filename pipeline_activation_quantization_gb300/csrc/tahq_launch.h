@@ -59,7 +59,8 @@ struct DecodeArgs {
   uint32_t* status;
   uint32_t* ticket;
   uint32_t* ctot;                // [decode_chunks] chunk offset inside its block of 8 chunks
-  unsigned long long* bsum;      // [decode_blocks] stream offset of each block of 8 chunks
+  unsigned long long* bsum;      // [decode_blocks + 1] stream offset of each block of 8
+                                 // chunks, then the end of the last slot
 };
 
 // Encode geometry: bytes of input per tiles item; tiles per compaction chunk, at most.
