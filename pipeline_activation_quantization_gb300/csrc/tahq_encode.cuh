@@ -98,7 +98,7 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
   float ta[C::kArr], tb[C::kArr], tc[C::kArr];
   uint8_t piv[C::kArr];
   uint16_t dl[C::CH];  // deferred tiles (line: one list per block; narrow: per warp)
-  uint32_t ndef;       // line layout: length of dl
+  uint32_t ndef[2];    // line layout: length of dl, one counter per item parity
   uint32_t hist[kCoarseBins];
   uint32_t scan[kWarps + 4];
   unsigned long long bar[2];  // the slot's input chunk has landed
@@ -116,7 +116,6 @@ struct EncParams {
   int lo, hi, h, flat_b;
   int direct;  // compaction copies slots straight from scratch (16-byte aligned throughout)
   int slot_lo, slot_hi;
-  uint32_t stage_lo_bytes;  // offset of the hi stage after the lo stage
   float c_h;
   uint8_t* codes;
   float* scales;
@@ -475,7 +474,7 @@ template <typename Tin, int G, int kLo, int kHi>
 __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& p, long long g,
                                            long long t0, int nt, const unsigned char* buf,
                                            bool flat, unsigned char* stage_lo,
-                                           unsigned char* stage_hi) {
+                                           unsigned char* stage_hi, uint32_t* ndef) {
   using LG = LineGeom<Tin, G>;
   constexpr int LPT = LG::LPT, NE = LG::NE;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -548,9 +547,9 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   // take them in turn (outlier channels sit at fixed tile positions, so per-warp lists
   // would load some warps far more than others).  The barrier also orders the main
   // pass's slot writes before the exact path overwrites flagged slots.
-  if (valid && deferred && sub == 0) s.dl[atomicAdd(&s.ndef, 1u)] = (uint16_t)kt;
+  if (valid && deferred && sub == 0) s.dl[atomicAdd(ndef, 1u)] = (uint16_t)kt;
   csync();
-  pass2_line<Tin, G>(p, buf, s.dl, (int)s.ndef, t0, flat, lo, hi, stage_lo, stage_hi);
+  pass2_line<Tin, G>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi, stage_lo, stage_hi);
 }
 
 // ====================================================================== tiles: narrow layout
@@ -817,27 +816,18 @@ __device__ __forceinline__ void tiles_range(const EncParams& p, const Item& it, 
 // the scratch streams.
 template <typename Tin, int G, int kLo, int kHi>
 __device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
-                         const unsigned char* buf, unsigned char* stage_lo,
-                         unsigned char* stage_hi) {
+                         const unsigned char* buf, uint32_t* ndef) {
   long long t0;
   int nt;
   tiles_range<Tin, G>(p, it, t0, nt);
+  // slots go straight to the scratch streams (L2-resident; every warp writes whole
+  // contiguous runs); the caller publishes the item after its next barrier
+  unsigned char* out_lo = p.scratch_lo + t0 * p.slot_lo;
+  unsigned char* out_hi = p.scratch_hi + t0 * p.slot_hi;
   if constexpr (Cfg<Tin, G>::kLine) {
-    tiles_line<Tin, G, kLo, kHi>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
+    tiles_line<Tin, G, kLo, kHi>(s, p, it.g, t0, nt, buf, false, out_lo, out_hi, ndef);
   } else {
-    tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, stage_lo, stage_hi);
-  }
-  const long long b_lo = t0 * p.slot_lo, b_hi = t0 * p.slot_hi;
-  const uint32_t n_lo = (uint32_t)nt * p.slot_lo, n_hi = (uint32_t)nt * p.slot_hi;
-  csync();
-  if (threadIdx.x == 0) s.ndef = 0u;
-  store_stage(stage_lo, p.scratch_lo, b_lo, (int)n_lo);
-  store_stage(stage_hi, p.scratch_hi, b_hi, (int)n_hi);
-  // the block's writes, ordered by the barrier, are published by one gpu-scope fence
-  csync();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&p.doneA[it.g], 1u);
+    tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, out_lo, out_hi);
   }
 }
 
@@ -1056,6 +1046,88 @@ __device__ __forceinline__ void discard_lines(const uint8_t* base, long long a, 
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(base + l * 128) : "memory");
 }
 
+// Compaction with 16-byte slots and stream (the common case): every warp owns whole
+// segments of 32 tiles of the chunk and needs no other warp.  The hi tiles before its
+// segment come from ballots over the chunk's width bytes; a tile's place from a ballot
+// over its own segment; every lane then issues up to four 16-byte loads before its
+// stores, and the warp drops its segment's scratch lines from L2.
+static __device__ void compact_direct(const EncParams& p, long long g, long long cc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long tl0 = cc * p.CHC;
+  const int nt = (int)min(p.CHC, p.n_g - tl0);
+  const int nseg = (nt + 31) >> 5;
+  if (warp >= nseg) return;
+  if (lane == 0) wait_counter(&p.selready[g], 2u, p.status);
+  __syncwarp();
+  const long long t0 = g * p.n_g + tl0;
+  const uint8_t hi = (uint8_t)p.hi;
+  const int slot_lo = p.slot_lo, slot_hi = p.slot_hi, slot_d = slot_hi - slot_lo;
+  const int UH = slot_hi >> 4, UL = slot_lo >> 4;
+  const long long base = g * p.group_bytes + tl0 * slot_lo +
+                         (long long)__ldcg(&p.lookback[g * p.nC + cc]) * slot_d;
+  uint32_t before = 0u;  // hi tiles of the chunk in segments [0, j)
+  int j = 0;
+  for (int seg = warp; seg < nseg; seg += kWarps) {
+    // segments j .. seg, eight at a time: loads first, then the ballots
+    uint32_t mask = 0u;
+    while (j <= seg) {
+      uint8_t v[8];
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        const int k = 32 * (j + q) + lane;
+        v[q] = (j + q <= seg && k < nt) ? __ldcg(&p.bits[t0 + k]) : (uint8_t)0;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        const uint32_t m = __ballot_sync(kFull, v[q] == hi);
+        if (j + q < seg) before += (uint32_t)__popc(m);
+        if (j + q == seg) mask = m;
+      }
+      j += 8;
+    }
+    const int nv = min(32, nt - 32 * seg);
+    const long long st0 = t0 + 32 * seg;  // the segment's first tile
+    const long long ob = base + 32ll * seg * slot_lo + (long long)before * slot_d;
+    for (int r0 = 0; r0 < UH; r0 += 4) {
+      uint4 val[4];
+      long long dst[4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const int i = lane + 32 * (r0 + q);
+        const int kt = i / UH, u = i - kt * UH;  // kt < 32 whenever r0 + q < UH
+        const bool ishi = r0 + q < UH && kt < nv && ((mask >> (kt & 31)) & 1u);
+        dst[q] = -1;
+        if (r0 + q < UH && kt < nv && (ishi || u < UL)) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              ishi ? p.scratch_hi + (st0 + kt) * slot_hi : p.scratch_lo + (st0 + kt) * slot_lo);
+          val[q] = __ldcg(src + u);
+          dst[q] = ob + (long long)kt * slot_lo +
+                   (long long)__popc(mask & ((1u << kt) - 1u)) * slot_d + 16 * u;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        if (dst[q] < 0) continue;
+        if (dst[q] + 16 <= p.codes_bytes) {
+          *reinterpret_cast<uint4*>(p.codes + dst[q]) = val[q];
+        } else {
+          set_status(p.status, kStSelectMismatch);  // only if the select went wrong
+        }
+      }
+    }
+    before += (uint32_t)__popc(mask);
+    j = seg + 1;
+    __syncwarp();
+    // 32 slots of 16-byte multiples are whole 128-byte lines
+    const long long lo0 = (st0 * slot_lo + 127) / 128, lo1 = (st0 + nv) * slot_lo / 128;
+    const long long hi0 = (st0 * slot_hi + 127) / 128, hi1 = (st0 + nv) * slot_hi / 128;
+    for (long long l = lo0 + lane; l < lo1; l += 32)
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_lo + l * 128) : "memory");
+    for (long long l = hi0 + lane; l < hi1; l += 32)
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_hi + l * 128) : "memory");
+  }
+}
+
 // ---- compaction item: widths from the offsets items, slots from scratch, the chunk's
 // place in the stream from the prefix of hi counts.  `stage` holds
 // the chunk's bytes, `off` / `cbits` (CHC entries each) every tile's place and width.
@@ -1063,6 +1135,10 @@ template <typename Tin, int G>
 __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
                            unsigned char* stage, uint16_t* off, uint8_t* cbits) {
   const long long g = it.g, cc = it.idx;
+  if (p.direct) {
+    compact_direct(p, g, cc);
+    return;
+  }
   if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status);
   csync();
   const long long tl0 = cc * p.CHC;
@@ -1090,31 +1166,6 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   }
   uint32_t chunk_hi;
   uint32_t before = block_exclusive_scan<kThreads>(cnt, chunk_hi, s.scan);
-  if (p.direct) {
-    // slots and chunk bases on 16-byte boundaries: copy straight from scratch
-#pragma unroll
-    for (int j = 0; j < kPer; j++) {
-      const int k = threadIdx.x * per + j;
-      if (j < per && k < nt) {
-        const bool ishi = (hiflags >> j) & 1u;
-        const int sb = ishi ? p.slot_hi : slot_lo;
-        const long long o = base + (long long)k * slot_lo + (long long)before * slot_d;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            ishi ? p.scratch_hi + (t0 + k) * p.slot_hi : p.scratch_lo + (t0 + k) * slot_lo);
-        uint4* dst = reinterpret_cast<uint4*>(p.codes + o);
-        if (o + sb <= p.codes_bytes) {
-          for (int u = 0; u < sb / 16; u++) dst[u] = __ldcg(src + u);
-        } else {
-          set_status(p.status, kStSelectMismatch);  // only if the select went wrong
-        }
-        before += ishi ? 1u : 0u;
-      }
-    }
-    csync();
-    discard_lines(p.scratch_lo, t0 * slot_lo, (t0 + nt) * slot_lo);
-    discard_lines(p.scratch_hi, t0 * p.slot_hi, (t0 + nt) * p.slot_hi);
-    return;
-  }
 #pragma unroll
   for (int j = 0; j < kPer; j++) {
     const int k = threadIdx.x * per + j;
@@ -1196,7 +1247,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
   unsigned char* stage_lo = reinterpret_cast<unsigned char*>(&s) + sizeof(EncSmem<Tin, G>);
-  unsigned char* stage_hi = stage_lo + p.stage_lo_bytes;
   init_tables<Tin, G>(s, p.tabs);
   for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) s.hist[i] = 0u;
   const unsigned long long pol = policy_evict_first();  // the input is read once
@@ -1220,16 +1270,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     mbar_init(&s.bar[0], 1);
     mbar_init(&s.bar[1], 1);
     fence_barrier_init();
-    s.ndef = 0u;
+    s.ndef[0] = s.ndef[1] = 0u;
     start(record(atomicAdd(p.ticket, 1u)), 0);
     tk1 = atomicAdd(p.ticket, 1u);
     rec1 = record(tk1);
     tk2 = atomicAdd(p.ticket, 1u);
   }
   uint32_t parity = 0u;  // bit s = phase parity of buffer s
+  long long done_g = -1;  // thread 0: group of a tiles item not yet published
   for (int slot = 0;; slot ^= 1) {
     csync();  // everyone is done with the previous item, its buffer and shared state
     if (threadIdx.x == 0) {
+      if (done_g >= 0) {
+        // the block's slot and metadata writes, ordered by the barrier, are published by
+        // one gpu-scope fence
+        __threadfence();
+        atomicAdd(&p.doneA[done_g], 1u);
+        done_g = -1;
+      }
+      s.ndef[slot ^ 1] = 0u;  // the previous item's list is consumed
       // a block holds up to four tickets and works through them in order; items only
       // wait for smaller tickets, so the smallest item in work never waits for an item
       // that has not started
@@ -1245,9 +1304,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     if (it.type == kItemTiles) {
       mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
       parity ^= 1u << slot;
-      do_tiles<Tin, G, kLo, kHi>(s, p, it, s.buf[slot], stage_lo, stage_hi);
+      do_tiles<Tin, G, kLo, kHi>(s, p, it, s.buf[slot], &s.ndef[slot]);
+      done_g = it.g;
     } else if (it.type == kItemCompact) {
-      // the tiles stages are free during a compaction: they hold its per-tile arrays
       do_compact<Tin, G>(s, p, it, s.buf[slot], reinterpret_cast<uint16_t*>(stage_lo),
                          stage_lo + 2 * kMaxCC);
     } else if (it.type == kItemSelect) {
@@ -1265,14 +1324,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
   using C = Cfg<Tin, G>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
-  unsigned char* stage = reinterpret_cast<unsigned char*>(&s) + sizeof(EncSmem<Tin, G>);
   if (threadIdx.x == 0) {
     mbar_init(&s.bar[0], 1);
     mbar_init(&s.bar[1], 1);
     fence_barrier_init();
-    s.ndef = 0u;
+    s.ndef[0] = s.ndef[1] = 0u;
   }
-  csync();
   const unsigned long long pol = policy_evict_first();
   uint32_t parity = 0u;
   const int slot_b = G * p.flat_b / 8;
@@ -1281,24 +1338,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
   if (threadIdx.x == 0 && c < n_chunks)
     issue_chunk<Tin, G>(s, p, c * C::CH, (int)min((long long)C::CH, p.n_tiles - c * C::CH), 0, pol);
   for (; c < n_chunks; c += gridDim.x) {
+    // everyone is done with the previous chunk: its buffer and list are free
+    csync();
     const long long nx = c + gridDim.x;
-    if (threadIdx.x == 0 && nx < n_chunks)
-      issue_chunk<Tin, G>(s, p, nx * C::CH, (int)min((long long)C::CH, p.n_tiles - nx * C::CH),
-                          slot ^ 1, pol);
+    if (threadIdx.x == 0) {
+      s.ndef[slot ^ 1] = 0u;
+      if (nx < n_chunks)
+        issue_chunk<Tin, G>(s, p, nx * C::CH, (int)min((long long)C::CH, p.n_tiles - nx * C::CH),
+                            slot ^ 1, pol);
+    }
     const long long t0 = c * C::CH;
     const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
     mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
     parity ^= 1u << slot;
-    csync();
+    // one width: tile t's slot is at t * slot_b in the stream
+    unsigned char* out = p.codes + t0 * slot_b;
     if constexpr (C::kLine) {
-      tiles_line<Tin, G, kB, 0>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
+      tiles_line<Tin, G, kB, 0>(s, p, 0, t0, nt, s.buf[slot], true, out, out, &s.ndef[slot]);
     } else {
-      tiles_narrow<Tin, G>(s, p, 0, t0, nt, s.buf[slot], true, stage, stage);
+      tiles_narrow<Tin, G>(s, p, 0, t0, nt, s.buf[slot], true, out, out);
     }
-    csync();
-    if (threadIdx.x == 0) s.ndef = 0u;
-    store_stage(stage, p.codes, t0 * slot_b, nt * slot_b);
-    csync();
     slot ^= 1;
   }
 }
@@ -1393,11 +1452,8 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   const int grid_cap = a.num_sms * 2;
   const bool flat = a.K == 0 || a.K == a.n_g;
   p.flat_b = a.K == 0 ? a.lo : a.hi;
-  const int b_first = flat ? p.flat_b : a.lo;
-  p.stage_lo_bytes = (uint32_t)((C::CH * G * b_first / 8 + 64 + 127) / 128 * 128);
-  const uint32_t stage_hi_bytes = flat ? 0u : (uint32_t)(C::CH * G * a.hi / 8 + 64);
-  // the stages also hold a compaction chunk's per-tile arrays (3 bytes per tile)
-  const size_t stages = std::max<size_t>(p.stage_lo_bytes + stage_hi_bytes, flat ? 0 : 3 * kMaxCC);
+  // a compaction chunk's per-tile arrays (3 bytes per tile) follow the shared state
+  const size_t stages = flat ? 0 : 3 * kMaxCC;
   const size_t smem = sizeof(EncSmem<Tin, G>) + 1024 + stages;
   if (flat) {
     void (*kern)(EncParams, long long) = k_encode_flat<Tin, G, 0>;
