@@ -485,7 +485,6 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   if (!flat) {
     float2 ls = line_sums<Tin>(buf, line, s.tabs, lg_consts(s.tabs, lane));
     ls = team_sum2<LPT>(ls);
-    int cb = -1;
     if (valid && sub == 0) {
       const float H = entropy_key(ls.x, ls.y, s.tabs);
       p.keys[t0 + kt] = H;
@@ -493,11 +492,10 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
         set_status(p.status, kStNonFinite);
       const int b = fine_bin(H);
       atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
-      cb = b >> 8;
+      // the coarse bins of a group's tiles are few (similar entropies): count them in
+      // the block first, one global add per bin and item below
+      atomicAdd(&s.hist[b >> 8], 1u);
     }
-    const unsigned same = __match_any_sync(kFull, cb);
-    if (cb >= 0 && lane == __ffs(same) - 1)
-      atomicAdd(&p.hist_coarse[g * kCoarseBins + cb], (uint32_t)__popc(same));
   }
 
   // range and the two-values pretest
@@ -549,6 +547,14 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   // pass's slot writes before the exact path overwrites flagged slots.
   if (valid && deferred && sub == 0) s.dl[atomicAdd(ndef, 1u)] = (uint16_t)kt;
   csync();
+  if (!flat) {
+    static_assert(kThreads == kCoarseBins, "one coarse bin per thread");
+    const uint32_t c = s.hist[threadIdx.x];
+    if (c) {
+      atomicAdd(&p.hist_coarse[g * kCoarseBins + threadIdx.x], c);
+      s.hist[threadIdx.x] = 0u;  // bins are all zero between items
+    }
+  }
   pass2_line<Tin, G>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi, stage_lo, stage_hi);
 }
 
