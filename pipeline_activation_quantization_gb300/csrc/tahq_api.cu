@@ -93,7 +93,7 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
 
 struct EncLayout {
   size_t status, ticket, cand_cnt, doneA, doneB, doneB2, selready, sel, hist_coarse, hist_fine, lookback,
-      ctrl_end, keys, cand, scratch_lo, scratch_hi, items, items_cap, total;
+      ctrl_end, keys, cand, segmask, scratch_lo, scratch_hi, items, items_cap, total;
 };
 
 // Offset words are sized for the input type that needs the most compaction chunks.
@@ -129,6 +129,8 @@ EncLayout enc_layout(const Shape& s) {
   off = align_up(off + 4 * (size_t)s.n);
   L.cand = off;
   off = align_up(off + 8 * (size_t)s.n);
+  L.segmask = off;
+  off = align_up(off + 4 * (size_t)s.n_groups * (size_t)((s.n_g + 31) / 32));
   // every tile quantised at both widths, fixed slots (read back by the compaction)
   L.scratch_lo = off;
   off = align_up(off + (size_t)s.n * (size_t)(s.G * s.lo / 8));
@@ -263,6 +265,7 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.lookback = at<unsigned long long>(workspace, L.lookback);
   a.keys = at<float>(workspace, L.keys);
   a.cand = at<unsigned long long>(workspace, L.cand);
+  a.segmask = at<uint32_t>(workspace, L.segmask);
   a.scratch_lo = at<uint8_t>(workspace, L.scratch_lo);
   a.scratch_hi = at<uint8_t>(workspace, L.scratch_hi);
   a.items = at<unsigned long long>(workspace, L.items);

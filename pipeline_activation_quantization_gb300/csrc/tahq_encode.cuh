@@ -57,6 +57,7 @@ constexpr int kChunkBytes = kEncChunkBytes;
 constexpr uint8_t kDeferred = 0xFE;  // narrow layout: pass-1 marker of a tile left to pass 2
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kDirectCC = 1024;  // tiles per compaction chunk of the direct path (<= 64 segments)
 constexpr int kMaxCC = kEncMaxCC;     // tiles per compaction chunk, at most
 constexpr int kRankMax = 2048;        // candidates ranked in one pass (else radix select)
 
@@ -126,6 +127,7 @@ struct EncParams {
   uint8_t* scratch_hi;
   float* keys;
   unsigned long long* cand;
+  uint32_t* segmask;  // per group, per 32-tile segment: bit k = tile k is hi
   uint32_t* cand_cnt;
   uint32_t* hist_coarse;
   uint32_t* hist_fine;
@@ -874,21 +876,26 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
   const float* kg = p.keys + g * p.n_g;
   unsigned long long* cg = p.cand + g * p.n_g;
   const int lane = threadIdx.x & 31;
-  for (long long base = lo; base < hi; base += kThreads) {
-    const long long i = base + threadIdx.x;
-    float hv = 0.0f;
-    bool hit = false;
-    if (i < hi) {
-      hv = __ldcg(&kg[i]);
-      hit = fine_bin(hv) == bstar;
+  constexpr int kB = 8;  // keys in flight per thread
+  for (long long base = lo; base < hi; base += kB * kThreads) {
+    float hv[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long i = base + u * kThreads + threadIdx.x;
+      hv[u] = i < hi ? __ldcg(&kg[i]) : 0.0f;
     }
-    const unsigned mask = __ballot_sync(kFull, hit);
-    if (mask) {
-      uint32_t pos0 = 0;
-      const int leader = __ffs(mask) - 1;
-      if (lane == leader) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)__popc(mask));
-      pos0 = __shfl_sync(kFull, pos0, leader);
-      if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv, (uint32_t)i);
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long i = base + u * kThreads + threadIdx.x;
+      const bool hit = i < hi && fine_bin(hv[u]) == bstar;
+      const unsigned mask = __ballot_sync(kFull, hit);
+      if (mask) {
+        uint32_t pos0 = 0;
+        const int leader = __ffs(mask) - 1;
+        if (lane == leader) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)__popc(mask));
+        pos0 = __shfl_sync(kFull, pos0, leader);
+        if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv[u], (uint32_t)i);
+      }
     }
   }
   csync();
@@ -973,25 +980,47 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   unsigned long long* words = p.lookback + g * p.nC;
   const long long per = (p.nC + p.J - 1) / p.J;
   const long long c0 = it.idx * per, c1 = min(p.nC, c0 + per);
-  // every thread one tile at a time; a warp's 32 tiles lie in one compaction chunk
-  // (chunks hold a multiple of 32 tiles), whose hi count collects in s.hist[c - c0]
+  // every thread one tile at a time, eight tiles' loads in flight; a warp's 32 tiles are
+  // one segment of one compaction chunk (chunks hold a multiple of 32 tiles): its hi mask
+  // goes to segmask, its hi count to the chunk's count in s.hist[c - c0]
   const long long tl_begin = c0 * p.CHC, tl_end = min(p.n_g, c1 * p.CHC);
   const int lane = threadIdx.x & 31;
-  for (long long tb = tl_begin; tb < tl_end; tb += kThreads) {
-    const long long tl = tb + threadIdx.x;
-    bool ishi = false;
-    if (tl < tl_end) {
-      const long long t = g * p.n_g + tl;
-      ishi = mode == kSelAll;
-      if (mode == kSelThreshold) ishi = rank_key(__ldcg(&p.keys[t]), (uint32_t)tl) >= theta;
-      const int b = ishi ? p.hi : p.lo;
-      p.bits[t] = (uint8_t)b;
-      // the range D left by the tiles pass becomes the scale D / Q
-      const float D = __ldcg(&p.scales[t]);
-      p.scales[t] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
+  const uint32_t chc = (uint32_t)p.CHC;
+  uint32_t* segmask = p.segmask + g * ((p.n_g + 31) / 32);
+  constexpr int kB = 8;
+  for (long long tb = tl_begin; tb < tl_end; tb += kB * kThreads) {
+    float key[kB], Dv[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long tl = tb + u * kThreads + threadIdx.x;
+      key[u] = 0.0f;
+      Dv[u] = 0.0f;
+      if (tl < tl_end) {
+        const long long t = g * p.n_g + tl;
+        if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t]);
+        Dv[u] = __ldcg(&p.scales[t]);
+      }
     }
-    const unsigned hm = __ballot_sync(kFull, ishi);
-    if (lane == 0 && hm) atomicAdd(&s.hist[(int)((tb + (threadIdx.x & ~31)) / p.CHC - c0)], (uint32_t)__popc(hm));
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long tw = tb + u * kThreads + (threadIdx.x & ~31);  // the warp's segment
+      const long long tl = tw + lane;
+      bool ishi = false;
+      if (tl < tl_end) {
+        const long long t = g * p.n_g + tl;
+        ishi = mode == kSelAll ||
+               (mode == kSelThreshold && rank_key(key[u], (uint32_t)tl) >= theta);
+        const int b = ishi ? p.hi : p.lo;
+        p.bits[t] = (uint8_t)b;
+        // the range D left by the tiles pass becomes the scale D / Q
+        p.scales[t] = (Dv[u] >= 0x1p-120f) ? __fdiv_rn(Dv[u], qmax_f(b)) : 0.0f;
+      }
+      const unsigned hm = __ballot_sync(kFull, ishi);
+      if (lane == 0 && tw < tl_end) {
+        segmask[tw >> 5] = hm;
+        if (hm) atomicAdd(&s.hist[(uint32_t)(tw - tl_begin) / chc], (uint32_t)__popc(hm));
+      }
+    }
   }
   csync();
   for (long long c = c0 + threadIdx.x; c < c1; c += kThreads) {
@@ -1053,10 +1082,11 @@ __device__ __forceinline__ void discard_lines(const uint8_t* base, long long a, 
 }
 
 // Compaction with 16-byte slots and stream (the common case): every warp owns whole
-// segments of 32 tiles of the chunk and needs no other warp.  The hi tiles before its
-// segment come from ballots over the chunk's width bytes; a tile's place from a ballot
-// over its own segment; every lane then issues up to four 16-byte loads before its
-// stores, and the warp drops its segment's scratch lines from L2.
+// segments of 32 tiles of the chunk and needs no other warp.  The offsets items left
+// each segment's hi mask; one load of the chunk's masks (two per lane, at most 64
+// segments) and a warp scan of their counts give every segment's place, the mask every
+// tile's.  Each lane then has up to eight 16-byte loads (two segments) in flight before
+// its stores, and the warp drops its segments' scratch lines from L2.
 static __device__ void compact_direct(const EncParams& p, long long g, long long cc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long tl0 = cc * p.CHC;
@@ -1066,71 +1096,84 @@ static __device__ void compact_direct(const EncParams& p, long long g, long long
   if (lane == 0) wait_counter(&p.selready[g], 2u, p.status);
   __syncwarp();
   const long long t0 = g * p.n_g + tl0;
-  const uint8_t hi = (uint8_t)p.hi;
+  const uint32_t* sm = p.segmask + g * ((p.n_g + 31) / 32) + (tl0 >> 5);
+  const uint32_t m0 = lane < nseg ? __ldcg(sm + lane) : 0u;
+  const uint32_t m1 = lane + 32 < nseg ? __ldcg(sm + lane + 32) : 0u;
+  const unsigned long long prefix = __ldcg(&p.lookback[g * p.nC + cc]);
+  // hi tiles of the chunk before segment lane (e0) and lane + 32 (e1)
+  const uint32_t c0 = (uint32_t)__popc(m0), c1 = (uint32_t)__popc(m1);
+  uint32_t e0 = c0, e1 = c1;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t a = __shfl_up_sync(kFull, e0, d), b = __shfl_up_sync(kFull, e1, d);
+    if (lane >= d) {
+      e0 += a;
+      e1 += b;
+    }
+  }
+  e1 += __shfl_sync(kFull, e0, 31) - c1;
+  e0 -= c0;
   const int slot_lo = p.slot_lo, slot_hi = p.slot_hi, slot_d = slot_hi - slot_lo;
   const int UH = slot_hi >> 4, UL = slot_lo >> 4;
-  const long long base = g * p.group_bytes + tl0 * slot_lo +
-                         (long long)__ldcg(&p.lookback[g * p.nC + cc]) * slot_d;
-  uint32_t before = 0u;  // hi tiles of the chunk in segments [0, j)
-  int j = 0;
-  for (int seg = warp; seg < nseg; seg += kWarps) {
-    // segments j .. seg, eight at a time: loads first, then the ballots
-    uint32_t mask = 0u;
-    while (j <= seg) {
-      uint8_t v[8];
+  const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
+  for (int sa = warp; sa < nseg; sa += 2 * kWarps) {
+    uint32_t mask[2];
+    long long ob[2], st0[2];
+    int nv[2];
 #pragma unroll
-      for (int q = 0; q < 8; q++) {
-        const int k = 32 * (j + q) + lane;
-        v[q] = (j + q <= seg && k < nt) ? __ldcg(&p.bits[t0 + k]) : (uint8_t)0;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; q++) {
-        const uint32_t m = __ballot_sync(kFull, v[q] == hi);
-        if (j + q < seg) before += (uint32_t)__popc(m);
-        if (j + q == seg) mask = m;
-      }
-      j += 8;
+    for (int h = 0; h < 2; h++) {
+      const int seg = sa + h * kWarps;           // warp-uniform
+      const int sx = seg < nseg ? seg : sa;
+      mask[h] = __shfl_sync(kFull, sx < 32 ? m0 : m1, sx & 31);
+      const uint32_t before = __shfl_sync(kFull, sx < 32 ? e0 : e1, sx & 31);
+      nv[h] = seg < nseg ? min(32, nt - 32 * seg) : 0;
+      st0[h] = t0 + 32 * seg;  // the segment's first tile
+      ob[h] = base + 32ll * seg * slot_lo + (long long)before * slot_d;
     }
-    const int nv = min(32, nt - 32 * seg);
-    const long long st0 = t0 + 32 * seg;  // the segment's first tile
-    const long long ob = base + 32ll * seg * slot_lo + (long long)before * slot_d;
     for (int r0 = 0; r0 < UH; r0 += 4) {
-      uint4 val[4];
-      long long dst[4];
+      uint4 val[2][4];
+      long long dst[2][4];
 #pragma unroll
-      for (int q = 0; q < 4; q++) {
-        const int i = lane + 32 * (r0 + q);
-        const int kt = i / UH, u = i - kt * UH;  // kt < 32 whenever r0 + q < UH
-        const bool ishi = r0 + q < UH && kt < nv && ((mask >> (kt & 31)) & 1u);
-        dst[q] = -1;
-        if (r0 + q < UH && kt < nv && (ishi || u < UL)) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              ishi ? p.scratch_hi + (st0 + kt) * slot_hi : p.scratch_lo + (st0 + kt) * slot_lo);
-          val[q] = __ldcg(src + u);
-          dst[q] = ob + (long long)kt * slot_lo +
-                   (long long)__popc(mask & ((1u << kt) - 1u)) * slot_d + 16 * u;
+      for (int h = 0; h < 2; h++) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const int i = lane + 32 * (r0 + q);
+          const int kt = i / UH, u = i - kt * UH;  // kt < 32 whenever r0 + q < UH
+          const bool in = r0 + q < UH && kt < nv[h];
+          const bool ishi = in && ((mask[h] >> (kt & 31)) & 1u);
+          dst[h][q] = -1;
+          if (in && (ishi || u < UL)) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                ishi ? p.scratch_hi + (st0[h] + kt) * slot_hi : p.scratch_lo + (st0[h] + kt) * slot_lo);
+            val[h][q] = __ldcg(src + u);
+            dst[h][q] = ob[h] + (long long)kt * slot_lo +
+                        (long long)__popc(mask[h] & ((1u << kt) - 1u)) * slot_d + 16 * u;
+          }
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; q++) {
-        if (dst[q] < 0) continue;
-        if (dst[q] + 16 <= p.codes_bytes) {
-          *reinterpret_cast<uint4*>(p.codes + dst[q]) = val[q];
-        } else {
-          set_status(p.status, kStSelectMismatch);  // only if the select went wrong
+      for (int h = 0; h < 2; h++) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (dst[h][q] < 0) continue;
+          if (dst[h][q] + 16 <= p.codes_bytes) {
+            *reinterpret_cast<uint4*>(p.codes + dst[h][q]) = val[h][q];
+          } else {
+            set_status(p.status, kStSelectMismatch);  // only if the select went wrong
+          }
         }
       }
     }
-    before += (uint32_t)__popc(mask);
-    j = seg + 1;
     __syncwarp();
     // 32 slots of 16-byte multiples are whole 128-byte lines
-    const long long lo0 = (st0 * slot_lo + 127) / 128, lo1 = (st0 + nv) * slot_lo / 128;
-    const long long hi0 = (st0 * slot_hi + 127) / 128, hi1 = (st0 + nv) * slot_hi / 128;
-    for (long long l = lo0 + lane; l < lo1; l += 32)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_lo + l * 128) : "memory");
-    for (long long l = hi0 + lane; l < hi1; l += 32)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_hi + l * 128) : "memory");
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const long long a = st0[h], b = st0[h] + nv[h];
+      for (long long l = (a * slot_lo + 127) / 128 + lane; l < b * slot_lo / 128; l += 32)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_lo + l * 128) : "memory");
+      for (long long l = (a * slot_hi + 127) / 128 + lane; l < b * slot_hi / 128; l += 32)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_hi + l * 128) : "memory");
+    }
   }
 }
 
@@ -1439,6 +1482,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.keys = a.keys;
   p.cand = a.cand;
   p.cand_cnt = a.cand_cnt;
+  p.segmask = a.segmask;
   p.hist_coarse = a.hist_coarse;
   p.hist_fine = a.hist_fine;
   p.doneA = a.doneA;
@@ -1476,6 +1520,9 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   }
   p.nA = (a.n_g + C::CH - 1) / C::CH;
   p.CHC = encode_cchunk_tiles(C::kBf16, G, a.hi);
+  // the direct compaction needs no stage: larger chunks, fewer items (never more chunks
+  // than the workspace sizing assumes)
+  if (p.direct) p.CHC = std::max<long long>(p.CHC, kDirectCC);
   p.nC = (a.n_g + p.CHC - 1) / p.CHC;
   // keep the scratch of three (or, for big groups, two) groups in L2 between a group's
   // tiles pass and its compaction

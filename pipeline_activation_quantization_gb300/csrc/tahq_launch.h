@@ -38,6 +38,7 @@ struct EncodeArgs {
   unsigned long long* lookback;  // [encode_chunks] compaction chunk counts, then offsets
   float* keys;               // [n_tiles]
   unsigned long long* cand;  // [n_tiles]
+  uint32_t* segmask;         // [n_groups * ceil(n_g / 32)] hi tiles of each 32-tile segment
   uint8_t* scratch_lo;       // [n_tiles * G * lo / 8] every tile quantised at bits_lo
   uint8_t* scratch_hi;       // [n_tiles * G * hi / 8] every tile quantised at bits_hi
   unsigned long long* items; // [items_cap] the decoded work queue
