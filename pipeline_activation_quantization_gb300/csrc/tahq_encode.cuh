@@ -345,21 +345,43 @@ __device__ __forceinline__ float warp_min_f(float x) {
   return r;
 }
 
+// Values a lane takes in the exact path of the line layout: more values a lane means
+// fewer shuffle stages and team reductions per tile and 32 / (G / V) tiles per warp step.
+// One lane's codes at the wider width must fit 64 bits (widths known at compile time,
+// else up to 8 bits), and a team has at least two lanes.
+constexpr int kP2Target = 8;
+template <typename Tin, int G, int kLo, int kHi>
+__host__ __device__ constexpr int p2_values() {
+  const int vpu = InTraits<Tin>::kBf16 ? 8 : 4;
+  const int bmax = (kLo > 0 && kHi > 0) ? (kLo > kHi ? kLo : kHi) : 8;
+  int v = kP2Target < vpu ? vpu : kP2Target;
+  while (v > vpu && (v * bmax > 64 || G / v < 2)) v /= 2;
+  return v;
+}
+
 // Deferred tiles of the line layout (the pretest could not rule out r > tau), one
-// block-wide list: teams of L = G / V lanes (V = 4 fp32 or 8 bf16 values, one 16-byte
-// unit per lane; a whole warp per fp32 tile of 128) take list entries warp * TPW + team,
-// + kWarps * TPW, ...  The main pass has already written every tile's slots and metadata
-// as untransformed; here the exact ratio test (eq. (3)) runs, and only the tiles it flags
-// get the pivot swap and Hadamard (eq. (4)), a new range and new slots of both widths
-// (8 / V lanes gather each group of 8 codes).
-template <typename Tin, int G>
+// block-wide list: teams of L = G / V lanes (V consecutive values a lane, in 16-byte
+// units of the line) take list entries warp * TPW + team, + kWarps * TPW, ...  The main
+// pass has already written every tile's slots and metadata as untransformed; here the
+// exact ratio test (eq. (3)) runs, and only the tiles it flags get the pivot swap and
+// Hadamard (eq. (4)), a new range and new slots of both widths.  V * bits <= 64 (one
+// lane's codes in one 64-bit word); for V < 8, 8 / V lanes gather each group of 8 codes.
+//
+// The ratio test RN(m1 / d) > 2 with d = RN(m2 + 1e-12) >= 1e-12 needs no division: it
+// holds iff m1 / d > 2 + 2^-23 (ties round to 2), i.e. m1 / 2 - d > d 2^-24.  m1 / 2 is
+// exact, m1 / 2 - d is exact by Sterbenz's lemma where it matters (d <= m1 <= 4 d; below,
+// it is negative; above, it rounds to at least d), and d 2^-24 is a normal number.
+template <typename Tin, int G, int V>
 __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned char* buf,
                                            const uint16_t* list, int n, long long t0, bool flat,
                                            int lo, int hi, unsigned char* stage_lo,
                                            unsigned char* stage_hi) {
   constexpr bool kBf = InTraits<Tin>::kBf16;
-  constexpr int V = kBf ? 8 : 4, L = G / V, TPW = 32 / L, LPT = LineGeom<Tin, G>::LPT;
-  constexpr int kGrp = 8 / V;  // lanes per group of 8 codes
+  constexpr int VPU = kBf ? 8 : 4;  // values per 16-byte unit
+  constexpr int NU = V / VPU;       // units per lane
+  constexpr int L = G / V, TPW = 32 / L, LPT = LineGeom<Tin, G>::LPT;
+  constexpr int kGrp = V < 8 ? 8 / V : 1;  // lanes per group of 8 codes
+  static_assert(NU >= 1 && 8 % NU == 0, "whole 16-byte units of one line");
   static_assert(L >= 2 && L <= 32, "team of 2..32 lanes");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = lane / L, sub = lane % L, base = lane - sub;
@@ -368,21 +390,24 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
     const int ci = j0 + team;
     const bool valid = ci < n;
     const int kt = valid ? (int)list[ci] : 0;
-    const int line = kt * LPT + (sub >> 3);
-    const uint4 q = *reinterpret_cast<const uint4*>(buf + line * 128 + (((sub & 7) ^ (line & 7)) << 4));
+    const int u0 = sub * NU;  // the lane's first unit in the tile
+    const int line = kt * LPT + (u0 >> 3);
     float v[V];
-    if constexpr (kBf) {
-      const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        v[2 * k] = __uint_as_float(wq[k] << 16);
-        v[2 * k + 1] = __uint_as_float(wq[k] & 0xFFFF0000u);
+    for (int k = 0; k < NU; k++) {
+      const int ju = (u0 & 7) + k;
+      const uint4 q = *reinterpret_cast<const uint4*>(buf + line * 128 + ((ju ^ (line & 7)) << 4));
+      const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+      if constexpr (kBf) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          v[8 * k + 2 * e] = __uint_as_float(wq[e] << 16);
+          v[8 * k + 2 * e + 1] = __uint_as_float(wq[e] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; e++) v[4 * k + e] = __uint_as_float(wq[e]);
       }
-    } else {
-      v[0] = __uint_as_float(q.x);
-      v[1] = __uint_as_float(q.y);
-      v[2] = __uint_as_float(q.z);
-      v[3] = __uint_as_float(q.w);
     }
     // top two magnitudes and the first arg-max of the tile
     float m1, m2;
@@ -421,7 +446,8 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
       }
       team_top2<L>(m1, i1, m2);
     }
-    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+    const float d = __fadd_rn(m2, 1e-12f);
+    const bool flag = valid && __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f);
     if (!__any_sync(kFull, flag)) continue;  // the main pass's slots stand
     float t[V];
 #pragma unroll
@@ -462,9 +488,13 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
         const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
         f |= (unsigned long long)(__float_as_uint(c) - 0x4B400000u) << (j * b);
       }
-      if constexpr (kGrp > 1) f |= __shfl_down_sync(kFull, f, 1) << (V * b);
       unsigned char* slot = (w2 ? stage_hi : stage_lo) + kt * (G * b / 8);
-      if (flag && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
+      if constexpr (kGrp > 1) {
+        f |= __shfl_down_sync(kFull, f, 1) << (V * b);
+        if (flag && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
+      } else {
+        if (flag) sts_bytes(slot + sub * (V * b / 8), f, 0ull, V * b / 8);
+      }
     }
     if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, flat ? r1 : D, flat);
   }
@@ -557,7 +587,8 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
       s.hist[threadIdx.x] = 0u;  // bins are all zero between items
     }
   }
-  pass2_line<Tin, G>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi, stage_lo, stage_hi);
+  pass2_line<Tin, G, p2_values<Tin, G, kLo, kHi>()>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi,
+                                                    stage_lo, stage_hi);
 }
 
 // ====================================================================== tiles: narrow layout
