@@ -184,6 +184,36 @@ def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0) -> dict:
                       f"single-threaded scalar C (-O2 -ffp-contract=off), {dt:.1f} s"}
 
 
+def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0) -> dict:
+    """The same oracle with its token groups (encode) and token ranges (decode) on all host
+    cores, whole tensor per step."""
+    import oracle
+    cores = os.cpu_count() or 1
+    S = w.tokens_per_group or w.tokens
+    used = max(1, min(cores, w.tokens // S))
+
+    def step():
+        r = oracle.encode(x, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, threads=cores)
+        oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], w.tokens,
+                      w.channels, w.tile, w.hblock, threads=cores)
+
+    t0 = time.perf_counter()
+    step()
+    one = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        step()
+    dt = time.perf_counter() - t0
+    toks = reps * w.tokens
+    gbs = toks * w.channels * (4 if w.dtype == "f32" else 2) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "tokens_per_s": round(toks / dt, 1),
+            "sample": f"{reps} x the whole tensor ({w.tokens} tokens) encoded+decoded, "
+                      f"{used} token groups on {used} of {cores} host threads "
+                      f"(scalar C, -O2 -ffp-contract=off), {dt:.1f} s"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -356,6 +386,7 @@ def run_gpu(args):
     if rank != 0:
         return 0
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, x_np)
+    cpu_all = None if args.no_cpu_baseline or world > 1 else cpu_baseline_all_cores(w, x_np)
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
@@ -376,7 +407,7 @@ def run_gpu(args):
                      "frac": round(dom[1] / (dom[2] * 1e-3) / 1e9 / peak, 4),
                      "traffic": _traffic_for(dom_name, w.name)},
         "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+        "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e, "gpu_launches": launches * args.steps,
         "gpu_launches_per_step": launches, "clocks": clocks,
         "wall_s_timed_loop": round(t_wall, 3),
     }

@@ -54,6 +54,7 @@ def lib():
                 "oracle_entropy_key": (f32, [p, i32]),
                 "oracle_entropy_literal": (C.c_double, [p, i32, C.c_double, C.c_double]),
                 "oracle_outlier": (None, [p, i32, p, p, p, p]),
+                "oracle_outlier_tau": (None, [p, i32, f32, p, p, p, p]),
                 "oracle_fwht": (None, [p, i32]),
                 "oracle_transform": (None, [p, i32, i32, i32]),
                 "oracle_inverse_transform": (None, [p, i32, i32, i32]),
@@ -66,6 +67,8 @@ def lib():
                 "oracle_payload_size": (i64, [i64, i64, i32, i32, i32, f32, i64]),
                 "oracle_encode": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64,
                                         p, p, p, p, p, p, p]),
+                "oracle_encode_tau": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
+                                            p, p, p, p, p, p, p]),
                 "oracle_decode": (i32, [p, i64, p, p, p, p, i64, i64, i32, i32, p]),
             }
             for name, (res, args) in sig.items():
@@ -114,12 +117,16 @@ def entropy_literal(a, eps: float = 1e-12, vsig: float = 1e-12) -> float:
     return float(lib().oracle_entropy_literal(_ptr(a), a.size, eps, vsig))
 
 
-def outlier(a):
-    """-> (pivot, flag, m1, m2) of one tile."""
+def outlier(a, tau: float | None = None):
+    """-> (pivot, flag, m1, m2) of one tile; flag = r > tau (the method's 2.0 by default)."""
     a = _f32(a)
     d, f = C.c_int(), C.c_int()
     m1, m2 = C.c_float(), C.c_float()
-    lib().oracle_outlier(_ptr(a), a.size, C.byref(d), C.byref(f), C.byref(m1), C.byref(m2))
+    if tau is None:
+        lib().oracle_outlier(_ptr(a), a.size, C.byref(d), C.byref(f), C.byref(m1), C.byref(m2))
+    else:
+        lib().oracle_outlier_tau(_ptr(a), a.size, float(tau), C.byref(d), C.byref(f),
+                                 C.byref(m1), C.byref(m2))
     return d.value, f.value, m1.value, m2.value
 
 
@@ -190,12 +197,14 @@ def payload_size(T, Cc, G, lo, hi, budget, S) -> int:
 # ------------------------------------------------------------------------ whole tensor
 
 def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: int = 0,
-           threads: int = 1, want_keys: bool = False, want_near: bool = False) -> dict:
+           threads: int = 1, want_keys: bool = False, want_near: bool = False,
+           tau: float | None = None) -> dict:
     """Encode ``x`` ([T, C] float32, or uint16 bf16 bit patterns).
 
     Returns a dict with ``codes, scales, zeros, bits, pivots`` (and ``keys`` [n_tiles]
     float32 entropy keys, ``near`` [T, C] boundary flags when asked).  With
-    ``threads > 1`` the independent token groups run on host threads.
+    ``threads > 1`` the independent token groups run on host threads.  ``tau`` is the
+    outlier threshold (None: the method's 2.0).
     """
     x = np.ascontiguousarray(x)
     dtype = BF16 if x.dtype == np.uint16 else F32
@@ -226,8 +235,11 @@ def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: in
 
     def run(g):
         sl = slice(g * n_g, (g + 1) * n_g)
-        rc = lib().oracle_encode(
-            _ptr(x[g * S:(g + 1) * S]), dtype, S, Cc, G, h, lo, hi, budget, S,
+        args = (_ptr(x[g * S:(g + 1) * S]), dtype, S, Cc, G, h, lo, hi, budget, S)
+        if tau is not None:
+            args = args + (float(tau),)
+        rc = (lib().oracle_encode if tau is None else lib().oracle_encode_tau)(
+            *args,
             _ptr(out["codes"][g * gbytes:(g + 1) * gbytes]), _ptr(out["scales"][sl]),
             _ptr(out["zeros"][sl]), _ptr(out["bits"][sl]), _ptr(out["pivots"][sl]),
             _ptr(out["keys"][sl]) if want_keys else None,

@@ -167,8 +167,10 @@ double oracle_entropy_literal(const float *a, int G, double eps, double vsig)
 }
 
 /* Top-2 magnitudes, pivot d (lowest index among equal maxima) and the outlier flag
- * r = m1 / (m2 + 1e-12f) > 2.0f. */
-void oracle_outlier(const float *a, int G, int *pivot, int *flag, float *m1_out, float *m2_out)
+ * r = m1 / (m2 + 1e-12f) > tau, r an IEEE fp32 division.  Appendix F of the pages varies
+ * tau: 0 transforms every tile (every tile whose r is above zero), +inf none. */
+void oracle_outlier_tau(const float *a, int G, float tau, int *pivot, int *flag,
+                        float *m1_out, float *m2_out)
 {
     int d = 0;
     float m1 = fabsf(a[0]);
@@ -179,9 +181,15 @@ void oracle_outlier(const float *a, int G, int *pivot, int *flag, float *m1_out,
         if (k != d && fabsf(a[k]) > m2) m2 = fabsf(a[k]);
     float r = m1 / (m2 + 1e-12f);
     *pivot = d;
-    *flag = (r > 2.0f) ? 1 : 0;
+    *flag = (r > tau) ? 1 : 0;
     if (m1_out) *m1_out = m1;
     if (m2_out) *m2_out = m2;
+}
+
+/* The method's own threshold, tau = 2.0 (§3.3). */
+void oracle_outlier(const float *a, int G, int *pivot, int *flag, float *m1_out, float *m2_out)
+{
+    oracle_outlier_tau(a, G, 2.0f, pivot, flag, m1_out, m2_out);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -372,13 +380,15 @@ static void load_tile(const void *x, int dtype, int64_t off, int G, float *a)
     }
 }
 
-/* Encode a [T, C] tensor.  keys (n_tiles floats) and near (T*C bytes) are optional
- * outputs for tests.  Returns 0, or -1 on invalid arguments / allocation failure. */
-int oracle_encode(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo, int hi,
-                  float budget, int64_t S, uint8_t *codes, float *scales, float *zeros,
-                  uint8_t *bits, uint8_t *pivots, float *keys, uint8_t *near)
+/* Encode a [T, C] tensor with outlier threshold tau (>= 0, +inf allowed).  keys (n_tiles
+ * floats) and near (T*C bytes) are optional outputs for tests.  Returns 0, or -1 on
+ * invalid arguments / allocation failure. */
+int oracle_encode_tau(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo,
+                      int hi, float budget, int64_t S, float tau, uint8_t *codes, float *scales,
+                      float *zeros, uint8_t *bits, uint8_t *pivots, float *keys, uint8_t *near)
 {
     if (!valid_shape(T, C, G, h) || !valid_bits(lo, hi, budget)) return -1;
+    if (!(tau >= 0.0f)) return -1;  /* negative or NaN */
     if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
     if (S == 0) S = T;
     if (T == 0) return 0;
@@ -394,7 +404,7 @@ int oracle_encode(const void *x, int dtype, int64_t T, int64_t C, int G, int h, 
     for (int64_t t = 0; t < n; t++) {
         load_tile(x, dtype, t * G, G, a);
         int d, flag;
-        oracle_outlier(a, G, &d, &flag, NULL, NULL);
+        oracle_outlier_tau(a, G, tau, &d, &flag, NULL, NULL);
         H[t] = oracle_entropy_key(a, G);
         piv[t] = flag ? d : -1;
     }
@@ -420,6 +430,15 @@ int oracle_encode(const void *x, int dtype, int64_t T, int64_t C, int G, int h, 
     if (!keys) free(H);
     free(piv);
     return 0;
+}
+
+/* The method as the pages state it: tau = 2.0 (§3.3). */
+int oracle_encode(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo, int hi,
+                  float budget, int64_t S, uint8_t *codes, float *scales, float *zeros,
+                  uint8_t *bits, uint8_t *pivots, float *keys, uint8_t *near)
+{
+    return oracle_encode_tau(x, dtype, T, C, G, h, lo, hi, budget, S, 2.0f, codes, scales,
+                             zeros, bits, pivots, keys, near);
 }
 
 /* Decode into fp32 [T, C].  Returns 0, or -1 on invalid arguments / a bit width outside

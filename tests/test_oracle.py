@@ -467,3 +467,92 @@ def test_invalid_arguments_rejected():
         oracle.encode(x, 64, 64, 3, 4, 4.5, 0)      # budget above hi
     with pytest.raises(ValueError):
         oracle.encode(x, 64, 64, 3, 4, 3.5, 3)      # group does not divide tokens
+
+
+# ------------------------------------------------------------------ the threshold tau
+# (Appendix F: tau = 0 transforms every tile, tau = inf none, tau = 4 fewer than 2)
+
+def test_outlier_tau_cases():
+    a = np.zeros(64, F32)
+    a[5], a[20] = 3.0, 1.0                       # r = 3 / (1 + 1e-12) rounds to 3.0
+    assert oracle.outlier(a, 2.9)[:2] == (5, 1)
+    assert oracle.outlier(a, 3.0)[:2] == (5, 0)  # strict: r == tau is no outlier
+    assert oracle.outlier(a, 4.0)[:2] == (5, 0)
+    assert oracle.outlier(a, 0.0)[:2] == (5, 1)
+    assert oracle.outlier(a, np.inf)[:2] == (5, 0)
+    assert oracle.outlier(np.zeros(64, F32), 0.0)[:2] == (0, 0)   # r = 0: not > 0
+    c = np.zeros(64, F32)
+    c[63] = 1e30                                 # r = 1e42 overflows to inf: inf > inf is false
+    assert oracle.outlier(c, np.inf)[:2] == (63, 0)
+    assert oracle.outlier(c, 3.4e38)[:2] == (63, 1)
+
+
+@pytest.mark.parametrize("G,h,S", [(64, 64, 16), (32, 16, 0), (8, 8, 12)])
+def test_encode_tau(G, h, S):
+    x = _small()
+    T, Cc = x.shape
+    tiles = x.reshape(-1, G)
+    base = oracle.encode(x, G, h, 3, 4, 3.5, S)
+    same = oracle.encode(x, G, h, 3, 4, 3.5, S, tau=2.0)
+    for k in base:
+        assert np.array_equal(base[k], same[k]), k
+    mags = np.abs(tiles)
+    first = np.argmax(mags, axis=1)
+    flagged = {}
+    for tau in (0.0, 1.5, 2.0, 4.0, np.inf):
+        r = oracle.encode(x, G, h, 3, 4, 3.5, S, tau=tau)
+        assert np.array_equal(r["bits"], base["bits"])      # the statistics use the raw tile
+        f = r["pivots"] != 255
+        assert np.array_equal(r["pivots"][f], first[f])
+        flagged[tau] = f
+        y = oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], T, Cc, G, h)
+        err = np.linalg.norm((y - x).reshape(-1, G).astype(np.float64), axis=1)
+        tol = np.sqrt(G) * 0.5 * r["scales"].astype(np.float64) * (1 + 1e-3) + 1e-5 * mags.max(axis=1)
+        assert np.all(err <= tol + 1e-30)
+    assert np.array_equal(flagged[0.0], mags.max(axis=1) > 0)   # every nonzero tile
+    assert not flagged[np.inf].any()
+    assert np.all(flagged[4.0] <= flagged[2.0]) and np.all(flagged[2.0] <= flagged[1.5])
+    assert np.all(flagged[1.5] <= flagged[0.0])
+    assert flagged[2.0].any() and (flagged[0.0] & ~flagged[2.0]).any()
+
+
+def test_encode_tau_untransformed_tiles_match_the_plain_quantizer():
+    # tau = inf: every tile is quantised as it is; the codes of tile t are those of the
+    # tile-level quantizer and packer applied to the raw tile
+    x = _small()[:, :256]
+    G = 64
+    r = oracle.encode(x, G, G, 3, 4, 3.5, 0, tau=np.inf)
+    off = 0
+    for t, a in enumerate(x.reshape(-1, G)):
+        b = int(r["bits"][t])
+        q, s, z, _ = oracle.quantize_tile(a, b)
+        assert s == r["scales"][t] and z == r["zeros"][t]
+        assert np.array_equal(oracle.pack_tile(q, b), r["codes"][off:off + G * b // 8])
+        off += G * b // 8
+
+
+def test_invalid_tau_rejected():
+    x = _small()
+    for tau in (-1.0, np.nan):
+        with pytest.raises(RuntimeError):
+            oracle.encode(x, 64, 64, 3, 4, 3.5, 0, tau=tau)
+
+
+# ------------------------------------------------------------------ width mixes
+# (Appendix G: 100% INT4, 50% INT4 + 50% INT3, 100% INT3; 80% INT2 + 20% INT3)
+
+@pytest.mark.parametrize("lo,hi,beta,frac_hi", [(3, 4, 4.0, 1.0), (3, 4, 3.5, 0.5),
+                                                 (3, 4, 3.0, 0.0), (2, 3, 2.2, 0.2)])
+def test_appendix_g_width_mixes(lo, hi, beta, frac_hi):
+    x = _small()
+    T, Cc = x.shape
+    G = 64
+    r = oracle.encode(x, G, G, lo, hi, beta, 16)
+    n_g = 16 * Cc // G
+    K = int(np.floor(frac_hi * n_g + 1e-9))
+    for g in range(T // 16):
+        assert np.count_nonzero(r["bits"][g * n_g:(g + 1) * n_g] == hi) == K
+    n = T * Cc // G
+    n_hi = np.count_nonzero(r["bits"] == hi)
+    assert r["codes"].size == (n * lo + n_hi * (hi - lo)) * G // 8
+    assert r["codes"].size * 8 <= beta * T * Cc
