@@ -64,11 +64,13 @@ def _workload(args) -> synth.Workload:
     return w.with_params(**kw) if kw else w
 
 
-def _config(w: synth.Workload, extra=None) -> dict:
+def _config(w: synth.Workload, extra=None, tau=None) -> dict:
     c = {"workload": w.name, "tokens": w.tokens, "channels": w.channels, "input_dtype": w.dtype,
          "tile": w.tile, "hblock": w.hblock, "bits": [w.bits_lo, w.bits_hi], "budget": w.budget,
          "tokens_per_group": w.tokens_per_group, "seed": w.seed,
          "l2": "flushed between steps (256 MiB write, outside the events)"}
+    if tau is not None:
+        c["tau"] = tau
     if extra:
         c.update(extra)
     return c
@@ -156,25 +158,25 @@ def _src_sha() -> str:
 
 # ------------------------------------------------------------------ the oracle (CPU)
 
-def _oracle_step(x, w, tokens):
+def _oracle_step(x, w, tokens, tau=None):
     import oracle
     xs = x[:tokens]
     S = min(w.tokens_per_group or w.tokens, tokens)
-    r = oracle.encode(xs, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S)
+    r = oracle.encode(xs, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, tau=tau)
     oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], tokens, w.channels,
                   w.tile, w.hblock)
 
 
-def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0) -> dict:
+def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0, tau=None) -> dict:
     """The oracle, single thread, on whole token groups of the same tensor."""
     S = w.tokens_per_group or w.tokens
     t0 = time.perf_counter()
-    _oracle_step(x, w, S)
+    _oracle_step(x, w, S, tau)
     one = time.perf_counter() - t0
     groups = max(1, min(w.tokens // S, int(target_s / max(one, 1e-3))))
     t0 = time.perf_counter()
     for g in range(groups):
-        _oracle_step(x[g * S:], w, S)
+        _oracle_step(x[g * S:], w, S, tau)
     dt = time.perf_counter() - t0
     toks = groups * S
     gbs = toks * w.channels * (4 if w.dtype == "f32" else 2) / dt / 1e9
@@ -184,7 +186,7 @@ def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0) -> dict:
                       f"single-threaded scalar C (-O2 -ffp-contract=off), {dt:.1f} s"}
 
 
-def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0) -> dict:
+def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0, tau=None) -> dict:
     """The same oracle with its token groups (encode) and token ranges (decode) on all host
     cores, whole tensor per step."""
     import oracle
@@ -193,7 +195,8 @@ def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0) -> dict:
     used = max(1, min(cores, w.tokens // S))
 
     def step():
-        r = oracle.encode(x, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, threads=cores)
+        r = oracle.encode(x, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, threads=cores,
+                          tau=tau)
         oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], w.tokens,
                       w.channels, w.tile, w.hblock, threads=cores)
 
@@ -223,15 +226,15 @@ def run_reference(args):
     S = w.tokens_per_group or w.tokens
     # size each step's sample so that warm-up + timed steps take about 90 s of host time
     t0 = time.perf_counter()
-    _oracle_step(x, w, 16)
+    _oracle_step(x, w, 16, args.tau)
     per_token = (time.perf_counter() - t0) / 16
     tok = int(max(1, min(S, 90.0 / max(1, args.steps + args.warmup) / max(per_token, 1e-9))))
     for _ in range(args.warmup):
-        _oracle_step(x, w, tok)
+        _oracle_step(x, w, tok, args.tau)
     t0 = time.perf_counter()
     for k in range(args.steps):
         g = k % max(1, w.tokens // tok)
-        _oracle_step(x[g * tok:], w, tok)
+        _oracle_step(x[g * tok:], w, tok, args.tau)
     dt = time.perf_counter() - t0
     in_b = tok * w.channels * (4 if w.dtype == "f32" else 2)
     gbs = in_b * args.steps / dt / 1e9
@@ -240,7 +243,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config(w, {"sample_tokens_per_step": tok}),
+        "config": _config(w, {"sample_tokens_per_step": tok}, tau=args.tau),
         "tokens_per_s": round(tok * args.steps / dt, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step encodes+decodes {tok} consecutive tokens of the "
@@ -291,7 +294,7 @@ def run_gpu(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     with torch.cuda.stream(stream):
-        enc = tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
+        enc = tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group, tau=args.tau)
         y = tq.decode(enc, T, C, G, h)
         dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8, device=dev)
     payload = enc["payload_bytes"]
@@ -309,7 +312,7 @@ def run_gpu(args):
     def step(ev, k=0):
         ev[0].record(stream)
         tq.encode(xs[k % n_tensors], G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
-                  out=out_bufs, workspace=ws, stream=stream)
+                  out=out_bufs, workspace=ws, stream=stream, tau=args.tau)
         ev[1].record(stream)
         tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
         ev[2].record(stream)
@@ -367,7 +370,7 @@ def run_gpu(args):
                 else:
                     x_dev.copy_(x_host, non_blocking=True)
                 tq.encode(x_dev, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
-                          out=out_bufs, workspace=ws, stream=stream)
+                          out=out_bufs, workspace=ws, stream=stream, tau=args.tau)
                 tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
                 y_host.copy_(y, non_blocking=True)
             e2e_step()
@@ -385,15 +388,17 @@ def run_gpu(args):
 
     if rank != 0:
         return 0
-    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, x_np)
-    cpu_all = None if args.no_cpu_baseline or world > 1 else cpu_baseline_all_cores(w, x_np)
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, x_np, tau=args.tau)
+    cpu_all = (None if args.no_cpu_baseline or world > 1
+               else cpu_baseline_all_cores(w, x_np, tau=args.tau))
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}",
-                                                     "fresh_tensors_cycled": n_tensors}),
+                                                     "fresh_tensors_cycled": n_tensors},
+                                                  tau=args.tau),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
         "encode": {"ms": round(e_ms, 5), "alg_bytes": enc_b, "GB_s": round(enc_gbs, 2),
@@ -405,7 +410,7 @@ def run_gpu(args):
                      "achieved": round(dom[1] / (dom[2] * 1e-3) / 1e9, 2), "peak": peak,
                      "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
                      "frac": round(dom[1] / (dom[2] * 1e-3) / 1e9 / peak, 4),
-                     "traffic": _traffic_for(dom_name, w.name)},
+                     "traffic": _traffic_for(dom_name, w.name) if args.tau is None else None},
         "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e, "gpu_launches": launches * args.steps,
         "gpu_launches_per_step": launches, "clocks": clocks,
@@ -431,6 +436,8 @@ def main():
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--hblock", type=int, default=0)
     ap.add_argument("--budget", type=float, default=None)
+    ap.add_argument("--tau", type=float, default=None,
+                    help="outlier threshold (default: the method's 2.0)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

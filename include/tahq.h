@@ -104,6 +104,20 @@ tahq_status tahq_encode(const void *x, tahq_dtype dtype, int64_t tokens, int64_t
                         uint8_t *bits, uint8_t *pivots, void *workspace, size_t workspace_bytes,
                         void *stream);
 
+/*
+ * tahq_encode with the outlier threshold as an argument ("TAH-Quant" §3.3 eq. (3); its
+ * Appendix F compares tau = 0, 2, 4 and infinity).  A tile is transformed when
+ * r = |a(1)| / (|a(2)| + 1e-12) > tau (fp32 IEEE division, strict): tau = 0 transforms
+ * every tile whose r is above zero, tau = INFINITY none, tau = 2.0f is tahq_encode.  The
+ * entropy keys, and so the widths, do not depend on tau.  Same arguments, layouts,
+ * ownership and errors as tahq_encode; a negative or NaN tau is TAHQ_ERR_ARG.
+ */
+tahq_status tahq_encode_ex(const void *x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                           int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                           int64_t tokens_per_group, float tau, uint8_t *codes, float *scales,
+                           float *zeros, uint8_t *bits, uint8_t *pivots, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
 /* Bytes of device workspace tahq_decode needs; 0 for invalid arguments. */
 size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile);
 

@@ -18,8 +18,8 @@ from . import build as _build
 
 __all__ = [
     "TAHQ_F32", "TAHQ_BF16", "TahqError", "lib", "tahq_payload_size", "tahq_hi_count",
-    "tahq_workspace_size", "tahq_decode_workspace_size", "tahq_encode", "tahq_decode",
-    "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
+    "tahq_workspace_size", "tahq_decode_workspace_size", "tahq_encode", "tahq_encode_ex",
+    "tahq_decode", "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
     "tahq_decode_noalloc", "encode", "decode", "EXPORTED_SYMBOLS",
 ]
 
@@ -30,7 +30,7 @@ DEV_NONFINITE, DEV_WAIT_TIMEOUT, DEV_SELECT_MISMATCH, DEV_BAD_BITS, DEV_STREAM_O
 
 # Every extern "C" function declared in include/tahq.h.
 EXPORTED_SYMBOLS = (
-    "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode",
+    "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode", "tahq_encode_ex",
     "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
 )
@@ -62,6 +62,8 @@ def lib(path: str | None = None):
         "tahq_decode_workspace_size": (sz, [i64, i64, i32]),
         "tahq_encode": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64,
                               p, p, p, p, p, p, sz, p]),
+        "tahq_encode_ex": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
+                                 p, p, p, p, p, p, sz, p]),
         "tahq_decode": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, p, p, sz, p]),
         "tahq_get_device_status": (i32, [p, C.POINTER(C.c_uint32), p]),
         "tahq_status_string": (C.c_char_p, [i32]),
@@ -122,6 +124,15 @@ def tahq_encode(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budg
                              _stream(stream))
 
 
+def tahq_encode_ex(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                   tokens_per_group, tau, codes, scales, zeros, bits, pivots, workspace,
+                   workspace_bytes, stream=None) -> int:
+    return lib().tahq_encode_ex(_ptr(x), dtype, tokens, channels, tile, hblock, bits_lo,
+                                bits_hi, budget, tokens_per_group, tau, _ptr(codes),
+                                _ptr(scales), _ptr(zeros), _ptr(bits), _ptr(pivots),
+                                _ptr(workspace), workspace_bytes, _stream(stream))
+
+
 def tahq_decode(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile, hblock,
                 out, workspace, workspace_bytes, stream=None) -> int:
     return lib().tahq_decode(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros), _ptr(bits),
@@ -169,8 +180,9 @@ def _check(rc: int, what: str):
 
 def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_hi: int = 4,
            budget: float = 3.5, tokens_per_group: int = 0, out: dict | None = None,
-           workspace=None, stream=None) -> dict:
-    """Encode a CUDA tensor ``x`` ([tokens, channels], float32 or bfloat16).
+           workspace=None, stream=None, tau: float | None = None) -> dict:
+    """Encode a CUDA tensor ``x`` ([tokens, channels], float32 or bfloat16).  ``tau`` is the
+    outlier threshold (None: the method's 2.0, through tahq_encode; else tahq_encode_ex).
 
     Returns ``{"codes", "scales", "zeros", "bits", "pivots", "workspace"}`` (torch tensors on
     x's device).  Pass ``out`` / ``workspace`` from an earlier call to reuse them.
@@ -203,9 +215,14 @@ def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_
         }
     if workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-    rc = tahq_encode(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
-                     out["codes"], out["scales"], out["zeros"], out["bits"], out["pivots"],
-                     workspace, workspace.numel(), stream)
+    if tau is None:
+        rc = tahq_encode(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
+                         out["codes"], out["scales"], out["zeros"], out["bits"], out["pivots"],
+                         workspace, workspace.numel(), stream)
+    else:
+        rc = tahq_encode_ex(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
+                            float(tau), out["codes"], out["scales"], out["zeros"], out["bits"],
+                            out["pivots"], workspace, workspace.numel(), stream)
     _check(rc, "tahq_encode")
     res = dict(out)
     res["codes"] = out["codes"][:pay]

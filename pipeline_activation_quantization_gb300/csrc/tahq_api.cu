@@ -206,11 +206,12 @@ size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile) {
   return dec_layout(s).total;
 }
 
-tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
-                        int tile, int hblock, int bits_lo, int bits_hi, float budget,
-                        int64_t tokens_per_group, uint8_t* codes, float* scales, float* zeros,
-                        uint8_t* bits, uint8_t* pivots, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                           int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                           int64_t tokens_per_group, float tau, uint8_t* codes, float* scales,
+                           float* zeros, uint8_t* bits, uint8_t* pivots, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!(tau >= 0.0f)) return TAHQ_ERR_ARG;  // negative or NaN
   Shape s;
   tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
                                tokens_per_group, s);
@@ -240,6 +241,7 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.lo = s.lo;
   a.hi = s.hi;
   a.c_h = (float)(1.0 / std::sqrt((double)s.h));
+  a.tau = tau;
   a.n_tiles = s.n;
   a.n_g = s.n_g;
   a.n_groups = s.n_groups;
@@ -271,6 +273,16 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.items = at<unsigned long long>(workspace, L.items);
   a.items_cap = (long long)L.items_cap;
   return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}
+
+tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                        int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                        int64_t tokens_per_group, uint8_t* codes, float* scales, float* zeros,
+                        uint8_t* bits, uint8_t* pivots, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  return tahq_encode_ex(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                        tokens_per_group, 2.0f, codes, scales, zeros, bits, pivots, workspace,
+                        workspace_bytes, stream);
 }
 
 tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* scales,

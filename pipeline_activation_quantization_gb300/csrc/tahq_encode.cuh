@@ -118,6 +118,7 @@ struct EncParams {
   int direct;  // compaction copies slots straight from scratch (16-byte aligned throughout)
   int slot_lo, slot_hi;
   float c_h;
+  float tau;  // outlier threshold (§3.3 eq. (3): transform where r > tau)
   uint8_t* codes;
   float* scales;
   float* zeros;
@@ -295,7 +296,7 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
       }
     }
     team_top2<L>(m1, i1, m2);
-    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > 2.0f;
+    const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > p.tau;
     if (__any_sync(kFull, flag)) {
       float t[V];
 #pragma unroll
@@ -367,10 +368,11 @@ __host__ __device__ constexpr int p2_values() {
 // Hadamard (eq. (4)), a new range and new slots of both widths.  V * bits <= 64 (one
 // lane's codes in one 64-bit word); for V < 8, 8 / V lanes gather each group of 8 codes.
 //
-// The ratio test RN(m1 / d) > 2 with d = RN(m2 + 1e-12) >= 1e-12 needs no division: it
-// holds iff m1 / d > 2 + 2^-23 (ties round to 2), i.e. m1 / 2 - d > d 2^-24.  m1 / 2 is
-// exact, m1 / 2 - d is exact by Sterbenz's lemma where it matters (d <= m1 <= 4 d; below,
-// it is negative; above, it rounds to at least d), and d 2^-24 is a normal number.
+// The ratio test RN(m1 / d) > tau, d = RN(m2 + 1e-12) >= 1e-12.  For the method's
+// tau = 2 it needs no division: it holds iff m1 / d > 2 + 2^-23 (ties round to 2), i.e.
+// m1 / 2 - d > d 2^-24.  m1 / 2 is exact, m1 / 2 - d is exact by Sterbenz's lemma where it
+// matters (d <= m1 <= 4 d; below, it is negative; above, it rounds to at least d), and
+// d 2^-24 is a normal number.  Other thresholds take the IEEE division.
 template <typename Tin, int G, int V>
 __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned char* buf,
                                            const uint16_t* list, int n, long long t0, bool flat,
@@ -447,7 +449,9 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
       team_top2<L>(m1, i1, m2);
     }
     const float d = __fadd_rn(m2, 1e-12f);
-    const bool flag = valid && __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f);
+    const bool flag =
+        valid && (p.tau == 2.0f ? __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f)
+                                : __fdiv_rn(m1, d) > p.tau);
     if (!__any_sync(kFull, flag)) continue;  // the main pass's slots stand
     float t[V];
 #pragma unroll
@@ -538,14 +542,16 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   mn = team_min<LPT>(mn);
   mx = team_max<LPT>(mx);
   const float m1 = fmaxf(mx, -mn);
-  const float thr = __fmul_rn(m1, 0.5f);  // exact halving for m1 >= 2^-120
+  // two values of at least m1 / tau give m2 >= m1 / tau, so r < tau: the threshold is
+  // rounded up to keep the test on the safe side (m1 / 2 is exact for m1 >= 2^-120)
+  const float thr = p.tau == 2.0f ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
   uint32_t cnt = 0;
 #pragma unroll
   for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
   cnt = team_sum_u<LPT>(cnt);
-  // a maximum below 2^-120 can never give r > tau (the ratio is below 1e-24); a tile whose
-  // maximum is not finite goes to the exact test
-  const bool small = m1 < 0x1p-120f;
+  // for tau >= 1 a maximum below 2^-120 can never give r > tau (the ratio is below 1e-24);
+  // a tile whose maximum is not finite goes to the exact test
+  const bool small = m1 < 0x1p-120f && p.tau >= 1.0f;
   const bool deferred = !small && (!(m1 <= FLT_MAX) || cnt < 2u);
 
   // widths: Q_lo / D and Q_hi / D (or D / Q_b), split over the team's lanes
@@ -681,7 +687,7 @@ __device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams
     mn = team_min<L>(mn);
     mx = team_max<L>(mx);
     const float m1 = fmaxf(mx, -mn);
-    const float thr = __fmul_rn(m1, 0.5f);
+    const float thr = p.tau == 2.0f ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
     bool two;
     if constexpr (L >= 2) {
       two = team_two_ge<L>(lane_amax, thr, team);
@@ -1500,6 +1506,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.hi = a.hi;
   p.h = a.h;
   p.c_h = a.c_h;
+  p.tau = a.tau;
   p.slot_lo = G * a.lo / 8;
   p.slot_hi = G * a.hi / 8;
   p.direct = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 1 : 0;

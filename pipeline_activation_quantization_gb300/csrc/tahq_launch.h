@@ -16,6 +16,7 @@ struct EncodeArgs {
   bool bf16;
   int G, h, lo, hi;
   float c_h;                 // RN(1/sqrt(h))
+  float tau;                 // outlier threshold: transform where r > tau (>= 0, +inf: never)
   long long n_tiles, n_g, n_groups, K, group_bytes;
   int num_sms;
   const LgTables* tabs;

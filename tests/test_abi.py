@@ -85,6 +85,14 @@ def test_invalid_arguments(args):
     assert rc == 1
 
 
+@pytest.mark.parametrize("tau", [-1.0, -0.0 - 1e-30, float("nan"), float("-inf")])
+def test_encode_ex_rejects_bad_tau(tau):
+    fake = 1 << 20   # rejected before any dereference or launch
+    rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, tau, fake, fake, fake,
+                           fake, fake, fake, 1 << 30, 0)
+    assert rc == 1
+
+
 def test_unsupported_tile_and_workspace_errors():
     fake = 1 << 20
     # tile 96 is valid for the method but not built (not a power of two)

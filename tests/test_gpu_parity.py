@@ -23,9 +23,9 @@ def _need_cuda():
     tq.lib()
 
 
-def _check(x, G, h, lo, hi, beta, S):
-    gpu = gpu_roundtrip(x, G, h, lo, hi, beta, S)
-    ora = oracle_roundtrip(x, G, h, lo, hi, beta, S)
+def _check(x, G, h, lo, hi, beta, S, tau=None):
+    gpu = gpu_roundtrip(x, G, h, lo, hi, beta, S, tau)
+    ora = oracle_roundtrip(x, G, h, lo, hi, beta, S, tau)
     return assert_parity(gpu, ora, G)
 
 
@@ -53,6 +53,49 @@ SMALL = [
 def test_small_grid(dtype, dist, G, h, lo, hi, beta, T, C, S):
     w = synth.Workload("small", T, C, dtype, G, h, lo, hi, beta, S, 100 + T + G, dist)
     _check(synth.generate(w), G, h, lo, hi, beta, S)
+
+
+# ------------------------------------------------------------------ the threshold tau
+# ("TAH-Quant" Appendix F: tau = 0 always transforms, tau = inf never, tau = 4); every
+# layout of the encoder, the one-width kernels included
+
+TAU = [
+    # dtype, dist, G, h, lo, hi, beta, T, C, S
+    ("f32", "laplace", 128, 128, 3, 4, 3.5, 40, 2176, 20),
+    ("f32", "gauss_rms_spikes", 64, 32, 3, 4, 3.5, 96, 1088, 32),
+    ("bf16", "gauss_rms_spikes", 64, 64, 3, 4, 3.5, 96, 1088, 32),
+    ("f32", "student_t", 16, 16, 3, 4, 3.5, 33, 400, 11),
+    ("bf16", "laplace", 32, 8, 3, 4, 3.25, 80, 2080, 16),
+    ("f32", "laplace", 64, 64, 3, 4, 3.0, 64, 512, 0),      # one width (K = 0)
+    ("bf16", "gauss_rms_spikes", 128, 128, 3, 4, 4.0, 48, 1152, 16),   # one width (K = n_g)
+]
+
+
+@pytest.mark.parametrize("tau", [0.0, 1.5, 4.0, float("inf")])
+@pytest.mark.parametrize("dtype,dist,G,h,lo,hi,beta,T,C,S", TAU)
+def test_tau(dtype, dist, G, h, lo, hi, beta, T, C, S, tau):
+    w = synth.Workload("tau", T, C, dtype, G, h, lo, hi, beta, S, 300 + T + G, dist)
+    rep = _check(synth.generate(w), G, h, lo, hi, beta, S, tau)
+    print("tau", tau, rep)
+
+
+def test_tau_rejects_negative_and_nan():
+    import torch
+    x = torch.zeros(8, 64, device="cuda")
+    for tau in (-1.0, float("nan")):
+        with pytest.raises(tq.TahqError):
+            tq.encode(x, 64, 64, 3, 4, 3.5, 0, tau=tau)
+
+
+# ------------------------------------------------------------------ width mixes
+# (Appendix G: 80% INT2 + 20% INT3, 50% INT4 + 50% INT3)
+
+@pytest.mark.parametrize("dtype,G,lo,hi,beta", [("f32", 128, 2, 3, 2.2), ("bf16", 64, 2, 3, 2.2),
+                                                ("f32", 32, 2, 3, 2.2), ("bf16", 16, 2, 3, 2.2),
+                                                ("f32", 64, 3, 4, 3.5)])
+def test_appendix_g_mixes(dtype, G, lo, hi, beta):
+    w = synth.Workload("mix", 64, 2048, dtype, G, G, lo, hi, beta, 16, 500 + G, "laplace")
+    print("mix", lo, hi, beta, _check(synth.generate(w), G, G, lo, hi, beta, 16))
 
 
 # ------------------------------------------------------------------ full-size workloads
