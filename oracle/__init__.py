@@ -4,7 +4,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
 import this package.  The product (``pipeline_activation_quantization_gb300``) never
 imports it and shares no code with it.
 
-The arithmetic lives in ``tahq_oracle.c`` (plain scalar C, compiled with gcc
+The arithmetic lives in ``tahq_oracle.c`` and, for the wire format,
+``tahq_wire_oracle.c`` (plain scalar C, compiled with gcc
 ``-O2 -ffp-contract=off``, no fast-math); this module only compiles it, marshals numpy
 arrays through ctypes, and can split a tensor into its independent token groups to run
 them on several host threads (the per-group results are the same as one sequential call).
@@ -20,7 +21,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "tahq_oracle.c")
+_SRCS = [os.path.join(_HERE, "tahq_oracle.c"), os.path.join(_HERE, "tahq_wire_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libtahq_oracle.so")
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-std=c11"]
@@ -33,9 +34,10 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle shared library (in-tree, under ``oracle/_build``)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(f) for f in _SRCS)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, *_SRCS, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -70,6 +72,15 @@ def lib():
                 "oracle_encode_tau": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
                                             p, p, p, p, p, p, p]),
                 "oracle_decode": (i32, [p, i64, p, p, p, p, i64, i64, i32, i32, p]),
+                "oracle_f16_value": (C.c_double, [C.c_uint16]),
+                "oracle_f16_round_down": (C.c_uint16, [f32]),
+                "oracle_f16_scale_up": (C.c_uint16, [f32, f32, i32]),
+                "oracle_quantize_tile_f16": (None, [p, i32, i32, p, p, p, p]),
+                "oracle_wire_layout": (i64, [i64, i64, i32, i32, i32, f32, i64, p]),
+                "oracle_encode_wire": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
+                                             p, i64]),
+                "oracle_wire_header": (i32, [p, i64, p]),
+                "oracle_decode_wire": (i32, [p, i64, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -289,3 +300,72 @@ def _run_all(fn, count: int, threads: int):
         return
     with ThreadPoolExecutor(max_workers=min(threads, count)) as ex:
         list(ex.map(fn, range(count)))
+
+
+# ------------------------------------------------------------------------ wire format
+
+def f16_value(h: int) -> float:
+    return float(lib().oracle_f16_value(int(h)))
+
+
+def f16_round_down(x: float) -> int:
+    return int(lib().oracle_f16_round_down(float(x)))
+
+
+def f16_scale_up(zero: float, mx: float, Q: int) -> int:
+    return int(lib().oracle_f16_scale_up(float(zero), float(mx), int(Q)))
+
+
+def quantize_tile_f16(v, b: int):
+    """-> (codes u8[G], scale16, zero16, near u8[G]) of the wire format's quantiser."""
+    v = _f32(v)
+    q = np.zeros(v.size, np.uint8); near = np.zeros(v.size, np.uint8)
+    s, z = C.c_uint16(), C.c_uint16()
+    lib().oracle_quantize_tile_f16(_ptr(v), v.size, b, _ptr(q), C.byref(s), C.byref(z), _ptr(near))
+    return q, s.value, z.value, near
+
+
+def wire_layout(T, Cc, G, lo, hi, budget, S=0):
+    """-> (total bytes, [map, meta, pivots, payload offsets], payload bytes)."""
+    off = np.zeros(5, np.int64)
+    total = int(lib().oracle_wire_layout(T, Cc, G, lo, hi, budget, S, _ptr(off)))
+    return total, [int(v) for v in off[:4]], int(off[4])
+
+
+def encode_wire(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: int = 0,
+                tau: float = 2.0) -> np.ndarray:
+    """The whole tensor as one wire buffer (uint8)."""
+    x = np.ascontiguousarray(x)
+    dtype = BF16 if x.dtype == np.uint16 else F32
+    if dtype == F32:
+        x = _f32(x)
+    T, Cc = x.shape
+    total, _, _ = wire_layout(T, Cc, G, lo, hi, budget, S)
+    if total < 0:
+        raise ValueError("invalid codec arguments")
+    out = np.zeros(total, np.uint8)
+    rc = lib().oracle_encode_wire(_ptr(x), dtype, T, Cc, G, h, lo, hi, budget, S, float(tau),
+                                  _ptr(out), total)
+    if rc != 0:
+        raise RuntimeError("oracle_encode_wire failed")
+    return out
+
+
+def wire_header(wire: np.ndarray) -> dict:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    f = np.zeros(15, np.int64)
+    if lib().oracle_wire_header(_ptr(wire), wire.size, _ptr(f)) != 0:
+        raise ValueError("not a wire buffer")
+    keys = ["tokens", "channels", "tokens_per_group", "tile", "hblock", "bits_lo", "bits_hi",
+            "pivot_bits", "tiles", "off_map", "off_meta", "off_pivots", "off_payload",
+            "payload_bytes", "total_bytes"]
+    return {k: int(v) for k, v in zip(keys, f)}
+
+
+def decode_wire(wire: np.ndarray) -> np.ndarray:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    hd = wire_header(wire)
+    out = np.zeros((hd["tokens"], hd["channels"]), np.float32)
+    if lib().oracle_decode_wire(_ptr(wire), wire.size, _ptr(out)) != 0:
+        raise RuntimeError("oracle_decode_wire rejected its input")
+    return out
