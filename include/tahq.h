@@ -54,6 +54,7 @@ typedef enum { TAHQ_F32 = 0, TAHQ_BF16 = 1 } tahq_dtype;
 #define TAHQ_DEV_SELECT_MISMATCH 0x4u    /* candidate count disagreed with histogram    */
 #define TAHQ_DEV_BAD_BITS 0x8u           /* decode: a bit width outside 1..8 or pivot   */
 #define TAHQ_DEV_STREAM_OVERRUN 0x10u    /* decode: slots run past codes_bytes          */
+#define TAHQ_DEV_BAD_WIRE 0x20u          /* decode_wire: header differs from the args   */
 
 /*
  * Exact size in bytes of the packed code stream for these parameters.  §3.4: the
@@ -169,6 +170,62 @@ tahq_status tahq_decode_noalloc(const uint8_t *codes, size_t codes_bytes, const 
                                 const float *zeros, const uint8_t *bits, const uint8_t *pivots,
                                 int64_t tokens, int64_t channels, int tile, int hblock,
                                 float *out, uint32_t *device_status, void *stream);
+
+/*
+ * WIRE FORMAT ("TAH-Quant" §3.2: the 1-bit per-tile width map travels with the payload
+ * as metadata; §3.4: heterogeneous precisions and metadata in one contiguous uint8 byte
+ * stream of fixed size per shape; the pages count about 0.61 metadata bits per element at
+ * a tile of 64, i.e. 39 bits a tile).  One buffer, sections at 16-byte boundaries:
+ *   [0, 128)      header, little-endian: u32 magic "TAHQ", u16 version 1, u16 128,
+ *                 i64 tokens, i64 channels, i64 tokens per group, u16 tile, u16 hblock,
+ *                 u8 bits_lo, u8 bits_hi, u8 pivot bits pb = log2(tile), u8 0, f32 budget,
+ *                 f32 tau, u64 tiles, u64 offsets of the four sections below, u64 payload
+ *                 bytes, u64 total bytes, zeros;
+ *   width map     bit t (LSB first) = tile t has bits_hi;
+ *   metadata      per tile a u32: fp16 scale in bits 0-14 with the transform flag in bit
+ *                 15 (a scale is never negative), fp16 zero in bits 16-31;
+ *   pivots        pb bits per tile (LSB first), the pivot of a transformed tile, else 0;
+ *   payload       the packed slots of tahq_encode (same layout, same size);
+ * padding bytes are zero.  Widths and transform decisions are those of tahq_encode_ex;
+ * the quantiser rounds to the wire's fp16 metadata: zero = the largest fp16 value <= the
+ * tile minimum, scale = the smallest fp16 value s >= 0 with zero + (2^b - 1) s >= the tile
+ * maximum (exact arithmetic), codes RNE((v - zero) * RN(1 / s)) (0 when s = 0), decode
+ * fmaf(q, s, zero).  Inputs beyond the fp16 range (|v| > 65504) give undefined codes.
+ */
+
+/* Bytes of the wire buffer for these parameters (fixed by the shape); 0 if invalid. */
+size_t tahq_wire_size(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                      float budget, int64_t tokens_per_group);
+
+/* Device workspace of tahq_encode_wire (the encoder's plus four per-tile arrays). */
+size_t tahq_wire_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock,
+                                int bits_lo, int bits_hi, float budget, int64_t tokens_per_group);
+
+/* Device workspace of tahq_decode_wire (the decoder's plus four per-tile arrays). */
+size_t tahq_wire_decode_workspace_size(int64_t tokens, int64_t channels, int tile);
+
+/*
+ * Encode x (as tahq_encode_ex, same arguments and threshold tau) into the wire buffer
+ * `wire` (device, 16-byte aligned, at least tahq_wire_size bytes; the caller owns it).
+ * Returns the errors of tahq_encode_ex, TAHQ_ERR_ARG for a missing, misaligned or short
+ * buffer, TAHQ_ERR_WORKSPACE for a workspace below tahq_wire_workspace_size.
+ */
+tahq_status tahq_encode_wire(const void *x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                             int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                             int64_t tokens_per_group, float tau, uint8_t *wire,
+                             size_t wire_bytes, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * Decode a wire buffer into out [tokens * channels] fp32 (device, 16-byte aligned).  The
+ * arguments are those the buffer was encoded with (they fix its layout); a header that
+ * differs from them (tau aside) sets TAHQ_DEV_BAD_WIRE in the workspace's status word,
+ * and invalid fields set the bits tahq_decode sets.  Host-side errors as tahq_decode.
+ */
+tahq_status tahq_decode_wire(const uint8_t *wire, size_t wire_bytes, int64_t tokens,
+                             int64_t channels, int tile, int hblock, int bits_lo, int bits_hi,
+                             float budget, int64_t tokens_per_group, float *out, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /*
  * Copy the device status word of the last call that used `workspace` into *status_out

@@ -78,7 +78,7 @@ def lib():
                 "oracle_quantize_tile_f16": (None, [p, i32, i32, p, p, p, p]),
                 "oracle_wire_layout": (i64, [i64, i64, i32, i32, i32, f32, i64, p]),
                 "oracle_encode_wire": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
-                                             p, i64]),
+                                             p, i64, p]),
                 "oracle_wire_header": (i32, [p, i64, p]),
                 "oracle_decode_wire": (i32, [p, i64, p]),
             }
@@ -333,8 +333,9 @@ def wire_layout(T, Cc, G, lo, hi, budget, S=0):
 
 
 def encode_wire(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: int = 0,
-                tau: float = 2.0) -> np.ndarray:
-    """The whole tensor as one wire buffer (uint8)."""
+                tau: float = 2.0, want_near: bool = False):
+    """The whole tensor as one wire buffer (uint8); with ``want_near`` also the [T, C]
+    rounding-boundary flags of its codes."""
     x = np.ascontiguousarray(x)
     dtype = BF16 if x.dtype == np.uint16 else F32
     if dtype == F32:
@@ -344,11 +345,12 @@ def encode_wire(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, 
     if total < 0:
         raise ValueError("invalid codec arguments")
     out = np.zeros(total, np.uint8)
+    near = np.zeros((T, Cc), np.uint8) if want_near else None
     rc = lib().oracle_encode_wire(_ptr(x), dtype, T, Cc, G, h, lo, hi, budget, S, float(tau),
-                                  _ptr(out), total)
+                                  _ptr(out), total, _ptr(near))
     if rc != 0:
         raise RuntimeError("oracle_encode_wire failed")
-    return out
+    return (out, near) if want_near else out
 
 
 def wire_header(wire: np.ndarray) -> dict:

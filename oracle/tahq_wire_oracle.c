@@ -167,11 +167,12 @@ static uint64_t get_u64(const uint8_t *p) { uint64_t v = 0; for (int i = 7; i >=
 
 /* Encode a [T, C] tensor (dtype as oracle_encode) into wire[0, wire_bytes).  The widths
  * and the transform decisions are the plain codec's (oracle_encode_tau); only the
- * quantiser's zero and scale differ.  Returns 0, or -1 on invalid arguments or a buffer
- * shorter than oracle_wire_layout says. */
+ * quantiser's zero and scale differ.  near (T*C bytes, optional) flags the elements whose
+ * scaled value lies within 1e-5 (relative) of a rounding boundary.  Returns 0, or -1 on
+ * invalid arguments or a buffer shorter than oracle_wire_layout says. */
 int oracle_encode_wire(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo,
                        int hi, float budget, int64_t S, float tau, uint8_t *wire,
-                       int64_t wire_bytes)
+                       int64_t wire_bytes, uint8_t *near)
 {
     int64_t off[5];
     int64_t total = oracle_wire_layout(T, C, G, lo, hi, budget, S, off);
@@ -224,7 +225,7 @@ int oracle_encode_wire(const void *x, int dtype, int64_t T, int64_t C, int G, in
         if (flag) oracle_transform(a, G, h, piv[t]);
         int b = bits[t];
         uint16_t s16, z16;
-        oracle_quantize_tile_f16(a, G, b, q, &s16, &z16, NULL);
+        oracle_quantize_tile_f16(a, G, b, q, &s16, &z16, near ? near + t * G : NULL);
         oracle_pack_tile(q, G, b, wire + off[3] + slot);
         slot += G * b / 8;
         if (b == hi) wire[off[0] + t / 8] |= (uint8_t)(1u << (t % 8));

@@ -20,19 +20,24 @@ __all__ = [
     "TAHQ_F32", "TAHQ_BF16", "TahqError", "lib", "tahq_payload_size", "tahq_hi_count",
     "tahq_workspace_size", "tahq_decode_workspace_size", "tahq_encode", "tahq_encode_ex",
     "tahq_decode", "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
-    "tahq_decode_noalloc", "encode", "decode", "EXPORTED_SYMBOLS",
+    "tahq_decode_noalloc", "tahq_wire_size", "tahq_wire_workspace_size",
+    "tahq_wire_decode_workspace_size", "tahq_encode_wire", "tahq_decode_wire", "encode", "decode",
+    "encode_wire", "decode_wire", "EXPORTED_SYMBOLS",
 ]
 
 TAHQ_F32, TAHQ_BF16 = 0, 1
 STATUS_NAMES = {0: "TAHQ_OK", 1: "TAHQ_ERR_ARG", 2: "TAHQ_ERR_UNSUPPORTED", 3: "TAHQ_ERR_WORKSPACE",
                 4: "TAHQ_ERR_CUDA", 5: "TAHQ_ERR_DEVICE_STATUS"}
 DEV_NONFINITE, DEV_WAIT_TIMEOUT, DEV_SELECT_MISMATCH, DEV_BAD_BITS, DEV_STREAM_OVERRUN = 1, 2, 4, 8, 16
+DEV_BAD_WIRE = 32
 
 # Every extern "C" function declared in include/tahq.h.
 EXPORTED_SYMBOLS = (
     "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode", "tahq_encode_ex",
     "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
+    "tahq_wire_size", "tahq_wire_workspace_size", "tahq_wire_decode_workspace_size",
+    "tahq_encode_wire", "tahq_decode_wire",
 )
 
 
@@ -70,6 +75,12 @@ def lib(path: str | None = None):
         "tahq_version": (i32, []),
         "tahq_log2_tables": (None, [p, p, p]),
         "tahq_decode_noalloc": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, p, p, p]),
+        "tahq_wire_size": (sz, [i64, i64, i32, i32, i32, f32, i64]),
+        "tahq_wire_workspace_size": (sz, [i64, i64, i32, i32, i32, i32, f32, i64]),
+        "tahq_wire_decode_workspace_size": (sz, [i64, i64, i32]),
+        "tahq_encode_wire": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32, p, sz,
+                                   p, sz, p]),
+        "tahq_decode_wire": (i32, [p, sz, i64, i64, i32, i32, i32, i32, f32, i64, p, p, sz, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -249,3 +260,90 @@ def decode(enc: dict, tokens: int, channels: int, tile: int = 64, hblock: int | 
                      tokens, channels, tile, h, out, workspace, workspace.numel(), stream)
     _check(rc, "tahq_decode")
     return out
+
+
+# ------------------------------------------------------------------ wire format
+
+def tahq_wire_size(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group) -> int:
+    return lib().tahq_wire_size(tokens, channels, tile, bits_lo, bits_hi, budget, tokens_per_group)
+
+
+def tahq_wire_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                             tokens_per_group) -> int:
+    return lib().tahq_wire_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi,
+                                          budget, tokens_per_group)
+
+
+def tahq_wire_decode_workspace_size(tokens, channels, tile) -> int:
+    return lib().tahq_wire_decode_workspace_size(tokens, channels, tile)
+
+
+def tahq_encode_wire(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                     tokens_per_group, tau, wire, wire_bytes, workspace, workspace_bytes,
+                     stream=None) -> int:
+    return lib().tahq_encode_wire(_ptr(x), dtype, tokens, channels, tile, hblock, bits_lo,
+                                  bits_hi, budget, tokens_per_group, tau, _ptr(wire), wire_bytes,
+                                  _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def tahq_decode_wire(wire, wire_bytes, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                     tokens_per_group, out, workspace, workspace_bytes, stream=None) -> int:
+    return lib().tahq_decode_wire(_ptr(wire), wire_bytes, tokens, channels, tile, hblock, bits_lo,
+                                  bits_hi, budget, tokens_per_group, _ptr(out), _ptr(workspace),
+                                  workspace_bytes, _stream(stream))
+
+
+def encode_wire(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_hi: int = 4,
+                budget: float = 3.5, tokens_per_group: int = 0, tau: float = 2.0, out=None,
+                workspace=None, stream=None):
+    """Encode a CUDA tensor into one wire buffer (uint8 CUDA tensor of tahq_wire_size bytes).
+
+    Returns ``(wire, workspace)``; pass them back in to reuse them.
+    """
+    import torch
+    if not x.is_cuda:
+        raise ValueError("tahq.encode_wire needs a CUDA tensor")
+    if x.dtype == torch.float32:
+        dt = TAHQ_F32
+    elif x.dtype == torch.bfloat16:
+        dt = TAHQ_BF16
+    else:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    x = x.contiguous()
+    T, Cc = x.shape
+    h = hblock or tile
+    size = tahq_wire_size(T, Cc, tile, bits_lo, bits_hi, budget, tokens_per_group)
+    ws = tahq_wire_workspace_size(T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group)
+    if size == 0 or ws == 0:
+        raise TahqError(1, "tahq_wire_size")
+    if out is None:
+        out = torch.empty(size, dtype=torch.uint8, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x.device)
+    rc = tahq_encode_wire(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
+                          float(tau), out, out.numel(), workspace, workspace.numel(), stream)
+    _check(rc, "tahq_encode_wire")
+    return out, workspace
+
+
+def decode_wire(wire, tokens: int, channels: int, tile: int = 64, hblock: int | None = None,
+                bits_lo: int = 3, bits_hi: int = 4, budget: float = 3.5, tokens_per_group: int = 0,
+                out=None, workspace=None, stream=None):
+    """Decode a wire buffer into a float32 CUDA tensor [tokens, channels].
+
+    Returns ``(out, workspace)``; the workspace's status word reports a header that does
+    not match the arguments (DEV_BAD_WIRE).
+    """
+    import torch
+    h = hblock or tile
+    ws = tahq_wire_decode_workspace_size(tokens, channels, tile)
+    if ws == 0:
+        raise TahqError(1, "tahq_wire_decode_workspace_size")
+    if out is None:
+        out = torch.empty((tokens, channels), dtype=torch.float32, device=wire.device)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=wire.device)
+    rc = tahq_decode_wire(wire, wire.numel(), tokens, channels, tile, h, bits_lo, bits_hi, budget,
+                          tokens_per_group, out, workspace, workspace.numel(), stream)
+    _check(rc, "tahq_decode_wire")
+    return out, workspace

@@ -206,11 +206,14 @@ size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile) {
   return dec_layout(s).total;
 }
 
-tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
-                           int tile, int hblock, int bits_lo, int bits_hi, float budget,
-                           int64_t tokens_per_group, float tau, uint8_t* codes, float* scales,
-                           float* zeros, uint8_t* bits, uint8_t* pivots, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+namespace {
+
+// tahq_encode_ex, and the wire format's encoder (wire: fp16 zero and scales).
+tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                        int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                        int64_t tokens_per_group, float tau, bool wire, uint8_t* codes,
+                        float* scales, float* zeros, uint8_t* bits, uint8_t* pivots,
+                        void* workspace, size_t workspace_bytes, void* stream) {
   if (!(tau >= 0.0f)) return TAHQ_ERR_ARG;  // negative or NaN
   Shape s;
   tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
@@ -242,6 +245,7 @@ tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int6
   a.hi = s.hi;
   a.c_h = (float)(1.0 / std::sqrt((double)s.h));
   a.tau = tau;
+  a.wire = wire;
   a.n_tiles = s.n;
   a.n_g = s.n_g;
   a.n_groups = s.n_groups;
@@ -275,6 +279,18 @@ tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int6
   return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 
+}  // namespace
+
+tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                           int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                           int64_t tokens_per_group, float tau, uint8_t* codes, float* scales,
+                           float* zeros, uint8_t* bits, uint8_t* pivots, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return encode_impl(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                     tokens_per_group, tau, false, codes, scales, zeros, bits, pivots, workspace,
+                     workspace_bytes, stream);
+}
+
 tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
                         int tile, int hblock, int bits_lo, int bits_hi, float budget,
                         int64_t tokens_per_group, uint8_t* codes, float* scales, float* zeros,
@@ -285,10 +301,14 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
                         workspace_bytes, stream);
 }
 
-tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* scales,
+namespace {
+
+// tahq_decode; clear = false when the caller has already cleared the status word (and
+// may have set bits in it on the same stream).
+tahq_status decode_impl(const uint8_t* codes, size_t codes_bytes, const float* scales,
                         const float* zeros, const uint8_t* bits, const uint8_t* pivots,
                         int64_t tokens, int64_t channels, int tile, int hblock, float* out,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+                        void* workspace, size_t workspace_bytes, void* stream, bool clear) {
   Shape s;
   tahq_status st = check_shape(tokens, channels, tile, hblock, s);
   if (st != TAHQ_OK) return st;
@@ -303,7 +323,7 @@ tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* s
   if (workspace_bytes < L.total) return TAHQ_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   // status and ticket; the offset arrays are written in full before they are read
-  if (cudaMemsetAsync(workspace, 0, L.ctot, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  if (clear && cudaMemsetAsync(workspace, 0, L.ctot, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
   if (s.n == 0) return TAHQ_OK;
   const int sms = num_sms_current();
   if (sms <= 0) return TAHQ_ERR_CUDA;
@@ -325,6 +345,195 @@ tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* s
   a.ctot = at<uint32_t>(workspace, L.ctot);
   a.bsum = at<unsigned long long>(workspace, L.bsum);
   return tahq::launch_decode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}
+
+}  // namespace
+
+tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* scales,
+                        const float* zeros, const uint8_t* bits, const uint8_t* pivots,
+                        int64_t tokens, int64_t channels, int tile, int hblock, float* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile,
+                     hblock, out, workspace, workspace_bytes, stream, true);
+}
+
+// ------------------------------------------------------------------------ wire format
+
+namespace {
+
+struct WireLayout {
+  long long off_map, off_meta, off_piv, off_pay, pay, total;
+  int pb;
+};
+
+long long up16(long long v) { return (v + 15) / 16 * 16; }
+
+// Sections at 16-byte boundaries: 128-byte header, width map (1 bit a tile), (scale, zero)
+// fp16 pairs (4 bytes a tile), pivot fields (log2 tile bits a tile), payload.
+WireLayout wire_layout(const Shape& s) {
+  WireLayout W{};
+  W.pb = 0;
+  while ((1 << W.pb) < s.G) W.pb++;
+  W.off_map = 128;
+  W.off_meta = W.off_map + up16((s.n + 7) / 8);
+  W.off_piv = W.off_meta + up16(4 * s.n);
+  W.off_pay = W.off_piv + up16((s.n * W.pb + 7) / 8);
+  W.pay = s.payload;
+  W.total = W.off_pay + up16(s.payload);
+  return W;
+}
+
+// The 128-byte header (little-endian fields; the host is little-endian like the device).
+void wire_header(const Shape& s, float budget, float tau, const WireLayout& W, uint32_t* words) {
+  unsigned char b[128];
+  std::memset(b, 0, sizeof(b));
+  auto put = [&](int off, const void* v, size_t n) { std::memcpy(b + off, v, n); };
+  const uint32_t magic = 0x51484154u;  // bytes 'T' 'A' 'H' 'Q'
+  const uint16_t version = 1, header_bytes = 128, G = (uint16_t)s.G, h = (uint16_t)s.h;
+  const int64_t T = s.T, C = s.C, S = s.n_g / (s.C / s.G);
+  const uint8_t lo = (uint8_t)s.lo, hi = (uint8_t)s.hi, pb = (uint8_t)W.pb;
+  const uint64_t n = (uint64_t)s.n;
+  const uint64_t offs[6] = {(uint64_t)W.off_map, (uint64_t)W.off_meta, (uint64_t)W.off_piv,
+                            (uint64_t)W.off_pay, (uint64_t)W.pay, (uint64_t)W.total};
+  put(0, &magic, 4);
+  put(4, &version, 2);
+  put(6, &header_bytes, 2);
+  put(8, &T, 8);
+  put(16, &C, 8);
+  put(24, &S, 8);
+  put(32, &G, 2);
+  put(34, &h, 2);
+  put(36, &lo, 1);
+  put(37, &hi, 1);
+  put(38, &pb, 1);
+  put(40, &budget, 4);
+  put(44, &tau, 4);
+  put(48, &n, 8);
+  put(56, offs, sizeof(offs));
+  std::memcpy(words, b, sizeof(b));
+}
+
+// Per-tile arrays after a codec workspace of `base` bytes: scales, zeros, bits, pivots.
+struct WireArrays {
+  size_t scales, zeros, bits, pivots, total;
+};
+WireArrays wire_arrays(size_t base, long long n) {
+  WireArrays A{};
+  A.scales = align_up(base);
+  A.zeros = align_up(A.scales + 4 * (size_t)n);
+  A.bits = align_up(A.zeros + 4 * (size_t)n);
+  A.pivots = align_up(A.bits + (size_t)n);
+  A.total = align_up(A.pivots + (size_t)n);
+  return A;
+}
+
+}  // namespace
+
+size_t tahq_wire_size(int64_t tokens, int64_t channels, int tile, int bits_lo, int bits_hi,
+                      float budget, int64_t tokens_per_group) {
+  Shape s;
+  if (check_codec(tokens, channels, tile, -1, bits_lo, bits_hi, budget, tokens_per_group, s) !=
+      TAHQ_OK)
+    return 0;
+  return (size_t)wire_layout(s).total;
+}
+
+size_t tahq_wire_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock,
+                                int bits_lo, int bits_hi, float budget,
+                                int64_t tokens_per_group) {
+  Shape s;
+  if (check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget, tokens_per_group,
+                  s) != TAHQ_OK)
+    return 0;
+  return wire_arrays(enc_layout(s).total, s.n).total;
+}
+
+size_t tahq_wire_decode_workspace_size(int64_t tokens, int64_t channels, int tile) {
+  Shape s;
+  if (check_shape(tokens, channels, tile, -1, s) != TAHQ_OK) return 0;
+  return wire_arrays(dec_layout(s).total, s.n).total;
+}
+
+tahq_status tahq_encode_wire(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                             int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                             int64_t tokens_per_group, float tau, uint8_t* wire, size_t wire_bytes,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                               tokens_per_group, s);
+  if (st != TAHQ_OK) return st;
+  if (hblock < 0 || !(tau >= 0.0f)) return TAHQ_ERR_ARG;
+  const WireLayout W = wire_layout(s);
+  if (!wire || !aligned(wire, 16) || wire_bytes < (size_t)W.total) return TAHQ_ERR_ARG;
+  if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
+  const EncLayout L = enc_layout(s);
+  const WireArrays A = wire_arrays(L.total, s.n);
+  if (workspace_bytes < A.total) return TAHQ_ERR_WORKSPACE;
+  float* scales = at<float>(workspace, A.scales);
+  float* zeros = at<float>(workspace, A.zeros);
+  uint8_t* bits = at<uint8_t>(workspace, A.bits);
+  uint8_t* pivots = at<uint8_t>(workspace, A.pivots);
+  st = encode_impl(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                   tokens_per_group, tau, true, wire + W.off_pay, scales, zeros, bits, pivots,
+                   workspace, L.total, stream);
+  if (st != TAHQ_OK) return st;
+  tahq::WirePackArgs a{};
+  a.scales = scales;
+  a.zeros = zeros;
+  a.bits = bits;
+  a.pivots = pivots;
+  a.wire = wire;
+  a.n = s.n;
+  a.off_map = W.off_map;
+  a.off_meta = W.off_meta;
+  a.off_piv = W.off_piv;
+  a.off_pay = W.off_pay;
+  a.pay = W.pay;
+  a.total = W.total;
+  a.hi = s.hi;
+  a.pb = W.pb;
+  wire_header(s, budget, tau, W, a.header);
+  return tahq::launch_wire_pack(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TAHQ_OK
+             : TAHQ_ERR_CUDA;
+}
+
+tahq_status tahq_decode_wire(const uint8_t* wire, size_t wire_bytes, int64_t tokens,
+                             int64_t channels, int tile, int hblock, int bits_lo, int bits_hi,
+                             float budget, int64_t tokens_per_group, float* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  Shape s;
+  tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                               tokens_per_group, s);
+  if (st != TAHQ_OK) return st;
+  if (hblock < 0) return TAHQ_ERR_ARG;
+  const WireLayout W = wire_layout(s);
+  if (!wire || !aligned(wire, 16) || wire_bytes < (size_t)W.total) return TAHQ_ERR_ARG;
+  if (s.n > 0 && (!out || !aligned(out, 16))) return TAHQ_ERR_ARG;
+  if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
+  const DecLayout L = dec_layout(s);
+  const WireArrays A = wire_arrays(L.total, s.n);
+  if (workspace_bytes < A.total) return TAHQ_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, L.ctot, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  tahq::WireUnpackArgs a{};
+  a.wire = wire;
+  a.scales = at<float>(workspace, A.scales);
+  a.zeros = at<float>(workspace, A.zeros);
+  a.bits = at<uint8_t>(workspace, A.bits);
+  a.pivots = at<uint8_t>(workspace, A.pivots);
+  a.status = at<uint32_t>(workspace, L.status);
+  a.n = s.n;
+  a.off_map = W.off_map;
+  a.off_meta = W.off_meta;
+  a.off_piv = W.off_piv;
+  a.lo = s.lo;
+  a.hi = s.hi;
+  a.pb = W.pb;
+  wire_header(s, budget, 0.0f, W, a.header);  // tau (word 11) is not compared
+  if (tahq::launch_wire_unpack(a, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  return decode_impl(wire + W.off_pay, (size_t)W.pay, a.scales, a.zeros, a.bits, a.pivots,
+                     tokens, channels, tile, hblock, out, workspace, L.total, stream, false);
 }
 
 tahq_status tahq_get_device_status(const void* workspace, uint32_t* status_out, void* stream) {

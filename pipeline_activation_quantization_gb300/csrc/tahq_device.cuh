@@ -11,6 +11,7 @@
 //   - u = (v - min) * inv, inv = Q / (max - min), code = rint(u) clamped to [0, Q].
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,6 +25,7 @@ constexpr uint32_t kStWaitTimeout = 0x2u;
 constexpr uint32_t kStSelectMismatch = 0x4u;
 constexpr uint32_t kStBadBits = 0x8u;
 constexpr uint32_t kStOverrun = 0x10u;
+constexpr uint32_t kStBadWire = 0x20u;
 
 // Tables of the canonical logarithm, passed to kernels by value and copied to shared
 // memory (indexed loads from the parameter bank would serialise).
@@ -380,5 +382,38 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* flag, uint32_t targ
     __nanosleep(64);
   }
 }
+
+// ------------------------------------------------------------------ wire-format quantiser
+// ("TAH-Quant" §3.4: fixed-size buffer with fp16 metadata.)  The zero is the largest fp16
+// value <= the tile minimum, the scale of width b the smallest fp16 value s >= 0 with
+// zero + Q_b s >= max (Q_b = 2^b - 1), and the codes use inv = RN(1 / s) (0 when s = 0).
+
+// The largest fp16 value <= mn, as fp32 (exact).
+__device__ __forceinline__ float wire_zero(float mn) {
+  return __half2float(__float2half_rd(mn));
+}
+
+// The smallest fp16 scale covering [zero, mx] at Q steps, as fp32 (exact; +inf when no
+// finite fp16 value does).  RU(RU(mx - zero) / Q) rounded up to fp16 is never below the
+// answer and at most one fp16 step above it (the fp32 over-estimate is under 2^-22
+// relative, the fp16 spacing 2^-10 relative or 2^-24 absolute), so an exact test of the
+// fp16 value below settles it: zero + Q s is a sum of multiples of 2^-24 below 2^25 in
+// size, exact in double, and so is its comparison with the fp32 mx.
+__device__ __forceinline__ float wire_scale(float zero, float mx, float Q) {
+  const double need = (double)mx - (double)zero;  // only its sign is used as is
+  if (!(need > 0.0)) return 0.0f;
+  uint16_t c = __half_as_ushort(__float2half_ru(__fdiv_ru(__fsub_ru(mx, zero), Q)));
+  if (c > 0x7C00u) c = 0x7C00u;  // NaN from out-of-range input: treated as +inf
+#pragma unroll
+  for (int step = 0; step < 2; step++) {
+    const uint16_t below = (uint16_t)(c - 1u);
+    if (c > 0u && (double)zero + (double)Q * (double)__half2float(__ushort_as_half(below)) >= (double)mx)
+      c = below;
+  }
+  return __half2float(__ushort_as_half(c));
+}
+
+// RN(1 / s), or 0 for a zero scale.
+__device__ __forceinline__ float wire_inv(float s) { return s > 0.0f ? __frcp_rn(s) : 0.0f; }
 
 }  // namespace tahq

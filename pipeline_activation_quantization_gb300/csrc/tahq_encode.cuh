@@ -119,6 +119,7 @@ struct EncParams {
   int slot_lo, slot_hi;
   float c_h;
   float tau;  // outlier threshold (§3.3 eq. (3): transform where r > tau)
+  int wire;   // quantise with the wire format's fp16 zero and scales
   uint8_t* codes;
   float* scales;
   float* zeros;
@@ -241,6 +242,25 @@ __device__ __forceinline__ float qmax_f(int b) {
   return __fsub_rn(__uint_as_float(0x4B000000u | ((1u << b) - 1u)), 8388608.0f);
 }
 
+// The wire format's quantiser for a tile of range [mn, mx]: off = the fp16 zero,
+// inv_lo / inv_hi = RN(1 / s_b) of the fp16 scales; meta = what the tile's scale slot
+// keeps: the scale of the one width (flat; inv_hi is then that scale too, like the fp32
+// path's), else mx, from which the offsets items take the scale of the chosen width.
+__device__ __forceinline__ void wire_params(float mn, float mx, int lo, int hi, bool flat,
+                                            float& off, float& inv_lo, float& inv_hi,
+                                            float& meta) {
+  off = wire_zero(mn);
+  const float s_lo = wire_scale(off, mx, qmax_f(lo));
+  inv_lo = wire_inv(s_lo);
+  if (flat) {
+    inv_hi = s_lo;
+    meta = s_lo;
+  } else {
+    inv_hi = wire_inv(wire_scale(off, mx, qmax_f(hi)));
+    meta = mx;
+  }
+}
+
 // Per-tile results of the tiles pass that do not depend on the width chosen later:
 // zero-point, pivot, and the range D (in `scales` until the compaction turns it into
 // D / Q).  In the one-width pass the scale and width are final at once.
@@ -320,11 +340,12 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
     float scale_lo, inv_lo, scale_hi, inv_hi;
     scale_inv<L>(D, valid ? lo : 1, sub, scale_lo, inv_lo);
     scale_inv<L>(D, valid ? hi : 1, sub, scale_hi, inv_hi);
+    float qoff = mn, meta = flat ? scale_lo : D;
+    if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, inv_hi, meta);
     if (valid) {
-      quant_store<V>(v, mn, inv_lo, lo, stage_lo + kt * slot_lo + sub * (V * lo / 8));
-      if (!flat) quant_store<V>(v, mn, inv_hi, hi, stage_hi + kt * p.slot_hi + sub * (V * hi / 8));
-      if (sub == 0)
-        put_meta(p, t0 + kt, mn, flag ? (uint8_t)i1 : (uint8_t)0xFF, flat ? scale_lo : D, flat);
+      quant_store<V>(v, qoff, inv_lo, lo, stage_lo + kt * slot_lo + sub * (V * lo / 8));
+      if (!flat) quant_store<V>(v, qoff, inv_hi, hi, stage_hi + kt * p.slot_hi + sub * (V * hi / 8));
+      if (sub == 0) put_meta(p, t0 + kt, qoff, flag ? (uint8_t)i1 : (uint8_t)0xFF, meta, flat);
     }
   }
 }
@@ -480,7 +501,9 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
     const float r = __fdiv_rn(num, den);
     const float r0 = __shfl_sync(kFull, r, base), r1s = __shfl_sync(kFull, r, base + 1);
     const bool degenerate = !(D >= 0x1p-120f);
-    const float inv_lo = degenerate ? 0.0f : r0, r1 = degenerate ? 0.0f : r1s;
+    float inv_lo = degenerate ? 0.0f : r0, r1 = degenerate ? 0.0f : r1s;
+    float qoff = mn, meta = flat ? r1 : D;
+    if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, r1, meta);
 #pragma unroll
     for (int w2 = 0; w2 < 2; w2++) {
       if (w2 == 1 && flat) break;
@@ -489,7 +512,7 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
       unsigned long long f = 0ull;
 #pragma unroll
       for (int j = 0; j < V; j++) {
-        const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
+        const float c = __fmaf_rn(__fsub_rn(v[j], qoff), inv, 12582912.0f);
         f |= (unsigned long long)(__float_as_uint(c) - 0x4B400000u) << (j * b);
       }
       unsigned char* slot = (w2 ? stage_hi : stage_lo) + kt * (G * b / 8);
@@ -500,7 +523,7 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
         if (flag) sts_bytes(slot + sub * (V * b / 8), f, 0ull, V * b / 8);
       }
     }
-    if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, flat ? r1 : D, flat);
+    if (flag && sub == 0) put_meta(p, t0 + kt, qoff, (uint8_t)i1, meta, flat);
   }
 }
 
@@ -572,12 +595,14 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
     r1 = flat ? __fdiv_rn(D, qmax_f(lo)) : __fdiv_rn(qmax_f(hi), D);
   }
   if (!(D >= 0x1p-120f)) inv_lo = r1 = 0.0f;
+  float qoff = mn, meta = flat ? r1 : D;
+  if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, r1, meta);
   // every tile as untransformed; the exact test below redoes the ones it flags
   if (valid) {
-    line_quant<Tin, kLo>(w, mn, inv_lo, lo, stage_lo + kt * (G * lo / 8) + sub * (NE * lo / 8));
+    line_quant<Tin, kLo>(w, qoff, inv_lo, lo, stage_lo + kt * (G * lo / 8) + sub * (NE * lo / 8));
     if (!flat)
-      line_quant<Tin, kHi>(w, mn, r1, hi, stage_hi + kt * (G * hi / 8) + sub * (NE * hi / 8));
-    if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, flat ? r1 : D, flat);
+      line_quant<Tin, kHi>(w, qoff, r1, hi, stage_hi + kt * (G * hi / 8) + sub * (NE * hi / 8));
+    if (sub == 0) put_meta(p, t0 + kt, qoff, (uint8_t)0xFF, meta, flat);
   }
   // tiles the pretest could not clear: one list for the block, teams of the whole block
   // take them in turn (outlier channels sit at fixed tile positions, so per-warp lists
@@ -719,11 +744,14 @@ __device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams
       const float D = __fsub_rn(mx, mn);
       const bool degenerate = !(D >= 0x1p-120f);
       const float inv_lo = degenerate ? 0.0f : __fdiv_rn(qmax_f(lo), D);
-      const float r1 =
+      float r1 =
           degenerate ? 0.0f : (flat ? __fdiv_rn(D, qmax_f(lo)) : __fdiv_rn(qmax_f(hi), D));
-      s.tb[kt] = inv_lo;
+      float il = inv_lo, qoff = mn, meta = flat ? r1 : D;
+      if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, il, r1, meta);
+      s.ta[kt] = qoff;  // phase 3 quantises from the offset
+      s.tb[kt] = il;
       s.tc[kt] = r1;
-      put_meta(p, t0 + kt, mn, (uint8_t)0xFF, flat ? r1 : D, flat);
+      put_meta(p, t0 + kt, qoff, (uint8_t)0xFF, meta, flat);
     }
   }
   __syncwarp();
@@ -1026,16 +1054,18 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   uint32_t* segmask = p.segmask + g * ((p.n_g + 31) / 32);
   constexpr int kB = 8;
   for (long long tb = tl_begin; tb < tl_end; tb += kB * kThreads) {
-    float key[kB], Dv[kB];
+    float key[kB], Dv[kB], Zv[kB];
 #pragma unroll
     for (int u = 0; u < kB; u++) {
       const long long tl = tb + u * kThreads + threadIdx.x;
       key[u] = 0.0f;
       Dv[u] = 0.0f;
+      Zv[u] = 0.0f;
       if (tl < tl_end) {
         const long long t = g * p.n_g + tl;
         if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t]);
         Dv[u] = __ldcg(&p.scales[t]);
+        if (p.wire) Zv[u] = __ldcg(&p.zeros[t]);
       }
     }
 #pragma unroll
@@ -1049,8 +1079,10 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
                (mode == kSelThreshold && rank_key(key[u], (uint32_t)tl) >= theta);
         const int b = ishi ? p.hi : p.lo;
         p.bits[t] = (uint8_t)b;
-        // the range D left by the tiles pass becomes the scale D / Q
-        p.scales[t] = (Dv[u] >= 0x1p-120f) ? __fdiv_rn(Dv[u], qmax_f(b)) : 0.0f;
+        // the range D left by the tiles pass becomes the scale D / Q (wire format: the
+        // maximum left there gives the fp16 scale of this width)
+        p.scales[t] = p.wire ? wire_scale(Zv[u], Dv[u], qmax_f(b))
+                             : ((Dv[u] >= 0x1p-120f) ? __fdiv_rn(Dv[u], qmax_f(b)) : 0.0f);
       }
       const unsigned hm = __ballot_sync(kFull, ishi);
       if (lane == 0 && tw < tl_end) {
@@ -1507,6 +1539,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.h = a.h;
   p.c_h = a.c_h;
   p.tau = a.tau;
+  p.wire = a.wire ? 1 : 0;
   p.slot_lo = G * a.lo / 8;
   p.slot_hi = G * a.hi / 8;
   p.direct = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 1 : 0;

@@ -17,6 +17,7 @@ struct EncodeArgs {
   int G, h, lo, hi;
   float c_h;                 // RN(1/sqrt(h))
   float tau;                 // outlier threshold: transform where r > tau (>= 0, +inf: never)
+  bool wire;                 // fp16 zero and scales of the wire format (else the fp32 quantiser)
   long long n_tiles, n_g, n_groups, K, group_bytes;
   int num_sms;
   const LgTables* tabs;
@@ -83,7 +84,33 @@ inline long long decode_blocks(int G, long long n_tiles) {
   return (decode_chunks(G, n_tiles) + kDecChunksPerBlock - 1) / kDecChunksPerBlock;
 }
 
+// Wire format (tahq_wire.cu): per-tile metadata into / out of one buffer.  Offsets are
+// byte offsets of the sections in `wire` (16-byte aligned); header = its 128 bytes.
+struct WirePackArgs {
+  const float* scales;   // [n] fp16-exact scales
+  const float* zeros;    // [n] fp16-exact zeros
+  const uint8_t* bits;   // [n]
+  const uint8_t* pivots; // [n] 0xFF = untransformed
+  uint8_t* wire;
+  long long n, off_map, off_meta, off_piv, off_pay, pay, total;
+  int hi, pb;
+  uint32_t header[32];
+};
+struct WireUnpackArgs {
+  const uint8_t* wire;
+  float* scales;
+  float* zeros;
+  uint8_t* bits;
+  uint8_t* pivots;
+  uint32_t* status;      // kStBadWire when the header differs from `header` (tau aside)
+  long long n, off_map, off_meta, off_piv;
+  int lo, hi, pb;
+  uint32_t header[32];
+};
+
 cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t st);
+cudaError_t launch_wire_pack(const WirePackArgs& a, cudaStream_t st);
+cudaError_t launch_wire_unpack(const WireUnpackArgs& a, cudaStream_t st);
 cudaError_t launch_encode_f32(const EncodeArgs& a, cudaStream_t st);
 cudaError_t launch_encode_bf16(const EncodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);

@@ -125,3 +125,30 @@ def test_lib_is_in_tree():
     assert os.path.exists(path)
     assert os.path.dirname(os.path.dirname(path)) == os.path.dirname(tq.__file__)
     assert ctypes.CDLL(path) is not None
+
+
+@pytest.mark.parametrize("T,C,G,lo,hi,beta,S", [(16, 256, 64, 3, 4, 3.8, 0), (48, 512, 128, 3, 4, 3.5, 16),
+                                                (33, 400, 16, 3, 5, 4.0, 11), (0, 256, 64, 3, 4, 3.5, 0),
+                                                (7, 64, 8, 1, 8, 4.4, 7)])
+def test_wire_size_agrees_with_oracle(T, C, G, lo, hi, beta, S):
+    assert tq.tahq_wire_size(T, C, G, lo, hi, beta, S) == oracle.wire_layout(T, C, G, lo, hi, beta, S)[0]
+    assert tq.tahq_wire_workspace_size(T, C, G, G, lo, hi, beta, S) >= tq.tahq_workspace_size(
+        T, C, G, G, lo, hi, beta, S)
+    assert tq.tahq_wire_decode_workspace_size(T, C, G) >= tq.tahq_decode_workspace_size(T, C, G)
+
+
+def test_wire_entry_points_reject_bad_buffers():
+    fake = 1 << 20
+    size = tq.tahq_wire_size(16, 128, 64, 3, 4, 3.5, 0)
+    # short, misaligned or missing buffers, bad tau: rejected before any launch
+    assert tq.tahq_encode_wire(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, 2.0, fake,
+                               size - 1, fake, 1 << 30, 0) == 1
+    assert tq.tahq_encode_wire(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, 2.0, fake + 8,
+                               size, fake, 1 << 30, 0) == 1
+    assert tq.tahq_encode_wire(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, -1.0, fake,
+                               size, fake, 1 << 30, 0) == 1
+    assert tq.tahq_decode_wire(0, size, 16, 128, 64, 64, 3, 4, 3.5, 0, fake, fake, 1 << 30, 0) == 1
+    assert tq.tahq_decode_wire(fake, size - 16, 16, 128, 64, 64, 3, 4, 3.5, 0, fake, fake,
+                               1 << 30, 0) == 1
+    assert tq.tahq_encode_wire(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, 2.0, fake, size,
+                               fake, 16, 0) == 3      # workspace too small
