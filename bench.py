@@ -293,28 +293,45 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    lo, hi, beta, S = w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group
+    tau = 2.0 if args.tau is None else args.tau
     with torch.cuda.stream(stream):
-        enc = tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group, tau=args.tau)
+        enc = tq.encode(x, G, h, lo, hi, beta, S, tau=args.tau)
         y = tq.decode(enc, T, C, G, h)
         dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8, device=dev)
+        if args.wire:
+            wbuf, wws = tq.encode_wire(x, G, h, lo, hi, beta, S, tau=tau)
+            y, wdws = tq.decode_wire(wbuf, T, C, G, h, lo, hi, beta, S)
     payload = enc["payload_bytes"]
     out_bufs = {k: enc[k] for k in ("codes", "scales", "zeros", "bits", "pivots")}
-    ws = enc["workspace"]
+    ws = wws if args.wire else enc["workspace"]
+
+    def do_encode(xk):
+        if args.wire:
+            tq.encode_wire(xk, G, h, lo, hi, beta, S, tau=tau, out=wbuf, workspace=wws, stream=stream)
+        else:
+            tq.encode(xk, G, h, lo, hi, beta, S, out=out_bufs, workspace=ws, stream=stream,
+                      tau=args.tau)
+
+    def do_decode():
+        if args.wire:
+            tq.decode_wire(wbuf, T, C, G, h, lo, hi, beta, S, out=y, workspace=wdws, stream=stream)
+        else:
+            tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
     K_hi = tq.tahq_hi_count(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
     n_g = (w.tokens_per_group or T) * (C // G)
     ranked = 0 < K_hi < n_g
     # encode: the queue table and the persistent kernel (ranked) or one kernel (one width);
     # decode: totals, scan, decode
-    launches = (2 if ranked else 1) + 3
+    launches = (2 if ranked else 1) + 3 + (2 if args.wire else 0)  # wire: pack, unpack
     enc_kernel = (f"k_encode<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}> (+ k_items)" if ranked
                   else f"k_encode_flat<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>")
 
     def step(ev, k=0):
         ev[0].record(stream)
-        tq.encode(xs[k % n_tensors], G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
-                  out=out_bufs, workspace=ws, stream=stream, tau=args.tau)
+        do_encode(xs[k % n_tensors])
         ev[1].record(stream)
-        tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
+        do_decode()
         ev[2].record(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -347,6 +364,9 @@ def run_gpu(args):
         tot_ms = float(t.item())
 
     in_b, enc_b, dec_b = _alg_bytes(w, payload)
+    if args.wire:  # the whole buffer is written, then read
+        wire_b = tq.tahq_wire_size(T, C, G, lo, hi, beta, S)
+        enc_b, dec_b = in_b + wire_b, wire_b + 4 * w.elements
     peak, peak_kind = _peaks()
     ms_step = tot_ms / args.steps
     value = world * in_b * args.steps / (tot_ms * 1e-3) / 1e9
@@ -354,6 +374,8 @@ def run_gpu(args):
     enc_gbs, dec_gbs = enc_b / (e_ms * 1e-3) / 1e9, dec_b / (d_ms * 1e-3) / 1e9
     dom = ("decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
     dom_name = f"k_decode<{G}> (+ k_dec_totals, k_dec_scan)" if dom[0] == "decode" else enc_kernel
+    if args.wire:
+        dom_name += " + k_wire_unpack" if dom[0] == "decode" else " + k_wire_pack"
 
     # end to end through the public API: pinned host input -> device, encode, decode,
     # decoded tensor -> pinned host
@@ -369,9 +391,8 @@ def run_gpu(args):
                     x_dev.view(torch.int16).copy_(x_host, non_blocking=True)
                 else:
                     x_dev.copy_(x_host, non_blocking=True)
-                tq.encode(x_dev, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group,
-                          out=out_bufs, workspace=ws, stream=stream, tau=args.tau)
-                tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
+                do_encode(x_dev)
+                do_decode()
                 y_host.copy_(y, non_blocking=True)
             e2e_step()
             stream.synchronize()
@@ -397,7 +418,8 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}",
-                                                     "fresh_tensors_cycled": n_tensors},
+                                                     "fresh_tensors_cycled": n_tensors,
+                                                     "format": "wire" if args.wire else "arrays"},
                                                   tau=args.tau),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -410,7 +432,8 @@ def run_gpu(args):
                      "achieved": round(dom[1] / (dom[2] * 1e-3) / 1e9, 2), "peak": peak,
                      "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
                      "frac": round(dom[1] / (dom[2] * 1e-3) / 1e9 / peak, 4),
-                     "traffic": _traffic_for(dom_name, w.name) if args.tau is None else None},
+                     "traffic": (_traffic_for(dom_name, w.name)
+                                 if args.tau is None and not args.wire else None)},
         "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e, "gpu_launches": launches * args.steps,
         "gpu_launches_per_step": launches, "clocks": clocks,
@@ -438,6 +461,8 @@ def main():
     ap.add_argument("--budget", type=float, default=None)
     ap.add_argument("--tau", type=float, default=None,
                     help="outlier threshold (default: the method's 2.0)")
+    ap.add_argument("--wire", action="store_true",
+                    help="time the wire format (tahq_encode_wire / tahq_decode_wire)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

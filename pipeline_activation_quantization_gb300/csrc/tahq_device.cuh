@@ -393,22 +393,31 @@ __device__ __forceinline__ float wire_zero(float mn) {
   return __half2float(__float2half_rd(mn));
 }
 
+// zero + Q s >= mx, decided exactly in fp32: Q s is exact (8 x 11 bits), TwoSum gives
+// zero + Q s = sum + err exactly with sum = RN(zero + Q s) and |err| <= ulp(sum) / 2, and
+// since sum and mx are floats the inequality holds iff sum > mx, or sum == mx and
+// err >= 0.  (An infinite zero gives NaN terms: not covered, as no finite scale covers.)
+__device__ __forceinline__ bool wire_covers(float zero, float Q, float s, float mx) {
+  const float a = __fmul_rn(Q, s);
+  const float sum = __fadd_rn(a, zero);
+  const float bb = __fsub_rn(sum, a);
+  const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(sum, bb)), __fsub_rn(zero, bb));
+  return sum > mx || (sum == mx && err >= 0.0f);
+}
+
 // The smallest fp16 scale covering [zero, mx] at Q steps, as fp32 (exact; +inf when no
 // finite fp16 value does).  RU(RU(mx - zero) / Q) rounded up to fp16 is never below the
 // answer and at most one fp16 step above it (the fp32 over-estimate is under 2^-22
 // relative, the fp16 spacing 2^-10 relative or 2^-24 absolute), so an exact test of the
-// fp16 value below settles it: zero + Q s is a sum of multiples of 2^-24 below 2^25 in
-// size, exact in double, and so is its comparison with the fp32 mx.
+// fp16 value below settles it.
 __device__ __forceinline__ float wire_scale(float zero, float mx, float Q) {
-  const double need = (double)mx - (double)zero;  // only its sign is used as is
-  if (!(need > 0.0)) return 0.0f;
+  if (!(mx > zero)) return 0.0f;
   uint16_t c = __half_as_ushort(__float2half_ru(__fdiv_ru(__fsub_ru(mx, zero), Q)));
   if (c > 0x7C00u) c = 0x7C00u;  // NaN from out-of-range input: treated as +inf
 #pragma unroll
   for (int step = 0; step < 2; step++) {
     const uint16_t below = (uint16_t)(c - 1u);
-    if (c > 0u && (double)zero + (double)Q * (double)__half2float(__ushort_as_half(below)) >= (double)mx)
-      c = below;
+    if (c > 0u && wire_covers(zero, Q, __half2float(__ushort_as_half(below)), mx)) c = below;
   }
   return __half2float(__ushort_as_half(c));
 }

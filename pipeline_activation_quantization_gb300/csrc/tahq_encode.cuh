@@ -503,7 +503,15 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
     const bool degenerate = !(D >= 0x1p-120f);
     float inv_lo = degenerate ? 0.0f : r0, r1 = degenerate ? 0.0f : r1s;
     float qoff = mn, meta = flat ? r1 : D;
-    if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, r1, meta);
+    if (p.wire) {
+      // lane 0 of the team searches the scale of bits_lo, the others that of bits_hi
+      qoff = wire_zero(mn);
+      const float sm = wire_scale(qoff, mx, qmax_f(sub != 0 && !flat ? hi : lo));
+      const float s_lo = __shfl_sync(kFull, sm, base), s_hi = __shfl_sync(kFull, sm, base + 1);
+      inv_lo = wire_inv(s_lo);
+      r1 = flat ? s_lo : wire_inv(s_hi);
+      meta = flat ? s_lo : mx;
+    }
 #pragma unroll
     for (int w2 = 0; w2 < 2; w2++) {
       if (w2 == 1 && flat) break;
@@ -596,7 +604,21 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   }
   if (!(D >= 0x1p-120f)) inv_lo = r1 = 0.0f;
   float qoff = mn, meta = flat ? r1 : D;
-  if (p.wire) wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, r1, meta);
+  if (p.wire) {
+    if constexpr (LPT >= 2) {
+      // the tile's even lanes search the scale of bits_lo, its odd lanes that of bits_hi
+      qoff = wire_zero(mn);
+      const bool odd = sub & 1;
+      const float sm = wire_scale(qoff, mx, qmax_f(odd && !flat ? hi : lo));
+      const float so = __shfl_xor_sync(kFull, sm, 1);
+      const float s_lo = odd ? so : sm, s_hi = odd ? sm : so;
+      inv_lo = wire_inv(s_lo);
+      r1 = flat ? s_lo : wire_inv(s_hi);
+      meta = flat ? s_lo : mx;
+    } else {
+      wire_params(mn, mx, lo, hi, flat, qoff, inv_lo, r1, meta);
+    }
+  }
   // every tile as untransformed; the exact test below redoes the ones it flags
   if (valid) {
     line_quant<Tin, kLo>(w, qoff, inv_lo, lo, stage_lo + kt * (G * lo / 8) + sub * (NE * lo / 8));

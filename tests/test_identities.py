@@ -67,3 +67,27 @@ def test_ratio_flag_without_division_random_and_special():
         for s in specials:
             m1 = np.full_like(m2, s)
             np.testing.assert_array_equal(_flag_div(m1, m2), _flag_nodiv(m1, m2))
+
+
+def _covers_fp32(z, Q, s, mx):
+    a = F(F(Q) * F(s))
+    sm = F(a + F(z))
+    bb = F(sm - a)
+    err = F(F(a - F(sm - bb)) + F(F(z) - bb))
+    return bool(sm > F(mx) or (sm == F(mx) and err >= 0))
+
+
+def test_wire_cover_test_in_fp32_is_exact():
+    # The wire format's scale is the smallest fp16 s with zero + Q s >= max (exact); the
+    # encoder decides the inequality in fp32 with an error-free TwoSum.  Checked against
+    # exact rationals where it is hardest: max at, just above and just below zero + Q s.
+    from fractions import Fraction
+    rng = np.random.default_rng(13)
+    for _ in range(40000):
+        z = float(np.float16(rng.standard_normal() * 10 ** rng.uniform(-7, 4)))
+        s = float(np.float16(abs(rng.standard_normal()) * 10 ** rng.uniform(-7, 3)))
+        Q = int(rng.choice([1, 3, 7, 15, 31, 255]))
+        exact = Fraction(z) + Q * Fraction(s)
+        near = F(float(exact))
+        for mx in (near, np.nextafter(near, F(np.inf)), np.nextafter(near, F(-np.inf))):
+            assert _covers_fp32(z, Q, s, float(mx)) == (exact >= Fraction(float(mx)))
