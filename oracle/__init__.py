@@ -71,6 +71,10 @@ def lib():
                                         p, p, p, p, p, p, p]),
                 "oracle_encode_tau": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
                                             p, p, p, p, p, p, p]),
+                "oracle_encode_alloc": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
+                                              i32, p, p, p, p, p, p, p]),
+                "oracle_entropy_key_n": (f32, [p, i64]),
+                "oracle_payload_size_alloc": (i64, [i64, i64, i32, i32, i32, i32, f32, i64]),
                 "oracle_decode": (i32, [p, i64, p, p, p, p, i64, i64, i32, i32, p]),
                 "oracle_f16_value": (C.c_double, [C.c_uint16]),
                 "oracle_f16_round_down": (C.c_uint16, [f32]),
@@ -201,21 +205,30 @@ def allocate(H, K: int, lo: int, hi: int) -> np.ndarray:
     return bits
 
 
-def payload_size(T, Cc, G, lo, hi, budget, S) -> int:
-    return int(lib().oracle_payload_size(T, Cc, G, lo, hi, budget, S))
+def payload_size(T, Cc, G, lo, hi, budget, S, alloc_tile: int | None = None) -> int:
+    if alloc_tile is None:
+        return int(lib().oracle_payload_size(T, Cc, G, lo, hi, budget, S))
+    return int(lib().oracle_payload_size_alloc(T, Cc, G, alloc_tile, lo, hi, budget, S))
+
+
+def entropy_key_n(a) -> float:
+    """Entropy key over any power-of-two number of values (an allocation tile)."""
+    a = _f32(a)
+    return float(lib().oracle_entropy_key_n(_ptr(a), a.size))
 
 
 # ------------------------------------------------------------------------ whole tensor
 
 def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: int = 0,
            threads: int = 1, want_keys: bool = False, want_near: bool = False,
-           tau: float | None = None) -> dict:
+           tau: float | None = None, alloc_tile: int | None = None) -> dict:
     """Encode ``x`` ([T, C] float32, or uint16 bf16 bit patterns).
 
     Returns a dict with ``codes, scales, zeros, bits, pivots`` (and ``keys`` [n_tiles]
     float32 entropy keys, ``near`` [T, C] boundary flags when asked).  With
     ``threads > 1`` the independent token groups run on host threads.  ``tau`` is the
-    outlier threshold (None: the method's 2.0).
+    outlier threshold (None: the method's 2.0); ``alloc_tile`` the allocation tile A
+    (None: A = G), with one key per allocation tile (``keys`` then has n / (A / G)).
     """
     x = np.ascontiguousarray(x)
     dtype = BF16 if x.dtype == np.uint16 else F32
@@ -224,7 +237,8 @@ def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: in
     T, Cc = x.shape
     S = S or T
     n = T * (Cc // G)
-    total = payload_size(T, Cc, G, lo, hi, budget, S)
+    A = alloc_tile or G
+    total = payload_size(T, Cc, G, lo, hi, budget, S, None if A == G else A)
     if total < 0:
         raise ValueError("invalid codec arguments")
     out = {
@@ -235,7 +249,7 @@ def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: in
         "pivots": np.zeros(n, np.uint8),
     }
     if want_keys:
-        out["keys"] = np.zeros(n, np.float32)
+        out["keys"] = np.zeros(n // (A // G), np.float32)
     if want_near:
         out["near"] = np.zeros((T, Cc), np.uint8)
     if T == 0:
@@ -244,16 +258,23 @@ def encode(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: in
     n_g = S * (Cc // G)
     gbytes = total // ng
 
+    na_g = n_g // (A // G)
+
     def run(g):
         sl = slice(g * n_g, (g + 1) * n_g)
+        ka = slice(g * na_g, (g + 1) * na_g)
         args = (_ptr(x[g * S:(g + 1) * S]), dtype, S, Cc, G, h, lo, hi, budget, S)
-        if tau is not None:
-            args = args + (float(tau),)
-        rc = (lib().oracle_encode if tau is None else lib().oracle_encode_tau)(
+        if A != G:
+            fn, args = lib().oracle_encode_alloc, args + (2.0 if tau is None else float(tau), A)
+        elif tau is not None:
+            fn, args = lib().oracle_encode_tau, args + (float(tau),)
+        else:
+            fn = lib().oracle_encode
+        rc = fn(
             *args,
             _ptr(out["codes"][g * gbytes:(g + 1) * gbytes]), _ptr(out["scales"][sl]),
             _ptr(out["zeros"][sl]), _ptr(out["bits"][sl]), _ptr(out["pivots"][sl]),
-            _ptr(out["keys"][sl]) if want_keys else None,
+            _ptr(out["keys"][ka]) if want_keys else None,
             _ptr(out["near"][g * S:(g + 1) * S]) if want_near else None)
         if rc != 0:
             raise RuntimeError(f"oracle_encode failed on group {g}")

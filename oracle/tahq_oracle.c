@@ -152,6 +152,30 @@ float oracle_entropy_key(const float *a, int G)
     return oracle_lg(L) - S / L;
 }
 
+/* The same key over n values (an allocation tile of n = A channels, §3.2 "Tile
+ * decomposition"; n a power of two >= 2), same order: fused first level of S over the
+ * pairs (2j, 2j+1), then both sums pairwise in natural order.  NaN if the scratch
+ * cannot be allocated. */
+float oracle_entropy_key_n(const float *a, int64_t n)
+{
+    if (n <= 128) return oracle_entropy_key(a, (int)n);
+    float *L1 = (float *)malloc((size_t)(n / 2) * sizeof(float));
+    float *S1 = (float *)malloc((size_t)(n / 2) * sizeof(float));
+    if (!L1 || !S1) { free(L1); free(S1); return NAN; }
+    for (int64_t j = 0; j < n / 2; j++) {
+        float m0 = fabsf(a[2 * j]), m1 = fabsf(a[2 * j + 1]);
+        float l0 = (m0 == 0.0f) ? 0.0f : oracle_lg(m0), l1 = (m1 == 0.0f) ? 0.0f : oracle_lg(m1);
+        L1[j] = m0 + m1;
+        S1[j] = fmaf(m1, l1, m0 * l0);
+    }
+    float L = oracle_pairwise_sum(L1, (int)(n / 2));
+    float S = oracle_pairwise_sum(S1, (int)(n / 2));
+    free(L1);
+    free(S1);
+    if (L == 0.0f) return 0.0f;
+    return oracle_lg(L) - S / L;
+}
+
 /* eq. (1)-(2) as printed (with the minus sign restored), in double with natural log:
  * p_k = |a_k| / (||a||_1 + eps),  H = -sum_k p_k log(p_k + vsig).  Diagnostic only. */
 double oracle_entropy_literal(const float *a, int G, double eps, double vsig)
@@ -358,6 +382,22 @@ static int valid_bits(int lo, int hi, float budget)
     return 1;
 }
 
+/* Payload bytes with allocation tiles of A channels (A = G: the plain codec): K of the
+ * n_gA = S C / A allocation tiles of a group get hi, i.e. K A / G quantisation tiles. */
+int64_t oracle_payload_size_alloc(int64_t T, int64_t C, int G, int A, int lo, int hi,
+                                  float budget, int64_t S)
+{
+    if (!valid_shape(T, C, G, G) || !valid_bits(lo, hi, budget)) return -1;
+    if (A < G || A % G || C % A || ((A / G) & (A / G - 1))) return -1;
+    if (S == 0) S = T;
+    if (T == 0) return 0;
+    if (S <= 0 || T % S) return -1;
+    int64_t n_g = S * (C / G), n_ga = S * (C / A);
+    int64_t K = oracle_hi_count(n_ga, lo, hi, budget);
+    int64_t per_group = n_g * G * lo / 8 + K * (A / G) * G * (hi - lo) / 8;
+    return (T / S) * per_group;
+}
+
 int64_t oracle_payload_size(int64_t T, int64_t C, int G, int lo, int hi, float budget, int64_t S)
 {
     if (!valid_shape(T, C, G, G) || !valid_bits(lo, hi, budget)) return -1;
@@ -383,39 +423,57 @@ static void load_tile(const void *x, int dtype, int64_t off, int G, float *a)
 /* Encode a [T, C] tensor with outlier threshold tau (>= 0, +inf allowed).  keys (n_tiles
  * floats) and near (T*C bytes) are optional outputs for tests.  Returns 0, or -1 on
  * invalid arguments / allocation failure. */
-int oracle_encode_tau(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo,
-                      int hi, float budget, int64_t S, float tau, uint8_t *codes, float *scales,
-                      float *zeros, uint8_t *bits, uint8_t *pivots, float *keys, uint8_t *near)
+/* Encode with allocation tiles of A channels (§3.2 "Tile decomposition": A a multiple
+ * of G aligned with the quantisation tiles, A = C the token-level allocation; here
+ * A / G a power of two and A | C): one entropy key per allocation tile over its A values,
+ * ranked per group, and every quantisation tile takes its allocation tile's width.  The
+ * outlier test, the transform and the quantiser stay per quantisation tile.  keys holds
+ * n / (A / G) floats. */
+int oracle_encode_alloc(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo,
+                        int hi, float budget, int64_t S, float tau, int A, uint8_t *codes,
+                        float *scales, float *zeros, uint8_t *bits, uint8_t *pivots, float *keys,
+                        uint8_t *near)
 {
     if (!valid_shape(T, C, G, h) || !valid_bits(lo, hi, budget)) return -1;
     if (!(tau >= 0.0f)) return -1;  /* negative or NaN */
+    if (A < G || A % G || C % A || ((A / G) & (A / G - 1))) return -1;
     if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
     if (S == 0) S = T;
     if (T == 0) return 0;
     if (S <= 0 || T % S) return -1;
-    int64_t W = C / G, n = T * W, n_g = S * W;
-    float *H = keys ? keys : (float *)malloc((size_t)n * sizeof(float));
+    int64_t W = C / G, n = T * W, m = A / G, na = n / m, n_ga = S * (C / A);
+    float *H = keys ? keys : (float *)malloc((size_t)na * sizeof(float));
     int *piv = (int *)malloc((size_t)n * sizeof(int));
-    if (!H || !piv) { if (!keys) free(H); free(piv); return -1; }
+    uint8_t *abits = (uint8_t *)malloc((size_t)na);
+    float *row = (float *)malloc((size_t)A * sizeof(float));
+    if (!H || !piv || !abits || !row) {
+        if (!keys) free(H);
+        free(piv); free(abits); free(row);
+        return -1;
+    }
     float a[128];
     uint8_t q[128];
 
-    /* 1. per-tile statistics on the raw tile */
+    /* 1. per-tile outlier test on the raw tile; per allocation tile its entropy key */
     for (int64_t t = 0; t < n; t++) {
         load_tile(x, dtype, t * G, G, a);
         int d, flag;
         oracle_outlier_tau(a, G, tau, &d, &flag, NULL, NULL);
-        H[t] = oracle_entropy_key(a, G);
         piv[t] = flag ? d : -1;
     }
-    /* 2. per-group allocation */
-    int64_t K = oracle_hi_count(n_g, lo, hi, budget);
+    for (int64_t i = 0; i < na; i++) {
+        for (int64_t k = 0; k < m; k++) load_tile(x, dtype, (i * m + k) * G, G, row + k * G);
+        H[i] = oracle_entropy_key_n(row, A);
+    }
+    /* 2. per-group allocation over the allocation tiles; each tile takes its tile's width */
+    int64_t K = oracle_hi_count(n_ga, lo, hi, budget);
     for (int64_t g = 0; g < T / S; g++)
-        if (oracle_allocate(H + g * n_g, n_g, K, lo, hi, bits + g * n_g)) {
+        if (oracle_allocate(H + g * n_ga, n_ga, K, lo, hi, abits + g * n_ga)) {
             if (!keys) free(H);
-            free(piv);
+            free(piv); free(abits); free(row);
             return -1;
         }
+    for (int64_t t = 0; t < n; t++) bits[t] = abits[t / m];
     /* 3. transform, quantise and pack, slots in tile order */
     int64_t off = 0;
     for (int64_t t = 0; t < n; t++) {
@@ -428,8 +486,17 @@ int oracle_encode_tau(const void *x, int dtype, int64_t T, int64_t C, int G, int
         off += G * b / 8;
     }
     if (!keys) free(H);
-    free(piv);
+    free(piv); free(abits); free(row);
     return 0;
+}
+
+/* Allocation tile = quantisation tile (the pages' default, A = G), threshold tau. */
+int oracle_encode_tau(const void *x, int dtype, int64_t T, int64_t C, int G, int h, int lo,
+                      int hi, float budget, int64_t S, float tau, uint8_t *codes, float *scales,
+                      float *zeros, uint8_t *bits, uint8_t *pivots, float *keys, uint8_t *near)
+{
+    return oracle_encode_alloc(x, dtype, T, C, G, h, lo, hi, budget, S, tau, G, codes, scales,
+                               zeros, bits, pivots, keys, near);
 }
 
 /* The method as the pages state it: tau = 2.0 (§3.3). */

@@ -556,3 +556,75 @@ def test_appendix_g_width_mixes(lo, hi, beta, frac_hi):
     n_hi = np.count_nonzero(r["bits"] == hi)
     assert r["codes"].size == (n * lo + n_hi * (hi - lo)) * G // 8
     assert r["codes"].size * 8 <= beta * T * Cc
+
+
+# ------------------------------------------------------------------ allocation tiles A != G
+# (§3.2 "Tile decomposition": one key per allocation tile of A channels, A a multiple of G
+# aligned with the quantisation tiles; A = C is the token-level allocation)
+
+@pytest.mark.parametrize("n", [256, 1024, 8192])
+def test_entropy_key_n_closed_forms(n):
+    assert oracle.entropy_key_n(np.full(n, 0.5, F32)) == np.log2(n)           # flat
+    for k in (1, 2, 4, 64):
+        a = np.zeros(n, F32)
+        a[np.arange(k) * (n // k)] = -4.0 if k % 2 else 0.5         # powers of two: exact
+        assert oracle.entropy_key_n(a) == np.log2(k)                          # k equal spikes
+    assert oracle.entropy_key_n(np.zeros(n, F32)) == 0.0
+
+
+def test_entropy_key_n_matches_the_literal_entropy():
+    rng = np.random.default_rng(31)
+    for n in (256, 2048):
+        for _ in range(20):
+            a = (rng.standard_normal(n) * rng.choice([1, 50], n, p=[0.99, 0.01])).astype(F32)
+            p = np.abs(a.astype(np.float64)) / np.abs(a.astype(np.float64)).sum()
+            lit = -np.sum(np.where(p > 0, p * np.log2(np.where(p > 0, p, 1)), 0.0))
+            assert abs(oracle.entropy_key_n(a) - lit) < 2e-5
+
+
+@pytest.mark.parametrize("A,S", [(128, 16), (256, 8), (512, 48), (64, 16)])
+def test_encode_alloc_tiles(A, S):
+    x = _small(C=512)
+    T, C = x.shape
+    G = 64
+    m = A // G
+    r = oracle.encode(x, G, G, 3, 4, 3.5, S, want_keys=True, alloc_tile=A)
+    n = T * C // G
+    assert r["keys"].size == n // m
+    bits = r["bits"].reshape(-1, m)
+    assert np.all(bits == bits[:, :1])                        # one width per allocation tile
+    n_ga = S * C // A
+    K = oracle.hi_count(n_ga, 3, 4, 3.5)
+    for g in range(T // S):
+        sl = slice(g * n_ga, (g + 1) * n_ga)
+        assert np.count_nonzero(bits[sl, 0] == 4) == K
+        assert np.array_equal(bits[sl, 0], oracle.allocate(r["keys"][sl], K, 3, 4))
+    rows = x.reshape(-1, A)
+    for i in range(0, rows.shape[0], 7):
+        assert r["keys"][i] == oracle.entropy_key_n(rows[i])
+    assert r["codes"].size == oracle.payload_size(T, C, G, 3, 4, 3.5, S, A) == \
+        T // S * (S * C // G * G * 3 // 8 + K * A // 8)
+    # the per-tile steps do not depend on A
+    base = oracle.encode(x, G, G, 3, 4, 3.5, S)
+    assert np.array_equal(r["pivots"], base["pivots"])
+    if A == G:
+        for k in base:
+            assert np.array_equal(base[k], r[k]), k
+
+
+def test_token_level_allocation_is_a_special_case():
+    x = _small(C=512)
+    T, C = x.shape
+    r = oracle.encode(x, 64, 64, 3, 4, 3.5, 0, want_keys=True, alloc_tile=C)
+    tok_bits = r["bits"].reshape(T, -1)
+    assert np.all(tok_bits == tok_bits[:, :1])
+    hi = tok_bits[:, 0] == 4
+    assert hi.sum() == oracle.hi_count(T, 3, 4, 3.5)
+    assert r["keys"][hi].min() >= r["keys"][~hi].max()
+
+
+def test_invalid_alloc_tile_rejected():
+    x = _small(C=512)
+    for A in (32, 96, 192, 1024):     # below G, not a multiple, not a power-of-two multiple, above C
+        with pytest.raises((RuntimeError, ValueError)):
+            oracle.encode(x, 64, 64, 3, 4, 3.5, 0, alloc_tile=A)
