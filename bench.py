@@ -158,25 +158,26 @@ def _src_sha() -> str:
 
 # ------------------------------------------------------------------ the oracle (CPU)
 
-def _oracle_step(x, w, tokens, tau=None):
+def _oracle_step(x, w, tokens, tau=None, alloc_tile=None):
     import oracle
     xs = x[:tokens]
     S = min(w.tokens_per_group or w.tokens, tokens)
-    r = oracle.encode(xs, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, tau=tau)
+    r = oracle.encode(xs, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, tau=tau,
+                      alloc_tile=alloc_tile)
     oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], tokens, w.channels,
                   w.tile, w.hblock)
 
 
-def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0, tau=None) -> dict:
+def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0, tau=None, alloc_tile=None) -> dict:
     """The oracle, single thread, on whole token groups of the same tensor."""
     S = w.tokens_per_group or w.tokens
     t0 = time.perf_counter()
-    _oracle_step(x, w, S, tau)
+    _oracle_step(x, w, S, tau, alloc_tile)
     one = time.perf_counter() - t0
     groups = max(1, min(w.tokens // S, int(target_s / max(one, 1e-3))))
     t0 = time.perf_counter()
     for g in range(groups):
-        _oracle_step(x[g * S:], w, S, tau)
+        _oracle_step(x[g * S:], w, S, tau, alloc_tile)
     dt = time.perf_counter() - t0
     toks = groups * S
     gbs = toks * w.channels * (4 if w.dtype == "f32" else 2) / dt / 1e9
@@ -186,7 +187,8 @@ def cpu_baseline(w: synth.Workload, x, target_s: float = 12.0, tau=None) -> dict
                       f"single-threaded scalar C (-O2 -ffp-contract=off), {dt:.1f} s"}
 
 
-def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0, tau=None) -> dict:
+def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0, tau=None,
+                           alloc_tile=None) -> dict:
     """The same oracle with its token groups (encode) and token ranges (decode) on all host
     cores, whole tensor per step."""
     import oracle
@@ -196,7 +198,7 @@ def cpu_baseline_all_cores(w: synth.Workload, x, target_s: float = 6.0, tau=None
 
     def step():
         r = oracle.encode(x, w.tile, w.hblock, w.bits_lo, w.bits_hi, w.budget, S, threads=cores,
-                          tau=tau)
+                          tau=tau, alloc_tile=alloc_tile)
         oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], w.tokens,
                       w.channels, w.tile, w.hblock, threads=cores)
 
@@ -226,15 +228,15 @@ def run_reference(args):
     S = w.tokens_per_group or w.tokens
     # size each step's sample so that warm-up + timed steps take about 90 s of host time
     t0 = time.perf_counter()
-    _oracle_step(x, w, 16, args.tau)
+    _oracle_step(x, w, 16, args.tau, args.alloc_tile or None)
     per_token = (time.perf_counter() - t0) / 16
     tok = int(max(1, min(S, 90.0 / max(1, args.steps + args.warmup) / max(per_token, 1e-9))))
     for _ in range(args.warmup):
-        _oracle_step(x, w, tok, args.tau)
+        _oracle_step(x, w, tok, args.tau, args.alloc_tile or None)
     t0 = time.perf_counter()
     for k in range(args.steps):
         g = k % max(1, w.tokens // tok)
-        _oracle_step(x[g * tok:], w, tok, args.tau)
+        _oracle_step(x[g * tok:], w, tok, args.tau, args.alloc_tile or None)
     dt = time.perf_counter() - t0
     in_b = tok * w.channels * (4 if w.dtype == "f32" else 2)
     gbs = in_b * args.steps / dt / 1e9
@@ -243,7 +245,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config(w, {"sample_tokens_per_step": tok}, tau=args.tau),
+        "config": _config(w, {"sample_tokens_per_step": tok,
+                              "alloc_tile": args.alloc_tile or w.tile}, tau=args.tau),
         "tokens_per_s": round(tok * args.steps / dt, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step encodes+decodes {tok} consecutive tokens of the "
@@ -296,7 +299,7 @@ def run_gpu(args):
     lo, hi, beta, S = w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group
     tau = 2.0 if args.tau is None else args.tau
     with torch.cuda.stream(stream):
-        enc = tq.encode(x, G, h, lo, hi, beta, S, tau=args.tau)
+        enc = tq.encode(x, G, h, lo, hi, beta, S, tau=args.tau, alloc_tile=args.alloc_tile or None)
         y = tq.decode(enc, T, C, G, h)
         dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8, device=dev)
         if args.wire:
@@ -311,7 +314,7 @@ def run_gpu(args):
             tq.encode_wire(xk, G, h, lo, hi, beta, S, tau=tau, out=wbuf, workspace=wws, stream=stream)
         else:
             tq.encode(xk, G, h, lo, hi, beta, S, out=out_bufs, workspace=ws, stream=stream,
-                      tau=args.tau)
+                      tau=args.tau, alloc_tile=args.alloc_tile or None)
 
     def do_decode():
         if args.wire:
@@ -320,6 +323,9 @@ def run_gpu(args):
             tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=stream)
     K_hi = tq.tahq_hi_count(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
     n_g = (w.tokens_per_group or T) * (C // G)
+    if args.alloc_tile:
+        n_g //= args.alloc_tile // G      # allocation tiles a group
+        K_hi = int(np.floor((w.budget - w.bits_lo) * n_g / (w.bits_hi - w.bits_lo)))
     ranked = 0 < K_hi < n_g
     # encode: the queue table and the persistent kernel (ranked) or one kernel (one width);
     # decode: totals, scan, decode
@@ -409,9 +415,11 @@ def run_gpu(args):
 
     if rank != 0:
         return 0
-    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, x_np, tau=args.tau)
+    A = args.alloc_tile or None
+    cpu = (None if args.no_cpu_baseline or world > 1
+           else cpu_baseline(w, x_np, tau=args.tau, alloc_tile=A))
     cpu_all = (None if args.no_cpu_baseline or world > 1
-               else cpu_baseline_all_cores(w, x_np, tau=args.tau))
+               else cpu_baseline_all_cores(w, x_np, tau=args.tau, alloc_tile=A))
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
@@ -419,7 +427,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": _config(w, {"parallelism": f"replicas{world}",
                                                      "fresh_tensors_cycled": n_tensors,
-                                                     "format": "wire" if args.wire else "arrays"},
+                                                     "format": "wire" if args.wire else "arrays",
+                                                     "alloc_tile": args.alloc_tile or G},
                                                   tau=args.tau),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
@@ -433,7 +442,8 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
                      "frac": round(dom[1] / (dom[2] * 1e-3) / 1e9 / peak, 4),
                      "traffic": (_traffic_for(dom_name, w.name)
-                                 if args.tau is None and not args.wire else None)},
+                                 if args.tau is None and not args.wire and not args.alloc_tile
+                                 else None)},
         "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e, "gpu_launches": launches * args.steps,
         "gpu_launches_per_step": launches, "clocks": clocks,
@@ -461,6 +471,8 @@ def main():
     ap.add_argument("--budget", type=float, default=None)
     ap.add_argument("--tau", type=float, default=None,
                     help="outlier threshold (default: the method's 2.0)")
+    ap.add_argument("--alloc-tile", type=int, default=0,
+                    help="allocation tile A in channels (default: the tile)")
     ap.add_argument("--wire", action="store_true",
                     help="time the wire format (tahq_encode_wire / tahq_decode_wire)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -106,18 +106,33 @@ tahq_status tahq_encode(const void *x, tahq_dtype dtype, int64_t tokens, int64_t
                         void *stream);
 
 /*
- * tahq_encode with the outlier threshold as an argument ("TAH-Quant" §3.3 eq. (3); its
- * Appendix F compares tau = 0, 2, 4 and infinity).  A tile is transformed when
- * r = |a(1)| / (|a(2)| + 1e-12) > tau (fp32 IEEE division, strict): tau = 0 transforms
- * every tile whose r is above zero, tau = INFINITY none, tau = 2.0f is tahq_encode.  The
- * entropy keys, and so the widths, do not depend on tau.  Same arguments, layouts,
- * ownership and errors as tahq_encode; a negative or NaN tau is TAHQ_ERR_ARG.
+ * tahq_encode with two of the method's parameters as arguments.
+ *   tau: the outlier threshold ("TAH-Quant" §3.3 eq. (3); its Appendix F compares
+ *     tau = 0, 2, 4 and infinity).  A tile is transformed when
+ *     r = |a(1)| / (|a(2)| + 1e-12) > tau (fp32 IEEE division, strict): tau = 0
+ *     transforms every tile whose r is above zero, tau = INFINITY none.  The entropy keys,
+ *     and so the widths, do not depend on tau.  Negative or NaN: TAHQ_ERR_ARG.
+ *   alloc_tile: the allocation tile A of §3.2 "Tile decomposition" (0 = tile, the pages'
+ *     default; A = channels is the token-level allocation).  One entropy key per A
+ *     consecutive channels of a token (the key over its A values, same canonical order),
+ *     ranked per group; K = floor((budget - bits_lo) * n_A / (bits_hi - bits_lo)) of the
+ *     group's n_A = tokens_per_group * channels / A allocation tiles get bits_hi, and every
+ *     tile takes its allocation tile's width; the outlier test, transform and quantiser
+ *     stay per tile.  A must be a power-of-two multiple of tile dividing channels
+ *     (else TAHQ_ERR_ARG) and A * sizeof(element) <= 32768 (else TAHQ_ERR_UNSUPPORTED).
+ *     The payload is then tahq_payload_size_ex's; tahq_workspace_size is enough for any A.
+ * tau = 2.0f, alloc_tile = 0 is tahq_encode.  Same arguments, layouts, ownership and
+ * errors as tahq_encode otherwise.
  */
 tahq_status tahq_encode_ex(const void *x, tahq_dtype dtype, int64_t tokens, int64_t channels,
                            int tile, int hblock, int bits_lo, int bits_hi, float budget,
-                           int64_t tokens_per_group, float tau, uint8_t *codes, float *scales,
-                           float *zeros, uint8_t *bits, uint8_t *pivots, void *workspace,
-                           size_t workspace_bytes, void *stream);
+                           int64_t tokens_per_group, float tau, int alloc_tile, uint8_t *codes,
+                           float *scales, float *zeros, uint8_t *bits, uint8_t *pivots,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Payload bytes with allocation tiles of alloc_tile channels (0 = tile); 0 if invalid. */
+size_t tahq_payload_size_ex(int64_t tokens, int64_t channels, int tile, int alloc_tile,
+                            int bits_lo, int bits_hi, float budget, int64_t tokens_per_group);
 
 /* Bytes of device workspace tahq_decode needs; 0 for invalid arguments. */
 size_t tahq_decode_workspace_size(int64_t tokens, int64_t channels, int tile);

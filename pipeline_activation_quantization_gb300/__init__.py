@@ -34,7 +34,7 @@ DEV_BAD_WIRE = 32
 # Every extern "C" function declared in include/tahq.h.
 EXPORTED_SYMBOLS = (
     "tahq_payload_size", "tahq_hi_count", "tahq_workspace_size", "tahq_encode", "tahq_encode_ex",
-    "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
+    "tahq_payload_size_ex", "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
     "tahq_wire_size", "tahq_wire_workspace_size", "tahq_wire_decode_workspace_size",
     "tahq_encode_wire", "tahq_decode_wire",
@@ -67,8 +67,9 @@ def lib(path: str | None = None):
         "tahq_decode_workspace_size": (sz, [i64, i64, i32]),
         "tahq_encode": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64,
                               p, p, p, p, p, p, sz, p]),
-        "tahq_encode_ex": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32,
+        "tahq_encode_ex": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32, i32,
                                  p, p, p, p, p, p, sz, p]),
+        "tahq_payload_size_ex": (sz, [i64, i64, i32, i32, i32, i32, f32, i64]),
         "tahq_decode": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, p, p, sz, p]),
         "tahq_get_device_status": (i32, [p, C.POINTER(C.c_uint32), p]),
         "tahq_status_string": (C.c_char_p, [i32]),
@@ -136,12 +137,18 @@ def tahq_encode(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budg
 
 
 def tahq_encode_ex(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
-                   tokens_per_group, tau, codes, scales, zeros, bits, pivots, workspace,
-                   workspace_bytes, stream=None) -> int:
+                   tokens_per_group, tau, alloc_tile, codes, scales, zeros, bits, pivots,
+                   workspace, workspace_bytes, stream=None) -> int:
     return lib().tahq_encode_ex(_ptr(x), dtype, tokens, channels, tile, hblock, bits_lo,
-                                bits_hi, budget, tokens_per_group, tau, _ptr(codes),
+                                bits_hi, budget, tokens_per_group, tau, alloc_tile, _ptr(codes),
                                 _ptr(scales), _ptr(zeros), _ptr(bits), _ptr(pivots),
                                 _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def tahq_payload_size_ex(tokens, channels, tile, alloc_tile, bits_lo, bits_hi, budget,
+                         tokens_per_group) -> int:
+    return lib().tahq_payload_size_ex(tokens, channels, tile, alloc_tile, bits_lo, bits_hi,
+                                      budget, tokens_per_group)
 
 
 def tahq_decode(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile, hblock,
@@ -191,9 +198,11 @@ def _check(rc: int, what: str):
 
 def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_hi: int = 4,
            budget: float = 3.5, tokens_per_group: int = 0, out: dict | None = None,
-           workspace=None, stream=None, tau: float | None = None) -> dict:
+           workspace=None, stream=None, tau: float | None = None,
+           alloc_tile: int | None = None) -> dict:
     """Encode a CUDA tensor ``x`` ([tokens, channels], float32 or bfloat16).  ``tau`` is the
-    outlier threshold (None: the method's 2.0, through tahq_encode; else tahq_encode_ex).
+    outlier threshold and ``alloc_tile`` the allocation tile A (None: the method's 2.0 and
+    A = tile, through tahq_encode; else tahq_encode_ex).
 
     Returns ``{"codes", "scales", "zeros", "bits", "pivots", "workspace"}`` (torch tensors on
     x's device).  Pass ``out`` / ``workspace`` from an earlier call to reuse them.
@@ -211,7 +220,10 @@ def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_
     T, Cc = x.shape
     h = hblock or tile
     n = T * (Cc // tile)
-    pay = tahq_payload_size(T, Cc, tile, bits_lo, bits_hi, budget, tokens_per_group)
+    pay = (tahq_payload_size(T, Cc, tile, bits_lo, bits_hi, budget, tokens_per_group)
+           if not alloc_tile else
+           tahq_payload_size_ex(T, Cc, tile, alloc_tile, bits_lo, bits_hi, budget,
+                                tokens_per_group))
     ws = tahq_workspace_size(T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group)
     if ws == 0:
         raise TahqError(1, "tahq_workspace_size")
@@ -226,13 +238,14 @@ def encode(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3, bits_
         }
     if workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-    if tau is None:
+    if tau is None and not alloc_tile:
         rc = tahq_encode(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
                          out["codes"], out["scales"], out["zeros"], out["bits"], out["pivots"],
                          workspace, workspace.numel(), stream)
     else:
         rc = tahq_encode_ex(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
-                            float(tau), out["codes"], out["scales"], out["zeros"], out["bits"],
+                            2.0 if tau is None else float(tau), int(alloc_tile or 0),
+                            out["codes"], out["scales"], out["zeros"], out["bits"],
                             out["pivots"], workspace, workspace.numel(), stream)
     _check(rc, "tahq_encode")
     res = dict(out)

@@ -53,6 +53,7 @@ int num_sms_current() {
 struct Shape {
   long long T, C, n, n_g, n_groups, K, group_bytes, payload;
   int G, h, lo, hi;
+  int mlog;  // allocation tile A = 2^mlog G; K counts allocation tiles (n_g >> mlog a group)
 };
 
 // Shape checks shared by every entry point.  hblock < 0 means "not given".
@@ -71,10 +72,15 @@ tahq_status check_shape(long long T, long long C, int G, int h, Shape& s) {
   return TAHQ_OK;
 }
 
+// A = the allocation tile (0: A = G), a power-of-two multiple of G that divides C.
 tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, float budget,
-                        long long S, Shape& s) {
+                        long long S, Shape& s, long long A = 0) {
   tahq_status st = check_shape(T, C, G, h, s);
   if (st != TAHQ_OK) return st;
+  if (A == 0) A = G;
+  if (A < G || A % G || C % A || !is_pow2(A / G)) return TAHQ_ERR_ARG;
+  s.mlog = 0;
+  while ((1ll << s.mlog) < A / G) s.mlog++;
   if (lo < 1 || hi > 8 || lo >= hi) return TAHQ_ERR_ARG;
   if (!(std::isfinite(budget) && (double)budget >= lo && (double)budget <= hi)) return TAHQ_ERR_ARG;
   if (S < 0) return TAHQ_ERR_ARG;
@@ -85,8 +91,9 @@ tahq_status check_codec(long long T, long long C, int G, int h, int lo, int hi, 
   s.n_g = S * (C / G);
   if (s.n_g >= (1ll << 31)) return TAHQ_ERR_UNSUPPORTED;
   s.n_groups = (T > 0) ? T / S : 0;
-  s.K = (long long)std::floor(((double)budget - lo) * (double)s.n_g / (double)(hi - lo));
-  s.group_bytes = s.n_g * G * lo / 8 + s.K * G * (hi - lo) / 8;
+  const long long n_ga = s.n_g >> s.mlog;
+  s.K = (long long)std::floor(((double)budget - lo) * (double)n_ga / (double)(hi - lo));
+  s.group_bytes = s.n_g * G * lo / 8 + (s.K << s.mlog) * G * (hi - lo) / 8;
   s.payload = s.n_groups * s.group_bytes;
   return TAHQ_OK;
 }
@@ -211,14 +218,18 @@ namespace {
 // tahq_encode_ex, and the wire format's encoder (wire: fp16 zero and scales).
 tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
                         int tile, int hblock, int bits_lo, int bits_hi, float budget,
-                        int64_t tokens_per_group, float tau, bool wire, uint8_t* codes,
-                        float* scales, float* zeros, uint8_t* bits, uint8_t* pivots,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+                        int64_t tokens_per_group, float tau, int alloc_tile, bool wire,
+                        uint8_t* codes, float* scales, float* zeros, uint8_t* bits,
+                        uint8_t* pivots, void* workspace, size_t workspace_bytes, void* stream) {
   if (!(tau >= 0.0f)) return TAHQ_ERR_ARG;  // negative or NaN
+  if (alloc_tile < 0) return TAHQ_ERR_ARG;
   Shape s;
   tahq_status st = check_codec(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
-                               tokens_per_group, s);
+                               tokens_per_group, s, alloc_tile);
   if (st != TAHQ_OK) return st;
+  // an allocation tile is never split between two of the encoder's 32 KB input chunks
+  if (((long long)tile << s.mlog) * (dtype == TAHQ_BF16 ? 2 : 4) > 32768)
+    return TAHQ_ERR_UNSUPPORTED;
   if (hblock < 0) return TAHQ_ERR_ARG;
   if (dtype != TAHQ_F32 && dtype != TAHQ_BF16) return TAHQ_ERR_ARG;
   if (s.n > 0) {
@@ -246,6 +257,7 @@ tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.c_h = (float)(1.0 / std::sqrt((double)s.h));
   a.tau = tau;
   a.wire = wire;
+  a.mlog = s.mlog;
   a.n_tiles = s.n;
   a.n_g = s.n_g;
   a.n_groups = s.n_groups;
@@ -283,12 +295,21 @@ tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
 
 tahq_status tahq_encode_ex(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
                            int tile, int hblock, int bits_lo, int bits_hi, float budget,
-                           int64_t tokens_per_group, float tau, uint8_t* codes, float* scales,
-                           float* zeros, uint8_t* bits, uint8_t* pivots, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           int64_t tokens_per_group, float tau, int alloc_tile, uint8_t* codes,
+                           float* scales, float* zeros, uint8_t* bits, uint8_t* pivots,
+                           void* workspace, size_t workspace_bytes, void* stream) {
   return encode_impl(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
-                     tokens_per_group, tau, false, codes, scales, zeros, bits, pivots, workspace,
-                     workspace_bytes, stream);
+                     tokens_per_group, tau, alloc_tile, false, codes, scales, zeros, bits, pivots,
+                     workspace, workspace_bytes, stream);
+}
+
+size_t tahq_payload_size_ex(int64_t tokens, int64_t channels, int tile, int alloc_tile,
+                            int bits_lo, int bits_hi, float budget, int64_t tokens_per_group) {
+  Shape s;
+  if (alloc_tile < 0 || check_codec(tokens, channels, tile, -1, bits_lo, bits_hi, budget,
+                                    tokens_per_group, s, alloc_tile) != TAHQ_OK)
+    return 0;
+  return (size_t)s.payload;
 }
 
 tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
@@ -297,7 +318,7 @@ tahq_status tahq_encode(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
                         uint8_t* bits, uint8_t* pivots, void* workspace, size_t workspace_bytes,
                         void* stream) {
   return tahq_encode_ex(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
-                        tokens_per_group, 2.0f, codes, scales, zeros, bits, pivots, workspace,
+                        tokens_per_group, 2.0f, 0, codes, scales, zeros, bits, pivots, workspace,
                         workspace_bytes, stream);
 }
 
@@ -474,7 +495,7 @@ tahq_status tahq_encode_wire(const void* x, tahq_dtype dtype, int64_t tokens, in
   uint8_t* bits = at<uint8_t>(workspace, A.bits);
   uint8_t* pivots = at<uint8_t>(workspace, A.pivots);
   st = encode_impl(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
-                   tokens_per_group, tau, true, wire + W.off_pay, scales, zeros, bits, pivots,
+                   tokens_per_group, tau, 0, true, wire + W.off_pay, scales, zeros, bits, pivots,
                    workspace, L.total, stream);
   if (st != TAHQ_OK) return st;
   tahq::WirePackArgs a{};

@@ -104,10 +104,14 @@ __device__ __forceinline__ unsigned long long rank_key(float h, uint32_t t_local
   return ((unsigned long long)order_key(h) << 32) | (unsigned long long)(0xFFFFFFFFu - t_local);
 }
 
-__device__ __forceinline__ int fine_bin(float h) {
+// Bucket of a key: keys of tiles of up to 256 values lie in [0, 8] bits (scale 8192),
+// of allocation tiles of up to 65536 values in [0, 16] (scale 4096); the scale is a power
+// of two, so h * scale is exact and the buckets keep the keys' order.
+__device__ __forceinline__ int fine_bin(float h, float scale) {
   if (!(h >= 0.0f)) return 0;          // negative rounding residue or NaN
-  if (!(h < 8.0f)) return kFineBins - 1;
-  return (int)__fmul_rn(h, 8192.0f);   // truncation == floor for h >= 0
+  const float x = __fmul_rn(h, scale);
+  if (!(x < (float)kFineBins)) return kFineBins - 1;
+  return (int)x;                       // truncation == floor for x >= 0
 }
 
 // ------------------------------------------------------------------ tile geometry

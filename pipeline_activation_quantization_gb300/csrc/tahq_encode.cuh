@@ -72,6 +72,7 @@ struct Cfg {
   static constexpr int kSteps = CH / (kWarps * TPW);  // warp steps per chunk
   static constexpr int NS = CH / kWarps;              // tiles owned by a warp
   static constexpr int kArr = kLine ? 1 : CH;         // per-tile arrays of the narrow layout
+  static constexpr int kAlloc = kLine ? CH : 1;       // line layout: per-tile sums (A != G)
   static_assert(kLine || kSteps * kWarps * TPW == CH, "chunk must be whole warp steps");
 };
 
@@ -97,6 +98,7 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
   // narrow layout, per tile of the input chunk: (L, S) in stats, then (min, max) and
   // (inv_lo, inv_hi or scale); deferred lists
   float ta[C::kArr], tb[C::kArr], tc[C::kArr];
+  float aL[C::kAlloc], aS[C::kAlloc];  // line layout: each tile's (L, S) when A != G
   uint8_t piv[C::kArr];
   uint16_t dl[C::CH];  // deferred tiles (line: one list per block; narrow: per warp)
   uint32_t ndef[2];    // line layout: length of dl, one counter per item parity
@@ -120,6 +122,9 @@ struct EncParams {
   float c_h;
   float tau;  // outlier threshold (§3.3 eq. (3): transform where r > tau)
   int wire;   // quantise with the wire format's fp16 zero and scales
+  int mlog;         // allocation tiles of 2^mlog tiles (§3.2 "Tile decomposition")
+  long long n_ga;   // allocation tiles per group (one key each)
+  float fscale;     // key -> fine histogram bucket scale (fine_bin)
   uint8_t* codes;
   float* scales;
   float* zeros;
@@ -367,6 +372,36 @@ __device__ __forceinline__ float warp_min_f(float x) {
   return r;
 }
 
+// Keys of the chunk's allocation tiles (2^mlog consecutive tiles each; §3.2 "Tile
+// decomposition"): the block adds the tiles' (L, S) pairwise in place, level by level
+// (pairs (j, j + w) for j a multiple of 2w: the natural-order pairwise sum over each
+// allocation tile's A values, whose halves are whole tiles), then one thread per
+// allocation tile forms the key and counts it in the group's histograms.  The chunk
+// starts on an allocation-tile boundary and holds whole allocation tiles.  Called by the
+// whole block.
+template <typename Tin, int G>
+__device__ __noinline__ void alloc_keys(EncSmem<Tin, G>& s, const EncParams& p, long long g,
+                                        long long t0, int nt, float* Ls, float* Ss) {
+  const int m = 1 << p.mlog;
+  for (int w = 1; w < m; w <<= 1) {
+    for (int j = threadIdx.x * 2 * w; j < nt; j += kThreads * 2 * w) {
+      Ls[j] = __fadd_rn(Ls[j], Ls[j + w]);
+      Ss[j] = __fadd_rn(Ss[j], Ss[j + w]);
+    }
+    csync();
+  }
+  for (int i = threadIdx.x; i < (nt >> p.mlog); i += kThreads) {
+    const float L = Ls[i * m], S = Ss[i * m];
+    const float H = entropy_key(L, S, s.tabs);
+    p.keys[(t0 >> p.mlog) + i] = H;
+    if (!(L <= FLT_MAX) || !(fabsf(S) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+      set_status(p.status, kStNonFinite);
+    const int b = fine_bin(H, p.fscale);
+    atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
+    atomicAdd(&p.hist_coarse[g * kCoarseBins + (b >> 8)], 1u);
+  }
+}
+
 // Values a lane takes in the exact path of the line layout: more values a lane means
 // fewer shuffle stages and team reductions per tile and 32 / (G / V) tiles per warp step.
 // One lane's codes at the wider width must fit 64 bits (widths known at compile time,
@@ -553,15 +588,20 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
     float2 ls = line_sums<Tin>(buf, line, s.tabs, lg_consts(s.tabs, lane));
     ls = team_sum2<LPT>(ls);
     if (valid && sub == 0) {
-      const float H = entropy_key(ls.x, ls.y, s.tabs);
-      p.keys[t0 + kt] = H;
-      if (!(ls.x <= FLT_MAX) || !(fabsf(ls.y) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
-        set_status(p.status, kStNonFinite);
-      const int b = fine_bin(H);
-      atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
-      // the coarse bins of a group's tiles are few (similar entropies): count them in
-      // the block first, one global add per bin and item below
-      atomicAdd(&s.hist[b >> 8], 1u);
+      if (p.mlog > 0) {  // the allocation tiles' keys follow the block barrier below
+        s.aL[kt] = ls.x;
+        s.aS[kt] = ls.y;
+      } else {
+        const float H = entropy_key(ls.x, ls.y, s.tabs);
+        p.keys[t0 + kt] = H;
+        if (!(ls.x <= FLT_MAX) || !(fabsf(ls.y) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+          set_status(p.status, kStNonFinite);
+        const int b = fine_bin(H, p.fscale);
+        atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
+        // the coarse bins of a group's tiles are few (similar entropies): count them in
+        // the block first, one global add per bin and item below
+        atomicAdd(&s.hist[b >> 8], 1u);
+      }
     }
   }
 
@@ -632,6 +672,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   // pass's slot writes before the exact path overwrites flagged slots.
   if (valid && deferred && sub == 0) s.dl[atomicAdd(ndef, 1u)] = (uint16_t)kt;
   csync();
+  if (!flat && p.mlog > 0) alloc_keys(s, p, g, t0, nt, s.aL, s.aS);
   if (!flat) {
     static_assert(kThreads == kCoarseBins, "one coarse bin per thread");
     const uint32_t c = s.hist[threadIdx.x];
@@ -695,8 +736,15 @@ __device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams
     __syncwarp();
     uint32_t* hf = p.hist_fine + g * (long long)kFineBins;
     uint32_t* hc = p.hist_coarse + g * kCoarseBins;
+    if (p.mlog > 0) {
+      // allocation tiles span warps: every tile's sums in place, then their keys, before
+      // phase 1 reuses the arrays
+      csync();
+      alloc_keys(s, p, g, t0, nt, s.ta, s.tb);
+      csync();
+    }
 #pragma unroll 1
-    for (int l0 = 0; l0 < NS; l0 += 32) {
+    for (int l0 = 0; l0 < (p.mlog > 0 ? 0 : NS); l0 += 32) {
       const int l = l0 + lane;
       const int kt = warp_tile<Tin, G>(l, warp);
       const bool valid = l < NS && kt < nt;
@@ -707,7 +755,7 @@ __device__ __forceinline__ void tiles_narrow(EncSmem<Tin, G>& s, const EncParams
         p.keys[t0 + kt] = H;
         if (!(Ls <= FLT_MAX) || !(fabsf(Ss) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
           set_status(p.status, kStNonFinite);
-        const int b = fine_bin(H);
+        const int b = fine_bin(H, p.fscale);
         atomicAdd(&hf[b], 1u);
         cb = b >> 8;
       }
@@ -958,10 +1006,11 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
   const int bstar = (int)s.scan[0];
   const uint32_t above = s.scan[1];
   // candidates of this item's slice of the group
-  const long long per = (p.n_g + p.J - 1) / p.J;
-  const long long lo = it.idx * per, hi = min(p.n_g, lo + per);
-  const float* kg = p.keys + g * p.n_g;
-  unsigned long long* cg = p.cand + g * p.n_g;
+  // the group's n_ga keys (one per allocation tile)
+  const long long per = (p.n_ga + p.J - 1) / p.J;
+  const long long lo = it.idx * per, hi = min(p.n_ga, lo + per);
+  const float* kg = p.keys + g * p.n_ga;
+  unsigned long long* cg = p.cand + g * p.n_ga;
   const int lane = threadIdx.x & 31;
   constexpr int kB = 8;  // keys in flight per thread
   for (long long base = lo; base < hi; base += kB * kThreads) {
@@ -974,7 +1023,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
 #pragma unroll
     for (int u = 0; u < kB; u++) {
       const long long i = base + u * kThreads + threadIdx.x;
-      const bool hit = i < hi && fine_bin(hv[u]) == bstar;
+      const bool hit = i < hi && fine_bin(hv[u], p.fscale) == bstar;
       const unsigned mask = __ballot_sync(kFull, hit);
       if (mask) {
         uint32_t pos0 = 0;
@@ -1085,7 +1134,7 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       Zv[u] = 0.0f;
       if (tl < tl_end) {
         const long long t = g * p.n_g + tl;
-        if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t]);
+        if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t >> p.mlog]);  // its allocation tile's
         Dv[u] = __ldcg(&p.scales[t]);
         if (p.wire) Zv[u] = __ldcg(&p.zeros[t]);
       }
@@ -1098,7 +1147,7 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       if (tl < tl_end) {
         const long long t = g * p.n_g + tl;
         ishi = mode == kSelAll ||
-               (mode == kSelThreshold && rank_key(key[u], (uint32_t)tl) >= theta);
+               (mode == kSelThreshold && rank_key(key[u], (uint32_t)(tl >> p.mlog)) >= theta);
         const int b = ishi ? p.hi : p.lo;
         p.bits[t] = (uint8_t)b;
         // the range D left by the tiles pass becomes the scale D / Q (wire format: the
@@ -1562,6 +1611,10 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.c_h = a.c_h;
   p.tau = a.tau;
   p.wire = a.wire ? 1 : 0;
+  p.mlog = a.mlog;
+  p.n_ga = a.n_g >> a.mlog;
+  // keys of A = 2^mlog G values lie in [0, log2 A]
+  p.fscale = ((long long)G << a.mlog) <= 256 ? 8192.0f : 4096.0f;
   p.slot_lo = G * a.lo / 8;
   p.slot_hi = G * a.hi / 8;
   p.direct = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 1 : 0;
@@ -1593,7 +1646,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   const int grid_cap = a.num_sms * 2;
-  const bool flat = a.K == 0 || a.K == a.n_g;
+  const bool flat = a.K == 0 || a.K == (a.n_g >> a.mlog);
   p.flat_b = a.K == 0 ? a.lo : a.hi;
   // a compaction chunk's per-tile arrays (3 bytes per tile) follow the shared state
   const size_t stages = flat ? 0 : 3 * kMaxCC;

@@ -18,6 +18,7 @@ struct EncodeArgs {
   float c_h;                 // RN(1/sqrt(h))
   float tau;                 // outlier threshold: transform where r > tau (>= 0, +inf: never)
   bool wire;                 // fp16 zero and scales of the wire format (else the fp32 quantiser)
+  int mlog;                  // allocation tiles of 2^mlog tiles (one key each); K counts them
   long long n_tiles, n_g, n_groups, K, group_bytes;
   int num_sms;
   const LgTables* tabs;

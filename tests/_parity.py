@@ -23,12 +23,12 @@ def to_device(x: np.ndarray):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
 
 
-def gpu_roundtrip(x: np.ndarray, G, h, lo, hi, beta, S, tau=None) -> dict:
+def gpu_roundtrip(x: np.ndarray, G, h, lo, hi, beta, S, tau=None, alloc_tile=None) -> dict:
     """Encode and decode on the GPU; return host copies plus both status words."""
     import torch
     T, C = x.shape
     xt = to_device(x)
-    enc = tq.encode(xt, G, h, lo, hi, beta, S, tau=tau)
+    enc = tq.encode(xt, G, h, lo, hi, beta, S, tau=tau, alloc_tile=alloc_tile)
     y = tq.decode(enc, T, C, G, h)
     torch.cuda.synchronize()
     rc_e, st_e = tq.tahq_get_device_status(enc["workspace"])
@@ -38,9 +38,10 @@ def gpu_roundtrip(x: np.ndarray, G, h, lo, hi, beta, S, tau=None) -> dict:
     return out
 
 
-def oracle_roundtrip(x: np.ndarray, G, h, lo, hi, beta, S, tau=None) -> dict:
+def oracle_roundtrip(x: np.ndarray, G, h, lo, hi, beta, S, tau=None, alloc_tile=None) -> dict:
     T, C = x.shape
-    r = oracle.encode(x, G, h, lo, hi, beta, S, threads=HOST_THREADS, want_near=True, tau=tau)
+    r = oracle.encode(x, G, h, lo, hi, beta, S, threads=HOST_THREADS, want_near=True, tau=tau,
+                      alloc_tile=alloc_tile)
     r["y"] = oracle.decode(r["codes"], r["scales"], r["zeros"], r["bits"], r["pivots"], T, C, G, h,
                            threads=HOST_THREADS)
     return r

@@ -88,7 +88,7 @@ def test_invalid_arguments(args):
 @pytest.mark.parametrize("tau", [-1.0, -0.0 - 1e-30, float("nan"), float("-inf")])
 def test_encode_ex_rejects_bad_tau(tau):
     fake = 1 << 20   # rejected before any dereference or launch
-    rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, tau, fake, fake, fake,
+    rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, tau, 0, fake, fake, fake,
                            fake, fake, fake, 1 << 30, 0)
     assert rc == 1
 
@@ -152,3 +152,27 @@ def test_wire_entry_points_reject_bad_buffers():
                                1 << 30, 0) == 1
     assert tq.tahq_encode_wire(fake, tq.TAHQ_F32, 16, 128, 64, 64, 3, 4, 3.5, 0, 2.0, fake, size,
                                fake, 16, 0) == 3      # workspace too small
+
+
+@pytest.mark.parametrize("T,C,G,A,lo,hi,beta,S", [(16, 512, 64, 128, 3, 4, 3.5, 8),
+                                                  (48, 512, 64, 512, 3, 4, 3.5, 0),
+                                                  (32, 8192, 128, 8192, 3, 4, 3.5, 16),
+                                                  (20, 256, 16, 64, 2, 3, 2.2, 10)])
+def test_payload_size_ex_agrees_with_oracle(T, C, G, A, lo, hi, beta, S):
+    assert tq.tahq_payload_size_ex(T, C, G, A, lo, hi, beta, S) == \
+        oracle.payload_size(T, C, G, lo, hi, beta, S, A)
+    assert tq.tahq_payload_size_ex(T, C, G, 0, lo, hi, beta, S) == \
+        tq.tahq_payload_size(T, C, G, lo, hi, beta, S)
+
+
+def test_alloc_tile_argument_errors():
+    fake = 1 << 20
+    for A in (32, 96, 192, 1024, -64):     # below tile, not a multiple, not 2^k tiles, above C
+        assert tq.tahq_payload_size_ex(16, 512, 64, A, 3, 4, 3.5, 0) == 0
+        rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 16, 512, 64, 64, 3, 4, 3.5, 0, 2.0, A, fake,
+                               fake, fake, fake, fake, fake, 1 << 30, 0)
+        assert rc == 1
+    # an fp32 allocation tile above 32 KB is valid for the method but not built
+    rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 4, 16384, 64, 64, 3, 4, 3.5, 0, 2.0, 16384, fake,
+                           fake, fake, fake, fake, fake, 1 << 30, 0)
+    assert rc == 2

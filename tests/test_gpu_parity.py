@@ -23,9 +23,9 @@ def _need_cuda():
     tq.lib()
 
 
-def _check(x, G, h, lo, hi, beta, S, tau=None):
-    gpu = gpu_roundtrip(x, G, h, lo, hi, beta, S, tau)
-    ora = oracle_roundtrip(x, G, h, lo, hi, beta, S, tau)
+def _check(x, G, h, lo, hi, beta, S, tau=None, alloc_tile=None):
+    gpu = gpu_roundtrip(x, G, h, lo, hi, beta, S, tau, alloc_tile)
+    ora = oracle_roundtrip(x, G, h, lo, hi, beta, S, tau, alloc_tile)
     return assert_parity(gpu, ora, G)
 
 
@@ -85,6 +85,28 @@ def test_tau_rejects_negative_and_nan():
     for tau in (-1.0, float("nan")):
         with pytest.raises(tq.TahqError):
             tq.encode(x, 64, 64, 3, 4, 3.5, 0, tau=tau)
+
+
+# ------------------------------------------------------------------ allocation tiles
+# ("TAH-Quant" §3.2 "Tile decomposition": one key per A channels; A = C is token-level)
+
+ALLOC = [
+    # dtype, dist, G, A, lo, hi, beta, T, C, S
+    ("f32", "laplace", 128, 256, 3, 4, 3.5, 64, 2048, 16),
+    ("f32", "gauss_rms_spikes", 128, 8192, 3, 4, 3.5, 64, 8192, 32),     # token-level, 32 KB
+    ("f32", "student_t", 64, 512, 3, 4, 3.25, 96, 1024, 32),
+    ("bf16", "gauss_rms_spikes", 64, 4096, 3, 4, 3.5, 80, 4096, 40),     # token-level
+    ("bf16", "laplace", 64, 128, 2, 3, 2.2, 96, 1152, 32),
+    ("bf16", "student_t", 32, 256, 3, 4, 3.5, 80, 2048, 16),             # narrow layout
+    ("f32", "gauss_rms_spikes", 16, 64, 3, 4, 3.5, 33, 448, 11),         # narrow layout
+    ("f32", "laplace", 64, 1024, 3, 4, 3.0, 64, 1024, 0),                # K = 0 (one width)
+]
+
+
+@pytest.mark.parametrize("dtype,dist,G,A,lo,hi,beta,T,C,S", ALLOC)
+def test_alloc_tiles(dtype, dist, G, A, lo, hi, beta, T, C, S):
+    w = synth.Workload("alloc", T, C, dtype, G, G, lo, hi, beta, S, 1100 + T + A, dist)
+    print("alloc", A, _check(synth.generate(w), G, G, lo, hi, beta, S, None, A))
 
 
 # ------------------------------------------------------------------ width mixes
