@@ -429,7 +429,7 @@ __host__ __device__ constexpr int p2_values() {
 // m1 / 2 - d > d 2^-24.  m1 / 2 is exact, m1 / 2 - d is exact by Sterbenz's lemma where it
 // matters (d <= m1 <= 4 d; below, it is negative; above, it rounds to at least d), and
 // d 2^-24 is a normal number.  Other thresholds take the IEEE division.
-template <typename Tin, int G, int V>
+template <typename Tin, int G, int V, bool kGen>
 __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned char* buf,
                                            const uint16_t* list, int n, long long t0, bool flat,
                                            int lo, int hi, unsigned char* stage_lo,
@@ -506,8 +506,9 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
     }
     const float d = __fadd_rn(m2, 1e-12f);
     const bool flag =
-        valid && (p.tau == 2.0f ? __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f)
-                                : __fdiv_rn(m1, d) > p.tau);
+        valid && ((!kGen || p.tau == 2.0f)
+                      ? __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f)
+                      : __fdiv_rn(m1, d) > p.tau);
     if (!__any_sync(kFull, flag)) continue;  // the main pass's slots stand
     float t[V];
 #pragma unroll
@@ -538,7 +539,7 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
     const bool degenerate = !(D >= 0x1p-120f);
     float inv_lo = degenerate ? 0.0f : r0, r1 = degenerate ? 0.0f : r1s;
     float qoff = mn, meta = flat ? r1 : D;
-    if (p.wire) {
+    if (kGen && p.wire) {
       // lane 0 of the team searches the scale of bits_lo, the others that of bits_hi
       qoff = wire_zero(mn);
       const float sm = wire_scale(qoff, mx, qmax_f(sub != 0 && !flat ? hi : lo));
@@ -572,7 +573,7 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
 
 // Tiles pass over one staged chunk, line layout: each warp takes 32 consecutive lines.
 // kLo / kHi: the two widths when known at compile time (0: from p).
-template <typename Tin, int G, int kLo, int kHi>
+template <typename Tin, int G, int kLo, int kHi, bool kGen>
 __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& p, long long g,
                                            long long t0, int nt, const unsigned char* buf,
                                            bool flat, unsigned char* stage_lo,
@@ -588,7 +589,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
     float2 ls = line_sums<Tin>(buf, line, s.tabs, lg_consts(s.tabs, lane));
     ls = team_sum2<LPT>(ls);
     if (valid && sub == 0) {
-      if (p.mlog > 0) {  // the allocation tiles' keys follow the block barrier below
+      if (kGen && p.mlog > 0) {  // the allocation tiles' keys follow the block barrier below
         s.aL[kt] = ls.x;
         s.aS[kt] = ls.y;
       } else {
@@ -615,14 +616,14 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   const float m1 = fmaxf(mx, -mn);
   // two values of at least m1 / tau give m2 >= m1 / tau, so r < tau: the threshold is
   // rounded up to keep the test on the safe side (m1 / 2 is exact for m1 >= 2^-120)
-  const float thr = p.tau == 2.0f ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
+  const float thr = (!kGen || p.tau == 2.0f) ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
   uint32_t cnt = 0;
 #pragma unroll
   for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
   cnt = team_sum_u<LPT>(cnt);
   // for tau >= 1 a maximum below 2^-120 can never give r > tau (the ratio is below 1e-24);
   // a tile whose maximum is not finite goes to the exact test
-  const bool small = m1 < 0x1p-120f && p.tau >= 1.0f;
+  const bool small = m1 < 0x1p-120f && (!kGen || p.tau >= 1.0f);
   const bool deferred = !small && (!(m1 <= FLT_MAX) || cnt < 2u);
 
   // widths: Q_lo / D and Q_hi / D (or D / Q_b), split over the team's lanes
@@ -644,7 +645,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   }
   if (!(D >= 0x1p-120f)) inv_lo = r1 = 0.0f;
   float qoff = mn, meta = flat ? r1 : D;
-  if (p.wire) {
+  if (kGen && p.wire) {
     if constexpr (LPT >= 2) {
       // the tile's even lanes search the scale of bits_lo, its odd lanes that of bits_hi
       qoff = wire_zero(mn);
@@ -672,7 +673,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
   // pass's slot writes before the exact path overwrites flagged slots.
   if (valid && deferred && sub == 0) s.dl[atomicAdd(ndef, 1u)] = (uint16_t)kt;
   csync();
-  if (!flat && p.mlog > 0) alloc_keys(s, p, g, t0, nt, s.aL, s.aS);
+  if (kGen && !flat && p.mlog > 0) alloc_keys(s, p, g, t0, nt, s.aL, s.aS);
   if (!flat) {
     static_assert(kThreads == kCoarseBins, "one coarse bin per thread");
     const uint32_t c = s.hist[threadIdx.x];
@@ -681,7 +682,7 @@ __device__ __forceinline__ void tiles_line(EncSmem<Tin, G>& s, const EncParams& 
       s.hist[threadIdx.x] = 0u;  // bins are all zero between items
     }
   }
-  pass2_line<Tin, G, p2_values<Tin, G, kLo, kHi>()>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi,
+  pass2_line<Tin, G, p2_values<Tin, G, kLo, kHi>(), kGen>(p, buf, s.dl, (int)*ndef, t0, flat, lo, hi,
                                                     stage_lo, stage_hi);
 }
 
@@ -957,7 +958,7 @@ __device__ __forceinline__ void tiles_range(const EncParams& p, const Item& it, 
 
 // ---- tiles item: the whole per-tile computation of one input chunk, both widths into
 // the scratch streams.
-template <typename Tin, int G, int kLo, int kHi>
+template <typename Tin, int G, int kLo, int kHi, bool kGen>
 __device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
                          const unsigned char* buf, uint32_t* ndef) {
   long long t0;
@@ -968,7 +969,7 @@ __device__ void do_tiles(EncSmem<Tin, G>& s, const EncParams& p, const Item& it,
   unsigned char* out_lo = p.scratch_lo + t0 * p.slot_lo;
   unsigned char* out_hi = p.scratch_hi + t0 * p.slot_hi;
   if constexpr (Cfg<Tin, G>::kLine) {
-    tiles_line<Tin, G, kLo, kHi>(s, p, it.g, t0, nt, buf, false, out_lo, out_hi, ndef);
+    tiles_line<Tin, G, kLo, kHi, kGen>(s, p, it.g, t0, nt, buf, false, out_lo, out_hi, ndef);
   } else {
     tiles_narrow<Tin, G>(s, p, it.g, t0, nt, buf, false, out_lo, out_hi);
   }
@@ -1106,7 +1107,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
 // ---- offsets item: the width and the scale of every tile of its compaction chunks and
 // their hi counts; the last offsets item of the group turns the counts into exclusive
 // prefixes.
-template <typename Tin, int G>
+template <typename Tin, int G, bool kGen>
 __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
   const long long g = it.g;
   if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status);
@@ -1122,6 +1123,7 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
   const long long tl_begin = c0 * p.CHC, tl_end = min(p.n_g, c1 * p.CHC);
   const int lane = threadIdx.x & 31;
   const uint32_t chc = (uint32_t)p.CHC;
+  const int mlog = kGen ? p.mlog : 0;
   uint32_t* segmask = p.segmask + g * ((p.n_g + 31) / 32);
   constexpr int kB = 8;
   for (long long tb = tl_begin; tb < tl_end; tb += kB * kThreads) {
@@ -1134,9 +1136,9 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       Zv[u] = 0.0f;
       if (tl < tl_end) {
         const long long t = g * p.n_g + tl;
-        if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t >> p.mlog]);  // its allocation tile's
+        if (mode == kSelThreshold) key[u] = __ldcg(&p.keys[t >> mlog]);  // its allocation tile's
         Dv[u] = __ldcg(&p.scales[t]);
-        if (p.wire) Zv[u] = __ldcg(&p.zeros[t]);
+        if (kGen && p.wire) Zv[u] = __ldcg(&p.zeros[t]);
       }
     }
 #pragma unroll
@@ -1147,12 +1149,12 @@ __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
       if (tl < tl_end) {
         const long long t = g * p.n_g + tl;
         ishi = mode == kSelAll ||
-               (mode == kSelThreshold && rank_key(key[u], (uint32_t)(tl >> p.mlog)) >= theta);
+               (mode == kSelThreshold && rank_key(key[u], (uint32_t)(tl >> mlog)) >= theta);
         const int b = ishi ? p.hi : p.lo;
         p.bits[t] = (uint8_t)b;
         // the range D left by the tiles pass becomes the scale D / Q (wire format: the
         // maximum left there gives the fp16 scale of this width)
-        p.scales[t] = p.wire ? wire_scale(Zv[u], Dv[u], qmax_f(b))
+        p.scales[t] = (kGen && p.wire) ? wire_scale(Zv[u], Dv[u], qmax_f(b))
                              : ((Dv[u] >= 0x1p-120f) ? __fdiv_rn(Dv[u], qmax_f(b)) : 0.0f);
       }
       const unsigned hm = __ballot_sync(kFull, ishi);
@@ -1431,7 +1433,10 @@ static __global__ void __launch_bounds__(256) k_items(const __grid_constant__ En
   if (q < p.n_items) p.items[q] = pack_item(decode_item(p, (uint32_t)q));
 }
 
-template <typename Tin, int G, int kLo, int kHi>
+// kGen: the general kernel (any tau, the wire format's quantiser, allocation tiles);
+// without it, the method's defaults (tau = 2, fp32 metadata, A = G) with their runtime
+// checks compiled out.
+template <typename Tin, int G, int kLo, int kHi, bool kGen>
 __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ EncParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
@@ -1493,7 +1498,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     if (it.type == kItemTiles) {
       mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
       parity ^= 1u << slot;
-      do_tiles<Tin, G, kLo, kHi>(s, p, it, s.buf[slot], &s.ndef[slot]);
+      do_tiles<Tin, G, kLo, kHi, kGen>(s, p, it, s.buf[slot], &s.ndef[slot]);
       done_g = it.g;
     } else if (it.type == kItemCompact) {
       do_compact<Tin, G>(s, p, it, s.buf[slot], reinterpret_cast<uint16_t*>(stage_lo),
@@ -1501,7 +1506,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     } else if (it.type == kItemSelect) {
       do_select<Tin, G>(s, p, it, s.buf[slot]);
     } else if (it.type == kItemOffsets) {
-      do_offsets<Tin, G>(s, p, it);
+      do_offsets<Tin, G, kGen>(s, p, it);
     }
   }
 }
@@ -1543,7 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
     // one width: tile t's slot is at t * slot_b in the stream
     unsigned char* out = p.codes + t0 * slot_b;
     if constexpr (C::kLine) {
-      tiles_line<Tin, G, kB, 0>(s, p, 0, t0, nt, s.buf[slot], true, out, out, &s.ndef[slot]);
+      tiles_line<Tin, G, kB, 0, true>(s, p, 0, t0, nt, s.buf[slot], true, out, out, &s.ndef[slot]);
     } else {
       tiles_narrow<Tin, G>(s, p, 0, t0, nt, s.buf[slot], true, out, out);
     }
@@ -1684,9 +1689,11 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   if (p.n_items >= (1ll << 31) || (p.nA + 2 * p.J + p.nC) * p.nC >= (1ll << 32))
     return cudaErrorInvalidValue;
   queue_segments(p);
-  void (*kern)(EncParams) = k_encode<Tin, G, 0, 0>;
+  void (*kern)(EncParams) = k_encode<Tin, G, 0, 0, true>;
   if constexpr (C::kLine) {
-    if (a.lo == 3 && a.hi == 4) kern = k_encode<Tin, G, 3, 4>;
+    // the method's defaults with widths {3, 4}: the specialised kernel
+    const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0;
+    if (a.lo == 3 && a.hi == 4) kern = plain ? k_encode<Tin, G, 3, 4, false> : k_encode<Tin, G, 3, 4, true>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
