@@ -142,15 +142,16 @@ def _traffic_for(kernel: str, workload: str):
     except Exception:
         return None
     e = rec.get(f"{kernel}|{workload}")
-    if not e or e.get("src_sha") != _src_sha():
+    if not e or e.get("src_sha") != _src_sha(e.get("src_files")):
         return None
     return e.get("dram_bytes_per_launch")
 
 
-def _src_sha() -> str:
+def _src_sha(files=None) -> str:
+    """Hash of the kernel's sources (the listed files of csrc/, else all of them)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "pipeline_activation_quantization_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in sorted(files or os.listdir(d)):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
