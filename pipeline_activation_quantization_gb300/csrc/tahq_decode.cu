@@ -122,16 +122,31 @@ __device__ __forceinline__ float2 addp(float2 a, float2 b) {
   return d;
 }
 
-// The lane's 8 codes of b bits (b whole bytes at stage byte `start`), de-quantised.
+// The lane's 8 codes of b bits (b whole bytes at stage byte `start`), de-quantised.  Up
+// to 4 bits the 8 codes sit in one 32-bit word.
 __device__ __forceinline__ void dequant8(const uint32_t* sw, int start, int b, float sc, float mn,
                                          float* v) {
   const int q = start >> 2, sh = (start & 3) * 8;
-  const uint32_t w0 = sw[q], w1 = sw[q + 1], w2 = sw[q + 2];
-  const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
-  const unsigned long long acc = ((unsigned long long)hi << 32) | lo;
+  const uint32_t w0 = sw[q], w1 = sw[q + 1];
+  const uint32_t lo = __funnelshift_r(w0, w1, sh);
   const uint32_t mask = (1u << b) - 1u;
   const float2 s2 = make_float2(sc, sc), z2 = make_float2(mn, mn);
   const float2 m2 = make_float2(-8388608.0f, -8388608.0f);
+  if (b <= 4) {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const uint32_t c0 = (lo >> (j * b)) & mask;
+      const uint32_t c1 = (lo >> ((j + 1) * b)) & mask;
+      const float2 qf = addp(make_float2(__uint_as_float(0x4B000000u | c0),
+                                         __uint_as_float(0x4B000000u | c1)), m2);
+      const float2 r = fma2(qf, s2, z2);
+      v[j] = r.x;
+      v[j + 1] = r.y;
+    }
+    return;
+  }
+  const uint32_t hi = __funnelshift_r(w1, sw[q + 2], sh);
+  const unsigned long long acc = ((unsigned long long)hi << 32) | lo;
 #pragma unroll
   for (int j = 0; j < 8; j += 2) {
     const uint32_t c0 = (uint32_t)(acc >> (j * b)) & mask;
@@ -312,22 +327,29 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
     for (int k = threadIdx.x; k < nt; k += kDecThreads) {
       s.scale[k] = a.scales[t0 + k];
       s.zero[k] = a.zeros[t0 + k];
-      s.piv[k] = a.pivots[t0 + k];
     }
     uint32_t chunk_bytes;
     uint32_t off = block_exclusive_scan_dec<kDecThreads>(mine, chunk_bytes, s.scan);
+    (void)chunk_bytes;
+    // the chunk's first byte in the stream (k_dec_totals, k_dec_scan); each tile's slot,
+    // and, settled once here, whether it decodes (width 0: its slot runs past the stream
+    // or its width or pivot is invalid, and it decodes to zeros) and is transformed
+    const unsigned long long base = a.bsum[c / kDecChunksPerBlock] + a.ctot[c];
 #pragma unroll
     for (int j = 0; j < C::kPer; j++) {
       const int k = threadIdx.x * C::kPer + j;
       if (k < nt) {
-        s.bits[k] = bl[j];
+        const int b = bl[j];
+        const int piv = a.pivots[t0 + k];
+        const bool bad_piv = piv != 0xFF && piv >= G;
+        if (bad_piv) set_status(a.status, kStBadBits);
+        const bool ok = b > 0 && !bad_piv && base + off + (unsigned long long)(G * b / 8) <= limit;
+        s.bits[k] = (uint8_t)(ok ? b : 0);
+        s.piv[k] = (uint8_t)(ok ? piv : 0xFF);
         s.off[k] = (uint16_t)off;
-        off += (uint32_t)(G * bl[j] / 8);
+        off += (uint32_t)(G * b / 8);
       }
     }
-    // written by k_dec_totals and k_dec_scan
-    const unsigned long long base = a.bsum[c / kDecChunksPerBlock] + a.ctot[c];
-    (void)chunk_bytes;
     cp_async_wait_prev();  // this chunk's bytes have landed
     __syncthreads();
 
@@ -337,18 +359,10 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
 #pragma unroll 1
     for (int st = 0; st < C::kSteps; st++) {
       const int kt = (st * kDecWarps + warp) * TPW + team;
-      bool valid = kt < nt, ok = false, flag = false;
-      int b = 0;
-      if (valid) {
-        b = s.bits[kt];
-        const int piv = s.piv[kt];
-        ok = b > 0 && base + s.off[kt] + (unsigned long long)(G * b / 8) <= limit;
-        if (piv != 0xFF && piv >= G) {
-          if (sub == 0) set_status(a.status, kStBadBits);
-          ok = false;
-        }
-        flag = ok && piv != 0xFF;
-      }
+      const bool valid = kt < nt;
+      const int b = valid ? (int)s.bits[kt] : 0;  // 0: decodes to zeros (settled above)
+      const bool ok = b > 0;
+      const bool flag = valid && s.piv[kt] != 0xFF;
       const unsigned fm = __ballot_sync(kFull, flag && sub == 0);
       if (flag && sub == 0) fl[nflag + __popc(fm & ((1u << lane) - 1u))] = (uint16_t)kt;
       nflag += __popc(fm);
