@@ -260,6 +260,29 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------------ replicas (N > 1)
+
+def replica_tensor_index(rank: int, n_tensors: int, i: int) -> int:
+    """Rank r encodes its own tensors: indices r * n_tensors .. r * n_tensors + n - 1 of the
+    workload's generator (replicas, no shared input and no exchange)."""
+    return rank * n_tensors + i
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The job's time: the slowest rank's (all-reduce MAX; the identity on one process)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, in_bytes_per_step: int, steps: int, tot_ms: float) -> float:
+    """Whole-job throughput in GB/s: the input bytes all ranks processed over the job time."""
+    return world * in_bytes_per_step * steps / (tot_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ the CUDA path
 
 def run_gpu(args):
@@ -286,7 +309,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     xs, x_np = [], None
     for i in range(n_tensors):
-        xi = synth.generate(w, index=rank * n_tensors + i)
+        xi = synth.generate(w, index=replica_tensor_index(rank, n_tensors, i))
         if x_np is None:
             x_np = xi
         if w.dtype == "bf16":
@@ -365,10 +388,7 @@ def run_gpu(args):
     rc, word = tq.tahq_get_device_status(ws, stream)
     if rc != 0:
         raise RuntimeError(f"device status {word:#x} after the timed loop")
-    if dist is not None:
-        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(tot_ms, dist, dev)
 
     in_b, enc_b, dec_b = _alg_bytes(w, payload)
     if args.wire:  # the whole buffer is written, then read
@@ -376,7 +396,7 @@ def run_gpu(args):
         enc_b, dec_b = in_b + wire_b, wire_b + 4 * w.elements
     peak, peak_kind = _peaks()
     ms_step = tot_ms / args.steps
-    value = world * in_b * args.steps / (tot_ms * 1e-3) / 1e9
+    value = job_value(world, in_b, args.steps, tot_ms)
     e_ms, d_ms = statistics.mean(enc_ms), statistics.mean(dec_ms)
     enc_gbs, dec_gbs = enc_b / (e_ms * 1e-3) / 1e9, dec_b / (d_ms * 1e-3) / 1e9
     dom = ("decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
@@ -456,7 +476,7 @@ def run_gpu(args):
     return 0
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -478,9 +498,14 @@ def main():
                     help="time the wire format (tahq_encode_wire / tahq_decode_wire)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    return args
+
+
+def main():
+    args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
