@@ -99,6 +99,8 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
   // (inv_lo, inv_hi or scale); deferred lists
   float ta[C::kArr], tb[C::kArr], tc[C::kArr];
   float aL[C::kAlloc], aS[C::kAlloc];  // line layout: each tile's (L, S) when A != G
+  uint16_t qoff[C::kAlloc];  // k_quant: each tile's slot offset in its chunk's run
+  uint8_t qb[C::kAlloc];     // k_quant: each tile's width
   uint8_t piv[C::kArr];
   uint16_t dl[C::CH];  // deferred tiles (line: one list per block; narrow: per warp)
   uint32_t ndef[2];    // line layout: length of dl, one counter per item parity
@@ -1556,6 +1558,507 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
   }
 }
 
+// ====================================================================== three-stage encoder
+//
+// The method's defaults on the line layout (widths {3, 4}, tau = 2, A = G, fp32
+// metadata, token groups of whole 32 KB chunks) in three streaming stages instead of the
+// work queue: k_stats (every tile's entropy key and its group's histograms), then the
+// select (k_select_groups: the K-th key of each group), the widths and each chunk's hi
+// count (k_widths) and the chunks' places in the stream (k_chunk_scan), then k_quant
+// (every tile quantised once, at its width, straight into its slot).  The input is read
+// twice, but each stage is a plain stream over 32 KB chunks without waits between blocks.
+
+// Stage 1: entropy keys and the per-group key histograms.
+template <typename Tin, int G>
+__global__ void __launch_bounds__(kThreads, 2) k_stats(const __grid_constant__ EncParams p,
+                                                       long long n_chunks) {
+  using C = Cfg<Tin, G>;
+  constexpr int LPT = LineGeom<Tin, G>::LPT;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
+  init_tables<Tin, G>(s, p.tabs);
+  for (int i = threadIdx.x; i < kCoarseBins; i += kThreads) s.hist[i] = 0u;
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+  }
+  const unsigned long long pol = policy_evict_normal();  // k_quant reads the last chunks again
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int line = warp * 32 + lane, kt = line / LPT, sub = line % LPT;
+  uint32_t parity = 0u;
+  int slot = 0;
+  long long c = blockIdx.x;
+  if (threadIdx.x == 0 && c < n_chunks)
+    issue_chunk<Tin, G>(s, p, c * C::CH, (int)min((long long)C::CH, p.n_tiles - c * C::CH), 0, pol);
+  for (; c < n_chunks; c += gridDim.x) {
+    csync();  // the previous chunk's buffer and bins are free
+    const long long nx = c + gridDim.x;
+    if (threadIdx.x == 0 && nx < n_chunks)
+      issue_chunk<Tin, G>(s, p, nx * C::CH, (int)min((long long)C::CH, p.n_tiles - nx * C::CH),
+                          slot ^ 1, pol);
+    const long long t0 = c * C::CH;
+    const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
+    const long long g = t0 / p.n_g;  // chunks never straddle groups here
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    parity ^= 1u << slot;
+    float2 ls = line_sums<Tin>(s.buf[slot], line, s.tabs, lg_consts(s.tabs, lane));
+    ls = team_sum2<LPT>(ls);
+    if (kt < nt && sub == 0) {
+      const float H = entropy_key(ls.x, ls.y, s.tabs);
+      p.keys[t0 + kt] = H;
+      if (!(ls.x <= FLT_MAX) || !(fabsf(ls.y) <= FLT_MAX) || !(fabsf(H) <= FLT_MAX))
+        set_status(p.status, kStNonFinite);
+      const int b = fine_bin(H, p.fscale);
+      atomicAdd(&p.hist_fine[g * (long long)kFineBins + b], 1u);
+      atomicAdd(&s.hist[b >> 8], 1u);  // the chunk's coarse counts, one global add per bin
+    }
+    csync();
+    const uint32_t cnt = s.hist[threadIdx.x];
+    if (cnt) {
+      atomicAdd(&p.hist_coarse[g * kCoarseBins + threadIdx.x], cnt);
+      s.hist[threadIdx.x] = 0u;
+    }
+    slot ^= 1;
+  }
+}
+
+// The fine bucket that holds a group's K-th ranked key and the keys ranked above that
+// bucket (warp 0 of the calling block; bins = 256 words of shared memory).
+__device__ __forceinline__ void find_bucket(const EncParams& p, long long g, uint32_t* bins,
+                                            int& bstar, uint32_t& above) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t K = (uint32_t)p.K;
+  for (int i = lane; i < 256; i += 32) bins[i] = __ldcg(&p.hist_coarse[g * kCoarseBins + i]);
+  __syncwarp();
+  int cb;
+  uint32_t above_c;
+  warp_find_from_top(bins, K, cb, above_c);
+  __syncwarp();
+  for (int i = lane; i < 256; i += 32)
+    bins[i] = __ldcg(&p.hist_fine[g * (long long)kFineBins + cb * 256 + i]);
+  __syncwarp();
+  int fb;
+  uint32_t above_f;
+  warp_find_from_top(bins, K - above_c, fb, above_f);
+  bstar = cb * 256 + fb;
+  above = above_c + above_f;
+}
+
+// Stage 2a: blocks (group, j) gather the rank keys of the group's keys in the bucket that
+// holds its K-th ranked key (rank = key descending, then tile index ascending), each from
+// its own slice of the group.
+static __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ EncParams p,
+                                                            int J) {
+  __shared__ uint32_t bins[256];
+  __shared__ int s_b;
+  const long long g = blockIdx.x / J, j = blockIdx.x % J;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    int bstar;
+    uint32_t above;
+    find_bucket(p, g, bins, bstar, above);
+    if (lane == 0) s_b = bstar;
+  }
+  __syncthreads();
+  const int bstar = s_b;
+  const long long per = (p.n_g + J - 1) / J;
+  const long long lo = j * per, hi = min(p.n_g, lo + per);
+  const float* kg = p.keys + g * p.n_g;
+  unsigned long long* cg = p.cand + g * p.n_g;
+  constexpr int kB = 8;
+  for (long long base = lo; base < hi; base += kB * kThreads) {
+    float hv[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long i = base + u * kThreads + threadIdx.x;
+      hv[u] = i < hi ? __ldcg(&kg[i]) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const long long i = base + u * kThreads + threadIdx.x;
+      const bool hit = i < hi && fine_bin(hv[u], p.fscale) == bstar;
+      const unsigned mask = __ballot_sync(kFull, hit);
+      if (mask) {
+        uint32_t pos0 = 0;
+        const int leader = __ffs(mask) - 1;
+        if (lane == leader) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)__popc(mask));
+        pos0 = __shfl_sync(kFull, pos0, leader);
+        if (hit) cg[pos0 + __popc(mask & ((1u << lane) - 1u))] = rank_key(hv[u], (uint32_t)i);
+      }
+    }
+  }
+}
+
+// Stage 2a': one block per group ranks the gathered candidates exactly (one pass up to
+// kRankMax of them, else an 8-pass radix select over their 64-bit rank keys).
+static __global__ void __launch_bounds__(kThreads) k_rank(const __grid_constant__ EncParams p) {
+  __shared__ uint32_t bins[256];
+  __shared__ uint32_t sc[8];
+  __shared__ unsigned long long ck[kRankMax];
+  const long long g = blockIdx.x;
+  if (threadIdx.x < 32) {
+    int bstar;
+    uint32_t above;
+    find_bucket(p, g, bins, bstar, above);
+    if (threadIdx.x == 0) {
+      sc[0] = (uint32_t)bstar;
+      sc[1] = above;
+    }
+  }
+  __syncthreads();
+  const int bstar = (int)sc[0];
+  const uint32_t above = sc[1];
+  const uint32_t K = (uint32_t)p.K;
+  const unsigned long long* cg = p.cand + g * p.n_g;
+  const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
+  const uint32_t expect = __ldcg(&p.hist_fine[g * (long long)kFineBins + bstar]);
+  if (threadIdx.x == 0 && cnt != expect) set_status(p.status, kStSelectMismatch);
+  const uint32_t r = max(1u, min(K - above, cnt));  // rank (from 1) inside the bucket
+  unsigned long long theta = 0ull;
+  if (cnt > 0u && cnt <= (uint32_t)kRankMax) {
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) ck[i] = __ldcg(&cg[i]);
+    __syncthreads();
+    // one pass: the candidate with exactly r - 1 larger rank keys (they are distinct)
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+      const unsigned long long ki = ck[i];
+      uint32_t larger = 0;
+      for (uint32_t j = 0; j < cnt; j++) larger += ck[j] > ki ? 1u : 0u;
+      if (larger == r - 1u) sc[3] = i;
+    }
+    __syncthreads();
+    theta = ck[sc[3]];
+  } else if (cnt > 0u) {
+    uint32_t rr = r;
+    unsigned long long prefix = 0ull, mask = 0ull;
+    for (int pass = 7; pass >= 0; --pass) {
+      const int shift = pass * 8;
+      for (int i = threadIdx.x; i < 256; i += kThreads) bins[i] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+        const unsigned long long v = __ldcg(&cg[i]);
+        if ((v & mask) == prefix) atomicAdd(&bins[(v >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        int d;
+        uint32_t ab;
+        warp_find_from_top(bins, rr, d, ab);
+        if (threadIdx.x == 0) {
+          sc[4] = (uint32_t)d;
+          sc[5] = ab;
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)sc[4] << shift;
+      rr -= sc[5];
+      mask |= 0xFFull << shift;
+      __syncthreads();
+    }
+    theta = prefix;
+  }
+  if (threadIdx.x == 0) p.sel[g] = SelResult{theta, cnt ? kSelThreshold : kSelNone, 0u};
+}
+
+// Stage 2b: every tile's width, each chunk's hi count, and per chunk its tiles in width
+// order (bits_lo first) as descriptors k | hi << 8 | (slot offset in the chunk's run)
+// << 16, so that stage 3 gives a warp tiles of one width (a block covers 256 tiles =
+// whole chunks of CH <= 256 tiles; chunks never straddle groups).
+template <int CH>
+__global__ void __launch_bounds__(kThreads) k_widths(const __grid_constant__ EncParams p,
+                                                     uint32_t* chunk_hi, uint32_t* desc) {
+  __shared__ uint32_t wcnt[kWarps];
+  const long long t = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  bool ishi = false;
+  if (t < p.n_tiles) {
+    // group and tile within it (32-bit: the host keeps n_tiles below 2^31 here)
+    const uint32_t g = (uint32_t)t / (uint32_t)p.n_g, tl = (uint32_t)t - g * (uint32_t)p.n_g;
+    const SelResult sr = p.sel[g];
+    ishi = sr.mode == kSelAll ||
+           (sr.mode == kSelThreshold && rank_key(__ldcg(&p.keys[t]), tl) >= sr.theta);
+    p.bits[t] = (uint8_t)(ishi ? p.hi : p.lo);
+  }
+  const unsigned m = __ballot_sync(kFull, ishi);
+  if (lane == 0) wcnt[warp] = (uint32_t)__popc(m);
+  __syncthreads();
+  constexpr int kWpc = CH / 32;  // warps a chunk
+  const int wc = warp - warp % kWpc;  // the chunk's first warp
+  uint32_t pre = (uint32_t)__popc(m & ((1u << lane) - 1u)), tot = 0;
+  for (int w = wc; w < warp; w++) pre += wcnt[w];
+  for (int w = wc; w < wc + kWpc; w++) tot += wcnt[w];
+  if (t < p.n_tiles) {
+    const long long c0 = t - t % CH;
+    const int k = (int)(t - c0), nt = (int)min((long long)CH, p.n_tiles - c0);
+    const int qo = k * p.slot_lo + (int)pre * (p.slot_hi - p.slot_lo);
+    const int pos = ishi ? nt - (int)tot + (int)pre : k - (int)pre;
+    desc[c0 + pos] = (uint32_t)k | (ishi ? 0x100u : 0u) | ((uint32_t)qo << 16);
+  }
+  if (threadIdx.x < kThreads / CH) {
+    uint32_t sum = 0;
+    for (int w = 0; w < kWpc; w++) sum += wcnt[threadIdx.x * kWpc + w];
+    const long long c = (long long)blockIdx.x * (kThreads / CH) + threadIdx.x;
+    if (c * CH < p.n_tiles) chunk_hi[c] = sum;
+  }
+}
+
+// Stage 2c: one block per group turns its chunks' hi counts into their byte offsets in
+// the stream (chunk c of the group starts at g * group_bytes + c CH slot_lo + (hi tiles
+// before it) (slot_hi - slot_lo)).
+template <int CH>
+__global__ void __launch_bounds__(kThreads) k_chunk_scan(const __grid_constant__ EncParams p,
+                                                         const uint32_t* chunk_hi,
+                                                         unsigned long long* chunk_off) {
+  __shared__ uint32_t s_warp[kWarps + 4];
+  const long long g = blockIdx.x;
+  const long long nc = p.n_g / CH, c0 = g * nc;
+  const long long run = (nc + kThreads - 1) / kThreads;
+  const long long r0 = min(nc, (long long)threadIdx.x * run), r1 = min(nc, r0 + run);
+  uint32_t mine = 0;
+  for (long long c = r0; c < r1; c++) mine += __ldcg(&chunk_hi[c0 + c]);
+  uint32_t tot;
+  unsigned long long acc = block_exclusive_scan<kThreads>(mine, tot, s_warp);
+  const long long slot_lo = p.slot_lo, slot_d = p.slot_hi - p.slot_lo;
+  for (long long c = r0; c < r1; c++) {
+    const uint32_t v = __ldcg(&chunk_hi[c0 + c]);
+    chunk_off[c0 + c] = (unsigned long long)(g * p.group_bytes + c * CH * slot_lo + (long long)acc * slot_d);
+    acc += v;
+  }
+}
+
+// Stage 3's exact path for the tiles the pretest could not clear (as pass2_line, one
+// width: the tile's own, into its slot at out + qoff[kt]).
+template <typename Tin, int G, int V>
+__device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char* buf,
+                                         const uint16_t* list, int n, long long t0,
+                                         unsigned char* out, const uint16_t* qoff,
+                                         const uint8_t* qb) {
+  constexpr bool kBf = InTraits<Tin>::kBf16;
+  constexpr int VPU = kBf ? 8 : 4, NU = V / VPU;
+  constexpr int L = G / V, TPW = 32 / L, LPT = LineGeom<Tin, G>::LPT;
+  constexpr int kGrp = V < 8 ? 8 / V : 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = lane / L, sub = lane % L, base = lane - sub;
+#pragma unroll 1
+  for (int j0 = warp * TPW; j0 < n; j0 += kWarps * TPW) {
+    const int ci = j0 + team;
+    const bool valid = ci < n;
+    const int kt = valid ? (int)list[ci] : 0;
+    const int u0 = sub * NU;
+    const int line = kt * LPT + (u0 >> 3);
+    float v[V];
+#pragma unroll
+    for (int k = 0; k < NU; k++) {
+      const int ju = (u0 & 7) + k;
+      const uint4 q = *reinterpret_cast<const uint4*>(buf + line * 128 + ((ju ^ (line & 7)) << 4));
+      const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+      if constexpr (kBf) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          v[8 * k + 2 * e] = __uint_as_float(wq[e] << 16);
+          v[8 * k + 2 * e + 1] = __uint_as_float(wq[e] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; e++) v[4 * k + e] = __uint_as_float(wq[e]);
+      }
+    }
+    float m1, m2;
+    int i1;
+    if constexpr (L == 32) {
+      float la = fabsf(v[0]);
+#pragma unroll
+      for (int j = 1; j < V; j++) la = fmaxf(la, fabsf(v[j]));
+      m1 = warp_max_abs(la);
+      int jj = V;
+#pragma unroll
+      for (int j = V - 1; j >= 0; j--)
+        if (fabsf(v[j]) == m1) jj = j;
+      const unsigned hit = __ballot_sync(kFull, jj < V);
+      const int src = hit ? __ffs(hit) - 1 : 0;
+      i1 = __shfl_sync(kFull, lane * V + (jj < V ? jj : 0), src);
+      float l2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < V; j++)
+        if (lane * V + j != i1) l2 = fmaxf(l2, fabsf(v[j]));
+      m2 = warp_max_f(l2);
+    } else {
+      m1 = fabsf(v[0]);
+      m2 = -1.0f;
+      i1 = sub * V;
+#pragma unroll
+      for (int j = 1; j < V; j++) {
+        const float m = fabsf(v[j]);
+        if (m > m1) {
+          m2 = m1;
+          m1 = m;
+          i1 = sub * V + j;
+        } else if (m > m2) {
+          m2 = m;
+        }
+      }
+      team_top2<L>(m1, i1, m2);
+    }
+    // the ratio test at tau = 2 without a division (see pass2_line)
+    const float d = __fadd_rn(m2, 1e-12f);
+    const bool flag = valid && __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f);
+    if (!__any_sync(kFull, flag)) continue;  // the main pass's slot stands
+    float t[V];
+#pragma unroll
+    for (int j = 0; j < V; j++) t[j] = v[j];
+    team_swap0<V>(t, flag ? i1 : 0, sub, base);
+    team_fwht<V, L>(t, p.h, sub);
+#pragma unroll
+    for (int j = 0; j < V; j++) v[j] = __fmul_rn(t[j], p.c_h);
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int j = 1; j < V; j++) {
+      mn = fminf(mn, v[j]);
+      mx = fmaxf(mx, v[j]);
+    }
+    if constexpr (L == 32) {
+      mn = warp_min_f(mn);
+      mx = warp_max_f(mx);
+    } else {
+      mn = team_min<L>(mn);
+      mx = team_max<L>(mx);
+    }
+    const int b = valid ? (int)qb[kt] : 3;
+    const float D = __fsub_rn(mx, mn);
+    // lane 0 of the team: Q_b / D; lane 1: D / Q_b (the tile's scale)
+    const float r = sub == 1 ? __fdiv_rn(D, qmax_f(b)) : __fdiv_rn(qmax_f(b), D);
+    const float r0 = __shfl_sync(kFull, r, base), r1 = __shfl_sync(kFull, r, base + 1);
+    const bool degenerate = !(D >= 0x1p-120f);
+    const float inv = degenerate ? 0.0f : r0, scale = degenerate ? 0.0f : r1;
+    unsigned long long f = 0ull;
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+      const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
+      f |= (unsigned long long)(__float_as_uint(c) - 0x4B400000u) << (j * b);
+    }
+    unsigned char* slot = out + (valid ? (int)qoff[kt] : 0);
+    if constexpr (kGrp > 1) {
+      f |= __shfl_down_sync(kFull, f, 1) << (V * b);
+      if (flag && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
+    } else {
+      if (flag) sts_bytes(slot + sub * (V * b / 8), f, 0ull, V * b / 8);
+    }
+    if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, scale, false);
+  }
+}
+
+// Stage 3: every tile quantised once, at its width, straight into its slot; the range,
+// the two-values pretest and the exact path as in the single-pass kernel.  Chunks in
+// reverse order: the first ones are the last that stage 1 read, partly still in L2.
+template <typename Tin, int G>
+__global__ void __launch_bounds__(kThreads, 2) k_quant(const __grid_constant__ EncParams p,
+                                                       long long n_chunks,
+                                                       const unsigned long long* chunk_off,
+                                                       const uint32_t* desc) {
+  using C = Cfg<Tin, G>;
+  using LG = LineGeom<Tin, G>;
+  constexpr int LPT = LG::LPT, NE = LG::NE;
+  static_assert(C::CH <= kThreads, "one thread per tile of a chunk");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  EncSmem<Tin, G>& s = enc_smem<Tin, G>(smem_raw);
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+    s.ndef[0] = s.ndef[1] = 0u;
+  }
+  const unsigned long long pol = policy_evict_first();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int line = warp * 32 + lane, pos = line / LPT, sub = line % LPT;
+  uint32_t parity = 0u;
+  int slot = 0;
+  auto chunk_of = [&](long long i) { return n_chunks - 1 - i; };
+  long long i = blockIdx.x;
+  // this lane's descriptor (its place `pos` in the chunk's width order), a chunk ahead
+  auto load_desc = [&](long long ii) -> uint32_t {
+    if (ii >= n_chunks) return 0u;
+    const long long cc = chunk_of(ii);
+    return pos < (int)min((long long)C::CH, p.n_tiles - cc * C::CH) ? __ldcg(&desc[cc * C::CH + pos])
+                                                                     : 0u;
+  };
+  uint32_t dnext = load_desc(i);
+  if (threadIdx.x == 0 && i < n_chunks) {
+    const long long c = chunk_of(i);
+    issue_chunk<Tin, G>(s, p, c * C::CH, (int)min((long long)C::CH, p.n_tiles - c * C::CH), 0, pol);
+  }
+  for (; i < n_chunks; i += gridDim.x) {
+    const uint32_t dcur = dnext;
+    dnext = load_desc(i + gridDim.x);
+    csync();  // the previous chunk's buffer, list and arrays are free
+    const long long nx = i + gridDim.x;
+    if (threadIdx.x == 0) {
+      s.ndef[slot ^ 1] = 0u;
+      if (nx < n_chunks) {
+        const long long cn = chunk_of(nx);
+        issue_chunk<Tin, G>(s, p, cn * C::CH, (int)min((long long)C::CH, p.n_tiles - cn * C::CH),
+                            slot ^ 1, pol);
+      }
+    }
+    const long long c = chunk_of(i);
+    const long long t0 = c * C::CH;
+    const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
+    unsigned char* out = p.codes + __ldcg(&chunk_off[c]);
+    // the chunk's tiles in width order (k_widths), so that a warp's tiles share one width
+    const bool valid = pos < nt;
+    const int kt = (int)(dcur & 0xFFu);
+    const int b = (dcur & 0x100u) ? 4 : 3;
+    const int qo = (int)(dcur >> 16);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    parity ^= 1u << slot;
+    const unsigned char* buf = s.buf[slot];
+    const int tline = kt * LPT + sub;  // this lane's line of the chunk
+    uint32_t w[32];
+    lds_line(buf, tline, w);
+    float mn, mx, ga[NE / 8];
+    line_minmax<Tin>(w, mn, mx, ga);
+    mn = team_min<LPT>(mn);
+    mx = team_max<LPT>(mx);
+    const float m1 = fmaxf(mx, -mn);
+    const float thr = __fmul_rn(m1, 0.5f);  // exact halving for m1 >= 2^-120
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
+    cnt = team_sum_u<LPT>(cnt);
+    const bool small = m1 < 0x1p-120f;
+    const bool deferred = !small && (!(m1 <= FLT_MAX) || cnt < 2u);
+    const float D = __fsub_rn(mx, mn);
+    float inv, scale;
+    if constexpr (LPT >= 2) {
+      const bool odd = sub & 1;
+      const float r = odd ? __fdiv_rn(D, qmax_f(b)) : __fdiv_rn(qmax_f(b), D);
+      const float o = __shfl_xor_sync(kFull, r, 1);
+      inv = odd ? o : r;
+      scale = odd ? r : o;
+    } else {
+      inv = __fdiv_rn(qmax_f(b), D);
+      scale = __fdiv_rn(D, qmax_f(b));
+    }
+    if (!(D >= 0x1p-120f)) inv = scale = 0.0f;
+    if (valid) {
+      if (b == 3) {
+        line_quant<Tin, 3>(w, mn, inv, 3, out + qo + sub * (NE * 3 / 8));
+      } else {
+        line_quant<Tin, 4>(w, mn, inv, 4, out + qo + sub * (NE * 4 / 8));
+      }
+      if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, scale, false);
+    }
+    if (valid && sub == 0) {
+      s.qoff[kt] = (uint16_t)qo;
+      s.qb[kt] = (uint8_t)b;
+      if (deferred) s.dl[atomicAdd(&s.ndef[slot], 1u)] = (uint16_t)kt;
+    }
+    csync();
+    pass2_k3<Tin, G, p2_values<Tin, G, 3, 4>()>(p, buf, s.dl, (int)s.ndef[slot], t0, out,
+                                                s.qoff, s.qb);
+    slot ^= 1;
+  }
+}
+
 // ====================================================================== launchers
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1668,6 +2171,36 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, n_chunks));
     kern<<<grid, kThreads, smem, st>>>(p, n_chunks);
     return cudaGetLastError();
+  }
+  if constexpr (C::kLine) {
+    // the method's defaults with widths {3, 4}, 16-byte slots and groups of whole chunks:
+    // the three-stage encoder
+    const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0;
+    if (plain && a.lo == 3 && a.hi == 4 && p.direct && a.n_g % C::CH == 0) {
+      static_assert(C::CH >= 64 && C::CH <= kThreads && (kThreads % C::CH) == 0,
+                    "chunks of 64..256 tiles");
+      const long long n_chunks = a.n_tiles / C::CH;
+      const int grid = (int)std::max<long long>(1, std::min<long long>(grid_cap, n_chunks));
+      // the candidates array is free once the select has run: each chunk's hi count; the
+      // offsets go where the work queue keeps its segment masks (n / CH words of 8 bytes
+      // fit in n / 32 words of 4)
+      uint32_t* chunk_hi = reinterpret_cast<uint32_t*>(a.cand);
+      uint32_t* desc = reinterpret_cast<uint32_t*>(a.cand + (n_chunks + 1) / 2 + 1);
+      unsigned long long* chunk_off = reinterpret_cast<unsigned long long*>(a.segmask);
+      if (a.n_tiles >= (1ll << 31)) return cudaErrorInvalidValue;
+      const int J = (int)std::max<long long>(1, std::min<long long>(64, a.n_g / 4096));
+      cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      k_stats<Tin, G><<<grid, kThreads, smem, st>>>(p, n_chunks);
+      k_gather<<<(unsigned)(a.n_groups * J), kThreads, 0, st>>>(p, J);
+      k_rank<<<(unsigned)a.n_groups, kThreads, 0, st>>>(p);
+      k_widths<C::CH><<<(unsigned)((a.n_tiles + kThreads - 1) / kThreads), kThreads, 0, st>>>(p, chunk_hi, desc);
+      k_chunk_scan<C::CH><<<(unsigned)a.n_groups, kThreads, 0, st>>>(p, chunk_hi, chunk_off);
+      k_quant<Tin, G><<<grid, kThreads, smem, st>>>(p, n_chunks, chunk_off, desc);
+      return cudaGetLastError();
+    }
   }
   p.nA = (a.n_g + C::CH - 1) / C::CH;
   p.CHC = encode_cchunk_tiles(C::kBf16, G, a.hi);
