@@ -351,11 +351,27 @@ def run_gpu(args):
         n_g //= args.alloc_tile // G      # allocation tiles a group
         K_hi = int(np.floor((w.budget - w.bits_lo) * n_g / (w.bits_hi - w.bits_lo)))
     ranked = 0 < K_hi < n_g
-    # encode: the queue table and the persistent kernel (ranked) or one kernel (one width);
-    # decode: totals, scan, decode
-    launches = (2 if ranked else 1) + 3 + (2 if args.wire else 0)  # wire: pack, unpack
-    enc_kernel = (f"k_encode<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}> (+ k_items)" if ranked
-                  else f"k_encode_flat<{'bf16' if w.dtype == 'bf16' else 'f32'},{G}>")
+    dt = "bf16" if w.dtype == "bf16" else "f32"
+    esize = 2 if w.dtype == "bf16" else 4
+    # the encoder's path, as the library chooses it: one kernel for one width; the
+    # three-stage encoder for the method's defaults with widths {3, 4} on 128-byte lines,
+    # 16-byte slots and groups of whole 32 KB chunks; else the work-queue kernel
+    slot_lo, slot_hi = G * w.bits_lo // 8, G * w.bits_hi // 8
+    group_bytes = tq.tahq_payload_size(T, C, G, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
+    group_bytes //= max(1, T // (w.tokens_per_group or T))
+    three = (ranked and G * esize >= 128 and (w.bits_lo, w.bits_hi) == (3, 4)
+             and args.tau in (None, 2.0) and not args.wire and args.alloc_tile in (0, G)
+             and slot_lo % 16 == 0 and slot_hi % 16 == 0 and group_bytes % 16 == 0
+             and (w.tokens_per_group or T) * (C // G) % (32768 // (G * esize)) == 0)
+    enc_launches = 6 if three else (2 if ranked else 1)
+    # decode: totals, scan, decode; the wire format adds pack and unpack
+    launches = enc_launches + 3 + (2 if args.wire else 0)
+    if three:
+        enc_kernel = f"k_stats<{dt},{G}> + k_quant<{dt},{G}> (+ k_gather, k_rank, k_widths, k_chunk_scan)"
+    elif ranked:
+        enc_kernel = f"k_encode<{dt},{G}> (+ k_items)"
+    else:
+        enc_kernel = f"k_encode_flat<{dt},{G}>"
 
     def step(ev, k=0):
         ev[0].record(stream)
