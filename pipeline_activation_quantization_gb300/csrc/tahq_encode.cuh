@@ -1950,8 +1950,11 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
 // Stage 3: every tile quantised once, at its width, straight into its slot; the range,
 // the two-values pretest and the exact path as in the single-pass kernel.  Chunks in
 // reverse order: the first ones are the last that stage 1 read, partly still in L2.
+// Three blocks per SM (no lg tables, <= 80 registers): while one block's warps wait at a
+// barrier for the exact path of its deferred tiles, the others issue.
+constexpr int kQuantBlocks = 3;
 template <typename Tin, int G>
-__global__ void __launch_bounds__(kThreads, 2) k_quant(const __grid_constant__ EncParams p,
+__global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_constant__ EncParams p,
                                                        long long n_chunks,
                                                        const unsigned long long* chunk_off,
                                                        const uint32_t* desc) {
@@ -2189,16 +2192,22 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       unsigned long long* chunk_off = reinterpret_cast<unsigned long long*>(a.segmask);
       if (a.n_tiles >= (1ll << 31)) return cudaErrorInvalidValue;
       const int J = (int)std::max<long long>(1, std::min<long long>(64, a.n_g / 4096));
-      cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      // neither stage uses the compaction's per-tile arrays
+      const size_t smem3 = sizeof(EncSmem<Tin, G>) + 1024;
+      const int grid_q = (int)std::max<long long>(1, std::min<long long>(a.num_sms * kQuantBlocks, n_chunks));
+      cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
-      k_stats<Tin, G><<<grid, kThreads, smem, st>>>(p, n_chunks);
+      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      k_stats<Tin, G><<<grid, kThreads, smem3, st>>>(p, n_chunks);
       k_gather<<<(unsigned)(a.n_groups * J), kThreads, 0, st>>>(p, J);
       k_rank<<<(unsigned)a.n_groups, kThreads, 0, st>>>(p);
       k_widths<C::CH><<<(unsigned)((a.n_tiles + kThreads - 1) / kThreads), kThreads, 0, st>>>(p, chunk_hi, desc);
       k_chunk_scan<C::CH><<<(unsigned)a.n_groups, kThreads, 0, st>>>(p, chunk_hi, chunk_off);
-      k_quant<Tin, G><<<grid, kThreads, smem, st>>>(p, n_chunks, chunk_off, desc);
+      k_quant<Tin, G><<<grid_q, kThreads, smem3, st>>>(p, n_chunks, chunk_off, desc);
       return cudaGetLastError();
     }
   }
