@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long l
   __shared__ uint32_t s_t[kDecWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long c = (long long)blockIdx.x * kDecWarps + warp;
+  dep_launch();
   const uint32_t tot = c < n_chunks ? warp_chunk_bytes<G>(a.bits, a.n_tiles, c) : 0u;
   if (lane == 0) s_t[warp] = tot;
   __syncthreads();
@@ -193,6 +194,8 @@ __global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blo
   __shared__ unsigned long long s_w[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long carry = 0;
+  dep_wait();
+  dep_launch();
   for (long long p0 = 0; p0 < n_blocks; p0 += kPass) {
     const long long i0 = p0 + (long long)threadIdx.x * kPer;
     unsigned long long v[kPer], mine = 0;
@@ -293,6 +296,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
 
   // the bytes of the block's first chunk; in each iteration the next chunk's bytes are
   // copied while this one is unpacked
+  dep_wait();  // the chunk offsets
   int slot = 0;
   int pad = blockIdx.x < n_chunks ? issue_chunk_bytes<G>(a, blockIdx.x, n_chunks, n_blocks, s.stage[0]) : 0;
   for (long long c = blockIdx.x; c < n_chunks; c += gridDim.x, slot ^= 1) {
@@ -414,16 +418,20 @@ template <int G>
 static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   const long long n_chunks = decode_chunks(G, a.n_tiles);
   const long long n_blocks = decode_blocks(G, a.n_tiles);
-  k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks);
-  k_dec_scan<<<1, 1024, 0, st>>>(a, n_blocks);
   // 6 blocks per SM: what registers (40) and shared memory allow, so that the blocks'
   // load, scan and unpack phases overlap
   const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   const size_t smem = sizeof(DecSmem<G>);
-  const cudaError_t e = cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_decode<G><<<blocks, kDecThreads, smem, st>>>(a, n_chunks, n_blocks);
-  return cudaGetLastError();
+  k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the scan and the unpack start while the kernel before drains (dep_wait inside)
+  e = launch_dependent(k_dec_scan, 1u, 1024u, 0, st, a, n_blocks);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(k_decode<G>, (unsigned)blocks, (unsigned)kDecThreads, smem, st, a, n_chunks,
+                          n_blocks);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {

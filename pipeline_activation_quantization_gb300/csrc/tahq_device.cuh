@@ -58,6 +58,35 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);
 }
 
+// ------------------------------------------------------------------ dependent launches
+
+// A kernel launched by launch_dependent may start while the kernel before it on the
+// stream is still running: dep_wait blocks until that kernel has finished and its writes
+// are visible (a no-op for a kernel launched the ordinary way), dep_launch lets the next
+// kernel on the stream start once every block of this one has called it or exited.  A
+// dependent kernel calls dep_wait before it reads anything the kernels before it wrote,
+// and before it ends, so that it also finishes after all of them.
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ------------------------------------------------------------------ canonical logarithm
 
 // The canonical base-2 logarithm of a positive finite float: x = 2^e m, m in [1, 2),

@@ -1567,6 +1567,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
 // count (k_widths) and the chunks' places in the stream (k_chunk_scan), then k_quant
 // (every tile quantised once, at its width, straight into its slot).  The input is read
 // twice, but each stage is a plain stream over 32 KB chunks without waits between blocks.
+// The stages after the first are dependent launches (launch_dependent): each starts while
+// the one before drains (k_quant with its first input copy) and waits for it with
+// dep_wait before it reads what that one wrote.
 
 // Stage 1: entropy keys and the per-group key histograms.
 template <typename Tin, int G>
@@ -1586,6 +1589,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stats(const __grid_constant__ E
   const unsigned long long pol = policy_evict_normal();  // k_quant reads the last chunks again
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int line = warp * 32 + lane, kt = line / LPT, sub = line % LPT;
+  dep_launch();
   uint32_t parity = 0u;
   int slot = 0;
   long long c = blockIdx.x;
@@ -1654,6 +1658,8 @@ static __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constan
   __shared__ int s_b;
   const long long g = blockIdx.x / J, j = blockIdx.x % J;
   const int lane = threadIdx.x & 31;
+  dep_wait();
+  dep_launch();
   if (threadIdx.x < 32) {
     int bstar;
     uint32_t above;
@@ -1697,6 +1703,8 @@ static __global__ void __launch_bounds__(kThreads) k_rank(const __grid_constant_
   __shared__ uint32_t sc[8];
   __shared__ unsigned long long ck[kRankMax];
   const long long g = blockIdx.x;
+  dep_wait();
+  dep_launch();
   if (threadIdx.x < 32) {
     int bstar;
     uint32_t above;
@@ -1770,6 +1778,8 @@ __global__ void __launch_bounds__(kThreads) k_widths(const __grid_constant__ Enc
   __shared__ uint32_t wcnt[kWarps];
   const long long t = (long long)blockIdx.x * kThreads + threadIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  dep_wait();
+  dep_launch();
   bool ishi = false;
   if (t < p.n_tiles) {
     // group and tile within it (32-bit: the host keeps n_tiles below 2^31 here)
@@ -1811,6 +1821,8 @@ __global__ void __launch_bounds__(kThreads) k_chunk_scan(const __grid_constant__
                                                          unsigned long long* chunk_off) {
   __shared__ uint32_t s_warp[kWarps + 4];
   const long long g = blockIdx.x;
+  dep_wait();
+  dep_launch();
   const long long nc = p.n_g / CH, c0 = g * nc;
   const long long run = (nc + kThreads - 1) / kThreads;
   const long long r0 = min(nc, (long long)threadIdx.x * run), r1 = min(nc, r0 + run);
@@ -1984,11 +1996,12 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
     return pos < (int)min((long long)C::CH, p.n_tiles - cc * C::CH) ? __ldcg(&desc[cc * C::CH + pos])
                                                                      : 0u;
   };
-  uint32_t dnext = load_desc(i);
   if (threadIdx.x == 0 && i < n_chunks) {
     const long long c = chunk_of(i);
     issue_chunk<Tin, G>(s, p, c * C::CH, (int)min((long long)C::CH, p.n_tiles - c * C::CH), 0, pol);
   }
+  dep_wait();  // descriptors and chunk offsets of the stages before
+  uint32_t dnext = load_desc(i);
   for (; i < n_chunks; i += gridDim.x) {
     const uint32_t dcur = dnext;
     dnext = load_desc(i + gridDim.x);
@@ -2203,12 +2216,20 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
                                (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       k_stats<Tin, G><<<grid, kThreads, smem3, st>>>(p, n_chunks);
-      k_gather<<<(unsigned)(a.n_groups * J), kThreads, 0, st>>>(p, J);
-      k_rank<<<(unsigned)a.n_groups, kThreads, 0, st>>>(p);
-      k_widths<C::CH><<<(unsigned)((a.n_tiles + kThreads - 1) / kThreads), kThreads, 0, st>>>(p, chunk_hi, desc);
-      k_chunk_scan<C::CH><<<(unsigned)a.n_groups, kThreads, 0, st>>>(p, chunk_hi, chunk_off);
-      k_quant<Tin, G><<<grid_q, kThreads, smem3, st>>>(p, n_chunks, chunk_off, desc);
-      return cudaGetLastError();
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_gather, (unsigned)(a.n_groups * J), kThreads, 0, st, p, J);
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_rank, (unsigned)a.n_groups, kThreads, 0, st, p);
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_widths<C::CH>, (unsigned)((a.n_tiles + kThreads - 1) / kThreads),
+                           kThreads, 0, st, p, chunk_hi, desc);
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_chunk_scan<C::CH>, (unsigned)a.n_groups, kThreads, 0, st, p,
+                           (const uint32_t*)chunk_hi, chunk_off);
+      if (e != cudaSuccess) return e;
+      return launch_dependent(k_quant<Tin, G>, (unsigned)grid_q, kThreads, smem3, st, p, n_chunks,
+                              (const unsigned long long*)chunk_off, (const uint32_t*)desc);
     }
   }
   p.nA = (a.n_g + C::CH - 1) / C::CH;
