@@ -190,6 +190,13 @@ __device__ __forceinline__ float team_max(float s) {
   return s;
 }
 
+template <int L>
+__device__ __forceinline__ int team_min_i(int s) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) s = min(s, __shfl_xor_sync(kFull, s, o));
+  return s;
+}
+
 // Top-2 magnitudes with the first arg-max, merged across the team.
 template <int L>
 __device__ __forceinline__ void team_top2(float& m1, int& i1, float& m2) {

@@ -43,6 +43,7 @@
 #include <cfloat>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 
@@ -1895,21 +1896,23 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
         if (lane * V + j != i1) l2 = fmaxf(l2, fabsf(v[j]));
       m2 = warp_max_f(l2);
     } else {
-      m1 = fabsf(v[0]);
-      m2 = -1.0f;
-      i1 = sub * V;
+      // without branches: the largest magnitude, its first index (the smallest index
+      // holding it), then the largest magnitude of the other positions
+      float a[V], la = 0.0f;
 #pragma unroll
-      for (int j = 1; j < V; j++) {
-        const float m = fabsf(v[j]);
-        if (m > m1) {
-          m2 = m1;
-          m1 = m;
-          i1 = sub * V + j;
-        } else if (m > m2) {
-          m2 = m;
-        }
+      for (int j = 0; j < V; j++) {
+        a[j] = fabsf(v[j]);
+        la = fmaxf(la, a[j]);
       }
-      team_top2<L>(m1, i1, m2);
+      m1 = team_max<L>(la);
+      int jj = V;
+#pragma unroll
+      for (int j = V - 1; j >= 0; j--) jj = a[j] == m1 ? j : jj;
+      i1 = team_min_i<L>(jj < V ? sub * V + jj : G);
+      float l2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < V; j++) l2 = fmaxf(l2, sub * V + j == i1 ? 0.0f : a[j]);
+      m2 = team_max<L>(l2);
     }
     // the ratio test at tau = 2 without a division (see pass2_line)
     const float d = __fadd_rn(m2, 1e-12f);
@@ -1942,14 +1945,31 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
     const float r0 = __shfl_sync(kFull, r, base), r1 = __shfl_sync(kFull, r, base + 1);
     const bool degenerate = !(D >= 0x1p-120f);
     const float inv = degenerate ? 0.0f : r0, scale = degenerate ? 0.0f : r1;
-    unsigned long long f = 0ull;
+    // the lane's field of V codes (one word for V = 8, b <= 4)
+    using Field = std::conditional_t<V == 8, uint32_t, unsigned long long>;
+    Field f = 0;
 #pragma unroll
     for (int j = 0; j < V; j++) {
       const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
-      f |= (unsigned long long)(__float_as_uint(c) - 0x4B400000u) << (j * b);
+      f |= (Field)(__float_as_uint(c) - 0x4B400000u) << (j * b);
     }
     unsigned char* slot = out + (valid ? (int)qoff[kt] : 0);
-    if constexpr (kGrp > 1) {
+    if constexpr (V == 8) {
+      // eight codes a lane: one word at b = 4; at b = 3 (the only other width of the
+      // three-stage encoder) the fields of four lanes make three words (slots start on
+      // 16-byte boundaries)
+      const uint32_t f0 = (uint32_t)f;
+      const uint32_t f1 = __shfl_down_sync(kFull, f0, 1), f2 = __shfl_down_sync(kFull, f0, 2);
+      const uint32_t f3 = __shfl_down_sync(kFull, f0, 3);
+      if (flag && b == 4) {
+        *reinterpret_cast<uint32_t*>(slot + 4 * sub) = f0;
+      } else if (flag && (sub & 3) == 0) {
+        uint32_t* d = reinterpret_cast<uint32_t*>(slot + 3 * sub);
+        d[0] = f0 | (f1 << 24);
+        d[1] = (f1 >> 8) | (f2 << 16);
+        d[2] = (f2 >> 16) | (f3 << 8);
+      }
+    } else if constexpr (kGrp > 1) {
       f |= __shfl_down_sync(kFull, f, 1) << (V * b);
       if (flag && sub % kGrp == 0) sts_bytes(slot + (sub / kGrp) * b, f, 0ull, b);
     } else {
