@@ -197,22 +197,27 @@ __device__ __forceinline__ int team_min_i(int s) {
   return s;
 }
 
-// Top-2 magnitudes with the first arg-max, merged across the team.
-template <int L>
-__device__ __forceinline__ void team_top2(float& m1, int& i1, float& m2) {
+// Top-2 of a tile spread over a team of L lanes, V values a lane (position sub * V + j):
+// m1 = the largest magnitude, i1 = the first position holding it, m2 = the largest
+// magnitude of the other positions.  No branches: three team reductions.
+template <int V, int L>
+__device__ __forceinline__ void team_top2_values(const float* v, int sub, float& m1, int& i1,
+                                                 float& m2) {
+  float a[V], la = 0.0f;
 #pragma unroll
-  for (int o = 1; o < L; o <<= 1) {
-    const float om1 = __shfl_xor_sync(kFull, m1, o);
-    const int oi1 = __shfl_xor_sync(kFull, i1, o);
-    const float om2 = __shfl_xor_sync(kFull, m2, o);
-    if (om1 > m1 || (om1 == m1 && oi1 < i1)) {
-      m2 = fmaxf(m1, om2);
-      m1 = om1;
-      i1 = oi1;
-    } else {
-      m2 = fmaxf(m2, om1);
-    }
+  for (int j = 0; j < V; j++) {
+    a[j] = fabsf(v[j]);
+    la = fmaxf(la, a[j]);
   }
+  m1 = team_max<L>(la);
+  int jj = V;
+#pragma unroll
+  for (int j = V - 1; j >= 0; j--) jj = a[j] == m1 ? j : jj;
+  i1 = team_min_i<L>(jj < V ? sub * V + jj : V * L);
+  float l2 = 0.0f;
+#pragma unroll
+  for (int j = 0; j < V; j++) l2 = fmaxf(l2, sub * V + j == i1 ? 0.0f : a[j]);
+  m2 = team_max<L>(l2);
 }
 
 // In-register Sylvester FWHT of every h-block of the team's tile (h | G, h a power of

@@ -310,20 +310,9 @@ __device__ __forceinline__ void pass2_teams(const EncParams& p, const unsigned c
     }
     float v[V];
     words_to_values<Tin, G>(w, v);
-    float m1 = fabsf(v[0]), m2 = -1.0f;
-    int i1 = sub * V;
-#pragma unroll
-    for (int j = 1; j < V; j++) {
-      const float m = fabsf(v[j]);
-      if (m > m1) {
-        m2 = m1;
-        m1 = m;
-        i1 = sub * V + j;
-      } else if (m > m2) {
-        m2 = m;
-      }
-    }
-    team_top2<L>(m1, i1, m2);
+    float m1, m2;
+    int i1;
+    team_top2_values<V, L>(v, sub, m1, i1, m2);
     const bool flag = valid && __fdiv_rn(m1, __fadd_rn(m2, 1e-12f)) > p.tau;
     if (__any_sync(kFull, flag)) {
       float t[V];
@@ -491,21 +480,7 @@ __device__ __forceinline__ void pass2_line(const EncParams& p, const unsigned ch
         if (lane * V + j != i1) l2 = fmaxf(l2, fabsf(v[j]));
       m2 = warp_max_f(l2);
     } else {
-      m1 = fabsf(v[0]);
-      m2 = -1.0f;
-      i1 = sub * V;
-#pragma unroll
-      for (int j = 1; j < V; j++) {
-        const float m = fabsf(v[j]);
-        if (m > m1) {
-          m2 = m1;
-          m1 = m;
-          i1 = sub * V + j;
-        } else if (m > m2) {
-          m2 = m;
-        }
-      }
-      team_top2<L>(m1, i1, m2);
+      team_top2_values<V, L>(v, sub, m1, i1, m2);
     }
     const float d = __fadd_rn(m2, 1e-12f);
     const bool flag =
@@ -1896,23 +1871,7 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
         if (lane * V + j != i1) l2 = fmaxf(l2, fabsf(v[j]));
       m2 = warp_max_f(l2);
     } else {
-      // without branches: the largest magnitude, its first index (the smallest index
-      // holding it), then the largest magnitude of the other positions
-      float a[V], la = 0.0f;
-#pragma unroll
-      for (int j = 0; j < V; j++) {
-        a[j] = fabsf(v[j]);
-        la = fmaxf(la, a[j]);
-      }
-      m1 = team_max<L>(la);
-      int jj = V;
-#pragma unroll
-      for (int j = V - 1; j >= 0; j--) jj = a[j] == m1 ? j : jj;
-      i1 = team_min_i<L>(jj < V ? sub * V + jj : G);
-      float l2 = 0.0f;
-#pragma unroll
-      for (int j = 0; j < V; j++) l2 = fmaxf(l2, sub * V + j == i1 ? 0.0f : a[j]);
-      m2 = team_max<L>(l2);
+      team_top2_values<V, L>(v, sub, m1, i1, m2);
     }
     // the ratio test at tau = 2 without a division (see pass2_line)
     const float d = __fadd_rn(m2, 1e-12f);
