@@ -65,6 +65,9 @@ struct DecCfg {
   static constexpr int NS = kSteps * TPW;              // tiles per warp
   static constexpr int kPer = (CH + kDecThreads - 1) / kDecThreads;
   static constexpr int kStage = CH * G + 64;           // b <= 8, plus pad and slack
+  // blocks per SM the registers must allow (six fit the shared memory; the prefetched
+  // metadata of 8 tiles a thread at G = 8 needs more registers than six leave)
+  static constexpr int kMinBlocks = G >= 16 ? 6 : 4;
 };
 
 template <int G>
@@ -284,7 +287,7 @@ __device__ __forceinline__ int issue_chunk_bytes(const DecodeArgs& a, long long 
 }
 
 template <int G>
-__global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long n_chunks,
+__global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(DecodeArgs a, long long n_chunks,
                                                         long long n_blocks) {
   using C = DecCfg<G>;
   constexpr int V = C::V, L = C::L, TPW = C::TPW, CH = C::CH, NS = C::NS;
@@ -295,10 +298,31 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
   const unsigned long long limit = a.codes_bytes;
 
   // the bytes of the block's first chunk; in each iteration the next chunk's bytes are
-  // copied while this one is unpacked
+  // copied while this one is unpacked, and the next chunk's per-tile metadata (width |
+  // pivot << 8, scale, zero of tile k = thread * kPer + j) and first byte are loaded into
+  // registers
   dep_wait();  // the chunk offsets
   int slot = 0;
   int pad = blockIdx.x < n_chunks ? issue_chunk_bytes<G>(a, blockIdx.x, n_chunks, n_blocks, s.stage[0]) : 0;
+  uint32_t nbp[C::kPer];
+  float nsc[C::kPer], nze[C::kPer];
+  unsigned long long nbase = 0ull;
+  auto load_meta = [&](long long cc) {
+    if (cc >= n_chunks) return;
+    const long long tt = cc * CH;
+    const int ntt = (int)min((long long)CH, a.n_tiles - tt);
+#pragma unroll
+    for (int j = 0; j < C::kPer; j++) {
+      const int k = threadIdx.x * C::kPer + j;
+      if (k < ntt) {
+        nbp[j] = (uint32_t)a.bits[tt + k] | ((uint32_t)a.pivots[tt + k] << 8);
+        nsc[j] = a.scales[tt + k];
+        nze[j] = a.zeros[tt + k];
+      }
+    }
+    nbase = a.bsum[cc / kDecChunksPerBlock] + a.ctot[cc];
+  };
+  load_meta(blockIdx.x);
   for (long long c = blockIdx.x; c < n_chunks; c += gridDim.x, slot ^= 1) {
     const long long cn = c + gridDim.x;
     int pad_next = 0;
@@ -310,8 +334,20 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
     const uint32_t* stage = s.stage[slot];
     const long long t0 = c * CH;
     const int nt = (int)min((long long)CH, a.n_tiles - t0);
+    uint32_t cbp[C::kPer];
+#pragma unroll
+    for (int j = 0; j < C::kPer; j++) {
+      const int k = threadIdx.x * C::kPer + j;
+      cbp[j] = nbp[j];
+      if (k < nt) {
+        s.scale[k] = nsc[j];
+        s.zero[k] = nze[j];
+      }
+    }
+    const unsigned long long base = nbase;
+    load_meta(cn);
 
-    // 1. slot sizes of this chunk and their exclusive running sum; metadata staged
+    // 1. slot sizes of this chunk and their exclusive running sum
     uint32_t mine = 0u;
     uint8_t bl[C::kPer];
 #pragma unroll
@@ -319,7 +355,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
       const int k = threadIdx.x * C::kPer + j;
       bl[j] = 0;
       if (k < nt) {
-        int b = a.bits[t0 + k];
+        int b = (int)(cbp[j] & 0xFFu);
         if (b < 1 || b > 8) {
           set_status(a.status, kStBadBits);
           b = 0;
@@ -328,23 +364,19 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a, long long 
         mine += (uint32_t)(G * b / 8);
       }
     }
-    for (int k = threadIdx.x; k < nt; k += kDecThreads) {
-      s.scale[k] = a.scales[t0 + k];
-      s.zero[k] = a.zeros[t0 + k];
-    }
     uint32_t chunk_bytes;
     uint32_t off = block_exclusive_scan_dec<kDecThreads>(mine, chunk_bytes, s.scan);
     (void)chunk_bytes;
-    // the chunk's first byte in the stream (k_dec_totals, k_dec_scan); each tile's slot,
-    // and, settled once here, whether it decodes (width 0: its slot runs past the stream
-    // or its width or pivot is invalid, and it decodes to zeros) and is transformed
-    const unsigned long long base = a.bsum[c / kDecChunksPerBlock] + a.ctot[c];
+    // each tile's slot (the chunk's first byte in the stream from k_dec_totals and
+    // k_dec_scan), and, settled once here, whether it decodes (width 0: its slot runs past
+    // the stream or its width or pivot is invalid, and it decodes to zeros) and is
+    // transformed
 #pragma unroll
     for (int j = 0; j < C::kPer; j++) {
       const int k = threadIdx.x * C::kPer + j;
       if (k < nt) {
         const int b = bl[j];
-        const int piv = a.pivots[t0 + k];
+        const int piv = (int)(cbp[j] >> 8);
         const bool bad_piv = piv != 0xFF && piv >= G;
         if (bad_piv) set_status(a.status, kStBadBits);
         const bool ok = b > 0 && !bad_piv && base + off + (unsigned long long)(G * b / 8) <= limit;
