@@ -1943,8 +1943,10 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
 // reverse order: the first ones are the last that stage 1 read, partly still in L2.
 // Three blocks per SM (no lg tables, <= 80 registers): while one block's warps wait at a
 // barrier for the exact path of its deferred tiles, the others issue.
+// kAL: the alignment of the slots (16 when every slot size and the group stride are
+// multiples of 16 bytes, else 4: widths 3 and 4 of tiles of 32 values or more).
 constexpr int kQuantBlocks = 3;
-template <typename Tin, int G>
+template <typename Tin, int G, int kAL>
 __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_constant__ EncParams p,
                                                        long long n_chunks,
                                                        const unsigned long long* chunk_off,
@@ -2036,9 +2038,9 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
     if (!(D >= 0x1p-120f)) inv = scale = 0.0f;
     if (valid) {
       if (b == 3) {
-        line_quant<Tin, 3>(w, mn, inv, 3, out + qo + sub * (NE * 3 / 8));
+        line_quant<Tin, 3, kAL>(w, mn, inv, 3, out + qo + sub * (NE * 3 / 8));
       } else {
-        line_quant<Tin, 4>(w, mn, inv, 4, out + qo + sub * (NE * 4 / 8));
+        line_quant<Tin, 4, kAL>(w, mn, inv, 4, out + qo + sub * (NE * 4 / 8));
       }
       if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, scale, false);
     }
@@ -2168,10 +2170,11 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     return cudaGetLastError();
   }
   if constexpr (C::kLine) {
-    // the method's defaults with widths {3, 4}, 16-byte slots and groups of whole chunks:
-    // the three-stage encoder
+    // the method's defaults with widths {3, 4} and groups of whole chunks: the three-stage
+    // encoder (its quantiser stores whole 16-byte units where every slot starts on a
+    // 16-byte boundary, else words)
     const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0;
-    if (plain && a.lo == 3 && a.hi == 4 && p.direct && a.n_g % C::CH == 0) {
+    if (plain && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0) {
       static_assert(C::CH >= 64 && C::CH <= kThreads && (kThreads % C::CH) == 0,
                     "chunks of 64..256 tiles");
       const long long n_chunks = a.n_tiles / C::CH;
@@ -2187,11 +2190,13 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       // neither stage uses the compaction's per-tile arrays
       const size_t smem3 = sizeof(EncSmem<Tin, G>) + 1024;
       const int grid_q = (int)std::max<long long>(1, std::min<long long>(a.num_sms * kQuantBlocks, n_chunks));
+      void (*quant)(EncParams, long long, const unsigned long long*, const uint32_t*) =
+          p.direct ? k_quant<Tin, G, 16> : k_quant<Tin, G, 4>;
       cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+      e = cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_quant<Tin, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      e = cudaFuncSetAttribute(quant, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       k_stats<Tin, G><<<grid, kThreads, smem3, st>>>(p, n_chunks);
@@ -2207,7 +2212,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       e = launch_dependent(k_chunk_scan<C::CH>, (unsigned)a.n_groups, kThreads, 0, st, p,
                            (const uint32_t*)chunk_hi, chunk_off);
       if (e != cudaSuccess) return e;
-      return launch_dependent(k_quant<Tin, G>, (unsigned)grid_q, kThreads, smem3, st, p, n_chunks,
+      return launch_dependent(quant, (unsigned)grid_q, kThreads, smem3, st, p, n_chunks,
                               (const unsigned long long*)chunk_off, (const uint32_t*)desc);
     }
   }

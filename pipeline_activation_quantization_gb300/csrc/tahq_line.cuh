@@ -403,8 +403,9 @@ __device__ __forceinline__ void store_fields(unsigned char* dst, const unsigned 
 }
 
 // Quantise the lane's line at B bits (compile time) and store its NE * B / 8 bytes; dst
-// is aligned to the largest power of two (<= 16) dividing NE * B / 8.
-template <typename Tin, int B>
+// is aligned to the largest power of two (<= 16) dividing NE * B / 8, or to AL bytes if
+// AL is smaller (AL = 0: no further limit).
+template <typename Tin, int B, int AL = 0>
 __device__ __forceinline__ void line_quant_store_ct(const uint32_t* w, float mn, float inv,
                                                     unsigned char* dst) {
   constexpr int NE = 128 / (int)sizeof(Tin), NF = NE / 8;
@@ -429,15 +430,17 @@ __device__ __forceinline__ void line_quant_store_ct(const uint32_t* w, float mn,
     }
     f[g] = pack8_ct<B>(q);
   }
-  store_fields<B, NF, lowbit_cap16(NE * B / 8)>(dst, f);
+  constexpr int kNat = lowbit_cap16(NE * B / 8);
+  store_fields<B, NF, (AL > 0 && AL < kNat) ? AL : kNat>(dst, f);
 }
 
-// Width B known at compile time (B > 0) or not (B == 0, width b).
-template <typename Tin, int B>
+// Width B known at compile time (B > 0) or not (B == 0, width b); AL as in
+// line_quant_store_ct.
+template <typename Tin, int B, int AL = 0>
 __device__ __forceinline__ void line_quant(const uint32_t* w, float mn, float inv, int b,
                                            unsigned char* dst) {
   if constexpr (B > 0) {
-    line_quant_store_ct<Tin, B>(w, mn, inv, dst);
+    line_quant_store_ct<Tin, B, AL>(w, mn, inv, dst);
   } else {
     line_quant_store<Tin>(w, mn, inv, b, dst);
   }

@@ -2,12 +2,13 @@
 (``-m gpu``, through the C ABI).
 
 The method's defaults — widths {3, 4}, tau = 2 ("TAH-Quant" §3.3 eq. (3)), allocation per
-tile (§3.2), tile = 128 — on groups of whole 32 KB input chunks (64 fp32 tiles, 128 bf16
-tiles) take the streaming encoder (keys and histograms; select; widths and chunk offsets;
-quantiser with the exact path).  These cases cover its special inputs: ties of every key,
-all tiles flagged (more deferred tiles in a chunk than the quantiser's stage holds),
-ratio exactly tau, zero and subnormal tiles, several chunks and groups.  The acceptance
-rule is ``_parity.assert_parity``.
+tile (§3.2) — on tiles of 128-byte lines or more (fp32 tiles of 32, 64, 128 values, bf16
+of 64, 128) and groups of whole 32 KB input chunks take the streaming encoder (keys and
+histograms; select; widths and chunk offsets; quantiser with the exact path); slots that
+are not 16-byte multiples (tiles of 32 and 64) are stored a word at a time.  These cases
+cover its special inputs: ties of every key, every tile flagged (all through the exact
+path), ratio exactly tau, zero and subnormal tiles, several chunks and groups.  The
+acceptance rule is ``_parity.assert_parity``.
 """
 import numpy as np
 import pytest
@@ -18,8 +19,6 @@ from _parity import assert_parity, gpu_roundtrip, oracle_roundtrip
 
 pytestmark = pytest.mark.gpu
 
-G = 128
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _need_cuda():
@@ -28,13 +27,13 @@ def _need_cuda():
     tq.lib()
 
 
-def _check(x, beta, S):
+def _check(x, beta, S, G=128):
     gpu = gpu_roundtrip(x, G, G, 3, 4, beta, S)
     ora = oracle_roundtrip(x, G, G, 3, 4, beta, S)
     return assert_parity(gpu, ora, G)
 
 
-def _edge(T, C, seed):
+def _edge(T, C, seed, G=128):
     rng = np.random.default_rng(seed)
     tiles = lambda a: a.reshape(-1, G)  # noqa: E731
     out = {"zeros": np.zeros((T, C), np.float32),
@@ -48,7 +47,7 @@ def _edge(T, C, seed):
     out["subnormal"] = (rng.standard_normal((T, C)) * 1e-39).astype(np.float32)
     edge = np.zeros((T, C), np.float32)
     tiles(edge)[:, 3] = 1.0
-    tiles(edge)[:, 70] = 0.5                                  # r == tau exactly
+    tiles(edge)[:, G - 9] = 0.5                               # r == tau exactly
     tiles(edge)[::2, 3] = np.float32(1.0 + 2.0 ** -23)        # r just above tau
     out["ratio_edge"] = edge
     mixed = rng.standard_normal((T, C)).astype(np.float32)
@@ -80,5 +79,27 @@ def test_edge_bf16(name):
     ("bf16", "student_t", 3.5, 48, 2048, 48),           # one group
 ])
 def test_distributions(dtype, dist, beta, T, C, S):
-    w = synth.Workload("three", T, C, dtype, G, G, 3, 4, beta, S, 900 + T, dist)
+    w = synth.Workload("three", T, C, dtype, 128, 128, 3, 4, beta, S, 900 + T, dist)
     print(dist, _check(synth.generate(w), beta, S))
+
+
+# tiles of 32 and 64 values: slots of 12 / 16 and 24 / 32 bytes, stored a word at a time;
+# groups of 16 tokens = 2, 4 and 2 chunks
+@pytest.mark.parametrize("dtype,G,C", [("f32", 32, 1024), ("f32", 64, 2048), ("bf16", 64, 2048)])
+@pytest.mark.parametrize("name", ["spike_every_tile", "ratio_edge", "mixed_scale", "zeros"])
+def test_word_slots_edge(dtype, G, C, name):
+    x = _edge(64, C, 13 + G, G)[name]
+    if dtype == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    print(dtype, G, name, _check(x, 3.5, 16, G))
+
+
+@pytest.mark.parametrize("dtype,G,dist,beta,T,C,S", [
+    ("f32", 32, "laplace", 3.5, 96, 2048, 32),
+    ("f32", 64, "gauss_rms_spikes", 3.25, 64, 4096, 16),
+    ("bf16", 64, "gauss_rms_spikes", 3.5, 128, 4096, 64),   # the bf16 pipeline-boundary shape
+    ("bf16", 64, "student_t", 3.75, 64, 2048, 32),
+])
+def test_word_slots_distributions(dtype, G, dist, beta, T, C, S):
+    w = synth.Workload("three", T, C, dtype, G, G, 3, 4, beta, S, 950 + T + G, dist)
+    print(dtype, G, dist, _check(synth.generate(w), beta, S, G))
