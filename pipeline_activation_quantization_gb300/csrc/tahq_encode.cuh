@@ -1815,8 +1815,9 @@ __global__ void __launch_bounds__(kThreads) k_chunk_scan(const __grid_constant__
 }
 
 // Stage 3's exact path for the tiles the pretest could not clear (as pass2_line, one
-// width: the tile's own, into its slot at out + qoff[kt]).
-template <typename Tin, int G, int V>
+// width: the tile's own, into its slot at out + qoff[kt]); kTau2: tau = 2, tested without
+// a division.
+template <typename Tin, int G, int V, bool kTau2>
 __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char* buf,
                                          const uint16_t* list, int n, long long t0,
                                          unsigned char* out, const uint16_t* qoff,
@@ -1873,9 +1874,11 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
     } else {
       team_top2_values<V, L>(v, sub, m1, i1, m2);
     }
-    // the ratio test at tau = 2 without a division (see pass2_line)
+    // the ratio test (at tau = 2 without a division, see pass2_line)
     const float d = __fadd_rn(m2, 1e-12f);
-    const bool flag = valid && __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f);
+    const bool flag =
+        valid && (kTau2 ? __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f)
+                        : __fdiv_rn(m1, d) > p.tau);
     if (!__any_sync(kFull, flag)) continue;  // the main pass's slot stands
     float t[V];
 #pragma unroll
@@ -1943,10 +1946,12 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
 // reverse order: the first ones are the last that stage 1 read, partly still in L2.
 // Three blocks per SM (no lg tables, <= 80 registers): while one block's warps wait at a
 // barrier for the exact path of its deferred tiles, the others issue.
+// kTau2: tau = 2 (the pretest's threshold by an exact halving, the exact test without a
+// division); else the threshold is m1 / tau rounded up and the test divides.
 // kAL: the alignment of the slots (16 when every slot size and the group stride are
 // multiples of 16 bytes, else 4: widths 3 and 4 of tiles of 32 values or more).
 constexpr int kQuantBlocks = 3;
-template <typename Tin, int G, int kAL>
+template <typename Tin, int G, int kAL, bool kTau2>
 __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_constant__ EncParams p,
                                                        long long n_chunks,
                                                        const unsigned long long* chunk_off,
@@ -2016,12 +2021,15 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
     mn = team_min<LPT>(mn);
     mx = team_max<LPT>(mx);
     const float m1 = fmaxf(mx, -mn);
-    const float thr = __fmul_rn(m1, 0.5f);  // exact halving for m1 >= 2^-120
+    // two values of at least m1 / tau rule out r > tau (for tau = 2 an exact halving,
+    // m1 >= 2^-120 here)
+    const float thr = kTau2 ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
     uint32_t cnt = 0;
 #pragma unroll
     for (int q = 0; q < NE / 8; q++) cnt += ga[q] >= thr ? 1u : 0u;
     cnt = team_sum_u<LPT>(cnt);
-    const bool small = m1 < 0x1p-120f;
+    // below 2^-120 the ratio cannot exceed a tau >= 1 (m2 + 1e-12 > m1 / tau)
+    const bool small = (kTau2 || p.tau >= 1.0f) && m1 < 0x1p-120f;
     const bool deferred = !small && (!(m1 <= FLT_MAX) || cnt < 2u);
     const float D = __fsub_rn(mx, mn);
     float inv, scale;
@@ -2050,7 +2058,7 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
       if (deferred) s.dl[atomicAdd(&s.ndef[slot], 1u)] = (uint16_t)kt;
     }
     csync();
-    pass2_k3<Tin, G, p2_values<Tin, G, 3, 4>()>(p, buf, s.dl, (int)s.ndef[slot], t0, out,
+    pass2_k3<Tin, G, p2_values<Tin, G, 3, 4>(), kTau2>(p, buf, s.dl, (int)s.ndef[slot], t0, out,
                                                 s.qoff, s.qb);
     slot ^= 1;
   }
@@ -2173,7 +2181,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     // the method's defaults with widths {3, 4} and groups of whole chunks: the three-stage
     // encoder (its quantiser stores whole 16-byte units where every slot starts on a
     // 16-byte boundary, else words)
-    const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0;
+    const bool plain = !a.wire && a.mlog == 0;
     if (plain && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0) {
       static_assert(C::CH >= 64 && C::CH <= kThreads && (kThreads % C::CH) == 0,
                     "chunks of 64..256 tiles");
@@ -2191,7 +2199,8 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       const size_t smem3 = sizeof(EncSmem<Tin, G>) + 1024;
       const int grid_q = (int)std::max<long long>(1, std::min<long long>(a.num_sms * kQuantBlocks, n_chunks));
       void (*quant)(EncParams, long long, const unsigned long long*, const uint32_t*) =
-          p.direct ? k_quant<Tin, G, 16> : k_quant<Tin, G, 4>;
+          a.tau == 2.0f ? (p.direct ? k_quant<Tin, G, 16, true> : k_quant<Tin, G, 4, true>)
+                        : (p.direct ? k_quant<Tin, G, 16, false> : k_quant<Tin, G, 4, false>);
       cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);

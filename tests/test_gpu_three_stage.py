@@ -27,9 +27,9 @@ def _need_cuda():
     tq.lib()
 
 
-def _check(x, beta, S, G=128):
-    gpu = gpu_roundtrip(x, G, G, 3, 4, beta, S)
-    ora = oracle_roundtrip(x, G, G, 3, 4, beta, S)
+def _check(x, beta, S, G=128, tau=None):
+    gpu = gpu_roundtrip(x, G, G, 3, 4, beta, S, tau)
+    ora = oracle_roundtrip(x, G, G, 3, 4, beta, S, tau)
     return assert_parity(gpu, ora, G)
 
 
@@ -103,3 +103,23 @@ def test_word_slots_edge(dtype, G, C, name):
 def test_word_slots_distributions(dtype, G, dist, beta, T, C, S):
     w = synth.Workload("three", T, C, dtype, G, G, 3, 4, beta, S, 950 + T + G, dist)
     print(dtype, G, dist, _check(synth.generate(w), beta, S, G))
+
+
+# the outlier threshold as a parameter (Appendix F: 0, 2, 4, infinity; 0.5 and 1.5 also
+# take the pretest's rounded-up threshold and, below 1, no shortcut for tiny tiles)
+@pytest.mark.parametrize("tau", [0.0, 0.5, 1.5, 4.0, float("inf")])
+@pytest.mark.parametrize("dtype,G,C,name", [("f32", 128, 512, "mixed_scale"),
+                                            ("f32", 128, 512, "ratio_edge"),
+                                            ("bf16", 64, 2048, "spike_every_tile"),
+                                            ("f32", 32, 1024, "subnormal")])
+def test_tau_edge(dtype, G, C, name, tau):
+    x = _edge(64, C, 17 + G, G)[name]
+    if dtype == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    print(dtype, G, name, tau, _check(x, 3.5, 16, G, tau))
+
+
+@pytest.mark.parametrize("tau", [0.0, 1.5, 4.0, float("inf")])
+def test_tau_distribution(tau):
+    w = synth.Workload("three", 96, 2048, "f32", 128, 128, 3, 4, 3.5, 16, 990, "gauss_rms_spikes")
+    print(tau, _check(synth.generate(w), 3.5, 16, 128, tau))
