@@ -355,9 +355,9 @@ def run_gpu(args):
     esize = 2 if w.dtype == "bf16" else 4
     # the encoder's path, as the library chooses it: one kernel for one width; the
     # three-stage encoder for widths {3, 4} on 128-byte lines, one key a tile and groups
-    # of whole 32 KB chunks (any tau); else the work-queue kernel
+    # of whole 32 KB chunks (any tau, arrays or the wire format); else the work-queue kernel
     three = (ranked and G * esize >= 128 and (w.bits_lo, w.bits_hi) == (3, 4)
-             and not args.wire and args.alloc_tile in (0, G)
+             and args.alloc_tile in (0, G)
              and (w.tokens_per_group or T) * (C // G) % (32768 // (G * esize)) == 0)
     enc_launches = 6 if three else (2 if ranked else 1)
     # decode: totals, scan, decode; the wire format adds pack and unpack

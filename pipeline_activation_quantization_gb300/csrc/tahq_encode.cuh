@@ -1816,8 +1816,8 @@ __global__ void __launch_bounds__(kThreads) k_chunk_scan(const __grid_constant__
 
 // Stage 3's exact path for the tiles the pretest could not clear (as pass2_line, one
 // width: the tile's own, into its slot at out + qoff[kt]); kTau2: tau = 2, tested without
-// a division.
-template <typename Tin, int G, int V, bool kTau2>
+// a division; kWire: the wire format's quantiser (fp16 zero and scale).
+template <typename Tin, int G, int V, bool kTau2, bool kWire>
 __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char* buf,
                                          const uint16_t* list, int n, long long t0,
                                          unsigned char* out, const uint16_t* qoff,
@@ -1906,13 +1906,19 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
     const float r = sub == 1 ? __fdiv_rn(D, qmax_f(b)) : __fdiv_rn(qmax_f(b), D);
     const float r0 = __shfl_sync(kFull, r, base), r1 = __shfl_sync(kFull, r, base + 1);
     const bool degenerate = !(D >= 0x1p-120f);
-    const float inv = degenerate ? 0.0f : r0, scale = degenerate ? 0.0f : r1;
+    float inv = degenerate ? 0.0f : r0, scale = degenerate ? 0.0f : r1;
+    float qz = mn;  // the quantiser's zero
+    if constexpr (kWire) {  // fp16 zero rounded down, smallest fp16 scale that covers max
+      qz = wire_zero(mn);
+      scale = wire_scale(qz, mx, qmax_f(b));
+      inv = wire_inv(scale);
+    }
     // the lane's field of V codes (one word for V = 8, b <= 4)
     using Field = std::conditional_t<V == 8, uint32_t, unsigned long long>;
     Field f = 0;
 #pragma unroll
     for (int j = 0; j < V; j++) {
-      const float c = __fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f);
+      const float c = __fmaf_rn(__fsub_rn(v[j], qz), inv, 12582912.0f);
       f |= (Field)(__float_as_uint(c) - 0x4B400000u) << (j * b);
     }
     unsigned char* slot = out + (valid ? (int)qoff[kt] : 0);
@@ -1937,7 +1943,7 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
     } else {
       if (flag) sts_bytes(slot + sub * (V * b / 8), f, 0ull, V * b / 8);
     }
-    if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, scale, false);
+    if (flag && sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)i1, scale, false);
   }
 }
 
@@ -1947,11 +1953,13 @@ __device__ __forceinline__ void pass2_k3(const EncParams& p, const unsigned char
 // Three blocks per SM (no lg tables, <= 80 registers): while one block's warps wait at a
 // barrier for the exact path of its deferred tiles, the others issue.
 // kTau2: tau = 2 (the pretest's threshold by an exact halving, the exact test without a
-// division); else the threshold is m1 / tau rounded up and the test divides.
+// division); else the threshold is m1 / tau rounded up and the test divides.  kWire: the
+// wire format's quantiser (fp16 zero rounded down, the smallest fp16 scale that covers the
+// maximum, codes from those).
 // kAL: the alignment of the slots (16 when every slot size and the group stride are
 // multiples of 16 bytes, else 4: widths 3 and 4 of tiles of 32 values or more).
 constexpr int kQuantBlocks = 3;
-template <typename Tin, int G, int kAL, bool kTau2>
+template <typename Tin, int G, int kAL, bool kTau2, bool kWire>
 __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_constant__ EncParams p,
                                                        long long n_chunks,
                                                        const unsigned long long* chunk_off,
@@ -2044,13 +2052,19 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
       scale = __fdiv_rn(D, qmax_f(b));
     }
     if (!(D >= 0x1p-120f)) inv = scale = 0.0f;
+    float qz = mn;  // the quantiser's zero
+    if constexpr (kWire) {  // fp16 zero rounded down, smallest fp16 scale that covers max
+      qz = wire_zero(mn);
+      scale = wire_scale(qz, mx, qmax_f(b));
+      inv = wire_inv(scale);
+    }
     if (valid) {
       if (b == 3) {
-        line_quant<Tin, 3, kAL>(w, mn, inv, 3, out + qo + sub * (NE * 3 / 8));
+        line_quant<Tin, 3, kAL>(w, qz, inv, 3, out + qo + sub * (NE * 3 / 8));
       } else {
-        line_quant<Tin, 4, kAL>(w, mn, inv, 4, out + qo + sub * (NE * 4 / 8));
+        line_quant<Tin, 4, kAL>(w, qz, inv, 4, out + qo + sub * (NE * 4 / 8));
       }
-      if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, scale, false);
+      if (sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)0xFF, scale, false);
     }
     if (valid && sub == 0) {
       s.qoff[kt] = (uint16_t)qo;
@@ -2058,13 +2072,21 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
       if (deferred) s.dl[atomicAdd(&s.ndef[slot], 1u)] = (uint16_t)kt;
     }
     csync();
-    pass2_k3<Tin, G, p2_values<Tin, G, 3, 4>(), kTau2>(p, buf, s.dl, (int)s.ndef[slot], t0, out,
+    pass2_k3<Tin, G, p2_values<Tin, G, 3, 4>(), kTau2, kWire>(p, buf, s.dl, (int)s.ndef[slot], t0, out,
                                                 s.qoff, s.qb);
     slot ^= 1;
   }
 }
 
 // ====================================================================== launchers
+
+using QuantFn = void (*)(EncParams, long long, const unsigned long long*, const uint32_t*);
+
+// The three-stage quantiser for tau = 2 or not, plain or wire, 16-byte or word slots.
+template <typename Tin, int G, bool kTau2, bool kWire>
+static QuantFn quant_kernel(bool direct) {
+  return direct ? k_quant<Tin, G, 16, kTau2, kWire> : k_quant<Tin, G, 4, kTau2, kWire>;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -2181,8 +2203,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     // the method's defaults with widths {3, 4} and groups of whole chunks: the three-stage
     // encoder (its quantiser stores whole 16-byte units where every slot starts on a
     // 16-byte boundary, else words)
-    const bool plain = !a.wire && a.mlog == 0;
-    if (plain && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0) {
+    if (a.mlog == 0 && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0) {
       static_assert(C::CH >= 64 && C::CH <= kThreads && (kThreads % C::CH) == 0,
                     "chunks of 64..256 tiles");
       const long long n_chunks = a.n_tiles / C::CH;
@@ -2198,9 +2219,10 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       // neither stage uses the compaction's per-tile arrays
       const size_t smem3 = sizeof(EncSmem<Tin, G>) + 1024;
       const int grid_q = (int)std::max<long long>(1, std::min<long long>(a.num_sms * kQuantBlocks, n_chunks));
-      void (*quant)(EncParams, long long, const unsigned long long*, const uint32_t*) =
-          a.tau == 2.0f ? (p.direct ? k_quant<Tin, G, 16, true> : k_quant<Tin, G, 4, true>)
-                        : (p.direct ? k_quant<Tin, G, 16, false> : k_quant<Tin, G, 4, false>);
+      QuantFn quant = a.wire ? (a.tau == 2.0f ? quant_kernel<Tin, G, true, true>(p.direct)
+                                              : quant_kernel<Tin, G, false, true>(p.direct))
+                             : (a.tau == 2.0f ? quant_kernel<Tin, G, true, false>(p.direct)
+                                              : quant_kernel<Tin, G, false, false>(p.direct));
       cudaError_t e = cudaFuncSetAttribute(k_stats<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);

@@ -78,6 +78,11 @@ WIRE = [
     ("f32", "gauss_rms_spikes", 8, 8, 3, 5, 4.0, 30, 264, 10),
     ("f32", "laplace", 64, 64, 3, 4, 3.0, 64, 512, 0),       # one width (K = 0)
     ("bf16", "laplace", 128, 64, 3, 4, 4.0, 48, 1152, 16),   # one width (K = n_g)
+    # groups of whole 32 KB chunks: the three-stage encoder with the wire quantiser
+    ("f32", "laplace", 128, 128, 3, 4, 3.5, 64, 512, 16),
+    ("bf16", "gauss_rms_spikes", 64, 64, 3, 4, 3.5, 64, 2048, 16),
+    ("f32", "student_t", 32, 32, 3, 4, 3.25, 64, 1024, 16),
+    ("bf16", "laplace", 128, 64, 3, 4, 3.75, 32, 1024, 16),
 ]
 
 
@@ -91,6 +96,15 @@ def test_wire_parity(dtype, dist, G, h, lo, hi, beta, T, C, S):
 def test_wire_tau(tau):
     w = synth.Workload("wire", 64, 1024, "f32", 64, 64, 3, 4, 3.5, 16, 901, "gauss_rms_spikes")
     print("wire tau", tau, _check_wire(synth.generate(w), 64, 64, 3, 4, 3.5, 16, tau))
+
+
+def test_wire_every_tile_flagged():
+    # one spike in every tile of 128: the three-stage encoder's exact path on all tiles
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((64, 512)) * 1e-3).astype(np.float32)
+    t = x.reshape(-1, 128)
+    t[np.arange(t.shape[0]), rng.integers(0, 128, t.shape[0])] = np.float32(-6.0)
+    print("wire spikes", _check_wire(x, 128, 128, 3, 4, 3.5, 16))
 
 
 def test_wire_full_c3():
