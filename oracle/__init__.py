@@ -4,8 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
 import this package.  The product (``pipeline_activation_quantization_gb300``) never
 imports it and shares no code with it.
 
-The arithmetic lives in ``tahq_oracle.c`` and, for the wire format,
-``tahq_wire_oracle.c`` (plain scalar C, compiled with gcc
+The arithmetic lives in ``tahq_oracle.c``, for the wire format in
+``tahq_wire_oracle.c`` and for the fixed-point gradient codec of the backward pass in
+``tahq_naive_oracle.c`` (plain scalar C, compiled with gcc
 ``-O2 -ffp-contract=off``, no fast-math); this module only compiles it, marshals numpy
 arrays through ctypes, and can split a tensor into its independent token groups to run
 them on several host threads (the per-group results are the same as one sequential call).
@@ -21,7 +22,8 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "tahq_oracle.c"), os.path.join(_HERE, "tahq_wire_oracle.c")]
+_SRCS = [os.path.join(_HERE, "tahq_oracle.c"), os.path.join(_HERE, "tahq_wire_oracle.c"),
+         os.path.join(_HERE, "tahq_naive_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libtahq_oracle.so")
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-std=c11"]
@@ -85,6 +87,9 @@ def lib():
                                              p, i64, p]),
                 "oracle_wire_header": (i32, [p, i64, p]),
                 "oracle_decode_wire": (i32, [p, i64, p]),
+                "oracle_naive_codes_bytes": (C.c_size_t, [i64, i64, i32, i32]),
+                "oracle_naive_encode": (i32, [p, i64, i64, i32, i32, f32, p, p, p, p]),
+                "oracle_naive_decode": (i32, [p, p, p, i64, i64, i32, i32, f32, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -391,4 +396,42 @@ def decode_wire(wire: np.ndarray) -> np.ndarray:
     out = np.zeros((hd["tokens"], hd["channels"]), np.float32)
     if lib().oracle_decode_wire(_ptr(wire), wire.size, _ptr(out)) != 0:
         raise RuntimeError("oracle_decode_wire rejected its input")
+    return out
+
+
+# ------------------------------------------------------------------ backward gradients
+
+def naive_codes_bytes(T: int, Cc: int, G: int, b: int) -> int:
+    """Bytes of the packed b-bit codes of a [T, Cc] tensor in tiles of G (0: invalid)."""
+    return int(lib().oracle_naive_codes_bytes(T, Cc, G, b))
+
+
+def naive_encode(g: np.ndarray, G: int, b: int, c: float = 1.0, want_near: bool = False):
+    """Q_Naive of an fp32 [T, C] gradient at b bits in tiles of G, after scaling by the
+    power of two c: (codes uint8, scales [T * C / G], zeros[, near [T, C]])."""
+    g = _f32(np.ascontiguousarray(g))
+    T, Cc = g.shape
+    nb = naive_codes_bytes(T, Cc, G, b)
+    if nb == 0 and T * Cc > 0:
+        raise ValueError("invalid codec arguments")
+    n = T * (Cc // G)
+    codes = np.zeros(nb, np.uint8)
+    scales = np.zeros(n, np.float32)
+    zeros = np.zeros(n, np.float32)
+    near = np.zeros((T, Cc), np.uint8) if want_near else None
+    if lib().oracle_naive_encode(_ptr(g), T, Cc, G, b, float(c), _ptr(codes), _ptr(scales),
+                                 _ptr(zeros), _ptr(near)) != 0:
+        raise ValueError("invalid codec arguments")
+    return (codes, scales, zeros, near) if want_near else (codes, scales, zeros)
+
+
+def naive_decode(codes, scales, zeros, T: int, Cc: int, G: int, b: int,
+                 c: float = 1.0) -> np.ndarray:
+    """The fp32 [T, C] gradient back from Q_Naive's codes, divided by c."""
+    out = np.zeros((T, Cc), np.float32)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales, zeros = _f32(scales), _f32(zeros)
+    if lib().oracle_naive_decode(_ptr(codes), _ptr(scales), _ptr(zeros), T, Cc, G, b,
+                                 float(c), _ptr(out)) != 0:
+        raise ValueError("invalid codec arguments")
     return out
