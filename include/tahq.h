@@ -242,6 +242,39 @@ tahq_status tahq_decode_wire(const uint8_t *wire, size_t wire_bytes, int64_t tok
                              float budget, int64_t tokens_per_group, float *out, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/* ---- the backward pass's gradient codec ----------------------------------------------
+ * "TAH-Quant" §3.5 and Algorithm 1 (the second stage sends a fixed-point quantisation of
+ * the gradient with respect to the activations back to the first; 6-8 bits, 10 after the
+ * NaN event of Appendix H) and Appendix H eq. (24) (g_hat = Q(c g) / c).  The §3.3
+ * asymmetric quantizer at one width `bits` (1..16) on tiles of `tile` consecutive channels
+ * of a token, no bit allocation, no outlier transform: per tile zero = min, scale =
+ * RN((max - min) / Q), codes RNE((v - min) * RN(Q / (max - min))), Q = 2^bits - 1 (scale 0
+ * and codes 0 when max - min < 2^-120), v = RN(scale_c * g); decode
+ * RN(fma(q, scale, zero) / scale_c).  scale_c must be a positive power of two (exact
+ * scaling).  Codes are packed least significant bit first at `bits` bits, tile after tile
+ * (tile * bits / 8 bytes each); scales and zeros hold one fp32 value per tile.
+ */
+
+/* Bytes of the packed codes; 0 for invalid arguments or a tile other than 32, 64, 128. */
+size_t tahq_naive_codes_bytes(int64_t tokens, int64_t channels, int tile, int bits);
+
+/*
+ * Encode grad [tokens * channels] fp32 (device, 16-byte aligned) into codes (device,
+ * 16-byte aligned, tahq_naive_codes_bytes), scales and zeros (device, tokens * channels /
+ * tile floats each).  All memory is the caller's; stream-ordered, no synchronisation.
+ * TAHQ_ERR_ARG: bits outside 1..16, channels not a multiple of tile, scale_c not a
+ * positive power of two, a NULL or misaligned pointer; TAHQ_ERR_UNSUPPORTED: tile other
+ * than 32, 64 or 128; TAHQ_ERR_CUDA: a launch failed.
+ */
+tahq_status tahq_naive_encode(const float *grad, int64_t tokens, int64_t channels, int tile,
+                              int bits, float scale_c, uint8_t *codes, float *scales,
+                              float *zeros, void *stream);
+
+/* Decode into out [tokens * channels] fp32 (device, 16-byte aligned); errors as encode. */
+tahq_status tahq_naive_decode(const uint8_t *codes, const float *scales, const float *zeros,
+                              int64_t tokens, int64_t channels, int tile, int bits,
+                              float scale_c, float *out, void *stream);
+
 /*
  * Copy the device status word of the last call that used `workspace` into *status_out
  * (may be NULL) after synchronising `stream` (only that stream).  Returns TAHQ_OK if

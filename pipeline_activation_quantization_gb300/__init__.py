@@ -22,7 +22,8 @@ __all__ = [
     "tahq_decode", "tahq_get_device_status", "tahq_status_string", "tahq_version", "tahq_log2_tables",
     "tahq_decode_noalloc", "tahq_wire_size", "tahq_wire_workspace_size",
     "tahq_wire_decode_workspace_size", "tahq_encode_wire", "tahq_decode_wire", "encode", "decode",
-    "encode_wire", "decode_wire", "EXPORTED_SYMBOLS",
+    "encode_wire", "decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
+    "tahq_naive_decode", "naive_encode", "naive_decode", "EXPORTED_SYMBOLS",
 ]
 
 TAHQ_F32, TAHQ_BF16 = 0, 1
@@ -37,7 +38,8 @@ EXPORTED_SYMBOLS = (
     "tahq_payload_size_ex", "tahq_decode_workspace_size", "tahq_decode", "tahq_get_device_status",
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
     "tahq_wire_size", "tahq_wire_workspace_size", "tahq_wire_decode_workspace_size",
-    "tahq_encode_wire", "tahq_decode_wire",
+    "tahq_encode_wire", "tahq_decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
+    "tahq_naive_decode",
 )
 
 
@@ -82,6 +84,9 @@ def lib(path: str | None = None):
         "tahq_encode_wire": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32, p, sz,
                                    p, sz, p]),
         "tahq_decode_wire": (i32, [p, sz, i64, i64, i32, i32, i32, i32, f32, i64, p, p, sz, p]),
+        "tahq_naive_codes_bytes": (sz, [i64, i64, i32, i32]),
+        "tahq_naive_encode": (i32, [p, i64, i64, i32, i32, f32, p, p, p, p]),
+        "tahq_naive_decode": (i32, [p, p, p, i64, i64, i32, i32, f32, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -360,3 +365,52 @@ def decode_wire(wire, tokens: int, channels: int, tile: int = 64, hblock: int | 
                           tokens_per_group, out, workspace, workspace.numel(), stream)
     _check(rc, "tahq_decode_wire")
     return out, workspace
+
+
+# ------------------------------------------------------------------ backward gradients
+
+def tahq_naive_codes_bytes(tokens, channels, tile, bits) -> int:
+    return lib().tahq_naive_codes_bytes(tokens, channels, tile, bits)
+
+
+def tahq_naive_encode(grad, tokens, channels, tile, bits, scale_c, codes, scales, zeros,
+                      stream=None) -> int:
+    return lib().tahq_naive_encode(_ptr(grad), tokens, channels, tile, bits, scale_c, _ptr(codes),
+                                   _ptr(scales), _ptr(zeros), _stream(stream))
+
+
+def tahq_naive_decode(codes, scales, zeros, tokens, channels, tile, bits, scale_c, out,
+                      stream=None) -> int:
+    return lib().tahq_naive_decode(_ptr(codes), _ptr(scales), _ptr(zeros), tokens, channels, tile,
+                                   bits, scale_c, _ptr(out), _stream(stream))
+
+
+def naive_encode(grad, tile: int = 64, bits: int = 8, scale_c: float = 1.0, stream=None):
+    """The backward pass's fixed-point codec of a float32 CUDA tensor [tokens, channels]:
+    ``(codes, scales, zeros)`` as CUDA tensors."""
+    import torch
+    if not grad.is_cuda or grad.dtype != torch.float32:
+        raise ValueError("tahq.naive_encode needs a float32 CUDA tensor")
+    grad = grad.contiguous()
+    T, Cc = grad.shape
+    nb = tahq_naive_codes_bytes(T, Cc, tile, bits)
+    if nb == 0 and T > 0:
+        raise TahqError(1, "tahq_naive_codes_bytes")
+    n = T * (Cc // tile)
+    codes = torch.empty(max(nb, 16), dtype=torch.uint8, device=grad.device)
+    scales = torch.empty(n, dtype=torch.float32, device=grad.device)
+    zeros = torch.empty(n, dtype=torch.float32, device=grad.device)
+    rc = tahq_naive_encode(grad, T, Cc, tile, bits, scale_c, codes, scales, zeros, stream)
+    _check(rc, "tahq_naive_encode")
+    return codes[:nb], scales, zeros
+
+
+def naive_decode(codes, scales, zeros, tokens: int, channels: int, tile: int = 64, bits: int = 8,
+                 scale_c: float = 1.0, out=None, stream=None):
+    """The float32 CUDA tensor [tokens, channels] back from naive_encode's outputs."""
+    import torch
+    if out is None:
+        out = torch.empty((tokens, channels), dtype=torch.float32, device=codes.device)
+    rc = tahq_naive_decode(codes, scales, zeros, tokens, channels, tile, bits, scale_c, out, stream)
+    _check(rc, "tahq_naive_decode")
+    return out

@@ -1,0 +1,195 @@
+// tahq_naive.cu -- the backward pass's fixed-point gradient codec and its C entry points.
+//
+// "TAH-Quant: Effective Activation Quantization in Pipeline Parallelism over Slow
+// Network", §3.5 and Algorithm 1: the second stage sends a fixed-point quantisation of
+// the gradient with respect to the activations back to the first (6-8 bits; 10 after the
+// NaN event of Appendix H); Appendix H eq. (24): g_hat = Q(c g) / c.  The quantiser is
+// the §3.3 asymmetric uniform one at a single width b (1..16) on tiles of G consecutive
+// channels of a token, with no bit allocation and no outlier transform: per tile
+// mn = min, mx = max, D = RN(mx - mn), inv = RN(Q / D), scale = RN(D / Q) (both 0 when
+// D < 2^-120), q = RNE(RN(v - mn) * inv) with the product exact, v = RN(c g); codes
+// packed least significant bit first at b bits; decode RN(fma(q, scale, mn) / c).  c is a
+// power of two, so the scaling is exact unless c g leaves the normal float range.
+//
+// One warp a tile (G = 32, 64 or 128: V = G / 32 values a lane, positions lane * V ...).
+// Encode stages the tile's codes in shared memory and writes each 32-bit word of the
+// slot from the codes it covers; decode extracts each code from the one or two words it
+// spans.  Both are streams bound by HBM (4 bytes read and b / 8 written an element, or
+// the reverse).
+#include <algorithm>
+#include <cmath>
+
+#include "../../include/tahq.h"
+#include "tahq_device.cuh"
+
+namespace tahq {
+namespace {
+
+constexpr int kNaiveWarps = 8;
+
+template <int G>
+__global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_encode(const float* __restrict__ g,
+                                                                   long long n_tiles, int b,
+                                                                   float c, uint8_t* codes,
+                                                                   float* scales, float* zeros) {
+  constexpr int V = G / 32;
+  __shared__ uint16_t sq[kNaiveWarps][G];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t Q = (1u << b) - 1u;
+  const int words = G * b / 32;  // the tile's slot, whole 32-bit words (G >= 32)
+  const long long stride = (long long)gridDim.x * kNaiveWarps;
+  for (long long t = (long long)blockIdx.x * kNaiveWarps + warp; t < n_tiles; t += stride) {
+    float v[V];
+    const float* src = g + t * G + lane * V;
+    if constexpr (V == 4) {
+      const float4 q = *reinterpret_cast<const float4*>(src);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else if constexpr (V == 2) {
+      const float2 q = *reinterpret_cast<const float2*>(src);
+      v[0] = q.x; v[1] = q.y;
+    } else {
+      v[0] = *src;
+    }
+    float mn, mx;
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+      v[j] = __fmul_rn(c, v[j]);
+      mn = j ? fminf(mn, v[j]) : v[j];
+      mx = j ? fmaxf(mx, v[j]) : v[j];
+    }
+    mn = team_min<32>(mn);
+    mx = team_max<32>(mx);
+    const float D = __fsub_rn(mx, mn);
+    const bool live = D >= 0x1p-120f;
+    const float inv = live ? __fdiv_rn((float)Q, D) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+      uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f)) - 0x4B400000u;
+      sq[warp][lane * V + j] = (uint16_t)(live ? min(q, Q) : 0u);
+    }
+    if (lane == 0) {
+      scales[t] = live ? __fdiv_rn(D, (float)Q) : 0.0f;
+      zeros[t] = __fadd_rn(mn, 0.0f);  // a zero minimum as +0
+    }
+    __syncwarp();
+    // word w of the slot holds bits [32 w, 32 w + 32): the codes from floor(32 w / b) on
+    uint32_t* dst = reinterpret_cast<uint32_t*>(codes + t * (long long)(G * b / 8));
+    for (int w = lane; w < words; w += 32) {
+      int k = (32 * w) / b;
+      int off = k * b - 32 * w;  // where code k starts, relative to the word (<= 0)
+      uint32_t acc = 0u;
+      for (; off < 32; ++k, off += b) {
+        const uint32_t q = sq[warp][k];
+        acc |= off >= 0 ? (q << off) : (q >> (-off));
+      }
+      dst[w] = acc;
+    }
+    __syncwarp();
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_decode(const uint8_t* __restrict__ codes,
+                                                                   const float* __restrict__ scales,
+                                                                   const float* __restrict__ zeros,
+                                                                   long long n_tiles, int b, float c,
+                                                                   float* out) {
+  constexpr int V = G / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t mask = (1u << b) - 1u;
+  const long long stride = (long long)gridDim.x * kNaiveWarps;
+  for (long long t = (long long)blockIdx.x * kNaiveWarps + warp; t < n_tiles; t += stride) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + t * (long long)(G * b / 8));
+    const float sc = scales[t], z = zeros[t];
+    float y[V];
+#pragma unroll
+    for (int j = 0; j < V; j++) {
+      const int bit = (lane * V + j) * b, w = bit >> 5, sh = bit & 31;
+      uint32_t q = __ldg(src + w) >> sh;
+      if (sh + b > 32) q |= __ldg(src + w + 1) << (32 - sh);
+      y[j] = __fdiv_rn(__fmaf_rn((float)(q & mask), sc, z), c);
+    }
+    float* dst = out + t * G + lane * V;
+    if constexpr (V == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+    } else if constexpr (V == 2) {
+      *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1]);
+    } else {
+      *dst = y[0];
+    }
+  }
+}
+
+int naive_blocks(long long n_tiles) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 0;
+  const long long want = (n_tiles + kNaiveWarps - 1) / kNaiveWarps;
+  return (int)std::max<long long>(1, std::min<long long>(want, (long long)sms * 8));
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape and argument checks shared by the three entry points.
+tahq_status naive_check(int64_t tokens, int64_t channels, int tile, int bits, float c) {
+  if (tokens < 0 || channels <= 0 || tile <= 0 || bits < 1 || bits > 16) return TAHQ_ERR_ARG;
+  if (channels % tile) return TAHQ_ERR_ARG;
+  int e = 0;
+  if (!(c > 0.0f) || !std::isfinite(c) || std::frexp(c, &e) != 0.5f) return TAHQ_ERR_ARG;
+  if (tile != 32 && tile != 64 && tile != 128) return TAHQ_ERR_UNSUPPORTED;
+  return TAHQ_OK;
+}
+
+}  // namespace
+}  // namespace tahq
+
+extern "C" size_t tahq_naive_codes_bytes(int64_t tokens, int64_t channels, int tile, int bits) {
+  if (tahq::naive_check(tokens, channels, tile, bits, 1.0f) != TAHQ_OK) return 0;
+  return (size_t)(tokens * (channels / tile)) * (size_t)(tile * bits / 8);
+}
+
+extern "C" tahq_status tahq_naive_encode(const float* grad, int64_t tokens, int64_t channels,
+                                         int tile, int bits, float scale_c, uint8_t* codes,
+                                         float* scales, float* zeros, void* stream) {
+  using namespace tahq;
+  const tahq_status st = naive_check(tokens, channels, tile, bits, scale_c);
+  if (st != TAHQ_OK) return st;
+  const long long n = tokens * (channels / tile);
+  if (n == 0) return TAHQ_OK;
+  if (!grad || !codes || !scales || !zeros) return TAHQ_ERR_ARG;
+  if (!aligned_to(grad, 16) || !aligned_to(codes, 16) || !aligned_to(scales, 4) ||
+      !aligned_to(zeros, 4))
+    return TAHQ_ERR_ARG;
+  const int blocks = naive_blocks(n);
+  if (blocks <= 0) return TAHQ_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const dim3 grid(blocks), block(32 * kNaiveWarps);
+  if (tile == 32) k_naive_encode<32><<<grid, block, 0, cs>>>(grad, n, bits, scale_c, codes, scales, zeros);
+  if (tile == 64) k_naive_encode<64><<<grid, block, 0, cs>>>(grad, n, bits, scale_c, codes, scales, zeros);
+  if (tile == 128) k_naive_encode<128><<<grid, block, 0, cs>>>(grad, n, bits, scale_c, codes, scales, zeros);
+  return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}
+
+extern "C" tahq_status tahq_naive_decode(const uint8_t* codes, const float* scales,
+                                         const float* zeros, int64_t tokens, int64_t channels,
+                                         int tile, int bits, float scale_c, float* out,
+                                         void* stream) {
+  using namespace tahq;
+  const tahq_status st = naive_check(tokens, channels, tile, bits, scale_c);
+  if (st != TAHQ_OK) return st;
+  const long long n = tokens * (channels / tile);
+  if (n == 0) return TAHQ_OK;
+  if (!codes || !scales || !zeros || !out) return TAHQ_ERR_ARG;
+  if (!aligned_to(codes, 16) || !aligned_to(out, 16) || !aligned_to(scales, 4) ||
+      !aligned_to(zeros, 4))
+    return TAHQ_ERR_ARG;
+  const int blocks = naive_blocks(n);
+  if (blocks <= 0) return TAHQ_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const dim3 grid(blocks), block(32 * kNaiveWarps);
+  if (tile == 32) k_naive_decode<32><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);
+  if (tile == 64) k_naive_decode<64><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);
+  if (tile == 128) k_naive_decode<128><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);
+  return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+}

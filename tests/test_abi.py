@@ -176,3 +176,21 @@ def test_alloc_tile_argument_errors():
     rc = tq.tahq_encode_ex(fake, tq.TAHQ_F32, 4, 16384, 64, 64, 3, 4, 3.5, 0, 2.0, 16384, fake,
                            fake, fake, fake, fake, fake, 1 << 30, 0)
     assert rc == 2
+
+
+def test_naive_codec_sizes_and_argument_errors():
+    # the backward pass's gradient codec: sizes, and every host-side rejection before any
+    # device call
+    assert tq.tahq_naive_codes_bytes(8, 256, 64, 8) == 8 * 256
+    assert tq.tahq_naive_codes_bytes(8, 256, 32, 10) == 8 * 256 * 10 // 8
+    assert tq.tahq_naive_codes_bytes(8, 256, 16, 8) == 0      # tile not built
+    assert tq.tahq_naive_codes_bytes(8, 250, 64, 8) == 0      # channels not whole tiles
+    assert tq.tahq_naive_codes_bytes(8, 256, 64, 17) == 0     # width beyond 16
+    L = tq.lib()
+    assert L.tahq_naive_encode(None, 4, 256, 64, 8, 3.0, None, None, None, None) == 1
+    assert L.tahq_naive_encode(None, 4, 256, 64, 0, 1.0, None, None, None, None) == 1
+    assert L.tahq_naive_encode(None, 4, 256, 16, 8, 1.0, None, None, None, None) == 2
+    assert L.tahq_naive_encode(None, 4, 256, 64, 8, 1.0, None, None, None, None) == 1
+    assert L.tahq_naive_encode(None, 0, 256, 64, 8, 1.0, None, None, None, None) == 0
+    assert L.tahq_naive_decode(None, None, None, 4, 256, 64, 8, 0.0, None, None) == 1
+    assert L.tahq_naive_decode(None, None, None, 0, 256, 64, 8, 1.0, None, None) == 0
