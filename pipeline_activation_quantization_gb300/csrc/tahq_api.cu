@@ -11,7 +11,7 @@ namespace {
 
 using tahq::LgTables;
 
-constexpr int kVersion = 20000;  // 2.0.0: one-rounding quantizer, fused entropy leaves
+constexpr int kVersion = 20100;  // 2.1.0: tau, allocation tiles, wire format, gradient codec
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
