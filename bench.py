@@ -283,6 +283,89 @@ def job_value(world: int, in_bytes_per_step: int, steps: int, tot_ms: float) -> 
     return world * in_bytes_per_step * steps / (tot_ms * 1e-3) / 1e9
 
 
+# ------------------------------------------------------------------ the other configs
+
+def per_config_workloads():
+    """The parity configs besides the headline one, as (key, workload): the 2048-channel
+    boundary, the 4096-channel boundary, and the 4096-channel sweep of tile = Hadamard block
+    over {32, 64, 128} and budget over {3.0, 3.5, 4.0} (8 x 2048 x 4096 bf16, seed 3)."""
+    out = [("c2", synth.WORKLOADS["c2"]), ("c3", synth.WORKLOADS["c3"])]
+    base = synth.WORKLOADS["c4"]
+    for g, b in synth.C4_SWEEP:
+        out.append((f"c4_g{g}_b{b}", base.with_params(tile=g, hblock=g, budget=b)))
+    return out
+
+
+def time_config(tq, w: synth.Workload, x, steps: int, warmup: int, flush, peak: float) -> dict:
+    """Encode on one stream and decode on another, each timed alone with CUDA events on its
+    own stream, L2 flushed before each; medians (and means) over `steps` calls."""
+    import torch
+    T, C, G, h = w.tokens, w.channels, w.tile, w.hblock
+    sa, sb = torch.cuda.Stream(device=x.device), torch.cuda.Stream(device=x.device)
+    with torch.cuda.stream(sa):
+        enc = tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group)
+    sa.synchronize()
+    with torch.cuda.stream(sb):
+        y = tq.decode(enc, T, C, G, h)
+        dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8,
+                          device=x.device)
+    sb.synchronize()
+    outs = {k: enc[k] for k in ("codes", "scales", "zeros", "bits", "pivots")}
+    ws = enc["workspace"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps + warmup)]
+    for k in range(steps + warmup):
+        e = ev[k]
+        with torch.cuda.stream(sa):
+            flush.fill_(k & 255)
+            e[0].record(sa)
+            tq.encode(x, G, h, w.bits_lo, w.bits_hi, w.budget, w.tokens_per_group, out=outs,
+                      workspace=ws, stream=sa)
+            e[1].record(sa)
+            flush.fill_((k + 7) & 255)
+        sb.wait_stream(sa)
+        with torch.cuda.stream(sb):
+            e[2].record(sb)
+            tq.decode(enc, T, C, G, h, out=y, workspace=dws, stream=sb)
+            e[3].record(sb)
+        sa.wait_stream(sb)
+    torch.cuda.synchronize()
+    rc, word = tq.tahq_get_device_status(ws, sa)
+    if rc != 0:
+        raise RuntimeError(f"{w.name}: device status {word:#x}")
+    enc_ms = [e[0].elapsed_time(e[1]) for e in ev[warmup:]]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev[warmup:]]
+    in_b, enc_b, dec_b = _alg_bytes(w, enc["payload_bytes"])
+
+    def side(ms, alg):
+        med = statistics.median(ms)
+        return {"ms_median": round(med, 5), "ms_mean": round(statistics.mean(ms), 5),
+                "alg_bytes": alg, "GB_s": round(alg / (med * 1e-3) / 1e9, 2),
+                "frac": round(alg / (med * 1e-3) / 1e9 / peak, 4),
+                "input_GB_s": round(in_b / (med * 1e-3) / 1e9, 2),
+                "tokens_per_s": round(T / (med * 1e-3), 1)}
+    return {"workload": w.name, "tile": G, "hblock": h, "budget": w.budget,
+            "tokens_per_group": w.tokens_per_group, "steps": steps,
+            "encode": side(enc_ms, enc_b), "decode": side(dec_ms, dec_b)}
+
+
+def run_per_config(tq, dev, steps: int, warmup: int, flush, peak: float) -> dict:
+    import torch
+    res, cache = {}, {}
+    for key, w in per_config_workloads():
+        src = (w.tokens, w.channels, w.dtype, w.seed, w.dist)
+        if src not in cache:
+            cache.clear()
+            xi = synth.generate(w)
+            cache[src] = torch.from_numpy(xi.view(np.int16)).to(dev).view(torch.bfloat16) \
+                if w.dtype == "bf16" else torch.from_numpy(xi).to(dev)
+        res[key] = time_config(tq, w, cache[src], steps, warmup, flush, peak)
+    target = [v for k, v in res.items() if k != "c2"]
+    res["min_frac_4096_channels"] = {
+        "encode": min(v["encode"]["frac"] for v in target),
+        "decode": min(v["decode"]["frac"] for v in target)}
+    return res
+
+
 # ------------------------------------------------------------------ the CUDA path
 
 def run_gpu(args):
@@ -373,11 +456,13 @@ def run_gpu(args):
         ev[0].record(stream)
         do_encode(xs[k % n_tensors])
         ev[1].record(stream)
-        do_decode()
+        flush.fill_((k + 7) & 255)  # the payload is not left in L2 for the decoder
         ev[2].record(stream)
+        do_decode()
+        ev[3].record(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    warm = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush.fill_(1)
@@ -395,7 +480,7 @@ def run_gpu(args):
         t_wall = time.perf_counter() - t_wall
     barrier()
     enc_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
     tot_ms = sum(enc_ms) + sum(dec_ms)
     rc, word = tq.tahq_get_device_status(ws, stream)
     if rc != 0:
@@ -448,6 +533,13 @@ def run_gpu(args):
 
     if rank != 0:
         return 0
+    per_config = None
+    if not args.no_per_config and args.workload == "c5" and not (args.tokens or args.tile or args.budget
+                                                                 or args.tau is not None
+                                                                 or args.alloc_tile or args.wire):
+        xs.clear()
+        per_config = run_per_config(tq, dev, max(20, args.steps), max(5, args.warmup), flush,
+                                    _peaks()[0])
     A = args.alloc_tile or None
     cpu = (None if args.no_cpu_baseline or world > 1
            else cpu_baseline(w, x_np, tau=args.tau, alloc_tile=A))
@@ -465,10 +557,12 @@ def run_gpu(args):
                                                   tau=args.tau),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "roofline_frac_round_trip": round((enc_b + dec_b) / (ms_step * 1e-3) / 1e9 / peak, 4),
-        "encode": {"ms": round(e_ms, 5), "alg_bytes": enc_b, "GB_s": round(enc_gbs, 2),
+        "encode": {"ms": round(e_ms, 5), "ms_median": round(statistics.median(enc_ms), 5),
+                   "alg_bytes": enc_b, "GB_s": round(enc_gbs, 2),
                    "frac": round(enc_gbs / peak, 4), "input_GB_s": round(in_b / (e_ms * 1e-3) / 1e9, 2),
                    "tokens_per_s": round(T / (e_ms * 1e-3), 1)},
-        "decode": {"ms": round(d_ms, 5), "alg_bytes": dec_b, "GB_s": round(dec_gbs, 2),
+        "decode": {"ms": round(d_ms, 5), "ms_median": round(statistics.median(dec_ms), 5),
+                   "alg_bytes": dec_b, "GB_s": round(dec_gbs, 2),
                    "frac": round(dec_gbs / peak, 4), "tokens_per_s": round(T / (d_ms * 1e-3), 1)},
         "roofline": {"bound": "hbm", "kernel": dom_name,
                      "achieved": round(dom[1] / (dom[2] * 1e-3) / 1e9, 2), "peak": peak,
@@ -479,7 +573,7 @@ def run_gpu(args):
                                  else None)},
         "payload_bytes": payload, "bits_per_element": round(payload * 8 / w.elements, 4),
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e, "gpu_launches": launches * args.steps,
-        "gpu_launches_per_step": launches, "clocks": clocks,
+        "gpu_launches_per_step": launches, "clocks": clocks, "per_config": per_config,
         "wall_s_timed_loop": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
@@ -510,6 +604,8 @@ def parse_args(argv=None):
                     help="time the wire format (tahq_encode_wire / tahq_decode_wire)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the 2048/4096-channel configs (timed after the headline one)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -2078,6 +2078,12 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
   }
 }
 
+}  // namespace tahq
+
+#include "tahq_run.cuh"
+
+namespace tahq {
+
 // ====================================================================== launchers
 
 using QuantFn = void (*)(EncParams, long long, const unsigned long long*, const uint32_t*);
@@ -2183,6 +2189,51 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   const int grid_cap = a.num_sms * 2;
   const bool flat = a.K == 0 || a.K == (a.n_g >> a.mlog);
   p.flat_b = a.K == 0 ? a.lo : a.hi;
+  if constexpr (G >= 32 && G <= 128) {
+    // the streaming encoder: the method's defaults (tau = 2, A = G, fp32 metadata), one
+    // width of 3 or 4 bits, or widths {3, 4} ranked per group of whole input chunks; the
+    // input in 128-byte rows
+    const long long esz = (long long)sizeof(Tin);
+    const bool rows = (a.n_tiles * G * esz) % 128 == 0 && (a.n_g * G) % 128 == 0 &&
+                      a.n_tiles < (1ll << 31);
+    const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0 && rows;
+    const size_t smem_r = sizeof(RunSmem<Tin, G>) + 1024;
+    const long long n_chunks = (a.n_tiles + C::CH - 1) / C::CH;
+    // three blocks an SM (<= 80 registers, two 32 KB stages each)
+    const int grid_r = (int)std::max<long long>(1, std::min<long long>(3ll * a.num_sms, n_chunks));
+    if (plain && flat && (p.flat_b == 3 || p.flat_b == 4)) {
+      cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
+      if (e != cudaSuccess) return e;
+      void (*kern)(EncParams, long long) =
+          p.flat_b == 3 ? k_run_flat<Tin, G, 3> : k_run_flat<Tin, G, 4>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      if (e != cudaSuccess) return e;
+      kern<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      return cudaGetLastError();
+    }
+    if (plain && !flat && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0 &&
+        (a.n_g + kEncMaxCC - 1) / kEncMaxCC <= 64 * 256) {
+      cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
+      if (e != cudaSuccess) return e;
+      p.CHC = kEncMaxCC;
+      p.nC = (a.n_g + p.CHC - 1) / p.CHC;
+      const int J2 = (int)std::max<long long>(1, std::min<long long>(64, a.n_g / 8192));
+      const int J3 = (int)std::max<long long>(1, std::min<long long>(64, p.nC / 2));
+      const int U = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 16
+                    : (p.slot_lo % 8 == 0 && p.slot_hi % 8 == 0 && a.group_bytes % 8 == 0) ? 8 : 4;
+      e = cudaFuncSetAttribute(k_run_tiles<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      if (e != cudaSuccess) return e;
+      k_run_tiles<Tin, G><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_run_select<Tin, G>, (unsigned)(a.n_groups * J2), kThreads, 0, st, p, J2);
+      if (e != cudaSuccess) return e;
+      e = launch_dependent(k_run_widths, (unsigned)(a.n_groups * J3), kThreads, 0, st, p, J3);
+      if (e != cudaSuccess) return e;
+      void (*comp)(EncParams) = U == 16 ? k_run_compact<16> : U == 8 ? k_run_compact<8> : k_run_compact<4>;
+      return launch_dependent(comp, (unsigned)(a.n_groups * p.nC), kThreads, 0, st, p);
+    }
+  }
   // a compaction chunk's per-tile arrays (3 bytes per tile) follow the shared state
   const size_t stages = flat ? 0 : 3 * kMaxCC;
   const size_t smem = sizeof(EncSmem<Tin, G>) + 1024 + stages;
