@@ -436,21 +436,37 @@ def run_gpu(args):
     ranked = 0 < K_hi < n_g
     dt = "bf16" if w.dtype == "bf16" else "f32"
     esize = 2 if w.dtype == "bf16" else 4
-    # the encoder's path, as the library chooses it: one kernel for one width; the
-    # three-stage encoder for widths {3, 4} on 128-byte lines, one key a tile and groups
-    # of whole 32 KB chunks (any tau, arrays or the wire format); else the work-queue kernel
-    three = (ranked and G * esize >= 128 and (w.bits_lo, w.bits_hi) == (3, 4)
-             and args.alloc_tile in (0, G)
-             and (w.tokens_per_group or T) * (C // G) % (32768 // (G * esize)) == 0)
-    enc_launches = 6 if three else (2 if ranked else 1)
-    # decode: totals, scan, decode; the wire format adds pack and unpack
-    launches = enc_launches + 3 + (2 if args.wire else 0)
-    if three:
+    # the encoder's path, as the library chooses it (the launcher in tahq_encode.cuh):
+    # the streaming encoder for the method's defaults (tau = 2, A = G, arrays) on tiles of
+    # 32..128 values in 128-byte rows: one kernel for one width of 3 or 4 bits, else four
+    # for widths {3, 4} ranked per group of whole 32 KB chunks; the three-stage encoder or
+    # the work queue for the variants
+    n_tiles = T * (C // G)
+    n_g_t = (w.tokens_per_group or T) * (C // G)
+    ch = 32768 // (G * esize)
+    flat_b = w.bits_lo if K_hi == 0 else w.bits_hi
+    streaming = ((args.tau is None or args.tau == 2.0) and not args.wire
+                 and args.alloc_tile in (0, G) and 32 <= G <= 128
+                 and (n_tiles * G * esize) % 128 == 0 and (n_g_t * G) % 128 == 0)
+    run_flat = streaming and not ranked and flat_b in (3, 4)
+    run_ranked = (streaming and ranked and (w.bits_lo, w.bits_hi) == (3, 4)
+                  and n_g_t % ch == 0)
+    three = (not run_ranked and ranked and G * esize >= 128 and (w.bits_lo, w.bits_hi) == (3, 4)
+             and args.alloc_tile in (0, G) and n_g_t % ch == 0)
+    if run_flat:
+        enc_launches, enc_kernel = 1, f"k_run_flat<{dt},{G},{flat_b}>"
+    elif run_ranked:
+        enc_launches = 4
+        enc_kernel = f"k_run_tiles<{dt},{G}> (+ k_run_select, k_run_widths, k_run_compact)"
+    elif three:
+        enc_launches = 6
         enc_kernel = f"k_stats<{dt},{G}> + k_quant<{dt},{G}> (+ k_gather, k_rank, k_widths, k_chunk_scan)"
     elif ranked:
-        enc_kernel = f"k_encode<{dt},{G}> (+ k_items)"
+        enc_launches, enc_kernel = 2, f"k_encode<{dt},{G}> (+ k_items)"
     else:
-        enc_kernel = f"k_encode_flat<{dt},{G}>"
+        enc_launches, enc_kernel = 1, f"k_encode_flat<{dt},{G}>"
+    # decode: totals, scan, decode; the wire format adds pack and unpack
+    launches = enc_launches + 3 + (2 if args.wire else 0)
 
     def step(ev, k=0):
         ev[0].record(stream)

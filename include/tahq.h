@@ -282,6 +282,21 @@ tahq_status tahq_naive_decode(const uint8_t *codes, const float *scales, const f
  */
 tahq_status tahq_get_device_status(const void *workspace, uint32_t *status_out, void *stream);
 
+/*
+ * Exercises the bounded wait that every cross-block wait of the kernels uses (the pages
+ * have no counterpart: this is the codec's own failure detection).  One thread waits in
+ * turn on eight counters in `workspace` that nothing advances, each wait limited to
+ * limit_ns nanoseconds of the device's global timer; the first gives up after the limit
+ * and sets TAHQ_DEV_WAIT_TIMEOUT in the status word, and the others return at once on
+ * seeing it.  workspace: device memory of at least 1024 bytes, 256-byte aligned (an
+ * encode workspace serves; its first 1024 bytes are cleared first); elapsed_ns: device
+ * pointer to two uint64 (may be NULL) that receive the time spent in the waits and the
+ * number of waits that gave up.  Stream-ordered; read the result with
+ * tahq_get_device_status(workspace, ...).  limit_ns must be in 1 .. 10^10.
+ */
+tahq_status tahq_test_wait_timeout(void *workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                   uint64_t *elapsed_ns, void *stream);
+
 /* Human-readable name of a tahq_status value (static string, never NULL). */
 const char *tahq_status_string(int status);
 

@@ -23,7 +23,8 @@ __all__ = [
     "tahq_decode_noalloc", "tahq_wire_size", "tahq_wire_workspace_size",
     "tahq_wire_decode_workspace_size", "tahq_encode_wire", "tahq_decode_wire", "encode", "decode",
     "encode_wire", "decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
-    "tahq_naive_decode", "naive_encode", "naive_decode", "EXPORTED_SYMBOLS",
+    "tahq_naive_decode", "naive_encode", "naive_decode", "tahq_test_wait_timeout",
+    "EXPORTED_SYMBOLS",
 ]
 
 TAHQ_F32, TAHQ_BF16 = 0, 1
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
     "tahq_wire_size", "tahq_wire_workspace_size", "tahq_wire_decode_workspace_size",
     "tahq_encode_wire", "tahq_decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
-    "tahq_naive_decode",
+    "tahq_naive_decode", "tahq_test_wait_timeout",
 )
 
 
@@ -87,6 +88,7 @@ def lib(path: str | None = None):
         "tahq_naive_codes_bytes": (sz, [i64, i64, i32, i32]),
         "tahq_naive_encode": (i32, [p, i64, i64, i32, i32, f32, p, p, p, p]),
         "tahq_naive_decode": (i32, [p, p, p, i64, i64, i32, i32, f32, p, p]),
+        "tahq_test_wait_timeout": (i32, [p, sz, C.c_uint64, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -170,6 +172,12 @@ def tahq_decode_noalloc(codes, codes_bytes, scales, zeros, bits, pivots, tokens,
     return lib().tahq_decode_noalloc(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros),
                                      _ptr(bits), _ptr(pivots), tokens, channels, tile, hblock,
                                      _ptr(out), _ptr(device_status), _stream(stream))
+
+
+def tahq_test_wait_timeout(workspace, workspace_bytes, limit_ns, elapsed_ns=None,
+                           stream=None) -> int:
+    return lib().tahq_test_wait_timeout(_ptr(workspace), workspace_bytes, int(limit_ns),
+                                        _ptr(elapsed_ns), _stream(stream))
 
 
 def tahq_get_device_status(workspace, stream=None) -> tuple[int, int]:

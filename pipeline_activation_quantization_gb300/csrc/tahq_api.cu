@@ -242,7 +242,11 @@ tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   const EncLayout L = enc_layout(s);
   if (workspace_bytes < L.total) return TAHQ_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, L.ctrl_end, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  // every tile at one width (K = 0 or K = all): only the status word and the ticket are
+  // used, else the histograms, counters and offsets too
+  const bool one_width = s.K == 0 || s.K == (s.n_g >> s.mlog);
+  if (cudaMemsetAsync(workspace, 0, one_width ? L.cand_cnt : L.ctrl_end, cs) != cudaSuccess)
+    return TAHQ_ERR_CUDA;
   if (s.n == 0) return TAHQ_OK;
   const int sms = num_sms_current();
   if (sms <= 0) return TAHQ_ERR_CUDA;
@@ -555,6 +559,41 @@ tahq_status tahq_decode_wire(const uint8_t* wire, size_t wire_bytes, int64_t tok
   if (tahq::launch_wire_unpack(a, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
   return decode_impl(wire + W.off_pay, (size_t)W.pay, a.scales, a.zeros, a.bits, a.pivots,
                      tokens, channels, tile, hblock, out, workspace, L.total, stream, false);
+}
+
+}  // extern "C"
+
+namespace {
+
+// One thread waits in turn on eight counters that nothing advances.
+__global__ void k_wait_probe(const uint32_t* counters, uint32_t* status,
+                             unsigned long long limit_ns, unsigned long long* elapsed) {
+  if (threadIdx.x != 0) return;
+  const unsigned long long t0 = tahq::global_ns();
+  unsigned long long gave_up = 0;
+  for (int i = 0; i < 8; i++) gave_up += tahq::wait_counter(counters + i, 1u, status, limit_ns) ? 0 : 1;
+  if (elapsed) {
+    elapsed[0] = tahq::global_ns() - t0;
+    elapsed[1] = gave_up;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+tahq_status tahq_test_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                   uint64_t* elapsed_ns, void* stream) {
+  if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < 1024) return TAHQ_ERR_WORKSPACE;
+  if (limit_ns < 1 || limit_ns > 10000000000ull) return TAHQ_ERR_ARG;
+  if (elapsed_ns && !aligned(elapsed_ns, 8)) return TAHQ_ERR_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 1024, cs) != cudaSuccess) return TAHQ_ERR_CUDA;
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  const uint32_t* counters = at<uint32_t>(workspace, 512);
+  k_wait_probe<<<1, 32, 0, cs>>>(counters, status, (unsigned long long)limit_ns,
+                                 reinterpret_cast<unsigned long long*>(elapsed_ns));
+  return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 
 tahq_status tahq_get_device_status(const void* workspace, uint32_t* status_out, void* stream) {

@@ -4,11 +4,14 @@
 // flag, the quantised codes) is spelled out with explicit round-to-nearest intrinsics
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fmaf_rn), so that no contraction or reordering
 // can change a result.  The evaluation order is the canonical one of the codec:
-//   - pairwise sums: sum(x[0..n)) = sum(x[0..n/2)) + sum(x[n/2..n)),
-//   - lg(x) = e + (T[i] + r * P(r)), r = (m - c_i) * R[i], P a Horner polynomial,
+//   - pairwise sums: sum(x[0..n)) = sum(x[0..n/2)) + sum(x[n/2..n)), the first level of
+//     S fused: fmaf(m_odd, lg m_odd, RN(m_even lg m_even)),
+//   - lg(x) = e + fmaf(P(r), r, T[i]), r = fmaf(m, R[i], -1) for x = 2^e m, i the top 7
+//     fraction bits, P(r) = fmaf(fmaf(k3, r, k2), r, k1) (Tang-style table logarithm),
 //   - entropy key H = lg(L) - S / L, L = sum |a|, S = sum |a| lg |a|,
 //   - Hadamard stages len = 1, 2, 4, ... then x RN(1/sqrt(h)),
-//   - u = (v - min) * inv, inv = Q / (max - min), code = rint(u) clamped to [0, Q].
+//   - code = the integer nearest (ties to even) to RN(v - min) * RN(Q / (max - min)),
+//     one rounding (fmaf(v - min, inv, 1.5 * 2^23)); it never exceeds Q, so no clamp.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -277,66 +280,22 @@ __device__ __forceinline__ void team_swap0(float* v, int d, int sub, int team_ba
 
 // ------------------------------------------------------------------ bounded waits
 
-constexpr long long kSpinLimit = 1ll << 22;  // ~0.5 s of 128 ns naps
+// Every wait of a kernel on another block or on a bulk copy is bounded in time: it gives
+// up after a limit in nanoseconds of the global timer (the kernel parameters carry it;
+// kWaitNs by default), sets kStWaitTimeout in the status word and returns, and a wait
+// that finds that bit already set returns at once, so that one lost publication costs a
+// call one limit, not one limit per later wait.
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
 }
 
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ bool timed_out(const uint32_t* status) {
+  return (*reinterpret_cast<const volatile uint32_t*>(status) & kStWaitTimeout) != 0u;
 }
-
-// Look-back words carry state and value in one 64-bit word, so reading them needs no
-// ordering with any other data: relaxed accesses at gpu scope are enough.
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Decoupled look-back words: top two bits = state, low 62 bits = value.
-constexpr unsigned long long kLbAgg = 1ull << 62;
-constexpr unsigned long long kLbPre = 2ull << 62;
-constexpr unsigned long long kLbVal = (1ull << 62) - 1;
-
-// Exclusive prefix of chunk `c` over chunks [first, c): called by one thread after it
-// published its own aggregate.  Chunks are handed out in increasing order by an atomic
-// ticket, so every predecessor is already running.  Gives up (status bit, prefix 0)
-// after kSpinLimit naps rather than wait without a bound.
-__device__ __forceinline__ unsigned long long lookback_prefix(const unsigned long long* words,
-                                                              long long c, long long first,
-                                                              uint32_t* status) {
-  unsigned long long acc = 0;
-  long long p = c - 1;
-  long long spins = 0;
-  while (p >= first) {
-    const unsigned long long w = ld_acquire_u64(words + p);
-    const unsigned long long st = w & ~kLbVal;
-    if (st == kLbPre) {
-      acc += w & kLbVal;
-      return acc;
-    }
-    if (st == kLbAgg) {
-      acc += w & kLbVal;
-      --p;
-      continue;
-    }
-    if (++spins > kSpinLimit) {
-      set_status(status, kStWaitTimeout);
-      return 0;
-    }
-    __nanosleep(128);
-  }
-  return acc;
-}
-
 
 // ------------------------------------------------------------------ bulk copies (TMA)
 
@@ -404,28 +363,31 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
 }
 
 // Wait for phase `parity` of `bar` to complete.  A bulk copy always completes unless the
-// device has faulted; the bound only keeps a broken device from spinning forever.
+// device has faulted; the bound (limit_ns) only keeps a broken device from spinning
+// forever.  The clock and the status word are looked at every 256 polls.
 __device__ __forceinline__ void mbar_wait(unsigned long long* bar, uint32_t parity,
-                                          uint32_t* status) {
-  long long spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if (++spins > kSpinLimit) {
+                                          uint32_t* status, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t n = 1;; n++) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((n & 255u) == 0u && (timed_out(status) || global_ns() - t0 > limit_ns)) {
       set_status(status, kStWaitTimeout);
       return;
     }
   }
 }
 
-// Bounded wait until *flag >= target (flag written by other blocks with release
-// semantics).  Returns false (and sets a status bit) if it gave up.
+// Wait until *flag >= target (flag written by other blocks with release semantics), at
+// most limit_ns; returns false (status bit set) if it gave up or another wait already had.
 __device__ __forceinline__ bool wait_counter(const uint32_t* flag, uint32_t target,
-                                             uint32_t* status) {
-  long long spins = 0;
+                                             uint32_t* status, unsigned long long limit_ns) {
+  const unsigned long long t0 = global_ns();
   for (;;) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
     if (v >= target) return true;
-    if (++spins > kSpinLimit) {
+    if (timed_out(status) || global_ns() - t0 > limit_ns) {
       set_status(status, kStWaitTimeout);
       return false;
     }

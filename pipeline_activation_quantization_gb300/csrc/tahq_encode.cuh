@@ -114,6 +114,7 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
 
 struct EncParams {
   TmaDesc tmap;  // line layout: the input as [rows of 128 bytes]
+  unsigned long long wait_ns;  // bound of every wait (see mbar_wait / wait_counter)
   const void* x;
   long long n_tiles, n_g, n_groups, K, group_bytes, codes_bytes;
   long long nA, nC, CHC, J, lag, pre1, pre2, n_items;
@@ -960,7 +961,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
                           unsigned char* scratch) {
   const long long g = it.g;
   const uint32_t K = (uint32_t)p.K;
-  if (threadIdx.x == 0) wait_counter(&p.doneA[g], (uint32_t)p.nA, p.status);
+  if (threadIdx.x == 0) wait_counter(&p.doneA[g], (uint32_t)p.nA, p.status, p.wait_ns);
   csync();
   uint32_t* bins = s.hist;  // all zero between items; left zero below
   if (threadIdx.x < 32) {
@@ -1088,7 +1089,7 @@ __device__ void do_select(EncSmem<Tin, G>& s, const EncParams& p, const Item& it
 template <typename Tin, int G, bool kGen>
 __device__ void do_offsets(EncSmem<Tin, G>& s, const EncParams& p, const Item& it) {
   const long long g = it.g;
-  if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status);
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 1u, p.status, p.wait_ns);
   csync();
   const unsigned long long theta = __ldcg(&p.sel[g].theta);
   const uint32_t mode = __ldcg(&p.sel[g].mode);
@@ -1213,7 +1214,7 @@ static __device__ void compact_direct(const EncParams& p, long long g, long long
   const int nt = (int)min(p.CHC, p.n_g - tl0);
   const int nseg = (nt + 31) >> 5;
   if (warp >= nseg) return;
-  if (lane == 0) wait_counter(&p.selready[g], 2u, p.status);
+  if (lane == 0) wait_counter(&p.selready[g], 2u, p.status, p.wait_ns);
   __syncwarp();
   const long long t0 = g * p.n_g + tl0;
   const uint32_t* sm = p.segmask + g * ((p.n_g + 31) / 32) + (tl0 >> 5);
@@ -1308,7 +1309,7 @@ __device__ void do_compact(EncSmem<Tin, G>& s, const EncParams& p, const Item& i
     compact_direct(p, g, cc);
     return;
   }
-  if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status);
+  if (threadIdx.x == 0) wait_counter(&p.selready[g], 2u, p.status, p.wait_ns);
   csync();
   const long long tl0 = cc * p.CHC;
   const int nt = (int)min(p.CHC, p.n_g - tl0);
@@ -1474,7 +1475,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(const __grid_constant__ 
     const Item it = s.item[slot];
     if (it.type < 0) break;
     if (it.type == kItemTiles) {
-      mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+      mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status, p.wait_ns);
       parity ^= 1u << slot;
       do_tiles<Tin, G, kLo, kHi, kGen>(s, p, it, s.buf[slot], &s.ndef[slot]);
       done_g = it.g;
@@ -1521,7 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode_flat(const __grid_consta
     }
     const long long t0 = c * C::CH;
     const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
-    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status, p.wait_ns);
     parity ^= 1u << slot;
     // one width: tile t's slot is at t * slot_b in the stream
     unsigned char* out = p.codes + t0 * slot_b;
@@ -1580,7 +1581,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stats(const __grid_constant__ E
     const long long t0 = c * C::CH;
     const int nt = (int)min((long long)C::CH, p.n_tiles - t0);
     const long long g = t0 / p.n_g;  // chunks never straddle groups here
-    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status, p.wait_ns);
     parity ^= 1u << slot;
     float2 ls = line_sums<Tin>(s.buf[slot], line, s.tabs, lg_consts(s.tabs, lane));
     ls = team_sum2<LPT>(ls);
@@ -2018,7 +2019,7 @@ __global__ void __launch_bounds__(kThreads, kQuantBlocks) k_quant(const __grid_c
     const int kt = (int)(dcur & 0xFFu);
     const int b = (dcur & 0x100u) ? 4 : 3;
     const int qo = (int)(dcur >> 16);
-    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status);
+    mbar_wait(&s.bar[slot], (parity >> slot) & 1u, p.status, p.wait_ns);
     parity ^= 1u << slot;
     const unsigned char* buf = s.buf[slot];
     const int tline = kt * LPT + sub;  // this lane's line of the chunk
@@ -2182,6 +2183,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.items = a.items;
   p.status = a.status;
   p.tabs = *a.tabs;
+  p.wait_ns = a.wait_ns ? a.wait_ns : kWaitNs;
   if constexpr (C::kLine) {
     const cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
     if (e != cudaSuccess) return e;
@@ -2206,8 +2208,11 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
       void (*kern)(EncParams, long long) =
           p.flat_b == 3 ? k_run_flat<Tin, G, 3> : k_run_flat<Tin, G, 4>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-      if (e != cudaSuccess) return e;
+      static const cudaError_t e3 =
+          cudaFuncSetAttribute(k_run_flat<Tin, G, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      static const cudaError_t e4 =
+          cudaFuncSetAttribute(k_run_flat<Tin, G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      if (e3 != cudaSuccess || e4 != cudaSuccess) return e3 != cudaSuccess ? e3 : e4;
       kern<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       return cudaGetLastError();
     }
@@ -2221,8 +2226,9 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       const int J3 = (int)std::max<long long>(1, std::min<long long>(64, p.nC / 2));
       const int U = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 16
                     : (p.slot_lo % 8 == 0 && p.slot_hi % 8 == 0 && a.group_bytes % 8 == 0) ? 8 : 4;
-      e = cudaFuncSetAttribute(k_run_tiles<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-      if (e != cudaSuccess) return e;
+      static const cudaError_t e_attr =
+          cudaFuncSetAttribute(k_run_tiles<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      if (e_attr != cudaSuccess) return e_attr;
       k_run_tiles<Tin, G><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

@@ -46,6 +46,7 @@ struct EncodeArgs {
   uint8_t* scratch_hi;       // [n_tiles * G * hi / 8] every tile quantised at bits_hi
   unsigned long long* items; // [items_cap] the decoded work queue
   long long items_cap;
+  unsigned long long wait_ns;  // bound of every wait in the kernels (0: kWaitNs)
 };
 
 struct DecodeArgs {

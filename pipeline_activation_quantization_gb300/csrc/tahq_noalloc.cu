@@ -1,7 +1,8 @@
 // tahq_noalloc.cu -- decode for callers that cannot allocate device memory.
 //
-// tahq_decode needs a small device workspace (a status word, a block ticket and one
-// look-back word per chunk of tiles).  Some callers have no way to provide it: a
+// tahq_decode needs a small device workspace (a status word, a block ticket, each decode
+// chunk's offset inside its block of chunks and each block's stream offset).  Some
+// callers have no way to provide it: a
 // receiving pipeline stage driven by a runtime that plans all device memory ahead of
 // time and hands the codec only its inputs and outputs, or a C caller without a
 // device allocator of its own, for which a cudaMalloc in the receive loop would also

@@ -201,6 +201,7 @@ struct alignas(1024) RunSmem {
   uint32_t hist[2][kCoarseBins];          // coarse key counts of the last two chunks
   LgTables tabs;
   unsigned long long bar[2];
+  long long cur[2];                       // the chunk in each stage (-1: none)
   uint32_t ndef[2];                       // deferred counts, by chunk parity
 };
 
@@ -476,7 +477,7 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
     const long long g = kFlat ? 0 : t0 / p.n_g;  // chunks never straddle groups here
     unsigned char* lo = (kFlat ? p.codes : p.scratch_lo) + t0 * slot_a;
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
-    mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status);
+    mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
     main_run<Tin, G, kFlat, kB>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
@@ -490,12 +491,89 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
   }
 }
 
+// The chunks of the input, each copied in while the one before is processed: the main
+// pass, one block barrier, the exact path of the chunk's deferred tiles (spread over the
+// block's warps).  kDyn: chunks handed out in increasing order by an atomic ticket
+// (faster blocks take more); else blockIdx.x, + gridDim.x, ... (measured faster for the
+// ranked pass, whose blocks all write the same group's histograms).
+template <typename Tin, int G, bool kFlat, int kB, bool kDyn>
+__device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncParams& p,
+                                           long long n_chunks) {
+  constexpr int CH = RunGeom<Tin, G>::CH;
+  const unsigned long long pol = policy_evict_first();  // the input is read once
+  for (int i = threadIdx.x; i < 2 * kCoarseBins; i += kThreads) (&s.hist[0][0])[i] = 0u;
+  if (!kFlat) {
+    const float* src = reinterpret_cast<const float*>(&p.tabs);
+    float* dst = reinterpret_cast<float*>(&s.tabs);
+    for (int i = threadIdx.x; i < (int)(sizeof(LgTables) / 4); i += kThreads) dst[i] = src[i];
+  }
+  const int slot_a = kFlat ? G * kB / 8 : G * 3 / 8, slot_b = G / 2;
+  long long nxt = -1;  // thread 0: the chunk after the staged ones
+  auto next_chunk = [&](long long cur) -> long long {
+    if constexpr (kDyn) {
+      return (long long)atomicAdd(p.ticket, 1u);
+    } else {
+      return cur + gridDim.x;
+    }
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    fence_barrier_init();
+    s.ndef[0] = s.ndef[1] = 0u;
+    const long long c0 = kDyn ? next_chunk(0) : (long long)blockIdx.x;
+    s.cur[0] = c0 < n_chunks ? c0 : -1;
+    if (c0 < n_chunks) issue_run_chunk<Tin, G>(s, p, c0 * CH, 0, pol);
+    nxt = c0 < n_chunks ? next_chunk(c0) : n_chunks;
+  }
+  uint32_t parity = 0u;
+  long long gp = 0;  // group of the previous chunk
+  int k = 0;
+  for (;; ++k) {
+    const int sl = k & 1;
+    csync();  // chunk k - 1 is done: its buffer, list and counts are free
+    const long long c = s.cur[sl];
+    if (c < 0) break;  // block-uniform
+    if (threadIdx.x == 0) {
+      s.ndef[sl ^ 1] = 0u;
+      s.cur[sl ^ 1] = nxt < n_chunks ? nxt : -1;
+      if (nxt < n_chunks) {
+        issue_run_chunk<Tin, G>(s, p, nxt * CH, sl ^ 1, pol);
+        nxt = next_chunk(nxt);
+      }
+    }
+    if constexpr (!kFlat) {  // coarse counts of chunk k - 1, one global add per bin
+      static_assert(kThreads == kCoarseBins, "one coarse bin per thread");
+      const uint32_t cb = s.hist[sl ^ 1][threadIdx.x];
+      if (cb) {
+        atomicAdd(&p.hist_coarse[gp * kCoarseBins + threadIdx.x], cb);
+        s.hist[sl ^ 1][threadIdx.x] = 0u;
+      }
+    }
+    const long long t0 = c * CH;
+    const int nt = (int)min((long long)CH, p.n_tiles - t0);
+    const long long g = kFlat ? 0 : t0 / p.n_g;  // chunks never straddle groups here
+    unsigned char* lo = (kFlat ? p.codes : p.scratch_lo) + t0 * slot_a;
+    unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
+    mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
+    parity ^= 1u << sl;
+    main_run<Tin, G, kFlat, kB>(s, p, g, t0, nt, k, lo, hi);
+    csync();  // the list is complete, and the codes written before the exact path's
+    pass2_run<Tin, G, kFlat, kB>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    gp = g;
+  }
+  if (!kFlat && k) {  // the last chunk's coarse counts (the loop ended after a barrier)
+    const uint32_t cb = s.hist[(k - 1) & 1][threadIdx.x];
+    if (cb) atomicAdd(&p.hist_coarse[gp * kCoarseBins + threadIdx.x], cb);
+  }
+}
+
 // Every tile gets the same width kB (K = 0 or K = n_g): codes at t G kB / 8.
 template <typename Tin, int G, int kB>
 __global__ void __launch_bounds__(kThreads, 3) k_run_flat(const __grid_constant__ EncParams p,
                                                           long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  run_chunks<Tin, G, true, kB>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks_dyn<Tin, G, true, kB, true>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // Stage 1 of widths {3, 4} ranked per group: keys, histograms, both widths into scratch.
@@ -734,13 +812,23 @@ __global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__
   const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
   if (threadIdx.x == 0 && cnt != s.scan[3]) set_status(p.status, kStSelectMismatch);
   const uint32_t r = max(1u, min(K - s.scan[2], cnt));  // rank (from 1) among them
-  // radix select (8 passes of 8 bits), from shared memory when the candidates fit
+  // the r-th largest rank key (they are distinct): by counting when the candidates are
+  // few, else a radix select (8 passes of 8 bits); from shared memory when they fit
   constexpr uint32_t kStage = kChunkBytes / 8;
   unsigned long long* ck = reinterpret_cast<unsigned long long*>(s.buf);
   const bool staged = cnt <= kStage;
   if (staged)
     for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) ck[i] = __ldcg(&cg[i]);
   __syncthreads();
+  if (cnt > 0u && cnt <= 1024u) {
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+      const unsigned long long ki = ck[i];
+      uint32_t larger = 0;
+      for (uint32_t j = 0; j < cnt; j++) larger += ck[j] > ki ? 1u : 0u;
+      if (larger == r - 1u) p.sel[g] = SelResult{ki, kSelThreshold, 0u};
+    }
+    return;
+  }
   uint32_t rr = r;
   unsigned long long prefix = 0ull, mask = 0ull;
   for (int pass = 7; pass >= 0 && cnt > 0u; --pass) {

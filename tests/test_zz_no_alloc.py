@@ -4,8 +4,9 @@ Some receivers of the activation stream cannot hand the codec a workspace: a sta
 runtime plans all device memory in advance and passes only inputs and outputs, or a C
 caller with no device allocator (where a cudaMalloc in the receive loop would also stall
 the device).  This entry point takes its scratch from a fixed array inside the library.
-Its output must match tahq_decode's, within the tolerance the other parity tests use,
-on two calls in a row (the second call reuses the shared array left by the first).
+Its output must match tahq_decode's, and the CPU oracle's decode of the same stream,
+within the tolerance the other parity tests use, on two calls in a row (the second call
+reuses the shared array left by the first).
 
 The file is named so that pytest collects it last.  It passes on its own in a fresh
 process (the first call sets up the array's device address) and after the other tests.
@@ -13,6 +14,7 @@ process (the first call sets up the array's device address) and after the other 
 import numpy as np
 import pytest
 
+import oracle
 import pipeline_activation_quantization_gb300 as tq
 import synth
 
@@ -39,6 +41,10 @@ def test_noalloc_decode_matches_decode_twice(name):
     ref = tq.decode(enc, T, C, G, h)
     torch.cuda.synchronize()
     ref_np = ref.cpu().numpy()
+    # the oracle's decode of the stream the GPU wrote
+    orc = oracle.decode(enc["codes"].cpu().numpy(), enc["scales"].cpu().numpy(),
+                        enc["zeros"].cpu().numpy(), enc["bits"].cpu().numpy(),
+                        enc["pivots"].cpu().numpy(), T, C, G, h)
     status = torch.full((1,), 0xFFFFFFFF, dtype=torch.int64, device="cuda")
     for call in range(2):
         out = torch.full((T, C), float("nan"), dtype=torch.float32, device="cuda")
@@ -49,7 +55,8 @@ def test_noalloc_decode_matches_decode_twice(name):
         torch.cuda.synchronize()
         got = out.cpu().numpy()
         assert np.isfinite(got).all(), f"call {call}: output not fully written"
-        assert _rel_l2(got, ref_np) <= 1e-5, f"call {call}"
+        assert _rel_l2(got, ref_np) <= 1e-5, f"call {call}: against tahq_decode"
+        assert _rel_l2(got, orc) <= 1e-5, f"call {call}: against the oracle's decode"
         assert int(status.cpu().item()) & 0xFFFFFFFF == 0, f"call {call}: device status"
 
 
