@@ -14,9 +14,13 @@
  *   - Q_Naive is the asymmetric uniform quantizer of §3.3 on the activation codec's tiles
  *     (G consecutive channels of one token), at one width b for every tile, 1 <= b <= 16
  *     (6-10 in the pages), with no bit allocation and no outlier transform.  Per tile:
- *     mn = min, mx = max, D = RN(mx - mn); D < 2^-120 gives scale 0 and codes 0; else
- *     scale = RN(D / Q), inv = RN(Q / D), Q = 2^b - 1, and q_k = RNE(RN(v_k - mn) * inv)
- *     (the product exact), clamped to [0, Q].  Decode: fmaf(q_k, scale, mn).
+ *     mn = min, mx = max, D = RN(mx - mn); a range below the cutoff
+ *     D_min(b) = max(2^-120, 2^(b - 126)) gives scale 0 and codes 0 (the tile decodes to
+ *     its minimum); else scale = RN(D / Q), inv = RN(Q / D), Q = 2^b - 1, and
+ *     q_k = RNE(RN(v_k - mn) * inv) (the product exact), clamped to [0, Q].  The cutoff
+ *     keeps inv finite and the scale a normal number at every width up to 16 (at 2^-120
+ *     alone, widths above 6 could give a subnormal scale or an infinite inv).  Decode:
+ *     fmaf(q_k, scale, mn).
  *   - Codes packed least significant bit first at b bits, tile after tile (G * b / 8
  *     bytes a tile); an fp32 scale and zero per tile.
  *   - Gradient scaling: the quantizer sees v = RN(c g) and the decoder returns
@@ -56,8 +60,9 @@ static void naive_quantize_tile(const float *v, int G, int b, uint16_t *q, float
     }
     const int Q = (1 << b) - 1;
     const float D = mx - mn;
+    const float cutoff = ldexpf(1.0f, b - 126 > -120 ? b - 126 : -120);
     *zero = mn + 0.0f;
-    if (!(D >= 0x1p-120f)) {
+    if (!(D >= cutoff)) {
         *scale = 0.0f;
         for (int k = 0; k < G; k++) { q[k] = 0; if (near) near[k] = 0; }
         return;

@@ -122,3 +122,26 @@ def test_matches_activation_codec_at_one_width(b):
 def test_rejects_invalid_arguments(G, b, c):
     with pytest.raises(ValueError):
         oracle.naive_encode(np.zeros((2, 384), np.float32), G, b, c)
+
+
+@pytest.mark.parametrize("b", [10, 16])
+def test_cutoff_keeps_inverse_finite_and_scale_normal(b):
+    # the range cutoff D_min(b) = 2^(b - 126) at widths above 6: a tile {0, D} just below
+    # it quantises to its minimum (scale 0, codes 0, decodes to 0); just above it the scale
+    # D / Q is a normal float, Q / D finite, and the error stays within half a step
+    cut = np.float32(2.0 ** (b - 126))
+    for D, live in ((np.nextafter(cut, np.float32(0)), False), (cut, True),
+                    (np.float32(cut * np.float32(1.5)), True)):
+        g = np.zeros((1, 32), np.float32)
+        g[0, 1::2] = D
+        codes, scales, zeros = oracle.naive_encode(g, 32, b)
+        y = oracle.naive_decode(codes, scales, zeros, 1, 32, 32, b)
+        if not live:
+            assert scales[0] == 0 and not codes.any() and not y.any()
+        else:
+            Q = (1 << b) - 1
+            assert scales[0] >= np.float32(2.0 ** -126)  # normal
+            assert np.isfinite(np.float32(Q) / D)
+            step = float(scales[0])
+            assert np.abs(y.astype(np.float64) - g).max() <= 0.5 * step * (1 + 1e-3)
+            assert y[0, 1] == D and y[0, 0] == 0  # the extremes are exact
