@@ -435,3 +435,40 @@ def naive_decode(codes, scales, zeros, T: int, Cc: int, G: int, b: int,
                                  float(c), _ptr(out)) != 0:
         raise ValueError("invalid codec arguments")
     return out
+
+
+# ------------------------------------------------------------------ TAH-Quant on gradients
+
+def _power_of_two(c: float) -> bool:
+    m, _ = np.frexp(np.float32(c))
+    return bool(np.isfinite(c) and c > 0 and m == 0.5)
+
+
+def scale_input(x: np.ndarray, c: float) -> np.ndarray:
+    """RN(c x) for a power of two c (exact unless c x leaves the normal range), in x's own
+    type: float32, or uint16 bf16 bit patterns (bf16 x 2^k is again a bf16 value)."""
+    if not _power_of_two(c):
+        raise ValueError("the gradient scale must be a positive finite power of two")
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        f = (x.astype(np.uint32) << np.uint32(16)).view(np.float32) * np.float32(c)
+        b = f.view(np.uint32)
+        return ((b + ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)) >> np.uint32(16)).astype(np.uint16)
+    return _f32(x) * np.float32(c)
+
+
+def encode_scaled(x: np.ndarray, G: int, h: int, lo: int, hi: int, budget: float, S: int = 0,
+                  c: float = 1.0, tau: float | None = None, threads: int = 1,
+                  want_keys: bool = False) -> dict:
+    """TAH-Quant applied to a gradient with the scaling of Appendix H eq. (24): the
+    activation codec on RN(c g), c a power of two (scales and zeros describe c g)."""
+    return encode(scale_input(x, c), G, h, lo, hi, budget, S, threads=threads, tau=tau,
+                  want_keys=want_keys)
+
+
+def decode_scaled(codes, scales, zeros, bits, pivots, T: int, Cc: int, G: int, h: int,
+                  c: float = 1.0, threads: int = 1) -> np.ndarray:
+    """The gradient back: RN(decode / c), float32 [T, C] (eq. (24): Q(c g) / c)."""
+    if not _power_of_two(c):
+        raise ValueError("the gradient scale must be a positive finite power of two")
+    return decode(codes, scales, zeros, bits, pivots, T, Cc, G, h, threads=threads) / np.float32(c)
