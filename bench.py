@@ -366,6 +366,88 @@ def run_per_config(tq, dev, steps: int, warmup: int, flush, peak: float) -> dict
     return res
 
 
+# ------------------------------------------------------------------ the backward pass
+
+def run_grad(args):
+    """The backward pass's gradient codecs on a gradient-shaped tensor (16 x 2048 x 8192
+    fp32 by default): the fixed-point codec (tahq_naive_encode / _decode, 8 bits, tile 64,
+    c = 2^16) and TAH-Quant on gradients with eq. (24)'s scaling (tahq_encode_scaled /
+    _decode_scaled, widths {3, 4} at 4 bits, Appendix H Table 10).  Outputs and workspaces
+    are allocated once; each call is timed alone with CUDA events, L2 flushed before it."""
+    import torch
+    import pipeline_activation_quantization_gb300 as tq
+    w = synth.WORKLOADS[args.grad_workload]
+    T, C, G = w.tokens, w.channels, w.tile
+    b, c = args.grad_bits, 2.0 ** 16
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x = torch.from_numpy(synth.generate(w)).to(dev)
+    n = T * (C // G)
+    nb = tq.tahq_naive_codes_bytes(T, C, G, b)
+    codes = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    scales = torch.empty(n, dtype=torch.float32, device=dev)
+    zeros = torch.empty(n, dtype=torch.float32, device=dev)
+    y = torch.empty((T, C), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    enc_s = tq.encode_scaled(x, G, G, 3, 4, 4.0, w.tokens_per_group, scale_c=c, stream=st)
+    outs = {k: enc_s[k] for k in ("codes", "scales", "zeros", "bits", "pivots")}
+    dws = torch.empty(tq.tahq_decode_workspace_size(T, C, G), dtype=torch.uint8, device=dev)
+    calls = {
+        "naive_encode": lambda: tq.tahq_naive_encode(x, T, C, G, b, c, codes, scales, zeros, st),
+        "naive_decode": lambda: tq.tahq_naive_decode(codes, scales, zeros, T, C, G, b, c, y, st),
+        "tahq_encode_scaled": lambda: tq.encode_scaled(x, G, G, 3, 4, 4.0, w.tokens_per_group,
+                                                       scale_c=c, out=outs,
+                                                       workspace=enc_s["workspace"], stream=st),
+        "tahq_decode_scaled": lambda: tq.decode_scaled(enc_s, T, C, G, G, scale_c=c, out=y,
+                                                       workspace=dws, stream=st),
+    }
+    pay4 = enc_s["payload_bytes"]
+    alg = {"naive_encode": 4 * T * C + nb + 8 * n, "naive_decode": nb + 8 * n + 4 * T * C,
+           "tahq_encode_scaled": 4 * T * C + pay4 + 10 * n,
+           "tahq_decode_scaled": pay4 + 10 * n + 4 * T * C}
+    peak, peak_kind = _peaks()
+    res = {}
+    with torch.cuda.stream(st):
+        for name, fn in calls.items():
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                  for _ in range(args.steps + args.warmup)]
+            for k, e in enumerate(ev):
+                flush.fill_(k & 255)
+                e[0].record(st)
+                rc = fn()
+                if isinstance(rc, int) and rc != 0:
+                    raise RuntimeError(f"{name}: {tq.tahq_status_string(rc)}")
+                e[1].record(st)
+            st.synchronize()
+            ms = [e[0].elapsed_time(e[1]) for e in ev[args.warmup:]]
+            med = statistics.median(ms)
+            gbs = alg[name] / (med * 1e-3) / 1e9
+            res[name] = {"ms_median": round(med, 5), "ms_mean": round(statistics.mean(ms), 5),
+                         "alg_bytes": alg[name], "GB_s": round(gbs, 2),
+                         "frac": round(gbs / peak, 4),
+                         "tokens_per_s": round(T / (med * 1e-3), 1)}
+    rt = res["naive_encode"]["ms_median"] + res["naive_decode"]["ms_median"]
+    dom = max(("naive_encode", "naive_decode"), key=lambda k: res[k]["ms_median"])
+    kern = {"naive_encode": f"k_naive_encode<{G}>", "naive_decode": f"k_naive_decode<{G}>"}[dom]
+    line = {
+        "metric": "gradient codec GB/s of gradients (fixed-point, 8 bits) and % of GB300 HBM "
+                  "roofline", "value": round(4 * T * C / (rt * 1e-3) / 1e9, 3), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(rt, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens": T, "channels": C, "tile": G, "bits": b,
+                   "scale_c": c, "l2": "flushed before each call (256 MiB write, outside the events)"},
+        "calls": res,
+        "roofline": {"bound": "hbm", "kernel": kern, "achieved": res[dom]["GB_s"], "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
+                     "frac": res[dom]["frac"], "traffic": None},
+        "gpu_launches_per_step": 2,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ the CUDA path
 
 def run_gpu(args):
@@ -620,6 +702,10 @@ def parse_args(argv=None):
                     help="time the wire format (tahq_encode_wire / tahq_decode_wire)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grad", action="store_true",
+                    help="time the backward pass's gradient codecs instead (one JSON line)")
+    ap.add_argument("--grad-workload", default="g5", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--grad-bits", type=int, default=8)
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the 2048/4096-channel configs (timed after the headline one)")
     args = ap.parse_args(argv)
@@ -632,6 +718,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.grad:
+        return run_grad(args)
     return run_gpu(args)
 
 

@@ -283,6 +283,35 @@ tahq_status tahq_naive_decode(const uint8_t *codes, const float *scales, const f
 tahq_status tahq_get_device_status(const void *workspace, uint32_t *status_out, void *stream);
 
 /*
+ * TAH-Quant on a gradient with the scaling of eq. (24) (TAH-Quant Appendix H, Table 10:
+ * the activation codec applied to backward gradients; eq. (24): g_hat = Q(c g) / c).
+ *
+ * tahq_encode_scaled: the codec of tahq_encode_ex (tau as there, allocation tile = tile)
+ * applied to RN(scale_c * x), with scale_c a positive finite power of two (so the scaling
+ * is exact unless scale_c * x leaves the normal float range; bf16 inputs stay bf16).  The
+ * outputs describe scale_c * x: scales and zeros are those of the scaled values.  The
+ * scaled copy of x is written into the workspace after the codec's own part, so the
+ * workspace must hold tahq_scaled_workspace_size() bytes (0 on invalid arguments).
+ * tahq_decode_scaled: tahq_decode followed by out = RN(out / scale_c) (the same workspace
+ * as tahq_decode).  Errors as for tahq_encode / tahq_decode; a scale_c that is not a
+ * positive finite power of two gives TAHQ_ERR_ARG.
+ */
+size_t tahq_scaled_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock,
+                                  int bits_lo, int bits_hi, float budget,
+                                  int64_t tokens_per_group, tahq_dtype dtype);
+tahq_status tahq_encode_scaled(const void *x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                               int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                               int64_t tokens_per_group, float tau, float scale_c,
+                               uint8_t *codes, float *scales, float *zeros, uint8_t *bits,
+                               uint8_t *pivots, void *workspace, size_t workspace_bytes,
+                               void *stream);
+tahq_status tahq_decode_scaled(const uint8_t *codes, size_t codes_bytes, const float *scales,
+                               const float *zeros, const uint8_t *bits, const uint8_t *pivots,
+                               int64_t tokens, int64_t channels, int tile, int hblock,
+                               float scale_c, float *out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
  * Exercises the bounded wait that every cross-block wait of the kernels uses (the pages
  * have no counterpart: this is the codec's own failure detection).  One thread waits in
  * turn on eight counters in `workspace` that nothing advances, each wait limited to

@@ -24,7 +24,8 @@ __all__ = [
     "tahq_wire_decode_workspace_size", "tahq_encode_wire", "tahq_decode_wire", "encode", "decode",
     "encode_wire", "decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
     "tahq_naive_decode", "naive_encode", "naive_decode", "tahq_test_wait_timeout",
-    "EXPORTED_SYMBOLS",
+    "tahq_scaled_workspace_size", "tahq_encode_scaled", "tahq_decode_scaled", "encode_scaled",
+    "decode_scaled", "EXPORTED_SYMBOLS",
 ]
 
 TAHQ_F32, TAHQ_BF16 = 0, 1
@@ -40,7 +41,8 @@ EXPORTED_SYMBOLS = (
     "tahq_status_string", "tahq_version", "tahq_log2_tables", "tahq_decode_noalloc",
     "tahq_wire_size", "tahq_wire_workspace_size", "tahq_wire_decode_workspace_size",
     "tahq_encode_wire", "tahq_decode_wire", "tahq_naive_codes_bytes", "tahq_naive_encode",
-    "tahq_naive_decode", "tahq_test_wait_timeout",
+    "tahq_naive_decode", "tahq_test_wait_timeout", "tahq_scaled_workspace_size",
+    "tahq_encode_scaled", "tahq_decode_scaled",
 )
 
 
@@ -89,6 +91,10 @@ def lib(path: str | None = None):
         "tahq_naive_encode": (i32, [p, i64, i64, i32, i32, f32, p, p, p, p]),
         "tahq_naive_decode": (i32, [p, p, p, i64, i64, i32, i32, f32, p, p]),
         "tahq_test_wait_timeout": (i32, [p, sz, C.c_uint64, p, p]),
+        "tahq_scaled_workspace_size": (sz, [i64, i64, i32, i32, i32, i32, f32, i64, i32]),
+        "tahq_encode_scaled": (i32, [p, i32, i64, i64, i32, i32, i32, i32, f32, i64, f32, f32,
+                                     p, p, p, p, p, p, sz, p]),
+        "tahq_decode_scaled": (i32, [p, sz, p, p, p, p, i64, i64, i32, i32, f32, p, p, sz, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -415,10 +421,110 @@ def naive_encode(grad, tile: int = 64, bits: int = 8, scale_c: float = 1.0, stre
 
 def naive_decode(codes, scales, zeros, tokens: int, channels: int, tile: int = 64, bits: int = 8,
                  scale_c: float = 1.0, out=None, stream=None):
-    """The float32 CUDA tensor [tokens, channels] back from naive_encode's outputs."""
+    """The float32 CUDA tensor [tokens, channels] back from naive_encode's outputs.  The
+    buffers are checked against the shape first (the C entry point trusts them)."""
     import torch
+    nb = tahq_naive_codes_bytes(tokens, channels, tile, bits)
+    n = tokens * (channels // tile) if tile > 0 else 0
+    if nb == 0 and tokens > 0:
+        raise TahqError(1, "tahq_naive_codes_bytes")
+    if codes.numel() < nb or scales.numel() != n or zeros.numel() != n:
+        raise ValueError("naive_decode: codes, scales or zeros do not match the shape")
+    if scales.dtype != torch.float32 or zeros.dtype != torch.float32:
+        raise ValueError("naive_decode: scales and zeros must be float32")
     if out is None:
         out = torch.empty((tokens, channels), dtype=torch.float32, device=codes.device)
+    elif (out.dtype != torch.float32 or not out.is_contiguous()
+          or tuple(out.shape) != (tokens, channels)):
+        raise ValueError("naive_decode: out must be a contiguous float32 [tokens, channels] tensor")
     rc = tahq_naive_decode(codes, scales, zeros, tokens, channels, tile, bits, scale_c, out, stream)
     _check(rc, "tahq_naive_decode")
+    return out
+
+
+# ------------------------------------------------------------------ gradients (eq. (24))
+
+def tahq_scaled_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                               tokens_per_group, dtype) -> int:
+    return lib().tahq_scaled_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi,
+                                            budget, tokens_per_group, dtype)
+
+
+def tahq_encode_scaled(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                       tokens_per_group, tau, scale_c, codes, scales, zeros, bits, pivots,
+                       workspace, workspace_bytes, stream=None) -> int:
+    return lib().tahq_encode_scaled(_ptr(x), dtype, tokens, channels, tile, hblock, bits_lo,
+                                    bits_hi, budget, tokens_per_group, tau, scale_c, _ptr(codes),
+                                    _ptr(scales), _ptr(zeros), _ptr(bits), _ptr(pivots),
+                                    _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def tahq_decode_scaled(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile,
+                       hblock, scale_c, out, workspace, workspace_bytes, stream=None) -> int:
+    return lib().tahq_decode_scaled(_ptr(codes), codes_bytes, _ptr(scales), _ptr(zeros),
+                                    _ptr(bits), _ptr(pivots), tokens, channels, tile, hblock,
+                                    scale_c, _ptr(out), _ptr(workspace), workspace_bytes,
+                                    _stream(stream))
+
+
+def encode_scaled(x, tile: int = 64, hblock: int | None = None, bits_lo: int = 3,
+                  bits_hi: int = 4, budget: float = 3.5, tokens_per_group: int = 0,
+                  tau: float = 2.0, scale_c: float = 1.0, out: dict | None = None,
+                  workspace=None, stream=None) -> dict:
+    """TAH-Quant on a gradient (float32 or bfloat16 CUDA tensor) with eq. (24)'s scaling by
+    the power of two ``scale_c``; returns the dict of ``encode`` (metadata of the scaled
+    values)."""
+    import torch
+    if not x.is_cuda:
+        raise ValueError("tahq.encode_scaled needs a CUDA tensor")
+    dt = {torch.float32: TAHQ_F32, torch.bfloat16: TAHQ_BF16}.get(x.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    x = x.contiguous()
+    T, Cc = x.shape
+    h = hblock or tile
+    n = T * (Cc // tile)
+    pay = tahq_payload_size(T, Cc, tile, bits_lo, bits_hi, budget, tokens_per_group)
+    ws = tahq_scaled_workspace_size(T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group, dt)
+    if ws == 0:
+        raise TahqError(1, "tahq_scaled_workspace_size")
+    dev = x.device
+    if out is None:
+        out = {"codes": torch.empty(max(pay, 16), dtype=torch.uint8, device=dev),
+               "scales": torch.empty(n, dtype=torch.float32, device=dev),
+               "zeros": torch.empty(n, dtype=torch.float32, device=dev),
+               "bits": torch.empty(n, dtype=torch.uint8, device=dev),
+               "pivots": torch.empty(n, dtype=torch.uint8, device=dev)}
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    rc = tahq_encode_scaled(x, dt, T, Cc, tile, h, bits_lo, bits_hi, budget, tokens_per_group,
+                            float(tau), float(scale_c), out["codes"], out["scales"], out["zeros"],
+                            out["bits"], out["pivots"], workspace, workspace.numel(), stream)
+    _check(rc, "tahq_encode_scaled")
+    res = dict(out)
+    res["codes"] = out["codes"][:pay]
+    res["workspace"] = workspace
+    res["payload_bytes"] = pay
+    return res
+
+
+def decode_scaled(enc: dict, tokens: int, channels: int, tile: int = 64,
+                  hblock: int | None = None, scale_c: float = 1.0, out=None, workspace=None,
+                  stream=None):
+    """The gradient back from ``encode_scaled``'s dict: RN(decode / scale_c), float32."""
+    import torch
+    dev = enc["scales"].device
+    h = hblock or tile
+    ws = tahq_decode_workspace_size(tokens, channels, tile)
+    if ws == 0:
+        raise TahqError(1, "tahq_decode_workspace_size")
+    if out is None:
+        out = torch.empty((tokens, channels), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    codes = enc["codes"]
+    rc = tahq_decode_scaled(codes, codes.numel(), enc["scales"], enc["zeros"], enc["bits"],
+                            enc["pivots"], tokens, channels, tile, h, float(scale_c), out,
+                            workspace, workspace.numel(), stream)
+    _check(rc, "tahq_decode_scaled")
     return out

@@ -11,7 +11,7 @@ namespace {
 
 using tahq::LgTables;
 
-constexpr int kVersion = 20100;  // 2.1.0: tau, allocation tiles, wire format, gradient codec
+constexpr int kVersion = 20200;  // 2.2.0: streaming encoder, scaled gradients, wait test
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -380,6 +380,122 @@ tahq_status tahq_decode(const uint8_t* codes, size_t codes_bytes, const float* s
                         void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile,
                      hblock, out, workspace, workspace_bytes, stream, true);
+}
+
+// ------------------------------------------------------------------------ gradients
+
+}  // extern "C"
+
+namespace {
+
+bool power_of_two(float c) {
+  int e = 0;
+  return c > 0.0f && std::isfinite(c) && std::frexp(c, &e) == 0.5f;
+}
+
+// y = RN(c x) elementwise (c a power of two: exact unless c x leaves the normal range),
+// 16 bytes a thread and step; bf16 values stay bf16 (x 2^k is again a bf16 value).
+template <bool kBf16>
+__global__ void k_scale_input(const uint4* __restrict__ x, uint4* __restrict__ y, long long n16, float c) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    uint4 q = x[i];
+    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      if constexpr (kBf16) {
+        const uint32_t lo = __float_as_uint(__fmul_rn(__uint_as_float(w[k] << 16), c));
+        const uint32_t hi = __float_as_uint(__fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), c));
+        // round to bf16, ties to even (exact here unless the range was left)
+        const uint32_t rl = (lo + ((lo >> 16) & 1u) + 0x7FFFu) >> 16;
+        const uint32_t rh = (hi + ((hi >> 16) & 1u) + 0x7FFFu) >> 16;
+        w[k] = (rl & 0xFFFFu) | (rh << 16);
+      } else {
+        w[k] = __float_as_uint(__fmul_rn(__uint_as_float(w[k]), c));
+      }
+    }
+    y[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// out = RN(out / c) in place (= out x (1 / c), both exact powers of two).
+__global__ void k_unscale(float4* __restrict__ out, long long n4, float inv_c) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 v = out[i];
+    v.x = __fmul_rn(v.x, inv_c);
+    v.y = __fmul_rn(v.y, inv_c);
+    v.z = __fmul_rn(v.z, inv_c);
+    v.w = __fmul_rn(v.w, inv_c);
+    out[i] = v;
+  }
+}
+
+unsigned stream_blocks(long long n) {
+  const int sms = num_sms_current();
+  return (unsigned)std::max<long long>(1, std::min<long long>((n + 255) / 256, (long long)std::max(sms, 1) * 8));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tahq_scaled_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock,
+                                  int bits_lo, int bits_hi, float budget,
+                                  int64_t tokens_per_group, tahq_dtype dtype) {
+  const size_t ws = tahq_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                                        tokens_per_group);
+  if (ws == 0 || (dtype != TAHQ_F32 && dtype != TAHQ_BF16)) return 0;
+  return ws + align_up((size_t)(tokens * channels) * (dtype == TAHQ_BF16 ? 2 : 4));
+}
+
+tahq_status tahq_encode_scaled(const void* x, tahq_dtype dtype, int64_t tokens, int64_t channels,
+                               int tile, int hblock, int bits_lo, int bits_hi, float budget,
+                               int64_t tokens_per_group, float tau, float scale_c,
+                               uint8_t* codes, float* scales, float* zeros, uint8_t* bits,
+                               uint8_t* pivots, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!power_of_two(scale_c)) return TAHQ_ERR_ARG;
+  const size_t ws = tahq_workspace_size(tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                                        tokens_per_group);
+  if (ws == 0 || (dtype != TAHQ_F32 && dtype != TAHQ_BF16)) return TAHQ_ERR_ARG;
+  const size_t esz = dtype == TAHQ_BF16 ? 2 : 4;
+  const size_t nbytes = (size_t)(tokens * channels) * esz;
+  if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
+  if (workspace_bytes < ws + align_up(nbytes)) return TAHQ_ERR_WORKSPACE;
+  if (nbytes && (!x || !aligned(x, 16))) return TAHQ_ERR_ARG;
+  void* xs = static_cast<unsigned char*>(workspace) + ws;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (nbytes) {  // channels are a multiple of 8, so the tensor is whole 16-byte units
+    const long long n16 = (long long)(nbytes / 16);
+    if (dtype == TAHQ_BF16)
+      k_scale_input<true><<<stream_blocks(n16), 256, 0, cs>>>(static_cast<const uint4*>(x),
+                                                              static_cast<uint4*>(xs), n16, scale_c);
+    else
+      k_scale_input<false><<<stream_blocks(n16), 256, 0, cs>>>(static_cast<const uint4*>(x),
+                                                               static_cast<uint4*>(xs), n16, scale_c);
+    if (cudaGetLastError() != cudaSuccess) return TAHQ_ERR_CUDA;
+  }
+  return encode_impl(xs, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi, budget,
+                     tokens_per_group, tau, 0, false, codes, scales, zeros, bits, pivots,
+                     workspace, ws, stream);
+}
+
+tahq_status tahq_decode_scaled(const uint8_t* codes, size_t codes_bytes, const float* scales,
+                               const float* zeros, const uint8_t* bits, const uint8_t* pivots,
+                               int64_t tokens, int64_t channels, int tile, int hblock,
+                               float scale_c, float* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!power_of_two(scale_c)) return TAHQ_ERR_ARG;
+  const tahq_status st = decode_impl(codes, codes_bytes, scales, zeros, bits, pivots, tokens,
+                                     channels, tile, hblock, out, workspace, workspace_bytes,
+                                     stream, true);
+  if (st != TAHQ_OK) return st;
+  const long long n4 = tokens * channels / 4;
+  if (n4 == 0) return TAHQ_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  k_unscale<<<stream_blocks(n4), 256, 0, cs>>>(reinterpret_cast<float4*>(out), n4, 1.0f / scale_c);
+  return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------------ wire format

@@ -7,15 +7,16 @@
 // the §3.3 asymmetric uniform one at a single width b (1..16) on tiles of G consecutive
 // channels of a token, with no bit allocation and no outlier transform: per tile
 // mn = min, mx = max, D = RN(mx - mn), inv = RN(Q / D), scale = RN(D / Q) (both 0 when
-// D < 2^-120), q = RNE(RN(v - mn) * inv) with the product exact, v = RN(c g); codes
+// D < max(2^-120, 2^(b - 126))), q = RNE(RN(v - mn) * inv) with the product exact,
+// v = RN(c g); codes
 // packed least significant bit first at b bits; decode RN(fma(q, scale, mn) / c).  c is a
 // power of two, so the scaling is exact unless c g leaves the normal float range.
 //
-// One warp a tile (G = 32, 64 or 128: V = G / 32 values a lane, positions lane * V ...).
-// Encode stages the tile's codes in shared memory and writes each 32-bit word of the
-// slot from the codes it covers; decode extracts each code from the one or two words it
-// spans.  Both are streams bound by HBM (4 bytes read and b / 8 written an element, or
-// the reverse).
+// A warp takes four consecutive tiles at a time (G = 32, 64 or 128: V = G / 32 values a
+// lane, positions lane * V ...), every load of the four in flight first.  Encode stages a
+// tile's codes in shared memory and writes each 32-bit word of the slot from the codes it
+// covers; decode extracts each code from the one or two words it spans.  Both are streams
+// bound by HBM (4 bytes read and b / 8 written an element, or the reverse).
 #include <algorithm>
 #include <cmath>
 
@@ -26,63 +27,101 @@ namespace tahq {
 namespace {
 
 constexpr int kNaiveWarps = 8;
+constexpr int kNaiveTiles = 4;  // tiles a warp has in flight
 
+// The range below which a tile quantises to its minimum: max(2^-120, 2^(b - 126)), so that
+// Q / D stays finite and D / Q a normal float at every width up to 16.
+__device__ __forceinline__ float naive_cutoff(int b) {
+  return __uint_as_float((uint32_t)(127 + max(-120, b - 126)) << 23);
+}
+
+__device__ __forceinline__ float warp_min(float x) {
+  float r;
+  asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+template <int V>
+__device__ __forceinline__ void load_v(const float* src, float* v) {
+  if constexpr (V == 4) {
+    const float4 q = __ldcs(reinterpret_cast<const float4*>(src));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  } else if constexpr (V == 2) {
+    const float2 q = __ldcs(reinterpret_cast<const float2*>(src));
+    v[0] = q.x; v[1] = q.y;
+  } else {
+    v[0] = __ldcs(src);
+  }
+}
+
+// One warp takes kNaiveTiles consecutive tiles at a time (every load of the group in
+// flight before any arithmetic), lane l holding values l V .. l V + V - 1 of each tile.
+// The codes of a tile are staged in shared memory; lane w then writes word w of the slot
+// (bits [32 w, 32 w + 32)) from the codes it covers.
 template <int G>
 __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_encode(const float* __restrict__ g,
                                                                    long long n_tiles, int b,
                                                                    float c, uint8_t* codes,
                                                                    float* scales, float* zeros) {
   constexpr int V = G / 32;
-  __shared__ uint16_t sq[kNaiveWarps][G];
+  __shared__ uint16_t sq[kNaiveWarps][kNaiveTiles][G];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t Q = (1u << b) - 1u;
+  const float Qf = (float)Q, cut = naive_cutoff(b);
   const int words = G * b / 32;  // the tile's slot, whole 32-bit words (G >= 32)
-  const long long stride = (long long)gridDim.x * kNaiveWarps;
-  for (long long t = (long long)blockIdx.x * kNaiveWarps + warp; t < n_tiles; t += stride) {
-    float v[V];
-    const float* src = g + t * G + lane * V;
-    if constexpr (V == 4) {
-      const float4 q = *reinterpret_cast<const float4*>(src);
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else if constexpr (V == 2) {
-      const float2 q = *reinterpret_cast<const float2*>(src);
-      v[0] = q.x; v[1] = q.y;
-    } else {
-      v[0] = *src;
-    }
-    float mn, mx;
+  const long long stride = (long long)gridDim.x * kNaiveWarps * kNaiveTiles;
+  for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kNaiveTiles; t0 < n_tiles;
+       t0 += stride) {
+    const int nu = (int)min((long long)kNaiveTiles, n_tiles - t0);
+    float v[kNaiveTiles][V];
 #pragma unroll
-    for (int j = 0; j < V; j++) {
-      v[j] = __fmul_rn(c, v[j]);
-      mn = j ? fminf(mn, v[j]) : v[j];
-      mx = j ? fmaxf(mx, v[j]) : v[j];
-    }
-    mn = team_min<32>(mn);
-    mx = team_max<32>(mx);
-    const float D = __fsub_rn(mx, mn);
-    const bool live = D >= 0x1p-120f;
-    const float inv = live ? __fdiv_rn((float)Q, D) : 0.0f;
+    for (int u = 0; u < kNaiveTiles; u++)
+      if (u < nu) load_v<V>(g + (t0 + u) * G + lane * V, v[u]);
 #pragma unroll
-    for (int j = 0; j < V; j++) {
-      uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[j], mn), inv, 12582912.0f)) - 0x4B400000u;
-      sq[warp][lane * V + j] = (uint16_t)(live ? min(q, Q) : 0u);
-    }
-    if (lane == 0) {
-      scales[t] = live ? __fdiv_rn(D, (float)Q) : 0.0f;
-      zeros[t] = __fadd_rn(mn, 0.0f);  // a zero minimum as +0
+    for (int u = 0; u < kNaiveTiles; u++) {
+      if (u >= nu) break;  // warp-uniform
+      float mn, mx;
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        v[u][j] = __fmul_rn(c, v[u][j]);
+        mn = j ? fminf(mn, v[u][j]) : v[u][j];
+        mx = j ? fmaxf(mx, v[u][j]) : v[u][j];
+      }
+      mn = warp_min(mn);
+      mx = warp_max(mx);
+      const float D = __fsub_rn(mx, mn);
+      const bool live = D >= cut;
+      const float inv = live ? __fdiv_rn(Qf, D) : 0.0f;
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        const uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[u][j], mn), inv, 12582912.0f)) - 0x4B400000u;
+        sq[warp][u][lane * V + j] = (uint16_t)(live ? min(q, Q) : 0u);
+      }
+      if (lane == 0) {
+        scales[t0 + u] = live ? __fdiv_rn(D, Qf) : 0.0f;
+        zeros[t0 + u] = __fadd_rn(mn, 0.0f);  // a zero minimum as +0
+      }
     }
     __syncwarp();
-    // word w of the slot holds bits [32 w, 32 w + 32): the codes from floor(32 w / b) on
-    uint32_t* dst = reinterpret_cast<uint32_t*>(codes + t * (long long)(G * b / 8));
-    for (int w = lane; w < words; w += 32) {
-      int k = (32 * w) / b;
-      int off = k * b - 32 * w;  // where code k starts, relative to the word (<= 0)
-      uint32_t acc = 0u;
-      for (; off < 32; ++k, off += b) {
-        const uint32_t q = sq[warp][k];
-        acc |= off >= 0 ? (q << off) : (q >> (-off));
+#pragma unroll
+    for (int u = 0; u < kNaiveTiles; u++) {
+      if (u >= nu) break;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(codes + (t0 + u) * (long long)(G * b / 8));
+      for (int w = lane; w < words; w += 32) {
+        int k = (32 * w) / b;
+        int off = k * b - 32 * w;  // where code k starts, relative to the word (<= 0)
+        uint32_t acc = 0u;
+        for (; off < 32; ++k, off += b) {
+          const uint32_t q = sq[warp][u][k];
+          acc |= off >= 0 ? (q << off) : (q >> (-off));
+        }
+        dst[w] = acc;
       }
-      dst[w] = acc;
     }
     __syncwarp();
   }
@@ -97,25 +136,41 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_decode(const uint8_t
   constexpr int V = G / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t mask = (1u << b) - 1u;
-  const long long stride = (long long)gridDim.x * kNaiveWarps;
-  for (long long t = (long long)blockIdx.x * kNaiveWarps + warp; t < n_tiles; t += stride) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + t * (long long)(G * b / 8));
-    const float sc = scales[t], z = zeros[t];
-    float y[V];
+  const float inv_c = 1.0f / c;  // c is a power of two: RN(y / c) = y * (1 / c)
+  const long long stride = (long long)gridDim.x * kNaiveWarps * kNaiveTiles;
+  for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kNaiveTiles; t0 < n_tiles;
+       t0 += stride) {
+    const int nu = (int)min((long long)kNaiveTiles, n_tiles - t0);
+    uint32_t qv[kNaiveTiles][V];
+    float sc[kNaiveTiles], z[kNaiveTiles];
 #pragma unroll
-    for (int j = 0; j < V; j++) {
-      const int bit = (lane * V + j) * b, w = bit >> 5, sh = bit & 31;
-      uint32_t q = __ldg(src + w) >> sh;
-      if (sh + b > 32) q |= __ldg(src + w + 1) << (32 - sh);
-      y[j] = __fdiv_rn(__fmaf_rn((float)(q & mask), sc, z), c);
+    for (int u = 0; u < kNaiveTiles; u++) {
+      if (u >= nu) break;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + (t0 + u) * (long long)(G * b / 8));
+      sc[u] = __ldg(scales + t0 + u);
+      z[u] = __ldg(zeros + t0 + u);
+#pragma unroll
+      for (int j = 0; j < V; j++) {
+        const int bit = (lane * V + j) * b, w = bit >> 5, sh = bit & 31;
+        uint32_t q = __ldg(src + w) >> sh;
+        if (sh + b > 32) q |= __ldg(src + w + 1) << (32 - sh);
+        qv[u][j] = q & mask;
+      }
     }
-    float* dst = out + t * G + lane * V;
-    if constexpr (V == 4) {
-      *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
-    } else if constexpr (V == 2) {
-      *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1]);
-    } else {
-      *dst = y[0];
+#pragma unroll
+    for (int u = 0; u < kNaiveTiles; u++) {
+      if (u >= nu) break;
+      float y[V];
+#pragma unroll
+      for (int j = 0; j < V; j++) y[j] = __fmul_rn(__fmaf_rn((float)qv[u][j], sc[u], z[u]), inv_c);
+      float* dst = out + (t0 + u) * G + lane * V;
+      if constexpr (V == 4) {
+        __stcs(reinterpret_cast<float4*>(dst), make_float4(y[0], y[1], y[2], y[3]));
+      } else if constexpr (V == 2) {
+        __stcs(reinterpret_cast<float2*>(dst), make_float2(y[0], y[1]));
+      } else {
+        __stcs(dst, y[0]);
+      }
     }
   }
 }
@@ -125,7 +180,8 @@ int naive_blocks(long long n_tiles) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return 0;
-  const long long want = (n_tiles + kNaiveWarps - 1) / kNaiveWarps;
+  const long long per = kNaiveWarps * kNaiveTiles;
+  const long long want = (n_tiles + per - 1) / per;
   return (int)std::max<long long>(1, std::min<long long>(want, (long long)sms * 8));
 }
 

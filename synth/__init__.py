@@ -71,6 +71,10 @@ WORKLOADS = {
     "c4": Workload("c4_8x2048x4096_bf16", 16384, 4096, "bf16", 64, 64, 3, 4, 3.5, 2048, 3, "gauss_rms_spikes"),
     # 16 x 2048 x 8192 fp32, Laplace(0,1), 0.1% channels x50; G=h=128, 3.5 bits, seed 4.
     "c5": Workload("c5_16x2048x8192_f32", 32768, 8192, "f32", 128, 128, 3, 4, 3.5, 2048, 4, "laplace"),
+    # Backward gradients at the 70B-width boundary: 16 x 2048 x 8192 fp32, N(0,1) times a
+    # per-token RMS LogNormal(0, 0.5) times 1e-5, 0.1% channels x30; the gradient codecs
+    # (tile 64, 8 bits for the fixed-point one, 4 bits for TAH-Quant on gradients).
+    "g5": Workload("g5_16x2048x8192_f32", 32768, 8192, "f32", 64, 64, 3, 4, 4.0, 2048, 5, "gradient"),
 }
 
 C4_SWEEP = [(g, b) for g in (32, 64, 128) for b in (3.0, 3.5, 4.0)]
@@ -131,6 +135,14 @@ def _values(w: Workload, rng: np.random.Generator, blocks, threads: int) -> np.n
         pos = rng.choice(T * C, m, replace=False)
         sign = rng.integers(0, 2, m).astype(np.float32) * 2.0 - 1.0
         x.reshape(-1)[pos] = np.float32(500.0) * sign
+        return x
+    if w.dist == "gradient":
+        x = _draw_rows(blocks, T, C, lambda g, s: g.standard_normal(s, dtype=np.float32), threads)
+        rms = rng.lognormal(0.0, 0.5, T).astype(np.float32)
+        x *= (rms * np.float32(1e-5))[:, None]
+        k = round(0.001 * C)
+        chans = rng.choice(C, k, replace=False)
+        x[:, chans] *= np.float32(30.0)
         return x
     if w.dist == "laplace":
         x = _draw_rows(blocks, T, C, lambda g, s: g.laplace(0.0, 1.0, s), threads)

@@ -82,3 +82,38 @@ def test_naive_empty_and_rejects():
         tq.naive_encode(torch.zeros((4, 128), device="cuda"), 64, 8, 3.0)
     with pytest.raises(tq.TahqError):
         tq.naive_encode(torch.zeros((4, 128), device="cuda"), 16, 8)
+
+
+@pytest.mark.parametrize("b", [10, 16])
+@pytest.mark.parametrize("G", [32, 128])
+def test_naive_range_cutoff(G, b):
+    # tiles {0, D} with D just below, at and above the width's cutoff 2^(b - 126): below it
+    # the tile quantises to its minimum; at and above it the scale is a normal float
+    import torch
+    cut = np.float32(2.0 ** (b - 126))
+    Ds = [np.nextafter(cut, np.float32(0)), cut, np.float32(cut * np.float32(1.5)),
+          np.float32(cut * np.float32(3.0))]
+    g = np.zeros((len(Ds), G), np.float32)
+    for i, D in enumerate(Ds):
+        g[i, 1::2] = D
+    codes, scales, zeros = tq.naive_encode(torch.from_numpy(g).cuda(), G, b)
+    y = tq.naive_decode(codes, scales, zeros, len(Ds), G, G, b)
+    torch.cuda.synchronize()
+    oc, os_, oz = oracle.naive_encode(g, G, b)
+    assert np.array_equal(scales.cpu().numpy(), os_) and os_[0] == 0 and (os_[1:] > 0).all()
+    assert np.array_equal(zeros.cpu().numpy(), oz)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(y.cpu().numpy(), oracle.naive_decode(oc, os_, oz, len(Ds), G, G, b))
+
+
+def test_naive_decode_checks_its_buffers():
+    import torch
+    g = torch.zeros((4, 128), device="cuda")
+    codes, scales, zeros = tq.naive_encode(g, 64, 8)
+    with pytest.raises(ValueError):
+        tq.naive_decode(codes[:-1], scales, zeros, 4, 128, 64, 8)
+    with pytest.raises(ValueError):
+        tq.naive_decode(codes, scales[:-1], zeros, 4, 128, 64, 8)
+    with pytest.raises(ValueError):
+        tq.naive_decode(codes, scales, zeros, 4, 128, 64, 8,
+                        out=torch.empty((4, 128), dtype=torch.float16, device="cuda"))
