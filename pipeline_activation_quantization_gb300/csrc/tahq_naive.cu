@@ -27,7 +27,7 @@ namespace tahq {
 namespace {
 
 constexpr int kNaiveWarps = 8;
-constexpr int kNaiveTiles = 4;  // tiles a warp has in flight
+constexpr int kNaiveTiles = 8;  // tiles a warp has in flight
 
 // The range below which a tile quantises to its minimum: max(2^-120, 2^(b - 126)), so that
 // Q / D stays finite and D / Q a normal float at every width up to 16.
@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_encode(const float* 
   const uint32_t Q = (1u << b) - 1u;
   const float Qf = (float)Q, cut = naive_cutoff(b);
   const int words = G * b / 32;  // the tile's slot, whole 32-bit words (G >= 32)
+  // a lane's V codes fill 1, 2, 4 or 8 whole bytes: stored straight from registers
+  const int fbytes = V * b / 8;
+  const bool direct = (V * b) % 8 == 0 && (fbytes == 1 || fbytes == 2 || fbytes == 4 || fbytes == 8);
   const long long stride = (long long)gridDim.x * kNaiveWarps * kNaiveTiles;
   for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kNaiveTiles; t0 < n_tiles;
        t0 += stride) {
@@ -97,16 +100,30 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_encode(const float* 
       const float D = __fsub_rn(mx, mn);
       const bool live = D >= cut;
       const float inv = live ? __fdiv_rn(Qf, D) : 0.0f;
+      unsigned long long field = 0ull;
 #pragma unroll
       for (int j = 0; j < V; j++) {
-        const uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[u][j], mn), inv, 12582912.0f)) - 0x4B400000u;
-        sq[warp][u][lane * V + j] = (uint16_t)(live ? min(q, Q) : 0u);
+        uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[u][j], mn), inv, 12582912.0f)) - 0x4B400000u;
+        q = live ? min(q, Q) : 0u;
+        if (direct) {
+          field |= (unsigned long long)q << (j * b);
+        } else {
+          sq[warp][u][lane * V + j] = (uint16_t)q;
+        }
+      }
+      if (direct) {  // the lane's V codes are whole bytes: one store
+        unsigned char* dst = codes + (t0 + u) * (long long)(G * b / 8) + lane * fbytes;
+        if (fbytes == 8) *reinterpret_cast<unsigned long long*>(dst) = field;
+        else if (fbytes == 4) *reinterpret_cast<uint32_t*>(dst) = (uint32_t)field;
+        else if (fbytes == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)field;
+        else *dst = (unsigned char)field;
       }
       if (lane == 0) {
         scales[t0 + u] = live ? __fdiv_rn(D, Qf) : 0.0f;
         zeros[t0 + u] = __fadd_rn(mn, 0.0f);  // a zero minimum as +0
       }
     }
+    if (direct) continue;  // warp-uniform
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < kNaiveTiles; u++) {
@@ -134,17 +151,18 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_decode(const uint8_t
                                                                    long long n_tiles, int b, float c,
                                                                    float* out) {
   constexpr int V = G / 32;
+  constexpr int kDecTiles = 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t mask = (1u << b) - 1u;
   const float inv_c = 1.0f / c;  // c is a power of two: RN(y / c) = y * (1 / c)
-  const long long stride = (long long)gridDim.x * kNaiveWarps * kNaiveTiles;
-  for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kNaiveTiles; t0 < n_tiles;
+  const long long stride = (long long)gridDim.x * kNaiveWarps * kDecTiles;
+  for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kDecTiles; t0 < n_tiles;
        t0 += stride) {
-    const int nu = (int)min((long long)kNaiveTiles, n_tiles - t0);
-    uint32_t qv[kNaiveTiles][V];
-    float sc[kNaiveTiles], z[kNaiveTiles];
+    const int nu = (int)min((long long)kDecTiles, n_tiles - t0);
+    uint32_t qv[kDecTiles][V];
+    float sc[kDecTiles], z[kDecTiles];
 #pragma unroll
-    for (int u = 0; u < kNaiveTiles; u++) {
+    for (int u = 0; u < kDecTiles; u++) {
       if (u >= nu) break;
       const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + (t0 + u) * (long long)(G * b / 8));
       sc[u] = __ldg(scales + t0 + u);
@@ -158,7 +176,7 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_decode(const uint8_t
       }
     }
 #pragma unroll
-    for (int u = 0; u < kNaiveTiles; u++) {
+    for (int u = 0; u < kDecTiles; u++) {
       if (u >= nu) break;
       float y[V];
 #pragma unroll
