@@ -547,8 +547,8 @@ def run_gpu(args):
         enc_launches, enc_kernel = 2, f"k_encode<{dt},{G}> (+ k_items)"
     else:
         enc_launches, enc_kernel = 1, f"k_encode_flat<{dt},{G}>"
-    # decode: totals, scan, decode; the wire format adds pack and unpack
-    launches = enc_launches + 3 + (2 if args.wire else 0)
+    # decode: totals (with the offsets scan), decode; the wire format adds pack and unpack
+    launches = enc_launches + 2 + (2 if args.wire else 0)
 
     def step(ev, k=0):
         ev[0].record(stream)
@@ -595,7 +595,7 @@ def run_gpu(args):
     e_ms, d_ms = statistics.mean(enc_ms), statistics.mean(dec_ms)
     enc_gbs, dec_gbs = enc_b / (e_ms * 1e-3) / 1e9, dec_b / (d_ms * 1e-3) / 1e9
     dom = ("decode", dec_b, d_ms) if d_ms >= e_ms else ("encode", enc_b, e_ms)
-    dom_name = f"k_decode<{G}> (+ k_dec_totals, k_dec_scan)" if dom[0] == "decode" else enc_kernel
+    dom_name = f"k_decode<{G}> (+ k_dec_totals)" if dom[0] == "decode" else enc_kernel
     if args.wire:
         dom_name += " + k_wire_unpack" if dom[0] == "decode" else " + k_wire_pack"
 

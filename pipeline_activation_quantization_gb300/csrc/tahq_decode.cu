@@ -5,9 +5,10 @@
 // values") and Algorithm 1 step 5 (stage b de-quantises what it received); the stream
 // layout is §3.4's contiguous uint8 buffer with slots in tile order.
 //
-// Three launches.  k_dec_totals: the slot bytes of every chunk of consecutive tiles (one
+// Two launches.  k_dec_totals: the slot bytes of every chunk of consecutive tiles (one
 // warp per chunk, from the bit widths) and their running sum inside each block of 8
-// chunks.  k_dec_scan: one block turns the block totals into stream offsets.  k_decode: blocks take chunks in a grid-stride
+// chunks; the last of its blocks to finish turns the block totals into stream offsets.
+// k_decode (a dependent launch): blocks take chunks in a grid-stride
 // loop; a block scan gives each tile's offset inside its chunk, the chunk's bytes and
 // metadata are staged in shared memory, and each team of G/8 lanes then
 // unpacks 8 codes per lane, de-quantises (fma(q, scale, zero)) and stores 8 floats per
@@ -165,14 +166,16 @@ __device__ __forceinline__ void dequant8(const uint32_t* sw, int start, int b, f
 
 // Slot bytes of every chunk (one warp per chunk, kDecChunksPerBlock chunks per block);
 // bit widths outside 1..8 count as 0.  Each chunk gets its offset inside its block
-// (ctot), each block its total (bsum, turned into stream offsets by k_dec_scan).
+// (ctot), each block its total (bsum, turned into stream offsets by the last block).
 static_assert(kDecWarps == kDecChunksPerBlock, "one warp per chunk of a block");
 template <int G>
-__global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long long n_chunks) {
+__global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long long n_chunks,
+                                                           long long n_blocks) {
   __shared__ uint32_t s_t[kDecWarps];
+  __shared__ unsigned long long s_w[kDecWarps + 1];
+  __shared__ uint32_t s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long c = (long long)blockIdx.x * kDecWarps + warp;
-  dep_launch();
   const uint32_t tot = c < n_chunks ? warp_chunk_bytes<G>(a.bits, a.n_tiles, c) : 0u;
   if (lane == 0) s_t[warp] = tot;
   __syncthreads();
@@ -188,24 +191,25 @@ __global__ void __launch_bounds__(kDecThreads) k_dec_totals(DecodeArgs a, long l
     if (lane < kDecWarps && cc < n_chunks) a.ctot[cc] = incl - v;
     if (lane == kDecWarps - 1) a.bsum[blockIdx.x] = incl;
   }
-}
-
-// Exclusive prefix of the block totals, in place (one block of 1024 threads, coalesced
-// passes of 4096 entries); flags a stream shorter than the sum of all slots.
-__global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blocks) {
-  constexpr int kPer = 4, kPass = 1024 * kPer;
-  __shared__ unsigned long long s_w[33];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long carry = 0;
-  dep_wait();
+  // the last block to finish turns the block totals into stream offsets
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1u ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the unpack kernel's blocks may now take the SMs (the other blocks have exited)
   dep_launch();
+  __threadfence();
+  constexpr int kPer = 4, kPass = kDecThreads * kPer;
+  unsigned long long carry = 0;
   for (long long p0 = 0; p0 < n_blocks; p0 += kPass) {
     const long long i0 = p0 + (long long)threadIdx.x * kPer;
     unsigned long long v[kPer], mine = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; j++) {
-      v[j] = i0 + j < n_blocks ? a.bsum[i0 + j] : 0ull;
-      mine += v[j];
+    for (int k = 0; k < kPer; k++) {
+      v[k] = i0 + k < n_blocks ? __ldcg(&a.bsum[i0 + k]) : 0ull;
+      mine += v[k];
     }
     unsigned long long incl = mine;
 #pragma unroll
@@ -216,25 +220,25 @@ __global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blo
     if (lane == 31) s_w[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      const unsigned long long w = s_w[lane];
+      const unsigned long long w = lane < kDecWarps ? s_w[lane] : 0ull;
       unsigned long long wi = w;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
+      for (int o = 1; o < kDecWarps; o <<= 1) {
         const unsigned long long y = __shfl_up_sync(kFull, wi, o);
         if (lane >= o) wi += y;
       }
       __syncwarp();
-      s_w[lane] = wi - w;
-      if (lane == 31) s_w[32] = wi;
+      if (lane < kDecWarps) s_w[lane] = wi - w;
+      if (lane == kDecWarps - 1) s_w[kDecWarps] = wi;
     }
     __syncthreads();
     unsigned long long acc = carry + s_w[warp] + incl - mine;
 #pragma unroll
-    for (int j = 0; j < kPer; j++) {
-      if (i0 + j < n_blocks) a.bsum[i0 + j] = acc;
-      acc += v[j];
+    for (int k = 0; k < kPer; k++) {
+      if (i0 + k < n_blocks) a.bsum[i0 + k] = acc;
+      acc += v[k];
     }
-    carry += s_w[32];
+    carry += s_w[kDecWarps];
     __syncthreads();
   }
   if (threadIdx.x == 0) {
@@ -242,6 +246,9 @@ __global__ void __launch_bounds__(1024) k_dec_scan(DecodeArgs a, long long n_blo
     if (carry > a.codes_bytes) set_status(a.status, kStOverrun);
   }
 }
+
+// Exclusive prefix of the block totals, in place (one block of 1024 threads, coalesced
+// passes of 4096 entries); flags a stream shorter than the sum of all slots.
 
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), in the thread's
 // current copy group.
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
     uint32_t off = block_exclusive_scan_dec<kDecThreads>(mine, chunk_bytes, s.scan);
     (void)chunk_bytes;
     // each tile's slot (the chunk's first byte in the stream from k_dec_totals and
-    // k_dec_scan), and, settled once here, whether it decodes (width 0: its slot runs past
+    // its last block), and, settled once here, whether it decodes (width 0: its slot runs past
     // the stream or its width or pivot is invalid, and it decodes to zeros) and is
     // transformed
 #pragma unroll
@@ -454,14 +461,13 @@ static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   // load, scan and unpack phases overlap
   const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   const size_t smem = sizeof(DecSmem<G>);
-  cudaError_t e = cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t e_attr =
+      cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e_attr != cudaSuccess) return e_attr;
+  k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks, n_blocks);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // the scan and the unpack start while the kernel before drains (dep_wait inside)
-  e = launch_dependent(k_dec_scan, 1u, 1024u, 0, st, a, n_blocks);
-  if (e != cudaSuccess) return e;
+  // the unpack starts while the kernel before drains (dep_wait inside)
   return launch_dependent(k_decode<G>, (unsigned)blocks, (unsigned)kDecThreads, smem, st, a, n_chunks,
                           n_blocks);
 }
