@@ -538,8 +538,8 @@ def run_gpu(args):
     if run_flat:
         enc_launches, enc_kernel = 1, f"k_run_flat<{dt},{G},{flat_b}>"
     elif run_ranked:
-        enc_launches = 4
-        enc_kernel = f"k_run_tiles<{dt},{G}> (+ k_run_select, k_run_widths, k_run_compact)"
+        enc_launches = 3
+        enc_kernel = f"k_run_tiles<{dt},{G}> (+ k_run_select, k_run_compact)"
     elif three:
         enc_launches = 6
         enc_kernel = f"k_stats<{dt},{G}> + k_quant<{dt},{G}> (+ k_gather, k_rank, k_widths, k_chunk_scan)"

@@ -2217,27 +2217,24 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       return cudaGetLastError();
     }
     if (plain && !flat && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0 &&
-        (a.n_g + kEncMaxCC - 1) / kEncMaxCC <= 64 * 256) {
+        (a.n_g + kEncMaxCC - 1) / kEncMaxCC <= 64 * 256 && a.group_bytes < (1ll << 31)) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
       p.CHC = kEncMaxCC;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
-      const int J2 = (int)std::max<long long>(1, std::min<long long>(64, a.n_g / 8192));
-      const int J3 = (int)std::max<long long>(1, std::min<long long>(64, p.nC / 2));
-      const int U = (p.slot_lo % 16 == 0 && p.slot_hi % 16 == 0 && a.group_bytes % 16 == 0) ? 16
-                    : (p.slot_lo % 8 == 0 && p.slot_hi % 8 == 0 && a.group_bytes % 8 == 0) ? 8 : 4;
+      const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
       static const cudaError_t e_attr =
           cudaFuncSetAttribute(k_run_tiles<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
       if (e_attr != cudaSuccess) return e_attr;
       k_run_tiles<Tin, G><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
-      e = launch_dependent(k_run_select<Tin, G>, (unsigned)(a.n_groups * J2), kThreads, 0, st, p, J2);
+      e = launch_dependent(k_run_select<Tin, G>, (unsigned)(a.n_groups * J2), kThreads, 0, st, p,
+                           J2, (long long)kSelPart);
       if (e != cudaSuccess) return e;
-      e = launch_dependent(k_run_widths, (unsigned)(a.n_groups * J3), kThreads, 0, st, p, J3);
-      if (e != cudaSuccess) return e;
-      void (*comp)(EncParams) = U == 16 ? k_run_compact<16> : U == 8 ? k_run_compact<8> : k_run_compact<4>;
-      return launch_dependent(comp, (unsigned)(a.n_groups * p.nC), kThreads, 0, st, p);
+      // slots of 3 and 4 units of G / 8 bytes: group strides are whole units
+      static_assert(G % 32 == 0, "units of G / 8 bytes");
+      return launch_dependent(k_run_compact<G>, (unsigned)(a.n_groups * p.nC), kThreads, 0, st, p);
     }
   }
   // a compaction chunk's per-tile arrays (3 bytes per tile) follow the shared state

@@ -23,8 +23,9 @@
 // The allocation stays exactly the canonical one: the select of a group finds the
 // histogram bucket of its K-th approximate key, and every tile whose approximate key
 // lies within kWinBins buckets of it gets its canonical key recomputed from the input
-// (do_select_run); all other tiles are at least 2 kKeyErr away from the K-th canonical
-// key, so their approximate keys rank them on the right side of it.
+// (k_run_select); all other tiles are at least 2 kKeyErr away from the K-th canonical
+// key, so their approximate keys rank them on the right side of it, and the select gives
+// them their widths at once.  Three launches: k_run_tiles, k_run_select, k_run_compact.
 #pragma once
 
 #include "tahq_encode.cuh"
@@ -668,22 +669,41 @@ __device__ __forceinline__ uint4 warp_tile_raw(const EncParams& p, long long t) 
   return r;
 }
 
+// Tiles of a select part (a multiple of 32 and of kThreads); candidates ranked through a
+// histogram when they are at most kRankHist (their rank keys and 4096 bins fill 32 KB).
+constexpr int kSelPart = 2048;
+constexpr uint32_t kRankHist = 2048;
+
 struct SelSmem {
   unsigned char buf[kChunkBytes];  // window tiles, then candidate rank keys
   LgTables tabs;
   uint32_t bins[256];
   uint32_t scan[16];
+  uint32_t wscan[kWarps + 4];
+  unsigned long long theta;
   uint32_t last;
 };
 
-// Stage 2, blocks (group g, j): every tile of the block's slice of the group whose
-// approximate key lies within kWinBins buckets of the bucket of the group's K-th key
-// gets its canonical key (written over the approximate one and appended, as a rank key,
-// to the group's candidates); the group's last block ranks them: the radix select of the
-// r-th largest rank key, r = K - tiles above the window, is the group's threshold.
+// Width b of tile t and its scale D / Q_b (D is what the tiles pass left in scales).
+__device__ __forceinline__ void put_width(const EncParams& p, long long t, bool hi, float D) {
+  const int b = hi ? 4 : 3;
+  p.bits[t] = (uint8_t)b;
+  p.scales[t] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
+}
+
+// Stage 2, blocks (group g, j): part j of the group, `per` tiles (a multiple of 32, at
+// most kSelPart).  The group's K-th approximate key lies in fine bucket b*; every tile
+// whose approximate key lies within kWinBins buckets of b* is a candidate: it gets its
+// canonical key (written over the approximate one and appended, as a rank key, to the
+// group's candidates).  Every other tile lies at least 2 kKeyErr from the K-th canonical
+// key, so its side of it is known now: hi above the window, lo below; its width, scale,
+// bit of its segment's hi mask and its chunk's hi count are written here.  The group's
+// last block ranks the candidates (the r-th largest rank key, r = K - tiles above the
+// window, is the group's threshold), gives them their widths, and turns the chunks' hi
+// counts into their byte offsets in the stream.
 template <typename Tin, int G>
-__global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__ EncParams p,
-                                                         int J) {
+__global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constant__ EncParams p,
+                                                         int J, long long per) {
   __shared__ __align__(16) SelSmem s;
   const long long g = blockIdx.x / J, jb = blockIdx.x % J;
   const uint32_t K = (uint32_t)p.K;
@@ -693,8 +713,20 @@ __global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__
     float* dst = reinterpret_cast<float*>(&s.tabs);
     for (int i = threadIdx.x; i < (int)(sizeof(LgTables) / 4); i += kThreads) dst[i] = src[i];
   }
+  const long long lo = jb * per, hi = min(p.n_g, lo + per);
   dep_wait();
   dep_launch();
+  // the part's keys and ranges, loaded while warp 0 finds the window
+  constexpr int kB = kSelPart / kThreads;
+  const float* kg = p.keys + g * p.n_g;
+  const float* dg = p.scales + g * p.n_g;
+  float hv[kB], dv[kB];
+#pragma unroll
+  for (int u = 0; u < kB; u++) {
+    const long long i = lo + u * kThreads + threadIdx.x;
+    hv[u] = i < hi ? __ldcg(&kg[i]) : 0.0f;
+    dv[u] = i < hi ? __ldcg(&dg[i]) : 0.0f;
+  }
   const uint32_t* hf = p.hist_fine + g * (long long)kFineBins;
   if (warp == 0) {
     for (int i = lane; i < 256; i += 32) s.bins[i] = __ldcg(&p.hist_coarse[g * kCoarseBins + i]);
@@ -713,7 +745,7 @@ __global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__
     uint32_t upper = 0, inwin = 0;  // tiles above bstar in the window; in the window
     const int b = blo + lane;
     if (b <= bhi) {
-      const uint32_t cnt = __ldcg(&hf[b]);
+      const uint32_t cnt = (b >> 8) == cb ? s.bins[b & 255] : __ldcg(&hf[b]);
       inwin = cnt;
       upper = b > bstar ? cnt : 0u;
     }
@@ -735,71 +767,68 @@ __global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__
   __syncthreads();
   const int blo = (int)s.scan[0], bhi = (int)s.scan[1];
   uint32_t* list = reinterpret_cast<uint32_t*>(s.buf);
-  constexpr int kB = 8;  // keys in flight per thread
-  constexpr int kCap = kChunkBytes / 4 - kB * kThreads;
-  const long long per = (p.n_g + J - 1) / J;
-  const long long lo = jb * per, hi = min(p.n_g, lo + per);
-  const float* kg = p.keys + g * p.n_g;
-  for (long long base = lo; base < hi; base += kB * kThreads) {
-    float hv[kB];
+  uint32_t* segmask = p.segmask + g * ((p.n_g + 31) / 32);
+  unsigned long long* words = p.lookback + g * p.nC;
 #pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const long long i = base + u * kThreads + threadIdx.x;
-      hv[u] = i < hi ? __ldcg(&kg[i]) : 0.0f;
+  for (int u = 0; u < kB; u++) {
+    const long long iw = lo + u * kThreads + warp * 32;  // the warp's segment
+    const long long i = iw + lane;
+    const int fbin = fine_bin(hv[u], p.fscale);
+    const bool in = i < hi;
+    const bool hit = in && fbin >= blo && fbin <= bhi;
+    const bool above = in && fbin > bhi;
+    if (in && !hit) put_width(p, g * p.n_g + i, above, dv[u]);
+    const unsigned hm = __ballot_sync(kFull, above);
+    if (lane == 0 && iw < hi) {
+      segmask[iw >> 5] = hm;  // the candidates' bits follow in the last block
+      if (hm) atomicAdd(&words[iw / p.CHC], (unsigned long long)__popc(hm));
     }
-#pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const long long i = base + u * kThreads + threadIdx.x;
-      const int fbin = fine_bin(hv[u], p.fscale);
-      const bool hit = i < hi && fbin >= blo && fbin <= bhi;
-      const unsigned mask = __ballot_sync(kFull, hit);
-      if (mask) {
-        uint32_t pos0 = 0;
-        const int leader = __ffs(mask) - 1;
-        if (lane == leader) pos0 = atomicAdd(&s.scan[4], (uint32_t)__popc(mask));
-        pos0 = __shfl_sync(kFull, pos0, leader);
-        if (hit) list[pos0 + __popc(mask & ((1u << lane) - 1u))] = (uint32_t)i;
-      }
-    }
-    __syncthreads();
-    const int n = (int)s.scan[4];
-    if (n > kCap || base + kB * kThreads >= hi) {  // block-uniform
-      // canonical keys, one warp a tile, eight tiles' loads in flight a warp
-      constexpr int kF = 8;
-#pragma unroll 1
-      for (int i0 = warp * kF; i0 < n; i0 += kWarps * kF) {
-        uint4 raw[kF];
-#pragma unroll
-        for (int q = 0; q < kF; q++) {
-          const int i = i0 + q;
-          raw[q] = i < n ? warp_tile_raw<Tin, G>(p, g * p.n_g + list[i]) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        uint32_t tl_mine = 0u;
-        float h_mine = 0.0f;
-#pragma unroll
-        for (int q = 0; q < kF; q++) {
-          if (i0 + q >= n) break;  // warp-uniform
-          const float H = warp_exact_key<Tin, G>(raw[q], s.tabs);
-          if (lane == q) {
-            tl_mine = list[i0 + q];
-            h_mine = H;
-          }
-        }
-        const int nk = min(kF, n - i0);
-        uint32_t pos0 = 0;
-        if (lane == 0) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)nk);
-        pos0 = __shfl_sync(kFull, pos0, 0);
-        if (lane < nk) {
-          p.keys[g * p.n_g + tl_mine] = h_mine;
-          p.cand[g * p.n_g + pos0 + lane] = rank_key(h_mine, tl_mine);
-          if (!(fabsf(h_mine) <= FLT_MAX)) set_status(p.status, kStNonFinite);
-        }
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) s.scan[4] = 0u;
-      __syncthreads();
+    const unsigned mask = __ballot_sync(kFull, hit);
+    if (mask) {
+      uint32_t pos0 = 0;
+      const int leader = __ffs(mask) - 1;
+      if (lane == leader) pos0 = atomicAdd(&s.scan[4], (uint32_t)__popc(mask));
+      pos0 = __shfl_sync(kFull, pos0, leader);
+      if (hit) list[pos0 + __popc(mask & ((1u << lane) - 1u))] = (uint32_t)i;
     }
   }
+  __syncthreads();
+  {
+    // canonical keys, one warp a tile, eight tiles' loads in flight a warp (four of 16
+    // bytes a lane)
+    const int n = (int)s.scan[4];
+    constexpr int kF = G * (int)sizeof(Tin) >= 512 ? 4 : 8;
+#pragma unroll 1
+    for (int i0 = warp * kF; i0 < n; i0 += kWarps * kF) {
+      uint4 raw[kF];
+#pragma unroll
+      for (int q = 0; q < kF; q++) {
+        const int i = i0 + q;
+        raw[q] = i < n ? warp_tile_raw<Tin, G>(p, g * p.n_g + list[i]) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      uint32_t tl_mine = 0u;
+      float h_mine = 0.0f;
+#pragma unroll
+      for (int q = 0; q < kF; q++) {
+        if (i0 + q >= n) break;  // warp-uniform
+        const float H = warp_exact_key<Tin, G>(raw[q], s.tabs);
+        if (lane == q) {
+          tl_mine = list[i0 + q];
+          h_mine = H;
+        }
+      }
+      const int nk = min(kF, n - i0);
+      uint32_t pos0 = 0;
+      if (lane == 0) pos0 = atomicAdd(&p.cand_cnt[g], (uint32_t)nk);
+      pos0 = __shfl_sync(kFull, pos0, 0);
+      if (lane < nk) {
+        p.keys[g * p.n_g + tl_mine] = h_mine;
+        p.cand[g * p.n_g + pos0 + lane] = rank_key(h_mine, tl_mine);
+        if (!(fabsf(h_mine) <= FLT_MAX)) set_status(p.status, kStNonFinite);
+      }
+    }
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const uint32_t prev = atomicAdd(&p.doneB[g], 1u);
@@ -812,125 +841,133 @@ __global__ void __launch_bounds__(kThreads) k_run_select(const __grid_constant__
   const uint32_t cnt = __ldcg(&p.cand_cnt[g]);
   if (threadIdx.x == 0 && cnt != s.scan[3]) set_status(p.status, kStSelectMismatch);
   const uint32_t r = max(1u, min(K - s.scan[2], cnt));  // rank (from 1) among them
-  // the r-th largest rank key (they are distinct): by counting when the candidates are
-  // few, else a radix select (8 passes of 8 bits); from shared memory when they fit
+  // the r-th largest rank key (they are distinct): through a histogram when the
+  // candidates are at most kRankHist, else a radix select (8 passes of 8 bits); from
+  // shared memory when they fit
   constexpr uint32_t kStage = kChunkBytes / 8;
   unsigned long long* ck = reinterpret_cast<unsigned long long*>(s.buf);
   const bool staged = cnt <= kStage;
   if (staged)
     for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) ck[i] = __ldcg(&cg[i]);
-  __syncthreads();
-  if (cnt > 0u && cnt <= 1024u) {
-    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
-      const unsigned long long ki = ck[i];
-      uint32_t larger = 0;
-      for (uint32_t j = 0; j < cnt; j++) larger += ck[j] > ki ? 1u : 0u;
-      if (larger == r - 1u) p.sel[g] = SelResult{ki, kSelThreshold, 0u};
-    }
-    return;
-  }
-  uint32_t rr = r;
-  unsigned long long prefix = 0ull, mask = 0ull;
-  for (int pass = 7; pass >= 0 && cnt > 0u; --pass) {
-    const int shift = pass * 8;
-    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
-      const unsigned long long v = staged ? ck[i] : __ldcg(&cg[i]);
-      if ((v & mask) == prefix) atomicAdd(&s.bins[(v >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int d;
-      uint32_t ab;
-      warp_find_from_top(s.bins, rr, d, ab);
-      if (lane == 0) {
-        s.scan[5] = (uint32_t)d;
-        s.scan[6] = ab;
-      }
-    }
-    __syncthreads();
-    prefix |= (unsigned long long)s.scan[5] << shift;
-    rr -= s.scan[6];
-    mask |= 0xFFull << shift;
-    for (int i = threadIdx.x; i < 256; i += kThreads) s.bins[i] = 0u;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) p.sel[g] = SelResult{prefix, cnt ? kSelThreshold : kSelNone, 0u};
-}
-
-// ------------------------------------------------------------------ stage 3: widths
-
-// Blocks (group g, j) take the group's compaction chunks [c0, c1) (CHC tiles each, whole
-// 32-tile segments): every tile's width (rank key against the group's threshold) and
-// scale D / Q of that width, each segment's hi mask, each chunk's hi count; the group's
-// last block turns the counts into the chunks' byte offsets in the stream.
-static __global__ void __launch_bounds__(kThreads) k_run_widths(const __grid_constant__ EncParams p, int J) {
-  __shared__ uint32_t cnt_s[256];
-  __shared__ uint32_t scan_s[kWarps + 4];
-  __shared__ uint32_t last_s;
-  const long long g = blockIdx.x / J, jb = blockIdx.x % J;
-  const int lane = threadIdx.x & 31;
-  dep_wait();
-  dep_launch();
-  const SelResult sr = p.sel[g];
-  const long long per = (p.nC + J - 1) / J;
-  const long long c0 = jb * per, c1 = min(p.nC, c0 + per);
-  for (long long c = c0 + threadIdx.x; c < c1; c += kThreads) cnt_s[c - c0] = 0u;
-  __syncthreads();
-  const long long tl_begin = c0 * p.CHC, tl_end = min(p.n_g, c1 * p.CHC);
-  uint32_t* segmask = p.segmask + g * ((p.n_g + 31) / 32);
-  constexpr int kB = 8;
-  for (long long tb = tl_begin; tb < tl_end; tb += kB * kThreads) {
-    float key[kB], Dv[kB];
-#pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const long long tl = tb + u * kThreads + threadIdx.x;
-      key[u] = 0.0f;
-      Dv[u] = 0.0f;
-      if (tl < tl_end) {
-        const long long t = g * p.n_g + tl;
-        key[u] = __ldcg(&p.keys[t]);
-        Dv[u] = __ldcg(&p.scales[t]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const long long tw = tb + u * kThreads + (threadIdx.x & ~31);  // the warp's segment
-      const long long tl = tw + lane;
-      bool ishi = false;
-      if (tl < tl_end) {
-        const long long t = g * p.n_g + tl;
-        ishi = sr.mode == kSelAll ||
-               (sr.mode == kSelThreshold && rank_key(key[u], (uint32_t)tl) >= sr.theta);
-        const int b = ishi ? 4 : 3;
-        p.bits[t] = (uint8_t)b;
-        p.scales[t] = (Dv[u] >= 0x1p-120f) ? __fdiv_rn(Dv[u], qmax_f(b)) : 0.0f;
-      }
-      const unsigned hm = __ballot_sync(kFull, ishi);
-      if (lane == 0 && tw < tl_end) {
-        segmask[tw >> 5] = hm;
-        if (hm) atomicAdd(&cnt_s[(uint32_t)((tw - tl_begin) / p.CHC)], (uint32_t)__popc(hm));
-      }
-    }
-  }
-  __syncthreads();
-  unsigned long long* words = p.lookback + g * p.nC;
-  for (long long c = c0 + threadIdx.x; c < c1; c += kThreads) words[c] = cnt_s[c - c0];
-  __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(&p.doneB2[g], 1u);
-    __threadfence();
-    last_s = (prev == (uint32_t)J - 1u) ? 1u : 0u;
+    s.theta = ~0ull;  // no candidate: none of them is hi
+    s.scan[7] = 0xFFFFFFFFu;
+    s.scan[8] = 0u;
   }
   __syncthreads();
-  if (!last_s) return;
+  if (cnt > 0u && cnt <= kRankHist) {
+    // the top words (entropy order) of the candidates' rank keys span a narrow range:
+    // a 4096-bin histogram of them, shifted to fit, finds the bin of the r-th largest;
+    // within it, counting among its members (rank keys are distinct)
+    uint32_t* hb = reinterpret_cast<uint32_t*>(s.buf + 8 * kRankHist);
+    for (int i = threadIdx.x; i < 4096; i += kThreads) hb[i] = 0u;
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+      const uint32_t h = (uint32_t)(ck[i] >> 32);
+      kmn = min(kmn, h);
+      kmx = max(kmx, h);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmn = min(kmn, __shfl_xor_sync(kFull, kmn, o));
+      kmx = max(kmx, __shfl_xor_sync(kFull, kmx, o));
+    }
+    if (lane == 0) {
+      atomicMin(&s.scan[7], kmn);
+      atomicMax(&s.scan[8], kmx);
+    }
+    __syncthreads();
+    kmn = s.scan[7];
+    const uint32_t span = s.scan[8] - kmn;
+    const int sh = max(0, 20 - __clz(span));  // (span >> sh) < 4096
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads)
+      atomicAdd(&hb[((uint32_t)(ck[i] >> 32) - kmn) >> sh], 1u);
+    __syncthreads();
+    // thread t holds bins 4095 - 16 t - j, j = 0..15 (from the top)
+    uint32_t c16[16], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+      c16[j] = hb[4095 - 16 * threadIdx.x - j];
+      sum += c16[j];
+    }
+    uint32_t tot;
+    uint32_t above = block_exclusive_scan<kThreads>(sum, tot, s.wscan);
+    if (above < r && above + sum >= r) {
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        if (above < r && above + c16[j] >= r) {
+          s.scan[9] = 4095u - 16u * threadIdx.x - (uint32_t)j;
+          s.scan[10] = above;
+        }
+        above += c16[j];
+      }
+    }
+    if (threadIdx.x == 0) s.scan[11] = 0u;
+    __syncthreads();
+    const uint32_t bstar_r = s.scan[9], rr = r - s.scan[10];
+    unsigned long long* mem = reinterpret_cast<unsigned long long*>(hb);  // the bin's members
+    for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+      const unsigned long long v = ck[i];
+      if ((((uint32_t)(v >> 32) - kmn) >> sh) == bstar_r) mem[atomicAdd(&s.scan[11], 1u)] = v;
+    }
+    __syncthreads();
+    const uint32_t m = s.scan[11];
+    for (uint32_t i = threadIdx.x; i < m; i += kThreads) {
+      const unsigned long long ki = mem[i];
+      uint32_t larger = 0;
+      for (uint32_t j = 0; j < m; j++) larger += mem[j] > ki ? 1u : 0u;
+      if (larger == rr - 1u) s.theta = ki;
+    }
+  } else if (cnt > 0u) {
+    uint32_t rr = r;
+    unsigned long long prefix = 0ull, mask = 0ull;
+    for (int pass = 7; pass >= 0; --pass) {
+      const int shift = pass * 8;
+      for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+        const unsigned long long v = staged ? ck[i] : __ldcg(&cg[i]);
+        if ((v & mask) == prefix) atomicAdd(&s.bins[(v >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int d;
+        uint32_t ab;
+        warp_find_from_top(s.bins, rr, d, ab);
+        if (lane == 0) {
+          s.scan[5] = (uint32_t)d;
+          s.scan[6] = ab;
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)s.scan[5] << shift;
+      rr -= s.scan[6];
+      mask |= 0xFFull << shift;
+      for (int i = threadIdx.x; i < 256; i += kThreads) s.bins[i] = 0u;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) s.theta = prefix;
+  }
+  __syncthreads();
+  const unsigned long long theta = s.theta;
+  if (threadIdx.x == 0) p.sel[g] = SelResult{theta, cnt ? kSelThreshold : kSelNone, 0u};
+  // the candidates' widths, mask bits and chunk counts
+  for (uint32_t i = threadIdx.x; i < cnt; i += kThreads) {
+    const unsigned long long v = staged ? ck[i] : __ldcg(&cg[i]);
+    const uint32_t tl = 0xFFFFFFFFu - (uint32_t)v;
+    const bool ishi = v >= theta;
+    put_width(p, g * p.n_g + tl, ishi, __ldcg(&p.scales[g * p.n_g + tl]));
+    if (ishi) {
+      atomicOr(&segmask[tl >> 5], 1u << (tl & 31));
+      atomicAdd(&words[tl / p.CHC], 1ull);
+    }
+  }
+  __syncthreads();
   // exclusive prefix of the nC counts: each thread sums a contiguous run, one block scan
   const long long run = (p.nC + kThreads - 1) / kThreads;
   const long long r0 = min(p.nC, (long long)threadIdx.x * run), r1 = min(p.nC, r0 + run);
   unsigned long long mine = 0;
   for (long long c = r0; c < r1; c++) mine += __ldcg(&words[c]);
   uint32_t tot;
-  unsigned long long acc = block_exclusive_scan<kThreads>((uint32_t)mine, tot, scan_s);
+  unsigned long long acc = block_exclusive_scan<kThreads>((uint32_t)mine, tot, s.wscan);
   for (long long c = r0; c < r1; c++) {
     const unsigned long long v = __ldcg(&words[c]);
     words[c] = acc;
@@ -938,15 +975,17 @@ static __global__ void __launch_bounds__(kThreads) k_run_widths(const __grid_con
   }
 }
 
-// ------------------------------------------------------------------ stage 4: compaction
+// ------------------------------------------------------------------ stage 3: compaction
 
 // Block (group g, chunk cc): every warp owns whole 32-tile segments of the chunk; the
-// segment masks and a warp scan of their counts give every tile's place; each lane copies
-// units of U bytes (4, 8 or 16: slots, group stride and chunk offsets are multiples of
-// U) from the scratch slot of the tile's width, several loads in flight, then the warp
-// drops its segments' scratch lines from L2.
-template <int U>
-__global__ void __launch_bounds__(kThreads) k_run_compact(const __grid_constant__ EncParams p) {
+// segment masks and a warp scan of their counts give every tile's place.  Widths {3, 4}
+// on tiles of G values: a lo slot is three units of U = G / 8 bytes, a hi slot four
+// (slots, group stride and chunk offsets are multiples of U).  A warp copies two
+// segments at a time, lane l unit l & 3 of tiles l / 4 + 8 q, q = 0..7: eight loads a
+// lane in flight.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 4) k_run_compact(const __grid_constant__ EncParams p) {
+  constexpr int U = G / 8;
   using Unit = std::conditional_t<U == 16, uint4, std::conditional_t<U == 8, uint2, uint32_t>>;
   const long long g = blockIdx.x / p.nC, cc = blockIdx.x % p.nC;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -955,7 +994,7 @@ __global__ void __launch_bounds__(kThreads) k_run_compact(const __grid_constant_
   const long long tl0 = cc * p.CHC;
   const int nt = (int)min(p.CHC, p.n_g - tl0);
   const int nseg = (nt + 31) >> 5;
-  if (warp >= nseg) return;
+  if (2 * warp >= nseg) return;
   const long long t0 = g * p.n_g + tl0;
   const uint32_t* sm = p.segmask + g * ((p.n_g + 31) / 32) + (tl0 >> 5);
   const uint32_t m0 = lane < nseg ? __ldcg(sm + lane) : 0u;
@@ -973,49 +1012,46 @@ __global__ void __launch_bounds__(kThreads) k_run_compact(const __grid_constant_
   }
   e1 += __shfl_sync(kFull, e0, 31) - c1;
   e0 -= c0;
-  const int slot_lo = p.slot_lo, slot_hi = p.slot_hi, slot_d = slot_hi - slot_lo;
-  const int UH = slot_hi / U, UL = slot_lo / U;
-  const long long base = g * p.group_bytes + tl0 * slot_lo + (long long)prefix * slot_d;
-  for (int seg = warp; seg < nseg; seg += kWarps) {
-    const uint32_t mask = __shfl_sync(kFull, seg < 32 ? m0 : m1, seg & 31);
-    const uint32_t before = __shfl_sync(kFull, seg < 32 ? e0 : e1, seg & 31);
-    const int nv = min(32, nt - 32 * seg);
-    const long long st0 = t0 + 32 * seg;  // the segment's first tile
-    const long long ob = base + 32ll * seg * slot_lo + (long long)before * slot_d;
-    for (int r0 = 0; r0 < UH; r0 += 8) {
-      Unit val[8];
-      long long dst[8];
+  // units within the group's stream (a group's stream is below 2^31 bytes)
+  Unit* gout = reinterpret_cast<Unit*>(p.codes + g * p.group_bytes);
+  const uint32_t gunits = (uint32_t)(p.group_bytes / U);
+  const uint32_t base = (uint32_t)(3 * tl0 + (long long)prefix);
+  const Unit* slo = reinterpret_cast<const Unit*>(p.scratch_lo) + 3 * t0;
+  const Unit* shi = reinterpret_cast<const Unit*>(p.scratch_hi) + 4 * t0;
+  const int u = lane & 3, kl = lane >> 2;
+  for (int sb = 2 * warp; sb < nseg; sb += 2 * kWarps) {
+    uint32_t mk[2], ob[2];
+    int nv[2];
 #pragma unroll
-      for (int q = 0; q < 8; q++) {
-        const int i = lane + 32 * (r0 + q);
-        const int kt = i / UH, u = i - kt * UH;  // kt < 32 whenever r0 + q < UH
-        const bool in = r0 + q < UH && kt < nv;
-        const bool ishi = in && ((mask >> (kt & 31)) & 1u);
-        dst[q] = -1;
-        if (in && (ishi || u < UL)) {
-          const Unit* src = reinterpret_cast<const Unit*>(
-              ishi ? p.scratch_hi + (st0 + kt) * slot_hi : p.scratch_lo + (st0 + kt) * slot_lo);
-          val[q] = __ldcg(src + u);
-          dst[q] = ob + (long long)kt * slot_lo +
-                   (long long)__popc(mask & ((1u << kt) - 1u)) * slot_d + U * u;
-        }
-      }
+    for (int j = 0; j < 2; j++) {
+      const int seg = sb + j;  // segments sb, sb + 1 lie in the same half of the chunk
+      mk[j] = __shfl_sync(kFull, seg < 32 ? m0 : m1, seg & 31);
+      const uint32_t before = __shfl_sync(kFull, seg < 32 ? e0 : e1, seg & 31);
+      nv[j] = seg < nseg ? min(32, nt - 32 * seg) : 0;
+      ob[j] = base + 96u * seg + before;  // the segment's first unit
+    }
+    Unit val[8];
+    uint32_t dst[8];  // 0xFFFFFFFF: no unit
 #pragma unroll
-      for (int q = 0; q < 8; q++) {
-        if (dst[q] < 0) continue;
-        if (dst[q] + U <= p.codes_bytes) {
-          *reinterpret_cast<Unit*>(p.codes + dst[q]) = val[q];
-        } else {
-          set_status(p.status, kStSelectMismatch);  // only if the select went wrong
-        }
+    for (int q = 0; q < 8; q++) {
+      const int j = q >> 2, kt = kl + 8 * (q & 3);  // tile kt of segment sb + j
+      const bool ishi = (mk[j] >> kt) & 1u;
+      dst[q] = 0xFFFFFFFFu;
+      if (kt < nv[j] && (ishi || u < 3)) {
+        const int tile = 32 * (sb + j) + kt;  // within the chunk
+        val[q] = __ldcg(ishi ? shi + 4 * tile + u : slo + 3 * tile + u);
+        dst[q] = ob[j] + 3u * kt + (uint32_t)__popc(mk[j] & ((1u << kt) - 1u)) + u;
       }
     }
-    __syncwarp();
-    // 32 slots of 4-byte multiples are whole 128-byte lines
-    for (long long l = (st0 * slot_lo + 127) / 128 + lane; l < (st0 + nv) * slot_lo / 128; l += 32)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_lo + l * 128) : "memory");
-    for (long long l = (st0 * slot_hi + 127) / 128 + lane; l < (st0 + nv) * slot_hi / 128; l += 32)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.scratch_hi + l * 128) : "memory");
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      if (dst[q] == 0xFFFFFFFFu) continue;
+      if (dst[q] < gunits) {
+        gout[dst[q]] = val[q];
+      } else {
+        set_status(p.status, kStSelectMismatch);  // only if the select went wrong
+      }
+    }
   }
 }
 
