@@ -191,6 +191,46 @@ def test_edge_cases(name, dtype):
     _check(x, 64, 64, 3, 4, 3.5, 4)
 
 
+# The same value patterns with token groups of whole 32 KB input chunks and tiles of 32 to
+# 128 values, the shapes the streaming encoder takes (ranked at 3.5 bits, one width at 3):
+# ties of every key in the group (zeros, constant, flat signs), subnormal and huge values,
+# ratios at tau and just above.
+@pytest.mark.parametrize("name", sorted(EDGE))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("beta", [3.5, 3.0])
+def test_edge_cases_whole_chunk_groups(name, dtype, beta):
+    x = np.tile(EDGE[name], (4, 4))  # 64 x 2048; tiles of 64 keep their values
+    if dtype == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    _check(x, 64, 64, 3, 4, beta, 16)
+
+
+SMALL_STREAM = [
+    # dtype, dist, G, h, beta, T, C, S: groups of whole input chunks
+    ("f32", "laplace", 64, 64, 3.5, 64, 2048, 16),
+    ("bf16", "gauss_rms_spikes", 64, 32, 3.5, 64, 2048, 16),
+    ("f32", "student_t", 32, 32, 3.25, 32, 4096, 8),
+    ("bf16", "laplace", 32, 16, 3.75, 64, 2048, 32),
+    ("f32", "gauss_fixed_channels", 128, 128, 3.5, 64, 2048, 32),
+    ("bf16", "student_t", 128, 64, 3.1, 64, 4096, 16),
+]
+
+
+@pytest.mark.parametrize("dtype,dist,G,h,beta,T,C,S", SMALL_STREAM)
+def test_small_whole_chunk_groups(dtype, dist, G, h, beta, T, C, S):
+    w = synth.Workload("small", T, C, dtype, G, h, 3, 4, beta, S, 200 + T + G, dist)
+    _check(synth.generate(w), G, h, 3, 4, beta, S)
+
+
+@pytest.mark.parametrize("T,C,S", [(16, 8192, 16), (64, 8192, 64)])
+def test_all_keys_tie_in_a_large_group(T, C, S):
+    """Every tile's key equal: the whole group is the select's window (2048 candidates:
+    the histogram rank; 8192: the radix select over the candidates in memory)."""
+    rng = np.random.default_rng(11)
+    x = (np.where(rng.random((T, C)) < 0.5, -1.0, 1.0) * 0.75).astype(np.float32)
+    _check(x, 64, 64, 3, 4, 3.5, S)
+
+
 def test_bf16_subnormal_and_single_tile():
     x = (np.arange(64, dtype=np.uint16) + np.uint16(1)).reshape(1, 64)   # bf16 subnormals
     x[0, 5] |= np.uint16(0x8000)
