@@ -164,6 +164,26 @@ __device__ __forceinline__ void dequant8(const uint32_t* sw, int start, int b, f
   }
 }
 
+// dequant8 for b <= 4 (the 8 codes in one word), for warps whose tiles all have b <= 4.
+__device__ __forceinline__ void dequant8_le4(const uint32_t* sw, int start, int b, float sc,
+                                             float mn, float* v) {
+  const int q = start >> 2, sh = (start & 3) * 8;
+  const uint32_t lo = __funnelshift_r(sw[q], sw[q + 1], sh);
+  const uint32_t mask = (1u << b) - 1u;
+  const float2 s2 = make_float2(sc, sc), z2 = make_float2(mn, mn);
+  const float2 m2 = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const uint32_t c0 = (lo >> (j * b)) & mask;
+    const uint32_t c1 = (lo >> ((j + 1) * b)) & mask;
+    const float2 qf = addp(make_float2(__uint_as_float(0x4B000000u | c0),
+                                       __uint_as_float(0x4B000000u | c1)), m2);
+    const float2 r = fma2(qf, s2, z2);
+    v[j] = r.x;
+    v[j + 1] = r.y;
+  }
+}
+
 // Slot bytes of every chunk (one warp per chunk, kDecChunksPerBlock chunks per block);
 // bit widths outside 1..8 count as 0.  Each chunk gets its offset inside its block
 // (ctot), each block its total (bsum, turned into stream offsets by the last block).
@@ -399,6 +419,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
     // 4. untransformed tiles; transformed ones are listed for the second pass
     uint16_t* fl = s.flagged + warp * NS;
     int nflag = 0;
+    float* outc = a.out + t0 * G;  // the chunk's first value
 #pragma unroll 1
     for (int st = 0; st < C::kSteps; st++) {
       const int kt = (st * kDecWarps + warp) * TPW + team;
@@ -409,15 +430,19 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
       const unsigned fm = __ballot_sync(kFull, flag && sub == 0);
       if (flag && sub == 0) fl[nflag + __popc(fm & ((1u << lane) - 1u))] = (uint16_t)kt;
       nflag += __popc(fm);
+      const bool narrow = __all_sync(kFull, b <= 4);  // warp-uniform
       if (!valid || flag) continue;
       float v[V];
-      if (ok) {
-        dequant8(stage, pad + (int)s.off[kt] + sub * b, b, s.scale[kt], s.zero[kt], v);
+      const int start = pad + (int)s.off[kt] + sub * b;
+      if (narrow) {  // b = 0 decodes to zeros: codes 0, scale and zero 0
+        dequant8_le4(stage, start, b, ok ? s.scale[kt] : 0.0f, ok ? s.zero[kt] : 0.0f, v);
+      } else if (ok) {
+        dequant8(stage, start, b, s.scale[kt], s.zero[kt], v);
       } else {
 #pragma unroll
         for (int j = 0; j < V; j++) v[j] = 0.0f;
       }
-      float4* o = reinterpret_cast<float4*>(a.out + (t0 + kt) * G + sub * V);
+      float4* o = reinterpret_cast<float4*>(outc + kt * G + sub * V);
       o[0] = make_float4(v[0], v[1], v[2], v[3]);
       o[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
@@ -431,8 +456,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
       const int b = valid ? (int)s.bits[kt] : 1;
       const int piv = valid ? (int)s.piv[kt] : 0;
       float v[V];
-      dequant8(stage, valid ? pad + (int)s.off[kt] + sub * b : 0, b, valid ? s.scale[kt] : 0.0f,
-               valid ? s.zero[kt] : 0.0f, v);
+      const int start = valid ? pad + (int)s.off[kt] + sub * b : 0;
+      const float sc = valid ? s.scale[kt] : 0.0f, zr = valid ? s.zero[kt] : 0.0f;
+      if (__all_sync(kFull, b <= 4)) {  // warp-uniform
+        dequant8_le4(stage, start, b, sc, zr, v);
+      } else {
+        dequant8(stage, start, b, sc, zr, v);
+      }
       team_fwht<V, L>(v, a.h, sub);
 #pragma unroll
       for (int j = 0; j < V; j++) v[j] = __fmul_rn(v[j], a.c_h);
