@@ -2192,13 +2192,13 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   const bool flat = a.K == 0 || a.K == (a.n_g >> a.mlog);
   p.flat_b = a.K == 0 ? a.lo : a.hi;
   if constexpr (G >= 32 && G <= 128) {
-    // the streaming encoder: the method's defaults (tau = 2, A = G, fp32 metadata), one
-    // width of 3 or 4 bits, or widths {3, 4} ranked per group of whole input chunks; the
-    // input in 128-byte rows
+    // the streaming encoder: the method's defaults (tau = 2, A = G; fp32 metadata or the
+    // wire format's quantiser), one width of 3 or 4 bits, or widths {3, 4} ranked per group
+    // of whole input chunks; the input in 128-byte rows
     const long long esz = (long long)sizeof(Tin);
     const bool rows = (a.n_tiles * G * esz) % 128 == 0 && (a.n_g * G) % 128 == 0 &&
                       a.n_tiles < (1ll << 31);
-    const bool plain = a.tau == 2.0f && !a.wire && a.mlog == 0 && rows;
+    const bool plain = a.tau == 2.0f && a.mlog == 0 && rows;
     const size_t smem_r = sizeof(RunSmem<Tin, G>) + 1024;
     const long long n_chunks = (a.n_tiles + C::CH - 1) / C::CH;
     // three blocks an SM (<= 80 registers, two 32 KB stages each)
@@ -2207,12 +2207,18 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
       void (*kern)(EncParams, long long) =
-          p.flat_b == 3 ? k_run_flat<Tin, G, 3> : k_run_flat<Tin, G, 4>;
-      static const cudaError_t e3 =
-          cudaFuncSetAttribute(k_run_flat<Tin, G, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-      static const cudaError_t e4 =
-          cudaFuncSetAttribute(k_run_flat<Tin, G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-      if (e3 != cudaSuccess || e4 != cudaSuccess) return e3 != cudaSuccess ? e3 : e4;
+          a.wire ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, true> : k_run_flat<Tin, G, 4, true>)
+                 : (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false> : k_run_flat<Tin, G, 4, false>);
+      static const cudaError_t e_attr = [smem_r] {
+        void (*ks[4])(EncParams, long long) = {k_run_flat<Tin, G, 3, false>, k_run_flat<Tin, G, 4, false>,
+                                               k_run_flat<Tin, G, 3, true>, k_run_flat<Tin, G, 4, true>};
+        for (auto k : ks) {
+          const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+          if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+      }();
+      if (e_attr != cudaSuccess) return e_attr;
       kern<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       return cudaGetLastError();
     }
@@ -2223,14 +2229,23 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       p.CHC = kEncMaxCC;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
       const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
-      static const cudaError_t e_attr =
-          cudaFuncSetAttribute(k_run_tiles<Tin, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+      static const cudaError_t e_attr = [smem_r] {
+        const cudaError_t e0 = cudaFuncSetAttribute(k_run_tiles<Tin, G, false>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+        const cudaError_t e1 = cudaFuncSetAttribute(k_run_tiles<Tin, G, true>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+        return e0 != cudaSuccess ? e0 : e1;
+      }();
       if (e_attr != cudaSuccess) return e_attr;
-      k_run_tiles<Tin, G><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      if (a.wire) {
+        k_run_tiles<Tin, G, true><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      } else {
+        k_run_tiles<Tin, G, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      }
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
-      e = launch_dependent(k_run_select<Tin, G>, (unsigned)(a.n_groups * J2), kThreads, 0, st, p,
-                           J2, (long long)kSelPart);
+      e = launch_dependent(a.wire ? k_run_select<Tin, G, true> : k_run_select<Tin, G, false>,
+                           (unsigned)(a.n_groups * J2), kThreads, 0, st, p, J2, (long long)kSelPart);
       if (e != cudaSuccess) return e;
       // slots of 3 and 4 units of G / 8 bytes: group strides are whole units
       static_assert(G % 32 == 0, "units of G / 8 bytes");

@@ -221,8 +221,10 @@ __device__ __forceinline__ RunSmem<Tin, G>& run_smem(unsigned char* raw) {
 // a division: RN(m1 / d) > 2 iff m1 / 2 - d > d 2^-24, d = RN(m2 + 1e-12), exact by
 // Sterbenz's lemma), and the tiles it flags get the pivot swap, the Hadamard of eq. (4),
 // a new range and new codes: at both widths into out_lo / out_hi (kFlat false: scales
-// keep the range D) or at width kB into out_lo (kFlat: the final scale).
-template <typename Tin, int G, bool kFlat, int kB>
+// keep the range D) or at width kB into out_lo (kFlat: the final scale).  kW: the wire
+// format's quantiser (zero = the fp16 value below the minimum, the smallest covering fp16
+// scale of each width); ranked, the scales field keeps the maximum.
+template <typename Tin, int G, bool kFlat, int kB, bool kW>
 __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned char* src,
                                           const uint16_t* list, int first, int n, long long t0,
                                           unsigned char* out_lo, unsigned char* out_hi) {
@@ -277,14 +279,25 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
     mn = team_min<L>(mn);
     mx = team_max<L>(mx);
     const float D = __fsub_rn(mx, mn);
-    // lane 0 of the team: Q_lo / D (flat: Q / D); lane 1: Q_hi / D (flat: D / Q)
     const float qa = qmax_f(kFlat ? kB : 3), qb = qmax_f(kFlat ? kB : 4);
-    const bool one = sub == 1;
-    const float r = kFlat ? __fdiv_rn(one ? D : qa, one ? qa : D) : __fdiv_rn(one ? qb : qa, D);
-    const float r0 = __shfl_sync(kFull, r, base), r1 = __shfl_sync(kFull, r, base + 1);
-    const bool degenerate = !(D >= 0x1p-120f);
-    const float inv0 = degenerate ? 0.0f : r0, r1d = degenerate ? 0.0f : r1;
-    const float2 nmn = make_float2(-mn, -mn), mg = make_float2(12582912.0f, 12582912.0f);
+    float inv0, r1d, qz = mn, meta = D;
+    if constexpr (kW) {
+      qz = wire_zero(mn);
+      const float sa = wire_scale(qz, mx, qa);
+      inv0 = wire_inv(sa);
+      r1d = kFlat ? sa : wire_inv(wire_scale(qz, mx, qb));
+      meta = kFlat ? sa : mx;
+    } else {
+      // lane 0 of the team: Q_lo / D (flat: Q / D); lane 1: Q_hi / D (flat: D / Q)
+      const bool one = sub == 1;
+      const float r = kFlat ? __fdiv_rn(one ? D : qa, one ? qa : D) : __fdiv_rn(one ? qb : qa, D);
+      const float r0 = __shfl_sync(kFull, r, base), r1 = __shfl_sync(kFull, r, base + 1);
+      const bool degenerate = !(D >= 0x1p-120f);
+      inv0 = degenerate ? 0.0f : r0;
+      r1d = degenerate ? 0.0f : r1;
+      if (kFlat) meta = r1d;
+    }
+    const float2 nmn = make_float2(-qz, -qz), mg = make_float2(12582912.0f, 12582912.0f);
     float2 u[V / 2];
 #pragma unroll
     for (int j = 0; j < V / 2; j++) u[j] = add2(make_float2(v[2 * j], v[2 * j + 1]), nmn);
@@ -314,7 +327,7 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
         dw[2] = (f2 >> 16) | (f3 << 8);
       }
     }
-    if (flag && sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)i1, kFlat ? r1d : D, kFlat);
+    if (flag && sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)i1, meta, kFlat);
   }
 }
 
@@ -323,8 +336,9 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
 // One staged chunk (tiles t0 .. t0 + nt of group g), chunk number k of the block.  kFlat:
 // every tile at width kB, codes straight into the stream at out_lo (slot t G kB / 8);
 // else keys, histograms and both widths into the scratch streams out_lo / out_hi.
-// Deferred tiles go to the list s.dl (s.ndef[k & 1] of them).
-template <typename Tin, int G, bool kFlat, int kB>
+// Deferred tiles go to the list s.dl (s.ndef[k & 1] of them).  kW: the wire format's
+// quantiser (see pass2_run).
+template <typename Tin, int G, bool kFlat, int kB, bool kW>
 __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p, long long g,
                                          long long t0, int nt, int k, unsigned char* out_lo,
                                          unsigned char* out_hi) {
@@ -385,30 +399,52 @@ __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p,
     // shares the two divisions)
     float r0, r1;
     const float qa = qmax_f(kFlat ? kB : 3), qb = qmax_f(kFlat ? kB : 4);
-    if constexpr (LPT >= 2) {
-      const bool odd = sub & 1;
-      const float rv = kFlat ? __fdiv_rn(odd ? D : qa, odd ? qa : D) : __fdiv_rn(odd ? qb : qa, D);
-      const float o = __shfl_xor_sync(kFull, rv, 1);
-      r0 = odd ? o : rv;
-      r1 = odd ? rv : o;
+    float qz = mn, meta = D;  // the quantiser's zero; the scales field (ranked)
+    if constexpr (kW) {
+      // wire: zero = the fp16 value below the minimum; the smallest covering fp16 scale of
+      // each width (a pair of lanes shares the two); ranked, the scales field keeps the
+      // maximum (the select derives the scale of the tile's width from zero and maximum)
+      qz = wire_zero(mn);
+      if constexpr (kFlat) {
+        r1 = wire_scale(qz, mx, qa);
+        r0 = wire_inv(r1);
+      } else if constexpr (LPT >= 2) {
+        const bool odd = sub & 1;
+        const float iv = wire_inv(wire_scale(qz, mx, odd ? qb : qa));
+        const float o = __shfl_xor_sync(kFull, iv, 1);
+        r0 = odd ? o : iv;
+        r1 = odd ? iv : o;
+      } else {
+        r0 = wire_inv(wire_scale(qz, mx, qa));
+        r1 = wire_inv(wire_scale(qz, mx, qb));
+      }
+      meta = mx;
     } else {
-      r0 = __fdiv_rn(qa, D);
-      r1 = kFlat ? __fdiv_rn(D, qa) : __fdiv_rn(qb, D);
+      if constexpr (LPT >= 2) {
+        const bool odd = sub & 1;
+        const float rv = kFlat ? __fdiv_rn(odd ? D : qa, odd ? qa : D) : __fdiv_rn(odd ? qb : qa, D);
+        const float o = __shfl_xor_sync(kFull, rv, 1);
+        r0 = odd ? o : rv;
+        r1 = odd ? rv : o;
+      } else {
+        r0 = __fdiv_rn(qa, D);
+        r1 = kFlat ? __fdiv_rn(D, qa) : __fdiv_rn(qb, D);
+      }
+      if (!(D >= 0x1p-120f)) r0 = r1 = 0.0f;
     }
-    if (!(D >= 0x1p-120f)) r0 = r1 = 0.0f;
     float2 u[16];
-    const float2 nmn = make_float2(-mn, -mn);
+    const float2 nmn = make_float2(-qz, -qz);
 #pragma unroll
     for (int j = 0; j < 16; j++) u[j] = add2(make_float2(v[2 * j], v[2 * j + 1]), nmn);
     if (valid) {
       if constexpr (kFlat) {
         unsigned char* dst = out_lo + (size_t)kt * (G * kB / 8) + sub * (4 * kB);
         quant_run<kB, kB == 4 ? 16 : 4>(u, r0, dst);
-        if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, r1, true);
+        if (sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)0xFF, r1, true);
       } else {
         quant_run<3, 4>(u, r0, out_lo + (size_t)kt * (G * 3 / 8) + sub * 12);
         quant_run<4, 16>(u, r1, out_hi + (size_t)kt * (G / 2) + sub * 16);
-        if (sub == 0) put_meta(p, t0 + kt, mn, (uint8_t)0xFF, D, false);
+        if (sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)0xFF, meta, false);
       }
     }
     if (deferred && sub == 0) s.dl[atomicAdd(&s.ndef[sl], 1u)] = (uint16_t)kt;
@@ -434,7 +470,7 @@ __device__ __forceinline__ void issue_run_chunk(RunSmem<Tin, G>& s, const EncPar
 // The chunks blockIdx.x, + gridDim.x, ... of the input, each copied in while the one
 // before is processed: the main pass, one block barrier, the exact path of the chunk's
 // deferred tiles (spread over the block's warps).
-template <typename Tin, int G, bool kFlat, int kB>
+template <typename Tin, int G, bool kFlat, int kB, bool kW>
 __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -480,9 +516,9 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts
@@ -497,7 +533,7 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
 // block's warps).  kDyn: chunks handed out in increasing order by an atomic ticket
 // (faster blocks take more); else blockIdx.x, + gridDim.x, ... (measured faster for the
 // ranked pass, whose blocks all write the same group's histograms).
-template <typename Tin, int G, bool kFlat, int kB, bool kDyn>
+template <typename Tin, int G, bool kFlat, int kB, bool kDyn, bool kW>
 __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -558,9 +594,9 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts (the loop ended after a barrier)
@@ -569,21 +605,23 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
   }
 }
 
-// Every tile gets the same width kB (K = 0 or K = n_g): codes at t G kB / 8.
-template <typename Tin, int G, int kB>
+// Every tile gets the same width kB (K = 0 or K = n_g): codes at t G kB / 8.  kW: the
+// wire format's quantiser.
+template <typename Tin, int G, int kB, bool kW>
 __global__ void __launch_bounds__(kThreads, 3) k_run_flat(const __grid_constant__ EncParams p,
                                                           long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  run_chunks_dyn<Tin, G, true, kB, true>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks_dyn<Tin, G, true, kB, true, kW>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // Stage 1 of widths {3, 4} ranked per group: keys, histograms, both widths into scratch.
-template <typename Tin, int G>
+// kW: the wire format's quantiser.
+template <typename Tin, int G, bool kW>
 __global__ void __launch_bounds__(kThreads, 3) k_run_tiles(const __grid_constant__ EncParams p,
                                                            long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   dep_launch();
-  run_chunks<Tin, G, false, 0>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks<Tin, G, false, 0, kW>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // ------------------------------------------------------------------ stage 2: the select
@@ -684,11 +722,18 @@ struct SelSmem {
   uint32_t last;
 };
 
-// Width b of tile t and its scale D / Q_b (D is what the tiles pass left in scales).
-__device__ __forceinline__ void put_width(const EncParams& p, long long t, bool hi, float D) {
+// Width b of tile t and its scale: D / Q_b (D is what the tiles pass left in scales), or
+// kW: the smallest fp16 scale covering [zero, x] at Q_b steps (x the tile's maximum).
+template <bool kW>
+__device__ __forceinline__ void put_width(const EncParams& p, long long t, bool hi, float D,
+                                          float zero) {
   const int b = hi ? 4 : 3;
   p.bits[t] = (uint8_t)b;
-  p.scales[t] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
+  if constexpr (kW) {
+    p.scales[t] = wire_scale(zero, D, qmax_f(b));
+  } else {
+    p.scales[t] = (D >= 0x1p-120f) ? __fdiv_rn(D, qmax_f(b)) : 0.0f;
+  }
 }
 
 // Stage 2, blocks (group g, j): part j of the group, `per` tiles (a multiple of 32, at
@@ -701,7 +746,7 @@ __device__ __forceinline__ void put_width(const EncParams& p, long long t, bool 
 // last block ranks the candidates (the r-th largest rank key, r = K - tiles above the
 // window, is the group's threshold), gives them their widths, and turns the chunks' hi
 // counts into their byte offsets in the stream.
-template <typename Tin, int G>
+template <typename Tin, int G, bool kW>
 __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constant__ EncParams p,
                                                          int J, long long per) {
   __shared__ __align__(16) SelSmem s;
@@ -720,12 +765,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constan
   constexpr int kB = kSelPart / kThreads;
   const float* kg = p.keys + g * p.n_g;
   const float* dg = p.scales + g * p.n_g;
-  float hv[kB], dv[kB];
+  float hv[kB], dv[kB], zv[kB];
 #pragma unroll
   for (int u = 0; u < kB; u++) {
     const long long i = lo + u * kThreads + threadIdx.x;
     hv[u] = i < hi ? __ldcg(&kg[i]) : 0.0f;
     dv[u] = i < hi ? __ldcg(&dg[i]) : 0.0f;
+    zv[u] = (kW && i < hi) ? __ldcg(&p.zeros[g * p.n_g + i]) : 0.0f;
   }
   const uint32_t* hf = p.hist_fine + g * (long long)kFineBins;
   if (warp == 0) {
@@ -777,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constan
     const bool in = i < hi;
     const bool hit = in && fbin >= blo && fbin <= bhi;
     const bool above = in && fbin > bhi;
-    if (in && !hit) put_width(p, g * p.n_g + i, above, dv[u]);
+    if (in && !hit) put_width<kW>(p, g * p.n_g + i, above, dv[u], zv[u]);
     const unsigned hm = __ballot_sync(kFull, above);
     if (lane == 0 && iw < hi) {
       segmask[iw >> 5] = hm;  // the candidates' bits follow in the last block
@@ -954,7 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constan
     const unsigned long long v = staged ? ck[i] : __ldcg(&cg[i]);
     const uint32_t tl = 0xFFFFFFFFu - (uint32_t)v;
     const bool ishi = v >= theta;
-    put_width(p, g * p.n_g + tl, ishi, __ldcg(&p.scales[g * p.n_g + tl]));
+    put_width<kW>(p, g * p.n_g + tl, ishi, __ldcg(&p.scales[g * p.n_g + tl]),
+                  kW ? __ldcg(&p.zeros[g * p.n_g + tl]) : 0.0f);
     if (ishi) {
       atomicOr(&segmask[tl >> 5], 1u << (tl & 31));
       atomicAdd(&words[tl / p.CHC], 1ull);
