@@ -289,11 +289,13 @@ tahq_status tahq_get_device_status(const void *workspace, uint32_t *status_out, 
  * tahq_encode_scaled: the codec of tahq_encode_ex (tau as there, allocation tile = tile)
  * applied to RN(scale_c * x), with scale_c a positive finite power of two (so the scaling
  * is exact unless scale_c * x leaves the normal float range; bf16 inputs stay bf16).  The
- * outputs describe scale_c * x: scales and zeros are those of the scaled values.  The
- * scaled copy of x is written into the workspace after the codec's own part, so the
- * workspace must hold tahq_scaled_workspace_size() bytes (0 on invalid arguments).
- * tahq_decode_scaled: tahq_decode followed by out = RN(out / scale_c) (the same workspace
- * as tahq_decode).  Errors as for tahq_encode / tahq_decode; a scale_c that is not a
+ * outputs describe scale_c * x: scales and zeros are those of the scaled values.  On the
+ * streaming encoder's shapes (tau = 2, tiles of 32..128 values, groups of whole 32 KB
+ * input chunks) the kernels read the scaled values directly; otherwise a scaled copy of x
+ * is written into the workspace after the codec's own part.  Either way the workspace
+ * must hold tahq_scaled_workspace_size() bytes (0 on invalid arguments).
+ * tahq_decode_scaled: tahq_decode with every output value RN(value / scale_c) (the
+ * decoder multiplies by 1 / scale_c as it stores; the same workspace as tahq_decode).  Errors as for tahq_encode / tahq_decode; a scale_c that is not a
  * positive finite power of two gives TAHQ_ERR_ARG.
  */
 size_t tahq_scaled_workspace_size(int64_t tokens, int64_t channels, int tile, int hblock,

@@ -220,7 +220,8 @@ tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
                         int tile, int hblock, int bits_lo, int bits_hi, float budget,
                         int64_t tokens_per_group, float tau, int alloc_tile, bool wire,
                         uint8_t* codes, float* scales, float* zeros, uint8_t* bits,
-                        uint8_t* pivots, void* workspace, size_t workspace_bytes, void* stream) {
+                        uint8_t* pivots, void* workspace, size_t workspace_bytes, void* stream,
+                        float scale_c = 1.0f) {
   if (!(tau >= 0.0f)) return TAHQ_ERR_ARG;  // negative or NaN
   if (alloc_tile < 0) return TAHQ_ERR_ARG;
   Shape s;
@@ -292,7 +293,10 @@ tahq_status encode_impl(const void* x, tahq_dtype dtype, int64_t tokens, int64_t
   a.scratch_hi = at<uint8_t>(workspace, L.scratch_hi);
   a.items = at<unsigned long long>(workspace, L.items);
   a.items_cap = (long long)L.items_cap;
-  return tahq::launch_encode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+  a.scale_c = scale_c;
+  const cudaError_t e = tahq::launch_encode(a, cs);
+  if (e == cudaErrorNotYetImplemented) return TAHQ_ERR_UNSUPPORTED;  // scale_c off the streaming path
+  return e == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -333,7 +337,8 @@ namespace {
 tahq_status decode_impl(const uint8_t* codes, size_t codes_bytes, const float* scales,
                         const float* zeros, const uint8_t* bits, const uint8_t* pivots,
                         int64_t tokens, int64_t channels, int tile, int hblock, float* out,
-                        void* workspace, size_t workspace_bytes, void* stream, bool clear) {
+                        void* workspace, size_t workspace_bytes, void* stream, bool clear,
+                        float inv_c = 1.0f) {
   Shape s;
   tahq_status st = check_shape(tokens, channels, tile, hblock, s);
   if (st != TAHQ_OK) return st;
@@ -369,6 +374,7 @@ tahq_status decode_impl(const uint8_t* codes, size_t codes_bytes, const float* s
   a.ticket = at<uint32_t>(workspace, L.ticket);
   a.ctot = at<uint32_t>(workspace, L.ctot);
   a.bsum = at<unsigned long long>(workspace, L.bsum);
+  a.inv_c = inv_c;
   return tahq::launch_decode(a, cs) == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
 }
 
@@ -418,19 +424,6 @@ __global__ void k_scale_input(const uint4* __restrict__ x, uint4* __restrict__ y
   }
 }
 
-// out = RN(out / c) in place (= out x (1 / c), both exact powers of two).
-__global__ void k_unscale(float4* __restrict__ out, long long n4, float inv_c) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (long long)gridDim.x * blockDim.x) {
-    float4 v = out[i];
-    v.x = __fmul_rn(v.x, inv_c);
-    v.y = __fmul_rn(v.y, inv_c);
-    v.z = __fmul_rn(v.z, inv_c);
-    v.w = __fmul_rn(v.w, inv_c);
-    out[i] = v;
-  }
-}
-
 unsigned stream_blocks(long long n) {
   const int sms = num_sms_current();
   return (unsigned)std::max<long long>(1, std::min<long long>((n + 255) / 256, (long long)std::max(sms, 1) * 8));
@@ -464,6 +457,11 @@ tahq_status tahq_encode_scaled(const void* x, tahq_dtype dtype, int64_t tokens, 
   if (!workspace || !aligned(workspace, kAlign)) return TAHQ_ERR_WORKSPACE;
   if (workspace_bytes < ws + align_up(nbytes)) return TAHQ_ERR_WORKSPACE;
   if (nbytes && (!x || !aligned(x, 16))) return TAHQ_ERR_ARG;
+  // the streaming encoder reads RN(c x) itself; the other encoders read a scaled copy
+  const tahq_status direct = encode_impl(x, dtype, tokens, channels, tile, hblock, bits_lo, bits_hi,
+                                         budget, tokens_per_group, tau, 0, false, codes, scales,
+                                         zeros, bits, pivots, workspace, ws, stream, scale_c);
+  if (direct != TAHQ_ERR_UNSUPPORTED) return direct;
   void* xs = static_cast<unsigned char*>(workspace) + ws;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (nbytes) {  // channels are a multiple of 8, so the tensor is whole 16-byte units
@@ -487,15 +485,9 @@ tahq_status tahq_decode_scaled(const uint8_t* codes, size_t codes_bytes, const f
                                float scale_c, float* out, void* workspace,
                                size_t workspace_bytes, void* stream) {
   if (!power_of_two(scale_c)) return TAHQ_ERR_ARG;
-  const tahq_status st = decode_impl(codes, codes_bytes, scales, zeros, bits, pivots, tokens,
-                                     channels, tile, hblock, out, workspace, workspace_bytes,
-                                     stream, true);
-  if (st != TAHQ_OK) return st;
-  const long long n4 = tokens * channels / 4;
-  if (n4 == 0) return TAHQ_OK;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  k_unscale<<<stream_blocks(n4), 256, 0, cs>>>(reinterpret_cast<float4*>(out), n4, 1.0f / scale_c);
-  return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+  // RN(decode / c) = decode x (1 / c), applied by the decoder to every value it stores
+  return decode_impl(codes, codes_bytes, scales, zeros, bits, pivots, tokens, channels, tile,
+                     hblock, out, workspace, workspace_bytes, stream, true, 1.0f / scale_c);
 }
 
 // ------------------------------------------------------------------------ wire format

@@ -313,7 +313,8 @@ __device__ __forceinline__ int issue_chunk_bytes(const DecodeArgs& a, long long 
   return pad;
 }
 
-template <int G>
+// kS: every value stored as RN(value x a.inv_c) (the gradient codec's 1 / c).
+template <int G, bool kS>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(DecodeArgs a, long long n_chunks,
                                                         long long n_blocks) {
   using C = DecCfg<G>;
@@ -442,6 +443,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
 #pragma unroll
         for (int j = 0; j < V; j++) v[j] = 0.0f;
       }
+      if constexpr (kS) {
+#pragma unroll
+        for (int j = 0; j < V; j++) v[j] = __fmul_rn(v[j], a.inv_c);
+      }
       float4* o = reinterpret_cast<float4*>(outc + kt * G + sub * V);
       o[0] = make_float4(v[0], v[1], v[2], v[3]);
       o[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -467,6 +472,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<G>::kMinBlocks) k_decode(D
 #pragma unroll
       for (int j = 0; j < V; j++) v[j] = __fmul_rn(v[j], a.c_h);
       team_swap0<V>(v, piv, sub, lane - sub);
+      if constexpr (kS) {
+#pragma unroll
+        for (int j = 0; j < V; j++) v[j] = __fmul_rn(v[j], a.inv_c);
+      }
       if (valid) {
         float4* o = reinterpret_cast<float4*>(a.out + (t0 + kt) * G + sub * V);
         o[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -491,15 +500,18 @@ static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   // load, scan and unpack phases overlap
   const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   const size_t smem = sizeof(DecSmem<G>);
-  static const cudaError_t e_attr =
-      cudaFuncSetAttribute(k_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t e_attr = [smem] {
+    const cudaError_t e0 = cudaFuncSetAttribute(k_decode<G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e1 = cudaFuncSetAttribute(k_decode<G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return e0 != cudaSuccess ? e0 : e1;
+  }();
   if (e_attr != cudaSuccess) return e_attr;
   k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks, n_blocks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the unpack starts while the kernel before drains (dep_wait inside)
-  return launch_dependent(k_decode<G>, (unsigned)blocks, (unsigned)kDecThreads, smem, st, a, n_chunks,
-                          n_blocks);
+  return launch_dependent(a.inv_c != 1.0f ? k_decode<G, true> : k_decode<G, false>, (unsigned)blocks,
+                          (unsigned)kDecThreads, smem, st, a, n_chunks, n_blocks);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {

@@ -115,6 +115,7 @@ struct alignas(128) EncSmem {  // placed on a 1024-byte boundary (enc_smem)
 struct EncParams {
   TmaDesc tmap;  // line layout: the input as [rows of 128 bytes]
   unsigned long long wait_ns;  // bound of every wait (see mbar_wait / wait_counter)
+  float scale_c;               // streaming encoder: the input is read as RN(c x) (1: as it is)
   const void* x;
   long long n_tiles, n_g, n_groups, K, group_bytes, codes_bytes;
   long long nA, nC, CHC, J, lag, pre1, pre2, n_items;
@@ -2184,6 +2185,7 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   p.status = a.status;
   p.tabs = *a.tabs;
   p.wait_ns = a.wait_ns ? a.wait_ns : kWaitNs;
+  p.scale_c = a.scale_c;
   if constexpr (C::kLine) {
     const cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
     if (e != cudaSuccess) return e;
@@ -2206,12 +2208,18 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
     if (plain && flat && (p.flat_b == 3 || p.flat_b == 4)) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
+      // the wire quantiser and the scaled read are never asked for together
+      if (a.wire && a.scale_c != 1.0f) return cudaErrorInvalidValue;
+      const bool sc = a.scale_c != 1.0f;
       void (*kern)(EncParams, long long) =
-          a.wire ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, true> : k_run_flat<Tin, G, 4, true>)
-                 : (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false> : k_run_flat<Tin, G, 4, false>);
+          a.wire ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, true, false> : k_run_flat<Tin, G, 4, true, false>)
+          : sc   ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false, true> : k_run_flat<Tin, G, 4, false, true>)
+                 : (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false, false> : k_run_flat<Tin, G, 4, false, false>);
       static const cudaError_t e_attr = [smem_r] {
-        void (*ks[4])(EncParams, long long) = {k_run_flat<Tin, G, 3, false>, k_run_flat<Tin, G, 4, false>,
-                                               k_run_flat<Tin, G, 3, true>, k_run_flat<Tin, G, 4, true>};
+        void (*ks[6])(EncParams, long long) = {
+            k_run_flat<Tin, G, 3, false, false>, k_run_flat<Tin, G, 4, false, false>,
+            k_run_flat<Tin, G, 3, true, false>,  k_run_flat<Tin, G, 4, true, false>,
+            k_run_flat<Tin, G, 3, false, true>,  k_run_flat<Tin, G, 4, false, true>};
         for (auto k : ks) {
           const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
           if (e != cudaSuccess) return e;
@@ -2229,18 +2237,24 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       p.CHC = kEncMaxCC;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
       const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
+      if (a.wire && a.scale_c != 1.0f) return cudaErrorInvalidValue;
       static const cudaError_t e_attr = [smem_r] {
-        const cudaError_t e0 = cudaFuncSetAttribute(k_run_tiles<Tin, G, false>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-        const cudaError_t e1 = cudaFuncSetAttribute(k_run_tiles<Tin, G, true>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-        return e0 != cudaSuccess ? e0 : e1;
+        void (*ks[3])(EncParams, long long) = {k_run_tiles<Tin, G, false, false>,
+                                               k_run_tiles<Tin, G, true, false>,
+                                               k_run_tiles<Tin, G, false, true>};
+        for (auto k : ks) {
+          const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+          if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
       }();
       if (e_attr != cudaSuccess) return e_attr;
       if (a.wire) {
-        k_run_tiles<Tin, G, true><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+        k_run_tiles<Tin, G, true, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+      } else if (a.scale_c != 1.0f) {
+        k_run_tiles<Tin, G, false, true><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       } else {
-        k_run_tiles<Tin, G, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
+        k_run_tiles<Tin, G, false, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       }
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
@@ -2252,6 +2266,8 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       return launch_dependent(k_run_compact<G>, (unsigned)(a.n_groups * p.nC), kThreads, 0, st, p);
     }
   }
+  // only the streaming encoder reads its input scaled (the caller scales a copy for the rest)
+  if (a.scale_c != 1.0f) return cudaErrorNotYetImplemented;
   // a compaction chunk's per-tile arrays (3 bytes per tile) follow the shared state
   const size_t stages = flat ? 0 : 3 * kMaxCC;
   const size_t smem = sizeof(EncSmem<Tin, G>) + 1024 + stages;

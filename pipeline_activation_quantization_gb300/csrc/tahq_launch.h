@@ -18,6 +18,7 @@ struct EncodeArgs {
   float c_h;                 // RN(1/sqrt(h))
   float tau;                 // outlier threshold: transform where r > tau (>= 0, +inf: never)
   bool wire;                 // fp16 zero and scales of the wire format (else the fp32 quantiser)
+  float scale_c = 1.0f;      // streaming encoder only: the codec sees RN(c x) (c a power of two)
   int mlog;                  // allocation tiles of 2^mlog tiles (one key each); K counts them
   long long n_tiles, n_g, n_groups, K, group_bytes;
   int num_sms;
@@ -66,6 +67,7 @@ struct DecodeArgs {
   uint32_t* ctot;                // [decode_chunks] chunk offset inside its block of 8 chunks
   unsigned long long* bsum;      // [decode_blocks + 1] stream offset of each block of 8
                                  // chunks, then the end of the last slot
+  float inv_c = 1.0f;            // every output value is RN(value x inv_c) (a power of two)
 };
 
 // Encode geometry: bytes of input per tiles item; tiles per compaction chunk, at most.

@@ -12,16 +12,18 @@
 // packed least significant bit first at b bits; decode RN(fma(q, scale, mn) / c).  c is a
 // power of two, so the scaling is exact unless c g leaves the normal float range.
 //
-// A warp takes four consecutive tiles at a time (G = 32, 64 or 128: V = G / 32 values a
-// lane, positions lane * V ...), every load of the four in flight first.  Encode stages a
-// tile's codes in shared memory and writes each 32-bit word of the slot from the codes it
-// covers; decode extracts each code from the one or two words it spans.  Both are streams
-// bound by HBM (4 bytes read and b / 8 written an element, or the reverse).
+// Encode: a warp takes eight consecutive tiles at a time (G = 32, 64 or 128: V = G / 32
+// values a lane, positions lane * V ...), every load in flight first; it stores a lane's
+// codes straight from registers when they make whole bytes, else composes the slot's
+// words in shared memory.  Decode: a thread takes groups of 4 consecutive values, a warp
+// 32 consecutive groups.  Both are streams bound by HBM (4 bytes read and b / 8 written an
+// element, or the reverse).
 #include <algorithm>
 #include <cmath>
 
 #include "../../include/tahq.h"
 #include "tahq_device.cuh"
+#include "tahq_tile.cuh"
 
 namespace tahq {
 namespace {
@@ -144,51 +146,153 @@ __global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_encode(const float* 
   }
 }
 
+// Encode at widths B = 4, 8, 16, where 16 codes make whole 8-, 16- or 32-byte fields:
+// thread i takes groups of 16 consecutive values (group i, i + S, ...; kEncGroups in
+// flight), a tile is G / 16 consecutive lanes (team reductions for its range), and a
+// lane stores its 16 codes with one or two vector stores.
+constexpr int kEncGroups = 2;
+constexpr int kEncBlockThreads = 256;
+
+template <int G, int B>
+__global__ void __launch_bounds__(kEncBlockThreads) k_naive_encode16(const float* __restrict__ g,
+                                                                     long long n_tiles, float c,
+                                                                     uint8_t* codes, float* scales,
+                                                                     float* zeros) {
+  constexpr int L = G / 16;  // lanes a tile
+  constexpr uint32_t Q = (1u << B) - 1u;
+  const float Qf = (float)Q, cut = naive_cutoff(B);
+  const int lane = threadIdx.x & 31, sub = lane % L;
+  const long long n16 = n_tiles * L;  // groups of 16 values
+  const long long S = (long long)gridDim.x * kEncBlockThreads;  // a multiple of 32
+  for (long long i0 = (long long)blockIdx.x * kEncBlockThreads + threadIdx.x; i0 - lane < n16;
+       i0 += S * kEncGroups) {  // the loop condition is warp-uniform
+    float v[kEncGroups][16];
+#pragma unroll
+    for (int u = 0; u < kEncGroups; u++) {
+      const long long i = i0 + u * S;
+      const float4* src = reinterpret_cast<const float4*>(g) + 4 * (i < n16 ? i : 0);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const float4 q = __ldcs(src + k);
+        v[u][4 * k] = q.x;
+        v[u][4 * k + 1] = q.y;
+        v[u][4 * k + 2] = q.z;
+        v[u][4 * k + 3] = q.w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kEncGroups; u++) {
+      const long long i = i0 + u * S;
+      float mn, mx;
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        v[u][j] = __fmul_rn(c, v[u][j]);
+        mn = j ? fminf(mn, v[u][j]) : v[u][j];
+        mx = j ? fmaxf(mx, v[u][j]) : v[u][j];
+      }
+#pragma unroll
+      for (int o = 1; o < L; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      }
+      const float D = __fsub_rn(mx, mn);
+      const bool live = D >= cut;
+      // lane 0 of the tile: Q / D; lane 1: D / Q (the scale)
+      const float r = (sub & 1) ? __fdiv_rn(D, Qf) : __fdiv_rn(Qf, D);
+      const float o = __shfl_xor_sync(kFull, r, 1);
+      const float inv = live ? ((sub & 1) ? o : r) : 0.0f;
+      const float scale = live ? ((sub & 1) ? r : o) : 0.0f;
+      uint32_t w[B / 2];  // 16 codes of B bits
+#pragma unroll
+      for (int k = 0; k < B / 2; k++) w[k] = 0u;
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        uint32_t q = __float_as_uint(__fmaf_rn(__fsub_rn(v[u][j], mn), inv, 12582912.0f)) - 0x4B400000u;
+        q = live ? min(q, Q) : 0u;
+        w[(j * B) / 32] |= q << ((j * B) % 32);
+      }
+      if (i < n16) {
+        uint8_t* dst = codes + i * (2 * B);
+        if constexpr (B == 4) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < B / 2; k += 4)
+            *reinterpret_cast<uint4*>(dst + 4 * k) = make_uint4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+        }
+        if (sub == 0) {
+          const long long t = i / L;
+          scales[t] = scale;
+          zeros[t] = __fadd_rn(mn, 0.0f);  // a zero minimum as +0
+        }
+      }
+    }
+  }
+}
+
+// Decode: thread i takes groups of 4 consecutive values (group i, i + S, ..., S the grid's
+// threads; kDecGroups of them in flight), so that a warp's stores are 512 contiguous
+// bytes and its code loads 32 consecutive words or so.  The 4 codes of group k start at
+// bit 4 k b: one word at b = 8, else a 64-bit window of up to three words (b <= 16).
+constexpr int kDecGroups = 4;
+constexpr int kDecBlockThreads = 256;
+
 template <int G>
-__global__ void __launch_bounds__(32 * kNaiveWarps) k_naive_decode(const uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(kDecBlockThreads) k_naive_decode(const uint8_t* __restrict__ codes,
                                                                    const float* __restrict__ scales,
                                                                    const float* __restrict__ zeros,
                                                                    long long n_tiles, int b, float c,
                                                                    float* out) {
-  constexpr int V = G / 32;
-  constexpr int kDecTiles = 4;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
+  const long long n4 = n_tiles * (G / 4);                    // groups of 4 values
+  const long long n_words = (n_tiles * G * (long long)b + 31) / 32;
   const uint32_t mask = (1u << b) - 1u;
   const float inv_c = 1.0f / c;  // c is a power of two: RN(y / c) = y * (1 / c)
-  const long long stride = (long long)gridDim.x * kNaiveWarps * kDecTiles;
-  for (long long t0 = ((long long)blockIdx.x * kNaiveWarps + warp) * kDecTiles; t0 < n_tiles;
-       t0 += stride) {
-    const int nu = (int)min((long long)kDecTiles, n_tiles - t0);
-    uint32_t qv[kDecTiles][V];
-    float sc[kDecTiles], z[kDecTiles];
+  const float2 ic2 = make_float2(inv_c, inv_c), m2 = make_float2(-8388608.0f, -8388608.0f);
+  const long long S = (long long)gridDim.x * kDecBlockThreads;
+  for (long long i0 = (long long)blockIdx.x * kDecBlockThreads + threadIdx.x; i0 < n4;
+       i0 += S * kDecGroups) {
+    unsigned long long v64[kDecGroups];
+    float sc[kDecGroups], z[kDecGroups];
 #pragma unroll
-    for (int u = 0; u < kDecTiles; u++) {
-      if (u >= nu) break;
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + (t0 + u) * (long long)(G * b / 8));
-      sc[u] = __ldg(scales + t0 + u);
-      z[u] = __ldg(zeros + t0 + u);
-#pragma unroll
-      for (int j = 0; j < V; j++) {
-        const int bit = (lane * V + j) * b, w = bit >> 5, sh = bit & 31;
-        uint32_t q = __ldg(src + w) >> sh;
-        if (sh + b > 32) q |= __ldg(src + w + 1) << (32 - sh);
-        qv[u][j] = q & mask;
+    for (int u = 0; u < kDecGroups; u++) {
+      const long long i = i0 + u * S;
+      v64[u] = 0ull;
+      sc[u] = z[u] = 0.0f;
+      if (i < n4) {
+        const long long t = i / (G / 4);
+        sc[u] = __ldg(scales + t);
+        z[u] = __ldg(zeros + t);
+        if (b == 8) {
+          v64[u] = __ldg(cw + i);
+        } else {
+          const long long bit = i * 4 * (long long)b, w = bit >> 5;
+          const int sh = (int)(bit & 31);
+          const uint32_t w0 = __ldg(cw + w);
+          const uint32_t w1 = w + 1 < n_words ? __ldg(cw + w + 1) : 0u;
+          const uint32_t w2 = (sh + 4 * b > 64 && w + 2 < n_words) ? __ldg(cw + w + 2) : 0u;
+          v64[u] = ((unsigned long long)__funnelshift_r(w1, w2, sh) << 32) | __funnelshift_r(w0, w1, sh);
+        }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kDecTiles; u++) {
-      if (u >= nu) break;
-      float y[V];
+    for (int u = 0; u < kDecGroups; u++) {
+      const long long i = i0 + u * S;
+      if (i >= n4) break;
+      const float2 s2 = make_float2(sc[u], sc[u]), z2 = make_float2(z[u], z[u]);
+      float y[4];
 #pragma unroll
-      for (int j = 0; j < V; j++) y[j] = __fmul_rn(__fmaf_rn((float)qv[u][j], sc[u], z[u]), inv_c);
-      float* dst = out + (t0 + u) * G + lane * V;
-      if constexpr (V == 4) {
-        __stcs(reinterpret_cast<float4*>(dst), make_float4(y[0], y[1], y[2], y[3]));
-      } else if constexpr (V == 2) {
-        __stcs(reinterpret_cast<float2*>(dst), make_float2(y[0], y[1]));
-      } else {
-        __stcs(dst, y[0]);
+      for (int j = 0; j < 4; j += 2) {
+        const uint32_t c0 = (uint32_t)(v64[u] >> (j * b)) & mask;
+        const uint32_t c1 = (uint32_t)(v64[u] >> ((j + 1) * b)) & mask;
+        // (float)q exactly: the bits 0x4B000000 | q are 2^23 + q
+        const float2 qf = add2(make_float2(__uint_as_float(0x4B000000u | c0),
+                                           __uint_as_float(0x4B000000u | c1)), m2);
+        const float2 r = fma2(qf, s2, z2);
+        y[j] = __fmul_rn(r.x, ic2.x);
+        y[j + 1] = __fmul_rn(r.y, ic2.y);
       }
+      __stcs(reinterpret_cast<float4*>(out) + i, make_float4(y[0], y[1], y[2], y[3]));
     }
   }
 }
@@ -235,9 +339,28 @@ extern "C" tahq_status tahq_naive_encode(const float* grad, int64_t tokens, int6
   if (!aligned_to(grad, 16) || !aligned_to(codes, 16) || !aligned_to(scales, 4) ||
       !aligned_to(zeros, 4))
     return TAHQ_ERR_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (bits == 4 || bits == 8 || bits == 16) {  // 16 codes a lane make whole vector stores
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return TAHQ_ERR_CUDA;
+    const long long groups = n * (tile / 16), per = (long long)kEncBlockThreads * kEncGroups;
+    const int blocks16 = (int)std::max<long long>(1, std::min<long long>((groups + per - 1) / per, 8ll * sms));
+    using EncFn = void (*)(const float*, long long, float, uint8_t*, float*, float*);
+    EncFn k = nullptr;
+#define TAHQ_NAIVE16(GG)                                                                        \
+    if (tile == GG) k = bits == 4 ? k_naive_encode16<GG, 4> : bits == 8 ? k_naive_encode16<GG, 8> \
+                                                                        : k_naive_encode16<GG, 16>;
+    TAHQ_NAIVE16(32)
+    TAHQ_NAIVE16(64)
+    TAHQ_NAIVE16(128)
+#undef TAHQ_NAIVE16
+    k<<<blocks16, kEncBlockThreads, 0, cs>>>(grad, n, scale_c, codes, scales, zeros);
+    return cudaGetLastError() == cudaSuccess ? TAHQ_OK : TAHQ_ERR_CUDA;
+  }
   const int blocks = naive_blocks(n);
   if (blocks <= 0) return TAHQ_ERR_CUDA;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const dim3 grid(blocks), block(32 * kNaiveWarps);
   if (tile == 32) k_naive_encode<32><<<grid, block, 0, cs>>>(grad, n, bits, scale_c, codes, scales, zeros);
   if (tile == 64) k_naive_encode<64><<<grid, block, 0, cs>>>(grad, n, bits, scale_c, codes, scales, zeros);
@@ -258,10 +381,14 @@ extern "C" tahq_status tahq_naive_decode(const uint8_t* codes, const float* scal
   if (!aligned_to(codes, 16) || !aligned_to(out, 16) || !aligned_to(scales, 4) ||
       !aligned_to(zeros, 4))
     return TAHQ_ERR_ARG;
-  const int blocks = naive_blocks(n);
-  if (blocks <= 0) return TAHQ_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return TAHQ_ERR_CUDA;
+  const long long groups = n * (tile / 4), per = (long long)kDecBlockThreads * kDecGroups;
+  const int blocks = (int)std::max<long long>(1, std::min<long long>((groups + per - 1) / per, 8ll * sms));
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const dim3 grid(blocks), block(32 * kNaiveWarps);
+  const dim3 grid(blocks), block(kDecBlockThreads);
   if (tile == 32) k_naive_decode<32><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);
   if (tile == 64) k_naive_decode<64><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);
   if (tile == 128) k_naive_decode<128><<<grid, block, 0, cs>>>(codes, scales, zeros, n, bits, scale_c, out);

@@ -115,6 +115,28 @@ __device__ __forceinline__ void lds_run(const unsigned char* buf, int r, float* 
   }
 }
 
+// The input value x as the codec sees it when the caller asks for RN(c x) (the gradient
+// codec; c a power of two): bf16 inputs rounded back to bf16 (nearest, ties to even), as a
+// scaled bf16 copy of the input would hold them.
+template <bool kBf>
+__device__ __forceinline__ float scaled_in(float x, float c) {
+  const float y = __fmul_rn(x, c);
+  if constexpr (!kBf) {
+    return y;
+  } else {
+    const uint32_t u = __float_as_uint(y);
+    return __uint_as_float(((u + ((u >> 16) & 1u) + 0x7FFFu) >> 16) << 16);
+  }
+}
+
+template <typename Tin, int N, bool kS>
+__device__ __forceinline__ void scale_values(const EncParams& p, float* v) {
+  if constexpr (kS) {
+#pragma unroll
+    for (int j = 0; j < N; j++) v[j] = scaled_in<InTraits<Tin>::kBf16>(v[j], p.scale_c);
+  }
+}
+
 // min / max of the run and the largest magnitude of each group of 8 values.
 __device__ __forceinline__ void run_minmax(const float* v, float& mn, float& mx, float* ga) {
 #pragma unroll
@@ -224,7 +246,7 @@ __device__ __forceinline__ RunSmem<Tin, G>& run_smem(unsigned char* raw) {
 // keep the range D) or at width kB into out_lo (kFlat: the final scale).  kW: the wire
 // format's quantiser (zero = the fp16 value below the minimum, the smallest covering fp16
 // scale of each width); ranked, the scales field keeps the maximum.
-template <typename Tin, int G, bool kFlat, int kB, bool kW>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
 __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned char* src,
                                           const uint16_t* list, int first, int n, long long t0,
                                           unsigned char* out_lo, unsigned char* out_hi) {
@@ -257,6 +279,7 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
         for (int e = 0; e < 4; e++) v[4 * k + e] = __uint_as_float(wq[e]);
       }
     }
+    scale_values<Tin, V, kS>(p, v);
     float m1, m2;
     int i1;
     team_top2_values<V, L>(v, sub, m1, i1, m2);
@@ -338,7 +361,7 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
 // else keys, histograms and both widths into the scratch streams out_lo / out_hi.
 // Deferred tiles go to the list s.dl (s.ndef[k & 1] of them).  kW: the wire format's
 // quantiser (see pass2_run).
-template <typename Tin, int G, bool kFlat, int kB, bool kW>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
 __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p, long long g,
                                          long long t0, int nt, int k, unsigned char* out_lo,
                                          unsigned char* out_hi) {
@@ -353,6 +376,7 @@ __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p,
     const bool valid = kt < nt;
     float v[32];
     lds_run<Tin>(buf, r, v);
+    scale_values<Tin, 32, kS>(p, v);
     float mn, mx, ga[4];
     run_minmax(v, mn, mx, ga);
     mn = team_min<LPT>(mn);
@@ -470,7 +494,7 @@ __device__ __forceinline__ void issue_run_chunk(RunSmem<Tin, G>& s, const EncPar
 // The chunks blockIdx.x, + gridDim.x, ... of the input, each copied in while the one
 // before is processed: the main pass, one block barrier, the exact path of the chunk's
 // deferred tiles (spread over the block's warps).
-template <typename Tin, int G, bool kFlat, int kB, bool kW>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
 __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -516,9 +540,9 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB, kW>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW, kS>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB, kW>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW, kS>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts
@@ -533,7 +557,7 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
 // block's warps).  kDyn: chunks handed out in increasing order by an atomic ticket
 // (faster blocks take more); else blockIdx.x, + gridDim.x, ... (measured faster for the
 // ranked pass, whose blocks all write the same group's histograms).
-template <typename Tin, int G, bool kFlat, int kB, bool kDyn, bool kW>
+template <typename Tin, int G, bool kFlat, int kB, bool kDyn, bool kW, bool kS>
 __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -594,9 +618,9 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB, kW>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW, kS>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB, kW>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW, kS>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts (the loop ended after a barrier)
@@ -606,22 +630,22 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
 }
 
 // Every tile gets the same width kB (K = 0 or K = n_g): codes at t G kB / 8.  kW: the
-// wire format's quantiser.
-template <typename Tin, int G, int kB, bool kW>
+// wire format's quantiser; kS: the input read as RN(c x) (scaled_in).
+template <typename Tin, int G, int kB, bool kW, bool kS>
 __global__ void __launch_bounds__(kThreads, 3) k_run_flat(const __grid_constant__ EncParams p,
                                                           long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  run_chunks_dyn<Tin, G, true, kB, true, kW>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks_dyn<Tin, G, true, kB, true, kW, kS>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // Stage 1 of widths {3, 4} ranked per group: keys, histograms, both widths into scratch.
-// kW: the wire format's quantiser.
-template <typename Tin, int G, bool kW>
+// kW: the wire format's quantiser; kS: the input read as RN(c x) (scaled_in).
+template <typename Tin, int G, bool kW, bool kS>
 __global__ void __launch_bounds__(kThreads, 3) k_run_tiles(const __grid_constant__ EncParams p,
                                                            long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   dep_launch();
-  run_chunks<Tin, G, false, 0, kW>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks<Tin, G, false, 0, kW, kS>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // ------------------------------------------------------------------ stage 2: the select
@@ -711,6 +735,23 @@ __device__ __forceinline__ uint4 warp_tile_raw(const EncParams& p, long long t) 
 // histogram when they are at most kRankHist (their rank keys and 4096 bins fill 32 KB).
 constexpr int kSelPart = 2048;
 constexpr uint32_t kRankHist = 2048;
+
+// A lane's raw input bytes (warp_tile_raw) read as RN(c x) (scaled_in).
+template <typename Tin>
+__device__ __forceinline__ uint4 scale_raw(uint4 r, float c) {
+  uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    if constexpr (!InTraits<Tin>::kBf16) {
+      w[k] = __float_as_uint(scaled_in<false>(__uint_as_float(w[k]), c));
+    } else {
+      const uint32_t lo = __float_as_uint(scaled_in<true>(__uint_as_float(w[k] << 16), c));
+      const uint32_t hi = __float_as_uint(scaled_in<true>(__uint_as_float(w[k] & 0xFFFF0000u), c));
+      w[k] = (lo >> 16) | (hi & 0xFFFF0000u);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 struct SelSmem {
   unsigned char buf[kChunkBytes];  // window tiles, then candidate rank keys
@@ -851,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constan
       for (int q = 0; q < kF; q++) {
         const int i = i0 + q;
         raw[q] = i < n ? warp_tile_raw<Tin, G>(p, g * p.n_g + list[i]) : make_uint4(0u, 0u, 0u, 0u);
+        if (p.scale_c != 1.0f) raw[q] = scale_raw<Tin>(raw[q], p.scale_c);
       }
       uint32_t tl_mine = 0u;
       float h_mine = 0.0f;
