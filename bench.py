@@ -527,8 +527,7 @@ def run_gpu(args):
     n_g_t = (w.tokens_per_group or T) * (C // G)
     ch = 32768 // (G * esize)
     flat_b = w.bits_lo if K_hi == 0 else w.bits_hi
-    streaming = ((args.tau is None or args.tau == 2.0)
-                 and args.alloc_tile in (0, G) and 32 <= G <= 128
+    streaming = (args.alloc_tile in (0, G) and 32 <= G <= 128
                  and (n_tiles * G * esize) % 128 == 0 and (n_g_t * G) % 128 == 0)
     run_flat = streaming and not ranked and flat_b in (3, 4)
     run_ranked = (streaming and ranked and (w.bits_lo, w.bits_hi) == (3, 4)

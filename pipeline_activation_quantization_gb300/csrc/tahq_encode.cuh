@@ -2194,68 +2194,68 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
   const bool flat = a.K == 0 || a.K == (a.n_g >> a.mlog);
   p.flat_b = a.K == 0 ? a.lo : a.hi;
   if constexpr (G >= 32 && G <= 128) {
-    // the streaming encoder: the method's defaults (tau = 2, A = G; fp32 metadata or the
-    // wire format's quantiser), one width of 3 or 4 bits, or widths {3, 4} ranked per group
-    // of whole input chunks; the input in 128-byte rows
+    // the streaming encoder: A = G, any tau (compiled for tau = 2 and for the rest), fp32
+    // metadata or the wire format's quantiser, one width of 3 or 4 bits, or widths {3, 4}
+    // ranked per group of whole input chunks; the input in 128-byte rows
     const long long esz = (long long)sizeof(Tin);
     const bool rows = (a.n_tiles * G * esz) % 128 == 0 && (a.n_g * G) % 128 == 0 &&
                       a.n_tiles < (1ll << 31);
-    const bool plain = a.tau == 2.0f && a.mlog == 0 && rows;
+    const bool plain = a.mlog == 0 && rows;
+    const bool t2 = a.tau == 2.0f;
+    // the scaled read is compiled for tau = 2 without the wire quantiser
+    const bool ok_mode = a.scale_c == 1.0f || (t2 && !a.wire);
     const size_t smem_r = sizeof(RunSmem<Tin, G>) + 1024;
     const long long n_chunks = (a.n_tiles + C::CH - 1) / C::CH;
     // three blocks an SM (<= 80 registers, two 32 KB stages each)
     const int grid_r = (int)std::max<long long>(1, std::min<long long>(3ll * a.num_sms, n_chunks));
-    if (plain && flat && (p.flat_b == 3 || p.flat_b == 4)) {
+    if (plain && ok_mode && flat && (p.flat_b == 3 || p.flat_b == 4)) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
-      // the wire quantiser and the scaled read are never asked for together
-      if (a.wire && a.scale_c != 1.0f) return cudaErrorInvalidValue;
-      const bool sc = a.scale_c != 1.0f;
-      void (*kern)(EncParams, long long) =
-          a.wire ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, true, false> : k_run_flat<Tin, G, 4, true, false>)
-          : sc   ? (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false, true> : k_run_flat<Tin, G, 4, false, true>)
-                 : (p.flat_b == 3 ? k_run_flat<Tin, G, 3, false, false> : k_run_flat<Tin, G, 4, false, false>);
+      // modes (wire, scaled, tau = 2): plain, wire, scaled at tau = 2; plain, wire at any tau
+      using FlatFn = void (*)(EncParams, long long);
+      static const FlatFn fl[2][5] = {
+          {k_run_flat<Tin, G, 3, false, false, true>, k_run_flat<Tin, G, 3, true, false, true>,
+           k_run_flat<Tin, G, 3, false, true, true>, k_run_flat<Tin, G, 3, false, false, false>,
+           k_run_flat<Tin, G, 3, true, false, false>},
+          {k_run_flat<Tin, G, 4, false, false, true>, k_run_flat<Tin, G, 4, true, false, true>,
+           k_run_flat<Tin, G, 4, false, true, true>, k_run_flat<Tin, G, 4, false, false, false>,
+           k_run_flat<Tin, G, 4, true, false, false>}};
+      const int mode = t2 ? (a.wire ? 1 : a.scale_c != 1.0f ? 2 : 0) : (a.wire ? 4 : 3);
+      FlatFn kern = fl[p.flat_b == 3 ? 0 : 1][mode];
       static const cudaError_t e_attr = [smem_r] {
-        void (*ks[6])(EncParams, long long) = {
-            k_run_flat<Tin, G, 3, false, false>, k_run_flat<Tin, G, 4, false, false>,
-            k_run_flat<Tin, G, 3, true, false>,  k_run_flat<Tin, G, 4, true, false>,
-            k_run_flat<Tin, G, 3, false, true>,  k_run_flat<Tin, G, 4, false, true>};
-        for (auto k : ks) {
-          const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
-          if (e != cudaSuccess) return e;
-        }
+        for (const auto& row : fl)
+          for (FlatFn k : row) {
+            const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
+            if (e != cudaSuccess) return e;
+          }
         return cudaSuccess;
       }();
       if (e_attr != cudaSuccess) return e_attr;
       kern<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       return cudaGetLastError();
     }
-    if (plain && !flat && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0 &&
+    if (plain && ok_mode && !flat && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0 &&
         (a.n_g + kEncMaxCC - 1) / kEncMaxCC <= 64 * 256 && a.group_bytes < (1ll << 31)) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
       p.CHC = kEncMaxCC;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
       const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
-      if (a.wire && a.scale_c != 1.0f) return cudaErrorInvalidValue;
+      // modes as for the one-width pass
+      using TilesFn = void (*)(EncParams, long long);
+      static const TilesFn tl[5] = {k_run_tiles<Tin, G, false, false, true>, k_run_tiles<Tin, G, true, false, true>,
+                                    k_run_tiles<Tin, G, false, true, true>, k_run_tiles<Tin, G, false, false, false>,
+                                    k_run_tiles<Tin, G, true, false, false>};
       static const cudaError_t e_attr = [smem_r] {
-        void (*ks[3])(EncParams, long long) = {k_run_tiles<Tin, G, false, false>,
-                                               k_run_tiles<Tin, G, true, false>,
-                                               k_run_tiles<Tin, G, false, true>};
-        for (auto k : ks) {
+        for (TilesFn k : tl) {
           const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_r);
           if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
       }();
       if (e_attr != cudaSuccess) return e_attr;
-      if (a.wire) {
-        k_run_tiles<Tin, G, true, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
-      } else if (a.scale_c != 1.0f) {
-        k_run_tiles<Tin, G, false, true><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
-      } else {
-        k_run_tiles<Tin, G, false, false><<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
-      }
+      const int mode = t2 ? (a.wire ? 1 : a.scale_c != 1.0f ? 2 : 0) : (a.wire ? 4 : 3);
+      tl[mode]<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       e = launch_dependent(a.wire ? k_run_select<Tin, G, true> : k_run_select<Tin, G, false>,

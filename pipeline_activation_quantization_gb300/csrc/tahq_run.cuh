@@ -1,6 +1,7 @@
-// tahq_run.cuh -- the streaming encoder of the TAH-Quant activation codec for the
-// method's defaults (widths {3, 4}, tau = 2, A = G, fp32 metadata) on tiles of 32, 64
-// or 128 values (included by tahq_encode.cuh, after the work-queue items it reuses).
+// tahq_run.cuh -- the streaming encoder of the TAH-Quant activation codec for widths
+// {3, 4} (or one width of 3 or 4 bits), one key per quantisation tile (A = G), any tau,
+// fp32 or wire metadata, on tiles of 32, 64 or 128 values (included by tahq_encode.cuh,
+// after the work-queue items it reuses).
 //
 // "TAH-Quant: Effective Activation Quantization in Pipeline Parallelism over Slow
 // Network" (arXiv 2506.01352v2): §3.2 eq. (1)-(2) entropy keys and "Top-p% tile
@@ -239,14 +240,14 @@ __device__ __forceinline__ RunSmem<Tin, G>& run_smem(unsigned char* raw) {
 // Deferred tiles list[first .. n) of a staged chunk (the pretest could not rule out
 // r > tau), teams of L = G / 8 lanes, 8 values a lane, several teams a warp and the list
 // spread over the block's warps.  The main pass has written every tile's codes and
-// metadata as untransformed; here the exact ratio test of eq. (3) runs (tau = 2 without
-// a division: RN(m1 / d) > 2 iff m1 / 2 - d > d 2^-24, d = RN(m2 + 1e-12), exact by
-// Sterbenz's lemma), and the tiles it flags get the pivot swap, the Hadamard of eq. (4),
+// metadata as untransformed; here the exact ratio test of eq. (3) runs (kT2, tau = 2,
+// without a division: RN(m1 / d) > 2 iff m1 / 2 - d > d 2^-24, d = RN(m2 + 1e-12), exact
+// by Sterbenz's lemma; else RN(m1 / d) > tau), and the tiles it flags get the pivot swap, the Hadamard of eq. (4),
 // a new range and new codes: at both widths into out_lo / out_hi (kFlat false: scales
 // keep the range D) or at width kB into out_lo (kFlat: the final scale).  kW: the wire
 // format's quantiser (zero = the fp16 value below the minimum, the smallest covering fp16
 // scale of each width); ranked, the scales field keeps the maximum.
-template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS, bool kT2>
 __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned char* src,
                                           const uint16_t* list, int first, int n, long long t0,
                                           unsigned char* out_lo, unsigned char* out_hi) {
@@ -284,7 +285,8 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
     int i1;
     team_top2_values<V, L>(v, sub, m1, i1, m2);
     const float d = __fadd_rn(m2, 1e-12f);
-    const bool flag = valid && __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f);
+    const bool flag = valid && (kT2 ? __fsub_rn(__fmul_rn(m1, 0.5f), d) > __fmul_rn(d, 0x1p-24f)
+                                    : __fdiv_rn(m1, d) > p.tau);
     if (!__any_sync(kFull, flag)) continue;  // the main pass's codes stand
     float t[V];
 #pragma unroll
@@ -361,7 +363,7 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
 // else keys, histograms and both widths into the scratch streams out_lo / out_hi.
 // Deferred tiles go to the list s.dl (s.ndef[k & 1] of them).  kW: the wire format's
 // quantiser (see pass2_run).
-template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS, bool kT2>
 __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p, long long g,
                                          long long t0, int nt, int k, unsigned char* out_lo,
                                          unsigned char* out_hi) {
@@ -382,15 +384,17 @@ __device__ __forceinline__ void main_run(RunSmem<Tin, G>& s, const EncParams& p,
     mn = team_min<LPT>(mn);
     mx = team_max<LPT>(mx);
     const float m1 = fmaxf(mx, -mn);
-    // two values of at least m1 / 2 (exact for m1 >= 2^-120) rule out r > 2
-    const float thr = __fmul_rn(m1, 0.5f);
+    // two values of at least m1 / tau rule out r > tau (tau = 2: an exact halving for
+    // m1 >= 2^-120; else m1 / tau rounded up)
+    const float thr = kT2 ? __fmul_rn(m1, 0.5f) : __fdiv_ru(m1, p.tau);
     uint32_t cnt = 0;
 #pragma unroll
     for (int q = 0; q < 4; q++) cnt += ga[q] >= thr ? 1u : 0u;
     cnt = team_sum_u<LPT>(cnt);
-    // below 2^-120 the ratio cannot exceed 2; a maximum that is not finite goes to the
-    // exact test
-    const bool deferred = valid && !(m1 < 0x1p-120f) && (!(m1 <= FLT_MAX) || cnt < 2u);
+    // below 2^-120 the ratio cannot exceed a tau >= 1 (m2 + 1e-12 > m1 / tau); a maximum
+    // that is not finite goes to the exact test
+    const bool small = (kT2 || p.tau >= 1.0f) && m1 < 0x1p-120f;
+    const bool deferred = valid && !small && (!(m1 <= FLT_MAX) || cnt < 2u);
     if constexpr (!kFlat) {
       // entropy key: approximate on tiles of moderate magnitude, canonical otherwise
       const bool special = !(m1 >= 0x1p-100f && m1 <= 0x1p100f);
@@ -494,7 +498,7 @@ __device__ __forceinline__ void issue_run_chunk(RunSmem<Tin, G>& s, const EncPar
 // The chunks blockIdx.x, + gridDim.x, ... of the input, each copied in while the one
 // before is processed: the main pass, one block barrier, the exact path of the chunk's
 // deferred tiles (spread over the block's warps).
-template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS>
+template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS, bool kT2>
 __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -540,9 +544,9 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB, kW, kS>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW, kS, kT2>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB, kW, kS>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW, kS, kT2>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts
@@ -557,7 +561,7 @@ __device__ __forceinline__ void run_chunks(RunSmem<Tin, G>& s, const EncParams& 
 // block's warps).  kDyn: chunks handed out in increasing order by an atomic ticket
 // (faster blocks take more); else blockIdx.x, + gridDim.x, ... (measured faster for the
 // ranked pass, whose blocks all write the same group's histograms).
-template <typename Tin, int G, bool kFlat, int kB, bool kDyn, bool kW, bool kS>
+template <typename Tin, int G, bool kFlat, int kB, bool kDyn, bool kW, bool kS, bool kT2>
 __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncParams& p,
                                            long long n_chunks) {
   constexpr int CH = RunGeom<Tin, G>::CH;
@@ -618,9 +622,9 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
     unsigned char* hi = kFlat ? lo : p.scratch_hi + t0 * slot_b;
     mbar_wait(&s.bar[sl], (parity >> sl) & 1u, p.status, p.wait_ns);
     parity ^= 1u << sl;
-    main_run<Tin, G, kFlat, kB, kW, kS>(s, p, g, t0, nt, k, lo, hi);
+    main_run<Tin, G, kFlat, kB, kW, kS, kT2>(s, p, g, t0, nt, k, lo, hi);
     csync();  // the list is complete, and the codes written before the exact path's
-    pass2_run<Tin, G, kFlat, kB, kW, kS>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
+    pass2_run<Tin, G, kFlat, kB, kW, kS, kT2>(p, s.buf[sl], s.dl, 0, (int)s.ndef[sl], t0, lo, hi);
     gp = g;
   }
   if (!kFlat && k) {  // the last chunk's coarse counts (the loop ended after a barrier)
@@ -630,22 +634,24 @@ __device__ __forceinline__ void run_chunks_dyn(RunSmem<Tin, G>& s, const EncPara
 }
 
 // Every tile gets the same width kB (K = 0 or K = n_g): codes at t G kB / 8.  kW: the
-// wire format's quantiser; kS: the input read as RN(c x) (scaled_in).
-template <typename Tin, int G, int kB, bool kW, bool kS>
+// wire format's quantiser; kS: the input read as RN(c x) (scaled_in); kT2: tau = 2 (else
+// p.tau, the pretest's threshold rounded up and the exact test by a division).
+template <typename Tin, int G, int kB, bool kW, bool kS, bool kT2>
 __global__ void __launch_bounds__(kThreads, 3) k_run_flat(const __grid_constant__ EncParams p,
                                                           long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  run_chunks_dyn<Tin, G, true, kB, true, kW, kS>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks_dyn<Tin, G, true, kB, true, kW, kS, kT2>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // Stage 1 of widths {3, 4} ranked per group: keys, histograms, both widths into scratch.
-// kW: the wire format's quantiser; kS: the input read as RN(c x) (scaled_in).
-template <typename Tin, int G, bool kW, bool kS>
+// kW: the wire format's quantiser; kS: the input read as RN(c x) (scaled_in); kT2: tau = 2
+// (else p.tau).
+template <typename Tin, int G, bool kW, bool kS, bool kT2>
 __global__ void __launch_bounds__(kThreads, 3) k_run_tiles(const __grid_constant__ EncParams p,
                                                            long long n_chunks) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   dep_launch();
-  run_chunks<Tin, G, false, 0, kW, kS>(run_smem<Tin, G>(smem_raw), p, n_chunks);
+  run_chunks<Tin, G, false, 0, kW, kS, kT2>(run_smem<Tin, G>(smem_raw), p, n_chunks);
 }
 
 // ------------------------------------------------------------------ stage 2: the select

@@ -222,6 +222,16 @@ def test_small_whole_chunk_groups(dtype, dist, G, h, beta, T, C, S):
     _check(synth.generate(w), G, h, 3, 4, beta, S)
 
 
+@pytest.mark.parametrize("tau", [0.0, 1.5, 4.0, float("inf")])
+@pytest.mark.parametrize("dtype,dist,G,h,beta,T,C,S", [SMALL_STREAM[4], SMALL_STREAM[1],
+                                                       ("bf16", "gauss_rms_spikes", 64, 64, 3.0, 64, 2048, 16)])
+def test_tau_whole_chunk_groups(dtype, dist, G, h, beta, T, C, S, tau):
+    """Outlier thresholds of Appendix F on the streaming encoder's shapes (ranked and one
+    width): the pretest's threshold m1 / tau rounded up, the exact test by a division."""
+    w = synth.Workload("small", T, C, dtype, G, h, 3, 4, beta, S, 300 + T + G, dist)
+    _check(synth.generate(w), G, h, 3, 4, beta, S, tau)
+
+
 @pytest.mark.parametrize("T,C,S", [(16, 8192, 16), (64, 8192, 64)])
 def test_all_keys_tie_in_a_large_group(T, C, S):
     """Every tile's key equal: the whole group is the select's window (2048 candidates:
