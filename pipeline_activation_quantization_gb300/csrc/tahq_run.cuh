@@ -237,9 +237,19 @@ __device__ __forceinline__ RunSmem<Tin, G>& run_smem(unsigned char* raw) {
 
 // ------------------------------------------------------------------ exact path
 
+// Values a lane in the exact path (a tile is a team of G / V lanes): 16 for bf16 tiles of
+// 64 or 128 values (fewer lane exchanges and less per-lane bookkeeping a value: measured
+// 3-7% faster on those shapes), else 8 (fp32 chunks hold a quarter as many deferred
+// tiles, and 16 a lane leaves fewer, longer team steps for the block barrier to wait on:
+// measured 3.5% slower at fp32 G = 128, 5% at bf16 G = 32).
+template <typename Tin, int G>
+__host__ __device__ constexpr int pass_v() {
+  return (InTraits<Tin>::kBf16 && G >= 64) ? 16 : 8;
+}
+
 // Deferred tiles list[first .. n) of a staged chunk (the pretest could not rule out
-// r > tau), teams of L = G / 8 lanes, 8 values a lane, several teams a warp and the list
-// spread over the block's warps.  The main pass has written every tile's codes and
+// r > tau), teams of L = G / V lanes, V = pass_v values a lane, several teams a warp and
+// the list spread over the block's warps.  The main pass has written every tile's codes and
 // metadata as untransformed; here the exact ratio test of eq. (3) runs (kT2, tau = 2,
 // without a division: RN(m1 / d) > 2 iff m1 / 2 - d > d 2^-24, d = RN(m2 + 1e-12), exact
 // by Sterbenz's lemma; else RN(m1 / d) > tau), and the tiles it flags get the pivot swap, the Hadamard of eq. (4),
@@ -251,7 +261,9 @@ template <typename Tin, int G, bool kFlat, int kB, bool kW, bool kS, bool kT2>
 __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned char* src,
                                           const uint16_t* list, int first, int n, long long t0,
                                           unsigned char* out_lo, unsigned char* out_hi) {
-  constexpr int V = 8, L = G / V, TPW = 32 / L;
+  constexpr int V = pass_v<Tin, G>(), L = G / V, TPW = 32 / L;
+  static_assert(V == 8 || V == 16, "8 or 16 values a lane");
+  static_assert(L >= 2, "a pair of lanes shares the two divisions");
   constexpr int ES = (int)sizeof(Tin), NU = V * ES / 16, UPT = G * ES / 16;
   constexpr bool kBf = InTraits<Tin>::kBf16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -272,8 +284,8 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
       if constexpr (kBf) {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-          v[2 * e] = __uint_as_float(wq[e] << 16);
-          v[2 * e + 1] = __uint_as_float(wq[e] & 0xFFFF0000u);
+          v[8 * k + 2 * e] = __uint_as_float(wq[e] << 16);
+          v[8 * k + 2 * e + 1] = __uint_as_float(wq[e] & 0xFFFF0000u);
         }
       } else {
 #pragma unroll
@@ -331,25 +343,46 @@ __device__ __forceinline__ void pass2_run(const EncParams& p, const unsigned cha
       const int b = kFlat ? kB : (w2 ? 4 : 3);
       const float inv = w2 ? r1d : inv0;
       const float2 inv2 = make_float2(inv, inv);
-      uint32_t f = 0u;
-#pragma unroll
-      for (int j = 0; j < V / 2; j++) {
-        const float2 c = fma2(u[j], inv2, mg);
-        f |= (__float_as_uint(c.x) - 0x4B400000u) << (2 * j * b);
-        f |= (__float_as_uint(c.y) - 0x4B400000u) << ((2 * j + 1) * b);
-      }
       unsigned char* slot = (w2 ? out_hi : out_lo) + (size_t)kt * (G * b / 8);
-      // eight codes a lane: one word at b = 4; at b = 3 the fields of four lanes make
-      // three words (slots start on 4-byte boundaries)
-      const uint32_t f1 = __shfl_down_sync(kFull, f, 1), f2 = __shfl_down_sync(kFull, f, 2);
-      const uint32_t f3 = __shfl_down_sync(kFull, f, 3);
-      if (flag && b == 4) {
-        *reinterpret_cast<uint32_t*>(slot + 4 * sub) = f;
-      } else if (flag && (sub & 3) == 0) {
-        uint32_t* dw = reinterpret_cast<uint32_t*>(slot + 3 * sub);
-        dw[0] = f | (f1 << 24);
-        dw[1] = (f1 >> 8) | (f2 << 16);
-        dw[2] = (f2 >> 16) | (f3 << 8);
+      if constexpr (V == 8) {
+        uint32_t f = 0u;
+#pragma unroll
+        for (int j = 0; j < V / 2; j++) {
+          const float2 c = fma2(u[j], inv2, mg);
+          f |= (__float_as_uint(c.x) - 0x4B400000u) << (2 * j * b);
+          f |= (__float_as_uint(c.y) - 0x4B400000u) << ((2 * j + 1) * b);
+        }
+        // eight codes a lane: one word at b = 4; at b = 3 the fields of four lanes make
+        // three words (slots start on 4-byte boundaries)
+        const uint32_t f1 = __shfl_down_sync(kFull, f, 1), f2 = __shfl_down_sync(kFull, f, 2);
+        const uint32_t f3 = __shfl_down_sync(kFull, f, 3);
+        if (flag && b == 4) {
+          *reinterpret_cast<uint32_t*>(slot + 4 * sub) = f;
+        } else if (flag && (sub & 3) == 0) {
+          uint32_t* dw = reinterpret_cast<uint32_t*>(slot + 3 * sub);
+          dw[0] = f | (f1 << 24);
+          dw[1] = (f1 >> 8) | (f2 << 16);
+          dw[2] = (f2 >> 16) | (f3 << 8);
+        }
+      } else {
+        unsigned long long f = 0ull;
+#pragma unroll
+        for (int j = 0; j < V / 2; j++) {
+          const float2 c = fma2(u[j], inv2, mg);
+          f |= (unsigned long long)(__float_as_uint(c.x) - 0x4B400000u) << (2 * j * b);
+          f |= (unsigned long long)(__float_as_uint(c.y) - 0x4B400000u) << ((2 * j + 1) * b);
+        }
+        // sixteen codes a lane: two words at b = 4 (slots start on 8-byte boundaries); at
+        // b = 3 the 48-bit fields of a pair of lanes make three words (4-byte boundaries)
+        const unsigned long long f1 = __shfl_down_sync(kFull, f, 1);
+        if (flag && b == 4) {
+          *reinterpret_cast<uint2*>(slot + 8 * sub) = make_uint2((uint32_t)f, (uint32_t)(f >> 32));
+        } else if (flag && (sub & 1) == 0) {
+          uint32_t* dw = reinterpret_cast<uint32_t*>(slot + 6 * sub);
+          dw[0] = (uint32_t)f;
+          dw[1] = (uint32_t)(f >> 32) | ((uint32_t)f1 << 16);
+          dw[2] = (uint32_t)(f1 >> 16);
+        }
       }
     }
     if (flag && sub == 0) put_meta(p, t0 + kt, qz, (uint8_t)i1, meta, kFlat);
