@@ -2234,11 +2234,17 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       kern<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       return cudaGetLastError();
     }
+    // compaction chunks: the largest power of two of tiles up to kEncMaxCC that still
+    // gives four blocks an SM (small tensors), and no smaller than the chunks the
+    // workspace holds counts for
+    long long chc = kEncMaxCC;
+    const long long min_chc = encode_cchunk_tiles(C::kBf16 ? 1 : 0, G, a.hi);
+    while (chc / 2 >= min_chc && chc / 2 >= 32 && a.n_tiles / chc < 4ll * a.num_sms) chc /= 2;
     if (plain && ok_mode && !flat && a.lo == 3 && a.hi == 4 && a.n_g % C::CH == 0 &&
-        (a.n_g + kEncMaxCC - 1) / kEncMaxCC <= 64 * 256 && a.group_bytes < (1ll << 31)) {
+        (a.n_g + chc - 1) / chc <= 64 * 256 && a.group_bytes < (1ll << 31)) {
       cudaError_t e = make_line_map(&p.tmap, a.x, C::kBf16, a.n_tiles, G);
       if (e != cudaSuccess) return e;
-      p.CHC = kEncMaxCC;
+      p.CHC = chc;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
       const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
       // modes as for the one-width pass
