@@ -496,9 +496,6 @@ template <int G>
 static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
   const long long n_chunks = decode_chunks(G, a.n_tiles);
   const long long n_blocks = decode_blocks(G, a.n_tiles);
-  // 6 blocks per SM: what registers (40) and shared memory allow, so that the blocks'
-  // load, scan and unpack phases overlap
-  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * 6, n_chunks));
   const size_t smem = sizeof(DecSmem<G>);
   static const cudaError_t e_attr = [smem] {
     const cudaError_t e0 = cudaFuncSetAttribute(k_decode<G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -506,6 +503,16 @@ static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
     return e0 != cudaSuccess ? e0 : e1;
   }();
   if (e_attr != cudaSuccess) return e_attr;
+  // one wave of the blocks an SM holds (registers and shared memory: 6 at tiles of 64 and
+  // 128, 5 at 32, whose stages and per-tile arrays are larger), so that the blocks' load,
+  // scan and unpack phases overlap and no block waits for a second wave
+  static const int per_sm = [smem] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<G, false>, kDecThreads, smem) != cudaSuccess || n < 1)
+      n = 1;
+    return n;
+  }();
+  const int blocks = (int)std::max<long long>(1, std::min<long long>((long long)a.num_sms * per_sm, n_chunks));
   k_dec_totals<G><<<(unsigned)n_blocks, kDecThreads, 0, st>>>(a, n_chunks, n_blocks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
