@@ -2246,7 +2246,11 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
       p.CHC = chc;
       p.nC = (a.n_g + p.CHC - 1) / p.CHC;
-      const int J2 = (int)((a.n_g + kSelPart - 1) / kSelPart);  // select parts a group
+      // select parts a group: of kSelPart tiles, or of kSelPartWide when the narrow parts
+      // would need a second wave of select blocks (five an SM)
+      const bool wide = a.n_groups * ((a.n_g + kSelPart - 1) / kSelPart) > 5ll * a.num_sms;
+      const int part = wide ? kSelPartWide : kSelPart;
+      const int J2 = (int)((a.n_g + part - 1) / part);
       // modes as for the one-width pass
       using TilesFn = void (*)(EncParams, long long);
       static const TilesFn tl[5] = {k_run_tiles<Tin, G, false, false, true>, k_run_tiles<Tin, G, true, false, true>,
@@ -2264,8 +2268,10 @@ static cudaError_t run_encode(const EncodeArgs& a, cudaStream_t st) {
       tl[mode]<<<grid_r, kThreads, smem_r, st>>>(p, n_chunks);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
-      e = launch_dependent(a.wire ? k_run_select<Tin, G, true> : k_run_select<Tin, G, false>,
-                           (unsigned)(a.n_groups * J2), kThreads, 0, st, p, J2, (long long)kSelPart);
+      constexpr int kN = kSelPart / kThreads, kWd = kSelPartWide / kThreads;
+      e = launch_dependent(wide ? (a.wire ? k_run_select<Tin, G, true, kWd> : k_run_select<Tin, G, false, kWd>)
+                                : (a.wire ? k_run_select<Tin, G, true, kN> : k_run_select<Tin, G, false, kN>),
+                           (unsigned)(a.n_groups * J2), kThreads, 0, st, p, J2, (long long)part);
       if (e != cudaSuccess) return e;
       // slots of 3 and 4 units of G / 8 bytes: group strides are whole units
       static_assert(G % 32 == 0, "units of G / 8 bytes");

@@ -770,9 +770,11 @@ __device__ __forceinline__ uint4 warp_tile_raw(const EncParams& p, long long t) 
   return r;
 }
 
-// Tiles of a select part (a multiple of 32 and of kThreads); candidates ranked through a
-// histogram when they are at most kRankHist (their rank keys and 4096 bins fill 32 KB).
+// Tiles of a select part: kSelPart (8 a thread), or kSelPartWide (12 a thread) when
+// parts of kSelPart would need a second wave of select blocks; candidates ranked through
+// a histogram when they are at most kRankHist (their rank keys and 4096 bins fill 32 KB).
 constexpr int kSelPart = 2048;
+constexpr int kSelPartWide = 3072;
 constexpr uint32_t kRankHist = 2048;
 
 // A lane's raw input bytes (warp_tile_raw) read as RN(c x) (scaled_in).
@@ -817,7 +819,7 @@ __device__ __forceinline__ void put_width(const EncParams& p, long long t, bool 
 }
 
 // Stage 2, blocks (group g, j): part j of the group, `per` tiles (a multiple of 32, at
-// most kSelPart).  The group's K-th approximate key lies in fine bucket b*; every tile
+// most kB kThreads).  The group's K-th approximate key lies in fine bucket b*; every tile
 // whose approximate key lies within kWinBins buckets of b* is a candidate: it gets its
 // canonical key (written over the approximate one and appended, as a rank key, to the
 // group's candidates).  Every other tile lies at least 2 kKeyErr from the K-th canonical
@@ -826,7 +828,7 @@ __device__ __forceinline__ void put_width(const EncParams& p, long long t, bool 
 // last block ranks the candidates (the r-th largest rank key, r = K - tiles above the
 // window, is the group's threshold), gives them their widths, and turns the chunks' hi
 // counts into their byte offsets in the stream.
-template <typename Tin, int G, bool kW>
+template <typename Tin, int G, bool kW, int kB>
 __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constant__ EncParams p,
                                                          int J, long long per) {
   __shared__ __align__(16) SelSmem s;
@@ -842,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_run_select(const __grid_constan
   dep_wait();
   dep_launch();
   // the part's keys and ranges, loaded while warp 0 finds the window
-  constexpr int kB = kSelPart / kThreads;
+  static_assert(kB * kThreads <= kChunkBytes / 4, "the part's list fits the buffer");
   const float* kg = p.keys + g * p.n_g;
   const float* dg = p.scales + g * p.n_g;
   float hv[kB], dv[kB], zv[kB];
